@@ -1,0 +1,115 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins catch them.
+
+Each mutation replaces one oracle function with a subtly wrong variant; at least
+one pin from ``test_oracle_pins`` must then fail.
+"""
+import numpy as np
+import pytest
+
+from oracle import hs2_oracle as O
+import tests.test_oracle_pins as P
+
+
+def _sel_no_lse(x, lse, n_far):  # dropped per-head normaliser
+    return np.exp(x[:, :n_far]).sum(axis=0) if n_far > 0 else np.zeros(0)
+
+
+def _sel_max_not_sum(x, lse, n_far):  # heads combined by max instead of sum
+    return np.exp(x[:, :n_far] - lse[:, None]).max(axis=0) if n_far > 0 else np.zeros(0)
+
+
+def _topk_upper_ties(score, k):  # ties to the higher position
+    n = len(score)
+    kk = min(int(k), n)
+    order = np.lexsort((-np.arange(n), -np.asarray(score)))
+    return np.sort(order[:kk])
+
+
+def _far_off_by_one(t, w):
+    return max(0, t - w + 1)
+
+
+def _window_short(t, w):
+    return np.arange(max(0, t - w + 1), t, dtype=np.int64)
+
+
+def _full_attn_transposed(q, K, V, scale):  # softmax over the wrong axis
+    x = (q @ K.T) * float(scale)
+    m = x.max(axis=0, keepdims=True)
+    p = np.exp(x - m)
+    p /= p.sum(axis=0, keepdims=True)
+    lse = np.log(np.exp(x).sum(axis=1))
+    return x, lse, p @ V
+
+
+def _sparse_two_softmaxes(q, K, V, scale):  # window and far positions normalised apart
+    half = max(1, K.shape[0] // 2)
+    outs = []
+    for sl in (slice(0, half), slice(half, None)):
+        x = (q @ K[sl].T) * float(scale)
+        if x.shape[1] == 0:
+            continue
+        p = np.exp(x - x.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        outs.append(p @ V[sl])
+    return sum(outs) / len(outs)
+
+
+def _lightning_no_relu(q_idx, w_idx, K):
+    return (np.asarray(w_idx)[:, None] * (q_idx @ K.T)).sum(axis=0)
+
+
+def _block_max_past_t(I, t, blk):
+    nb = (t + blk - 1) // blk
+    padded = np.concatenate([I, np.full(nb * blk - len(I), 1e9)])
+    return padded.reshape(nb, blk).max(axis=1)
+
+
+def _gather_wrong_slot(pool, bt_row, g, positions, page, dtype):
+    positions = np.asarray(positions, dtype=np.int64)
+    pages = np.asarray(bt_row, dtype=np.int64)[positions // page]
+    return O.to_f64(pool[pages, g, (positions + 1) % page, :], dtype)
+
+
+MUTATIONS = [
+    ("selection_scores", _sel_no_lse),
+    ("selection_scores", _sel_max_not_sum),
+    ("topk_lower_index", _topk_upper_ties),
+    ("far_count", _far_off_by_one),
+    ("window", _window_short),
+    ("full_attention", _full_attn_transposed),
+    ("sparse_attention", _sparse_two_softmaxes),
+    ("lightning_scores", _lightning_no_relu),
+    ("block_max", _block_max_past_t),
+    ("gather_rows", _gather_wrong_slot),
+]
+
+PINS = [
+    lambda: P.test_fa_prefill_matches_masked_dense(4, 2),
+    P.test_fa_closed_forms,
+    P.test_gather_rows_follows_block_table,
+    P.test_window_and_far_range_match_one_based_statement,
+    P.test_selection_scores_against_ratio_form,
+    *[(lambda s=s: P.test_topk_is_best_subset_bruteforce(s)) for s in range(6)],
+    P.test_selection_invariants_and_short_context,
+    P.test_ties_go_to_lower_position,
+    P.test_sa_equals_dense_when_k_covers_far_range,
+    P.test_sa_window_zero_with_everything_selected_is_dense,
+    P.test_sa_renormalisation_error_bound,
+    P.test_lightning_score_special_cases,
+    P.test_block_max_bruteforce_and_tail,
+    P.test_reindex_over_all_blocks_is_flat_indexer,
+    P.test_csa2_attention_over_whole_pool_is_dense_over_pool,
+]
+
+
+@pytest.mark.parametrize("name,fn", MUTATIONS, ids=[f"{n}:{f.__name__}" for n, f in MUTATIONS])
+def test_some_pin_catches_mutation(monkeypatch, name, fn):
+    monkeypatch.setattr(O, name, fn)
+    caught = 0
+    for pin in PINS:
+        try:
+            pin()
+        except Exception:  # noqa: BLE001 - any failure of a pin counts as a catch
+            caught += 1
+    assert caught > 0, f"no pin caught the mutation of {name}"

@@ -1,0 +1,394 @@
+"""Pins of the CPU oracle to things other than itself (CPU only).
+
+Each test checks the oracle against brute force on tiny inputs written in a
+different form (explicit masks and Python loops over ``math.exp``), closed
+forms, special cases the pages state, or invariants; a dropped term, wrong
+sign, wrong index or transposed operand in the oracle fails one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import hs2_oracle as O
+from top_hs2_fa_gb300 import workloads as W
+from top_hs2_fa_gb300 import counting as C
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden", "counting_examples.json")
+
+
+# ----------------------------------------------------------------------------- brute-force helpers
+def dense_masked_bruteforce(Q, K, V, scale):
+    """Causal attention of rows Q[i] (row i sees keys 0..i) with an explicit boolean
+    n x n mask and a per-row softmax written with Python loops and math.exp."""
+    n, d = Q.shape
+    mask = [[s <= i for s in range(n)] for i in range(n)]
+    out = np.zeros((n, V.shape[1]))
+    lse = np.zeros(n)
+    for i in range(n):
+        logits = [float(Q[i] @ K[s]) * scale if mask[i][s] else -math.inf for s in range(n)]
+        m = max(logits)
+        ex = [math.exp(x - m) if x != -math.inf else 0.0 for x in logits]
+        z = sum(ex)
+        lse[i] = m + math.log(z)
+        for s in range(n):
+            out[i] += (ex[s] / z) * V[s]
+    return out, lse
+
+
+def prob_table(Q, K, scale):
+    """p[h][s] = exp(x) / sum exp(x) with Python loops (ratio form, no lse)."""
+    H = Q.shape[0]
+    t = K.shape[0]
+    p = np.zeros((H, t))
+    for h in range(H):
+        ex = [math.exp(float(Q[h] @ K[s]) * scale) for s in range(t)]
+        z = sum(ex)
+        for s in range(t):
+            p[h, s] = ex[s] / z
+    return p
+
+
+def contiguous_rows(kv, b, g, t):
+    return O.gather_rows(kv.k, kv.block_table[b], g, np.arange(t), kv.page, kv.dtype), \
+        O.gather_rows(kv.v, kv.block_table[b], g, np.arange(t), kv.page, kv.dtype)
+
+
+# ----------------------------------------------------------------------------- FA output
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (2, 1), (3, 3)])
+def test_fa_prefill_matches_masked_dense(Hq, Hkv):
+    n, d = 37, 8
+    grp = W.prefill_group(n, Hq, Hkv, d, w=4, k=5, dtype="f32", seed=11, n_sa=0, page=8, permute=True)
+    kv = grp.kv
+    o, lse, _, _ = O.fa_prefill_rows(grp.q_fa, kv, np.arange(n), grp.w, grp.k, grp.scale)
+    Q = O.to_f64(grp.q_fa, "f32")
+    G = Hq // Hkv
+    for g in range(Hkv):
+        K, V = contiguous_rows(kv, 0, g, n)
+        for h in range(g * G, (g + 1) * G):
+            ref, ref_lse = dense_masked_bruteforce(Q[:, h], K, V, grp.scale)
+            np.testing.assert_allclose(o[:, h], ref, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[:, h], ref_lse, rtol=0, atol=1e-12)
+
+
+def test_fa_closed_forms():
+    # identical keys -> uniform attention: o = mean of visible V, lse = x0 + log t
+    d, t = 8, 20
+    rng = np.random.default_rng(0)
+    q = rng.standard_normal((3, d))
+    k0 = rng.standard_normal(d)
+    K = np.repeat(k0[None], t, 0)
+    V = rng.standard_normal((t, d))
+    x, lse, o = O.full_attention(q, K, V, 0.5)
+    np.testing.assert_allclose(o, np.repeat(V.mean(0)[None], 3, 0), atol=1e-13)
+    np.testing.assert_allclose(lse, 0.5 * (q @ k0) + math.log(t), atol=1e-13)
+    # identical values -> output is that value whatever the logits
+    V2 = np.repeat(V[:1], t, 0)
+    _, _, o2 = O.full_attention(q, rng.standard_normal((t, d)), V2, 0.5)
+    np.testing.assert_allclose(o2, V2[:3], atol=1e-13)
+
+
+def test_gather_rows_follows_block_table():
+    kv = W.random_paged_kv([150, 70], Hkv=2, d=4, dtype="f32", seed=5, page=16)
+    for b, t in enumerate([150, 70]):
+        for s in (0, 15, 16, t - 1):
+            page = kv.block_table[b][s // 16]
+            row = O.gather_rows(kv.k, kv.block_table[b], 1, np.array([s]), 16, "f32")[0]
+            np.testing.assert_array_equal(row, kv.k[page, 1, s % 16].astype(np.float64))
+
+
+# ----------------------------------------------------------------------------- selection
+def test_window_and_far_range_match_one_based_statement():
+    # window [t-w+1, t] in 1-based positions == [t-w, t-1] 0-based; far count min(k, t-w)
+    for t, w in [(10, 3), (3, 3), (2, 5), (1, 1)]:
+        win = O.window(t, w)
+        assert list(win + 1) == list(range(max(1, t - w + 1), t + 1))
+        assert O.far_count(t, w) == max(0, t - w)
+
+
+def test_selection_scores_against_ratio_form():
+    rng = np.random.default_rng(3)
+    t, d, G, w = 12, 5, 3, 4
+    Q = rng.standard_normal((G, d)) * np.array([[3.0], [0.3], [1.0]])  # very different lse per head
+    K = rng.standard_normal((t, d))
+    x, lse, _ = O.full_attention(Q, K, K, 0.7)
+    sc = O.selection_scores(x, lse, t - w)
+    p = prob_table(Q, K, 0.7)
+    np.testing.assert_allclose(sc, p[:, :t - w].sum(0), atol=1e-14)
+    # over all positions each head's probabilities sum to one
+    np.testing.assert_allclose(O.selection_scores(x, lse, t).sum(), G, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_is_best_subset_bruteforce(seed):
+    rng = np.random.default_rng(100 + seed)
+    t, w, d, G = int(rng.integers(5, 12)), int(rng.integers(0, 4)), 4, 2
+    k = int(rng.integers(1, 4))
+    Q = rng.standard_normal((G, d))
+    K = rng.standard_normal((t, d)) * 1.5
+    x, lse, _ = O.full_attention(Q, K, K, 1.0)
+    nf = O.far_count(t, w)
+    sc = O.selection_scores(x, lse, nf)
+    sel = O.topk_lower_index(sc, k)
+    p = prob_table(Q, K, 1.0)
+    best, best_sum = None, -1.0
+    for sub in itertools.combinations(range(nf), min(k, nf)):
+        s = sum(p[h, j] for h in range(G) for j in sub)
+        if s > best_sum:
+            best, best_sum = sub, s
+    assert tuple(sel) == tuple(best)
+
+
+def test_selection_invariants_and_short_context():
+    grp = W.decode_group([5, 20, 130, 131, 700], Hq=4, Hkv=2, d=16, w=8, k=100, dtype="f32",
+                         seed=7, n_sa=0, needles=0, page=16)
+    o, lse, idx, cnt = O.fa_decode(grp.q_fa, grp.kv, 8, 100, grp.scale)
+    for b, t in enumerate([5, 20, 130, 131, 700]):
+        for g in range(2):
+            sel = idx[b, g, :cnt[b, g]]
+            assert cnt[b, g] == min(100, max(0, t - 8))
+            assert np.all(idx[b, g, cnt[b, g]:] == -1)
+            assert np.all(np.diff(sel) > 0)
+            assert sel.size == 0 or (sel.min() >= 0 and sel.max() < t - 8)
+            assert not set(sel) & set(O.window(t, 8))
+            if t - 8 <= 100:  # k covers the far range: S = F
+                assert list(sel) == list(range(max(0, t - 8)))
+
+
+def test_ties_go_to_lower_position():
+    # identical keys -> every far position has the same score -> the first k win
+    d, t, w, k = 8, 50, 5, 7
+    rng = np.random.default_rng(1)
+    K = np.repeat(rng.standard_normal(d)[None], t, 0)
+    q = rng.standard_normal((2, d))
+    x, lse, _ = O.full_attention(q, K, K, 0.3)
+    sel = O.topk_lower_index(O.selection_scores(x, lse, t - w), k)
+    assert list(sel) == list(range(k))
+    assert list(O.topk_lower_index(np.array([1.0, 2.0, 2.0, 1.0, 2.0]), 2)) == [1, 2]
+
+
+def test_mqa_order_equals_logit_order():
+    rng = np.random.default_rng(9)
+    t, d, w, k = 300, 16, 10, 40
+    q = rng.standard_normal((1, d))
+    K = rng.standard_normal((t, d))
+    x, lse, _ = O.full_attention(q, K, K, 0.25)
+    sel = O.topk_lower_index(O.selection_scores(x, lse, t - w), k)
+    ref = np.sort(np.argsort(-x[0, :t - w], kind="stable")[:k])
+    assert list(sel) == list(ref)
+
+
+def test_needles_are_selected():
+    tg = W.tiny_group(n=600, Hq=4, Hkv=1, d=64, w=16, k=64, needles=8, seed=0)
+    dec = tg.decode
+    _, _, idx, cnt = O.fa_decode(dec.q_fa, dec.kv, dec.w, dec.k, dec.scale)
+    assert set(dec.needles[0].tolist()) <= set(idx[0, 0, :cnt[0, 0]].tolist())
+
+
+# ----------------------------------------------------------------------------- SA
+def test_sa_equals_dense_when_k_covers_far_range():
+    grp = W.decode_group([40, 64, 65, 129], Hq=4, Hkv=2, d=8, w=6, k=200, dtype="f32", seed=2,
+                         n_sa=1, needles=0, page=16)
+    kv = grp.kv
+    _, _, idx, cnt = O.fa_decode(grp.q_fa, kv, grp.w, grp.k, grp.scale)
+    o_sa = O.sa_decode(grp.q_sa[0], kv, grp.w, idx, cnt, grp.scale)
+    Qs = O.to_f64(grp.q_sa[0], "f32")
+    for b, t in enumerate([40, 64, 65, 129]):
+        for h in range(4):
+            K, V = contiguous_rows(kv, b, h // 2, t)
+            # dense attention of the SA query over all t keys = last row of a causal pass
+            Qfull = np.zeros((t, 8))
+            Qfull[t - 1] = Qs[b, h]
+            ref, _ = dense_masked_bruteforce(Qfull, K, V, grp.scale)
+            np.testing.assert_allclose(o_sa[b, h], ref[t - 1], atol=1e-12)
+
+
+def test_sa_window_zero_with_everything_selected_is_dense():
+    rng = np.random.default_rng(4)
+    t, d = 33, 8
+    kv = W.random_paged_kv([t], Hkv=1, d=d, dtype="f32", seed=8, page=8)
+    q = rng.standard_normal((1, 2, d)).astype(np.float32)
+    idx = np.arange(t, dtype=np.int32).reshape(1, 1, t)
+    o = O.sa_decode(q, kv, 0, idx, np.array([[t]], np.int32), 0.4)
+    K, V = contiguous_rows(kv, 0, 0, t)
+    p = prob_table(q[0].astype(np.float64), K, 0.4)
+    np.testing.assert_allclose(o[0], p @ V, atol=1e-12)
+
+
+def test_sa_renormalisation_error_bound():
+    grp = W.decode_group([300] * 3, Hq=8, Hkv=2, d=16, w=8, k=20, dtype="f32", seed=12, n_sa=1,
+                         needles=4, page=16)
+    kv = grp.kv
+    _, _, idx, cnt = O.fa_decode(grp.q_fa, kv, grp.w, grp.k, grp.scale)
+    o_sa = O.sa_decode(grp.q_sa[0], kv, grp.w, idx, cnt, grp.scale)
+    Qs = O.to_f64(grp.q_sa[0], "f32")
+    for b in range(3):
+        for h in range(8):
+            g = h // 4
+            K, V = contiguous_rows(kv, b, g, 300)
+            _, _, o_dense = O.full_attention(Qs[b, h:h + 1], K, V, grp.scale)
+            p = prob_table(Qs[b, h:h + 1], K, grp.scale)[0]
+            keep = np.concatenate([O.window(300, grp.w), idx[b, g, :cnt[b, g]]])
+            err = np.sqrt(((o_sa[b, h] - o_dense[0]) ** 2).sum())
+            assert err <= O.renormalisation_bound(p, keep, V) + 1e-12
+
+
+def test_paging_is_invisible():
+    grp = W.decode_group([100, 37], Hq=2, Hkv=1, d=8, w=4, k=9, dtype="bf16", seed=21, n_sa=1,
+                         needles=2, page=16, permute=True)
+    kv = grp.kv
+    res1 = O.fa_decode(grp.q_fa, kv, 4, 9, grp.scale)
+    # move every page to a new physical slot and rewrite the table
+    perm = np.random.default_rng(0).permutation(kv.num_pages)
+    inv = np.argsort(perm)
+    kv2 = W.PagedKV(k=kv.k[perm], v=kv.v[perm], block_table=np.where(kv.block_table >= 0, inv[np.maximum(kv.block_table, 0)], -1).astype(np.int32),
+                    seq_len=kv.seq_len, dtype=kv.dtype, page=kv.page)
+    res2 = O.fa_decode(grp.q_fa, kv2, 4, 9, grp.scale)
+    for a, b in zip(res1, res2):
+        np.testing.assert_array_equal(a, b)
+    s1 = O.sa_decode(grp.q_sa[0], kv, 4, res1[2], res1[3], grp.scale)
+    s2 = O.sa_decode(grp.q_sa[0], kv2, 4, res1[2], res1[3], grp.scale)
+    np.testing.assert_array_equal(s1, s2)
+
+
+def test_sa_rejects_overlapping_sets():
+    kv = W.random_paged_kv([20], Hkv=1, d=4, dtype="f32", seed=1, page=8)
+    q = np.zeros((1, 1, 4), np.float32)
+    with pytest.raises(ValueError):
+        O.sa_decode(q, kv, 4, np.array([[[17, -1]]], np.int32), np.array([[1]], np.int32), 1.0)
+
+
+def test_decode_equals_last_prefill_row():
+    tg = W.tiny_group(n=200, Hq=4, Hkv=1, d=16, w=8, k=12, needles=3, seed=4)
+    dec, pre = tg.decode, tg.prefill
+    kv_full = W.PagedKV(k=pre.kv.k, v=pre.kv.v, block_table=pre.kv.block_table,
+                        seq_len=np.array([201], np.int32), dtype="f32", page=pre.kv.page)
+    q_all = np.concatenate([pre.q_fa, dec.q_fa], 0)
+    r = O.fa_prefill_rows(q_all, kv_full, [200], 8, 12, dec.scale)
+    d_ = O.fa_decode(dec.q_fa, dec.kv, 8, 12, dec.scale)
+    for a, b in zip(r, d_):
+        np.testing.assert_allclose(a, b, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- CSA2
+def _csa2_small(seed=0, t=(333, 100, 8), pool_blocks=20, k_top=30):
+    grp = W.csa2_group(list(t), Hq=4, d=16, Hi=6, di=16, k_top=k_top, blk=8, max_blocks=pool_blocks,
+                       n_reuse=1, needles=5, dtype="bf16", seed=seed, page=16)
+    return grp
+
+
+def test_lightning_score_special_cases():
+    rng = np.random.default_rng(0)
+    K = rng.standard_normal((50, 6))
+    q = rng.standard_normal((4, 6))
+    wv = rng.uniform(0, 1, 4)
+    I = O.lightning_scores(q, wv, K)
+    # single head, unit weight: relu of the dot product
+    np.testing.assert_allclose(O.lightning_scores(q[:1], np.ones(1), K), np.maximum(K @ q[0], 0), atol=1e-14)
+    # linear in w, zero when every dot product is negative, never negative
+    np.testing.assert_allclose(O.lightning_scores(q, 3 * wv, K), 3 * I, atol=1e-12)
+    Kneg = -np.sign(q[0])[None, :] * np.abs(K)
+    qpos = np.abs(q[:1]) * np.sign(q[0])
+    assert np.all(O.lightning_scores(qpos, np.ones(1), Kneg) == 0)
+    assert np.all(I >= 0)
+    # loop form
+    for s in (0, 17, 49):
+        ref = sum(wv[j] * max(0.0, float(q[j] @ K[s])) for j in range(4))
+        assert abs(I[s] - ref) < 1e-12
+
+
+def test_block_max_bruteforce_and_tail():
+    I = np.random.default_rng(2).standard_normal(37)
+    bm = O.block_max(I, 37, 8)
+    assert len(bm) == 5
+    for b in range(5):
+        assert bm[b] == max(I[s] for s in range(8 * b, min(37, 8 * b + 8)))
+
+
+def test_reindex_over_all_blocks_is_flat_indexer():
+    grp = _csa2_small(seed=1, pool_blocks=2048)  # pool = every block
+    idx, cnt, pool, pcnt = O.indexer_full(grp.q_idx[0], grp.w_idx[0], grp.kidx, grp.k_top, 8, 2048)
+    for b, t in enumerate(grp.kidx.seq_len):
+        assert pcnt[b] == (int(t) + 7) // 8
+    # Reindex with its own query over the full pool == flat top-k of that query
+    ridx, rcnt = O.indexer_reindex(grp.q_idx[1], grp.w_idx[1], grp.kidx, grp.k_top, 8, pool, pcnt)
+    fidx, fcnt, _, _ = O.indexer_full(grp.q_idx[1], grp.w_idx[1], grp.kidx, grp.k_top, 8, 2048)
+    np.testing.assert_array_equal(ridx, fidx)
+    np.testing.assert_array_equal(rcnt, fcnt)
+
+
+def test_reindex_with_full_query_reproduces_full_topk():
+    # pool_blocks >= k_top, pool smaller than the 42 blocks of t=333: a block holding a
+    # top-k position has a maximum >= the k-th score, and at most k_top blocks do
+    grp = _csa2_small(seed=3, pool_blocks=24, k_top=20)
+    idx, cnt, pool, pcnt = O.indexer_full(grp.q_idx[0], grp.w_idx[0], grp.kidx, 20, 8, 24)
+    assert pcnt[0] == 24
+    ridx, rcnt = O.indexer_reindex(grp.q_idx[0], grp.w_idx[0], grp.kidx, 20, 8, pool, pcnt)
+    for b, t in enumerate(grp.kidx.seq_len):
+        sel = set(idx[b, :cnt[b]].tolist())
+        pos = set(O.pool_positions(pool[b, :pcnt[b]], int(t), 8).tolist())
+        assert sel <= pos  # a block holding a top-k position has max >= the k-th score
+        assert list(ridx[b, :rcnt[b]]) == list(idx[b, :cnt[b]])
+
+
+def test_csa2_attention_over_whole_pool_is_dense_over_pool():
+    grp = _csa2_small(seed=5, pool_blocks=6, k_top=10_000)
+    idx, cnt, pool, pcnt = O.indexer_full(grp.q_idx[0], grp.w_idx[0], grp.kidx, 10_000, 8, 6)
+    ridx, rcnt = O.indexer_reindex(grp.q_idx[1], grp.w_idx[1], grp.kidx, 10_000, 8, pool, pcnt)
+    kv = grp.kv
+    o = O.sa_decode(grp.q_main[1], kv, 0, ridx.reshape(len(rcnt), 1, -1), rcnt.reshape(-1, 1), grp.scale)
+    Q = O.to_f64(grp.q_main[1], "bf16")
+    for b, t in enumerate(kv.seq_len):
+        pos = O.pool_positions(pool[b, :pcnt[b]], int(t), 8)
+        assert list(ridx[b, :rcnt[b]]) == list(pos)  # k >= pool size: everything in the pool
+        K = O.gather_rows(kv.k, kv.block_table[b], 0, pos, kv.page, "bf16")
+        V = O.gather_rows(kv.v, kv.block_table[b], 0, pos, kv.page, "bf16")
+        p = prob_table(Q[b], K, grp.scale)
+        np.testing.assert_allclose(o[b], p @ V, atol=1e-12)
+
+
+def test_csa2_needles_in_full_topk():
+    grp = _csa2_small(seed=6)
+    idx, cnt, _, _ = O.indexer_full(grp.q_idx[0], grp.w_idx[0], grp.kidx, grp.k_top, 8, 20)
+    for b in range(len(cnt)):
+        assert set(grp.needles[b].tolist()) <= set(idx[b, :cnt[b]].tolist())
+
+
+# ----------------------------------------------------------------------------- counting model
+def test_counting_examples_from_pages():
+    gold = json.load(open(GOLD))
+    g = gold["csa2_group_nc32768"]
+    flat, hier = C.selector_comparisons(g["n_c"], g["pool"], g["n_full"], g["n_reindex"], g["n_reuse"])
+    assert (flat, hier) == (g["flat"], g["hierarchical"])
+    assert hier / flat == g["ratio"]
+    g = gold["csa2_group_1m"]
+    assert g["n"] // g["m"] == g["n_c"]
+    flat, hier = C.selector_comparisons(g["n_c"], g["pool"], g["n_full"], g["n_reindex"], g["n_reuse"])
+    assert (flat, hier) == (g["flat"], g["hierarchical"])
+    assert round(100 * hier / flat, 2) == g["ratio_percent_2dp"]
+    assert (g["n_full"] + g["n_reindex"] + g["n_reuse"]) * g["k_top"] == g["attention_entry_reads"]
+    g = gold["dsa_decode_crossover"]
+    assert C.dsa_crossover(g["latent_bytes"], g["index_key_bytes"], g["k"]) == g["crossover_L"]
+    dense, dsa = C.dsa_decode_bytes(g["crossover_L"] + 1, g["latent_bytes"], g["index_key_bytes"], g["k"])
+    assert dsa < dense
+    dense, dsa = C.dsa_decode_bytes(g["crossover_L"] - 1, g["latent_bytes"], g["index_key_bytes"], g["k"])
+    assert dsa > dense
+    g = gold["dsa_prefill_speedup"]
+    assert round(g["dense_pflop"] / (g["main_pflop"] + g["indexer_pflop_fp8_equiv"]), 1) == g["speedup_1dp"]
+
+
+def test_prefill_flops_model():
+    f = C.prefill_flops(32768, 32, 128, 128, 1024)
+    assert abs(f["fa"] - 8.796e12) / 8.796e12 < 1e-3  # 4*d*Hq*n(n+1)/2
+    # SA row cost saturates at w + k keys
+    small = C.prefill_flops(10, 1, 1, 2, 3)
+    assert small["sa_per_layer"] == 4 * sum(min(2, t) + min(3, max(0, t - 2)) for t in range(1, 11))
+
+
+def test_decode_bytes_model():
+    m = C.decode_group_bytes([100, 2000], Hq=8, Hkv=2, d=16, w=8, k=64, elem=2, n_sa=5)
+    assert m["fa"] == (100 + 2000) * 2 * 16 * 2 * 2
+    assert m["sa_per_layer"] == 2 * ((8 + 64) + (8 + 64)) * 16 * 2 * 2
