@@ -1,0 +1,173 @@
+/*
+ * hs2.h — C ABI of the group-shared top-k sparse attention library (libhs2).
+ *
+ * One Cross group of a HySparse2 model = one FA layer + its SA layers over one
+ * shared paged KV cache. The FA layer attends causally to every visible key and
+ * emits, per query and KV head, the top-k positions outside a forced recent
+ * window; each SA layer reuses that KV and those positions with its own query,
+ * attending to window ∪ top-k under one softmax. The CSA2 variant replaces the
+ * FA selection by a hierarchical lightning indexer (Full / Reindex / Reuse).
+ *
+ * Pages this interface restates (cited by title and section):
+ *   [HS2]  "HySparse2：整体架构、KV 生命周期与 PD 分离"
+ *          §5 (KV Reuse), §7.1-7.4 (forced window + out-of-window top-k, one
+ *          normalisation, direct access to paged KV).
+ *   [CSA2] "2.3.1 · CSA、HCA 与 CSA2: 压缩序列上的稀疏检索和跨层复用"
+ *          §3.1 (Full / Reindex / Reuse), §3.2 (hierarchical sparse indexer).
+ *   [L10]  "Lecture 10 · 混合架构与稀疏注意力：Mamba、Marconi 与 DeepSeek-V3.2"
+ *          §5.1 (lightning indexer score), §5.5 (paged gather through a block table).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Positions are 0-based. A query that sees t keys sits at position t-1; its
+ *   own key is already in the cache. Window W(t) = [max(0,t-w), t-1]; far range
+ *   F(t) = [0, t-w-1]; the FA selects min(k, max(0, t-w)) positions of F(t).
+ * - GQA: query head h reads KV head g = h / (Hq / Hkv).
+ * - All pointers are DEVICE pointers unless stated otherwise. The caller owns
+ *   every buffer (inputs, outputs, workspace, dev_err). The library never
+ *   allocates, frees or synchronises; every call is asynchronous on `stream`
+ *   (a cudaStream_t passed as void*; NULL = the legacy default stream).
+ * - Return value: host-side validation and launch status. HS2_ERR_ARG means
+ *   nothing was launched. HS2_ERR_CUDA means a launch failed (the CUDA error is
+ *   cleared and reported by hs2_last_cuda_error()).
+ * - dev_err (optional, may be NULL): int32 device word the kernels OR error bits
+ *   into (HS2_DEV_*) when they meet an out-of-range block-table entry or index,
+ *   or give up a bounded wait. Bad accesses are skipped, never performed. The
+ *   caller zeroes it and reads it after synchronising.
+ * - Outputs are float32 whatever the input dtype (fp32 accumulation).
+ * - Index sets are written sorted ascending, padded with -1, with a count array.
+ *   Among equal scores the lower position (or lower block id) wins.
+ */
+#ifndef HS2_H
+#define HS2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HS2_ABI_VERSION 1
+
+typedef enum {
+  HS2_OK = 0,
+  HS2_ERR_ARG = -1,         /* invalid shape, pointer, alignment or workspace size */
+  HS2_ERR_UNSUPPORTED = -2, /* valid but not implemented combination (e.g. head_dim 96) */
+  HS2_ERR_CUDA = -3,        /* a CUDA launch / runtime call failed */
+  HS2_ERR_DEVICE = -4       /* reserved for callers that fold dev_err into a status */
+} hs2_status;
+
+/* device-side error bits (ORed into *dev_err) */
+#define HS2_DEV_BAD_PAGE 1    /* block-table entry outside [0, num_pages) */
+#define HS2_DEV_BAD_INDEX 2   /* selected position outside F(t) (or outside [0,t) with w=0) */
+#define HS2_DEV_TIMEOUT 4     /* a bounded wait (mbarrier / TMA / MMA) gave up */
+#define HS2_DEV_BAD_LENGTH 8  /* seq_len < 1 or beyond max_pages * page_size */
+
+typedef enum { HS2_F32 = 0, HS2_BF16 = 1 } hs2_dtype;
+
+/* Paged KV of ONE group, shared by its FA and SA layers ([HS2] §5, §7.2).
+ * k, v:        [num_pages][Hkv][page_size][d] elements of `dtype`, 16-byte aligned.
+ *              v may be NULL for an indexer-key cache (hs2_hier_reindex).
+ * block_table: int32 [batch][max_pages]; entry j of sequence b is the physical page
+ *              holding logical positions [j*page_size, (j+1)*page_size).
+ * seq_len:     int32 [batch], keys visible to the query (its own included), >= 1.
+ * page_size must be 64; d must be 64 or 128.                                        */
+typedef struct {
+  const void* k;
+  const void* v;
+  const int32_t* block_table;
+  const int32_t* seq_len;
+  int32_t batch;
+  int32_t num_pages;
+  int32_t max_pages;
+  int32_t page_size;
+  int32_t Hkv;
+  int32_t d;
+  hs2_dtype dtype;
+} hs2_kv;
+
+/* ---------------------------------------------------------------------------
+ * FA layer + window-excluding top-k selection  ([HS2] §5, §7.2; the "oracle"
+ * selection of the appendix: the FA's own exactly computed attention scores).
+ *
+ * decode (prefill = 0): one query per sequence; q is [batch][Hq][d] of kv->dtype,
+ *   B_or_n must equal kv->batch; query b sees t_b = seq_len[b] keys.
+ * prefill (prefill = 1): one sequence (kv->batch == 1), n = B_or_n query rows,
+ *   q is [n][Hq][d]; row i sees t_i = i + 1 keys; requires n <= seq_len[0].
+ *
+ * Per query and head h: x_h(s) = scale * q_h . k_g(s) for s < t;
+ *   o[..][h][:] = sum_s softmax(x_h)(s) v_g(s);  lse[..][h] = log sum_s exp x_h(s).
+ * Per query and KV head g: score_g(s) = sum_{h in g} exp(x_h(s) - lse_h) over
+ *   s in F(t); idx[..][g][:] = the min(k, |F|) best positions (score descending,
+ *   lower position first on ties), ascending, -1 padded; idx_cnt[..][g] = count.
+ * Outputs: o float32 [B_or_n][Hq][d]; lse float32 [B_or_n][Hq] (may be NULL);
+ *   idx int32 [B_or_n][Hkv][k]; idx_cnt int32 [B_or_n][Hkv].
+ * workspace: device scratch of at least hs2_fa_select_workspace(...) bytes,
+ *   256-byte aligned; contents on entry are ignored.
+ * max_t: the largest seq_len of the call (decode) or n (prefill).
+ * Requirements: Hq % Hkv == 0, Hq / Hkv <= 32, k >= 0, w >= 0.                     */
+size_t hs2_fa_select_workspace(int B_or_n, int Hq, const hs2_kv* kv, int max_t, int k, int prefill);
+hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w,
+                         int k, float scale, int prefill, float* o, float* lse, int32_t* idx,
+                         int32_t* idx_cnt, void* workspace, size_t ws_bytes, int32_t* dev_err,
+                         void* stream);
+
+/* ---------------------------------------------------------------------------
+ * SA layer: KV and index reuse with the layer's own query  ([HS2] §5, §7.2, §7.4).
+ * For each query and head h of KV head g:
+ *   U = W(t) ∪ {idx[..][g][j] : j < idx_cnt[..][g]}   (the caller guarantees the
+ *   indices lie in F(t), i.e. outside the window; with w = 0 any s < t),
+ *   o[..][h][:] = sum_{s in U} softmax_U(scale * q_h . k_g(s)) v_g(s), one softmax.
+ * Shapes and the decode / prefill convention are those of hs2_fa_select; idx and
+ * idx_cnt have the layout hs2_fa_select writes ([B_or_n][Hkv][k], [B_or_n][Hkv]).
+ * workspace: at least hs2_sa_reuse_workspace(...) bytes, 256-byte aligned.        */
+size_t hs2_sa_reuse_workspace(int B_or_n, int Hq, const hs2_kv* kv, int w, int k, int prefill);
+hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int w,
+                        const int32_t* idx, const int32_t* idx_cnt, int k, float scale, int prefill,
+                        float* o, void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * CSA2 hierarchical sparse indexer  ([CSA2] §3.1-3.2; score from [L10] §5.1).
+ * I(s) = sum_j w_idx[b][j] * max(0, q_idx[b][j] . k_idx(s)), unscaled, where k_idx(s)
+ * is row s of the indexer-key cache k_idx (Hkv = 1, d = di, v = NULL), shared by
+ * all Hi indexer heads.
+ * HS2_FULL: score every s < t; idx[b] = top-min(k_top, t) positions; block maxima
+ *   over blocks [blk*j, blk*j+blk) ∩ [0,t); pool_blocks[b] = top-min(max_blocks,
+ *   ceil(t/blk)) block ids (maximum descending, lower id first), ascending, -1
+ *   padded; pool_cnt[b] = count.  (pool_blocks / pool_cnt are outputs.)
+ * HS2_REINDEX: score only the positions of the given pool (inputs pool_blocks /
+ *   pool_cnt); idx[b] = top-min(k_top, |pool positions|), ascending.
+ * (Reuse layers call nothing: they pass the previous idx to hs2_sa_reuse.)
+ * q_idx: [batch][Hi][di] of k_idx->dtype; w_idx: float32 [batch][Hi];
+ * idx: int32 [batch][k_top]; idx_cnt: int32 [batch]; blk must divide page_size.
+ * workspace: at least hs2_hier_reindex_workspace(...) bytes, 256-byte aligned.     */
+typedef enum { HS2_FULL = 0, HS2_REINDEX = 1 } hs2_idx_mode;
+size_t hs2_hier_reindex_workspace(hs2_idx_mode mode, int Hi, const hs2_kv* k_idx, int max_t,
+                                  int k_top, int blk, int max_blocks);
+hs2_status hs2_hier_reindex(hs2_idx_mode mode, const void* q_idx, const float* w_idx, int Hi,
+                            const hs2_kv* k_idx, int max_t, int k_top, int blk, int max_blocks,
+                            int32_t* pool_blocks, int32_t* pool_cnt, int32_t* idx, int32_t* idx_cnt,
+                            void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics.
+ * hs2_profile_next: the next call on this host thread that runs `stage` records the
+ * cudaEvent_t handles `start` and `stop` (passed as void*, created by the caller) on
+ * that call's stream immediately before and after the stage's main kernel; one-shot,
+ * NULL events clear it. Lets a caller time the dominant kernel inside a running step. */
+typedef enum {
+  HS2_STAGE_FA_SCAN = 0,    /* FA scan over all visible keys (hs2_fa_select) */
+  HS2_STAGE_SA_GATHER = 1,  /* SA gather-attention (hs2_sa_reuse) */
+  HS2_STAGE_INDEXER = 2     /* lightning-indexer scan (hs2_hier_reindex) */
+} hs2_stage;
+void hs2_profile_next(hs2_stage stage, void* start, void* stop);
+const char* hs2_strerror(hs2_status st);
+int hs2_last_cuda_error(void); /* cudaError_t of the last HS2_ERR_CUDA, 0 if none */
+int hs2_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HS2_H */

@@ -1,0 +1,144 @@
+"""GPU parity of the decode path (FA + selection, SA reuse) against the CPU oracle.
+
+Every call goes through the C ABI (ctypes binding). Oracle inputs are the same
+seeded arrays the GPU receives; no expected value comes from the GPU.
+"""
+import numpy as np
+import pytest
+
+from oracle import hs2_oracle as O
+from top_hs2_fa_gb300 import workloads as W
+
+from hs2_testutil import check_index_sets, kv_to_device, max_abs, to_torch, tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def H():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from top_hs2_fa_gb300 import build
+    build.build()
+    from top_hs2_fa_gb300 import hs2
+    hs2.load()
+    return hs2
+
+
+def run_decode_group(H, grp, sa_layers=None):
+    import torch
+
+    kv = grp.kv
+    dkv = kv_to_device(kv)
+    q = to_torch(grp.q_fa, kv.dtype)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse, idx, cnt = H.hs2_fa_select(q, dkv, grp.w, grp.k, grp.scale, max_t=int(kv.seq_len.max()), dev_err=err)
+    sa = []
+    for j in range(len(grp.q_sa) if sa_layers is None else sa_layers):
+        qs = to_torch(grp.q_sa[j], kv.dtype)
+        sa.append(H.hs2_sa_reuse(qs, dkv, grp.w, idx, cnt, grp.k, grp.scale, dev_err=err).cpu().numpy())
+    torch.cuda.synchronize()
+    return o.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy(), cnt.cpu().numpy(), sa, int(err.item())
+
+
+def check_group(H, grp, batches=None, sa_layers=None):
+    kv = grp.kv
+    o, lse, idx, cnt, sa, err = run_decode_group(H, grp, sa_layers)
+    assert err == 0, f"device error flags {err}"
+    sel = list(range(kv.B)) if batches is None else list(batches)
+    sub = W.PagedKV(k=kv.k, v=kv.v, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel], dtype=kv.dtype,
+                    page=kv.page)
+    o_r, lse_r, idx_r, cnt_r, scores = O.fa_decode(grp.q_fa[sel], sub, grp.w, grp.k, grp.scale,
+                                                   return_scores=True)
+    t_ = tol(kv.dtype)
+    assert max_abs(o[sel], o_r) <= t_, f"FA output error {max_abs(o[sel], o_r)}"
+    assert max_abs(lse[sel], lse_r) <= t_, f"lse error {max_abs(lse[sel], lse_r)}"
+    check_index_sets(idx[sel], cnt[sel], idx_r, cnt_r, scores, "decode ")
+    for j, osa in enumerate(sa):
+        # SA parity with the GPU's own index sets (near-tie swaps are not output errors) ...
+        ref = O.sa_decode(grp.q_sa[j][sel], sub, grp.w, idx[sel], cnt[sel], grp.scale)
+        assert max_abs(osa[sel], ref) <= t_, f"SA{j} error {max_abs(osa[sel], ref)}"
+    if sa:
+        # ... and with the oracle's index sets fed to both
+        import torch
+        dkv = kv_to_device(sub)
+        o2 = H.hs2_sa_reuse(to_torch(grp.q_sa[0][sel], kv.dtype), dkv, grp.w, to_torch(idx_r, "i32"),
+                            to_torch(cnt_r, "i32"), grp.k, grp.scale).cpu().numpy()
+        ref2 = O.sa_decode(grp.q_sa[0][sel], sub, grp.w, idx_r, cnt_r, grp.scale)
+        assert max_abs(o2, ref2) <= t_
+    return o, idx, cnt
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_ragged_small(H, dtype):
+    # lengths around page and window boundaries, a multi-split sequence, G=4 (padded MMA columns)
+    lens = [1, 15, 16, 17, 63, 64, 65, 100, 129, 1000, 3001, 4097]
+    grp = W.decode_group(lens, Hq=8, Hkv=2, d=128, w=16, k=64, dtype=dtype, seed=1, n_sa=2, needles=4)
+    check_group(H, grp)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_gqa8(H, d):
+    grp = W.decode_group([2000, 5000, 777, 4096], Hq=32, Hkv=4, d=d, w=128, k=256, dtype="bf16", seed=2,
+                         n_sa=1, needles=16)
+    check_group(H, grp)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(16, 1), (32, 1), (4, 4)])
+def test_decode_other_head_ratios(H, Hq, Hkv):
+    grp = W.decode_group([300, 1500], Hq=Hq, Hkv=Hkv, d=128, w=32, k=100, dtype="bf16", seed=3, n_sa=1,
+                         needles=8)
+    check_group(H, grp)
+
+
+def test_decode_sharp_logits(H):
+    # Q, K ~ N(0,1) without the 1/sqrt(d) damping: concentrated attention makes the set check bite
+    grp = W.decode_group([2500, 3300], Hq=8, Hkv=1, d=128, w=16, k=64, dtype="f32", seed=4, n_sa=1, needles=0)
+    o, idx, cnt = check_group(H, grp)
+    assert (cnt == 64).all()
+
+
+def test_decode_degenerate(H):
+    # k = 0; w = 0; w >= t; k >= far range
+    for w, k, lens in [(16, 0, [50, 200]), (0, 10, [50, 200]), (500, 10, [50, 200]), (8, 1000, [50, 200])]:
+        grp = W.decode_group(lens, Hq=4, Hkv=1, d=64, w=w, k=k, dtype="bf16", seed=5, n_sa=1, needles=0)
+        check_group(H, grp)
+
+
+def test_tiny_fp32_decode(H):
+    tg = W.tiny_group(seed=0)
+    o, idx, cnt = check_group(H, tg.decode)
+    assert set(tg.decode.needles[0].tolist()) <= set(idx[0, 0, :cnt[0, 0]].tolist())
+
+
+def test_bad_block_table_entry_is_flagged(H):
+    import torch
+
+    grp = W.decode_group([300, 300], Hq=8, Hkv=1, d=128, w=16, k=32, dtype="bf16", seed=6, n_sa=0, needles=0)
+    kv = grp.kv
+    bt = kv.block_table.copy()
+    bt[1, 2] = kv.num_pages + 5  # out of range: the kernels must skip and flag it
+    dkv = kv_to_device(W.PagedKV(k=kv.k, v=kv.v, block_table=bt, seq_len=kv.seq_len, dtype=kv.dtype))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    H.hs2_fa_select(to_torch(grp.q_fa, "bf16"), dkv, 16, 32, grp.scale, max_t=300, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & H.DEV_BAD_PAGE
+
+
+@pytest.mark.slow
+def test_decode_bf16_full_size_sampled(H):
+    """Decode workload at full size (B=64, t ~ U[16K, 32K], Hq=32, Hkv=4, d=128, w=128, k=1024,
+    five SA layers): every sequence checked for set invariants, 6 sampled sequences against the
+    oracle element by element."""
+    grp = W.decode_bf16_workload(seed=0)
+    rng = np.random.default_rng(123)
+    sample = sorted(rng.choice(64, size=6, replace=False).tolist())
+    o, idx, cnt = check_group(H, grp, batches=sample)
+    t = grp.kv.seq_len
+    assert np.array_equal(cnt, np.repeat(np.minimum(1024, t - 128)[:, None], 4, 1))
+    for b in range(64):
+        for g in range(4):
+            s = idx[b, g, :cnt[b, g]]
+            assert s.min() >= 0 and s.max() < t[b] - 128 and np.all(np.diff(s) > 0)
+            assert set(grp.needles[b].tolist()) <= set(s.tolist())

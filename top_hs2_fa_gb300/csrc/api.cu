@@ -1,0 +1,317 @@
+// api.cu — the extern "C" boundary of libhs2: argument validation, workspace layout,
+// launches. No allocation, no synchronisation; every call is asynchronous on `stream`.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "../../include/hs2.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+thread_local void* g_prof[3][2] = {{nullptr, nullptr}, {nullptr, nullptr}, {nullptr, nullptr}};
+
+// Records the one-shot profiling events of `stage` around `launch` (a callable returning cudaError_t).
+template <typename F>
+cudaError_t profiled(int stage, cudaStream_t s, F launch) {
+  void* ev0 = g_prof[stage][0];
+  void* ev1 = g_prof[stage][1];
+  g_prof[stage][0] = g_prof[stage][1] = nullptr;
+  if (ev0) {
+    cudaError_t e = cudaEventRecord((cudaEvent_t)ev0, s);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = launch();
+  if (e == cudaSuccess && ev1) e = cudaEventRecord((cudaEvent_t)ev1, s);
+  return e;
+}
+
+hs2_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  (void)cudaGetLastError();  // clear the sticky-free error state of the calling thread
+  return HS2_ERR_CUDA;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+bool valid_kv(const hs2_kv* kv, bool need_v) {
+  if (!kv || !kv->k || !kv->block_table || !kv->seq_len) return false;
+  if (need_v && !kv->v) return false;
+  if (kv->batch < 1 || kv->num_pages < 1 || kv->max_pages < 1 || kv->Hkv < 1) return false;
+  if (kv->page_size != 64) return false;
+  if (kv->d != 64 && kv->d != 128) return false;
+  if (kv->dtype != HS2_F32 && kv->dtype != HS2_BF16) return false;
+  if (!aligned16(kv->k) || (need_v && !aligned16(kv->v))) return false;
+  return true;
+}
+
+bool pow2_le32(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16 || g == 32; }
+
+// ---------------------------------------------------------------------------- FA layout
+struct FaPlan {
+  bool mma;   // bf16 tensor-core scan (else CUDA-core)
+  int pps;    // pages per split
+  int nsplit;
+  long long ld;  // logits row length
+  size_t off_ml, off_o, off_logits, off_scores, total;
+};
+
+FaPlan fa_plan(int Bq, int Hq, const hs2_kv* kv, int max_t) {
+  FaPlan p{};
+  const int G = Hq / kv->Hkv;
+  p.mma = kv->dtype == HS2_BF16 && G <= 32 && (G <= 8 || G == 16 || G == 32);
+  const int maxpg = cdiv(max_t, 64);
+  if (p.mma) {
+    // enough CTAs to fill 152 SMs several times over, splits of at most 16 pages
+    p.pps = 16;
+    while (p.pps > 1 && (long long)Bq * kv->Hkv * cdiv(maxpg, p.pps) < 152LL * 8) p.pps >>= 1;
+  } else {
+    p.pps = 2;
+  }
+  p.nsplit = cdiv(maxpg, p.pps);
+  p.ld = (long long)maxpg * 64;
+  size_t off = 0;
+  p.off_ml = off;
+  off = align256(off + (size_t)Bq * Hq * p.nsplit * sizeof(float) * 2);
+  p.off_o = off;
+  off = align256(off + (size_t)Bq * Hq * p.nsplit * kv->d * sizeof(float));
+  p.off_logits = off;
+  off = align256(off + (size_t)Bq * Hq * p.ld * sizeof(float));
+  p.off_scores = off;
+  off = align256(off + (size_t)Bq * kv->Hkv * p.ld * sizeof(uint32_t));
+  p.total = off;
+  return p;
+}
+
+struct SaPlan {
+  int nsplit;
+  size_t off_ml, off_o, total;
+};
+
+SaPlan sa_plan(int Bq, int Hq, const hs2_kv* kv, int w, int k) {
+  SaPlan p{};
+  p.nsplit = std::max(1, cdiv((long long)w + k, 128));
+  size_t off = 0;
+  p.off_ml = off;
+  off = align256(off + (size_t)Bq * Hq * p.nsplit * sizeof(float) * 2);
+  p.off_o = off;
+  off = align256(off + (size_t)Bq * Hq * p.nsplit * kv->d * sizeof(float));
+  p.total = off;
+  return p;
+}
+
+hs2_status common_checks(const void* q, int Bq, int Hq, const hs2_kv* kv, int prefill, bool need_v) {
+  if (!valid_kv(kv, need_v)) return HS2_ERR_ARG;
+  if (!q || !aligned16(q) || Bq < 0 || Hq < 1) return HS2_ERR_ARG;
+  if (Hq % kv->Hkv != 0) return HS2_ERR_ARG;
+  if (!pow2_le32(Hq / kv->Hkv)) return HS2_ERR_UNSUPPORTED;
+  if (prefill) {
+    if (kv->batch != 1) return HS2_ERR_ARG;
+    if ((long long)Bq > (long long)kv->max_pages * 64) return HS2_ERR_ARG;
+  } else if (Bq != kv->batch) {
+    return HS2_ERR_ARG;
+  }
+  return HS2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int hs2_abi_version(void) { return HS2_ABI_VERSION; }
+
+void hs2_profile_next(hs2_stage stage, void* start, void* stop) {
+  if ((int)stage < 0 || (int)stage > 2) return;
+  g_prof[stage][0] = start;
+  g_prof[stage][1] = stop;
+}
+
+int hs2_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* hs2_strerror(hs2_status st) {
+  switch (st) {
+    case HS2_OK: return "ok";
+    case HS2_ERR_ARG: return "invalid argument";
+    case HS2_ERR_UNSUPPORTED: return "unsupported configuration";
+    case HS2_ERR_CUDA: return "CUDA launch or runtime error";
+    case HS2_ERR_DEVICE: return "device-side error flag set";
+  }
+  return "unknown status";
+}
+
+size_t hs2_fa_select_workspace(int B_or_n, int Hq, const hs2_kv* kv, int max_t, int k, int prefill) {
+  (void)k;
+  (void)prefill;
+  if (!kv || kv->Hkv < 1 || Hq < 1 || max_t < 1 || B_or_n < 0 || (kv->d != 64 && kv->d != 128)) return 0;
+  return fa_plan(B_or_n, Hq, kv, max_t).total;
+}
+
+hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w, int k,
+                         float scale, int prefill, float* o, float* lse, int32_t* idx, int32_t* idx_cnt,
+                         void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  hs2_status st = common_checks(q, B_or_n, Hq, kv, prefill, true);
+  if (st != HS2_OK) return st;
+  if (w < 0 || k < 0 || max_t < 1 || !std::isfinite(scale)) return HS2_ERR_ARG;
+  if ((long long)max_t > (long long)kv->max_pages * 64) return HS2_ERR_ARG;
+  if (prefill && B_or_n > max_t) return HS2_ERR_ARG;
+  if (!o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
+  if (B_or_n == 0) return HS2_OK;
+  const FaPlan p = fa_plan(B_or_n, Hq, kv, max_t);
+  if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+
+  hs2::AttnArgs a{};
+  a.q = q;
+  a.Hq = Hq;
+  a.G = Hq / kv->Hkv;
+  a.D = kv->d;
+  a.k = kv->k;
+  a.v = kv->v;
+  a.bt = kv->block_table;
+  a.seq_len = kv->seq_len;
+  a.max_pages = kv->max_pages;
+  a.num_pages = kv->num_pages;
+  a.Hkv = kv->Hkv;
+  a.max_t = max_t;
+  a.prefill = prefill ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.gather = 0;
+  a.pps = p.pps;
+  a.nsplit = p.nsplit;
+  a.part_ml = (float2*)(ws + p.off_ml);
+  a.part_o = (float*)(ws + p.off_o);
+  a.logits = (float*)(ws + p.off_logits);
+  a.ld_logits = p.ld;
+  a.dev_err = dev_err;
+  cudaError_t e = profiled(HS2_STAGE_FA_SCAN, s, [&] {
+    return p.mma ? hs2::launch_fa_decode_mma(a, B_or_n, s)
+                 : hs2::launch_attn_partial(a, B_or_n, kv->dtype == HS2_BF16, s);
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  hs2::CombineArgs c{};
+  c.part_ml = a.part_ml;
+  c.part_o = a.part_o;
+  c.nsplit = p.nsplit;
+  c.G = a.G;
+  c.Hq = Hq;
+  c.Hkv = kv->Hkv;
+  c.D = kv->d;
+  c.prefill = a.prefill;
+  c.seq_len = kv->seq_len;
+  c.max_pages = kv->max_pages;
+  c.max_t = max_t;
+  c.gather = 0;
+  c.w = w;
+  c.pps = p.pps;
+  c.o = o;
+  c.lse = lse;
+  c.select = 1;
+  c.k = k;
+  c.kcap = k;
+  c.idx = idx;
+  c.cnt = idx_cnt;
+  c.logits = a.logits;
+  c.scores = (uint32_t*)(ws + p.off_scores);
+  c.ld_logits = p.ld;
+  c.dev_err = dev_err;
+  e = hs2::launch_combine(c, B_or_n, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return HS2_OK;
+}
+
+size_t hs2_sa_reuse_workspace(int B_or_n, int Hq, const hs2_kv* kv, int w, int k, int prefill) {
+  (void)prefill;
+  if (!kv || kv->Hkv < 1 || Hq < 1 || B_or_n < 0 || w < 0 || k < 0 || (kv->d != 64 && kv->d != 128)) return 0;
+  return sa_plan(B_or_n, Hq, kv, w, k).total;
+}
+
+hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int w, const int32_t* idx,
+                        const int32_t* idx_cnt, int k, float scale, int prefill, float* o, void* workspace,
+                        size_t ws_bytes, int32_t* dev_err, void* stream) {
+  hs2_status st = common_checks(q, B_or_n, Hq, kv, prefill, true);
+  if (st != HS2_OK) return st;
+  if (w < 0 || k < 0 || !std::isfinite(scale) || !o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
+  if (B_or_n == 0) return HS2_OK;
+  const SaPlan p = sa_plan(B_or_n, Hq, kv, w, k);
+  if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+
+  hs2::AttnArgs a{};
+  a.q = q;
+  a.Hq = Hq;
+  a.G = Hq / kv->Hkv;
+  a.D = kv->d;
+  a.k = kv->k;
+  a.v = kv->v;
+  a.bt = kv->block_table;
+  a.seq_len = kv->seq_len;
+  a.max_pages = kv->max_pages;
+  a.num_pages = kv->num_pages;
+  a.Hkv = kv->Hkv;
+  a.max_t = prefill ? B_or_n : kv->max_pages * 64;
+  a.prefill = prefill ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.gather = 1;
+  a.pps = 1;
+  a.nsplit = p.nsplit;
+  a.w = w;
+  a.idx = idx;
+  a.cnt = idx_cnt;
+  a.kcap = k;
+  a.part_ml = (float2*)(ws + p.off_ml);
+  a.part_o = (float*)(ws + p.off_o);
+  a.logits = nullptr;
+  a.dev_err = dev_err;
+  cudaError_t e = profiled(HS2_STAGE_SA_GATHER, s,
+                           [&] { return hs2::launch_attn_partial(a, B_or_n, kv->dtype == HS2_BF16, s); });
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  hs2::CombineArgs c{};
+  c.part_ml = a.part_ml;
+  c.part_o = a.part_o;
+  c.nsplit = p.nsplit;
+  c.G = a.G;
+  c.Hq = Hq;
+  c.Hkv = kv->Hkv;
+  c.D = kv->d;
+  c.prefill = a.prefill;
+  c.seq_len = kv->seq_len;
+  c.max_pages = kv->max_pages;
+  c.max_t = a.max_t;
+  c.gather = 1;
+  c.w = w;
+  c.sa_cnt = idx_cnt;
+  c.kcap = k;
+  c.o = o;
+  c.select = 0;
+  c.dev_err = dev_err;
+  e = hs2::launch_combine(c, B_or_n, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return HS2_OK;
+}
+
+size_t hs2_hier_reindex_workspace(hs2_idx_mode mode, int Hi, const hs2_kv* k_idx, int max_t, int k_top,
+                                  int blk, int max_blocks) {
+  (void)mode; (void)Hi; (void)k_idx; (void)max_t; (void)k_top; (void)blk; (void)max_blocks;
+  return 0;
+}
+
+hs2_status hs2_hier_reindex(hs2_idx_mode mode, const void* q_idx, const float* w_idx, int Hi,
+                            const hs2_kv* k_idx, int max_t, int k_top, int blk, int max_blocks,
+                            int32_t* pool_blocks, int32_t* pool_cnt, int32_t* idx, int32_t* idx_cnt,
+                            void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  (void)mode; (void)q_idx; (void)w_idx; (void)Hi; (void)k_idx; (void)max_t; (void)k_top; (void)blk;
+  (void)max_blocks; (void)pool_blocks; (void)pool_cnt; (void)idx; (void)idx_cnt; (void)workspace;
+  (void)ws_bytes; (void)dev_err; (void)stream;
+  return HS2_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// common.cuh — device helpers shared by the hs2 kernels (sm_103a).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hs2.h"
+
+#define HS2_DEVI __device__ __forceinline__
+
+namespace hs2 {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kPage = 64;
+
+// ---------------------------------------------------------------------------- element access
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static HS2_DEVI float to_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static HS2_DEVI float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+};
+
+HS2_DEVI float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+HS2_DEVI float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+HS2_DEVI uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+HS2_DEVI uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+HS2_DEVI void flag_error(int32_t* dev_err, int bits) {
+  if (dev_err) atomicOr(dev_err, bits);
+}
+
+// ---------------------------------------------------------------------------- warp helpers
+HS2_DEVI float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+HS2_DEVI float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// exp2 of a (possibly -inf) base-2 logit relative to a (possibly -inf) max:
+// a row whose max is still -inf contributes exactly zero.
+HS2_DEVI float exp2_rel(float x, float m) { return (m == -INFINITY) ? 0.f : exp2f(x - m); }
+
+// m16n8k16 bf16 MMA with fp32 accumulate (legacy warp-level tensor path; used where
+// one warp owns a small contraction: decode FA over 8 query heads)
+HS2_DEVI void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+HS2_DEVI uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------------------- query geometry
+// Query qi of a call: decode -> sequence qi, t = seq_len[qi];
+// prefill -> sequence 0, t = qi + 1 (causal row qi).
+struct QueryGeom {
+  int b;
+  int t;
+};
+HS2_DEVI QueryGeom query_geom(int qi, int prefill, const int32_t* seq_len) {
+  QueryGeom q;
+  if (prefill) {
+    q.b = 0;
+    q.t = qi + 1;
+  } else {
+    q.b = qi;
+    q.t = seq_len[qi];
+  }
+  return q;
+}
+
+}  // namespace hs2

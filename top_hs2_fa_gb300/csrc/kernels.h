@@ -1,0 +1,65 @@
+// kernels.h — launch parameters shared between the C ABI layer and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hs2 {
+
+constexpr int kCombineThreads = 512;
+
+// One attention pass over a set of rows of one group's paged KV, producing per
+// (query, head, chunk) partial softmax state (m, l in base 2; unnormalised o).
+struct AttnArgs {
+  const void* q;  // [Bq][Hq][D], kv dtype
+  int Hq, G, D;
+  const void* k;
+  const void* v;
+  const int32_t* bt;
+  const int32_t* seq_len;
+  int max_pages, num_pages, Hkv;
+  int max_t;         // host-declared bound on t; longer queries are flagged and skipped
+  int prefill;       // 1: query qi is causal row qi of sequence 0 (t = qi + 1)
+  float scale_log2;  // softmax scale * log2(e)
+  int gather;        // 0: rows = split of pps pages (FA); 1: rows = W(t) ∪ S(t) (SA)
+  int pps;           // pages per split (FA)
+  int nsplit;        // chunk stride of the partial arrays
+  int w;
+  const int32_t* idx;  // [Bq][Hkv][kcap] (SA)
+  const int32_t* cnt;  // [Bq][Hkv] (SA)
+  int kcap;
+  float2* part_ml;  // [Bq][Hq][nsplit]
+  float* part_o;    // [Bq][Hq][nsplit][D]
+  float* logits;    // [Bq][Hq][ld_logits] base-2 logits, or null
+  long long ld_logits;
+  int32_t* dev_err;
+};
+
+struct CombineArgs {
+  const float2* part_ml;
+  const float* part_o;
+  int nsplit, G, Hq, Hkv, D;
+  int prefill;
+  const int32_t* seq_len;
+  int max_pages;
+  int max_t;
+  int gather;  // partials are SA chunks of 128 rows of W ∪ S (1) or FA splits of pps pages (0)
+  int w;
+  const int32_t* sa_cnt;  // SA: [Bq][Hkv] selected counts
+  int pps;
+  float* o;    // [Bq][Hq][D]
+  float* lse;  // [Bq][Hq] natural log, or null
+  int select;  // 1: run the window-excluding top-k from the logits
+  int k, kcap;
+  int32_t* idx;  // [Bq][Hkv][kcap]
+  int32_t* cnt;  // [Bq][Hkv]
+  const float* logits;
+  uint32_t* scores;  // [Bq][Hkv][ld_logits] scratch
+  long long ld_logits;
+  int32_t* dev_err;
+};
+
+cudaError_t launch_fa_decode_mma(const AttnArgs& a, int Bq, cudaStream_t s);
+cudaError_t launch_attn_partial(const AttnArgs& a, int Bq, int bf16, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s);
+
+}  // namespace hs2

@@ -1,0 +1,216 @@
+"""Thin Python binding of libhs2 (argument marshalling only).
+
+Functions carry the C names (``hs2_fa_select``, ``hs2_sa_reuse``,
+``hs2_hier_reindex``, the ``*_workspace`` queries) and take torch CUDA tensors;
+every step of the path runs in the library's kernels. PyTorch only provides
+device memory and the current stream. There is no fallback: if the library
+cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+F32, BF16 = 0, 1
+FULL, REINDEX = 0, 1
+DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH = 1, 2, 4, 8
+EXPORTS = (
+    "hs2_fa_select_workspace", "hs2_fa_select", "hs2_sa_reuse_workspace", "hs2_sa_reuse",
+    "hs2_hier_reindex_workspace", "hs2_hier_reindex", "hs2_strerror", "hs2_last_cuda_error",
+    "hs2_abi_version", "hs2_profile_next",
+)
+STAGE_FA_SCAN, STAGE_SA_GATHER, STAGE_INDEXER = 0, 1, 2
+
+
+class hs2_kv(ctypes.Structure):
+    _fields_ = [
+        ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+        ("seq_len", ctypes.c_void_p), ("batch", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+        ("max_pages", ctypes.c_int32), ("page_size", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32), ("dtype", ctypes.c_int32),
+    ]
+
+
+class HS2Error(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libhs2.so (built in-tree by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise HS2Error(f"libhs2 not built ({path}); run top_hs2_fa_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    kvp = ctypes.POINTER(hs2_kv)
+    lib.hs2_fa_select_workspace.argtypes = [i32, i32, kvp, i32, i32, i32]
+    lib.hs2_fa_select_workspace.restype = sz
+    lib.hs2_fa_select.argtypes = [vp, i32, i32, kvp, i32, i32, i32, f32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.hs2_fa_select.restype = i32
+    lib.hs2_sa_reuse_workspace.argtypes = [i32, i32, kvp, i32, i32, i32]
+    lib.hs2_sa_reuse_workspace.restype = sz
+    lib.hs2_sa_reuse.argtypes = [vp, i32, i32, kvp, i32, vp, vp, i32, f32, i32, vp, vp, sz, vp, vp]
+    lib.hs2_sa_reuse.restype = i32
+    lib.hs2_hier_reindex_workspace.argtypes = [i32, i32, kvp, i32, i32, i32, i32]
+    lib.hs2_hier_reindex_workspace.restype = sz
+    lib.hs2_hier_reindex.argtypes = [i32, vp, vp, i32, kvp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.hs2_hier_reindex.restype = i32
+    lib.hs2_strerror.argtypes = [i32]
+    lib.hs2_strerror.restype = ctypes.c_char_p
+    lib.hs2_last_cuda_error.restype = i32
+    lib.hs2_abi_version.restype = i32
+    lib.hs2_profile_next.argtypes = [i32, vp, vp]
+    lib.hs2_profile_next.restype = None
+    _lib = lib
+    return lib
+
+
+def _check(st: int) -> None:
+    if st != 0:
+        lib = load()
+        msg = lib.hs2_strerror(st).decode()
+        if st == -3:
+            msg += f" (cudaError {lib.hs2_last_cuda_error()})"
+        raise HS2Error(f"hs2 status {st}: {msg}")
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+@dataclass
+class KV:
+    """Device tensors of one group's paged KV cache."""
+
+    k: torch.Tensor  # [num_pages][Hkv][64][d], float32 or bfloat16
+    v: torch.Tensor | None
+    block_table: torch.Tensor  # int32 [B][max_pages]
+    seq_len: torch.Tensor  # int32 [B]
+
+    def c(self) -> hs2_kv:
+        dt = BF16 if self.k.dtype == torch.bfloat16 else F32
+        if self.k.dtype not in (torch.bfloat16, torch.float32):
+            raise HS2Error(f"unsupported KV dtype {self.k.dtype}")
+        for t in (self.k, self.v, self.block_table, self.seq_len):
+            if t is not None and not t.is_contiguous():
+                raise HS2Error("KV tensors must be contiguous")
+        return hs2_kv(_ptr(self.k), _ptr(self.v), _ptr(self.block_table), _ptr(self.seq_len),
+                      int(self.seq_len.shape[0]), int(self.k.shape[0]), int(self.block_table.shape[1]),
+                      int(self.k.shape[2]), int(self.k.shape[1]), int(self.k.shape[3]), dt)
+
+
+def _workspace(nbytes: int, device, ws):
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise HS2Error("workspace too small")
+        return ws
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def hs2_fa_select_workspace(B_or_n: int, Hq: int, kv: KV, max_t: int, k: int, prefill: bool = False) -> int:
+    c = kv.c()
+    return int(load().hs2_fa_select_workspace(B_or_n, Hq, ctypes.byref(c), max_t, k, int(prefill)))
+
+
+def hs2_fa_select(q: torch.Tensor, kv: KV, w: int, k: int, scale: float, prefill: bool = False,
+                  max_t: int | None = None, out=None, workspace=None, dev_err=None, stream=None):
+    """FA layer + window-excluding top-k. Returns (o, lse, idx, idx_cnt) (float32, float32,
+    int32, int32). ``max_t`` defaults to the table's capacity (decode) or n (prefill)."""
+    lib = load()
+    Bq, Hq, d = q.shape
+    c = kv.c()
+    Hkv = c.Hkv
+    if max_t is None:
+        max_t = Bq if prefill else c.max_pages * c.page_size
+    dev = q.device
+    if out is None:
+        o = torch.empty((Bq, Hq, d), dtype=torch.float32, device=dev)
+        lse = torch.empty((Bq, Hq), dtype=torch.float32, device=dev)
+        idx = torch.empty((Bq, Hkv, k), dtype=torch.int32, device=dev)
+        cnt = torch.empty((Bq, Hkv), dtype=torch.int32, device=dev)
+    else:
+        o, lse, idx, cnt = out
+    nb = int(lib.hs2_fa_select_workspace(Bq, Hq, ctypes.byref(c), max_t, k, int(prefill)))
+    ws = _workspace(nb, dev, workspace)
+    st = lib.hs2_fa_select(_ptr(q), Bq, Hq, ctypes.byref(c), max_t, w, k, float(scale), int(prefill),
+                           _ptr(o), _ptr(lse), _ptr(idx), _ptr(cnt), _ptr(ws), ws.numel() * ws.element_size(),
+                           _ptr(dev_err), _stream(stream))
+    _check(st)
+    return o, lse, idx, cnt
+
+
+def hs2_sa_reuse_workspace(B_or_n: int, Hq: int, kv: KV, w: int, k: int, prefill: bool = False) -> int:
+    c = kv.c()
+    return int(load().hs2_sa_reuse_workspace(B_or_n, Hq, ctypes.byref(c), w, k, int(prefill)))
+
+
+def hs2_sa_reuse(q: torch.Tensor, kv: KV, w: int, idx: torch.Tensor, idx_cnt: torch.Tensor, k: int,
+                 scale: float, prefill: bool = False, out=None, workspace=None, dev_err=None, stream=None):
+    """SA layer reusing the FA's KV and indices with its own query. Returns o (float32)."""
+    lib = load()
+    Bq, Hq, d = q.shape
+    c = kv.c()
+    o = out if out is not None else torch.empty((Bq, Hq, d), dtype=torch.float32, device=q.device)
+    nb = int(lib.hs2_sa_reuse_workspace(Bq, Hq, ctypes.byref(c), w, k, int(prefill)))
+    ws = _workspace(nb, q.device, workspace)
+    st = lib.hs2_sa_reuse(_ptr(q), Bq, Hq, ctypes.byref(c), w, _ptr(idx), _ptr(idx_cnt), k, float(scale),
+                          int(prefill), _ptr(o), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_err),
+                          _stream(stream))
+    _check(st)
+    return o
+
+
+def hs2_hier_reindex_workspace(mode: int, Hi: int, k_idx: KV, max_t: int, k_top: int, blk: int,
+                               max_blocks: int) -> int:
+    c = k_idx.c()
+    return int(load().hs2_hier_reindex_workspace(mode, Hi, ctypes.byref(c), max_t, k_top, blk, max_blocks))
+
+
+def hs2_hier_reindex(mode: int, q_idx: torch.Tensor, w_idx: torch.Tensor, k_idx: KV, k_top: int, blk: int,
+                     max_blocks: int, pool_blocks=None, pool_cnt=None, max_t: int | None = None, out=None,
+                     workspace=None, dev_err=None, stream=None):
+    """CSA2 hierarchical indexer (Full or Reindex). Returns (idx, idx_cnt, pool_blocks, pool_cnt)."""
+    lib = load()
+    B, Hi, di = q_idx.shape
+    c = k_idx.c()
+    dev = q_idx.device
+    if max_t is None:
+        max_t = c.max_pages * c.page_size
+    if pool_blocks is None:
+        pool_blocks = torch.empty((B, max_blocks), dtype=torch.int32, device=dev)
+        pool_cnt = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out is None:
+        idx = torch.empty((B, k_top), dtype=torch.int32, device=dev)
+        cnt = torch.empty((B,), dtype=torch.int32, device=dev)
+    else:
+        idx, cnt = out
+    nb = int(lib.hs2_hier_reindex_workspace(mode, Hi, ctypes.byref(c), max_t, k_top, blk, max_blocks))
+    ws = _workspace(nb, dev, workspace)
+    st = lib.hs2_hier_reindex(mode, _ptr(q_idx), _ptr(w_idx), Hi, ctypes.byref(c), max_t, k_top, blk,
+                              max_blocks, _ptr(pool_blocks), _ptr(pool_cnt), _ptr(idx), _ptr(cnt), _ptr(ws),
+                              ws.numel() * ws.element_size(), _ptr(dev_err), _stream(stream))
+    _check(st)
+    return idx, cnt, pool_blocks, pool_cnt
+
+
+def hs2_profile_next(stage: int, start, stop) -> None:
+    """Have the next call running ``stage`` record torch.cuda.Event ``start``/``stop`` around
+    its main kernel (events must already have been recorded once so that they exist)."""
+    load().hs2_profile_next(stage, start.cuda_event if start is not None else None,
+                            stop.cuda_event if stop is not None else None)
