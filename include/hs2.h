@@ -55,7 +55,8 @@ typedef enum {
   HS2_ERR_ARG = -1,         /* invalid shape, pointer, alignment or workspace size */
   HS2_ERR_UNSUPPORTED = -2, /* valid but not implemented combination (e.g. head_dim 96) */
   HS2_ERR_CUDA = -3,        /* a CUDA launch / runtime call failed */
-  HS2_ERR_DEVICE = -4       /* reserved for callers that fold dev_err into a status */
+  HS2_ERR_DEVICE = -4,      /* reserved for callers that fold dev_err into a status */
+  HS2_ERR_SCRATCH_LIMIT = -5 /* problem needs more scratch than hs2_fa_select_noalloc holds */
 } hs2_status;
 
 /* device-side error bits (ORed into *dev_err) */
@@ -112,6 +113,27 @@ hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, in
                          int k, float scale, int prefill, float* o, float* lse, int32_t* idx,
                          int32_t* idx_cnt, void* workspace, size_t ws_bytes, int32_t* dev_err,
                          void* stream);
+
+/* ---------------------------------------------------------------------------
+ * hs2_fa_select_noalloc — hs2_fa_select for callers that cannot allocate device
+ * memory (an engine that has reserved nearly all HBM for its KV pool and forbids
+ * further cudaMalloc, or a latency-critical thread that must not call cudaMalloc /
+ * cudaFree because they can synchronise the device). It takes no workspace: its
+ * scratch is a file-scope device array of hs2_fa_select_noalloc_capacity() bytes
+ * (64 MiB) that every GPU loading the library holds until the process exits. The
+ * pages have no counterpart to this entry point; it is a deployment convenience.
+ * Arguments, outputs and results are exactly those of hs2_fa_select.
+ * - Returns HS2_ERR_SCRATCH_LIMIT, launching nothing, when
+ *   hs2_fa_select_workspace(...) of the call exceeds the capacity.
+ * - The first call on a device looks up the array's device address on that device
+ *   (it must be the current device); make that first call before any stream capture.
+ * - All calls share the one array: calls that overlap on the GPU (concurrent streams
+ *   or host threads) race and corrupt each other's results; serialise them.
+ * - It allocates nothing and calls no cudaMalloc / cudaFree.                        */
+size_t hs2_fa_select_noalloc_capacity(void);
+hs2_status hs2_fa_select_noalloc(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w,
+                                 int k, float scale, int prefill, float* o, float* lse, int32_t* idx,
+                                 int32_t* idx_cnt, int32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------------------
  * SA layer: KV and index reuse with the layer's own query  ([HS2] §5, §7.2, §7.4).

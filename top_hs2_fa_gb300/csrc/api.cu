@@ -140,6 +140,7 @@ const char* hs2_strerror(hs2_status st) {
     case HS2_ERR_UNSUPPORTED: return "unsupported configuration";
     case HS2_ERR_CUDA: return "CUDA launch or runtime error";
     case HS2_ERR_DEVICE: return "device-side error flag set";
+    case HS2_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the no-allocation entry point holds";
   }
   return "unknown status";
 }

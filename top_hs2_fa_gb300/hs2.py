@@ -22,7 +22,7 @@ DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH = 1, 2, 4, 8
 EXPORTS = (
     "hs2_fa_select_workspace", "hs2_fa_select", "hs2_sa_reuse_workspace", "hs2_sa_reuse",
     "hs2_hier_reindex_workspace", "hs2_hier_reindex", "hs2_strerror", "hs2_last_cuda_error",
-    "hs2_abi_version", "hs2_profile_next",
+    "hs2_abi_version", "hs2_profile_next", "hs2_fa_select_noalloc", "hs2_fa_select_noalloc_capacity",
 )
 STAGE_FA_SCAN, STAGE_SA_GATHER, STAGE_INDEXER = 0, 1, 2
 
@@ -72,6 +72,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.hs2_abi_version.restype = i32
     lib.hs2_profile_next.argtypes = [i32, vp, vp]
     lib.hs2_profile_next.restype = None
+    lib.hs2_fa_select_noalloc.argtypes = [vp, i32, i32, kvp, i32, i32, i32, f32, i32, vp, vp, vp, vp, vp, vp]
+    lib.hs2_fa_select_noalloc.restype = i32
+    lib.hs2_fa_select_noalloc_capacity.argtypes = []
+    lib.hs2_fa_select_noalloc_capacity.restype = sz
     _lib = lib
     return lib
 
@@ -214,3 +218,27 @@ def hs2_profile_next(stage: int, start, stop) -> None:
     its main kernel (events must already have been recorded once so that they exist)."""
     load().hs2_profile_next(stage, start.cuda_event if start is not None else None,
                             stop.cuda_event if stop is not None else None)
+
+
+def hs2_fa_select_noalloc(q: torch.Tensor, kv: KV, w: int, k: int, scale: float, prefill: bool = False,
+                          max_t: int | None = None, out=None, dev_err=None, stream=None):
+    """hs2_fa_select without a workspace, for callers that cannot allocate device memory:
+    the library's own static scratch (hs2_fa_select_noalloc_capacity() bytes) is used.
+    Only the outputs are allocated here when ``out`` is None; pass ``out`` to allocate
+    nothing. Concurrent calls on the GPU race on the shared scratch."""
+    lib = load()
+    Bq, Hq, d = q.shape
+    c = kv.c()
+    if max_t is None:
+        max_t = Bq if prefill else c.max_pages * c.page_size
+    if out is None:
+        dev = q.device
+        out = (torch.empty((Bq, Hq, d), dtype=torch.float32, device=dev),
+               torch.empty((Bq, Hq), dtype=torch.float32, device=dev),
+               torch.empty((Bq, c.Hkv, k), dtype=torch.int32, device=dev),
+               torch.empty((Bq, c.Hkv), dtype=torch.int32, device=dev))
+    o, lse, idx, cnt = out
+    st = lib.hs2_fa_select_noalloc(_ptr(q), Bq, Hq, ctypes.byref(c), max_t, w, k, float(scale), int(prefill),
+                                   _ptr(o), _ptr(lse), _ptr(idx), _ptr(cnt), _ptr(dev_err), _stream(stream))
+    _check(st)
+    return o, lse, idx, cnt
