@@ -85,7 +85,7 @@ def test_decode_gqa8(H, d):
     check_group(H, grp)
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(16, 1), (32, 1), (4, 4)])
+@pytest.mark.parametrize("Hq,Hkv", [(16, 1), (32, 1), (4, 4), (8, 4)])
 def test_decode_other_head_ratios(H, Hq, Hkv):
     grp = W.decode_group([300, 1500], Hq=Hq, Hkv=Hkv, d=128, w=32, k=100, dtype="bf16", seed=3, n_sa=1,
                          needles=8)

@@ -58,7 +58,7 @@ struct FaPlan {
   int pps;    // pages per split
   int nsplit;
   long long ld;  // logits row length
-  size_t off_ml, off_o, off_logits, off_scores, total;
+  size_t off_ml, off_o, off_logits, off_scores, off_hist, total;
 };
 
 FaPlan fa_plan(int Bq, int Hq, const hs2_kv* kv, int max_t) {
@@ -84,6 +84,8 @@ FaPlan fa_plan(int Bq, int Hq, const hs2_kv* kv, int max_t) {
   off = align256(off + (size_t)Bq * Hq * p.ld * sizeof(float));
   p.off_scores = off;
   off = align256(off + (size_t)Bq * kv->Hkv * p.ld * sizeof(uint32_t));
+  p.off_hist = off;
+  off = align256(off + (size_t)Bq * kv->Hkv * 4096 * sizeof(uint32_t));
   p.total = off;
   return p;
 }
@@ -220,8 +222,12 @@ hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, in
   c.cnt = idx_cnt;
   c.logits = a.logits;
   c.scores = (uint32_t*)(ws + p.off_scores);
+  c.hist = (uint32_t*)(ws + p.off_hist);
   c.ld_logits = p.ld;
+  c.smem_keys = (int)std::min<long long>(p.ld, hs2::kMaxSmemKeys);
   c.dev_err = dev_err;
+  e = cudaMemsetAsync(c.hist, 0, (size_t)B_or_n * kv->Hkv * 4096 * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e);
   e = hs2::launch_combine(c, B_or_n, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return HS2_OK;
@@ -270,7 +276,14 @@ hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int
   a.part_ml = (float2*)(ws + p.off_ml);
   a.part_o = (float*)(ws + p.off_o);
   a.logits = nullptr;
+  a.out_o = o;
   a.dev_err = dev_err;
+  if (hs2::sa_gather_supported(a.G, a.D, kv->dtype == HS2_BF16)) {
+    // one CTA per (query, KV head) stages W ∪ S through shared memory; no partials
+    cudaError_t e = profiled(HS2_STAGE_SA_GATHER, s, [&] { return hs2::launch_sa_gather(a, B_or_n, s); });
+    if (e != cudaSuccess) return cuda_fail(e);
+    return HS2_OK;
+  }
   cudaError_t e = profiled(HS2_STAGE_SA_GATHER, s,
                            [&] { return hs2::launch_attn_partial(a, B_or_n, kv->dtype == HS2_BF16, s); });
   if (e != cudaSuccess) return cuda_fail(e);

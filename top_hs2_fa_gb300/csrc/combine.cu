@@ -1,110 +1,200 @@
-// combine.cu — merge of split softmax partials, plus the window-excluding top-k.
+// combine.cu — merge of split softmax partials, and the window-excluding top-k.
 //
 // The selection score of a far position is the FA's own attention probability summed
 // over the query heads of a KV head ("HySparse2：整体架构、KV 生命周期与 PD 分离", §5 and
-// the appendix on the FA's "oracle" scores); ranking uses the final per-head normaliser,
-// so it runs after the merge, from the base-2 logits the scan wrote. Ties go to the lower
-// position; the result is sorted ascending (§7.2: the window is excluded from the budget).
+// the appendix on the FA's "oracle" scores). Ranking needs the final per-head
+// normaliser, so it runs after the scan, from the base-2 logits the scan wrote. Ties go
+// to the lower position; the result is sorted ascending; the window is excluded from
+// the candidates (§7.2).
+//
+// merge_score_kernel  grid (score chunks, Hkv, queries), 256 threads. Every CTA derives
+//                     lse from the (m, l) partials; chunk 0 also writes o and lse. With
+//                     selection on, each CTA scores 2048 far positions (8 per thread,
+//                     128-bit logit loads), writes them as uint32 keys and adds the
+//                     histogram of their top 12 bits into a per-(query, KV head) global
+//                     histogram (zeroed by the host call).
+// select_kernel       one CTA (512 threads) per (query, KV head): starts from that
+//                     histogram, refines the k-th key with two more digits over keys held
+//                     in shared memory (or in the L2-resident key scratch when the far
+//                     range is too long), and compacts the chosen positions in order.
 #include "common.cuh"
 #include "kernels.h"
 #include "topk.cuh"
 
 namespace hs2 {
 
-// ============================================================================ combine (+ select)
-// One CTA per (query, KV head). Merges the partials of the query's chunks:
-//   M = max m_c, L = sum l_c 2^(m_c - M), o = sum o_c 2^(m_c - M) / L, lse2 = M + log2 L.
-// With a.select: score(s) = sum_h 2^(x_h(s) - lse2_h) for s in F(t) from the base-2 logits,
-// stored as uint32 bit patterns in a.scores, then the block radix top-k.
+constexpr int kScoreChunk = 2048;
+constexpr int kMergeThreads = 256;
+constexpr int kSelectThreads = 512;
+
 template <int D>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
-  constexpr int NT = kCombineThreads;
-  const int qi = blockIdx.x, g = blockIdx.y;
+__global__ void __launch_bounds__(kMergeThreads) merge_score_kernel(const CombineArgs a) {
+  constexpr int NT = kMergeThreads;
+  const int chunk = blockIdx.x, g = blockIdx.y, qi = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = a.G;
   const QueryGeom qg = query_geom(qi, a.prefill, a.seq_len);
   const int t = qg.t;
-  __shared__ float lse2_s[32];
-  __shared__ float M_s[32], Linv_s[32];
-  __shared__ TopkSmem<NT> tk;
-  const bool bad_len = (t < 1) || (t > a.max_t) || ((t + kPage - 1) / kPage > a.max_pages);
-  if (bad_len) {
-    if (tid == 0) flag_error(a.dev_err, HS2_DEV_BAD_LENGTH);
-    for (int e = tid; e < G * D; e += NT) a.o[((size_t)qi * a.Hq + (size_t)g * G) * D + e] = 0.f;
-    if (a.select) {
-      for (int j = tid; j < a.kcap; j += NT) a.idx[((size_t)qi * a.Hkv + g) * a.kcap + j] = -1;
-      if (tid == 0) a.cnt[(size_t)qi * a.Hkv + g] = 0;
+  __shared__ float lse2_s[32], M_s[32], Linv_s[32];
+  __shared__ uint32_t hist[kRadixBins];
+  float* o_out = a.o + ((size_t)qi * a.Hq + (size_t)g * G) * D;
+  int32_t* out = a.select ? a.idx + ((size_t)qi * a.Hkv + g) * a.kcap : nullptr;
+  if ((t < 1) || (t > a.max_t) || ((t + kPage - 1) / kPage > a.max_pages)) {
+    if (chunk == 0) {
+      if (tid == 0) flag_error(a.dev_err, HS2_DEV_BAD_LENGTH);
+      for (int e = tid; e < G * D; e += NT) o_out[e] = 0.f;
+      if (a.select) {
+        for (int j = tid; j < a.kcap; j += NT) out[j] = -1;
+        if (tid == 0) a.cnt[(size_t)qi * a.Hkv + g] = 0;
+      }
     }
     return;
   }
+  const int nF = max(0, t - a.w);
+  const int kk = min(a.k, nF);
+  const bool scoring = a.select && kk > 0 && kk < nF;
+  const int s_lo = chunk * kScoreChunk;
+  if (chunk > 0 && (!scoring || s_lo >= nF)) return;
+
   int nchunk;
   if (a.gather) {
     const int c0 = a.sa_cnt[(size_t)qi * a.Hkv + g];
-    if (tid == 0 && (c0 < 0 || c0 > a.kcap)) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
-    const int nS = max(0, min(a.kcap, c0));
-    nchunk = (min(a.w, t) + nS + 127) / 128;
+    if (tid == 0 && chunk == 0 && (c0 < 0 || c0 > a.kcap)) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+    nchunk = (min(a.w, t) + max(0, min(a.kcap, c0)) + 127) / 128;
   } else {
     nchunk = ((t + kPage - 1) / kPage + a.pps - 1) / a.pps;
   }
-  // per-head merge statistics (warp h handles head h)
+  // ---- per-head merge statistics (warp w handles heads w, w+8, ...)
   for (int h = warp; h < G; h += NT / 32) {
-    const size_t ph = ((size_t)qi * a.Hq + (size_t)g * G + h) * a.nsplit;
+    const float2* ml = a.part_ml + ((size_t)qi * a.Hq + (size_t)g * G + h) * a.nsplit;
     float M = -INFINITY;
-    for (int c = lane; c < nchunk; c += 32) M = fmaxf(M, a.part_ml[ph + c].x);
+    for (int c = lane; c < nchunk; c += 32) M = fmaxf(M, ml[c].x);
     M = warp_max(M);
     float L = 0.f;
-    for (int c = lane; c < nchunk; c += 32) {
-      const float2 ml = a.part_ml[ph + c];
-      L += exp2_rel(ml.x, M) * ml.y;
-    }
+    for (int c = lane; c < nchunk; c += 32) L += exp2_rel(ml[c].x, M) * ml[c].y;
     L = warp_sum(L);
     if (lane == 0) {
       M_s[h] = M;
       Linv_s[h] = L > 0.f ? 1.f / L : 0.f;
       lse2_s[h] = M + log2f(L);
-      if (a.lse) a.lse[(size_t)qi * a.Hq + (size_t)g * G + h] = (M + log2f(L)) / kLog2e;
     }
   }
   __syncthreads();
-  for (int e = tid; e < G * D; e += NT) {
-    const int h = e / D, dd = e % D;
-    const size_t ph = ((size_t)qi * a.Hq + (size_t)g * G + h) * a.nsplit;
-    const float M = M_s[h];
-    float acc = 0.f;
-    for (int c = 0; c < nchunk; ++c) acc += exp2_rel(a.part_ml[ph + c].x, M) * a.part_o[(ph + c) * D + dd];
-    a.o[((size_t)qi * a.Hq + (size_t)g * G + h) * D + dd] = acc * Linv_s[h];
+  if (chunk == 0) {
+    if (a.lse && tid < G) a.lse[(size_t)qi * a.Hq + (size_t)g * G + tid] = lse2_s[tid] / kLog2e;
+    // o = sum_c 2^(m_c - M) o_c / L; thread -> 4 consecutive outputs of one head
+    for (int e4 = tid; e4 < G * D / 4; e4 += NT) {
+      const int h = (4 * e4) / D, d0 = (4 * e4) % D;
+      const size_t ph = ((size_t)qi * a.Hq + (size_t)g * G + h) * a.nsplit;
+      const float M = M_s[h];
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int c = 0; c < nchunk; ++c) {
+        const float wgt = exp2_rel(a.part_ml[ph + c].x, M);
+        const float4 v = *reinterpret_cast<const float4*>(a.part_o + (ph + c) * D + d0);
+        acc.x = fmaf(wgt, v.x, acc.x);
+        acc.y = fmaf(wgt, v.y, acc.y);
+        acc.z = fmaf(wgt, v.z, acc.z);
+        acc.w = fmaf(wgt, v.w, acc.w);
+      }
+      const float li = Linv_s[h];
+      *reinterpret_cast<float4*>(o_out + (size_t)h * D + d0) = make_float4(acc.x * li, acc.y * li, acc.z * li, acc.w * li);
+    }
+    if (a.select) {
+      for (int j = kk + tid; j < a.kcap; j += NT) out[j] = -1;
+      if (tid == 0) a.cnt[(size_t)qi * a.Hkv + g] = kk;
+      if (kk == nF)  // the budget covers the whole far range
+        for (int j = tid; j < nF; j += NT) out[j] = j;
+    }
   }
-  if (!a.select) return;
+  if (!scoring || s_lo >= nF) return;
 
-  // ---- selection over the far range F(t) = [0, t-w)
-  const int nF = max(0, t - a.w);
-  const int kk = min(a.k, nF);
-  int32_t* out = a.idx + ((size_t)qi * a.Hkv + g) * a.kcap;
-  if (tid == 0) a.cnt[(size_t)qi * a.Hkv + g] = kk;
-  for (int j = kk + tid; j < a.kcap; j += NT) out[j] = -1;
-  if (kk == 0) return;
-  if (kk == nF) {  // the budget covers the whole far range
-    for (int j = tid; j < nF; j += NT) out[j] = j;
-    return;
-  }
-  uint32_t* keys = a.scores + ((size_t)qi * a.Hkv + g) * a.ld_logits;
-  const float* lg = a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits;
-  for (int s = tid; s < nF; s += NT) {
-    float sc = 0.f;
-    for (int h = 0; h < G; ++h) sc += exp2f(lg[(size_t)h * a.ld_logits + s] - lse2_s[h]);
-    keys[s] = __float_as_uint(sc);
-  }
+  // ---- score 2048 far positions, 8 per thread
+  for (int i = tid; i < kRadixBins; i += NT) hist[i] = 0;
   __syncthreads();
-  block_topk<NT>(
-      nF, kk, [&](int i) { return keys[i]; }, [&](int j, int i) { out[j] = i; }, tk);
+  const int s0 = s_lo + 8 * tid;
+  float sc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (s0 < nF) {
+    const float* lg = a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits + s0;
+    for (int h = 0; h < G; ++h) {
+      const float4 x0 = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)h * a.ld_logits));
+      const float4 x1 = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)h * a.ld_logits + 4));
+      const float l2 = lse2_s[h];
+      sc[0] += exp2f(x0.x - l2); sc[1] += exp2f(x0.y - l2); sc[2] += exp2f(x0.z - l2); sc[3] += exp2f(x0.w - l2);
+      sc[4] += exp2f(x1.x - l2); sc[5] += exp2f(x1.y - l2); sc[6] += exp2f(x1.z - l2); sc[7] += exp2f(x1.w - l2);
+    }
+  }
+  uint32_t key[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) key[e] = (s0 + e < nF) ? __float_as_uint(sc[e]) : 0u;
+  uint32_t* keys = a.scores + ((size_t)qi * a.Hkv + g) * a.ld_logits;
+  if (s0 < nF) {
+    *reinterpret_cast<uint4*>(keys + s0) = make_uint4(key[0], key[1], key[2], key[3]);
+    *reinterpret_cast<uint4*>(keys + s0 + 4) = make_uint4(key[4], key[5], key[6], key[7]);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) hist_add_warp(hist, s0 + e < nF, key[e] >> 20);
+  __syncthreads();
+  uint32_t* gh = a.hist + ((size_t)qi * a.Hkv + g) * kRadixBins;
+  for (int i = tid; i < kRadixBins; i += NT) {
+    const uint32_t c = hist[i];
+    if (c) atomicAdd(&gh[i], c);
+  }
 }
 
-// ============================================================================ launcher
+__global__ void __launch_bounds__(kSelectThreads) select_kernel(const CombineArgs a) {
+  constexpr int NT = kSelectThreads;
+  const int g = blockIdx.x, qi = blockIdx.y;
+  const int tid = threadIdx.x;
+  const QueryGeom qg = query_geom(qi, a.prefill, a.seq_len);
+  const int t = qg.t;
+  if ((t < 1) || (t > a.max_t) || ((t + kPage - 1) / kPage > a.max_pages)) return;
+  const int nF = max(0, t - a.w);
+  const int kk = min(a.k, nF);
+  if (kk == 0 || kk >= nF) return;  // written by merge_score_kernel
+  __shared__ TopkSmem<NT> sm;
+  extern __shared__ uint32_t keys_smem[];
+  const uint32_t* gkeys = a.scores + ((size_t)qi * a.Hkv + g) * a.ld_logits;
+  const bool in_smem = nF <= a.smem_keys;
+  if (in_smem) {
+    const int n4 = (nF + 3) / 4;  // the scratch row is long enough for the rounded-up tail
+    for (int i = tid; i < n4; i += NT)
+      reinterpret_cast<uint4*>(keys_smem)[i] = __ldcg(reinterpret_cast<const uint4*>(gkeys) + i);
+  }
+  const uint32_t* gh = a.hist + ((size_t)qi * a.Hkv + g) * kRadixBins;
+  for (int i = tid; i < kRadixBins; i += NT) sm.hist[i] = __ldcg(gh + i);
+  __syncthreads();
+  int remaining = kk;
+  uint32_t prefix = find_digit<NT>(sm.hist, kRadixBins, remaining, sm) << 20;
+  uint32_t mask = 0xfff00000u;
+  int32_t* out = a.idx + ((size_t)qi * a.Hkv + g) * a.kcap;
+  auto emit = [&](int j, int i) { out[j] = i; };
+  if (in_smem) {
+    auto key = [&](int i) { return keys_smem[i]; };
+    radix_pass<NT>(nF, key, 8, 12, prefix, mask, remaining, sm);
+    radix_pass<NT>(nF, key, 0, 8, prefix, mask, remaining, sm);
+    compact_selected<NT>(nF, key, prefix, remaining, emit, sm);
+  } else {
+    auto key = [&](int i) { return __ldcg(gkeys + i); };
+    radix_pass<NT>(nF, key, 8, 12, prefix, mask, remaining, sm);
+    radix_pass<NT>(nF, key, 0, 8, prefix, mask, remaining, sm);
+    compact_selected<NT>(nF, key, prefix, remaining, emit, sm);
+  }
+}
+
+// ============================================================================ launchers
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s) {
-  dim3 grid(Bq, a.Hkv);
-  if (a.D == 128) combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(a);
-  else if (a.D == 64) combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(a);
+  const int nscore = a.select ? (int)((a.ld_logits + kScoreChunk - 1) / kScoreChunk) : 1;
+  dim3 grid(nscore, a.Hkv, Bq);
+  if (a.D == 128) merge_score_kernel<128><<<grid, kMergeThreads, 0, s>>>(a);
+  else if (a.D == 64) merge_score_kernel<64><<<grid, kMergeThreads, 0, s>>>(a);
   else return cudaErrorInvalidValue;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !a.select) return e;
+  const size_t sm = (size_t)a.smem_keys * sizeof(uint32_t);
+  e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  select_kernel<<<dim3(a.Hkv, Bq), kSelectThreads, sm, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -6,6 +6,7 @@
 namespace hs2 {
 
 constexpr int kCombineThreads = 512;
+constexpr int kMaxSmemKeys = 48 * 1024;  // 192 KB of uint32 keys
 
 // One attention pass over a set of rows of one group's paged KV, producing per
 // (query, head, chunk) partial softmax state (m, l in base 2; unnormalised o).
@@ -30,6 +31,7 @@ struct AttnArgs {
   float2* part_ml;  // [Bq][Hq][nsplit]
   float* part_o;    // [Bq][Hq][nsplit][D]
   float* logits;    // [Bq][Hq][ld_logits] base-2 logits, or null
+  float* out_o;     // [Bq][Hq][D] final output (kernels that normalise in place)
   long long ld_logits;
   int32_t* dev_err;
 };
@@ -53,13 +55,17 @@ struct CombineArgs {
   int32_t* idx;  // [Bq][Hkv][kcap]
   int32_t* cnt;  // [Bq][Hkv]
   const float* logits;
-  uint32_t* scores;  // [Bq][Hkv][ld_logits] scratch
+  uint32_t* scores;  // [Bq][Hkv][ld_logits] selection keys (scratch)
+  uint32_t* hist;    // [Bq][Hkv][4096] top-digit histograms (scratch, zeroed per call)
   long long ld_logits;
+  int smem_keys;     // capacity of the shared-memory key array (elements)
   int32_t* dev_err;
 };
 
 cudaError_t launch_fa_decode_mma(const AttnArgs& a, int Bq, cudaStream_t s);
 cudaError_t launch_attn_partial(const AttnArgs& a, int Bq, int bf16, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s);
+bool sa_gather_supported(int G, int D, int bf16);
+cudaError_t launch_sa_gather(const AttnArgs& a, int Bq, cudaStream_t s);
 
 }  // namespace hs2

@@ -1,0 +1,295 @@
+// sa_decode.cu — SA gather-attention over window ∪ top-k, staged through shared memory.
+//
+// An SA layer of a HySparse2 Cross group reuses the group's KV and the FA's index set
+// with its own query ("HySparse2：整体架构、KV 生命周期与 PD 分离", §5). Its query
+// attends to the forced window W(t) and the selected far positions S(t) under ONE
+// softmax (§7.2, §7.4: both kinds of positions join the same normalisation), reading
+// entries in place through the block table rather than copying them (§7.2, last
+// paragraph; "Lecture 10 · 混合架构与稀疏注意力", §5.5: a second lookup through the table).
+//
+// One CTA per (query, KV head) walks U = W(t) ++ S(t) in chunks of 64 rows. For each
+// chunk the K and V rows are gathered into shared memory with 16-byte cp.async copies
+// (double-buffered: chunk c+1 streams in while chunk c is computed); the query heads of
+// the KV head share every gathered row, which is what makes the gather worth its cost.
+// Logits: each thread keeps 2 query heads x 32 contraction elements in registers and
+// the 4 partial sums of a row are combined with shuffles. P.V: each thread accumulates
+// 8 output elements of 2 heads over a quarter of the rows. The online softmax merges
+// chunks inside the CTA, so no partials leave the SM. CUDA cores only (fp32 FMA).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace hs2 {
+
+namespace {
+
+constexpr int kSaThreads = 256;
+constexpr int kSaRows = 64;  // rows per chunk
+
+HS2_DEVI void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  const int n = valid ? 16 : 0;  // zero-fill when the row is invalid (no global read)
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
+HS2_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+HS2_DEVI void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// 16-byte chunk c of a staged row r lives at chunk c ^ (4 * (r & 1)): the two rows a warp
+// reads together in the logits phase then hit disjoint bank groups.
+HS2_DEVI int swz(int r, int c) { return c ^ ((r & 1) << 2); }
+
+}  // namespace
+
+template <int D, int G>
+__global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a) {
+  constexpr int HPT = G >= 2 ? 2 : 1;        // heads per thread (logits and P.V)
+  constexpr int NHP = G / HPT;                // head groups
+  constexpr int NDS = D / 32;                 // contraction slices of 32 per row
+  constexpr int LPR = NDS * NHP;              // lanes per row in the logits phase
+  static_assert(32 % LPR == 0, "row task must tile a warp");
+  constexpr int RPW = 32 / LPR;               // rows per warp per logits pass
+  constexpr int RPP = RPW * (kSaThreads / 32);  // rows per logits pass per CTA
+  constexpr int CPR = D / 8;                  // 16-byte chunks per bf16 row
+  constexpr int PV_GROUPS = CPR * NHP;        // (chunk, head group) tasks in P.V
+  static_assert(kSaThreads % PV_GROUPS == 0, "P.V tasks must tile the CTA");
+  constexpr int RQ = kSaThreads / PV_GROUPS;  // row residue classes in P.V
+
+  const int qi = blockIdx.y, g = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const QueryGeom qg = query_geom(qi, a.prefill, a.seq_len);
+  const int t = qg.t;
+  float* out = a.out_o + ((size_t)qi * a.Hq + (size_t)g * G) * D;
+  if (t < 1 || t > a.max_t || (t + kPage - 1) / kPage > a.max_pages) {
+    if (tid == 0) flag_error(a.dev_err, HS2_DEV_BAD_LENGTH);
+    for (int e = tid; e < G * D; e += kSaThreads) out[e] = 0.f;
+    return;
+  }
+  const int nW = min(a.w, t);
+  const int c0 = a.cnt[(size_t)qi * a.Hkv + g];
+  if (tid == 0 && (c0 < 0 || c0 > a.kcap)) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+  const int nS = max(0, min(a.kcap, c0));
+  const int nU = nW + nS;
+  const int32_t* sel = a.idx + ((size_t)qi * a.Hkv + g) * a.kcap;
+  const int32_t* bt = a.bt + (size_t)qg.b * a.max_pages;
+  const int lim = a.w > 0 ? t - a.w : t;  // selected positions must lie in F(t)
+
+  extern __shared__ float smem[];
+  uint4* kst = reinterpret_cast<uint4*>(smem);            // [2][kSaRows][CPR]
+  uint4* vst = kst + 2 * kSaRows * CPR;                   // [2][kSaRows][CPR]
+  float* p_s = reinterpret_cast<float*>(vst + 2 * kSaRows * CPR);  // [kSaRows][G]
+  float* red = p_s + kSaRows * G;                         // [RQ][G][D] (end) / scratch
+  float* m_s = red + RQ * G * D;                          // [G]
+  float* l_s = m_s + G;                                   // [G]
+  float* alpha_s = l_s + G;                               // [G]
+  long long* rowk = reinterpret_cast<long long*>(alpha_s + G + (G & 1));  // [2][kSaRows] element offsets, -1 = invalid
+
+  // ---- q in registers: heads (hp*HPT .. +HPT), contraction slice ds, elements
+  //      {8*(NDS*i + ds) .. +8} for i < 4 (interleaved so lanes of a row hit distinct banks)
+  const int r_in = lane / LPR;            // row within the warp's pass
+  const int hp = (lane % LPR) / NDS;      // head group
+  const int ds = lane % NDS;              // contraction slice
+  float qr[HPT][32];
+  {
+    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)qi * a.Hq + (size_t)g * G) * D;
+#pragma unroll
+    for (int hh = 0; hh < HPT; ++hh)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = *reinterpret_cast<const uint4*>(q + (size_t)(hp * HPT + hh) * D + 8 * (NDS * i + ds));
+        qr[hh][8 * i + 0] = bf16_lo(u.x); qr[hh][8 * i + 1] = bf16_hi(u.x);
+        qr[hh][8 * i + 2] = bf16_lo(u.y); qr[hh][8 * i + 3] = bf16_hi(u.y);
+        qr[hh][8 * i + 4] = bf16_lo(u.z); qr[hh][8 * i + 5] = bf16_hi(u.z);
+        qr[hh][8 * i + 6] = bf16_lo(u.w); qr[hh][8 * i + 7] = bf16_hi(u.w);
+      }
+  }
+  // P.V task of this thread
+  const int pv_c = tid % CPR;             // 16-byte chunk = 8 output elements
+  const int pv_hp = (tid / CPR) % NHP;    // head group
+  const int pv_rq = tid / PV_GROUPS;      // row residue class
+  float acc[HPT][8];
+#pragma unroll
+  for (int hh = 0; hh < HPT; ++hh)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[hh][e] = 0.f;
+  if (tid < G) {
+    m_s[tid] = -INFINITY;
+    l_s[tid] = 0.f;
+  }
+
+  const int nchunk = (nU + kSaRows - 1) / kSaRows;
+  // resolve the rows of chunk c into rowk[buf] (nullptr = invalid) and issue their copies
+  auto stage = [&](int c, int buf) {
+    if (tid < kSaRows) {
+      const int r = c * kSaRows + tid;
+      long long p = -1;
+      if (r < nU) {
+        int pos;
+        bool ok = true;
+        if (r < nW) {
+          pos = t - nW + r;
+        } else {
+          pos = sel[r - nW];
+          if (pos < 0 || pos >= lim) {
+            flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+            ok = false;
+          }
+        }
+        if (ok) {
+          const int phys = bt[pos / kPage];
+          if (phys < 0 || phys >= a.num_pages) {
+            flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+          } else {
+            p = (((long long)phys * a.Hkv + g) * kPage + pos % kPage) * D;
+          }
+        }
+      }
+      rowk[buf * kSaRows + tid] = p;
+    }
+    __syncthreads();
+    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
+    const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(a.v);
+    for (int e = tid; e < kSaRows * CPR; e += kSaThreads) {
+      const int r = e / CPR, cc = e % CPR;
+      const long long p = rowk[buf * kSaRows + r];
+      const bool ok = p >= 0;
+      const long long off = ok ? p + 8 * cc : 0;
+      cp_async16(&kst[(buf * kSaRows + r) * CPR + swz(r, cc)], kb + off, ok);
+      cp_async16(&vst[(buf * kSaRows + r) * CPR + cc], vb + off, ok);
+    }
+    cp_async_commit();
+  };
+
+  if (nchunk > 0) stage(0, 0);
+  for (int c = 0; c < nchunk; ++c) {
+    const int buf = c & 1;
+    if (c + 1 < nchunk) {
+      stage(c + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const int rows = min(kSaRows, nU - c * kSaRows);
+    // ---- logits of this chunk (base 2) into p_s
+    for (int r0 = warp * RPW; r0 < kSaRows; r0 += RPP) {
+      const int r = r0 + r_in;
+      float x[HPT];
+#pragma unroll
+      for (int hh = 0; hh < HPT; ++hh) x[hh] = 0.f;
+      const uint4* krow = &kst[(buf * kSaRows + r) * CPR];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = krow[swz(r, NDS * i + ds)];
+        const float kv[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                             bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+#pragma unroll
+        for (int hh = 0; hh < HPT; ++hh)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[hh] = fmaf(kv[e], qr[hh][8 * i + e], x[hh]);
+      }
+#pragma unroll
+      for (int hh = 0; hh < HPT; ++hh) {
+#pragma unroll
+        for (int o = 1; o < NDS; o <<= 1) x[hh] += __shfl_xor_sync(0xffffffffu, x[hh], o);
+      }
+      if (ds == 0) {
+        const bool ok = r < rows && rowk[buf * kSaRows + r] >= 0;
+#pragma unroll
+        for (int hh = 0; hh < HPT; ++hh) p_s[r * G + hp * HPT + hh] = ok ? x[hh] * a.scale_log2 : -INFINITY;
+      }
+    }
+    __syncthreads();
+    // ---- chunk max per head, running max, weights (warp h handles head h)
+    for (int h = warp; h < G; h += kSaThreads / 32) {
+      float mx = -INFINITY;
+      for (int r = lane; r < kSaRows; r += 32) mx = fmaxf(mx, p_s[r * G + h]);
+      mx = warp_max(mx);
+      const float mo = m_s[h];
+      const float mn = fmaxf(mo, mx);
+      const float al = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+      float ls = 0.f;
+      for (int r = lane; r < kSaRows; r += 32) {
+        const float p = exp2_rel(p_s[r * G + h], mn);
+        p_s[r * G + h] = p;
+        ls += p;
+      }
+      ls = warp_sum(ls);
+      if (lane == 0) {
+        m_s[h] = mn;
+        l_s[h] = l_s[h] * al + ls;
+        alpha_s[h] = al;
+      }
+    }
+    __syncthreads();
+    // ---- P.V over this chunk
+#pragma unroll
+    for (int hh = 0; hh < HPT; ++hh) {
+      const float al = alpha_s[pv_hp * HPT + hh];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[hh][e] *= al;
+    }
+    for (int r = pv_rq; r < rows; r += RQ) {
+      const uint4 u = vst[(buf * kSaRows + r) * CPR + pv_c];
+      const float vv[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                           bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+#pragma unroll
+      for (int hh = 0; hh < HPT; ++hh) {
+        const float p = p_s[r * G + pv_hp * HPT + hh];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[hh][e] = fmaf(p, vv[e], acc[hh][e]);
+      }
+    }
+    __syncthreads();  // buffers of this chunk are refilled two iterations later
+  }
+  // ---- reduce the row residue classes and normalise
+#pragma unroll
+  for (int hh = 0; hh < HPT; ++hh)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red[(pv_rq * G + pv_hp * HPT + hh) * D + 8 * pv_c + e] = acc[hh][e];
+  __syncthreads();
+  for (int e = tid; e < G * D; e += kSaThreads) {
+    float s = 0.f;
+#pragma unroll
+    for (int q2 = 0; q2 < RQ; ++q2) s += red[q2 * G * D + e];
+    const float L = l_s[e / D];
+    out[e] = L > 0.f ? s / L : 0.f;
+  }
+}
+
+template <int D, int G>
+static cudaError_t launch_sa(const AttnArgs& a, int Bq, cudaStream_t s) {
+  constexpr int NHP = G / (G >= 2 ? 2 : 1);
+  constexpr int RQ = kSaThreads / ((D / 8) * NHP);
+  const size_t sm = (size_t)4 * kSaRows * (D / 8) * 16 + (size_t)(kSaRows * G + RQ * G * D + 3 * G + 1) * 4 +
+                    2 * kSaRows * sizeof(long long);
+  auto kern = sa_gather_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(a.Hkv, Bq), kSaThreads, sm, s>>>(a);
+  return cudaGetLastError();
+}
+
+bool sa_gather_supported(int G, int D, int bf16) {
+  return bf16 && (D == 64 || D == 128) && (G == 2 || G == 4 || G == 8 || G == 16);
+}
+
+cudaError_t launch_sa_gather(const AttnArgs& a, int Bq, cudaStream_t s) {
+  if (a.D == 128) {
+    switch (a.G) {
+      case 2: return launch_sa<128, 2>(a, Bq, s);
+      case 4: return launch_sa<128, 4>(a, Bq, s);
+      case 8: return launch_sa<128, 8>(a, Bq, s);
+      case 16: return launch_sa<128, 16>(a, Bq, s);
+    }
+  } else if (a.D == 64) {
+    switch (a.G) {
+      case 2: return launch_sa<64, 2>(a, Bq, s);
+      case 4: return launch_sa<64, 4>(a, Bq, s);
+      case 8: return launch_sa<64, 8>(a, Bq, s);
+      case 16: return launch_sa<64, 16>(a, Bq, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace hs2
