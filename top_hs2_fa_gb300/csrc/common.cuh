@@ -30,6 +30,25 @@ HS2_DEVI uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// d = a * b + c with a and b bfloat16 halves of 32-bit words (fp32 c, d; the product of
+// two bfloat16 values is exact in fp32, so this equals widening both and an fp32 FMA).
+// LL: low half of a times low half of b; HH: high times high; LH/HL likewise.
+#define HS2_FMA_BF16(NAME, SA, SB)                                                          \
+  HS2_DEVI float NAME(uint32_t a, uint32_t b, float c) {                                   \
+    float d;                                                                               \
+    asm("{.reg .b16 a0, a1, b0, b1;\n\t"                                                   \
+        "mov.b32 {a0, a1}, %1;\n\t"                                                        \
+        "mov.b32 {b0, b1}, %2;\n\t"                                                        \
+        "fma.rn.f32.bf16 %0, a" #SA ", b" #SB ", %3;}"                                      \
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));                                               \
+    return d;                                                                              \
+  }
+HS2_FMA_BF16(fmab_ll, 0, 0)
+HS2_FMA_BF16(fmab_hh, 1, 1)
+HS2_FMA_BF16(fmab_lh, 0, 1)
+HS2_FMA_BF16(fmab_hl, 1, 0)
+#undef HS2_FMA_BF16
+
 HS2_DEVI uint4 ldg_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -11,9 +11,11 @@
 // chunk the K and V rows are gathered into shared memory with 16-byte cp.async copies
 // (double-buffered: chunk c+1 streams in while chunk c is computed); the query heads of
 // the KV head share every gathered row, which is what makes the gather worth its cost.
-// Logits: each thread keeps 2 query heads x 32 contraction elements in registers and
-// the 4 partial sums of a row are combined with shuffles. P.V: each thread accumulates
-// 8 output elements of 2 heads over a quarter of the rows. The online softmax merges
+// Logits: each thread keeps 2 query heads x 32 contraction elements in registers (bf16)
+// and the 4 partial sums of a row are combined with shuffles. P.V: each thread
+// accumulates 8 output elements of 2 heads over a quarter of the rows. Products are
+// bf16 x bf16 with fp32 accumulation (mixed-precision FMA, no widening instructions);
+// the softmax weights enter P.V rounded to bf16 and the normaliser sums the same values. The online softmax merges
 // chunks inside the CTA, so no partials leave the SM. CUDA cores only (fp32 FMA).
 #include "common.cuh"
 #include "kernels.h"
@@ -76,9 +78,11 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
   extern __shared__ float smem[];
   uint4* kst = reinterpret_cast<uint4*>(smem);            // [2][kSaRows][CPR]
   uint4* vst = kst + 2 * kSaRows * CPR;                   // [2][kSaRows][CPR]
-  float* p_s = reinterpret_cast<float*>(vst + 2 * kSaRows * CPR);  // [kSaRows][G]
-  float* red = p_s + kSaRows * G;                         // [RQ][G][D] (end) / scratch
-  float* m_s = red + RQ * G * D;                          // [G]
+  float* p_s = reinterpret_cast<float*>(vst + 2 * kSaRows * CPR);  // [kSaRows][G] base-2 logits
+  uint16_t* pb_s = reinterpret_cast<uint16_t*>(p_s + kSaRows * G);  // [kSaRows][G] bf16 weights
+  float* red = reinterpret_cast<float*>(smem);            // [RQ][G][D], reuses the stage buffers at the end
+  static_assert(RQ * G * D * 4 <= 4 * kSaRows * CPR * 16, "reduction buffer must fit the stage buffers");
+  float* m_s = p_s + kSaRows * G + kSaRows * G / 2;       // [G]
   float* l_s = m_s + G;                                   // [G]
   float* alpha_s = l_s + G;                               // [G]
   long long* rowk = reinterpret_cast<long long*>(alpha_s + G + (G & 1));  // [2][kSaRows] element offsets, -1 = invalid
@@ -88,19 +92,14 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
   const int r_in = lane / LPR;            // row within the warp's pass
   const int hp = (lane % LPR) / NDS;      // head group
   const int ds = lane % NDS;              // contraction slice
-  float qr[HPT][32];
+  uint4 qw[HPT][4];  // bf16 pairs: head (hp*HPT+hh), elements 8*(NDS*i+ds) .. +8
   {
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)qi * a.Hq + (size_t)g * G) * D;
 #pragma unroll
     for (int hh = 0; hh < HPT; ++hh)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 u = *reinterpret_cast<const uint4*>(q + (size_t)(hp * HPT + hh) * D + 8 * (NDS * i + ds));
-        qr[hh][8 * i + 0] = bf16_lo(u.x); qr[hh][8 * i + 1] = bf16_hi(u.x);
-        qr[hh][8 * i + 2] = bf16_lo(u.y); qr[hh][8 * i + 3] = bf16_hi(u.y);
-        qr[hh][8 * i + 4] = bf16_lo(u.z); qr[hh][8 * i + 5] = bf16_hi(u.z);
-        qr[hh][8 * i + 6] = bf16_lo(u.w); qr[hh][8 * i + 7] = bf16_hi(u.w);
-      }
+      for (int i = 0; i < 4; ++i)
+        qw[hh][i] = *reinterpret_cast<const uint4*>(q + (size_t)(hp * HPT + hh) * D + 8 * (NDS * i + ds));
   }
   // P.V task of this thread
   const int pv_c = tid % CPR;             // 16-byte chunk = 8 output elements
@@ -180,12 +179,14 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 u = krow[swz(r, NDS * i + ds)];
-        const float kv[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                             bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
 #pragma unroll
-        for (int hh = 0; hh < HPT; ++hh)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[hh] = fmaf(kv[e], qr[hh][8 * i + e], x[hh]);
+        for (int hh = 0; hh < HPT; ++hh) {
+          const uint4 qv = qw[hh][i];
+          x[hh] = fmab_ll(u.x, qv.x, x[hh]); x[hh] = fmab_hh(u.x, qv.x, x[hh]);
+          x[hh] = fmab_ll(u.y, qv.y, x[hh]); x[hh] = fmab_hh(u.y, qv.y, x[hh]);
+          x[hh] = fmab_ll(u.z, qv.z, x[hh]); x[hh] = fmab_hh(u.z, qv.z, x[hh]);
+          x[hh] = fmab_ll(u.w, qv.w, x[hh]); x[hh] = fmab_hh(u.w, qv.w, x[hh]);
+        }
       }
 #pragma unroll
       for (int hh = 0; hh < HPT; ++hh) {
@@ -209,9 +210,10 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
       const float al = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
       float ls = 0.f;
       for (int r = lane; r < kSaRows; r += 32) {
-        const float p = exp2_rel(p_s[r * G + h], mn);
-        p_s[r * G + h] = p;
-        ls += p;
+        // weights enter P.V as bf16; the normaliser sums the same rounded values
+        const __nv_bfloat16 pb = __float2bfloat16_rn(exp2_rel(p_s[r * G + h], mn));
+        pb_s[r * G + h] = __bfloat16_as_ushort(pb);
+        ls += __bfloat162float(pb);
       }
       ls = warp_sum(ls);
       if (lane == 0) {
@@ -230,13 +232,23 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
     }
     for (int r = pv_rq; r < rows; r += RQ) {
       const uint4 u = vst[(buf * kSaRows + r) * CPR + pv_c];
-      const float vv[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                           bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+      uint32_t pw;  // bf16 weights of this thread's heads: low half head 0, high half head 1
+      if constexpr (HPT == 2) pw = *reinterpret_cast<const uint32_t*>(&pb_s[r * G + pv_hp * 2]);
+      else pw = (uint32_t)pb_s[r * G + pv_hp];
 #pragma unroll
       for (int hh = 0; hh < HPT; ++hh) {
-        const float p = p_s[r * G + pv_hp * HPT + hh];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[hh][e] = fmaf(p, vv[e], acc[hh][e]);
+        float* ac = acc[hh];
+        if (hh == 0) {
+          ac[0] = fmab_ll(pw, u.x, ac[0]); ac[1] = fmab_lh(pw, u.x, ac[1]);
+          ac[2] = fmab_ll(pw, u.y, ac[2]); ac[3] = fmab_lh(pw, u.y, ac[3]);
+          ac[4] = fmab_ll(pw, u.z, ac[4]); ac[5] = fmab_lh(pw, u.z, ac[5]);
+          ac[6] = fmab_ll(pw, u.w, ac[6]); ac[7] = fmab_lh(pw, u.w, ac[7]);
+        } else {
+          ac[0] = fmab_hl(pw, u.x, ac[0]); ac[1] = fmab_hh(pw, u.x, ac[1]);
+          ac[2] = fmab_hl(pw, u.y, ac[2]); ac[3] = fmab_hh(pw, u.y, ac[3]);
+          ac[4] = fmab_hl(pw, u.z, ac[4]); ac[5] = fmab_hh(pw, u.z, ac[5]);
+          ac[6] = fmab_hl(pw, u.w, ac[6]); ac[7] = fmab_hh(pw, u.w, ac[7]);
+        }
       }
     }
     __syncthreads();  // buffers of this chunk are refilled two iterations later
@@ -260,8 +272,8 @@ template <int D, int G>
 static cudaError_t launch_sa(const AttnArgs& a, int Bq, cudaStream_t s) {
   constexpr int NHP = G / (G >= 2 ? 2 : 1);
   constexpr int RQ = kSaThreads / ((D / 8) * NHP);
-  const size_t sm = (size_t)4 * kSaRows * (D / 8) * 16 + (size_t)(kSaRows * G + RQ * G * D + 3 * G + 1) * 4 +
-                    2 * kSaRows * sizeof(long long);
+  const size_t sm = (size_t)4 * kSaRows * (D / 8) * 16 +
+                    (size_t)(kSaRows * G + kSaRows * G / 2 + 3 * G + 1) * 4 + 2 * kSaRows * sizeof(long long);
   auto kern = sa_gather_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
