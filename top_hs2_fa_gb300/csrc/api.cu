@@ -1,5 +1,7 @@
 // api.cu — the extern "C" boundary of libhs2: argument validation, workspace layout,
 // launches. No allocation, no synchronisation; every call is asynchronous on `stream`.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -105,6 +107,51 @@ SaPlan sa_plan(int Bq, int Hq, const hs2_kv* kv, int w, int k) {
   off = align256(off + (size_t)Bq * Hq * p.nsplit * kv->d * sizeof(float));
   p.total = off;
   return p;
+}
+
+// ---------------------------------------------------------------------------- CSA2 indexer layout
+struct IdxPlan {
+  long long ld_keys, ld_bkeys;
+  size_t off_keys, off_bkeys, off_hist, total;
+};
+
+IdxPlan idx_plan(hs2_idx_mode mode, int B, int max_t, int max_blocks) {
+  IdxPlan p{};
+  p.ld_keys = mode == HS2_FULL ? ((long long)max_t + 63) / 64 * 64 : (long long)max_blocks * 8;
+  p.ld_bkeys = ((long long)(max_t + 7) / 8 + 63) / 64 * 64;
+  size_t off = 0;
+  p.off_keys = off;
+  off = align256(off + (size_t)B * p.ld_keys * 4);
+  p.off_bkeys = off;
+  off = align256(off + (size_t)B * p.ld_bkeys * 4);
+  p.off_hist = off;
+  off = align256(off + 2 * (size_t)B * 4096 * 4);
+  p.total = off;
+  return p;
+}
+
+// 2-D bf16 tensor map: rows x cols (cols contiguous), box of 64 columns x box_rows rows,
+// 128-byte swizzle. cuTensorMapEncodeTiled is fetched from the driver at run time so the
+// library has no link-time dependency on libcuda.
+bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  }
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 hs2_status common_checks(const void* q, int Bq, int Hq, const hs2_kv* kv, int prefill, bool need_v) {
@@ -314,18 +361,95 @@ hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int
 
 size_t hs2_hier_reindex_workspace(hs2_idx_mode mode, int Hi, const hs2_kv* k_idx, int max_t, int k_top,
                                   int blk, int max_blocks) {
-  (void)mode; (void)Hi; (void)k_idx; (void)max_t; (void)k_top; (void)blk; (void)max_blocks;
-  return 0;
+  (void)Hi;
+  (void)k_top;
+  (void)blk;
+  if (!k_idx || k_idx->batch < 1 || max_t < 1 || max_blocks < 1) return 0;
+  return idx_plan(mode, k_idx->batch, max_t, max_blocks).total;
 }
 
 hs2_status hs2_hier_reindex(hs2_idx_mode mode, const void* q_idx, const float* w_idx, int Hi,
                             const hs2_kv* k_idx, int max_t, int k_top, int blk, int max_blocks,
                             int32_t* pool_blocks, int32_t* pool_cnt, int32_t* idx, int32_t* idx_cnt,
                             void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
-  (void)mode; (void)q_idx; (void)w_idx; (void)Hi; (void)k_idx; (void)max_t; (void)k_top; (void)blk;
-  (void)max_blocks; (void)pool_blocks; (void)pool_cnt; (void)idx; (void)idx_cnt; (void)workspace;
-  (void)ws_bytes; (void)dev_err; (void)stream;
-  return HS2_ERR_UNSUPPORTED;
+  if (mode != HS2_FULL && mode != HS2_REINDEX) return HS2_ERR_ARG;
+  if (!valid_kv(k_idx, false) || !q_idx || !aligned16(q_idx) || !w_idx) return HS2_ERR_ARG;
+  if (max_t < 1 || (long long)max_t > (long long)k_idx->max_pages * 64 || k_top < 0 || max_blocks < 1) return HS2_ERR_ARG;
+  if (!pool_blocks || !pool_cnt || !idx_cnt || (k_top > 0 && !idx)) return HS2_ERR_ARG;
+  if (Hi != 64 || k_idx->d != 128 || k_idx->Hkv != 1 || k_idx->dtype != HS2_BF16 || blk != 8) return HS2_ERR_UNSUPPORTED;
+  const IdxPlan p = idx_plan(mode, k_idx->batch, max_t, max_blocks);
+  if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+  const int B = k_idx->batch;
+
+  CUtensorMap tm_k, tm_q;
+  const int box_rows = mode == HS2_FULL ? 64 : 8;
+  if (!encode_2d_bf16(&tm_k, k_idx->k, 128, (uint64_t)k_idx->num_pages * 64, box_rows) ||
+      !encode_2d_bf16(&tm_q, q_idx, 128, (uint64_t)B * 64, 64))
+    return HS2_ERR_ARG;
+  cudaError_t e = cudaMemsetAsync(ws + p.off_hist, 0, 2 * (size_t)B * 4096 * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  hs2::IdxArgs a{};
+  a.mode = mode == HS2_FULL ? 0 : 1;
+  a.w_idx = w_idx;
+  a.bt = k_idx->block_table;
+  a.seq_len = k_idx->seq_len;
+  a.max_pages = k_idx->max_pages;
+  a.num_pages = k_idx->num_pages;
+  a.max_t = max_t;
+  a.pool = pool_blocks;
+  a.pool_cnt = pool_cnt;
+  a.max_blocks = max_blocks;
+  a.keys = (uint32_t*)(ws + p.off_keys);
+  a.ld_keys = p.ld_keys;
+  a.bkeys = (uint32_t*)(ws + p.off_bkeys);
+  a.ld_bkeys = p.ld_bkeys;
+  a.hist = (uint32_t*)(ws + p.off_hist);
+  a.bhist = a.hist + (size_t)B * 4096;
+  a.dev_err = dev_err;
+  const long long ntile_max = (p.ld_keys + 127) / 128;
+  // one wave of 152 SMs (one CTA per SM) over every batch row
+  const long long per_cta = std::max<long long>(1, (ntile_max * B + 151) / 152);
+  a.tiles_per_cta = (int)per_cta;
+  const int grid_x = (int)((ntile_max + per_cta - 1) / per_cta);
+  e = profiled(HS2_STAGE_INDEXER, s, [&] { return hs2::launch_lightning_scan(tm_k, tm_q, a, B, grid_x, s); });
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  hs2::SelectArgs sa{};
+  sa.seq_len = k_idx->seq_len;
+  sa.max_t = max_t;
+  sa.max_pages = k_idx->max_pages;
+  sa.pool = pool_blocks;
+  sa.pool_cnt = pool_cnt;
+  sa.max_blocks = max_blocks;
+  sa.dev_err = dev_err;
+  sa.mode = mode == HS2_FULL ? 1 : 3;
+  sa.k = k_top;
+  sa.kcap = k_top;
+  sa.keys = a.keys;
+  sa.ld_keys = p.ld_keys;
+  sa.hist = a.hist;
+  sa.out = idx;
+  sa.cnt = idx_cnt;
+  sa.smem_keys = (int)std::min<long long>(p.ld_keys, hs2::kMaxSmemKeys);
+  e = hs2::launch_select_rows(sa, B, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (mode == HS2_FULL) {
+    sa.mode = 2;
+    sa.k = max_blocks;
+    sa.kcap = max_blocks;
+    sa.keys = a.bkeys;
+    sa.ld_keys = p.ld_bkeys;
+    sa.hist = a.bhist;
+    sa.out = pool_blocks;
+    sa.cnt = pool_cnt;
+    sa.smem_keys = (int)std::min<long long>(p.ld_bkeys, hs2::kMaxSmemKeys);
+    e = hs2::launch_select_rows(sa, B, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return HS2_OK;
 }
 
 }  // extern "C"

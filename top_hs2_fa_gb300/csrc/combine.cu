@@ -182,6 +182,73 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const CombineArg
   }
 }
 
+// ============================================================================ generic row top-k
+__global__ void __launch_bounds__(kSelectThreads) select_rows_kernel(const SelectArgs a) {
+  constexpr int NT = kSelectThreads;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int t = a.seq_len[b];
+  int32_t* out = a.out + (size_t)b * a.kcap;
+  const bool bad = t < 1 || t > a.max_t || (t + kPage - 1) / kPage > a.max_pages;
+  int n = 0;
+  const int32_t* pool = nullptr;
+  if (!bad) {
+    if (a.mode == 1) {
+      n = t;
+    } else if (a.mode == 2) {
+      n = (t + 7) / 8;
+    } else {
+      pool = a.pool + (size_t)b * a.max_blocks;
+      const int pc = max(0, min(a.max_blocks, a.pool_cnt[b]));
+      if (pc > 0) n = (pc - 1) * 8 + max(0, min(8, t - 8 * pool[pc - 1]));
+    }
+  }
+  const int kk = min(a.k, n);
+  if (tid == 0) a.cnt[b] = kk;
+  for (int j = kk + tid; j < a.kcap; j += NT) out[j] = -1;
+  auto map = [&](int i) { return a.mode == 3 ? pool[i >> 3] * 8 + (i & 7) : i; };
+  if (kk == 0) return;
+  if (kk == n) {
+    for (int i = tid; i < n; i += NT) out[i] = map(i);
+    return;
+  }
+  __shared__ TopkSmem<NT> sm;
+  extern __shared__ uint32_t keys_smem[];
+  const uint32_t* gkeys = a.keys + (size_t)b * a.ld_keys;
+  const bool in_smem = n <= a.smem_keys;
+  if (in_smem) {
+    const int n4 = (n + 3) / 4;
+    for (int i = tid; i < n4; i += NT)
+      reinterpret_cast<uint4*>(keys_smem)[i] = __ldcg(reinterpret_cast<const uint4*>(gkeys) + i);
+  }
+  const uint32_t* gh = a.hist + (size_t)b * kRadixBins;
+  for (int i = tid; i < kRadixBins; i += NT) sm.hist[i] = __ldcg(gh + i);
+  __syncthreads();
+  int remaining = kk;
+  uint32_t prefix = find_digit<NT>(sm.hist, kRadixBins, remaining, sm) << 20;
+  uint32_t mask = 0xfff00000u;
+  auto emit = [&](int j, int i) { out[j] = map(i); };
+  if (in_smem) {
+    auto key = [&](int i) { return keys_smem[i]; };
+    radix_pass<NT>(n, key, 8, 12, prefix, mask, remaining, sm);
+    radix_pass<NT>(n, key, 0, 8, prefix, mask, remaining, sm);
+    compact_selected<NT>(n, key, prefix, remaining, emit, sm);
+  } else {
+    auto key = [&](int i) { return __ldcg(gkeys + i); };
+    radix_pass<NT>(n, key, 8, 12, prefix, mask, remaining, sm);
+    radix_pass<NT>(n, key, 0, 8, prefix, mask, remaining, sm);
+    compact_selected<NT>(n, key, prefix, remaining, emit, sm);
+  }
+}
+
+cudaError_t launch_select_rows(const SelectArgs& a, int B, cudaStream_t s) {
+  const size_t sm = (size_t)a.smem_keys * sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(select_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  select_rows_kernel<<<B, kSelectThreads, sm, s>>>(a);
+  return cudaGetLastError();
+}
+
 // ============================================================================ launchers
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s) {
   const int nscore = a.select ? (int)((a.ld_logits + kScoreChunk - 1) / kScoreChunk) : 1;

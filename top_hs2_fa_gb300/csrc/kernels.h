@@ -1,5 +1,6 @@
 // kernels.h — launch parameters shared between the C ABI layer and the kernels.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -62,10 +63,52 @@ struct CombineArgs {
   int32_t* dev_err;
 };
 
+// CSA2 lightning-indexer scan (mode 0: every position s < t; mode 1: the pool's positions).
+struct IdxArgs {
+  int mode;
+  const float* w_idx;  // [B][64]
+  const int32_t* bt;
+  const int32_t* seq_len;
+  int max_pages, num_pages, max_t;
+  int tiles_per_cta;
+  const int32_t* pool;      // [B][max_blocks] (mode 1)
+  const int32_t* pool_cnt;  // [B] (mode 1)
+  int max_blocks;
+  uint32_t* keys;  // [B][ld_keys] candidate keys
+  long long ld_keys;
+  uint32_t* bkeys;  // [B][ld_bkeys] 8-block maxima (mode 0)
+  long long ld_bkeys;
+  uint32_t* hist;   // [B][4096]
+  uint32_t* bhist;  // [B][4096] (mode 0)
+  int32_t* dev_err;
+};
+
+// Row-wise exact top-k over precomputed keys, starting from a global top-digit histogram.
+struct SelectArgs {
+  int mode;  // 1: positions [0, t); 2: 8-blocks [0, ceil(t/8)); 3: pool candidates (mapped)
+  const int32_t* seq_len;
+  int max_t, max_pages;
+  const int32_t* pool;
+  const int32_t* pool_cnt;
+  int max_blocks;
+  int k, kcap;
+  const uint32_t* keys;
+  long long ld_keys;
+  const uint32_t* hist;
+  int32_t* out;  // [B][kcap]
+  int32_t* cnt;  // [B]
+  int smem_keys;
+  int32_t* dev_err;
+};
+
 cudaError_t launch_fa_decode_mma(const AttnArgs& a, int Bq, cudaStream_t s);
 cudaError_t launch_attn_partial(const AttnArgs& a, int Bq, int bf16, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s);
 bool sa_gather_supported(int G, int D, int bf16);
+size_t lightning_scan_smem();
+cudaError_t launch_lightning_scan(const CUtensorMap& tm_k, const CUtensorMap& tm_q, const IdxArgs& a, int B,
+                                  int grid_x, cudaStream_t s);
+cudaError_t launch_select_rows(const SelectArgs& a, int B, cudaStream_t s);
 cudaError_t launch_sa_gather(const AttnArgs& a, int Bq, cudaStream_t s);
 
 }  // namespace hs2

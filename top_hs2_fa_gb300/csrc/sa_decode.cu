@@ -270,8 +270,6 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
 
 template <int D, int G>
 static cudaError_t launch_sa(const AttnArgs& a, int Bq, cudaStream_t s) {
-  constexpr int NHP = G / (G >= 2 ? 2 : 1);
-  constexpr int RQ = kSaThreads / ((D / 8) * NHP);
   const size_t sm = (size_t)4 * kSaRows * (D / 8) * 16 +
                     (size_t)(kSaRows * G + kSaRows * G / 2 + 3 * G + 1) * 4 + 2 * kSaRows * sizeof(long long);
   auto kern = sa_gather_kernel<D, G>;
