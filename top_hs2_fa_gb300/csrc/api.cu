@@ -154,6 +154,46 @@ bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t 
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1,
+                    uint32_t b2) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  }
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint32_t box[3] = {64, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------- bf16 prefill layout
+bool use_prefill_tc(const hs2_kv* kv, int prefill) { return prefill && kv->dtype == HS2_BF16 && kv->d == 128; }
+
+struct PrefillPlan {
+  size_t off_lse2, total;
+};
+
+PrefillPlan prefill_plan(int n, int Hq, const hs2_kv* kv, int k) {
+  (void)kv;
+  (void)k;
+  PrefillPlan p{};
+  size_t off = 0;
+  p.off_lse2 = off;
+  off = align256(off + (size_t)n * Hq * sizeof(float));
+  p.total = off;
+  return p;
+}
+
 hs2_status common_checks(const void* q, int Bq, int Hq, const hs2_kv* kv, int prefill, bool need_v) {
   if (!valid_kv(kv, need_v)) return HS2_ERR_ARG;
   if (!q || !aligned16(q) || Bq < 0 || Hq < 1) return HS2_ERR_ARG;
@@ -195,10 +235,43 @@ const char* hs2_strerror(hs2_status st) {
 }
 
 size_t hs2_fa_select_workspace(int B_or_n, int Hq, const hs2_kv* kv, int max_t, int k, int prefill) {
-  (void)k;
-  (void)prefill;
   if (!kv || kv->Hkv < 1 || Hq < 1 || max_t < 1 || B_or_n < 0 || (kv->d != 64 && kv->d != 128)) return 0;
+  if (use_prefill_tc(kv, prefill)) return prefill_plan(B_or_n, Hq, kv, k).total;
   return fa_plan(B_or_n, Hq, kv, max_t).total;
+}
+
+static hs2_status fa_select_prefill_tc(const void* q, int n, int Hq, const hs2_kv* kv, int w, int k, float scale,
+                                       float* o, float* lse, int32_t* idx, int32_t* idx_cnt, void* workspace,
+                                       size_t ws_bytes, int32_t* dev_err, cudaStream_t s) {
+  const PrefillPlan p = prefill_plan(n, Hq, kv, k);
+  if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
+  if (k > 0 && n - w > k) return HS2_ERR_UNSUPPORTED;  // ranking rows of a causal prefill: next kernel
+  char* ws = (char*)workspace;
+  CUtensorMap tq, tk, tv;
+  const uint64_t rows = (uint64_t)kv->num_pages * kv->Hkv * 64;
+  if (!encode_3d_bf16(&tq, q, 128, (uint64_t)Hq, (uint64_t)n, 1, 128) || !encode_2d_bf16(&tk, kv->k, 128, rows, 64) ||
+      !encode_2d_bf16(&tv, kv->v, 128, rows, 64))
+    return HS2_ERR_ARG;
+  hs2::PfArgs a{};
+  a.n = n;
+  a.Hq = Hq;
+  a.Hkv = kv->Hkv;
+  a.G = Hq / kv->Hkv;
+  a.bt = kv->block_table;
+  a.max_pages = kv->max_pages;
+  a.num_pages = kv->num_pages;
+  a.seq_len = kv->seq_len;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.o = o;
+  a.lse = lse;
+  a.lse2 = (float*)(ws + p.off_lse2);
+  a.dev_err = dev_err;
+  cudaError_t e = profiled(HS2_STAGE_FA_SCAN, s, [&] { return hs2::launch_fa_prefill_fwd(tq, tk, tv, a, s); });
+  if (e != cudaSuccess) return cuda_fail(e);
+  // rows whose far range is empty or fits the budget take all of it: no ranking needed
+  e = hs2::launch_prefill_trivial_select(idx, idx_cnt, n, kv->Hkv, w, k, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return HS2_OK;
 }
 
 hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w, int k,
@@ -211,6 +284,9 @@ hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, in
   if (prefill && B_or_n > max_t) return HS2_ERR_ARG;
   if (!o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
   if (B_or_n == 0) return HS2_OK;
+  if (use_prefill_tc(kv, prefill))
+    return fa_select_prefill_tc(q, B_or_n, Hq, kv, w, k, scale, o, lse, idx, idx_cnt, workspace, ws_bytes, dev_err,
+                                (cudaStream_t)stream);
   const FaPlan p = fa_plan(B_or_n, Hq, kv, max_t);
   if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;

@@ -249,6 +249,23 @@ cudaError_t launch_select_rows(const SelectArgs& a, int B, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Prefill rows i whose far range F(i+1) = [0, i+1-w) fits the budget take all of it.
+__global__ void prefill_trivial_select_kernel(int32_t* idx, int32_t* cnt, int n, int Hkv, int w, int k) {
+  const int row = blockIdx.x;  // row * Hkv + g
+  const int i = row / Hkv;
+  if (i >= n) return;
+  const int nF = max(0, i + 1 - w);
+  const int kk = min(k, nF);
+  if (threadIdx.x == 0) cnt[row] = kk;
+  int32_t* out = idx + (size_t)row * k;
+  for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < kk ? j : -1;
+}
+
+cudaError_t launch_prefill_trivial_select(int32_t* idx, int32_t* cnt, int n, int Hkv, int w, int k, cudaStream_t s) {
+  prefill_trivial_select_kernel<<<n * Hkv, 128, 0, s>>>(idx, cnt, n, Hkv, w, k);
+  return cudaGetLastError();
+}
+
 // ============================================================================ launchers
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s) {
   const int nscore = a.select ? (int)((a.ld_logits + kScoreChunk - 1) / kScoreChunk) : 1;

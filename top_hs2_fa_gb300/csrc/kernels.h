@@ -83,6 +83,19 @@ struct IdxArgs {
   int32_t* dev_err;
 };
 
+// Causal FA forward of one sequence's n query rows (bf16, head_dim 128, tcgen05).
+struct PfArgs {
+  int n, Hq, Hkv, G;
+  const int32_t* bt;  // block table row of the sequence
+  int max_pages, num_pages;
+  const int32_t* seq_len;  // [1]
+  float scale_log2;
+  float* o;     // [n][Hq][128]
+  float* lse;   // [n][Hq] natural log, or null
+  float* lse2;  // [n][Hq] base-2 (scratch for the selection)
+  int32_t* dev_err;
+};
+
 // Row-wise exact top-k over precomputed keys, starting from a global top-digit histogram.
 struct SelectArgs {
   int mode;  // 1: positions [0, t); 2: 8-blocks [0, ceil(t/8)); 3: pool candidates (mapped)
@@ -109,6 +122,10 @@ size_t lightning_scan_smem();
 cudaError_t launch_lightning_scan(const CUtensorMap& tm_k, const CUtensorMap& tm_q, const IdxArgs& a, int B,
                                   int grid_x, cudaStream_t s);
 cudaError_t launch_select_rows(const SelectArgs& a, int B, cudaStream_t s);
+cudaError_t launch_prefill_trivial_select(int32_t* idx, int32_t* cnt, int n, int Hkv, int w, int k, cudaStream_t s);
+size_t fa_prefill_fwd_smem();
+cudaError_t launch_fa_prefill_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PfArgs& a,
+                                  cudaStream_t s);
 cudaError_t launch_sa_gather(const AttnArgs& a, int Bq, cudaStream_t s);
 
 }  // namespace hs2
