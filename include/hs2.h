@@ -64,6 +64,8 @@ typedef enum {
 #define HS2_DEV_BAD_INDEX 2   /* selected position outside F(t) (or outside [0,t) with w=0) */
 #define HS2_DEV_TIMEOUT 4     /* a bounded wait (mbarrier / TMA / MMA) gave up */
 #define HS2_DEV_BAD_LENGTH 8  /* seq_len < 1 or beyond max_pages * page_size */
+#define HS2_DEV_SELECT 16     /* a prefill row's streamed candidates could not prove its top-k
+                                 (its idx_cnt is written as -1); see hs2_fa_select */
 
 typedef enum { HS2_F32 = 0, HS2_BF16 = 1 } hs2_dtype;
 

@@ -71,3 +71,53 @@ def test_prefill_trivial_selection_rows(H):
         nf = max(0, i + 1 - 16)
         assert (cnt[i] == nf).all()
         assert (idx[i, :, :nf] == np.arange(nf)).all() and (idx[i, :, nf:] == -1).all()
+
+
+def check_selection(H, grp, rows=None):
+    o, lse, idx, cnt = run_fa(H, grp)
+    n = grp.q_fa.shape[0]
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    o_r, lse_r, idx_r, cnt_r, sc = O.fa_prefill_rows(grp.q_fa, grp.kv, rows, grp.w, grp.k, grp.scale,
+                                                     return_scores=True)
+    assert max_abs(o[rows], o_r) <= tol("bf16")
+    differ = check_index_sets(idx[rows], cnt[rows], idx_r, cnt_r, sc, "prefill ")
+    return idx, cnt, differ
+
+
+def test_prefill_selection_small_all_rows(H):
+    grp = W.prefill_group(1000, 8, 2, 128, w=16, k=64, dtype="bf16", seed=31, n_sa=0, rho=0.99, permute=True)
+    check_selection(H, grp)
+
+
+def test_prefill_selection_gqa8_sampled(H):
+    grp = W.prefill_group(2048, 32, 4, 128, w=128, k=256, dtype="bf16", seed=32, n_sa=0, rho=0.999)
+    rows = np.unique(np.concatenate([np.random.default_rng(1).choice(2048, 150, replace=False),
+                                     [0, 127, 128, 383, 384, 385, 1023, 2047]]))
+    check_selection(H, grp, rows)
+
+
+def test_prefill_selection_ties_take_lowest_positions(H):
+    # identical keys: every far score is equal, so each row takes its first k positions
+    grp = W.prefill_group(1500, 8, 1, 128, w=16, k=100, dtype="bf16", seed=33, n_sa=0)
+    kv = grp.kv
+    kv.k[:] = kv.k[0:1, :, 0:1, :]
+    o, lse, idx, cnt = run_fa(H, grp)
+    for i in (200, 700, 1499):
+        assert cnt[i, 0] == 100 and (idx[i, 0] == np.arange(100)).all()
+
+
+def test_prefill_selection_needles(H):
+    grp = W.prefill_group(3000, 8, 1, 128, w=32, k=128, dtype="bf16", seed=34, n_sa=0, needles=16)
+    idx, cnt, _ = check_selection(H, grp, rows=[2999, 2500, 1200, 160, 161])
+
+
+@pytest.mark.slow
+def test_prefill_full_size_sampled_rows(H):
+    """Prefill workload at full size (n=32768, Hq=32, Hkv=4, d=128, w=128, k=1024, AR(1) keys):
+    256 seeded random rows plus {0, w-1, w, w+k-1, w+k, n-1}, each exact against all its keys."""
+    n, w, k = 32768, 128, 1024
+    grp = W.prefill_group(n, 32, 4, 128, w=w, k=k, dtype="bf16", seed=0, n_sa=0, rho=0.999)
+    rows = np.unique(np.concatenate([np.random.default_rng(7).choice(n, 256, replace=False),
+                                     [0, w - 1, w, w + k - 1, w + k, n - 1]]))
+    idx, cnt, _ = check_selection(H, grp, rows)
+    assert (cnt >= 0).all()

@@ -179,17 +179,33 @@ bool encode_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1
 // ---------------------------------------------------------------------------- bf16 prefill layout
 bool use_prefill_tc(const hs2_kv* kv, int prefill) { return prefill && kv->dtype == HS2_BF16 && kv->d == 128; }
 
+// Rows are ranked in chunks of kPrefillChunk rows; each chunk's candidate buffers hold cap
+// entries per (row, KV head), cap = max(256, 4k).
+constexpr int kPrefillChunk = 8192;
+
 struct PrefillPlan {
-  size_t off_lse2, total;
+  int chunk, cap;
+  size_t off_lse2, off_ckey, off_cpos, off_ccnt, off_cdrop, off_ctau, total;
 };
 
 PrefillPlan prefill_plan(int n, int Hq, const hs2_kv* kv, int k) {
-  (void)kv;
-  (void)k;
   PrefillPlan p{};
+  p.chunk = std::max(1, std::min(n, kPrefillChunk));
+  p.cap = std::max(256, 4 * k);
+  const size_t rows = (size_t)p.chunk * kv->Hkv;
   size_t off = 0;
   p.off_lse2 = off;
   off = align256(off + (size_t)n * Hq * sizeof(float));
+  p.off_ckey = off;
+  off = align256(off + rows * p.cap * 4);
+  p.off_cpos = off;
+  off = align256(off + rows * p.cap * 4);
+  p.off_ccnt = off;
+  off = align256(off + rows * 4);
+  p.off_cdrop = off;
+  off = align256(off + rows * 4);
+  p.off_ctau = off;
+  off = align256(off + rows * 4);
   p.total = off;
   return p;
 }
@@ -245,7 +261,8 @@ static hs2_status fa_select_prefill_tc(const void* q, int n, int Hq, const hs2_k
                                        size_t ws_bytes, int32_t* dev_err, cudaStream_t s) {
   const PrefillPlan p = prefill_plan(n, Hq, kv, k);
   if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
-  if (k > 0 && n - w > k) return HS2_ERR_UNSUPPORTED;  // ranking rows of a causal prefill: next kernel
+  const bool ranked = k > 0 && n - w > k;  // some row's far range exceeds the budget
+  if (ranked && Hq / kv->Hkv > 8) return HS2_ERR_UNSUPPORTED;
   char* ws = (char*)workspace;
   CUtensorMap tq, tk, tv;
   const uint64_t rows = (uint64_t)kv->num_pages * kv->Hkv * 64;
@@ -268,9 +285,40 @@ static hs2_status fa_select_prefill_tc(const void* q, int n, int Hq, const hs2_k
   a.dev_err = dev_err;
   cudaError_t e = profiled(HS2_STAGE_FA_SCAN, s, [&] { return hs2::launch_fa_prefill_fwd(tq, tk, tv, a, s); });
   if (e != cudaSuccess) return cuda_fail(e);
-  // rows whose far range is empty or fits the budget take all of it: no ranking needed
-  e = hs2::launch_prefill_trivial_select(idx, idx_cnt, n, kv->Hkv, w, k, s);
-  if (e != cudaSuccess) return cuda_fail(e);
+  if (!ranked) {
+    // every row's far range is empty or fits the budget: each row takes all of it
+    e = hs2::launch_prefill_trivial_select(idx, idx_cnt, n, kv->Hkv, w, k, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return HS2_OK;
+  }
+  hs2::PsArgs b{};
+  b.n = n;
+  b.Hq = Hq;
+  b.Hkv = kv->Hkv;
+  b.G = Hq / kv->Hkv;
+  b.w = w;
+  b.k = k;
+  b.cap = p.cap;
+  b.bt = kv->block_table;
+  b.max_pages = kv->max_pages;
+  b.num_pages = kv->num_pages;
+  b.seq_len = kv->seq_len;
+  b.scale_log2 = a.scale_log2;
+  b.lse2 = a.lse2;
+  b.cand_key = (uint32_t*)(ws + p.off_ckey);
+  b.cand_pos = (int32_t*)(ws + p.off_cpos);
+  b.cand_cnt = (int32_t*)(ws + p.off_ccnt);
+  b.cand_drop = (uint32_t*)(ws + p.off_cdrop);
+  b.cand_tau = (uint32_t*)(ws + p.off_ctau);
+  b.idx = idx;
+  b.cnt = idx_cnt;
+  b.dev_err = dev_err;
+  for (int r0 = 0; r0 < n; r0 += p.chunk) {
+    b.row0 = r0;
+    b.row1 = std::min(n, r0 + p.chunk);
+    e = hs2::launch_prefill_select(tq, tk, b, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   return HS2_OK;
 }
 

@@ -96,6 +96,24 @@ struct PfArgs {
   int32_t* dev_err;
 };
 
+// Window-excluding top-k of the causal rows [row0, row1) of a bf16 prefill.
+struct PsArgs {
+  int n, row0, row1, Hq, Hkv, G, w, k, cap;
+  const int32_t* bt;
+  int max_pages, num_pages;
+  const int32_t* seq_len;
+  float scale_log2;
+  const float* lse2;    // [n][Hq] base-2 lse from the forward kernel
+  uint32_t* cand_key;   // [(row1-row0)][Hkv][cap]
+  int32_t* cand_pos;    // [(row1-row0)][Hkv][cap]
+  int32_t* cand_cnt;    // [(row1-row0)][Hkv]
+  uint32_t* cand_drop;  // [(row1-row0)][Hkv] largest key dropped past capacity
+  uint32_t* cand_tau;   // [(row1-row0)][Hkv] threshold (diagnostic)
+  int32_t* idx;         // [n][Hkv][k]
+  int32_t* cnt;         // [n][Hkv]
+  int32_t* dev_err;
+};
+
 // Row-wise exact top-k over precomputed keys, starting from a global top-digit histogram.
 struct SelectArgs {
   int mode;  // 1: positions [0, t); 2: 8-blocks [0, ceil(t/8)); 3: pool candidates (mapped)
@@ -124,6 +142,8 @@ cudaError_t launch_lightning_scan(const CUtensorMap& tm_k, const CUtensorMap& tm
 cudaError_t launch_select_rows(const SelectArgs& a, int B, cudaStream_t s);
 cudaError_t launch_prefill_trivial_select(int32_t* idx, int32_t* cnt, int n, int Hkv, int w, int k, cudaStream_t s);
 size_t fa_prefill_fwd_smem();
+size_t prefill_scan_smem();
+cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, const PsArgs& a, cudaStream_t s);
 cudaError_t launch_fa_prefill_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PfArgs& a,
                                   cudaStream_t s);
 cudaError_t launch_sa_gather(const AttnArgs& a, int Bq, cudaStream_t s);

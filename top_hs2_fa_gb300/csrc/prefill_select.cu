@@ -1,0 +1,340 @@
+// prefill_select.cu — window-excluding top-k for every causal row of a bf16 prefill.
+//
+// Row i's selection score of a far position s (s < i+1-w) is the FA attention
+// probability summed over the query heads of a KV head ("HySparse2：整体架构、KV 生命周期
+// 与 PD 分离", §5, §7.2), normalised with the row's final lse (written by the forward
+// kernel). The n x n score matrix is never stored: scores are produced tile by tile from
+// a tcgen05 recomputation of Q K^T and consumed on the fly.
+//
+// prefill_scan_kernel — one CTA per (128-row tile, KV head), one row per scoring thread:
+//   sweep 0 (sampled): every 2nd key tile, every 2nd column; each thread bins the sampled
+//            scores of its row into a 256-bin log histogram (1/8 octave per bin) held in
+//            shared memory, then picks a threshold tau whose estimated count of keys at or
+//            above it is twice the budget;
+//   sweep 1 (exact): every key tile; each thread appends (key, position) of the scores >= tau
+//            of its row, in ascending position, into its row's candidate buffer (capacity C);
+//            past capacity it keeps only the largest dropped key.
+//   Warp 0 streams K tiles and, per head, the head's Q tile (TMA); warp 1 issues
+//   S_h = Q_h K^T (M=128 rows, N=128 keys, K=128) into double-buffered TMEM.
+// prefill_topk_kernel — per (row, KV head): exact top-k over the row's candidates (radix
+//   select, ties to the lower position, ascending output). The candidates are a superset of
+//   the answer when (a) at least k of them are >= tau and (b) no dropped key exceeds the k-th
+//   largest kept key (dropped positions come after every kept one, so equal keys lose);
+//   otherwise the row is flagged (HS2_DEV_SELECT) and written as count -1.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+#include "topk.cuh"
+
+namespace hs2 {
+
+namespace {
+
+constexpr int kST = 128;        // rows per tile = keys per key tile
+constexpr int kSThreads = 192;  // TMA warp, MMA warp, 4 scoring warps
+constexpr uint32_t kSTile = kST * 128 * 2;
+constexpr int kBins = 256;
+constexpr uint32_t kBinBase = 0x410 - (kBins - 1);  // bin 255 holds keys >> 20 == 0x410 (score 8.0)
+constexpr int kMaxSelG = 8;  // query heads per KV head handled by the scan
+
+struct PsSmem {
+  uint8_t q[2][kSTile];            // A of S (query rows x d), one head per stage
+  uint8_t k[2][kSTile];            // B of S (keys x d)
+  uint16_t hist[kBins][kST];       // per-row sample histograms ([bin][row])
+  uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], s_full[2], s_empty[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+HS2_DEVI bool aborted(PsSmem& sm) { return *(volatile int*)&sm.abort != 0; }
+HS2_DEVI void set_abort(PsSmem& sm, int32_t* dev_err) {
+  flag_error(dev_err, HS2_DEV_TIMEOUT);
+  atomicExch(&sm.abort, 1);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kSThreads, 1)
+    prefill_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const PsArgs a) {
+  extern __shared__ __align__(1024) uint8_t dsmem[];
+  PsSmem& sm = *reinterpret_cast<PsSmem*>(dsmem + ((1024 - (tc::smem_u32(dsmem) & 1023)) & 1023));
+  const int tiles = (a.row1 - a.row0 + kST - 1) / kST;
+  const int tile = tiles - 1 - blockIdx.x;  // heaviest first
+  const int g = blockIdx.y, G = a.G;
+  const int i0 = a.row0 + tile * kST;
+  const int i_last = min(a.row1, i0 + kST) - 1;
+  const int keys_needed = max(0, i_last + 1 - a.w);
+  const int J = (keys_needed + kST - 1) / kST;  // key tiles of the exact sweep
+  const int J0 = (J + 1) / 2;                   // sampled key tiles (even j)
+  const int NKT = J0 + J;                       // key-tile items over both sweeps
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = a.seq_len[0];
+  const int npages = (t + kPage - 1) / kPage;
+  if (J == 0) return;
+  if (t < a.n || npages > a.max_pages) {
+    if (threadIdx.x == 0) flag_error(a.dev_err, HS2_DEV_BAD_LENGTH);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&sm.q_full[s], 1);
+      tc::mbar_init(&sm.q_empty[s], 1);
+      tc::mbar_init(&sm.k_full[s], 1);
+      tc::mbar_init(&sm.k_empty[s], 1);
+      tc::mbar_init(&sm.s_full[s], 1);
+      tc::mbar_init(&sm.s_empty[s], 128);
+    }
+    sm.abort = 0;
+    tc::fence_mbar_init();
+  }
+  for (int e = threadIdx.x; e < kBins * kST / 2; e += kSThreads) reinterpret_cast<uint32_t*>(sm.hist)[e] = 0;
+  if (warp == 1) tc::tmem_alloc(&sm.tmem_base, 256);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tS = sm.tmem_base;
+  auto jof = [&](int kt) { return kt < J0 ? 2 * kt : kt - J0; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int kissued = 0, qissued = 0;
+      for (int kt = 0; kt < NKT && !aborted(sm); ++kt) {
+        const int ks = kt & 1;
+        if (!tc::mbar_wait(&sm.k_empty[ks], ((kt >> 1) & 1) ^ 1)) { set_abort(sm, a.dev_err); break; }
+        const int j = jof(kt);
+        int rows[2];
+        uint32_t bytes = 0;
+        for (int pg = 0; pg < 2; ++pg) {
+          const int lp = 2 * j + pg;
+          rows[pg] = -1;
+          if (lp < npages) {
+            const int phys = a.bt[lp];
+            if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+            else { rows[pg] = (phys * a.Hkv + g) * kPage; bytes += 2 * 8192; }
+          }
+        }
+        tc::mbar_arrive_expect_tx(&sm.k_full[ks], bytes);
+        for (int pg = 0; pg < 2; ++pg)
+          if (rows[pg] >= 0)
+            for (int hh = 0; hh < 2; ++hh)
+              tc::tma_load_2d(sm.k[ks] + hh * 16384 + pg * 8192, &tm_k, 64 * hh, rows[pg], &sm.k_full[ks]);
+        kissued = kt + 1;
+        bool ok = true;
+        for (int hl = 0; hl < G; ++hl) {
+          const int it = kt * G + hl, qs = it & 1;
+          if (!tc::mbar_wait(&sm.q_empty[qs], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(&sm.q_full[qs], kSTile);
+          tc::tma_load_3d(sm.q[qs], &tm_q, 0, g * G + hl, i0, &sm.q_full[qs]);
+          tc::tma_load_3d(sm.q[qs] + kSTile / 2, &tm_q, 64, g * G + hl, i0, &sm.q_full[qs]);
+          qissued = it + 1;
+        }
+        if (!ok) { set_abort(sm, a.dev_err); break; }
+      }
+      for (int kt = max(0, kissued - 2); kt < kissued; ++kt) (void)tc::mbar_wait(&sm.k_full[kt & 1], (kt >> 1) & 1);
+      for (int it = max(0, qissued - 2); it < qissued; ++it) (void)tc::mbar_wait(&sm.q_full[it & 1], (it >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t idS = tc::idesc_bf16_f32(kST, kST);
+      int last = -1;
+      bool ok = true;
+      for (int kt = 0; kt < NKT && ok && !aborted(sm); ++kt) {
+        const int ks = kt & 1;
+        if (!tc::mbar_wait(&sm.k_full[ks], (kt >> 1) & 1)) { ok = false; break; }
+        const uint32_t kb = tc::smem_u32(sm.k[ks]);
+        for (int hl = 0; hl < G; ++hl) {
+          const int it = kt * G + hl, qs = it & 1;
+          if (!tc::mbar_wait(&sm.q_full[qs], (it >> 1) & 1) || !tc::mbar_wait(&sm.s_empty[qs], ((it >> 1) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t qb = tc::smem_u32(sm.q[qs]);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
+            tc::mma_bf16(tS + qs * 128, tc::sdesc_sw128(qb + off), tc::sdesc_sw128(kb + off), idS, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(&sm.s_full[qs]);
+          tc::mma_commit(&sm.q_empty[qs]);
+          last = it;
+        }
+        if (ok) tc::mma_commit(&sm.k_empty[ks]);
+      }
+      if (!ok) set_abort(sm, a.dev_err);
+      if (last >= 0) (void)tc::mbar_wait(&sm.s_full[last & 1], (last >> 1) & 1);
+    }
+  } else {
+    // ---------------------------------------------------------------- scoring warps
+    const int qd = warp & 3;
+    const int r = qd * 32 + lane;
+    const int i = i0 + r;
+    const bool row_ok = i < a.row1;
+    const int nF = row_ok ? max(0, i + 1 - a.w) : 0;
+    const bool ranked = nF > a.k;  // rows whose far range fits the budget need no candidates
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    float lse2r[kMaxSelG];
+#pragma unroll
+    for (int hl = 0; hl < kMaxSelG; ++hl)
+      lse2r[hl] = (hl < G && row_ok) ? a.lse2[(size_t)i * a.Hq + g * G + hl] : 0.f;
+    const size_t slot = ((size_t)(i - a.row0) * a.Hkv + g) * a.cap;
+    uint32_t* bkey = a.cand_key + slot;
+    int32_t* bpos = a.cand_pos + slot;
+    uint32_t tau = 0xffffffffu;
+    int n_samp = 0;  // far positions of this row seen by the sampled sweep
+    int cnt = 0;
+    uint32_t dropped = 0;
+    bool ok = true;
+    for (int kt = 0; kt < NKT && ok; ++kt) {
+      const bool sample = kt < J0;
+      const int j = jof(kt);
+      float sc[128];
+#pragma unroll
+      for (int e = 0; e < 128; ++e) sc[e] = 0.f;
+      for (int hl = 0; hl < G; ++hl) {
+        const int it = kt * G + hl, qs = it & 1;
+        if (!__all_sync(0xffffffffu, !aborted(sm) && tc::mbar_wait(&sm.s_full[qs], (it >> 1) & 1))) { ok = false; break; }
+        __syncwarp();
+        tc::tc_fence_after();
+        float l2 = lse2r[0];
+#pragma unroll
+        for (int u = 1; u < kMaxSelG; ++u) l2 = (hl == u) ? lse2r[u] : l2;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          tc::tmem_ld32(tS + lane_off + qs * 128 + c * 32, x);
+          if (sample) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) sc[c * 32 + e] += tc::ex2(fmaf(x[e], a.scale_log2, -l2));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sc[c * 32 + e] += tc::ex2(fmaf(x[e], a.scale_log2, -l2));
+          }
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&sm.s_empty[qs]);
+      }
+      if (!ok) break;
+      const int s0 = j * kST;
+      if (!ranked) {
+        // rows whose far range fits the budget keep no candidates
+      } else if (sample) {
+#pragma unroll
+        for (int e = 0; e < 128; e += 2) {
+          if (s0 + e < nF) {
+            const int bin = min(kBins - 1, max(0, (int)(__float_as_uint(sc[e]) >> 20) - (int)kBinBase));
+            sm.hist[bin][r] += 1;
+            ++n_samp;
+          }
+        }
+        if (kt == J0 - 1) {
+          // threshold: the estimated count at or above it (sample count scaled by the row's
+          // sampling rate) reaches twice the budget
+          const float scale = n_samp > 0 ? (float)nF / (float)n_samp : 0.f;
+          const float target = 2.f * (float)a.k;
+          float cum = 0.f;
+          tau = 0u;
+          for (int b = kBins - 1; b >= 0; --b) {
+            cum += scale * (float)sm.hist[b][r];
+            if (cum >= target) {
+              tau = b == 0 ? 0u : (uint32_t)(kBinBase + b) << 20;
+              break;
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 128; ++e) {
+          const uint32_t key = __float_as_uint(sc[e]);
+          if (s0 + e < nF && key >= tau) {
+            if (cnt < a.cap) {
+              bkey[cnt] = key;
+              bpos[cnt] = s0 + e;
+              ++cnt;
+            } else {
+              dropped = max(dropped, key);
+            }
+          }
+        }
+      }
+    }
+    if (!ok) set_abort(sm, a.dev_err);
+    if (row_ok) {
+      const size_t rs = (size_t)(i - a.row0) * a.Hkv + g;
+      a.cand_cnt[rs] = ranked ? cnt : 0;
+      a.cand_drop[rs] = dropped;
+      a.cand_tau[rs] = tau;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(sm.tmem_base, 256);
+}
+
+// One CTA per (row, KV head) of the chunk.
+__global__ void __launch_bounds__(256) prefill_topk_kernel(const PsArgs a) {
+  constexpr int NT = 256;
+  const int rs = blockIdx.x;  // (i - row0) * Hkv + g
+  const int i = a.row0 + rs / a.Hkv;
+  if (i >= a.row1) return;
+  const int nF = max(0, i + 1 - a.w);
+  const int kk = min(a.k, nF);
+  int32_t* out = a.idx + ((size_t)i * a.Hkv + rs % a.Hkv) * a.k;
+  int32_t* cnt_out = a.cnt + (size_t)i * a.Hkv + rs % a.Hkv;
+  if (kk == nF) {  // trivial rows: all of F
+    if (threadIdx.x == 0) *cnt_out = kk;
+    for (int j = threadIdx.x; j < a.k; j += NT) out[j] = j < kk ? j : -1;
+    return;
+  }
+  const int c = a.cand_cnt[rs];
+  const uint32_t* keys = a.cand_key + (size_t)rs * a.cap;
+  const int32_t* pos = a.cand_pos + (size_t)rs * a.cap;
+  __shared__ TopkSmem<NT> sm;
+  __shared__ int fail;
+  if (threadIdx.x == 0) fail = c < kk;
+  __syncthreads();
+  if (!fail) {
+    uint32_t prefix = 0, mask = 0;
+    int remaining = kk;
+    auto key = [&](int e) { return __ldcg(keys + e); };
+    radix_pass<NT>(c, key, 20, 12, prefix, mask, remaining, sm);
+    radix_pass<NT>(c, key, 8, 12, prefix, mask, remaining, sm);
+    radix_pass<NT>(c, key, 0, 8, prefix, mask, remaining, sm);
+    // prefix = the kk-th largest kept key; a larger dropped key would belong in the answer
+    if (threadIdx.x == 0 && a.cand_drop[rs] > prefix) fail = 1;
+    __syncthreads();
+    if (!fail) {
+      compact_selected<NT>(c, key, prefix, remaining, [&](int j, int e) { out[j] = __ldcg(pos + e); }, sm);
+      if (threadIdx.x == 0) *cnt_out = kk;
+      for (int j = kk + threadIdx.x; j < a.k; j += NT) out[j] = -1;
+    }
+  }
+  if (fail) {
+    if (threadIdx.x == 0) {
+      *cnt_out = -1;
+      flag_error(a.dev_err, HS2_DEV_SELECT);
+    }
+    for (int j = threadIdx.x; j < a.k; j += NT) out[j] = -1;
+  }
+}
+
+size_t prefill_scan_smem() { return sizeof(PsSmem) + 1024; }
+
+cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, const PsArgs& a, cudaStream_t s) {
+  const size_t sm = prefill_scan_smem();
+  cudaError_t e = cudaFuncSetAttribute(prefill_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  const int tiles = (a.row1 - a.row0 + kST - 1) / kST;
+  prefill_scan_kernel<<<dim3(tiles, a.Hkv), kSThreads, sm, s>>>(tq, tk, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prefill_topk_kernel<<<(a.row1 - a.row0) * a.Hkv, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace hs2
