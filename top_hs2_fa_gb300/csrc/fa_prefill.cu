@@ -180,8 +180,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (!__all_sync(0xffffffffu, !aborted(sm) && tc::mbar_wait(&sm.s_full[sb], (j >> 1) & 1))) { ok = false; break; }
       tc::tc_fence_after();
       float x[4][32];
+      {
+        uint32_t raw[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + lane_off + sb * 128 + c * 32, x[c]);
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32_async(tS + lane_off + sb * 128 + c * 32, raw[c]);
+        tc::tmem_wait_ld(raw[3]);
+        tc::tmem_regs_ready(raw[0]);
+        tc::tmem_regs_ready(raw[1]);
+        tc::tmem_regs_ready(raw[2]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[c][e] = __uint_as_float(raw[c][e]);
+      }
       tc::tc_fence_before();
       tc::mbar_arrive(&sm.s_empty[sb]);
       const int kbase = j * kPT;

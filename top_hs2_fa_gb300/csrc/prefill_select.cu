@@ -33,17 +33,20 @@ namespace hs2 {
 namespace {
 
 constexpr int kST = 128;        // rows per tile = keys per key tile
-constexpr int kSThreads = 192;  // TMA warp, MMA warp, 4 scoring warps
+constexpr int kSThreads = 320;  // TMA warp, MMA warp, 8 scoring warps (two per TMEM lane quadrant)
 constexpr uint32_t kSTile = kST * 128 * 2;
 constexpr int kBins = 256;
 constexpr uint32_t kBinBase = 0x410 - (kBins - 1);  // bin 255 holds keys >> 20 == 0x410 (score 8.0)
 constexpr int kMaxSelG = 8;  // query heads per KV head handled by the scan
 
+constexpr int kQStages = 2;
+
 struct PsSmem {
-  uint8_t q[2][kSTile];            // A of S (query rows x d), one head per stage
+  uint8_t q[kQStages][kSTile];     // A of S (query rows x d), one head per stage
   uint8_t k[2][kSTile];            // B of S (keys x d)
-  uint16_t hist[kBins][kST];       // per-row sample histograms ([bin][row])
-  uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], s_full[2], s_empty[2];
+  uint8_t hist[kBins][kST];        // per-row sample histograms ([bin][row]), saturating counts
+  float xch[64][kST];              // columns 64-127 of a key tile's scores, handed to the row owner
+  uint64_t q_full[kQStages], q_empty[kQStages], k_full[2], k_empty[2], s_full[2], s_empty[2], x_full, x_empty;
   uint32_t tmem_base;
   int abort;
 };
@@ -79,18 +82,22 @@ __global__ void __launch_bounds__(kSThreads, 1)
     return;
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kQStages; ++s) {
       tc::mbar_init(&sm.q_full[s], 1);
       tc::mbar_init(&sm.q_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&sm.k_full[s], 1);
       tc::mbar_init(&sm.k_empty[s], 1);
       tc::mbar_init(&sm.s_full[s], 1);
-      tc::mbar_init(&sm.s_empty[s], 128);
+      tc::mbar_init(&sm.s_empty[s], 256);
     }
+    tc::mbar_init(&sm.x_full, 128);
+    tc::mbar_init(&sm.x_empty, 128);
     sm.abort = 0;
     tc::fence_mbar_init();
   }
-  for (int e = threadIdx.x; e < kBins * kST / 2; e += kSThreads) reinterpret_cast<uint32_t*>(sm.hist)[e] = 0;
+  for (int e = threadIdx.x; e < kBins * kST / 4; e += kSThreads) reinterpret_cast<uint32_t*>(sm.hist)[e] = 0;
   if (warp == 1) tc::tmem_alloc(&sm.tmem_base, 256);
   tc::tc_fence_before();
   __syncthreads();
@@ -125,8 +132,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         kissued = kt + 1;
         bool ok = true;
         for (int hl = 0; hl < G; ++hl) {
-          const int it = kt * G + hl, qs = it & 1;
-          if (!tc::mbar_wait(&sm.q_empty[qs], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
+          const int it = kt * G + hl, qs = it % kQStages;
+          if (!tc::mbar_wait(&sm.q_empty[qs], ((it / kQStages) & 1) ^ 1)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(&sm.q_full[qs], kSTile);
           tc::tma_load_3d(sm.q[qs], &tm_q, 0, g * G + hl, i0, &sm.q_full[qs]);
           tc::tma_load_3d(sm.q[qs] + kSTile / 2, &tm_q, 64, g * G + hl, i0, &sm.q_full[qs]);
@@ -135,7 +142,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (!ok) { set_abort(sm, a.dev_err); break; }
       }
       for (int kt = max(0, kissued - 2); kt < kissued; ++kt) (void)tc::mbar_wait(&sm.k_full[kt & 1], (kt >> 1) & 1);
-      for (int it = max(0, qissued - 2); it < qissued; ++it) (void)tc::mbar_wait(&sm.q_full[it & 1], (it >> 1) & 1);
+      for (int it = max(0, qissued - kQStages); it < qissued; ++it)
+        (void)tc::mbar_wait(&sm.q_full[it % kQStages], (it / kQStages) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -148,8 +156,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (!tc::mbar_wait(&sm.k_full[ks], (kt >> 1) & 1)) { ok = false; break; }
         const uint32_t kb = tc::smem_u32(sm.k[ks]);
         for (int hl = 0; hl < G; ++hl) {
-          const int it = kt * G + hl, qs = it & 1;
-          if (!tc::mbar_wait(&sm.q_full[qs], (it >> 1) & 1) || !tc::mbar_wait(&sm.s_empty[qs], ((it >> 1) & 1) ^ 1)) {
+          const int it = kt * G + hl, qs = it % kQStages, sb = it & 1;
+          if (!tc::mbar_wait(&sm.q_full[qs], (it / kQStages) & 1) || !tc::mbar_wait(&sm.s_empty[sb], ((it >> 1) & 1) ^ 1)) {
             ok = false;
             break;
           }
@@ -158,9 +166,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
-            tc::mma_bf16(tS + qs * 128, tc::sdesc_sw128(qb + off), tc::sdesc_sw128(kb + off), idS, kk > 0 ? 1u : 0u);
+            tc::mma_bf16(tS + sb * 128, tc::sdesc_sw128(qb + off), tc::sdesc_sw128(kb + off), idS, kk > 0 ? 1u : 0u);
           }
-          tc::mma_commit(&sm.s_full[qs]);
+          tc::mma_commit(&sm.s_full[sb]);
           tc::mma_commit(&sm.q_empty[qs]);
           last = it;
         }
@@ -171,6 +179,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- scoring warps
+    // warps 2-5 own rows and columns 0-63 of every S tile; warps 6-9 take columns 64-127
+    // of the same rows and hand their partial scores over through shared memory.
+    const int half = (warp - 2) >> 2;
     const int qd = warp & 3;
     const int r = qd * 32 + lane;
     const int i = i0 + r;
@@ -193,33 +204,50 @@ __global__ void __launch_bounds__(kSThreads, 1)
     for (int kt = 0; kt < NKT && ok; ++kt) {
       const bool sample = kt < J0;
       const int j = jof(kt);
-      float sc[128];
+      float sc[64];
 #pragma unroll
-      for (int e = 0; e < 128; ++e) sc[e] = 0.f;
+      for (int e = 0; e < 64; ++e) sc[e] = 0.f;
       for (int hl = 0; hl < G; ++hl) {
-        const int it = kt * G + hl, qs = it & 1;
-        if (!__all_sync(0xffffffffu, !aborted(sm) && tc::mbar_wait(&sm.s_full[qs], (it >> 1) & 1))) { ok = false; break; }
+        const int it = kt * G + hl, sb = it & 1;
+        // votes keep the warp converged for the warp-collective TMEM loads
+        if (!__all_sync(0xffffffffu, !aborted(sm) && tc::mbar_wait(&sm.s_full[sb], (it >> 1) & 1))) { ok = false; break; }
         __syncwarp();
         tc::tc_fence_after();
         float l2 = lse2r[0];
 #pragma unroll
         for (int u = 1; u < kMaxSelG; ++u) l2 = (hl == u) ? lse2r[u] : l2;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float x[32];
-          tc::tmem_ld32(tS + lane_off + qs * 128 + c * 32, x);
-          if (sample) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) sc[c * 32 + e] += tc::ex2(fmaf(x[e], a.scale_log2, -l2));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) sc[c * 32 + e] += tc::ex2(fmaf(x[e], a.scale_log2, -l2));
-          }
-        }
+        uint32_t raw[2][32];
+        const uint32_t ta = tS + lane_off + sb * 128 + half * 64;
+        tc::tmem_ld32_async(ta, raw[0]);
+        tc::tmem_ld32_async(ta + 32, raw[1]);
+        tc::tmem_wait_ld(raw[1]);
+        tc::tmem_regs_ready(raw[0]);
         tc::tc_fence_before();
-        tc::mbar_arrive(&sm.s_empty[qs]);
+        tc::mbar_arrive(&sm.s_empty[sb]);
+        if (sample) {
+#pragma unroll
+          for (int e = 0; e < 64; e += 2)
+            sc[e] += tc::ex2(fmaf(__uint_as_float(raw[e >> 5][e & 31]), a.scale_log2, -l2));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            sc[e] += tc::ex2(fmaf(__uint_as_float(raw[e >> 5][e & 31]), a.scale_log2, -l2));
+        }
       }
       if (!ok) break;
+      if (half == 1) {
+        // hand columns 64-127 to the row owner
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.x_empty, (kt & 1) ^ 1))) { ok = false; break; }
+#pragma unroll
+        for (int e = 0; e < 64; ++e) sm.xch[e][r] = sc[e];
+        tc::mbar_arrive(&sm.x_full);
+        continue;
+      }
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.x_full, kt & 1))) { ok = false; break; }
+      float sc2[64];
+#pragma unroll
+      for (int e = 0; e < 64; ++e) sc2[e] = sm.xch[e][r];
+      tc::mbar_arrive(&sm.x_empty);
       const int s0 = j * kST;
       if (!ranked) {
         // rows whose far range fits the budget keep no candidates
@@ -227,8 +255,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
         for (int e = 0; e < 128; e += 2) {
           if (s0 + e < nF) {
-            const int bin = min(kBins - 1, max(0, (int)(__float_as_uint(sc[e]) >> 20) - (int)kBinBase));
-            sm.hist[bin][r] += 1;
+            const float v = e < 64 ? sc[e] : sc2[e - 64];
+            const int bin = min(kBins - 1, max(0, (int)(__float_as_uint(v) >> 20) - (int)kBinBase));
+            const uint8_t hv = sm.hist[bin][r];
+            sm.hist[bin][r] = hv == 255 ? hv : (uint8_t)(hv + 1);  // saturating: undercounts only lower tau
             ++n_samp;
           }
         }
@@ -250,7 +280,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       } else {
 #pragma unroll
         for (int e = 0; e < 128; ++e) {
-          const uint32_t key = __float_as_uint(sc[e]);
+          const uint32_t key = __float_as_uint(e < 64 ? sc[e] : sc2[e - 64]);
           if (s0 + e < nF && key >= tau) {
             if (cnt < a.cap) {
               bkey[cnt] = key;
@@ -264,7 +294,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
     }
     if (!ok) set_abort(sm, a.dev_err);
-    if (row_ok) {
+    if (half == 0 && row_ok) {
       const size_t rs = (size_t)(i - a.row0) * a.Hkv + g;
       a.cand_cnt[rs] = ranked ? cnt : 0;
       a.cand_drop[rs] = dropped;
