@@ -179,9 +179,10 @@ bool encode_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1
 // ---------------------------------------------------------------------------- bf16 prefill layout
 bool use_prefill_tc(const hs2_kv* kv, int prefill) { return prefill && kv->dtype == HS2_BF16 && kv->d == 128; }
 
-// Rows are ranked in chunks of kPrefillChunk rows; each chunk's candidate buffers hold cap
-// entries per (row, KV head), cap = max(256, 4k).
-constexpr int kPrefillChunk = 8192;
+// Rows are ranked in chunks of kPrefillChunk rows (one scan launch per chunk; a single
+// chunk keeps the heaviest-first schedule balanced); each chunk's candidate buffers hold
+// cap entries per (row, KV head), cap = max(256, 4k).
+constexpr int kPrefillChunk = 32768;
 
 struct PrefillPlan {
   int chunk, cap;

@@ -7,7 +7,7 @@
 // a tcgen05 recomputation of Q K^T and consumed on the fly.
 //
 // prefill_scan_kernel — one CTA per (128-row tile, KV head), one row per scoring thread:
-//   sweep 0 (sampled): every 2nd key tile, every 2nd column; each thread bins the sampled
+//   sweep 0 (sampled): every key tile, every 4th column; each thread bins the sampled
 //            scores of its row into a 256-bin log histogram (1/8 octave per bin) held in
 //            shared memory, then picks a threshold tau whose estimated count of keys at or
 //            above it is twice the budget;
@@ -38,6 +38,9 @@ constexpr uint32_t kSTile = kST * 128 * 2;
 constexpr int kBins = 256;
 constexpr uint32_t kBinBase = 0x410 - (kBins - 1);  // bin 255 holds keys >> 20 == 0x410 (score 8.0)
 constexpr int kMaxSelG = 8;  // query heads per KV head handled by the scan
+// The sampled sweep scores every 4th position of every key tile (position-correlated
+// scores would bias a sample of whole tiles).
+constexpr int kSampleStride = 4;
 
 constexpr int kQStages = 2;
 
@@ -71,7 +74,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int i_last = min(a.row1, i0 + kST) - 1;
   const int keys_needed = max(0, i_last + 1 - a.w);
   const int J = (keys_needed + kST - 1) / kST;  // key tiles of the exact sweep
-  const int J0 = (J + 1) / 2;                   // sampled key tiles (even j)
+  const int J0 = J;                             // sampled sweep: every key tile, every 4th column
   const int NKT = J0 + J;                       // key-tile items over both sweeps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = a.seq_len[0];
@@ -103,7 +106,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tS = sm.tmem_base;
-  auto jof = [&](int kt) { return kt < J0 ? 2 * kt : kt - J0; };
+  auto jof = [&](int kt) { return kt < J0 ? kt : kt - J0; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         tc::mbar_arrive(&sm.s_empty[sb]);
         if (sample) {
 #pragma unroll
-          for (int e = 0; e < 64; e += 2)
+          for (int e = 0; e < 64; e += kSampleStride)
             sc[e] += tc::ex2(fmaf(__uint_as_float(raw[e >> 5][e & 31]), a.scale_log2, -l2));
         } else {
 #pragma unroll
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // rows whose far range fits the budget keep no candidates
       } else if (sample) {
 #pragma unroll
-        for (int e = 0; e < 128; e += 2) {
+        for (int e = 0; e < 128; e += kSampleStride) {
           if (s0 + e < nF) {
             const float v = e < 64 ? sc[e] : sc2[e - 64];
             const int bin = min(kBins - 1, max(0, (int)(__float_as_uint(v) >> 20) - (int)kBinBase));
@@ -306,9 +309,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (warp == 1) tc::tmem_dealloc(sm.tmem_base, 256);
 }
 
-// One CTA per (row, KV head) of the chunk.
-__global__ void __launch_bounds__(256) prefill_topk_kernel(const PsArgs a) {
-  constexpr int NT = 256;
+// One CTA per (row, KV head) of the chunk; each thread keeps a contiguous run of the row's
+// candidate keys in registers, so the three radix passes and the ordered compaction read
+// global memory once.
+constexpr int kTopkThreads = 256;
+constexpr int kTopkSeg = 16;  // candidates per thread (cap <= 4096)
+
+__global__ void __launch_bounds__(kTopkThreads) prefill_topk_kernel(const PsArgs a) {
+  constexpr int NT = kTopkThreads;
+  const int tid = threadIdx.x;
   const int rs = blockIdx.x;  // (i - row0) * Hkv + g
   const int i = a.row0 + rs / a.Hkv;
   if (i >= a.row1) return;
@@ -317,40 +326,75 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(const PsArgs a) {
   int32_t* out = a.idx + ((size_t)i * a.Hkv + rs % a.Hkv) * a.k;
   int32_t* cnt_out = a.cnt + (size_t)i * a.Hkv + rs % a.Hkv;
   if (kk == nF) {  // trivial rows: all of F
-    if (threadIdx.x == 0) *cnt_out = kk;
-    for (int j = threadIdx.x; j < a.k; j += NT) out[j] = j < kk ? j : -1;
+    if (tid == 0) *cnt_out = kk;
+    for (int j = tid; j < a.k; j += NT) out[j] = j < kk ? j : -1;
     return;
   }
-  const int c = a.cand_cnt[rs];
+  const int c = min(a.cand_cnt[rs], a.cap);
   const uint32_t* keys = a.cand_key + (size_t)rs * a.cap;
   const int32_t* pos = a.cand_pos + (size_t)rs * a.cap;
   __shared__ TopkSmem<NT> sm;
-  __shared__ int fail;
-  if (threadIdx.x == 0) fail = c < kk;
-  __syncthreads();
+  bool fail = c < kk;
+  uint32_t T = 0;
+  int take_eq = 0;
+  const int seg = (c + NT - 1) / NT;
+  const int lo = min(c, tid * seg), hi = min(c, lo + seg);
+  uint32_t kr[kTopkSeg];
+#pragma unroll
+  for (int e = 0; e < kTopkSeg; ++e) kr[e] = (lo + e < hi) ? __ldcg(keys + lo + e) : 0u;
   if (!fail) {
     uint32_t prefix = 0, mask = 0;
     int remaining = kk;
-    auto key = [&](int e) { return __ldcg(keys + e); };
-    radix_pass<NT>(c, key, 20, 12, prefix, mask, remaining, sm);
-    radix_pass<NT>(c, key, 8, 12, prefix, mask, remaining, sm);
-    radix_pass<NT>(c, key, 0, 8, prefix, mask, remaining, sm);
-    // prefix = the kk-th largest kept key; a larger dropped key would belong in the answer
-    if (threadIdx.x == 0 && a.cand_drop[rs] > prefix) fail = 1;
-    __syncthreads();
-    if (!fail) {
-      compact_selected<NT>(c, key, prefix, remaining, [&](int j, int e) { out[j] = __ldcg(pos + e); }, sm);
-      if (threadIdx.x == 0) *cnt_out = kk;
-      for (int j = kk + threadIdx.x; j < a.k; j += NT) out[j] = -1;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int sh = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
+      const int nb = pass == 2 ? 256 : 4096;
+      for (int b = tid; b < nb; b += NT) sm.hist[b] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int e = 0; e < kTopkSeg; ++e) {
+        const bool part = lo + e < hi && (kr[e] & mask) == prefix;
+        hist_add_warp(sm.hist, part, (kr[e] >> sh) & (uint32_t)(nb - 1));
+      }
+      __syncthreads();
+      const uint32_t dig = find_digit<NT>(sm.hist, nb, remaining, sm);
+      prefix |= dig << sh;
+      mask |= (uint32_t)(nb - 1) << sh;
     }
+    T = prefix;  // the kk-th largest kept key
+    take_eq = remaining;
+    // a larger dropped key would belong in the answer (equal ones come later and lose)
+    fail = a.cand_drop[rs] > T;
   }
   if (fail) {
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
       *cnt_out = -1;
       flag_error(a.dev_err, HS2_DEV_SELECT);
     }
-    for (int j = threadIdx.x; j < a.k; j += NT) out[j] = -1;
+    for (int j = tid; j < a.k; j += NT) out[j] = -1;
+    return;
   }
+  int n_eq = 0, n_gt = 0;
+#pragma unroll
+  for (int e = 0; e < kTopkSeg; ++e)
+    if (lo + e < hi) {
+      n_eq += kr[e] == T;
+      n_gt += kr[e] > T;
+    }
+  const int eq_before = block_exclusive_scan<NT>(n_eq, sm.warp_tot);
+  const int eq_take = max(0, min(n_eq, take_eq - eq_before));
+  int p = block_exclusive_scan<NT>(n_gt + eq_take, sm.warp_tot);
+  int eq_seen = eq_before;
+#pragma unroll
+  for (int e = 0; e < kTopkSeg; ++e) {
+    if (lo + e < hi) {
+      bool sel = kr[e] > T;
+      if (kr[e] == T) sel = eq_seen++ < take_eq;
+      if (sel) out[p++] = __ldcg(pos + lo + e);
+    }
+  }
+  if (tid == 0) *cnt_out = kk;
+  for (int j = kk + tid; j < a.k; j += NT) out[j] = -1;
 }
 
 size_t prefill_scan_smem() { return sizeof(PsSmem) + 1024; }
@@ -363,7 +407,8 @@ cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, 
   prefill_scan_kernel<<<dim3(tiles, a.Hkv), kSThreads, sm, s>>>(tq, tk, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prefill_topk_kernel<<<(a.row1 - a.row0) * a.Hkv, 256, 0, s>>>(a);
+  if (a.cap > kTopkThreads * kTopkSeg) return cudaErrorInvalidValue;
+  prefill_topk_kernel<<<(a.row1 - a.row0) * a.Hkv, kTopkThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
