@@ -121,3 +121,29 @@ def test_prefill_full_size_sampled_rows(H):
                                      [0, w - 1, w, w + k - 1, w + k, n - 1]]))
     idx, cnt, _ = check_selection(H, grp, rows)
     assert (cnt >= 0).all()
+
+
+@pytest.mark.parametrize("n,Hq,Hkv,w,k", [(1000, 8, 2, 16, 64), (777, 32, 4, 128, 256), (600, 16, 1, 32, 100)])
+def test_prefill_sa_rows(H, n, Hq, Hkv, w, k):
+    """SA prefill (tensor-core gather) on every row, with the GPU's own index sets, and with
+    the oracle's index sets fed to both."""
+    import torch
+
+    grp = W.prefill_group(n, Hq, Hkv, 128, w=w, k=k, dtype="bf16", seed=41, n_sa=2, rho=0.99, permute=True)
+    o, lse, idx, cnt = run_fa(H, grp)
+    dkv = kv_to_device(grp.kv)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rows = np.arange(n)
+    for j in range(2):
+        qs = to_torch(grp.q_sa[j], "bf16")
+        osa = H.hs2_sa_reuse(qs, dkv, w, to_torch(idx, "i32"), to_torch(cnt, "i32"), k, grp.scale, prefill=True,
+                             dev_err=err).cpu().numpy()
+        ref = O.sa_prefill_rows(grp.q_sa[j], grp.kv, rows, w, idx, cnt, grp.scale)
+        assert max_abs(osa, ref) <= tol("bf16"), max_abs(osa, ref)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    _, _, idx_r, cnt_r = O.fa_prefill_rows(grp.q_fa, grp.kv, rows, w, k, grp.scale)
+    osa = H.hs2_sa_reuse(to_torch(grp.q_sa[0], "bf16"), dkv, w, to_torch(idx_r, "i32"), to_torch(cnt_r, "i32"), k,
+                         grp.scale, prefill=True).cpu().numpy()
+    ref = O.sa_prefill_rows(grp.q_sa[0], grp.kv, rows, w, idx_r, cnt_r, grp.scale)
+    assert max_abs(osa, ref) <= tol("bf16")

@@ -263,7 +263,6 @@ static hs2_status fa_select_prefill_tc(const void* q, int n, int Hq, const hs2_k
   const PrefillPlan p = prefill_plan(n, Hq, kv, k);
   if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
   const bool ranked = k > 0 && n - w > k;  // some row's far range exceeds the budget
-  if (ranked && Hq / kv->Hkv > 8) return HS2_ERR_UNSUPPORTED;
   char* ws = (char*)workspace;
   CUtensorMap tq, tk, tv;
   const uint64_t rows = (uint64_t)kv->num_pages * kv->Hkv * 64;
@@ -450,6 +449,12 @@ hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int
   a.logits = nullptr;
   a.out_o = o;
   a.dev_err = dev_err;
+  if (prefill && hs2::sa_mma_supported(a.G, a.D, kv->dtype == HS2_BF16, w, k)) {
+    // prefill rows: per-row gathered Q.K and P.V are dense contractions -> tensor cores
+    cudaError_t e = profiled(HS2_STAGE_SA_GATHER, s, [&] { return hs2::launch_sa_mma(a, B_or_n, s); });
+    if (e != cudaSuccess) return cuda_fail(e);
+    return HS2_OK;
+  }
   if (hs2::sa_gather_supported(a.G, a.D, kv->dtype == HS2_BF16)) {
     // one CTA per (query, KV head) stages W ∪ S through shared memory; no partials
     cudaError_t e = profiled(HS2_STAGE_SA_GATHER, s, [&] { return hs2::launch_sa_gather(a, B_or_n, s); });

@@ -136,6 +136,8 @@ cudaError_t launch_fa_decode_mma(const AttnArgs& a, int Bq, cudaStream_t s);
 cudaError_t launch_attn_partial(const AttnArgs& a, int Bq, int bf16, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s);
 bool sa_gather_supported(int G, int D, int bf16);
+bool sa_mma_supported(int G, int D, int bf16, int w, int k);
+cudaError_t launch_sa_mma(const AttnArgs& a, int Bq, cudaStream_t s);
 size_t lightning_scan_smem();
 cudaError_t launch_lightning_scan(const CUtensorMap& tm_k, const CUtensorMap& tm_q, const IdxArgs& a, int B,
                                   int grid_x, cudaStream_t s);

@@ -37,7 +37,6 @@ constexpr int kSThreads = 320;  // TMA warp, MMA warp, 8 scoring warps (two per 
 constexpr uint32_t kSTile = kST * 128 * 2;
 constexpr int kBins = 256;
 constexpr uint32_t kBinBase = 0x410 - (kBins - 1);  // bin 255 holds keys >> 20 == 0x410 (score 8.0)
-constexpr int kMaxSelG = 8;  // query heads per KV head handled by the scan
 // The sampled sweep scores every 4th position of every key tile (position-correlated
 // scores would bias a sample of whole tiles).
 constexpr int kSampleStride = 4;
@@ -192,10 +191,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int nF = row_ok ? max(0, i + 1 - a.w) : 0;
     const bool ranked = nF > a.k;  // rows whose far range fits the budget need no candidates
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-    float lse2r[kMaxSelG];
-#pragma unroll
-    for (int hl = 0; hl < kMaxSelG; ++hl)
-      lse2r[hl] = (hl < G && row_ok) ? a.lse2[(size_t)i * a.Hq + g * G + hl] : 0.f;
+    const float* lse2_row = a.lse2 + (size_t)(row_ok ? i : a.row0) * a.Hq + g * G;
     const size_t slot = ((size_t)(i - a.row0) * a.Hkv + g) * a.cap;
     uint32_t* bkey = a.cand_key + slot;
     int32_t* bpos = a.cand_pos + slot;
@@ -216,9 +212,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (!__all_sync(0xffffffffu, !aborted(sm) && tc::mbar_wait(&sm.s_full[sb], (it >> 1) & 1))) { ok = false; break; }
         __syncwarp();
         tc::tc_fence_after();
-        float l2 = lse2r[0];
-#pragma unroll
-        for (int u = 1; u < kMaxSelG; ++u) l2 = (hl == u) ? lse2r[u] : l2;
+        const float l2 = __ldg(lse2_row + hl);
         uint32_t raw[2][32];
         const uint32_t ta = tS + lane_off + sb * 128 + half * 64;
         tc::tmem_ld32_async(ta, raw[0]);

@@ -1,0 +1,151 @@
+// sa_prefill.cu — SA gather-attention for every row of a bf16 prefill, on tensor cores.
+//
+// Each row's SA query attends to its forced window and its FA-selected far positions
+// under one softmax ("HySparse2：整体架构、KV 生命周期与 PD 分离", §5, §7.2, §7.4), entries
+// read in place through the block table. In prefill the gathered Q.K and P.V per row are
+// dense contractions over the row's |W ∪ S| keys and the query heads sharing a KV head,
+// so they run on mma.sync (keys as M, heads as N; see mma_attn.cuh).
+//
+// One CTA (4 warps) per (row, KV head). The CTA first resolves the row's positions —
+// window then selected — through the block table into pool row ids in shared memory
+// (one round of dependent loads for the whole row), then each warp walks 16-key steps
+// (steps w, w+4, ...), loading K and V rows straight into MMA fragments with 128-bit
+// loads, and the four warps' online-softmax states are merged at the end.
+#include "common.cuh"
+#include "kernels.h"
+#include "mma_attn.cuh"
+
+namespace hs2 {
+
+template <int D, int NT>
+__global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
+  using Attn = MmaAttn<D, NT>;
+  constexpr int KC = Attn::KC, VC = Attn::VC;
+  const int qi = blockIdx.y, g = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int G = a.G;
+  const QueryGeom qg = query_geom(qi, a.prefill, a.seq_len);
+  const int t = qg.t;
+  float* out = a.out_o + ((size_t)qi * a.Hq + (size_t)g * G) * D;
+  if (t < 1 || t > a.max_t || (t + kPage - 1) / kPage > a.max_pages) {
+    if (tid == 0) flag_error(a.dev_err, HS2_DEV_BAD_LENGTH);
+    for (int e = tid; e < G * D; e += 128) out[e] = 0.f;
+    return;
+  }
+  const int nW = min(a.w, t);
+  const int c0 = a.cnt[(size_t)qi * a.Hkv + g];
+  if (tid == 0 && (c0 < 0 || c0 > a.kcap)) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+  const int nS = max(0, min(a.kcap, c0));
+  const int nU = nW + nS;
+  const int32_t* sel = a.idx + ((size_t)qi * a.Hkv + g) * a.kcap;
+  const int32_t* bt = a.bt + (size_t)qg.b * a.max_pages;
+  const int lim = a.w > 0 ? t - a.w : t;
+
+  extern __shared__ float smem[];
+  float* sm_m = smem;                  // [4][NT*8]
+  float* sm_l = sm_m + 4 * NT * 8;     // [4][NT*8]
+  float* sm_o = sm_l + 4 * NT * 8;     // [4][NT*8][D]
+  int32_t* rowid = reinterpret_cast<int32_t*>(sm_o + 4 * NT * 8 * D);  // [nU] pool row, -1 invalid
+
+  for (int u = tid; u < nU; u += 128) {
+    int pos, r = -1;
+    bool ok = true;
+    if (u < nW) {
+      pos = t - nW + u;
+    } else {
+      pos = sel[u - nW];
+      if (pos < 0 || pos >= lim) {
+        flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+        ok = false;
+      }
+    }
+    if (ok) {
+      const int phys = bt[pos / kPage];
+      if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+      else r = (phys * a.Hkv + g) * kPage + pos % kPage;
+    }
+    rowid[u] = r;
+  }
+  Attn at;
+  at.init(reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)qi * a.Hq + (size_t)g * G) * D, G);
+  __syncthreads();
+
+  const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(a.v);
+  const int nsteps = (nU + 15) / 16;
+  for (int st = warp; st < nsteps; st += 4) {
+    const int u0 = st * 16;
+    const int ua = u0 + gid, ub = u0 + gid + 8;
+    const int ra = ua < nU ? rowid[ua] : -1;
+    const int rb = ub < nU ? rowid[ub] : -1;
+    uint4 kr0[KC], kr1[KC], vr[4][VC];
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      kr0[j] = ra >= 0 ? ldg_nc_v4(kb + (size_t)ra * D + 32 * j + 8 * tig) : make_uint4(0, 0, 0, 0);
+      kr1[j] = rb >= 0 ? ldg_nc_v4(kb + (size_t)rb * D + 32 * j + 8 * tig) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int uv = u0 + 2 * tig + (e & 1) + 8 * (e >> 1);
+      const int rv = uv < nU ? rowid[uv] : -1;
+#pragma unroll
+      for (int j = 0; j < VC; ++j)
+        vr[e][j] = rv >= 0 ? ldg_nc_v4(vb + (size_t)rv * D + (D / 8) * gid + 8 * j) : make_uint4(0, 0, 0, 0);
+    }
+    float x[NT][4];
+    at.step(kr0, kr1, vr, ra >= 0, rb >= 0, a.scale_log2, x);
+  }
+  at.store(warp, sm_m, sm_l, sm_o);
+  __syncthreads();
+  for (int e = tid; e < G * D; e += 128) {
+    const int hl = e / D, dd = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w * NT * 8 + hl]);
+    float L = 0.f, Ov = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float f = exp2_rel(sm_m[w * NT * 8 + hl], M);
+      L += f * sm_l[w * NT * 8 + hl];
+      Ov += f * sm_o[((size_t)w * NT * 8 + hl) * D + dd];
+    }
+    out[e] = L > 0.f ? Ov / L : 0.f;
+  }
+}
+
+template <int D, int NT>
+static cudaError_t launch_sa_mma_t(const AttnArgs& a, int Bq, cudaStream_t s) {
+  const size_t sm = (size_t)(64 * NT + 32 * NT * D) * sizeof(float) + (size_t)(a.w + a.kcap) * sizeof(int32_t);
+  auto kern = sa_mma_kernel<D, NT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(a.Hkv, Bq), 128, sm, s>>>(a);
+  return cudaGetLastError();
+}
+
+bool sa_mma_supported(int G, int D, int bf16, int w, int k) {
+  if (!bf16 || (D != 64 && D != 128) || G > 32 || (G > 8 && G != 16 && G != 32)) return false;
+  const long long NT = (G + 7) / 8;
+  return (64 * NT + 32 * NT * D) * 4 + ((long long)w + k) * 4 <= 227LL * 1024;
+}
+
+cudaError_t launch_sa_mma(const AttnArgs& a, int Bq, cudaStream_t s) {
+  const int NTl = (a.G + 7) / 8;
+  if (a.D == 128) {
+    switch (NTl) {
+      case 1: return launch_sa_mma_t<128, 1>(a, Bq, s);
+      case 2: return launch_sa_mma_t<128, 2>(a, Bq, s);
+      case 4: return launch_sa_mma_t<128, 4>(a, Bq, s);
+    }
+  } else if (a.D == 64) {
+    switch (NTl) {
+      case 1: return launch_sa_mma_t<64, 1>(a, Bq, s);
+      case 2: return launch_sa_mma_t<64, 2>(a, Bq, s);
+      case 4: return launch_sa_mma_t<64, 4>(a, Bq, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace hs2
