@@ -1,21 +1,25 @@
 #!/usr/bin/env python3
-"""Benchmark: one decode step of one HySparse2 Cross group (FA + selection, 5 SA layers).
+"""Benchmark of the group-shared top-k sparse attention hot path on one GB300.
 
-Workload (synthetic, seeded): batch 64, context lengths uniform in [16384, 32768],
-Hq=32, Hkv=4, head_dim=128, window w=128, top-k=1024, bf16 paged KV (page 64,
-permuted block table), queries x @ W_Q with a distinct W_Q per layer, 32 needles
-per sequence. One step = hs2_fa_select + 5 x hs2_sa_reuse on resident inputs.
+Default workload (the decode metric's configuration): one decode step of one
+HySparse2 Cross group — batch 64, context lengths uniform in [16384, 32768],
+Hq=32, Hkv=4, head_dim=128, window 128, top-k 1024, bf16 paged KV (page 64,
+permuted block table), queries x @ W_Q with a distinct W_Q per layer, 32
+needles per sequence. One step = hs2_fa_select + 5 x hs2_sa_reuse on resident
+inputs. ``--workload`` selects the other configurations for measurement:
+``prefill`` (n=32768), ``long_decode`` (batch 16 x 131072, 4 independent
+caches, 24 layers) and ``csa2`` (Full + Reindex indexer, 5 MQA layers).
 
-Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle instead.
-Multi-GPU (torchrun): every rank runs its own independent batch (weak scaling, no
-data-path collective); the reported time is the max over ranks.
+Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload. Under torchrun every rank runs its own
+independent batch (weak scaling, no data-path collective); the reported time is
+the max over ranks.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
-import math
 import os
 import signal
 import statistics
@@ -27,10 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode queries/s and HBM GB/s (FA+5 SA group); prefill tok/s and TFLOP/s"
-WORKLOAD = "decode_bf16_b64_t16k-32k"
-B, T_LO, T_HI, HQ, HKV, D, WIN, TOPK, NSA = 64, 16384, 32768, 32, 4, 128, 128, 1024, 5
-FA_KERNEL = "fa_decode_mma_kernel"
-FA_SOURCE = os.path.join(ROOT, "top_hs2_fa_gb300", "csrc", "fa_decode.cu")
+NSA = 5
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -41,20 +42,23 @@ def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         j = json.load(open(p))
-        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
-    return 6800.0, 1900.0, "fallback"
+        return {"hbm": float(j["hbm_gbs"]), "bf16": float(j["bf16_tflops"]),
+                "bf16_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "src": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
 
 
-def source_sha() -> str:
-    return hashlib.sha256(open(FA_SOURCE, "rb").read()).hexdigest()[:16]
+def source_sha(paths) -> str:
+    h = hashlib.sha256()
+    for p in ([paths] if isinstance(paths, str) else paths):
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """ncu DRAM bytes per FA-scan launch, if taken on the current kernel source."""
+def recorded_traffic(workload: str, kernel: str, source: str):
+    """ncu DRAM bytes per launch of the roofline kernel, if taken on the current kernel source."""
     try:
-        j = json.load(open(TRAFFIC_FILE))
-        e = j.get(WORKLOAD, {}).get(FA_KERNEL)
-        if e and e.get("source_sha") == source_sha():
+        e = json.load(open(TRAFFIC_FILE)).get(workload, {}).get(kernel)
+        if e and e.get("source_sha") == source_sha(source):
             return float(e["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
         pass
@@ -65,7 +69,6 @@ class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons while the GPU is busy."""
 
     def __init__(self, gpu_index: int):
-        self.proc = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits", "-lms", "200",
@@ -95,8 +98,7 @@ class ClockSampler:
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         smax = max(r["smax"] for r in rows)
-        busy = [r for r in rows if r["power"] > 0] or rows
-        busy = sorted(busy, key=lambda r: r["power"])[len(busy) // 2:] or busy  # upper half by power
+        busy = sorted(rows, key=lambda r: r["power"])[len(rows) // 2:] or rows  # upper half by power draw
         reasons = set()
         for r in rows:
             for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
@@ -107,75 +109,358 @@ class ClockSampler:
                 "power_w_max": max(r["power"] for r in rows), "samples": len(rows), "reasons": sorted(reasons)}
 
 
-# ---------------------------------------------------------------------------- workload
-def make_workload(seed: int):
-    from top_hs2_fa_gb300 import workloads as W
-
-    return W.decode_bf16_workload(seed=seed)
-
-
-def algorithmic(grp):
-    from top_hs2_fa_gb300 import counting as C
-
-    m = C.decode_group_bytes(grp.kv.seq_len, HQ, HKV, D, WIN, TOPK, 2, NSA, grp.kv.max_pages)
-    return m
-
-
-# ---------------------------------------------------------------------------- reference arm
-def cpu_baseline(grp, budget_s: float = 15.0):
-    """The oracle as it stands, on the host cores, over the first sequences of the same
-    workload until ``budget_s`` of CPU work has been spent."""
-    done, elapsed = 0, 0.0
-    while elapsed < budget_s and done < B:
-        elapsed += oracle_sample_time_offset(grp, done, 1)
-        done += 1
-    return {"value": done / elapsed, "unit": "queries/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{done} of the {B} decode queries (FA + 5 SA each), numpy float64 on host cores "
-                      f"(BLAS threads = {os.cpu_count()})", "seconds": round(elapsed, 2)}
-
-
-def oracle_sample_time_offset(grp, start: int, n: int):
+def up(a, dev, bf16=False):
     import numpy as np
-    from oracle import hs2_oracle as O
-    from top_hs2_fa_gb300 import workloads as W
+    import torch
 
-    kv = grp.kv
-    sel = list(range(start, start + n))
-    sub = W.PagedKV(k=kv.k, v=kv.v, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel], dtype=kv.dtype,
-                    page=kv.page)
-    t0 = time.perf_counter()
-    _, _, idx, cnt = O.fa_decode(grp.q_fa[sel], sub, WIN, TOPK, grp.scale)
-    for j in range(NSA):
-        O.sa_decode(grp.q_sa[j][sel], sub, WIN, idx, cnt, grp.scale)
-    return time.perf_counter() - t0
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf16 else np.ascontiguousarray(a)).to(dev)
+    return t.view(torch.bfloat16) if bf16 else t
 
 
+def pinned_copies(h_in, d_in, xs, dev, as_bf16):
+    """Append pinned host buffers for inputs xs (uploaded into fresh device tensors)."""
+    import numpy as np
+    import torch
+
+    for x in xs:
+        if as_bf16:
+            h_in.append(torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory())
+        else:
+            h_in.append(torch.from_numpy(np.ascontiguousarray(x)).pin_memory())
+        d_in.append(torch.empty(h_in[-1].shape, dtype=h_in[-1].dtype, device=dev))
+
+
+# ============================================================================ scenarios
+class Decode:
+    """Decode step of one or more Cross groups: per group hs2_fa_select + 5 x hs2_sa_reuse."""
+
+    roofline_kernel, bound = "fa_decode_mma_kernel", "hbm"
+    roofline_source = ("top_hs2_fa_gb300/csrc/fa_decode.cu", "top_hs2_fa_gb300/csrc/mma_attn.cuh")
+    unit = "queries/s"
+
+    def __init__(self, name, B, t_lo, t_hi, groups, needles, qproj):
+        self.name, self.B, self.t_lo, self.t_hi, self.groups = name, B, t_lo, t_hi, groups
+        self.needles, self.qproj = needles, qproj
+        self.Hq, self.Hkv, self.D, self.w, self.k = 32, 4, 128, 128, 1024
+
+    def host_setup(self, seed):
+        import numpy as np
+        from top_hs2_fa_gb300 import workloads as W
+
+        self.host = []
+        for gi in range(self.groups):
+            s_len, s_grp = np.random.SeedSequence([seed, gi]).spawn(2)
+            lens = W.uniform_lengths(self.B, self.t_lo, self.t_hi, s_len)
+            self.host.append(W.decode_group(lens, self.Hq, self.Hkv, self.D, self.w, self.k, "bf16", s_grp,
+                                            n_sa=NSA, needles=self.needles, qproj=self.qproj))
+
+    def setup(self, dev, seed):
+        import torch
+        from top_hs2_fa_gb300 import counting as C, hs2
+
+        self.hs2 = hs2
+        self.host_setup(seed)
+        self.dev = []
+        fa, total = [], 0
+        for grp in self.host:
+            kv = grp.kv
+            d = {"kv": hs2.KV(k=up(kv.k, dev, True), v=up(kv.v, dev, True), block_table=up(kv.block_table, dev),
+                              seq_len=up(kv.seq_len, dev)),
+                 "max_t": int(kv.seq_len.max()), "q": [up(x, dev, True) for x in [grp.q_fa, *grp.q_sa]]}
+            B = self.B
+            d["o"] = [torch.empty((B, self.Hq, self.D), dtype=torch.float32, device=dev) for _ in range(1 + NSA)]
+            d["lse"] = torch.empty((B, self.Hq), dtype=torch.float32, device=dev)
+            d["idx"] = torch.empty((B, self.Hkv, self.k), dtype=torch.int32, device=dev)
+            d["cnt"] = torch.empty((B, self.Hkv), dtype=torch.int32, device=dev)
+            d["ws_fa"] = torch.empty(hs2.hs2_fa_select_workspace(B, self.Hq, d["kv"], d["max_t"], self.k),
+                                     dtype=torch.uint8, device=dev)
+            d["ws_sa"] = torch.empty(hs2.hs2_sa_reuse_workspace(B, self.Hq, d["kv"], self.w, self.k),
+                                     dtype=torch.uint8, device=dev)
+            self.dev.append(d)
+            m = C.decode_group_bytes(kv.seq_len, self.Hq, self.Hkv, self.D, self.w, self.k, 2, NSA, kv.max_pages)
+            fa.append(m["fa"])
+            total += m["total"]
+        self.alg_per_launch = fa[0]  # the profiled launch is group 0's FA scan
+        self.alg_total = total
+        self.units_per_step = self.B
+        self.launches_per_step = self.groups * (3 + NSA)
+
+    def step(self, stream, err, qs=None, profile=None):
+        hs2 = self.hs2
+        for gi, d in enumerate(self.dev):
+            q = qs[gi] if qs is not None else d["q"]
+            if profile is not None and gi == 0:
+                hs2.hs2_profile_next(hs2.STAGE_FA_SCAN, *profile)
+            hs2.hs2_fa_select(q[0], d["kv"], self.w, self.k, self.host[gi].scale, max_t=d["max_t"],
+                              out=(d["o"][0], d["lse"], d["idx"], d["cnt"]), workspace=d["ws_fa"], dev_err=err,
+                              stream=stream)
+            for j in range(NSA):
+                hs2.hs2_sa_reuse(q[1 + j], d["kv"], self.w, d["idx"], d["cnt"], self.k, self.host[gi].scale,
+                                 out=d["o"][1 + j], workspace=d["ws_sa"], dev_err=err, stream=stream)
+
+    def e2e_buffers(self, dev):
+        """Pinned host inputs (every layer's queries, table, lengths) and outputs (all layers, indices)."""
+        import torch
+
+        self.h_in, self.d_in, self.h_out, self.d_out, self.q_views = [], [], [], [], []
+        for grp, d in zip(self.host, self.dev):
+            pinned_copies(self.h_in, self.d_in, [grp.q_fa, *grp.q_sa], dev, True)
+            self.q_views.append([x.view(torch.bfloat16) for x in self.d_in[-(1 + NSA):]])
+            pinned_copies(self.h_in, self.d_in, [grp.kv.block_table, grp.kv.seq_len], dev, False)
+            self.d_in[-2:] = [d["kv"].block_table, d["kv"].seq_len]
+            for t in [*d["o"], d["idx"], d["cnt"]]:
+                self.h_out.append(torch.empty(t.shape, dtype=t.dtype).pin_memory())
+                self.d_out.append(t)
+
+    def config(self):
+        return {"workload": self.name, "batch": self.B,
+                "seq_len": f"U[{self.t_lo},{self.t_hi}]" if self.t_lo != self.t_hi else self.t_lo,
+                "groups": self.groups, "Hq": self.Hq, "Hkv": self.Hkv, "head_dim": self.D, "window": self.w,
+                "top_k": self.k, "sa_layers_per_group": NSA, "page": 64, "kv_dtype": "bf16"}
+
+    def oracle_sample(self, budget_s):
+        """Oracle FA + 5 SA per query (in every group) on the host cores, query by query."""
+        from oracle import hs2_oracle as O
+        from top_hs2_fa_gb300 import workloads as W
+
+        done, elapsed = 0, 0.0
+        while done < self.B and (done == 0 or elapsed < budget_s):
+            t0 = time.perf_counter()
+            for grp in self.host:
+                kv, sel = grp.kv, [done]
+                sub = W.PagedKV(k=kv.k, v=kv.v, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel],
+                                dtype=kv.dtype, page=kv.page)
+                _, _, idx, cnt = O.fa_decode(grp.q_fa[sel], sub, self.w, self.k, grp.scale)
+                for j in range(NSA):
+                    O.sa_decode(grp.q_sa[j][sel], sub, self.w, idx, cnt, grp.scale)
+            elapsed += time.perf_counter() - t0
+            done += 1
+        return done, elapsed, f"{done} of the {self.B} queries (FA + 5 SA in each of {self.groups} group(s))"
+
+
+class Prefill:
+    """Prefill of one sequence: hs2_fa_select (causal FA + per-row top-k) + 5 x hs2_sa_reuse."""
+
+    roofline_kernel, roofline_source, bound = "fa_prefill_fwd_kernel", "top_hs2_fa_gb300/csrc/fa_prefill.cu", "tensor"
+    unit = "tok/s"
+
+    def __init__(self, n=32768):
+        self.name = f"prefill_bf16_n{n}"
+        self.n, self.Hq, self.Hkv, self.D, self.w, self.k = n, 32, 4, 128, 128, 1024
+
+    def host_setup(self, seed):
+        from top_hs2_fa_gb300 import workloads as W
+
+        self.host = [W.prefill_group(self.n, self.Hq, self.Hkv, self.D, self.w, self.k, "bf16", seed, n_sa=NSA,
+                                     rho=0.999)]
+
+    def setup(self, dev, seed):
+        import torch
+        from top_hs2_fa_gb300 import counting as C, hs2
+
+        self.hs2 = hs2
+        self.host_setup(seed)
+        g, n = self.host[0], self.n
+        kv = g.kv
+        d = {"kv": hs2.KV(k=up(kv.k, dev, True), v=up(kv.v, dev, True), block_table=up(kv.block_table, dev),
+                          seq_len=up(kv.seq_len, dev)), "q": [up(x, dev, True) for x in [g.q_fa, *g.q_sa]]}
+        d["o"] = [torch.empty((n, self.Hq, self.D), dtype=torch.float32, device=dev) for _ in range(1 + NSA)]
+        d["lse"] = torch.empty((n, self.Hq), dtype=torch.float32, device=dev)
+        d["idx"] = torch.empty((n, self.Hkv, self.k), dtype=torch.int32, device=dev)
+        d["cnt"] = torch.empty((n, self.Hkv), dtype=torch.int32, device=dev)
+        d["ws_fa"] = torch.empty(hs2.hs2_fa_select_workspace(n, self.Hq, d["kv"], n, self.k, True), dtype=torch.uint8,
+                                 device=dev)
+        d["ws_sa"] = torch.empty(hs2.hs2_sa_reuse_workspace(n, self.Hq, d["kv"], self.w, self.k, True),
+                                 dtype=torch.uint8, device=dev)
+        self.dev = [d]
+        f = C.prefill_flops(n, self.Hq, self.D, self.w, self.k)
+        self.alg_per_launch = f["fa"]
+        self.alg_total = f["fa"] + NSA * f["sa_per_layer"]
+        self.units_per_step = n
+        self.launches_per_step = 3 + NSA
+
+    def step(self, stream, err, qs=None, profile=None):
+        hs2, d, g = self.hs2, self.dev[0], self.host[0]
+        q = qs[0] if qs is not None else d["q"]
+        if profile is not None:
+            hs2.hs2_profile_next(hs2.STAGE_FA_SCAN, *profile)
+        hs2.hs2_fa_select(q[0], d["kv"], self.w, self.k, g.scale, prefill=True,
+                          out=(d["o"][0], d["lse"], d["idx"], d["cnt"]), workspace=d["ws_fa"], dev_err=err,
+                          stream=stream)
+        for j in range(NSA):
+            hs2.hs2_sa_reuse(q[1 + j], d["kv"], self.w, d["idx"], d["cnt"], self.k, g.scale, prefill=True,
+                             out=d["o"][1 + j], workspace=d["ws_sa"], dev_err=err, stream=stream)
+
+    e2e_buffers = Decode.e2e_buffers
+    groups = 1
+
+    def config(self):
+        return {"workload": self.name, "n": self.n, "Hq": self.Hq, "Hkv": self.Hkv, "head_dim": self.D,
+                "window": self.w, "top_k": self.k, "sa_layers": NSA, "keys": "AR(1) drifting mean, rho=0.999",
+                "fa_tflop": 4.0 * self.D * self.Hq * self.n * (self.n + 1) / 2 / 1e12}
+
+    def oracle_sample(self, budget_s):
+        import numpy as np
+        from oracle import hs2_oracle as O
+
+        g = self.host[0]
+        rng = np.random.default_rng(5)
+        full_idx = np.full((self.n, self.Hkv, self.k), -1, np.int32)
+        full_cnt = np.zeros((self.n, self.Hkv), np.int32)
+        done, elapsed = 0, 0.0
+        while done < 64 and (done == 0 or elapsed < budget_s):
+            i = int(rng.integers(0, self.n))
+            t0 = time.perf_counter()
+            _, _, idx, cnt = O.fa_prefill_rows(g.q_fa, g.kv, [i], self.w, self.k, g.scale)
+            full_idx[i], full_cnt[i] = idx[0], cnt[0]
+            for j in range(NSA):
+                O.sa_prefill_rows(g.q_sa[j], g.kv, [i], self.w, full_idx, full_cnt, g.scale)
+            elapsed += time.perf_counter() - t0
+            done += 1
+        return done, elapsed, f"{done} uniformly drawn rows (FA + top-k + 5 SA each) of the n={self.n} prefill"
+
+
+class Csa2:
+    """CSA2 decode group: Full indexer -> SA, Reindex -> SA, 3 x Reuse SA (MQA, w = 0)."""
+
+    roofline_kernel, roofline_source, bound = "lightning_scan_kernel", "top_hs2_fa_gb300/csrc/indexer.cu", "hbm"
+    unit = "queries/s"
+    groups = 1
+
+    def __init__(self):
+        self.name = "csa2_decode_bf16_b8_t131072"
+        self.B, self.t, self.Hq, self.D, self.k_top, self.max_blocks = 8, 131072, 32, 128, 512, 2048
+
+    def host_setup(self, seed):
+        from top_hs2_fa_gb300 import workloads as W
+
+        self.host = [W.csa2_group([self.t] * self.B, Hq=self.Hq, d=self.D, Hi=64, di=128, k_top=self.k_top, blk=8,
+                                  max_blocks=self.max_blocks, n_reuse=3, needles=32, seed=seed)]
+
+    def setup(self, dev, seed):
+        import torch
+        from top_hs2_fa_gb300 import counting as C, hs2
+
+        self.hs2 = hs2
+        self.host_setup(seed)
+        g, B = self.host[0], self.B
+        d = {"kv": hs2.KV(k=up(g.kv.k, dev, True), v=up(g.kv.v, dev, True), block_table=up(g.kv.block_table, dev),
+                          seq_len=up(g.kv.seq_len, dev)),
+             "kidx": hs2.KV(k=up(g.kidx.k, dev, True), v=None, block_table=up(g.kidx.block_table, dev),
+                            seq_len=up(g.kidx.seq_len, dev)),
+             "qi": [up(x, dev, True) for x in g.q_idx], "wi": [up(x, dev) for x in g.w_idx],
+             "q": [up(x, dev, True) for x in g.q_main]}
+        d["o"] = [torch.empty((B, self.Hq, self.D), dtype=torch.float32, device=dev) for _ in range(5)]
+        d["pool"] = torch.empty((B, self.max_blocks), dtype=torch.int32, device=dev)
+        d["pcnt"] = torch.empty((B,), dtype=torch.int32, device=dev)
+        d["idx"] = [torch.empty((B, 1, self.k_top), dtype=torch.int32, device=dev) for _ in range(2)]
+        d["cnt"] = [torch.empty((B, 1), dtype=torch.int32, device=dev) for _ in range(2)]
+        d["ws_i"] = torch.empty(max(hs2.hs2_hier_reindex_workspace(m, 64, d["kidx"], self.t, self.k_top, 8,
+                                                                   self.max_blocks) for m in (0, 1)),
+                                dtype=torch.uint8, device=dev)
+        d["ws_sa"] = torch.empty(hs2.hs2_sa_reuse_workspace(B, self.Hq, d["kv"], 0, self.k_top), dtype=torch.uint8,
+                                 device=dev)
+        self.dev = [d]
+        m = C.csa2_decode_bytes([self.t] * B, self.D, 128, 2, self.k_top, self.max_blocks * 8, 5)
+        self.alg_per_launch = m["full"]
+        self.alg_total = m["total"]
+        self.units_per_step = B
+        self.launches_per_step = 3 + 2 + 5 * 2
+
+    def step(self, stream, err, qs=None, profile=None):
+        hs2, d, g = self.hs2, self.dev[0], self.host[0]
+        q = qs[0] if qs is not None else d["q"]
+        if profile is not None:
+            hs2.hs2_profile_next(hs2.STAGE_INDEXER, *profile)
+        for mode in (hs2.FULL, hs2.REINDEX):
+            hs2.hs2_hier_reindex(mode, d["qi"][mode], d["wi"][mode], d["kidx"], self.k_top, 8, self.max_blocks,
+                                 pool_blocks=d["pool"], pool_cnt=d["pcnt"], max_t=self.t,
+                                 out=(d["idx"][mode].view(self.B, self.k_top), d["cnt"][mode].view(self.B)),
+                                 workspace=d["ws_i"], dev_err=err, stream=stream)
+            hs2.hs2_sa_reuse(q[mode], d["kv"], 0, d["idx"][mode], d["cnt"][mode], self.k_top, g.scale,
+                             out=d["o"][mode], workspace=d["ws_sa"], dev_err=err, stream=stream)
+        for j in range(2, 5):  # Reuse layers read the Reindex layer's indices
+            hs2.hs2_sa_reuse(q[j], d["kv"], 0, d["idx"][1], d["cnt"][1], self.k_top, g.scale, out=d["o"][j],
+                             workspace=d["ws_sa"], dev_err=err, stream=stream)
+
+    def e2e_buffers(self, dev):
+        import torch
+
+        g, d = self.host[0], self.dev[0]
+        self.h_in, self.d_in, self.h_out, self.d_out = [], [], [], []
+        pinned_copies(self.h_in, self.d_in, g.q_main, dev, True)
+        self.q_views = [[x.view(torch.bfloat16) for x in self.d_in]]
+        pinned_copies(self.h_in, self.d_in, g.q_idx, dev, True)
+        self.d_in[-2:] = [t.view(torch.int16) for t in d["qi"]]
+        pinned_copies(self.h_in, self.d_in, g.w_idx, dev, False)
+        self.d_in[-2:] = d["wi"]
+        for t in [*d["o"], *d["idx"], *d["cnt"], d["pool"], d["pcnt"]]:
+            self.h_out.append(torch.empty(t.shape, dtype=t.dtype).pin_memory())
+            self.d_out.append(t)
+
+    def config(self):
+        return {"workload": self.name, "batch": self.B, "seq_len": self.t, "Hq": self.Hq, "Hkv": 1,
+                "head_dim": self.D, "indexer_heads": 64, "indexer_dim": 128, "top_k": self.k_top, "block": 8,
+                "max_blocks": self.max_blocks, "layers": "Full, Reindex, 3 x Reuse"}
+
+    def oracle_sample(self, budget_s):
+        from oracle import hs2_oracle as O
+        from top_hs2_fa_gb300 import workloads as W
+
+        g = self.host[0]
+        done, elapsed = 0, 0.0
+        while done < self.B and (done == 0 or elapsed < budget_s):
+            sel = [done]
+            sub_i = W.PagedKV(k=g.kidx.k, v=None, block_table=g.kidx.block_table[sel], seq_len=g.kidx.seq_len[sel],
+                              dtype="bf16")
+            sub = W.PagedKV(k=g.kv.k, v=g.kv.v, block_table=g.kv.block_table[sel], seq_len=g.kv.seq_len[sel],
+                            dtype="bf16")
+            t0 = time.perf_counter()
+            fi, fc, pool, pc = O.indexer_full(g.q_idx[0][sel], g.w_idx[0][sel], sub_i, self.k_top, 8, self.max_blocks)
+            ri, rc = O.indexer_reindex(g.q_idx[1][sel], g.w_idx[1][sel], sub_i, self.k_top, 8, pool, pc)
+            O.sa_decode(g.q_main[0][sel], sub, 0, fi[:, None], fc[:, None], g.scale)
+            for j in range(1, 5):
+                O.sa_decode(g.q_main[j][sel], sub, 0, ri[:, None], rc[:, None], g.scale)
+            elapsed += time.perf_counter() - t0
+            done += 1
+        return done, elapsed, f"{done} of the {self.B} queries (Full, Reindex and 5 SA layers each)"
+
+
+SCENARIOS = {
+    "decode": lambda: Decode("decode_bf16_b64_t16k-32k", 64, 16384, 32768, 1, 32, True),
+    "long_decode": lambda: Decode("long_decode_bf16_b16_t131072_x4", 16, 131072, 131072, 4, 64, False),
+    "prefill": lambda: Prefill(32768),
+    "csa2": lambda: Csa2(),
+}
+
+
+# ============================================================================ arms
 def run_reference(args, rank, world):
+    """The oracle on the host cores, on bounded samples of the selected workload."""
     if rank != 0:
         return 0
-    grp = make_workload(seed=0)
-    per_step = 2  # sequences per reference step (bounded sample of the workload)
-    for i in range(args.warmup):
-        oracle_sample_time_offset(grp, (i * per_step) % B, per_step)
-    times = []
-    for i in range(args.steps):
-        times.append(oracle_sample_time_offset(grp, ((args.warmup + i) * per_step) % B, per_step))
-    total = sum(times)
-    value = args.steps * per_step / total
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+    sc = SCENARIOS[args.workload]()
+    sc.host_setup(0)
+    for _ in range(args.warmup):
+        sc.oracle_sample(0.0)
+    tot_units, tot_s, sample = 0, 0.0, ""
+    for _ in range(args.steps):
+        u, s, sample = sc.oracle_sample(2.0)
+        tot_units += u
+        tot_s += s
+    value = tot_units / tot_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": sc.unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample_per_step": f"{per_step} of {B} queries"},
-            "cpu_baseline": {"value": value, "unit": "queries/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"{per_step} decode queries (FA + 5 SA) per step, numpy float64"},
-            "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "config": sc.config(),
+            "cpu_baseline": {"value": value, "unit": sc.unit, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"per step: {sample}; numpy float64"},
+            "e2e": {"value": value, "unit": sc.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
-# ---------------------------------------------------------------------------- GPU arm
 def run_gpu(args, rank, world, local_rank):
-    import numpy as np
     import torch
 
     from top_hs2_fa_gb300 import build as _build
@@ -188,141 +473,109 @@ def run_gpu(args, rank, world, local_rank):
         torch.distributed.barrier()
     hs2.load()
     dev = torch.device("cuda", local_rank)
-    grp = make_workload(seed=rank)
-    kv = grp.kv
-    alg = algorithmic(grp)
-
-    def up(a, bf16=False):
-        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf16 else np.ascontiguousarray(a))
-        t = t.to(dev)
-        return t.view(torch.bfloat16) if bf16 else t
-
-    dkv = hs2.KV(k=up(kv.k, True), v=up(kv.v, True), block_table=up(kv.block_table), seq_len=up(kv.seq_len))
-    max_t = int(kv.seq_len.max())
-    q_fa = up(grp.q_fa, True)
-    q_sa = [up(q, True) for q in grp.q_sa]
-    o = torch.empty((B, HQ, D), dtype=torch.float32, device=dev)
-    lse = torch.empty((B, HQ), dtype=torch.float32, device=dev)
-    idx = torch.empty((B, HKV, TOPK), dtype=torch.int32, device=dev)
-    cnt = torch.empty((B, HKV), dtype=torch.int32, device=dev)
-    o_sa = [torch.empty((B, HQ, D), dtype=torch.float32, device=dev) for _ in range(NSA)]
-    ws_fa = torch.empty(hs2.hs2_fa_select_workspace(B, HQ, dkv, max_t, TOPK), dtype=torch.uint8, device=dev)
-    ws_sa = torch.empty(hs2.hs2_sa_reuse_workspace(B, HQ, dkv, WIN, TOPK), dtype=torch.uint8, device=dev)
+    sc = SCENARIOS[args.workload]()
+    sc.setup(dev, seed=rank)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-    launches_per_step = 2 + 2 * NSA
-
-    def step(qf=q_fa, qs=q_sa, outs=None):
-        oo = outs if outs is not None else (o, lse, idx, cnt, o_sa)
-        hs2.hs2_fa_select(qf, dkv, WIN, TOPK, grp.scale, max_t=max_t, out=oo[:4], workspace=ws_fa, dev_err=err,
-                          stream=stream)
-        for j in range(NSA):
-            hs2.hs2_sa_reuse(qs[j], dkv, WIN, oo[2], oo[3], TOPK, grp.scale, out=oo[4][j], workspace=ws_sa,
-                             dev_err=err, stream=stream)
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
     for _ in range(max(3, args.warmup)):
-        step()
-    # keep the GPU busy (untimed) long enough for the clock sampler to see it under load
+        sc.step(stream, err)
     torch.cuda.synchronize()
     t_w = time.perf_counter()
-    while time.perf_counter() - t_w < args.clock_warm_s:
-        step()
+    while time.perf_counter() - t_w < args.clock_warm_s:  # untimed: lets the clock sampler see load
+        sc.step(stream, err)
         torch.cuda.synchronize()
 
-    # FA-scan events, one pair per timed step
+    # one event pair per timed step around the roofline kernel's launch
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a_, b_ in ev:
         a_.record(stream)
         b_.record(stream)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_stop = torch.cuda.Event(enable_timing=True)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    t_start.record(stream)
+    t0.record(stream)
     for i in range(args.steps):
-        hs2.hs2_profile_next(hs2.STAGE_FA_SCAN, ev[i][0], ev[i][1])
-        step()
-    t_stop.record(stream)
+        sc.step(stream, err, profile=ev[i])
+    t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    ms = t_start.elapsed_time(t_stop)
-    fa_ms = sum(a_.elapsed_time(b_) for a_, b_ in ev) / args.steps
+    ms = t0.elapsed_time(t1)
+    k_ms = sum(a_.elapsed_time(b_) for a_, b_ in ev) / args.steps
 
-    # end to end through the C ABI with host buffers: H2D of the step's queries, table and
-    # lengths from pinned memory, D2H of every layer's output and the index sets
-    h_q = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory() for x in [grp.q_fa, *grp.q_sa]]
-    h_bt = torch.from_numpy(np.ascontiguousarray(kv.block_table)).pin_memory()
-    h_sl = torch.from_numpy(np.ascontiguousarray(kv.seq_len)).pin_memory()
-    d_q = [torch.empty(x.shape, dtype=torch.int16, device=dev) for x in h_q]
-    h_out = [torch.empty((B, HQ, D), dtype=torch.float32).pin_memory() for _ in range(1 + NSA)]
-    h_idx = torch.empty((B, HKV, TOPK), dtype=torch.int32).pin_memory()
-    h_cnt = torch.empty((B, HKV), dtype=torch.int32).pin_memory()
-    h2d = sum(x.numel() * 2 for x in h_q) + h_bt.numel() * 4 + h_sl.numel() * 4
-    d2h = (1 + NSA) * B * HQ * D * 4 + h_idx.numel() * 4 + h_cnt.numel() * 4
+    # end to end through the C ABI with host buffers: H2D of every layer's queries (and the
+    # indexer inputs, tables, lengths) from pinned memory, D2H of every output and index set
+    sc.e2e_buffers(dev)
+    h2d = sum(x.numel() * x.element_size() for x in sc.h_in)
+    d2h = sum(x.numel() * x.element_size() for x in sc.h_out)
 
     def e2e_step():
-        for hq, dq in zip(h_q, d_q):
-            dq.copy_(hq, non_blocking=True)
-        dkv.block_table.copy_(h_bt, non_blocking=True)
-        dkv.seq_len.copy_(h_sl, non_blocking=True)
-        qs = [x.view(torch.bfloat16) for x in d_q]
-        step(qs[0], qs[1:])
-        h_out[0].copy_(o, non_blocking=True)
-        for j in range(NSA):
-            h_out[1 + j].copy_(o_sa[j], non_blocking=True)
-        h_idx.copy_(idx, non_blocking=True)
-        h_cnt.copy_(cnt, non_blocking=True)
+        for h, d in zip(sc.h_in, sc.d_in):
+            d.copy_(h, non_blocking=True)
+        sc.step(stream, err, qs=sc.q_views)
+        for h, d in zip(sc.h_out, sc.d_out):
+            h.copy_(d, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_stop = torch.cuda.Event(enable_timing=True)
-    e_start.record(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
     for _ in range(args.steps):
         e2e_step()
-    e_stop.record(stream)
+    e1.record(stream)
     torch.cuda.synchronize()
-    e_ms = e_start.elapsed_time(e_stop)
+    e_ms = e0.elapsed_time(e1)
     clocks = sampler.stop() if sampler else None
     bad = int(err.item())
 
     if world > 1:
-        tt = torch.tensor([ms, e_ms, fa_ms], device=dev)
+        tt = torch.tensor([ms, e_ms, k_ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms, e_ms, fa_ms = [float(x) for x in tt.tolist()]
+        ms, e_ms, k_ms = [float(x) for x in tt.tolist()]
     if rank != 0:
         return 0
-    hbm, tflops, src = peaks()
+    pk = peaks()
     per_step_s = ms / 1e3 / args.steps
-    value = world * B / per_step_s
-    fa_bytes = alg["fa"]
-    achieved = fa_bytes / (fa_ms / 1e3) / 1e9
-    traffic = recorded_traffic()
+    value = world * sc.units_per_step / per_step_s
+    cfg = sc.config()
+    cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single"
+    if sc.bound == "hbm":
+        achieved = sc.alg_per_launch / (k_ms / 1e3) / 1e9
+        peak, unit, psrc = pk["hbm"], "GB/s", f"hbm_gbs ({pk['src']})"
+        traffic = recorded_traffic(sc.name, sc.roofline_kernel, sc.roofline_source)
+        cfg["l2"] = "inputs larger than L2 (%.2f GB read by the roofline kernel per step)" % (sc.alg_per_launch / 1e9)
+        cfg["hbm_gbs_step"] = world * sc.alg_total / per_step_s / 1e9
+        cfg["algorithmic_bytes_per_step"] = sc.alg_total
+    else:
+        achieved = sc.alg_per_launch / (k_ms / 1e3) / 1e12
+        peak, unit = pk["bf16_sustained"], "TFLOP/s"
+        psrc = f"bf16_tflops_sustained ({pk['src']}; kernel timed inside a long step)"
+        traffic = None
+        cfg["l2"] = "sequence K/V (64 MB) L2-resident by design; queries and outputs larger than L2"
+        cfg["algorithmic_tflop_per_step"] = sc.alg_total / 1e12
+        cfg["tflops_step"] = world * sc.alg_total / per_step_s / 1e12
     line = {
-        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": sc.unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": B, "seq_len": f"U[{T_LO},{T_HI}]", "Hq": HQ, "Hkv": HKV,
-                   "head_dim": D, "window": WIN, "top_k": TOPK, "sa_layers": NSA, "page": 64,
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (%.2f GB of K/V read per step)" % (fa_bytes / 1e9),
-                   "hbm_gbs_step": alg["total"] / per_step_s / 1e9 * world,
-                   "algorithmic_bytes_per_step": alg["total"]},
-        "roofline": {"bound": "hbm", "kernel": FA_KERNEL, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic, "peak_source": f"hbm_gbs ({src})",
-                     "algorithmic_bytes_per_launch": fa_bytes, "launch_ms": fa_ms},
-        "e2e": {"value": world * B / (e_ms / 1e3 / args.steps), "unit": "queries/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": sc.bound, "kernel": sc.roofline_kernel, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": psrc,
+                     "algorithmic_per_launch": sc.alg_per_launch, "launch_ms": k_ms},
+        "e2e": {"value": world * sc.units_per_step / (e_ms / 1e3 / args.steps), "unit": sc.unit,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": sc.launches_per_step * args.steps,
         "clocks": clocks,
         "device_errors": bad,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(grp)
+        u, s, sample = sc.oracle_sample(15.0)
+        line["cpu_baseline"] = {"value": u / s, "unit": sc.unit, "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{sample}; numpy float64 on the host cores (BLAS threads = "
+                                          f"{os.cpu_count()})", "seconds": round(s, 2)}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -333,6 +586,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(SCENARIOS), default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-warm-s", type=float, default=1.0,
                     help="seconds of untimed steps before timing, so the clock sampler sees load")
