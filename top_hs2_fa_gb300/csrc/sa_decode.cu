@@ -7,10 +7,12 @@
 // entries in place through the block table rather than copying them (§7.2, last
 // paragraph; "Lecture 10 · 混合架构与稀疏注意力", §5.5: a second lookup through the table).
 //
-// One CTA per (query, KV head) walks U = W(t) ++ S(t) in chunks of 64 rows. For each
-// chunk the K and V rows are gathered into shared memory with 16-byte cp.async copies
-// (double-buffered: chunk c+1 streams in while chunk c is computed); the query heads of
-// the KV head share every gathered row, which is what makes the gather worth its cost.
+// One CTA per (query, KV head) walks U = W(t) ++ S(t) in chunks of 64 rows. Every entry
+// of U is first resolved through the block table into a pool row id in shared memory
+// (one round of dependent loads per CTA); the K and V rows of each chunk are then
+// gathered into shared memory with 16-byte cp.async copies, three chunks in flight.
+// The query heads of the KV head share every gathered row, which is what makes the
+// gather worth its cost.
 // Logits: each thread keeps 2 query heads x 32 contraction elements in registers (bf16)
 // and the 4 partial sums of a row are combined with shuffles. P.V: each thread
 // accumulates 8 output elements of 2 heads over a quarter of the rows. Products are
@@ -25,7 +27,8 @@ namespace hs2 {
 namespace {
 
 constexpr int kSaThreads = 256;
-constexpr int kSaRows = 64;  // rows per chunk
+constexpr int kSaRows = 64;    // rows per chunk
+constexpr int kSaStages = 3;   // chunks in flight (cp.async ring)
 
 HS2_DEVI void cp_async16(void* smem, const void* gmem, bool valid) {
   const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
@@ -76,16 +79,16 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
   const int lim = a.w > 0 ? t - a.w : t;  // selected positions must lie in F(t)
 
   extern __shared__ float smem[];
-  uint4* kst = reinterpret_cast<uint4*>(smem);            // [2][kSaRows][CPR]
-  uint4* vst = kst + 2 * kSaRows * CPR;                   // [2][kSaRows][CPR]
-  float* p_s = reinterpret_cast<float*>(vst + 2 * kSaRows * CPR);  // [kSaRows][G] base-2 logits
+  uint4* kst = reinterpret_cast<uint4*>(smem);                     // [kSaStages][kSaRows][CPR]
+  uint4* vst = kst + kSaStages * kSaRows * CPR;                    // [kSaStages][kSaRows][CPR]
+  float* p_s = reinterpret_cast<float*>(vst + kSaStages * kSaRows * CPR);  // [kSaRows][G] base-2 logits
   uint16_t* pb_s = reinterpret_cast<uint16_t*>(p_s + kSaRows * G);  // [kSaRows][G] bf16 weights
   float* red = reinterpret_cast<float*>(smem);            // [RQ][G][D], reuses the stage buffers at the end
-  static_assert(RQ * G * D * 4 <= 4 * kSaRows * CPR * 16, "reduction buffer must fit the stage buffers");
+  static_assert(RQ * G * D * 4 <= 2 * kSaStages * kSaRows * CPR * 16, "reduction buffer must fit the stage buffers");
   float* m_s = p_s + kSaRows * G + kSaRows * G / 2;       // [G]
   float* l_s = m_s + G;                                   // [G]
   float* alpha_s = l_s + G;                               // [G]
-  long long* rowk = reinterpret_cast<long long*>(alpha_s + G + (G & 1));  // [2][kSaRows] element offsets, -1 = invalid
+  int32_t* rowid = reinterpret_cast<int32_t*>(alpha_s + G);  // [w + kcap] pool row of each U entry, -1 = invalid
 
   // ---- q in registers: heads (hp*HPT .. +HPT), contraction slice ds, elements
   //      {8*(NDS*i + ds) .. +8} for i < 4 (interleaved so lanes of a row hit distinct banks)
@@ -115,59 +118,53 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
     l_s[tid] = 0.f;
   }
 
-  const int nchunk = (nU + kSaRows - 1) / kSaRows;
-  // resolve the rows of chunk c into rowk[buf] (nullptr = invalid) and issue their copies
-  auto stage = [&](int c, int buf) {
-    if (tid < kSaRows) {
-      const int r = c * kSaRows + tid;
-      long long p = -1;
-      if (r < nU) {
-        int pos;
-        bool ok = true;
-        if (r < nW) {
-          pos = t - nW + r;
-        } else {
-          pos = sel[r - nW];
-          if (pos < 0 || pos >= lim) {
-            flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
-            ok = false;
-          }
-        }
-        if (ok) {
-          const int phys = bt[pos / kPage];
-          if (phys < 0 || phys >= a.num_pages) {
-            flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
-          } else {
-            p = (((long long)phys * a.Hkv + g) * kPage + pos % kPage) * D;
-          }
-        }
+  // resolve every entry of U through the block table once (one round of dependent loads)
+  for (int u = tid; u < nU; u += kSaThreads) {
+    int pos, rid = -1;
+    bool ok = true;
+    if (u < nW) {
+      pos = t - nW + u;
+    } else {
+      pos = sel[u - nW];
+      if (pos < 0 || pos >= lim) {
+        flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+        ok = false;
       }
-      rowk[buf * kSaRows + tid] = p;
     }
-    __syncthreads();
-    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
-    const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(a.v);
+    if (ok) {
+      const int phys = bt[pos / kPage];
+      if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+      else rid = (phys * a.Hkv + g) * kPage + pos % kPage;
+    }
+    rowid[u] = rid;
+  }
+  __syncthreads();
+  const int nchunk = (nU + kSaRows - 1) / kSaRows;
+  const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(a.v);
+  // gather the rows of chunk c into ring slot `slot` (invalid rows are zero-filled)
+  auto stage = [&](int c, int slot) {
     for (int e = tid; e < kSaRows * CPR; e += kSaThreads) {
       const int r = e / CPR, cc = e % CPR;
-      const long long p = rowk[buf * kSaRows + r];
-      const bool ok = p >= 0;
-      const long long off = ok ? p + 8 * cc : 0;
-      cp_async16(&kst[(buf * kSaRows + r) * CPR + swz(r, cc)], kb + off, ok);
-      cp_async16(&vst[(buf * kSaRows + r) * CPR + cc], vb + off, ok);
+      const int u = c * kSaRows + r;
+      const int rid = u < nU ? rowid[u] : -1;
+      const bool ok = rid >= 0;
+      const long long off = ok ? (long long)rid * D + 8 * cc : 0;
+      cp_async16(&kst[(slot * kSaRows + r) * CPR + swz(r, cc)], kb + off, ok);
+      cp_async16(&vst[(slot * kSaRows + r) * CPR + cc], vb + off, ok);
     }
-    cp_async_commit();
   };
-
-  if (nchunk > 0) stage(0, 0);
+#pragma unroll
+  for (int c = 0; c < kSaStages - 1; ++c) {
+    if (c < nchunk) stage(c, c);
+    cp_async_commit();
+  }
   for (int c = 0; c < nchunk; ++c) {
-    const int buf = c & 1;
-    if (c + 1 < nchunk) {
-      stage(c + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
+    const int buf = c % kSaStages;
+    cp_async_wait<kSaStages - 2>();
+    __syncthreads();  // chunk c landed for every thread; the slot refilled below is free
+    if (c + kSaStages - 1 < nchunk) stage(c + kSaStages - 1, (c + kSaStages - 1) % kSaStages);
+    cp_async_commit();
     const int rows = min(kSaRows, nU - c * kSaRows);
     // ---- logits of this chunk (base 2) into p_s
     for (int r0 = warp * RPW; r0 < kSaRows; r0 += RPP) {
@@ -194,7 +191,8 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
         for (int o = 1; o < NDS; o <<= 1) x[hh] += __shfl_xor_sync(0xffffffffu, x[hh], o);
       }
       if (ds == 0) {
-        const bool ok = r < rows && rowk[buf * kSaRows + r] >= 0;
+        const int u = c * kSaRows + r;
+        const bool ok = r < rows && rowid[u] >= 0;
 #pragma unroll
         for (int hh = 0; hh < HPT; ++hh) p_s[r * G + hp * HPT + hh] = ok ? x[hh] * a.scale_log2 : -INFINITY;
       }
@@ -251,8 +249,10 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
         }
       }
     }
-    __syncthreads();  // buffers of this chunk are refilled two iterations later
+    __syncthreads();  // the next iteration refills this chunk's slot only after its barrier
   }
+  cp_async_wait<0>();
+  __syncthreads();
   // ---- reduce the row residue classes and normalise
 #pragma unroll
   for (int hh = 0; hh < HPT; ++hh)
@@ -270,8 +270,8 @@ __global__ void __launch_bounds__(kSaThreads) sa_gather_kernel(const AttnArgs a)
 
 template <int D, int G>
 static cudaError_t launch_sa(const AttnArgs& a, int Bq, cudaStream_t s) {
-  const size_t sm = (size_t)4 * kSaRows * (D / 8) * 16 +
-                    (size_t)(kSaRows * G + kSaRows * G / 2 + 3 * G + 1) * 4 + 2 * kSaRows * sizeof(long long);
+  const size_t sm = (size_t)2 * kSaStages * kSaRows * (D / 8) * 16 +
+                    (size_t)(kSaRows * G + kSaRows * G / 2 + 3 * G) * 4 + (size_t)(a.w + a.kcap) * sizeof(int32_t);
   auto kern = sa_gather_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
