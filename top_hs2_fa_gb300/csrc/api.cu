@@ -93,14 +93,36 @@ FaPlan fa_plan(int Bq, int Hq, const hs2_kv* kv, int max_t) {
 }
 
 struct SaPlan {
-  int nsplit;
-  size_t off_ml, off_o, total;
+  bool stream;  // bf16 decode: persistent warp stream
+  int nsplit;   // CUDA-core path: chunks of 128 entries of W ∪ S
+  hs2::SaStreamArgs sp;
+  int grid;
+  size_t off_ml, off_o, off_arrive, total;
 };
 
-SaPlan sa_plan(int Bq, int Hq, const hs2_kv* kv, int w, int k) {
+SaPlan sa_plan(int Bq, int Hq, const hs2_kv* kv, int w, int k, int prefill) {
   SaPlan p{};
-  p.nsplit = std::max(1, cdiv((long long)w + k, 128));
+  const int G = Hq / kv->Hkv;
+  const bool bf16 = kv->dtype == HS2_BF16;
   size_t off = 0;
+  if (!prefill && hs2::sa_stream_plan(G, kv->d, bf16, w, k, Bq, kv->Hkv, &p.sp, &p.grid)) {
+    p.stream = true;
+    const size_t slots = (size_t)Bq * kv->Hkv * p.sp.maxc * G;
+    p.off_ml = off;
+    off = align256(off + slots * sizeof(float) * 2);
+    p.off_o = off;
+    off = align256(off + slots * kv->d * sizeof(float));
+    p.off_arrive = off;
+    off = align256(off + (size_t)Bq * kv->Hkv * sizeof(int32_t));
+    p.total = off;
+    return p;
+  }
+  if (hs2::sa_mma_supported(G, kv->d, bf16, w, k)) {  // no partials
+    p.nsplit = 1;
+    p.total = 256;
+    return p;
+  }
+  p.nsplit = std::max(1, cdiv((long long)w + k, 128));
   p.off_ml = off;
   off = align256(off + (size_t)Bq * Hq * p.nsplit * sizeof(float) * 2);
   p.off_o = off;
@@ -405,9 +427,8 @@ hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, in
 }
 
 size_t hs2_sa_reuse_workspace(int B_or_n, int Hq, const hs2_kv* kv, int w, int k, int prefill) {
-  (void)prefill;
   if (!kv || kv->Hkv < 1 || Hq < 1 || B_or_n < 0 || w < 0 || k < 0 || (kv->d != 64 && kv->d != 128)) return 0;
-  return sa_plan(B_or_n, Hq, kv, w, k).total;
+  return sa_plan(B_or_n, Hq, kv, w, k, prefill).total;
 }
 
 hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int w, const int32_t* idx,
@@ -417,7 +438,7 @@ hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int
   if (st != HS2_OK) return st;
   if (w < 0 || k < 0 || !std::isfinite(scale) || !o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
   if (B_or_n == 0) return HS2_OK;
-  const SaPlan p = sa_plan(B_or_n, Hq, kv, w, k);
+  const SaPlan p = sa_plan(B_or_n, Hq, kv, w, k, prefill);
   if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   char* ws = (char*)workspace;
@@ -449,15 +470,19 @@ hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int
   a.logits = nullptr;
   a.out_o = o;
   a.dev_err = dev_err;
-  if (prefill && hs2::sa_mma_supported(a.G, a.D, kv->dtype == HS2_BF16, w, k)) {
-    // prefill rows: per-row gathered Q.K and P.V are dense contractions -> tensor cores
-    cudaError_t e = profiled(HS2_STAGE_SA_GATHER, s, [&] { return hs2::launch_sa_mma(a, B_or_n, s); });
+  if (p.stream) {
+    // bf16 decode: one persistent warp stream over all (query, KV head) pairs' entries
+    a.arrive = (int32_t*)(ws + p.off_arrive);
+    cudaError_t e = cudaMemsetAsync(a.arrive, 0, (size_t)B_or_n * kv->Hkv * sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = profiled(HS2_STAGE_SA_GATHER, s, [&] { return hs2::launch_sa_stream(a, p.sp, p.grid, s); });
     if (e != cudaSuccess) return cuda_fail(e);
     return HS2_OK;
   }
-  if (hs2::sa_gather_supported(a.G, a.D, kv->dtype == HS2_BF16)) {
-    // one CTA per (query, KV head) stages W ∪ S through shared memory; no partials
-    cudaError_t e = profiled(HS2_STAGE_SA_GATHER, s, [&] { return hs2::launch_sa_gather(a, B_or_n, s); });
+  if (hs2::sa_mma_supported(a.G, a.D, kv->dtype == HS2_BF16, w, k)) {
+    // bf16: per-row gathered Q.K and P.V over the heads sharing a KV head are small dense
+    // contractions -> mma.sync; decode splits each row over a thread-block cluster
+    cudaError_t e = profiled(HS2_STAGE_SA_GATHER, s, [&] { return hs2::launch_sa_mma(a, B_or_n, s); });
     if (e != cudaSuccess) return cuda_fail(e);
     return HS2_OK;
   }

@@ -33,8 +33,16 @@ struct AttnArgs {
   float* part_o;    // [Bq][Hq][nsplit][D]
   float* logits;    // [Bq][Hq][ld_logits] base-2 logits, or null
   float* out_o;     // [Bq][Hq][D] final output (kernels that normalise in place)
+  int32_t* arrive;  // [Bq][Hkv] split arrival counters, zero at launch (SA staged, nsplit > 1)
   long long ld_logits;
   int32_t* dev_err;
+};
+
+// Decode SA stream: `total` = pairs * ms steps of 16 entries cut into nwarps equal ranges;
+// partials hold up to maxc warps per (row, KV head) pair.
+struct SaStreamArgs {
+  int nwarps, ms, maxc;
+  long long total;
 };
 
 struct CombineArgs {
@@ -135,8 +143,11 @@ struct SelectArgs {
 cudaError_t launch_fa_decode_mma(const AttnArgs& a, int Bq, cudaStream_t s);
 cudaError_t launch_attn_partial(const AttnArgs& a, int Bq, int bf16, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s);
-bool sa_gather_supported(int G, int D, int bf16);
 bool sa_mma_supported(int G, int D, int bf16, int w, int k);
+// Decode: plan the warp stream on the current device (false if it does not apply);
+// a.part_ml / a.part_o hold [pairs][maxc][G] partials and a.arrive [pairs] zeroed counters.
+bool sa_stream_plan(int G, int D, int bf16, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid);
+cudaError_t launch_sa_stream(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s);
 cudaError_t launch_sa_mma(const AttnArgs& a, int Bq, cudaStream_t s);
 size_t lightning_scan_smem();
 cudaError_t launch_lightning_scan(const CUtensorMap& tm_k, const CUtensorMap& tm_q, const IdxArgs& a, int B,
@@ -148,6 +159,5 @@ size_t prefill_scan_smem();
 cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, const PsArgs& a, cudaStream_t s);
 cudaError_t launch_fa_prefill_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PfArgs& a,
                                   cudaStream_t s);
-cudaError_t launch_sa_gather(const AttnArgs& a, int Bq, cudaStream_t s);
 
 }  // namespace hs2

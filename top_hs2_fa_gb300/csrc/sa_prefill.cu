@@ -6,38 +6,59 @@
 // dense contractions over the row's |W ∪ S| keys and the query heads sharing a KV head,
 // so they run on mma.sync (keys as M, heads as N; see mma_attn.cuh).
 //
-// One CTA (4 warps) per (row, KV head). The CTA first resolves the row's positions —
-// window then selected — through the block table into pool row ids in shared memory
-// (one round of dependent loads for the whole row), then each warp walks 16-key steps
+// One CTA (4 warps) per (row, KV head, split). The CTA first resolves its share of the
+// row's positions — window then selected — through the block table into pool row ids in
+// shared memory (one round of dependent loads), then each warp walks 16-key steps
 // (steps w, w+4, ...), loading K and V rows straight into MMA fragments with 128-bit
 // loads, and the four warps' online-softmax states are merged at the end.
+//
+// Decode has one row per sequence, so (row, KV head) pairs alone leave most SMs of the
+// GPU with one or two CTAs. There the row's |W ∪ S| entries are split across the CTAs of
+// a thread-block cluster (grid z = cluster z = split count); each CTA merges its warps,
+// and CTA rank 0 merges the cluster's partial states through distributed shared memory.
+#include <cooperative_groups.h>
+
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "mma_attn.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace hs2 {
+
+constexpr int kSaMaxSplit = 8;  // portable cluster size
 
 template <int D, int NT>
 __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
   using Attn = MmaAttn<D, NT>;
   constexpr int KC = Attn::KC, VC = Attn::VC;
   const int qi = blockIdx.y, g = blockIdx.x;
+  const int split = blockIdx.z, nsplit = gridDim.z;  // cluster rank and size along z
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int G = a.G;
   const QueryGeom qg = query_geom(qi, a.prefill, a.seq_len);
   const int t = qg.t;
   float* out = a.out_o + ((size_t)qi * a.Hq + (size_t)g * G) * D;
+  // every CTA of a cluster shares (qi, g), so all of them take this exit or none does
   if (t < 1 || t > a.max_t || (t + kPage - 1) / kPage > a.max_pages) {
-    if (tid == 0) flag_error(a.dev_err, HS2_DEV_BAD_LENGTH);
-    for (int e = tid; e < G * D; e += 128) out[e] = 0.f;
+    if (split == 0) {
+      if (tid == 0) flag_error(a.dev_err, HS2_DEV_BAD_LENGTH);
+      for (int e = tid; e < G * D; e += 128) out[e] = 0.f;
+    }
     return;
   }
   const int nW = min(a.w, t);
   const int c0 = a.cnt[(size_t)qi * a.Hkv + g];
-  if (tid == 0 && (c0 < 0 || c0 > a.kcap)) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+  if (tid == 0 && split == 0 && (c0 < 0 || c0 > a.kcap)) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
   const int nS = max(0, min(a.kcap, c0));
-  const int nU = nW + nS;
+  const int nUall = nW + nS;
+  // this CTA's share: whole 16-entry steps [st0, st1) of W ∪ S
+  const int nst_all = (nUall + 15) / 16;
+  const int st0 = (int)((long long)nst_all * split / nsplit), st1 = (int)((long long)nst_all * (split + 1) / nsplit);
+  const int u_lo = st0 * 16, nU = min(nUall, st1 * 16) - u_lo;  // entries u_lo .. u_lo + nU - 1
   const int32_t* sel = a.idx + ((size_t)qi * a.Hkv + g) * a.kcap;
   const int32_t* bt = a.bt + (size_t)qg.b * a.max_pages;
   const int lim = a.w > 0 ? t - a.w : t;
@@ -46,9 +67,13 @@ __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
   float* sm_m = smem;                  // [4][NT*8]
   float* sm_l = sm_m + 4 * NT * 8;     // [4][NT*8]
   float* sm_o = sm_l + 4 * NT * 8;     // [4][NT*8][D]
-  int32_t* rowid = reinterpret_cast<int32_t*>(sm_o + 4 * NT * 8 * D);  // [nU] pool row, -1 invalid
+  float* cta_m = sm_o + 4 * NT * 8 * D;  // [NT*8]     this CTA's merged state
+  float* cta_l = cta_m + NT * 8;         // [NT*8]
+  float* cta_o = cta_l + NT * 8;         // [NT*8][D]  (unnormalised, relative to cta_m)
+  int32_t* rowid = reinterpret_cast<int32_t*>(cta_o + NT * 8 * D);  // [nU] pool row, -1 invalid
 
-  for (int u = tid; u < nU; u += 128) {
+  for (int ul = tid; ul < nU; ul += 128) {
+    const int u = u_lo + ul;
     int pos, r = -1;
     bool ok = true;
     if (u < nW) {
@@ -65,7 +90,7 @@ __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
       if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
       else r = (phys * a.Hkv + g) * kPage + pos % kPage;
     }
-    rowid[u] = r;
+    rowid[ul] = r;
   }
   Attn at;
   at.init(reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)qi * a.Hq + (size_t)g * G) * D, G);
@@ -110,24 +135,80 @@ __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
       L += f * sm_l[w * NT * 8 + hl];
       Ov += f * sm_o[((size_t)w * NT * 8 + hl) * D + dd];
     }
-    out[e] = L > 0.f ? Ov / L : 0.f;
+    if (nsplit == 1) {
+      out[e] = L > 0.f ? Ov / L : 0.f;
+    } else {
+      cta_o[e] = Ov;
+      if (dd == 0) {
+        cta_m[hl] = M;
+        cta_l[hl] = L;
+      }
+    }
   }
+  if (nsplit == 1) return;
+  // cluster merge: rank 0 reads every CTA's (m, l, o) through distributed shared memory;
+  // the second barrier keeps the peers' shared memory alive until it has done so
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  if (split == 0) {
+    for (int e = tid; e < G * D; e += 128) {
+      const int hl = e / D;
+      float M = -INFINITY;
+      for (int r = 0; r < nsplit; ++r) M = fmaxf(M, cluster.map_shared_rank(cta_m, r)[hl]);
+      float L = 0.f, Ov = 0.f;
+      for (int r = 0; r < nsplit; ++r) {
+        const float f = exp2_rel(cluster.map_shared_rank(cta_m, r)[hl], M);
+        L += f * cluster.map_shared_rank(cta_l, r)[hl];
+        Ov += f * cluster.map_shared_rank(cta_o, r)[e];
+      }
+      out[e] = L > 0.f ? Ov / L : 0.f;
+    }
+  }
+  cluster.sync();
+}
+
+static long long sa_mma_smem(int NT, int D, long long w, long long k) {
+  return (64LL * NT + 32LL * NT * D + 16LL * NT + 8LL * NT * D) * 4 + (w + k) * 4;
 }
 
 template <int D, int NT>
 static cudaError_t launch_sa_mma_t(const AttnArgs& a, int Bq, cudaStream_t s) {
-  const size_t sm = (size_t)(64 * NT + 32 * NT * D) * sizeof(float) + (size_t)(a.w + a.kcap) * sizeof(int32_t);
+  const size_t sm = (size_t)sa_mma_smem(NT, D, a.w, a.kcap);
   auto kern = sa_mma_kernel<D, NT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(a.Hkv, Bq), 128, sm, s>>>(a);
-  return cudaGetLastError();
+  // split each (row, KV head) over a cluster when the pairs alone cannot fill the GPU
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, sm)) != cudaSuccess) return e;
+  const long long pairs = (long long)a.Hkv * Bq, slots = (long long)sms * std::max(per_sm, 1);
+  const int max_steps = (a.w + a.kcap + 15) / 16;
+  int nsplit = 1;
+  if (pairs < slots) nsplit = (int)std::min<long long>(kSaMaxSplit, (slots + pairs - 1) / pairs);
+  nsplit = std::max(1, std::min(nsplit, max_steps / 4));  // at least ~4 steps of 16 per CTA
+  if (nsplit == 1) {
+    kern<<<dim3(a.Hkv, Bq), 128, sm, s>>>(a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hkv, Bq, nsplit);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = nsplit;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 bool sa_mma_supported(int G, int D, int bf16, int w, int k) {
   if (!bf16 || (D != 64 && D != 128) || G > 32 || (G > 8 && G != 16 && G != 32)) return false;
-  const long long NT = (G + 7) / 8;
-  return (64 * NT + 32 * NT * D) * 4 + ((long long)w + k) * 4 <= 227LL * 1024;
+  return sa_mma_smem((G + 7) / 8, D, w, k) <= 227LL * 1024;
 }
 
 cudaError_t launch_sa_mma(const AttnArgs& a, int Bq, cudaStream_t s) {

@@ -1,0 +1,369 @@
+// sa_stream.cu — SA gather-attention (bf16) for decode as a persistent, warp-granular stream.
+//
+// Each SA query attends to its forced recent window and to the positions its group's FA
+// layer selected, under one softmax, reading the group's shared KV in place through the
+// paged block table ("HySparse2：整体架构、KV 生命周期与 PD 分离", §5 (Cross group), §7.2
+// (SA reads window plus top-k), §7.4 (reuse of the FA layer's KV and indices)).
+//
+// Decode has one query row per sequence, so there are few (row, KV head) pairs and each
+// covers |W ∪ S| = w + k entries. Here every pair's entries are cut into 16-entry steps
+// (ms steps per pair, empty steps where a pair has fewer entries), the steps of all pairs
+// are laid end to end, and each warp of a grid sized to fill the GPU takes one contiguous,
+// equal range of them. A warp
+//   1. resolves every entry of its range (window positions directly, selected positions
+//      through the index array, then through the block table) into pool row ids in its
+//      own shared memory, lane-parallel, in three rounds of independent loads;
+//   2. streams its steps through a ring of kStrStages slots: cp.async copies of the 16 K
+//      rows and 16 V rows (whole 256-byte rows, zero rows for invalid entries) into the
+//      128-byte swizzle layout while it computes an earlier step (staged_attn.cuh:
+//      ldmatrix fragments, S^T = K.Q^T and O^T += V^T.P^T on mma.sync, one online
+//      softmax over all of a pair's entries), without any CTA-wide barrier;
+//   3. at the end of each pair in its range, writes the pair's output directly when it
+//      covered the whole pair, otherwise writes a partial (m, l, o) and arrives on the
+//      pair's counter; the last warp to arrive merges the partials and resets the counter.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "staged_attn.cuh"
+
+namespace hs2 {
+
+constexpr int kStrStages = 2;     // ring slots per warp
+constexpr int kStrMaxSteps = 32;  // steps per warp (row-id capacity 512 entries)
+
+template <int D>
+constexpr uint32_t str_slot_bytes() {  // 16 K rows and 16 V rows
+  return 2u * (D / 64) * 2048u;
+}
+template <int D>
+constexpr size_t str_warp_bytes() {  // ring + row ids + step table
+  return (size_t)kStrStages * str_slot_bytes<D>() + (kStrMaxSteps * 16 + 6 * kStrMaxSteps) * sizeof(int32_t);
+}
+template <int D>
+constexpr size_t str_smem_bytes() {
+  return 1024 + 4 * str_warp_bytes<D>();
+}
+
+// Warp holding global step s when `total` steps are cut into `nw` equal ranges
+// [floor(total*w/nw), floor(total*(w+1)/nw)) (every range non-empty when nw <= total).
+HS2_DEVI int warp_of_step(long long s, long long total, int nw) { return (int)(((s + 1) * nw - 1) / total); }
+
+template <int D, int NT>
+__global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const SaStreamArgs sp) {
+  constexpr int HALVES = D / 64;
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  constexpr uint32_t kSlot = str_slot_bytes<D>();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int wid = blockIdx.x * 4 + warp;
+  if (wid >= sp.nwarps) return;
+  const int G = a.G, ms = sp.ms;
+  const long long total = sp.total;
+  const long long s0 = total * wid / sp.nwarps, s1 = total * (wid + 1) / sp.nwarps;
+  const int ns = (int)(s1 - s0);  // <= kStrMaxSteps (host-checked)
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t ring = base + (uint32_t)warp * kStrStages * kSlot;
+  int32_t* rowid = reinterpret_cast<int32_t*>(smem_raw + (base - raw) + 4 * (size_t)kStrStages * kSlot) +
+                   warp * (kStrMaxSteps * 16 + 6 * kStrMaxSteps);
+  int32_t* st_p = rowid + kStrMaxSteps * 16;  // step table: pair, step within the pair,
+  int32_t* st_i = st_p + kStrMaxSteps;         // t, sequence, |W|, |S|
+  int32_t* st_t = st_i + kStrMaxSteps;
+  int32_t* st_b = st_t + kStrMaxSteps;
+  int32_t* st_nw = st_b + kStrMaxSteps;
+  int32_t* st_ns = st_nw + kStrMaxSteps;
+
+  // ---- 1a. step table: lane j < ns describes step j (32-bit from here on)
+  const int p_first = (int)(s0 / ms), i_first = (int)(s0 % ms);
+  if (lane < ns) {
+    const int ii = i_first + lane;
+    const int p = p_first + ii / ms, i = ii % ms;
+    const QueryGeom qg = query_geom(p / a.Hkv, a.prefill, a.seq_len);
+    const int c0 = __ldg(&a.cnt[p]);
+    const int t = qg.t;
+    int nW = 0, nS = 0;
+    if (t < 1 || t > a.max_t || (t + kPage - 1) / kPage > a.max_pages) {
+      if (i == 0) flag_error(a.dev_err, HS2_DEV_BAD_LENGTH);
+    } else {
+      nW = min(a.w, t);
+      if (i == 0 && (c0 < 0 || c0 > a.kcap)) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+      nS = max(0, min(a.kcap, c0));
+    }
+    st_p[lane] = p;
+    st_i[lane] = i;
+    st_t[lane] = t;
+    st_b[lane] = qg.b;
+    st_nw[lane] = nW;
+    st_ns[lane] = nS;
+  }
+  __syncwarp();
+  // ---- 1b. resolve the range's entries (lane takes entries lane, lane + 32, ...) into
+  // pool row ids: window positions directly, selected ones through the index array, then
+  // every position through the block table
+  {
+    int posv[16], aux[16];  // aux: selected-index slot, or -1 (window / none)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int e = lane + 32 * j, st = e >> 4;
+      posv[j] = -1;
+      aux[j] = -1;
+      if (st < ns) {
+        const int u = 16 * st_i[st] + (e & 15), nW = st_nw[st];
+        if (u < nW) posv[j] = st_t[st] - nW + u;
+        else if (u < nW + st_ns[st]) aux[j] = u - nW;
+      }
+    }
+    // all loads of a round are issued before any check (a flagged error is an atomic
+    // that later loads could not be moved across)
+    int selv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      selv[j] = aux[j] >= 0 ? __ldg(&a.idx[(size_t)st_p[(lane + 32 * j) >> 4] * a.kcap + aux[j]]) : 0;
+    bool bad_idx = false;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (aux[j] >= 0) {
+        const int t = st_t[(lane + 32 * j) >> 4];
+        const int lim = a.w > 0 ? t - a.w : t;
+        if (selv[j] < 0 || selv[j] >= lim) bad_idx = true;
+        else posv[j] = selv[j];
+      }
+    }
+    int physv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      physv[j] = posv[j] >= 0 ? __ldg(&a.bt[(size_t)st_b[(lane + 32 * j) >> 4] * a.max_pages + posv[j] / kPage]) : -1;
+    bool bad_page = false;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int e = lane + 32 * j, st = e >> 4;
+      if (st < ns) {
+        int r = -1;
+        if (posv[j] >= 0) {
+          if (physv[j] < 0 || physv[j] >= a.num_pages) bad_page = true;
+          else r = (physv[j] * a.Hkv + st_p[st] % a.Hkv) * kPage + posv[j] % kPage;
+        }
+        rowid[e] = r;
+      }
+    }
+    if (bad_idx) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+    if (bad_page) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+  }
+  __syncwarp();
+
+  // ---- 2. stream the steps
+  const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(a.v);
+  auto issue = [&](int j, int slot) {
+    const uint32_t dst = ring + (uint32_t)slot * kSlot;
+#pragma unroll
+    for (int m = 0; m < 16 * CPR / 32; ++m) {
+      const int c = lane + 32 * m;
+      const int r = c / CPR, cc = c % CPR;
+      const int rid = rowid[16 * j + r];
+      const size_t off = (size_t)(rid >= 0 ? rid : 0) * D + 8 * cc;
+      const uint32_t so = (uint32_t)(cc >> 3) * 2048u + sw128(r, cc & 7);
+      cp_async16(dst + so, kb + off, rid >= 0);
+      cp_async16(dst + HALVES * 2048u + so, vb + off, rid >= 0);
+    }
+  };
+#pragma unroll
+  for (int j = 0; j < kStrStages - 1; ++j) {
+    if (j < ns) issue(j, j);
+    cp_async_commit();
+  }
+  StagedAttn<D, NT> at;
+  int cur_p = -1;
+  for (int j = 0; j < ns; ++j) {
+    if (j + kStrStages - 1 < ns) issue(j + kStrStages - 1, (j + kStrStages - 1) % kStrStages);
+    cp_async_commit();
+    cp_async_wait<kStrStages - 1>();
+    __syncwarp();
+    const int p = st_p[j], i = st_i[j];
+    if (p != cur_p) {
+      const int qi = p / a.Hkv, g = p % a.Hkv;
+      at.init(reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)qi * a.Hq + (size_t)g * G) * D, G);
+      cur_p = p;
+    }
+    const bool okA = rowid[16 * j + gid] >= 0, okB = rowid[16 * j + gid + 8] >= 0;
+    if (__any_sync(0xffffffffu, okA || okB)) at.step(ring + (uint32_t)(j % kStrStages) * kSlot, okA, okB, a.scale_log2);
+    __syncwarp();
+    if (i != ms - 1 && j != ns - 1) continue;
+
+    // ---- 3. the pair ends in this range: write its output or a partial
+    const int qi = p / a.Hkv, g = p % a.Hkv;
+    const int first = warp_of_step((long long)p * ms, total, sp.nwarps);
+    const int last = warp_of_step((long long)(p + 1) * ms - 1, total, sp.nwarps);
+    float lsum[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hs = 0; hs < 2; ++hs) {
+        float lv = at.l[nt][hs];
+        lv += __shfl_xor_sync(0xffffffffu, lv, 4);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 8);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 16);
+        lsum[nt][hs] = lv;
+      }
+    float* out = a.out_o + ((size_t)qi * a.Hq + (size_t)g * G) * D;
+    if (first == last) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          const int hl = nt * 8 + 2 * tig + hs;
+          if (hl < G) {
+            const float inv = lsum[nt][hs] > 0.f ? 1.f / lsum[nt][hs] : 0.f;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              out[hl * D + 16 * mt + gid] = at.acc[mt][nt][hs] * inv;
+              out[hl * D + 16 * mt + gid + 8] = at.acc[mt][nt][hs + 2] * inv;
+            }
+          }
+        }
+      continue;
+    }
+    const int slotc = wid - first, nc = last - first + 1;
+    const size_t pbase = ((size_t)p * sp.maxc + slotc) * G;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hs = 0; hs < 2; ++hs) {
+        const int hl = nt * 8 + 2 * tig + hs;
+        if (hl < G) {
+          if (gid == 0) a.part_ml[pbase + hl] = make_float2(at.m[nt][hs], lsum[nt][hs]);
+          float* po = a.part_o + (pbase + hl) * D;
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            po[16 * mt + gid] = at.acc[mt][nt][hs];
+            po[16 * mt + gid + 8] = at.acc[mt][nt][hs + 2];
+          }
+        }
+      }
+    __threadfence();
+    __syncwarp();
+    int is_last = 0;
+    if (lane == 0) is_last = atomicAdd(&a.arrive[p], 1) == nc - 1;
+    is_last = __shfl_sync(0xffffffffu, is_last, 0);
+    if (!is_last) continue;
+    __threadfence();
+    // merge (nc <= 32), eight heads at a time: lane r holds partial r's (m, l) of each head;
+    // lanes then sweep the heads' D columns four at a time, weights broadcast by shuffle
+    const size_t p0 = (size_t)p * sp.maxc * G;
+    for (int hg = 0; hg < G; hg += 8) {
+      float2 mlv[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        mlv[h] = (lane < nc && hg + h < G) ? __ldcg(&a.part_ml[p0 + (size_t)lane * G + hg + h])
+                                           : make_float2(-INFINITY, 0.f);
+      float f[8], inv[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float M = warp_max(mlv[h].x);
+        f[h] = lane < nc ? exp2_rel(mlv[h].x, M) : 0.f;
+        const float L = warp_sum(f[h] * mlv[h].y);
+        inv[h] = L > 0.f ? 1.f / L : 0.f;
+      }
+      float4 o4[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) o4[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float* pob = a.part_o + (p0 + hg) * D + 4 * lane;
+#pragma unroll 2
+      for (int r = 0; r < nc; ++r) {
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const float fr = __shfl_sync(0xffffffffu, f[h], r);
+          if (hg + h < G && 4 * lane < D) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(pob + ((size_t)r * G + h) * D));
+            o4[h].x += fr * v.x;
+            o4[h].y += fr * v.y;
+            o4[h].z += fr * v.z;
+            o4[h].w += fr * v.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        if (hg + h < G && 4 * lane < D)
+          *reinterpret_cast<float4*>(out + (hg + h) * D + 4 * lane) =
+              make_float4(o4[h].x * inv[h], o4[h].y * inv[h], o4[h].z * inv[h], o4[h].w * inv[h]);
+    }
+    if (lane == 0) a.arrive[p] = 0;
+  }
+  cp_async_wait<0>();
+}
+
+template <int D, int NT>
+static bool stream_plan_t(int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
+  int dev = 0, sms = 0, per_sm = 0;
+  const size_t sm = str_smem_bytes<D>();
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaFuncSetAttribute(sa_stream_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sa_stream_kernel<D, NT>, 128, sm) != cudaSuccess || per_sm < 1) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  const int ms = (w + k + 15) / 16;
+  const long long total = (long long)Bq * Hkv * ms;
+  if (total < 1) return false;
+  const long long resident = 4LL * sms * per_sm;  // every warp of the grid resident at once
+  long long nw = std::min(resident, total);
+  long long per = total / nw;  // >= 1; ranges hold per or per + 1 steps
+  // at most 32 warps share a pair (the merge holds one partial per lane)
+  const long long per_min = (ms + 30) / 31;
+  if (per < per_min) {
+    per = per_min;
+    nw = std::max(1LL, total / per);
+    per = total / nw;
+  }
+  if ((total + nw - 1) / nw > kStrMaxSteps) return false;
+  sp->nwarps = (int)nw;
+  sp->ms = ms;
+  sp->total = total;
+  sp->maxc = (int)((ms + per - 1) / per + 1);
+  *grid = (int)((nw + 3) / 4);
+  return true;
+}
+
+bool sa_stream_plan(int G, int D, int bf16, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
+  if (!bf16 || (D != 64 && D != 128) || G < 1 || G > 32 || (G > 8 && G != 16 && G != 32)) return false;
+  const int NT = (G + 7) / 8;
+  if (D == 128)
+    return NT == 1 ? stream_plan_t<128, 1>(w, k, Bq, Hkv, sp, grid)
+           : NT == 2 ? stream_plan_t<128, 2>(w, k, Bq, Hkv, sp, grid)
+                     : stream_plan_t<128, 4>(w, k, Bq, Hkv, sp, grid);
+  return NT == 1 ? stream_plan_t<64, 1>(w, k, Bq, Hkv, sp, grid)
+         : NT == 2 ? stream_plan_t<64, 2>(w, k, Bq, Hkv, sp, grid)
+                   : stream_plan_t<64, 4>(w, k, Bq, Hkv, sp, grid);
+}
+
+template <int D, int NT>
+static cudaError_t launch_stream_t(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
+  const size_t sm = str_smem_bytes<D>();
+  cudaError_t e = cudaFuncSetAttribute(sa_stream_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  sa_stream_kernel<D, NT><<<grid, 128, sm, s>>>(a, sp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sa_stream(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
+  const int NTl = (a.G + 7) / 8;
+  if (a.D == 128) {
+    switch (NTl) {
+      case 1: return launch_stream_t<128, 1>(a, sp, grid, s);
+      case 2: return launch_stream_t<128, 2>(a, sp, grid, s);
+      case 4: return launch_stream_t<128, 4>(a, sp, grid, s);
+    }
+  } else if (a.D == 64) {
+    switch (NTl) {
+      case 1: return launch_stream_t<64, 1>(a, sp, grid, s);
+      case 2: return launch_stream_t<64, 2>(a, sp, grid, s);
+      case 4: return launch_stream_t<64, 4>(a, sp, grid, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+}  // namespace hs2
