@@ -107,13 +107,14 @@ SaPlan sa_plan(int Bq, int Hq, const hs2_kv* kv, int w, int k, int prefill) {
   size_t off = 0;
   if (!prefill && hs2::sa_stream_plan(G, kv->d, bf16, w, k, Bq, kv->Hkv, &p.sp, &p.grid)) {
     p.stream = true;
-    const size_t slots = (size_t)Bq * kv->Hkv * p.sp.maxc * G;
+    const size_t units = (size_t)Bq * kv->Hkv * p.sp.hg;
+    const size_t slots = units * p.sp.maxc * 8;
     p.off_ml = off;
     off = align256(off + slots * sizeof(float) * 2);
     p.off_o = off;
     off = align256(off + slots * kv->d * sizeof(float));
     p.off_arrive = off;
-    off = align256(off + (size_t)Bq * kv->Hkv * sizeof(int32_t));
+    off = align256(off + units * sizeof(int32_t));
     p.total = off;
     return p;
   }
@@ -473,7 +474,7 @@ hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int
   if (p.stream) {
     // bf16 decode: one persistent warp stream over all (query, KV head) pairs' entries
     a.arrive = (int32_t*)(ws + p.off_arrive);
-    cudaError_t e = cudaMemsetAsync(a.arrive, 0, (size_t)B_or_n * kv->Hkv * sizeof(int32_t), s);
+    cudaError_t e = cudaMemsetAsync(a.arrive, 0, (size_t)B_or_n * kv->Hkv * p.sp.hg * sizeof(int32_t), s);
     if (e != cudaSuccess) return cuda_fail(e);
     e = profiled(HS2_STAGE_SA_GATHER, s, [&] { return hs2::launch_sa_stream(a, p.sp, p.grid, s); });
     if (e != cudaSuccess) return cuda_fail(e);

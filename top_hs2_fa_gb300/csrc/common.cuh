@@ -57,6 +57,21 @@ HS2_DEVI uint4 ldg_nc_v4(const void* p) {
   return r;
 }
 
+// L2 cache policy that keeps lines (evict last): for K/V rows that the same kernel, or
+// the next SA layer of the group, reads again while other traffic streams past.
+HS2_DEVI uint64_t l2_keep_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+HS2_DEVI uint4 ldg_nc_v4_keep(const void* p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+
 HS2_DEVI void flag_error(int32_t* dev_err, int bits) {
   if (dev_err) atomicOr(dev_err, bits);
 }
@@ -98,6 +113,11 @@ HS2_DEVI void cp_async16(void* smem, const void* gmem, bool valid) {
 HS2_DEVI void cp_async16(uint32_t s, const void* gmem, bool valid) {
   const int n = valid ? 16 : 0;
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
+HS2_DEVI void cp_async16_keep(uint32_t s, const void* gmem, bool valid, uint64_t pol) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(s), "l"(gmem), "r"(n), "l"(pol)
+               : "memory");
 }
 HS2_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>

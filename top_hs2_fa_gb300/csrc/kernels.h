@@ -38,10 +38,11 @@ struct AttnArgs {
   int32_t* dev_err;
 };
 
-// Decode SA stream: `total` = pairs * ms steps of 16 entries cut into nwarps equal ranges;
-// partials hold up to maxc warps per (row, KV head) pair.
+// Decode SA stream: units = (row, KV head, group of 8 query heads), hg groups per pair;
+// `total` = units * ms steps of 16 entries cut into nwarps equal ranges; partials hold up
+// to maxc warps per unit, 8 heads each.
 struct SaStreamArgs {
-  int nwarps, ms, maxc;
+  int nwarps, hg, ms, maxc;
   long long total;
 };
 
@@ -145,7 +146,7 @@ cudaError_t launch_attn_partial(const AttnArgs& a, int Bq, int bf16, cudaStream_
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s);
 bool sa_mma_supported(int G, int D, int bf16, int w, int k);
 // Decode: plan the warp stream on the current device (false if it does not apply);
-// a.part_ml / a.part_o hold [pairs][maxc][G] partials and a.arrive [pairs] zeroed counters.
+// a.part_ml / a.part_o hold [units][maxc][8] partials and a.arrive [units] zeroed counters.
 bool sa_stream_plan(int G, int D, int bf16, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid);
 cudaError_t launch_sa_stream(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s);
 cudaError_t launch_sa_mma(const AttnArgs& a, int Bq, cudaStream_t s);

@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
     if (u < nW) {
       pos = t - nW + u;
     } else {
-      pos = sel[u - nW];
+      pos = __ldcs(&sel[u - nW]);  // read once: do not keep in L2
       if (pos < 0 || pos >= lim) {
         flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
         ok = false;
@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
 
   const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(a.v);
+  const uint64_t keep = l2_keep_policy();  // rows are re-read by other rows' CTAs
   const int nsteps = (nU + 15) / 16;
   for (int st = warp; st < nsteps; st += 4) {
     const int u0 = st * 16;
@@ -107,8 +108,8 @@ __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
     uint4 kr0[KC], kr1[KC], vr[4][VC];
 #pragma unroll
     for (int j = 0; j < KC; ++j) {
-      kr0[j] = ra >= 0 ? ldg_nc_v4(kb + (size_t)ra * D + 32 * j + 8 * tig) : make_uint4(0, 0, 0, 0);
-      kr1[j] = rb >= 0 ? ldg_nc_v4(kb + (size_t)rb * D + 32 * j + 8 * tig) : make_uint4(0, 0, 0, 0);
+      kr0[j] = ra >= 0 ? ldg_nc_v4_keep(kb + (size_t)ra * D + 32 * j + 8 * tig, keep) : make_uint4(0, 0, 0, 0);
+      kr1[j] = rb >= 0 ? ldg_nc_v4_keep(kb + (size_t)rb * D + 32 * j + 8 * tig, keep) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
       const int rv = uv < nU ? rowid[uv] : -1;
 #pragma unroll
       for (int j = 0; j < VC; ++j)
-        vr[e][j] = rv >= 0 ? ldg_nc_v4(vb + (size_t)rv * D + (D / 8) * gid + 8 * j) : make_uint4(0, 0, 0, 0);
+        vr[e][j] = rv >= 0 ? ldg_nc_v4_keep(vb + (size_t)rv * D + (D / 8) * gid + 8 * j, keep) : make_uint4(0, 0, 0, 0);
     }
     float x[NT][4];
     at.step(kr0, kr1, vr, ra >= 0, rb >= 0, a.scale_log2, x);
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
       Ov += f * sm_o[((size_t)w * NT * 8 + hl) * D + dd];
     }
     if (nsplit == 1) {
-      out[e] = L > 0.f ? Ov / L : 0.f;
+      __stcs(&out[e], L > 0.f ? Ov / L : 0.f);  // streaming store: keep L2 for the K/V rows
     } else {
       cta_o[e] = Ov;
       if (dd == 0) {

@@ -49,8 +49,9 @@ constexpr size_t str_smem_bytes() {
 // [floor(total*w/nw), floor(total*(w+1)/nw)) (every range non-empty when nw <= total).
 HS2_DEVI int warp_of_step(long long s, long long total, int nw) { return (int)(((s + 1) * nw - 1) / total); }
 
-template <int D, int NT>
+template <int D>
 __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const SaStreamArgs sp) {
+  constexpr int NT = 1;  // 8 query heads per unit
   constexpr int HALVES = D / 64;
   constexpr int CPR = D / 8;  // 16-byte chunks per row
   constexpr uint32_t kSlot = str_slot_bytes<D>();
@@ -58,7 +59,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
   const int gid = lane >> 2, tig = lane & 3;
   const int wid = blockIdx.x * 4 + warp;
   if (wid >= sp.nwarps) return;
-  const int G = a.G, ms = sp.ms;
+  const int G = a.G, HG = sp.hg, ms = sp.ms;
   const long long total = sp.total;
   const long long s0 = total * wid / sp.nwarps, s1 = total * (wid + 1) / sp.nwarps;
   const int ns = (int)(s1 - s0);  // <= kStrMaxSteps (host-checked)
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
   const uint32_t ring = base + (uint32_t)warp * kStrStages * kSlot;
   int32_t* rowid = reinterpret_cast<int32_t*>(smem_raw + (base - raw) + 4 * (size_t)kStrStages * kSlot) +
                    warp * (kStrMaxSteps * 16 + 6 * kStrMaxSteps);
-  int32_t* st_p = rowid + kStrMaxSteps * 16;  // step table: pair, step within the pair,
+  int32_t* st_p = rowid + kStrMaxSteps * 16;  // step table: unit, step within the unit,
   int32_t* st_i = st_p + kStrMaxSteps;         // t, sequence, |W|, |S|
   int32_t* st_t = st_i + kStrMaxSteps;
   int32_t* st_b = st_t + kStrMaxSteps;
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
   const int p_first = (int)(s0 / ms), i_first = (int)(s0 % ms);
   if (lane < ns) {
     const int ii = i_first + lane;
-    const int p = p_first + ii / ms, i = ii % ms;
+    const int un = p_first + ii / ms, i = ii % ms, p = un / HG;
     const QueryGeom qg = query_geom(p / a.Hkv, a.prefill, a.seq_len);
     const int c0 = __ldg(&a.cnt[p]);
     const int t = qg.t;
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
       if (i == 0 && (c0 < 0 || c0 > a.kcap)) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
       nS = max(0, min(a.kcap, c0));
     }
-    st_p[lane] = p;
+    st_p[lane] = un;
     st_i[lane] = i;
     st_t[lane] = t;
     st_b[lane] = qg.b;
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
     int selv[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      selv[j] = aux[j] >= 0 ? __ldg(&a.idx[(size_t)st_p[(lane + 32 * j) >> 4] * a.kcap + aux[j]]) : 0;
+      selv[j] = aux[j] >= 0 ? __ldg(&a.idx[(size_t)(st_p[(lane + 32 * j) >> 4] / HG) * a.kcap + aux[j]]) : 0;
     bool bad_idx = false;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
         int r = -1;
         if (posv[j] >= 0) {
           if (physv[j] < 0 || physv[j] >= a.num_pages) bad_page = true;
-          else r = (physv[j] * a.Hkv + st_p[st] % a.Hkv) * kPage + posv[j] % kPage;
+          else r = (physv[j] * a.Hkv + (st_p[st] / HG) % a.Hkv) * kPage + posv[j] % kPage;
         }
         rowid[e] = r;
       }
@@ -157,6 +158,8 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
   // ---- 2. stream the steps
   const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(a.v);
+  // the group's SA layers re-read the same rows: ask L2 to keep them
+  const uint64_t keep = l2_keep_policy();
   auto issue = [&](int j, int slot) {
     const uint32_t dst = ring + (uint32_t)slot * kSlot;
 #pragma unroll
@@ -166,8 +169,8 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
       const int rid = rowid[16 * j + r];
       const size_t off = (size_t)(rid >= 0 ? rid : 0) * D + 8 * cc;
       const uint32_t so = (uint32_t)(cc >> 3) * 2048u + sw128(r, cc & 7);
-      cp_async16(dst + so, kb + off, rid >= 0);
-      cp_async16(dst + HALVES * 2048u + so, vb + off, rid >= 0);
+      cp_async16_keep(dst + so, kb + off, rid >= 0, keep);
+      cp_async16_keep(dst + HALVES * 2048u + so, vb + off, rid >= 0, keep);
     }
   };
 #pragma unroll
@@ -175,18 +178,19 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
     if (j < ns) issue(j, j);
     cp_async_commit();
   }
-  StagedAttn<D, NT> at;
+  StagedAttn<D, 1> at;
   int cur_p = -1;
   for (int j = 0; j < ns; ++j) {
     if (j + kStrStages - 1 < ns) issue(j + kStrStages - 1, (j + kStrStages - 1) % kStrStages);
     cp_async_commit();
     cp_async_wait<kStrStages - 1>();
     __syncwarp();
-    const int p = st_p[j], i = st_i[j];
-    if (p != cur_p) {
+    const int un = st_p[j], i = st_i[j];
+    const int p = un / HG, h0 = (un % HG) * 8, Gh = min(8, G - h0);  // pair, first head, heads
+    if (un != cur_p) {
       const int qi = p / a.Hkv, g = p % a.Hkv;
-      at.init(reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)qi * a.Hq + (size_t)g * G) * D, G);
-      cur_p = p;
+      at.init(reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)qi * a.Hq + (size_t)g * G + h0) * D, Gh);
+      cur_p = un;
     }
     const bool okA = rowid[16 * j + gid] >= 0, okB = rowid[16 * j + gid + 8] >= 0;
     if (__any_sync(0xffffffffu, okA || okB)) at.step(ring + (uint32_t)(j % kStrStages) * kSlot, okA, okB, a.scale_log2);
@@ -195,8 +199,8 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
 
     // ---- 3. the pair ends in this range: write its output or a partial
     const int qi = p / a.Hkv, g = p % a.Hkv;
-    const int first = warp_of_step((long long)p * ms, total, sp.nwarps);
-    const int last = warp_of_step((long long)(p + 1) * ms - 1, total, sp.nwarps);
+    const int first = warp_of_step((long long)un * ms, total, sp.nwarps);
+    const int last = warp_of_step((long long)(un + 1) * ms - 1, total, sp.nwarps);
     float lsum[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -208,14 +212,14 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
         lv += __shfl_xor_sync(0xffffffffu, lv, 16);
         lsum[nt][hs] = lv;
       }
-    float* out = a.out_o + ((size_t)qi * a.Hq + (size_t)g * G) * D;
+    float* out = a.out_o + ((size_t)qi * a.Hq + (size_t)g * G + h0) * D;
     if (first == last) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int hs = 0; hs < 2; ++hs) {
           const int hl = nt * 8 + 2 * tig + hs;
-          if (hl < G) {
+          if (hl < Gh) {
             const float inv = lsum[nt][hs] > 0.f ? 1.f / lsum[nt][hs] : 0.f;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
@@ -227,13 +231,13 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
       continue;
     }
     const int slotc = wid - first, nc = last - first + 1;
-    const size_t pbase = ((size_t)p * sp.maxc + slotc) * G;
+    const size_t pbase = ((size_t)un * sp.maxc + slotc) * 8;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int hs = 0; hs < 2; ++hs) {
         const int hl = nt * 8 + 2 * tig + hs;
-        if (hl < G) {
+        if (hl < Gh) {
           if (gid == 0) a.part_ml[pbase + hl] = make_float2(at.m[nt][hs], lsum[nt][hs]);
           float* po = a.part_o + (pbase + hl) * D;
 #pragma unroll
@@ -246,73 +250,71 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
     __threadfence();
     __syncwarp();
     int is_last = 0;
-    if (lane == 0) is_last = atomicAdd(&a.arrive[p], 1) == nc - 1;
+    if (lane == 0) is_last = atomicAdd(&a.arrive[un], 1) == nc - 1;
     is_last = __shfl_sync(0xffffffffu, is_last, 0);
     if (!is_last) continue;
     __threadfence();
-    // merge (nc <= 32), eight heads at a time: lane r holds partial r's (m, l) of each head;
-    // lanes then sweep the heads' D columns four at a time, weights broadcast by shuffle
-    const size_t p0 = (size_t)p * sp.maxc * G;
-    for (int hg = 0; hg < G; hg += 8) {
-      float2 mlv[8];
+    // merge (nc <= 32): lane r holds partial r's (m, l) of each head; lanes then sweep the
+    // heads' D columns four at a time, weights broadcast by shuffle
+    const size_t p0 = (size_t)un * sp.maxc * 8;
+    float2 mlv[8];
 #pragma unroll
-      for (int h = 0; h < 8; ++h)
-        mlv[h] = (lane < nc && hg + h < G) ? __ldcg(&a.part_ml[p0 + (size_t)lane * G + hg + h])
-                                           : make_float2(-INFINITY, 0.f);
-      float f[8], inv[8];
+    for (int h = 0; h < 8; ++h)
+      mlv[h] = (lane < nc && h < Gh) ? __ldcg(&a.part_ml[p0 + (size_t)lane * 8 + h]) : make_float2(-INFINITY, 0.f);
+    float f[8], inv[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const float M = warp_max(mlv[h].x);
+      f[h] = lane < nc ? exp2_rel(mlv[h].x, M) : 0.f;
+      const float L = warp_sum(f[h] * mlv[h].y);
+      inv[h] = L > 0.f ? 1.f / L : 0.f;
+    }
+    float4 o4[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) o4[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* pob = a.part_o + p0 * D + 4 * lane;
+#pragma unroll 2
+    for (int r = 0; r < nc; ++r) {
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
-        const float M = warp_max(mlv[h].x);
-        f[h] = lane < nc ? exp2_rel(mlv[h].x, M) : 0.f;
-        const float L = warp_sum(f[h] * mlv[h].y);
-        inv[h] = L > 0.f ? 1.f / L : 0.f;
-      }
-      float4 o4[8];
-#pragma unroll
-      for (int h = 0; h < 8; ++h) o4[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float* pob = a.part_o + (p0 + hg) * D + 4 * lane;
-#pragma unroll 2
-      for (int r = 0; r < nc; ++r) {
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          const float fr = __shfl_sync(0xffffffffu, f[h], r);
-          if (hg + h < G && 4 * lane < D) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(pob + ((size_t)r * G + h) * D));
-            o4[h].x += fr * v.x;
-            o4[h].y += fr * v.y;
-            o4[h].z += fr * v.z;
-            o4[h].w += fr * v.w;
-          }
+        const float fr = __shfl_sync(0xffffffffu, f[h], r);
+        if (h < Gh && 4 * lane < D) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(pob + ((size_t)r * 8 + h) * D));
+          o4[h].x += fr * v.x;
+          o4[h].y += fr * v.y;
+          o4[h].z += fr * v.z;
+          o4[h].w += fr * v.w;
         }
       }
-#pragma unroll
-      for (int h = 0; h < 8; ++h)
-        if (hg + h < G && 4 * lane < D)
-          *reinterpret_cast<float4*>(out + (hg + h) * D + 4 * lane) =
-              make_float4(o4[h].x * inv[h], o4[h].y * inv[h], o4[h].z * inv[h], o4[h].w * inv[h]);
     }
-    if (lane == 0) a.arrive[p] = 0;
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+      if (h < Gh && 4 * lane < D)
+        *reinterpret_cast<float4*>(out + h * D + 4 * lane) =
+            make_float4(o4[h].x * inv[h], o4[h].y * inv[h], o4[h].z * inv[h], o4[h].w * inv[h]);
+    if (lane == 0) a.arrive[un] = 0;
   }
   cp_async_wait<0>();
 }
 
-template <int D, int NT>
-static bool stream_plan_t(int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
+template <int D>
+static bool stream_plan_t(int G, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
   int dev = 0, sms = 0, per_sm = 0;
   const size_t sm = str_smem_bytes<D>();
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaFuncSetAttribute(sa_stream_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sa_stream_kernel<D, NT>, 128, sm) != cudaSuccess || per_sm < 1) {
+      cudaFuncSetAttribute(sa_stream_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sa_stream_kernel<D>, 128, sm) != cudaSuccess || per_sm < 1) {
     (void)cudaGetLastError();
     return false;
   }
+  const int hg = (G + 7) / 8;  // units of 8 query heads per (row, KV head)
   const int ms = (w + k + 15) / 16;
-  const long long total = (long long)Bq * Hkv * ms;
+  const long long total = (long long)Bq * Hkv * hg * ms;
   if (total < 1) return false;
   const long long resident = 4LL * sms * per_sm;  // every warp of the grid resident at once
   long long nw = std::min(resident, total);
   long long per = total / nw;  // >= 1; ranges hold per or per + 1 steps
-  // at most 32 warps share a pair (the merge holds one partial per lane)
+  // at most 32 warps share a unit (the merge holds one partial per lane)
   const long long per_min = (ms + 30) / 31;
   if (per < per_min) {
     per = per_min;
@@ -321,6 +323,7 @@ static bool stream_plan_t(int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* 
   }
   if ((total + nw - 1) / nw > kStrMaxSteps) return false;
   sp->nwarps = (int)nw;
+  sp->hg = hg;
   sp->ms = ms;
   sp->total = total;
   sp->maxc = (int)((ms + per - 1) / per + 1);
@@ -329,41 +332,17 @@ static bool stream_plan_t(int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* 
 }
 
 bool sa_stream_plan(int G, int D, int bf16, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
-  if (!bf16 || (D != 64 && D != 128) || G < 1 || G > 32 || (G > 8 && G != 16 && G != 32)) return false;
-  const int NT = (G + 7) / 8;
-  if (D == 128)
-    return NT == 1 ? stream_plan_t<128, 1>(w, k, Bq, Hkv, sp, grid)
-           : NT == 2 ? stream_plan_t<128, 2>(w, k, Bq, Hkv, sp, grid)
-                     : stream_plan_t<128, 4>(w, k, Bq, Hkv, sp, grid);
-  return NT == 1 ? stream_plan_t<64, 1>(w, k, Bq, Hkv, sp, grid)
-         : NT == 2 ? stream_plan_t<64, 2>(w, k, Bq, Hkv, sp, grid)
-                   : stream_plan_t<64, 4>(w, k, Bq, Hkv, sp, grid);
-}
-
-template <int D, int NT>
-static cudaError_t launch_stream_t(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
-  const size_t sm = str_smem_bytes<D>();
-  cudaError_t e = cudaFuncSetAttribute(sa_stream_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  if (e != cudaSuccess) return e;
-  sa_stream_kernel<D, NT><<<grid, 128, sm, s>>>(a, sp);
-  return cudaGetLastError();
+  if (!bf16 || (D != 64 && D != 128) || G < 1 || G > 32) return false;
+  return D == 128 ? stream_plan_t<128>(G, w, k, Bq, Hkv, sp, grid) : stream_plan_t<64>(G, w, k, Bq, Hkv, sp, grid);
 }
 
 cudaError_t launch_sa_stream(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
-  const int NTl = (a.G + 7) / 8;
-  if (a.D == 128) {
-    switch (NTl) {
-      case 1: return launch_stream_t<128, 1>(a, sp, grid, s);
-      case 2: return launch_stream_t<128, 2>(a, sp, grid, s);
-      case 4: return launch_stream_t<128, 4>(a, sp, grid, s);
-    }
-  } else if (a.D == 64) {
-    switch (NTl) {
-      case 1: return launch_stream_t<64, 1>(a, sp, grid, s);
-      case 2: return launch_stream_t<64, 2>(a, sp, grid, s);
-      case 4: return launch_stream_t<64, 4>(a, sp, grid, s);
-    }
-  }
-  return cudaErrorInvalidValue;
+  const size_t sm = a.D == 128 ? str_smem_bytes<128>() : str_smem_bytes<64>();
+  auto kern = a.D == 128 ? sa_stream_kernel<128> : sa_stream_kernel<64>;
+  if (a.D != 128 && a.D != 64) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 128, sm, s>>>(a, sp);
+  return cudaGetLastError();
 }
 }  // namespace hs2
