@@ -460,6 +460,22 @@ def run_reference(args, rank, world):
     return 0
 
 
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of per-rank timings over all ranks (the slowest rank sets the time)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(world, units_per_step, ms_total, steps):
+    """Units per second of the whole job: every rank processes its own batch (weak scaling)."""
+    return world * units_per_step / (ms_total / 1e3 / steps)
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
 
@@ -532,15 +548,12 @@ def run_gpu(args, rank, world, local_rank):
     clocks = sampler.stop() if sampler else None
     bad = int(err.item())
 
-    if world > 1:
-        tt = torch.tensor([ms, e_ms, k_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms, e_ms, k_ms = [float(x) for x in tt.tolist()]
+    ms, e_ms, k_ms = max_over_ranks([ms, e_ms, k_ms], world, dev)
     if rank != 0:
         return 0
     pk = peaks()
     per_step_s = ms / 1e3 / args.steps
-    value = world * sc.units_per_step / per_step_s
+    value = whole_job_rate(world, sc.units_per_step, ms, args.steps)
     cfg = sc.config()
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single"
     if sc.bound == "hbm":
@@ -565,7 +578,7 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": {"bound": sc.bound, "kernel": sc.roofline_kernel, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic, "peak_source": psrc,
                      "algorithmic_per_launch": sc.alg_per_launch, "launch_ms": k_ms},
-        "e2e": {"value": world * sc.units_per_step / (e_ms / 1e3 / args.steps), "unit": sc.unit,
+        "e2e": {"value": whole_job_rate(world, sc.units_per_step, e_ms, args.steps), "unit": sc.unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": sc.launches_per_step * args.steps,
         "clocks": clocks,
