@@ -106,6 +106,19 @@ def test_decode_degenerate(H):
         check_group(H, grp)
 
 
+@pytest.mark.parametrize("lens", [[3000, 2100], [9000, 6000]])
+def test_decode_all_far_scores_tied(H, lens):
+    # identical keys: every far score is equal, so each (query, KV head) takes its first k
+    # positions; 3000 tied keys fit the one-pass select's candidate list, 9000 overflow it and
+    # take the radix passes over all keys
+    grp = W.decode_group(lens, Hq=8, Hkv=2, d=128, w=32, k=100, dtype="bf16", seed=8, n_sa=1, needles=0)
+    grp.kv.k[:] = grp.kv.k[0:1, :, 0:1, :]
+    o, idx, cnt = check_group(H, grp)
+    for b in range(len(lens)):
+        for g in range(2):
+            assert cnt[b, g] == 100 and (idx[b, g] == np.arange(100)).all()
+
+
 def test_tiny_fp32_decode(H):
     tg = W.tiny_group(seed=0)
     o, idx, cnt = check_group(H, tg.decode)

@@ -418,7 +418,6 @@ hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, in
   c.scores = (uint32_t*)(ws + p.off_scores);
   c.hist = (uint32_t*)(ws + p.off_hist);
   c.ld_logits = p.ld;
-  c.smem_keys = (int)std::min<long long>(p.ld, hs2::kMaxSmemKeys);
   c.dev_err = dev_err;
   e = cudaMemsetAsync(c.hist, 0, (size_t)B_or_n * kv->Hkv * 4096 * sizeof(uint32_t), s);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -589,7 +588,6 @@ hs2_status hs2_hier_reindex(hs2_idx_mode mode, const void* q_idx, const float* w
   sa.hist = a.hist;
   sa.out = idx;
   sa.cnt = idx_cnt;
-  sa.smem_keys = (int)std::min<long long>(p.ld_keys, hs2::kMaxSmemKeys);
   e = hs2::launch_select_rows(sa, B, s);
   if (e != cudaSuccess) return cuda_fail(e);
   if (mode == HS2_FULL) {
@@ -601,7 +599,6 @@ hs2_status hs2_hier_reindex(hs2_idx_mode mode, const void* q_idx, const float* w
     sa.hist = a.bhist;
     sa.out = pool_blocks;
     sa.cnt = pool_cnt;
-    sa.smem_keys = (int)std::min<long long>(p.ld_bkeys, hs2::kMaxSmemKeys);
     e = hs2::launch_select_rows(sa, B, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }

@@ -13,10 +13,12 @@
 //                     128-bit logit loads), writes them as uint32 keys and adds the
 //                     histogram of their top 12 bits into a per-(query, KV head) global
 //                     histogram (zeroed by the host call).
-// select_kernel       one CTA (512 threads) per (query, KV head): starts from that
-//                     histogram, refines the k-th key with two more digits over keys held
-//                     in shared memory (or in the L2-resident key scratch when the far
-//                     range is too long), and compacts the chosen positions in order.
+// select_kernel       one CTA (512 threads) per (query, KV head): from that histogram,
+//                     the digit holding the k-th key; one coalesced pass over the keys
+//                     splits them into "above the digit" (all taken) and "in the digit"
+//                     (candidates) lists in shared memory; a radix select over the
+//                     candidates alone fixes the k-th key and the ties to take; the two
+//                     sorted lists are merged into the ascending output (topk.cuh).
 #include "common.cuh"
 #include "kernels.h"
 #include "topk.cuh"
@@ -142,10 +144,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_score_kernel(const Combin
   }
 }
 
-__global__ void __launch_bounds__(kSelectThreads) select_kernel(const CombineArgs a) {
+// Shared memory of the selection kernels: A list (kcap), chosen-C list (kcap), C list.
+constexpr int kFilterCap = 4096;
+static size_t select_smem(int kcap) { return (size_t)2 * kcap * sizeof(int) + (size_t)kFilterCap * sizeof(uint2); }
+
+__global__ void __launch_bounds__(kSelectThreads, 2) select_kernel(const CombineArgs a) {
   constexpr int NT = kSelectThreads;
   const int g = blockIdx.x, qi = blockIdx.y;
-  const int tid = threadIdx.x;
   const QueryGeom qg = query_geom(qi, a.prefill, a.seq_len);
   const int t = qg.t;
   if ((t < 1) || (t > a.max_t) || ((t + kPage - 1) / kPage > a.max_pages)) return;
@@ -153,37 +158,23 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const CombineArg
   const int kk = min(a.k, nF);
   if (kk == 0 || kk >= nF) return;  // written by merge_score_kernel
   __shared__ TopkSmem<NT> sm;
-  extern __shared__ uint32_t keys_smem[];
+  extern __shared__ int fbuf[];
+  int* la = fbuf;
+  int* lsel = la + a.kcap;
+  uint2* lc = reinterpret_cast<uint2*>(lsel + a.kcap);
   const uint32_t* gkeys = a.scores + ((size_t)qi * a.Hkv + g) * a.ld_logits;
-  const bool in_smem = nF <= a.smem_keys;
-  if (in_smem) {
-    const int n4 = (nF + 3) / 4;  // the scratch row is long enough for the rounded-up tail
-    for (int i = tid; i < n4; i += NT)
-      reinterpret_cast<uint4*>(keys_smem)[i] = __ldcg(reinterpret_cast<const uint4*>(gkeys) + i);
-  }
   const uint32_t* gh = a.hist + ((size_t)qi * a.Hkv + g) * kRadixBins;
-  for (int i = tid; i < kRadixBins; i += NT) sm.hist[i] = __ldcg(gh + i);
-  __syncthreads();
-  int remaining = kk;
-  uint32_t prefix = find_digit<NT>(sm.hist, kRadixBins, remaining, sm) << 20;
-  uint32_t mask = 0xfff00000u;
   int32_t* out = a.idx + ((size_t)qi * a.Hkv + g) * a.kcap;
   auto emit = [&](int j, int i) { out[j] = i; };
-  if (in_smem) {
-    auto key = [&](int i) { return keys_smem[i]; };
-    radix_pass<NT>(nF, key, 8, 12, prefix, mask, remaining, sm);
-    radix_pass<NT>(nF, key, 0, 8, prefix, mask, remaining, sm);
-    compact_selected<NT>(nF, key, prefix, remaining, emit, sm);
-  } else {
-    auto key = [&](int i) { return __ldcg(gkeys + i); };
-    radix_pass<NT>(nF, key, 8, 12, prefix, mask, remaining, sm);
-    radix_pass<NT>(nF, key, 0, 8, prefix, mask, remaining, sm);
-    compact_selected<NT>(nF, key, prefix, remaining, emit, sm);
-  }
+  if (filter_topk<NT, 16>(gkeys, nF, kk, gh, la, a.kcap, lc, kFilterCap, lsel, emit, sm)) return;
+  // more candidates share the k-th key's top digit than the buffer holds: radix passes
+  // over all keys
+  auto key = [&](int i) { return __ldcg(gkeys + i); };
+  block_topk<NT>(nF, kk, key, emit, sm);
 }
 
 // ============================================================================ generic row top-k
-__global__ void __launch_bounds__(kSelectThreads) select_rows_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(kSelectThreads, 2) select_rows_kernel(const SelectArgs a) {
   constexpr int NT = kSelectThreads;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
@@ -213,36 +204,20 @@ __global__ void __launch_bounds__(kSelectThreads) select_rows_kernel(const Selec
     return;
   }
   __shared__ TopkSmem<NT> sm;
-  extern __shared__ uint32_t keys_smem[];
+  extern __shared__ int fbuf[];
+  int* la = fbuf;
+  int* lsel = la + a.kcap;
+  uint2* lc = reinterpret_cast<uint2*>(lsel + a.kcap);
   const uint32_t* gkeys = a.keys + (size_t)b * a.ld_keys;
-  const bool in_smem = n <= a.smem_keys;
-  if (in_smem) {
-    const int n4 = (n + 3) / 4;
-    for (int i = tid; i < n4; i += NT)
-      reinterpret_cast<uint4*>(keys_smem)[i] = __ldcg(reinterpret_cast<const uint4*>(gkeys) + i);
-  }
   const uint32_t* gh = a.hist + (size_t)b * kRadixBins;
-  for (int i = tid; i < kRadixBins; i += NT) sm.hist[i] = __ldcg(gh + i);
-  __syncthreads();
-  int remaining = kk;
-  uint32_t prefix = find_digit<NT>(sm.hist, kRadixBins, remaining, sm) << 20;
-  uint32_t mask = 0xfff00000u;
   auto emit = [&](int j, int i) { out[j] = map(i); };
-  if (in_smem) {
-    auto key = [&](int i) { return keys_smem[i]; };
-    radix_pass<NT>(n, key, 8, 12, prefix, mask, remaining, sm);
-    radix_pass<NT>(n, key, 0, 8, prefix, mask, remaining, sm);
-    compact_selected<NT>(n, key, prefix, remaining, emit, sm);
-  } else {
-    auto key = [&](int i) { return __ldcg(gkeys + i); };
-    radix_pass<NT>(n, key, 8, 12, prefix, mask, remaining, sm);
-    radix_pass<NT>(n, key, 0, 8, prefix, mask, remaining, sm);
-    compact_selected<NT>(n, key, prefix, remaining, emit, sm);
-  }
+  if (filter_topk<NT, 16>(gkeys, n, kk, gh, la, a.kcap, lc, kFilterCap, lsel, emit, sm)) return;
+  auto key = [&](int i) { return __ldcg(gkeys + i); };
+  block_topk<NT>(n, kk, key, emit, sm);
 }
 
 cudaError_t launch_select_rows(const SelectArgs& a, int B, cudaStream_t s) {
-  const size_t sm = (size_t)a.smem_keys * sizeof(uint32_t);
+  const size_t sm = select_smem(a.kcap);
   cudaError_t e = cudaFuncSetAttribute(select_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   select_rows_kernel<<<B, kSelectThreads, sm, s>>>(a);
@@ -275,7 +250,7 @@ cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s) {
   else return cudaErrorInvalidValue;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !a.select) return e;
-  const size_t sm = (size_t)a.smem_keys * sizeof(uint32_t);
+  const size_t sm = select_smem(a.kcap);
   e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   select_kernel<<<dim3(a.Hkv, Bq), kSelectThreads, sm, s>>>(a);

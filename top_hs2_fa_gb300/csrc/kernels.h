@@ -7,7 +7,6 @@
 namespace hs2 {
 
 constexpr int kCombineThreads = 512;
-constexpr int kMaxSmemKeys = 48 * 1024;  // 192 KB of uint32 keys
 
 // One attention pass over a set of rows of one group's paged KV, producing per
 // (query, head, chunk) partial softmax state (m, l in base 2; unnormalised o).
@@ -68,7 +67,6 @@ struct CombineArgs {
   uint32_t* scores;  // [Bq][Hkv][ld_logits] selection keys (scratch)
   uint32_t* hist;    // [Bq][Hkv][4096] top-digit histograms (scratch, zeroed per call)
   long long ld_logits;
-  int smem_keys;     // capacity of the shared-memory key array (elements)
   int32_t* dev_err;
 };
 
@@ -137,7 +135,6 @@ struct SelectArgs {
   const uint32_t* hist;
   int32_t* out;  // [B][kcap]
   int32_t* cnt;  // [B]
-  int smem_keys;
   int32_t* dev_err;
 };
 

@@ -184,4 +184,90 @@ __device__ void block_topk(int n, int kk, KeyFn key, EmitFn emit, TopkSmem<NT>& 
   compact_selected<NT>(n, key, prefix, remaining, emit, sm);
 }
 
+// Number of entries of the ascending array a[0..n) that are < x.
+HS2_DEVI int count_below(const int* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Exact top-kk of n keys read from global memory, given the global histogram of their top
+// 12 bits (ghist, kRadixBins bins). The row must start 16-byte aligned and be readable up to
+// n rounded up to a multiple of 4. One coalesced pass (V keys per thread per chunk, V a
+// multiple of 4) splits the keys into
+//   A: top 12 bits above the digit d that holds the kk-th key — all selected, and
+//   C: top 12 bits equal to d — the candidates,
+// both in index order in shared memory (la: cap_a ints, lc: cap_c (index, key) pairs). The
+// rank inside C is refined by radix select over C alone; the chosen part of C goes to lsel
+// (kk ints) in index order, and A and it are merged: emit(j, i) writes output slot j (ascending
+// index order) <- key index i. Returns false, having emitted nothing, when C or A exceed their
+// buffers (the caller then runs block_topk-style passes over all keys). All NT threads call.
+template <int NT, int V, typename EmitFn>
+__device__ bool filter_topk(const uint32_t* gkeys, int n, int kk, const uint32_t* ghist, int* la, int cap_a,
+                            uint2* lc, int cap_c, int* lsel, EmitFn emit, TopkSmem<NT>& sm) {
+  static_assert(V % 4 == 0 && NT * V < 65536, "chunk counts are packed in 16 bits");
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kRadixBins; i += NT) sm.hist[i] = __ldcg(ghist + i);
+  __syncthreads();
+  int remaining = kk;
+  const uint32_t d = find_digit<NT>(sm.hist, kRadixBins, remaining, sm);
+  const int nA = kk - remaining, nC = (int)sm.hist[d];
+  if (nC > cap_c || nA > cap_a) return false;  // block-uniform (shared values)
+  int baseA = 0, baseC = 0;
+  for (int c0 = 0; c0 < n; c0 += NT * V) {
+    const int i0 = c0 + tid * V;
+    uint32_t kv[V];
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q) {
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
+      if (i0 + 4 * q < n) x = __ldcg(reinterpret_cast<const uint4*>(gkeys + i0 + 4 * q));
+      kv[4 * q] = x.x;
+      kv[4 * q + 1] = x.y;
+      kv[4 * q + 2] = x.z;
+      kv[4 * q + 3] = x.w;
+    }
+    int ca = 0, cc = 0;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const bool ok = i0 + v < n;
+      const uint32_t dg = kv[v] >> 20;
+      ca += ok && dg > d;
+      cc += ok && dg == d;
+    }
+    const int mine = ca | (cc << 16);
+    const int off = block_exclusive_scan<NT>(mine, sm.warp_tot);
+    int oa = baseA + (off & 0xffff), oc = baseC + (off >> 16);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int i = i0 + v;
+      if (i < n) {
+        const uint32_t dg = kv[v] >> 20;
+        if (dg > d) la[oa++] = i;
+        else if (dg == d) lc[oc++] = make_uint2((uint32_t)i, kv[v]);
+      }
+    }
+    if (tid == NT - 1) sm.bcast[0] = off + mine;
+    __syncthreads();
+    const int tot = sm.bcast[0];
+    baseA += tot & 0xffff;
+    baseC += tot >> 16;
+    __syncthreads();
+  }
+  // refine inside C (keys share the top 12 bits d), then take its chosen part in order
+  uint32_t prefix = d << 20, mask = 0xfff00000u;
+  auto ckey = [&](int j) { return lc[j].y; };
+  radix_pass<NT>(nC, ckey, 8, 12, prefix, mask, remaining, sm);
+  radix_pass<NT>(nC, ckey, 0, 8, prefix, mask, remaining, sm);
+  compact_selected<NT>(nC, ckey, prefix, remaining, [&](int j, int i) { lsel[j] = (int)lc[i].x; }, sm);
+  const int nS = kk - nA;
+  for (int j = tid; j < nA; j += NT) emit(j + count_below(lsel, nS, la[j]), la[j]);
+  for (int j = tid; j < nS; j += NT) emit(j + count_below(la, nA, lsel[j]), lsel[j]);
+  __syncthreads();
+  return true;
+}
+
 }  // namespace hs2
