@@ -460,6 +460,25 @@ def run_reference(args, rank, world):
     return 0
 
 
+def graph_of(body, stream):
+    """Capture body() (stream-ordered library calls and copies) once as a CUDA graph; return
+    a function that replays it on `stream`."""
+    import torch
+
+    body()  # warm on the capture path: kernel attributes set, nothing allocated later
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        body()
+    torch.cuda.synchronize()
+
+    def replay():
+        with torch.cuda.stream(stream):
+            g.replay()
+
+    return replay
+
+
 def max_over_ranks(values, world, device=None):
     """Element-wise max of per-rank timings over all ranks (the slowest rank sets the time)."""
     if world <= 1:
@@ -503,24 +522,34 @@ def run_gpu(args, rank, world, local_rank):
         sc.step(stream, err)
         torch.cuda.synchronize()
 
-    # one event pair per timed step around the roofline kernel's launch
+    # the roofline kernel's launch time: eager steps, one event pair per step around it
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a_, b_ in ev:
         a_.record(stream)
         b_.record(stream)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        sc.step(stream, err, profile=ev[i])
+    torch.cuda.synchronize()
+    k_ms = sum(a_.elapsed_time(b_) for a_, b_ in ev) / args.steps
+
+    # the step itself: captured once as a CUDA graph and replayed (no per-launch gaps)
+    run_step = graph_of(lambda: sc.step(torch.cuda.current_stream(), err), stream) if args.graph \
+        else (lambda: sc.step(stream, err))
+    for _ in range(3):
+        run_step()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(args.steps):
-        sc.step(stream, err, profile=ev[i])
+        run_step()
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     ms = t0.elapsed_time(t1)
-    k_ms = sum(a_.elapsed_time(b_) for a_, b_ in ev) / args.steps
 
     # end to end through the C ABI with host buffers: H2D of every layer's queries (and the
     # indexer inputs, tables, lengths) from pinned memory, D2H of every output and index set
@@ -528,12 +557,15 @@ def run_gpu(args, rank, world, local_rank):
     h2d = sum(x.numel() * x.element_size() for x in sc.h_in)
     d2h = sum(x.numel() * x.element_size() for x in sc.h_out)
 
-    def e2e_step():
+    def e2e_body():
+        st = torch.cuda.current_stream()
         for h, d in zip(sc.h_in, sc.d_in):
             d.copy_(h, non_blocking=True)
-        sc.step(stream, err, qs=sc.q_views)
+        sc.step(st, err, qs=sc.q_views)
         for h, d in zip(sc.h_out, sc.d_out):
             h.copy_(d, non_blocking=True)
+
+    e2e_step = graph_of(e2e_body, stream) if args.graph else e2e_body
 
     for _ in range(3):
         e2e_step()
@@ -556,6 +588,7 @@ def run_gpu(args, rank, world, local_rank):
     value = whole_job_rate(world, sc.units_per_step, ms, args.steps)
     cfg = sc.config()
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single"
+    cfg["cuda_graph"] = bool(args.graph)
     if sc.bound == "hbm":
         achieved = sc.alg_per_launch / (k_ms / 1e3) / 1e9
         peak, unit, psrc = pk["hbm"], "GB/s", f"hbm_gbs ({pk['src']})"
@@ -601,6 +634,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(SCENARIOS), default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=True,
+                    help="replay each step as a captured CUDA graph (default) or launch eagerly")
     ap.add_argument("--clock-warm-s", type=float, default=1.0,
                     help="seconds of untimed steps before timing, so the clock sampler sees load")
     args = ap.parse_args()
