@@ -5,16 +5,18 @@
 // the FA builds the cache and attends over all positions). Row i sees keys [0, i].
 //
 // One CTA per (128-row query tile, query head); heaviest tiles are scheduled first.
-//   warp 0      TMA producer: Q tile once (3-D map over [n][Hq][d]); K and V tiles of
-//               128 keys (two 64-row pages each, through the block table) into a 2-stage
-//               ring, 128-byte swizzle.
+//   warps 0, 6  TMA producers: Q tile once (3-D map over [n][Hq][d]); K tiles (warp 0) and
+//               V tiles (warp 6) of 128 keys (two 64-row pages each, through the block
+//               table) into 2-slot rings, 128-byte swizzle; a K slot frees when its QK is
+//               done, a V slot when its PV is done.
 //   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers (M=128, N=128,
 //               K=128), then O += P_j V_j (A = P from shared memory, B = V MN-major);
 //               S_{j+1} is issued before waiting for P_j so the tensor core stays busy.
 //   warps 2-5   softmax, one query row per thread: row max, exp2 (base-2 logits), P in
-//               bf16 to shared memory (the normaliser sums the same rounded values), and a
-//               lazy O rescale: the reference max only moves when the row max grows by more
-//               than 2^8, which keeps every weight below 256 and needs no approximation.
+//               bf16 to one of two shared-memory buffers (the normaliser sums the same
+//               rounded values), and a lazy O rescale: the reference max only moves when
+//               the row max grows by more than 2^8, which keeps every weight below 256 and
+//               needs no approximation; only a rescale waits for the previous PV.
 // TMEM: S0 columns [0,128), S1 [128,256), O [256,384). Every mbarrier wait is bounded.
 #include <cuda.h>
 
@@ -27,7 +29,7 @@ namespace hs2 {
 namespace {
 
 constexpr int kPT = 128;           // query rows per tile = keys per KV tile
-constexpr int kPThreads = 192;     // TMA warp, MMA warp, 4 softmax warps
+constexpr int kPThreads = 224;     // TMA warps (K; Q and V), MMA warp, 4 softmax warps
 constexpr uint32_t kTileBytes = kPT * 128 * 2;  // 32 KB: 128 rows x 128 bf16
 constexpr uint32_t kTmemColsPf = 512;
 constexpr float kRescaleLog2 = 8.f;
@@ -36,8 +38,8 @@ struct PfSmem {
   uint8_t q[kTileBytes];      // A of S: K-blocks (d 0-63, d 64-127) x [128 rows x 128 B]
   uint8_t k[2][kTileBytes];   // B of S: same layout, rows = keys
   uint8_t v[2][kTileBytes];   // B of PV (MN-major): d-halves x [128 keys x 128 B]
-  uint8_t p[kTileBytes];      // A of PV: K-blocks (keys 0-63, 64-127) x [128 rows x 128 B]
-  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, o_done;
+  uint8_t p[2][kTileBytes];   // A of PV, double-buffered: K-blocks (keys 0-63, 64-127) x [128 rows x 128 B]
+  uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -70,13 +72,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (threadIdx.x == 0) {
     tc::mbar_init(&sm.q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&sm.kv_full[s], 1);
-      tc::mbar_init(&sm.kv_empty[s], 1);
+      tc::mbar_init(&sm.k_full[s], 1);
+      tc::mbar_init(&sm.k_empty[s], 1);  // QK of the slot's tile done
+      tc::mbar_init(&sm.v_full[s], 1);
+      tc::mbar_init(&sm.v_empty[s], 1);  // PV of the slot's tile done
       tc::mbar_init(&sm.s_full[s], 1);
       tc::mbar_init(&sm.s_empty[s], 128);
+      tc::mbar_init(&sm.p_full[s], 128);
+      tc::mbar_init(&sm.p_empty[s], 1);  // PV of the buffer's tile done (and every MMA before it)
     }
-    tc::mbar_init(&sm.p_full, 128);
-    tc::mbar_init(&sm.o_done, 1);
     sm.abort = 0;
     tc::fence_mbar_init();
   }
@@ -87,17 +91,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   const uint32_t tS = tmem, tO = tmem + 256;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 6) {
+    // ------------------------------------------------------------------ TMA producers
+    // warp 0: Q once, then K tiles; warp 6: V tiles. K slots free up when a tile's QK is
+    // done and V slots when its PV is done, so the K loads run ahead of the V loads.
     if (lane == 0) {
+      const bool is_k = warp == 0;
       const int32_t* bt = a.bt;
-      tc::mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
-      tc::tma_load_3d(sm.q, &tm_q, 0, h, i0, &sm.q_full);
-      tc::tma_load_3d(sm.q + kTileBytes / 2, &tm_q, 64, h, i0, &sm.q_full);
+      if (is_k) {
+        tc::mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
+        tc::tma_load_3d(sm.q, &tm_q, 0, h, i0, &sm.q_full);
+        tc::tma_load_3d(sm.q + kTileBytes / 2, &tm_q, 64, h, i0, &sm.q_full);
+      }
+      uint64_t* full = is_k ? sm.k_full : sm.v_full;
+      uint64_t* empty = is_k ? sm.k_empty : sm.v_empty;
+      const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
       int issued = 0;
       for (int j = 0; j < J && !aborted(sm); ++j) {
         const int st = j & 1;
-        if (!tc::mbar_wait(&sm.kv_empty[st], ((j >> 1) & 1) ^ 1)) {
+        if (!tc::mbar_wait(&empty[st], ((j >> 1) & 1) ^ 1)) {
           set_abort(sm, a.dev_err);
           break;
         }
@@ -109,32 +121,30 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (lp < npages) {
             const int phys = bt[lp];
             if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
-            else { rows[pg] = (phys * a.Hkv + g) * kPage; bytes += 4 * 8192; }
+            else { rows[pg] = (phys * a.Hkv + g) * kPage; bytes += 2 * 8192; }
           }
         }
-        tc::mbar_arrive_expect_tx(&sm.kv_full[st], bytes);
+        tc::mbar_arrive_expect_tx(&full[st], bytes);
+        uint8_t* dst = is_k ? sm.k[st] : sm.v[st];
         for (int pg = 0; pg < 2; ++pg) {
           if (rows[pg] < 0) continue;
-          for (int hh = 0; hh < 2; ++hh) {
-            tc::tma_load_2d(sm.k[st] + hh * 16384 + pg * 8192, &tm_k, 64 * hh, rows[pg], &sm.kv_full[st]);
-            tc::tma_load_2d(sm.v[st] + hh * 16384 + pg * 8192, &tm_v, 64 * hh, rows[pg], &sm.kv_full[st]);
-          }
+          for (int hh = 0; hh < 2; ++hh) tc::tma_load_2d(dst + hh * 16384 + pg * 8192, tm, 64 * hh, rows[pg], &full[st]);
         }
         issued = j + 1;
       }
-      for (int j = max(0, issued - 2); j < issued; ++j) (void)tc::mbar_wait(&sm.kv_full[j & 1], (j >> 1) & 1);
-      (void)tc::mbar_wait(&sm.q_full, 0);
+      for (int j = max(0, issued - 2); j < issued; ++j) (void)tc::mbar_wait(&full[j & 1], (j >> 1) & 1);
+      if (is_k) (void)tc::mbar_wait(&sm.q_full, 0);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16_f32(kPT, kPT);
       constexpr uint32_t idO = tc::idesc_bf16_f32_bmn(kPT, 128);
-      const uint32_t qb = tc::smem_u32(sm.q), pb = tc::smem_u32(sm.p);
+      const uint32_t qb = tc::smem_u32(sm.q);
       int pv_issued = 0;
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!tc::mbar_wait(&sm.kv_full[st], (j >> 1) & 1) || !tc::mbar_wait(&sm.s_empty[st], ((j >> 1) & 1) ^ 1))
+        if (!tc::mbar_wait(&sm.k_full[st], (j >> 1) & 1) || !tc::mbar_wait(&sm.s_empty[st], ((j >> 1) & 1) ^ 1))
           return false;
         tc::tc_fence_after();
         const uint32_t kb = tc::smem_u32(sm.k[st]);
@@ -144,27 +154,31 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tc::mma_bf16(tS + st * 128, tc::sdesc_sw128(qb + off), tc::sdesc_sw128(kb + off), idS, ks > 0 ? 1u : 0u);
         }
         tc::mma_commit(&sm.s_full[st]);
+        tc::mma_commit(&sm.k_empty[st]);
         return true;
       };
       bool ok = tc::mbar_wait(&sm.q_full, 0) && issue_s(0);
       for (int j = 0; ok && j < J; ++j) {
         if (j + 1 < J && !issue_s(j + 1)) { ok = false; break; }
-        if (!tc::mbar_wait(&sm.p_full, j & 1)) { ok = false; break; }
-        tc::tc_fence_after();
         const int st = j & 1;
-        const uint32_t vb = tc::smem_u32(sm.v[st]);
+        if (!tc::mbar_wait(&sm.p_full[st], (j >> 1) & 1) || !tc::mbar_wait(&sm.v_full[st], (j >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t vb = tc::smem_u32(sm.v[st]), pb = tc::smem_u32(sm.p[st]);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t ad = tc::sdesc_sw128(pb + (ks >> 2) * 16384u + (ks & 3) * 32u);
           const uint64_t bd = tc::sdesc_sw128_mn(vb + ks * 2048u, 16384u, 1024u);
           tc::mma_bf16(tO, ad, bd, idO, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        tc::mma_commit(&sm.kv_empty[st]);
-        tc::mma_commit(&sm.o_done);
+        tc::mma_commit(&sm.v_empty[st]);
+        tc::mma_commit(&sm.p_empty[st]);
         pv_issued = j + 1;
       }
       if (!ok) set_abort(sm, a.dev_err);
-      if (pv_issued > 0) (void)tc::mbar_wait(&sm.o_done, (pv_issued - 1) & 1);
+      if (pv_issued > 0) (void)tc::mbar_wait(&sm.p_empty[(pv_issued - 1) & 1], ((pv_issued - 1) >> 1) & 1);
     }
   } else {
     // ------------------------------------------------------------------ softmax warps
@@ -195,25 +209,38 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&sm.s_empty[sb]);
-      const int kbase = j * kPT;
+      // raw logits: only the diagonal tile crosses the causal boundary; the scale (> 0) is
+      // applied to the max and folded into the exponent's FMA below
+      if (j == J - 1) {
+        const int kbase = j * kPT;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (kbase + c * 32 + e > i) x[c][e] = -INFINITY;
+      }
       float mt = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int key = kbase + c * 32 + e;
-          x[c][e] = key <= i ? x[c][e] * a.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[c][e]);
-        }
-      const float m_new = fmaxf(m_used, mt);
+        for (int e = 0; e < 32; ++e) mt = fmaxf(mt, x[c][e]);
+      const float m_new = fmaxf(m_used, mt * a.scale_log2);
       const bool need = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new > -INFINITY);
       const float alpha = (need && m_used > -INFINITY) ? tc::ex2(m_used - m_new) : 1.f;
       if (need) m_used = m_new;
+      // P buffer j&1 is free once PV_{j-2} is done
+      if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(&sm.p_empty[j & 1], ((j >> 1) - 1) & 1))) {
+        ok = false;
+        break;
+      }
       if (j > 0) {
-        // P_{j-1} has been consumed and O holds every earlier tile once PV_{j-1} is done
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.o_done, (j - 1) & 1))) { ok = false; break; }
-        tc::tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          // O holds every earlier tile once PV_{j-1} is done
+          if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float ov[32];
@@ -225,24 +252,29 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         l *= alpha;
       }
-      // P row (bf16) into shared memory, 128-byte swizzled K-major layout
-      uint8_t* prow = sm.p + (r >> 3) * 1024 + (r & 7) * 128;
+      // P row (bf16) into shared memory, 128-byte swizzled K-major layout. p = 2^(x*s - m):
+      // one FMA and ex2 (which maps -inf to +0); the normaliser adds the same bf16-rounded
+      // weights through a mixed-precision FMA against bf16 1.0 (exact: no unpacking).
+      uint8_t* prow = sm.p[j & 1] + (r >> 3) * 1024 + (r & 7) * 128;
+      const float neg_m = -m_used;
+      constexpr uint32_t kOnes = 0x3F803F80u;  // bf16 1.0, 1.0
 #pragma unroll
       for (int cc = 0; cc < 16; ++cc) {
         uint32_t w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float p0 = x[cc >> 2][(cc & 3) * 8 + 2 * u] == -INFINITY ? 0.f : tc::ex2(x[cc >> 2][(cc & 3) * 8 + 2 * u] - m_used);
-          const float p1 = x[cc >> 2][(cc & 3) * 8 + 2 * u + 1] == -INFINITY ? 0.f : tc::ex2(x[cc >> 2][(cc & 3) * 8 + 2 * u + 1] - m_used);
+          const float p0 = tc::ex2(fmaf(x[cc >> 2][(cc & 3) * 8 + 2 * u], a.scale_log2, neg_m));
+          const float p1 = tc::ex2(fmaf(x[cc >> 2][(cc & 3) * 8 + 2 * u + 1], a.scale_log2, neg_m));
           w[u] = pack_bf16(p0, p1);
-          l += bf16_lo(w[u]) + bf16_hi(w[u]);
+          l = fmab_ll(w[u], kOnes, l);
+          l = fmab_hl(w[u], kOnes, l);
         }
         *reinterpret_cast<uint4*>(prow + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       tc::fence_async_smem();
-      tc::mbar_arrive(&sm.p_full);
+      tc::mbar_arrive(&sm.p_full[j & 1]);
     }
-    if (__all_sync(0xffffffffu, ok && !aborted(sm) && tc::mbar_wait(&sm.o_done, (J - 1) & 1))) {
+    if (__all_sync(0xffffffffu, ok && !aborted(sm) && tc::mbar_wait(&sm.p_empty[(J - 1) & 1], ((J - 1) >> 1) & 1))) {
       tc::tc_fence_after();
       const float linv = l > 0.f ? 1.f / l : 0.f;
       float* orow = a.o + ((size_t)i * a.Hq + h) * 128;
