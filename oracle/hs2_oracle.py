@@ -160,14 +160,33 @@ def fa_decode(q: np.ndarray, kv, w: int, k: int, scale: float, return_scores: bo
 
 
 # ----------------------------------------------------------------------------- SA layer
-def sparse_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
+def sparse_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float, sink=None) -> np.ndarray:
     """One softmax over the gathered entries (window and far positions together,
-    [HS2] §7.2 and §7.4: "一起参加同一次归一化")."""
+    [HS2] §7.2 and §7.4: "一起参加同一次归一化").
+
+    ``sink`` (one natural-log logit per query head, or None): the per-head learnable sink
+    bias of the SA layers ([HS2] §17.1) read as one more key with that logit and a zero
+    value, so it only enlarges the softmax denominator by exp(sink)."""
     x = (q @ K.T) * float(scale)
-    x = x - x.max(axis=1, keepdims=True)
-    p = np.exp(x)
-    p /= p.sum(axis=1, keepdims=True)
-    return p @ V
+    if sink is None:
+        x = x - x.max(axis=1, keepdims=True)
+        p = np.exp(x)
+        p /= p.sum(axis=1, keepdims=True)
+        return p @ V
+    b = np.asarray(sink, dtype=np.float64).reshape(-1)
+    m = np.maximum(x.max(axis=1) if x.shape[1] else np.full(x.shape[0], -np.inf), b)
+    p = np.exp(x - m[:, None])
+    den = p.sum(axis=1) + np.exp(b - m)
+    return (p @ V) / den[:, None]
+
+
+def output_gate(o: np.ndarray, gate) -> np.ndarray:
+    """The SA layers' output sigmoid gate ([HS2] §17.1), elementwise: o * sigmoid(gate);
+    ``gate`` has o's shape (a per-head gate is the same value across d), None = no gate."""
+    if gate is None:
+        return o
+    g = np.asarray(gate, dtype=np.float64)
+    return o / (1.0 + np.exp(-g))
 
 
 def _union(t: int, w: int, sel: np.ndarray) -> np.ndarray:
@@ -180,9 +199,12 @@ def _union(t: int, w: int, sel: np.ndarray) -> np.ndarray:
     return np.concatenate([win, sel])
 
 
-def sa_decode(q: np.ndarray, kv, w: int, idx: np.ndarray, cnt: np.ndarray, scale: float) -> np.ndarray:
+def sa_decode(q: np.ndarray, kv, w: int, idx: np.ndarray, cnt: np.ndarray, scale: float, sink=None,
+              gate=None) -> np.ndarray:
     """SA layer reusing the FA's KV and indices with its own query ([HS2] §5):
-    O_h = sum over U = W(t) ∪ S(t) of softmax_U(scale q_h.k) v. Returns float64 [B][Hq][d]."""
+    O_h = sum over U = W(t) ∪ S(t) of softmax_U(scale q_h.k) v. Optional sink bias [Hq] and
+    output gate logits [B][Hq][d] ([HS2] §17.1, see sparse_attention / output_gate).
+    Returns float64 [B][Hq][d]."""
     qf = to_f64(q, kv.dtype)
     B, Hq, d = qf.shape
     Hkv = kv.k.shape[1]
@@ -195,8 +217,8 @@ def sa_decode(q: np.ndarray, kv, w: int, idx: np.ndarray, cnt: np.ndarray, scale
             K = gather_rows(kv.k, kv.block_table[b], g, U, kv.page, kv.dtype)
             V = gather_rows(kv.v, kv.block_table[b], g, U, kv.page, kv.dtype)
             hs = slice(g * G, (g + 1) * G)
-            o[b, hs] = sparse_attention(qf[b, hs], K, V, scale)
-    return o
+            o[b, hs] = sparse_attention(qf[b, hs], K, V, scale, None if sink is None else np.asarray(sink)[hs])
+    return output_gate(o, None if gate is None else to_f64(gate, "f32"))
 
 
 # ----------------------------------------------------------------------------- prefill (row by row)
@@ -241,9 +263,10 @@ def fa_prefill_rows(q: np.ndarray, kv, rows, w: int, k: int, scale: float, retur
 
 
 def sa_prefill_rows(q: np.ndarray, kv, rows, w: int, idx: np.ndarray, cnt: np.ndarray,
-                    scale: float) -> np.ndarray:
+                    scale: float, sink=None, gate=None) -> np.ndarray:
     """SA prefill at the listed rows; ``idx``/``cnt`` are indexed by the row itself
-    ([n][Hkv][k] and [n][Hkv]). Returns float64 [R][Hq][d]."""
+    ([n][Hkv][k] and [n][Hkv]); optional sink [Hq] and gate logits [n][Hq][d].
+    Returns float64 [R][Hq][d]."""
     rows = np.asarray(rows, dtype=np.int64)
     qf = to_f64(q, kv.dtype)
     _, Hq, d = qf.shape
@@ -257,8 +280,8 @@ def sa_prefill_rows(q: np.ndarray, kv, rows, w: int, idx: np.ndarray, cnt: np.nd
             K = gather_rows(kv.k, kv.block_table[0], g, U, kv.page, kv.dtype)
             V = gather_rows(kv.v, kv.block_table[0], g, U, kv.page, kv.dtype)
             hs = slice(g * G, (g + 1) * G)
-            o[r, hs] = sparse_attention(qf[i, hs], K, V, scale)
-    return o
+            o[r, hs] = sparse_attention(qf[i, hs], K, V, scale, None if sink is None else np.asarray(sink)[hs])
+    return output_gate(o, None if gate is None else to_f64(np.asarray(gate)[rows], "f32"))
 
 
 # ----------------------------------------------------------------------------- CSA2 indexer

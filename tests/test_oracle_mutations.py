@@ -42,7 +42,7 @@ def _full_attn_transposed(q, K, V, scale):  # softmax over the wrong axis
     return x, lse, p @ V
 
 
-def _sparse_two_softmaxes(q, K, V, scale):  # window and far positions normalised apart
+def _sparse_two_softmaxes(q, K, V, scale, sink=None):  # window and far positions normalised apart
     half = max(1, K.shape[0] // 2)
     outs = []
     for sl in (slice(0, half), slice(half, None)):
@@ -53,6 +53,21 @@ def _sparse_two_softmaxes(q, K, V, scale):  # window and far positions normalise
         p /= p.sum(axis=1, keepdims=True)
         outs.append(p @ V[sl])
     return sum(outs) / len(outs)
+
+
+_sparse_ref = O.sparse_attention
+
+
+def _sparse_sink_ignored(q, K, V, scale, sink=None):  # sink bias dropped
+    return _sparse_ref(q, K, V, scale)
+
+
+def _sparse_sink_base2(q, K, V, scale, sink=None):  # sink added as 2^b instead of e^b
+    return _sparse_ref(q, K, V, scale, None if sink is None else np.asarray(sink) * np.log(2.0))
+
+
+def _gate_wrong_side(o, gate):  # o * (1 - sigmoid(g))
+    return o if gate is None else o / (1.0 + np.exp(np.asarray(gate, np.float64)))
 
 
 def _lightning_no_relu(q_idx, w_idx, K):
@@ -82,6 +97,9 @@ MUTATIONS = [
     ("lightning_scores", _lightning_no_relu),
     ("block_max", _block_max_past_t),
     ("gather_rows", _gather_wrong_slot),
+    ("sparse_attention", _sparse_sink_ignored),
+    ("sparse_attention", _sparse_sink_base2),
+    ("output_gate", _gate_wrong_side),
 ]
 
 PINS = [
@@ -100,6 +118,9 @@ PINS = [
     P.test_block_max_bruteforce_and_tail,
     P.test_reindex_over_all_blocks_is_flat_indexer,
     P.test_csa2_attention_over_whole_pool_is_dense_over_pool,
+    P.test_sa_sink_limits_and_closed_form,
+    P.test_output_gate_limits,
+    P.test_sa_decode_sink_and_gate_reach_their_heads,
 ]
 
 

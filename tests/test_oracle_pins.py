@@ -392,3 +392,48 @@ def test_decode_bytes_model():
     m = C.decode_group_bytes([100, 2000], Hq=8, Hkv=2, d=16, w=8, k=64, elem=2, n_sa=5)
     assert m["fa"] == (100 + 2000) * 2 * 16 * 2 * 2
     assert m["sa_per_layer"] == 2 * ((8 + 64) + (8 + 64)) * 16 * 2 * 2
+
+
+# ----------------------------------------------------------------------------- sink bias and gate
+def test_sa_sink_limits_and_closed_form():
+    """The per-head sink bias ([HS2] §17.1) as a zero-value key: a sink at -inf changes
+    nothing, a sink far above every logit takes all the mass, and with identical keys and
+    values the output is v / (1 + e^(b - x0) / n) in closed form."""
+    rng = np.random.default_rng(11)
+    q, K, V = rng.standard_normal((3, 8)), rng.standard_normal((5, 8)), rng.standard_normal((5, 8))
+    base = O.sparse_attention(q, K, V, 0.3)
+    assert np.allclose(O.sparse_attention(q, K, V, 0.3, sink=np.full(3, -np.inf)), base, atol=1e-15)
+    assert np.abs(O.sparse_attention(q, K, V, 0.3, sink=np.full(3, 80.0))).max() < 1e-25
+    k0, v0, n = rng.standard_normal(8), rng.standard_normal(8), 7
+    b = np.array([-1.0, 0.5, 2.0])
+    x0 = (q @ k0) * 0.3
+    expect = v0[None, :] / (1.0 + np.exp(b - x0) / n)[:, None]
+    got = O.sparse_attention(q, np.tile(k0, (n, 1)), np.tile(v0, (n, 1)), 0.3, sink=b)
+    assert np.allclose(got, expect, rtol=1e-12, atol=1e-13)
+
+
+def test_output_gate_limits():
+    """The output sigmoid gate: logit 0 halves the output, large logits pass it or zero it."""
+    o = np.random.default_rng(12).standard_normal((2, 4, 8))
+    assert np.allclose(O.output_gate(o, np.zeros_like(o)), 0.5 * o)
+    assert np.allclose(O.output_gate(o, np.full_like(o, 60.0)), o)
+    assert np.abs(O.output_gate(o, np.full_like(o, -80.0))).max() < 1e-30
+    assert O.output_gate(o, None) is o
+
+
+def test_sa_decode_sink_and_gate_reach_their_heads():
+    """sa_decode applies sink b_h to query head h (not to its KV head) and the gate element by
+    element: a huge sink on one head zeroes that head only; a zero gate halves one query."""
+    grp = W.decode_group([40, 70], Hq=4, Hkv=2, d=16, w=4, k=8, dtype="f32", seed=13, n_sa=1, needles=0)
+    _, _, idx, cnt = O.fa_decode(grp.q_fa, grp.kv, grp.w, grp.k, grp.scale)
+    base = O.sa_decode(grp.q_sa[0], grp.kv, grp.w, idx, cnt, grp.scale)
+    sink = np.full(4, -np.inf)
+    sink[1] = 90.0
+    o = O.sa_decode(grp.q_sa[0], grp.kv, grp.w, idx, cnt, grp.scale, sink=sink)
+    assert np.abs(o[:, 1]).max() < 1e-25
+    keep = [0, 2, 3]
+    assert np.allclose(o[:, keep], base[:, keep], atol=1e-15)
+    gate = np.full(base.shape, 60.0, dtype=np.float32)
+    gate[1] = 0.0
+    og = O.sa_decode(grp.q_sa[0], grp.kv, grp.w, idx, cnt, grp.scale, gate=gate)
+    assert np.allclose(og[1], 0.5 * base[1]) and np.allclose(og[0], base[0])
