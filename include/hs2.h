@@ -151,6 +151,18 @@ hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int
                         const int32_t* idx, const int32_t* idx_cnt, int k, float scale, int prefill,
                         float* o, void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
 
+/* hs2_sa_reuse with the SA layers' per-head sink bias and output sigmoid gate
+ * ([HS2] §17.1). sink: float32 [Hq] natural-log logits, or NULL: one more key per head
+ * with logit sink[h] and a zero value, i.e. the single softmax denominator over W ∪ S
+ * gains exp(sink[h]) (-inf = no sink). gate: float32 [B_or_n][Hq][d] logits, or NULL:
+ * the output is multiplied elementwise by 1 / (1 + exp(-gate)). Both are read-only,
+ * device memory, owned by the caller. Everything else as hs2_sa_reuse (which is this
+ * call with sink = gate = NULL); the workspace size does not change. */
+hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int w,
+                           const int32_t* idx, const int32_t* idx_cnt, int k, float scale, int prefill,
+                           const float* sink, const float* gate, float* o, void* workspace, size_t ws_bytes,
+                           int32_t* dev_err, void* stream);
+
 /* ---------------------------------------------------------------------------
  * CSA2 hierarchical sparse indexer  ([CSA2] §3.1-3.2; score from [L10] §5.1).
  * I(s) = sum_j w_idx[b][j] * max(0, q_idx[b][j] . k_idx(s)), unscaled, where k_idx(s)

@@ -155,3 +155,30 @@ def test_decode_bf16_full_size_sampled(H):
             s = idx[b, g, :cnt[b, g]]
             assert s.min() >= 0 and s.max() < t[b] - 128 and np.all(np.diff(s) > 0)
             assert set(grp.needles[b].tolist()) <= set(s.tolist())
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv", [("bf16", 32, 4), ("bf16", 32, 1), ("f32", 8, 2)])
+def test_sa_sink_bias_and_output_gate(H, dtype, Hq, Hkv):
+    """hs2_sa_reuse_ex: per-head sink logits (one -inf, one dominant) and elementwise gate
+    logits against the oracle, on the decode stream (bf16, 8 and 32 heads per KV head) and
+    the fp32 path."""
+    import torch
+
+    lens = [900, 2500, 130, 4000]
+    grp = W.decode_group(lens, Hq=Hq, Hkv=Hkv, d=128, w=32, k=100, dtype=dtype, seed=17, n_sa=1, needles=4)
+    kv = grp.kv
+    dkv = kv_to_device(kv)
+    _, _, idx, cnt = H.hs2_fa_select(to_torch(grp.q_fa, dtype), dkv, grp.w, grp.k, grp.scale,
+                                     max_t=int(kv.seq_len.max()))
+    rng = np.random.default_rng(3)
+    sink = rng.normal(0.0, 2.0, Hq).astype(np.float32)
+    sink[0], sink[1] = -np.inf, 30.0
+    gate = rng.normal(0.0, 2.0, (len(lens), Hq, 128)).astype(np.float32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    osa = H.hs2_sa_reuse(to_torch(grp.q_sa[0], dtype), dkv, grp.w, idx, cnt, grp.k, grp.scale, dev_err=err,
+                         sink=torch.from_numpy(sink).cuda(), gate=torch.from_numpy(gate).cuda()).cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = O.sa_decode(grp.q_sa[0], kv, grp.w, idx.cpu().numpy(), cnt.cpu().numpy(), grp.scale, sink=sink, gate=gate)
+    assert max_abs(osa, ref) <= tol(dtype), max_abs(osa, ref)
+    assert np.abs(osa[:, 1]).max() < 1e-6  # the dominant sink takes the head's mass

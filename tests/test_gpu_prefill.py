@@ -147,3 +147,21 @@ def test_prefill_sa_rows(H, n, Hq, Hkv, w, k):
                          grp.scale, prefill=True).cpu().numpy()
     ref = O.sa_prefill_rows(grp.q_sa[0], grp.kv, rows, w, idx_r, cnt_r, grp.scale)
     assert max_abs(osa, ref) <= tol("bf16")
+
+
+@pytest.mark.parametrize("n,Hq,Hkv", [(1000, 8, 2), (600, 16, 1)])
+def test_prefill_sa_sink_bias_and_output_gate(H, n, Hq, Hkv):
+    """SA prefill (tensor-core gather) with per-head sink logits and elementwise gate logits."""
+    import torch
+
+    grp = W.prefill_group(n, Hq, Hkv, 128, w=16, k=64, dtype="bf16", seed=43, n_sa=1, rho=0.99, permute=True)
+    _, _, idx, cnt = run_fa(H, grp)
+    rng = np.random.default_rng(5)
+    sink = rng.normal(0.0, 2.0, Hq).astype(np.float32)
+    sink[0] = -np.inf
+    gate = rng.normal(0.0, 2.0, (n, Hq, 128)).astype(np.float32)
+    osa = H.hs2_sa_reuse(to_torch(grp.q_sa[0], "bf16"), kv_to_device(grp.kv), 16, to_torch(idx, "i32"),
+                         to_torch(cnt, "i32"), 64, grp.scale, prefill=True, sink=torch.from_numpy(sink).cuda(),
+                         gate=torch.from_numpy(gate).cuda()).cpu().numpy()
+    ref = O.sa_prefill_rows(grp.q_sa[0], grp.kv, np.arange(n), 16, idx, cnt, grp.scale, sink=sink, gate=gate)
+    assert max_abs(osa, ref) <= tol("bf16"), max_abs(osa, ref)

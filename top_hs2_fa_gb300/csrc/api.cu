@@ -434,6 +434,14 @@ size_t hs2_sa_reuse_workspace(int B_or_n, int Hq, const hs2_kv* kv, int w, int k
 hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int w, const int32_t* idx,
                         const int32_t* idx_cnt, int k, float scale, int prefill, float* o, void* workspace,
                         size_t ws_bytes, int32_t* dev_err, void* stream) {
+  return hs2_sa_reuse_ex(q, B_or_n, Hq, kv, w, idx, idx_cnt, k, scale, prefill, nullptr, nullptr, o, workspace,
+                         ws_bytes, dev_err, stream);
+}
+
+hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int w, const int32_t* idx,
+                           const int32_t* idx_cnt, int k, float scale, int prefill, const float* sink,
+                           const float* gate, float* o, void* workspace, size_t ws_bytes, int32_t* dev_err,
+                           void* stream) {
   hs2_status st = common_checks(q, B_or_n, Hq, kv, prefill, true);
   if (st != HS2_OK) return st;
   if (w < 0 || k < 0 || !std::isfinite(scale) || !o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
@@ -469,6 +477,8 @@ hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int
   a.part_o = (float*)(ws + p.off_o);
   a.logits = nullptr;
   a.out_o = o;
+  a.sink = sink;
+  a.gate = gate;
   a.dev_err = dev_err;
   if (p.stream) {
     // bf16 decode: one persistent warp stream over all (query, KV head) pairs' entries
@@ -507,6 +517,8 @@ hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int
   c.sa_cnt = idx_cnt;
   c.kcap = k;
   c.o = o;
+  c.sink = sink;
+  c.gate = gate;
   c.select = 0;
   c.dev_err = dev_err;
   e = hs2::launch_combine(c, B_or_n, s);

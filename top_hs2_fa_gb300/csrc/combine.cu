@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_score_kernel(const Combin
     L = warp_sum(L);
     if (lane == 0) {
       M_s[h] = M;
-      Linv_s[h] = L > 0.f ? 1.f / L : 0.f;
+      Linv_s[h] = sa_norm_factor(M, L, sink_b2(a.sink, g * G + h));  // SA sink bias, if any
       lse2_s[h] = M + log2f(L);
     }
   }
@@ -100,7 +100,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_score_kernel(const Combin
         acc.w = fmaf(wgt, v.w, acc.w);
       }
       const float li = Linv_s[h];
-      *reinterpret_cast<float4*>(o_out + (size_t)h * D + d0) = make_float4(acc.x * li, acc.y * li, acc.z * li, acc.w * li);
+      float4 r4 = make_float4(acc.x * li, acc.y * li, acc.z * li, acc.w * li);
+      if (a.gate) {  // SA output gate
+        const float4 g4 = __ldg(reinterpret_cast<const float4*>(a.gate + ((size_t)qi * a.Hq + (size_t)g * G + h) * D + d0));
+        r4.x *= sa_gate(g4.x);
+        r4.y *= sa_gate(g4.y);
+        r4.z *= sa_gate(g4.z);
+        r4.w *= sa_gate(g4.w);
+      }
+      *reinterpret_cast<float4*>(o_out + (size_t)h * D + d0) = r4;
     }
     if (a.select) {
       for (int j = kk + tid; j < a.kcap; j += NT) out[j] = -1;

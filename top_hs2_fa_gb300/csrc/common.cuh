@@ -123,6 +123,20 @@ HS2_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "mem
 template <int N>
 HS2_DEVI void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// Final scaling of an SA output from its merged state (max M and sum L of the weights,
+// base 2): out = Ov * factor. b2 is the head's sink logit in base 2 (-inf: no sink), i.e.
+// one more key with a zero value whose weight 2^(b2 - M) joins the denominator
+// ("HySparse2：整体架构、KV 生命周期与 PD 分离", §17.1: per-head learnable sink bias).
+HS2_DEVI float sa_norm_factor(float M, float L, float b2) {
+  const float M2 = fmaxf(M, b2);
+  const float sc = exp2_rel(M, M2);
+  const float den = L * sc + exp2_rel(b2, M2);
+  return den > 0.f ? sc / den : 0.f;
+}
+// The SA output's sigmoid gate (same section): out * 1 / (1 + e^-g).
+HS2_DEVI float sa_gate(float g) { return 1.f / (1.f + __expf(-g)); }
+HS2_DEVI float sink_b2(const float* sink, int head) { return sink ? sink[head] * kLog2e : -INFINITY; }
+
 HS2_DEVI uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));

@@ -32,7 +32,9 @@ struct AttnArgs {
   float* part_o;    // [Bq][Hq][nsplit][D]
   float* logits;    // [Bq][Hq][ld_logits] base-2 logits, or null
   float* out_o;     // [Bq][Hq][D] final output (kernels that normalise in place)
-  int32_t* arrive;  // [Bq][Hkv] split arrival counters, zero at launch (SA staged, nsplit > 1)
+  int32_t* arrive;  // SA stream: per-unit arrival counters, zero at launch
+  const float* sink;  // SA: [Hq] sink logits (natural log), or null
+  const float* gate;  // SA: [Bq][Hq][D] output gate logits, or null
   long long ld_logits;
   int32_t* dev_err;
 };
@@ -59,6 +61,8 @@ struct CombineArgs {
   int pps;
   float* o;    // [Bq][Hq][D]
   float* lse;  // [Bq][Hq] natural log, or null
+  const float* sink;  // SA partials: [Hq] sink logits, or null
+  const float* gate;  // SA partials: [Bq][Hq][D] output gate logits, or null
   int select;  // 1: run the window-excluding top-k from the logits
   int k, kcap;
   int32_t* idx;  // [Bq][Hkv][kcap]

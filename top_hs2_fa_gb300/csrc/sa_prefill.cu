@@ -137,7 +137,10 @@ __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
       Ov += f * sm_o[((size_t)w * NT * 8 + hl) * D + dd];
     }
     if (nsplit == 1) {
-      __stcs(&out[e], L > 0.f ? Ov / L : 0.f);  // streaming store: keep L2 for the K/V rows
+      const int hq = g * G + hl;
+      float v = Ov * sa_norm_factor(M, L, sink_b2(a.sink, hq));
+      if (a.gate) v *= sa_gate(__ldcs(&a.gate[((size_t)qi * a.Hq + hq) * D + dd]));
+      __stcs(&out[e], v);  // streaming store: keep L2 for the K/V rows
     } else {
       cta_o[e] = Ov;
       if (dd == 0) {
@@ -162,7 +165,10 @@ __global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
         L += f * cluster.map_shared_rank(cta_l, r)[hl];
         Ov += f * cluster.map_shared_rank(cta_o, r)[e];
       }
-      out[e] = L > 0.f ? Ov / L : 0.f;
+      const int hq = g * G + hl;
+      float v = Ov * sa_norm_factor(M, L, sink_b2(a.sink, hq));
+      if (a.gate) v *= sa_gate(a.gate[((size_t)qi * a.Hq + hq) * D + e % D]);
+      out[e] = v;
     }
   }
   cluster.sync();

@@ -220,11 +220,14 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
         for (int hs = 0; hs < 2; ++hs) {
           const int hl = nt * 8 + 2 * tig + hs;
           if (hl < Gh) {
-            const float inv = lsum[nt][hs] > 0.f ? 1.f / lsum[nt][hs] : 0.f;
+            const int hq = g * G + h0 + hl;  // query head
+            const float inv = sa_norm_factor(at.m[nt][hs], lsum[nt][hs], sink_b2(a.sink, hq));
+            const float* gl = a.gate ? a.gate + ((size_t)qi * a.Hq + hq) * D : nullptr;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
-              out[hl * D + 16 * mt + gid] = at.acc[mt][nt][hs] * inv;
-              out[hl * D + 16 * mt + gid + 8] = at.acc[mt][nt][hs + 2] * inv;
+              const int d0 = 16 * mt + gid;
+              out[hl * D + d0] = at.acc[mt][nt][hs] * inv * (gl ? sa_gate(gl[d0]) : 1.f);
+              out[hl * D + d0 + 8] = at.acc[mt][nt][hs + 2] * inv * (gl ? sa_gate(gl[d0 + 8]) : 1.f);
             }
           }
         }
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
       const float M = warp_max(mlv[h].x);
       f[h] = lane < nc ? exp2_rel(mlv[h].x, M) : 0.f;
       const float L = warp_sum(f[h] * mlv[h].y);
-      inv[h] = L > 0.f ? 1.f / L : 0.f;
+      inv[h] = sa_norm_factor(M, L, h < Gh ? sink_b2(a.sink, g * G + h0 + h) : -INFINITY);
     }
     float4 o4[8];
 #pragma unroll
@@ -289,9 +292,17 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
     }
 #pragma unroll
     for (int h = 0; h < 8; ++h)
-      if (h < Gh && 4 * lane < D)
-        *reinterpret_cast<float4*>(out + h * D + 4 * lane) =
-            make_float4(o4[h].x * inv[h], o4[h].y * inv[h], o4[h].z * inv[h], o4[h].w * inv[h]);
+      if (h < Gh && 4 * lane < D) {
+        float4 r4 = make_float4(o4[h].x * inv[h], o4[h].y * inv[h], o4[h].z * inv[h], o4[h].w * inv[h]);
+        if (a.gate) {
+          const float4 g4 = __ldg(reinterpret_cast<const float4*>(a.gate + ((size_t)qi * a.Hq + g * G + h0 + h) * D) + lane);
+          r4.x *= sa_gate(g4.x);
+          r4.y *= sa_gate(g4.y);
+          r4.z *= sa_gate(g4.z);
+          r4.w *= sa_gate(g4.w);
+        }
+        *reinterpret_cast<float4*>(out + h * D + 4 * lane) = r4;
+      }
     if (lane == 0) a.arrive[un] = 0;
   }
   cp_async_wait<0>();

@@ -20,7 +20,7 @@ F32, BF16 = 0, 1
 FULL, REINDEX = 0, 1
 DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH = 1, 2, 4, 8
 EXPORTS = (
-    "hs2_fa_select_workspace", "hs2_fa_select", "hs2_sa_reuse_workspace", "hs2_sa_reuse",
+    "hs2_fa_select_workspace", "hs2_fa_select", "hs2_sa_reuse_workspace", "hs2_sa_reuse", "hs2_sa_reuse_ex",
     "hs2_hier_reindex_workspace", "hs2_hier_reindex", "hs2_strerror", "hs2_last_cuda_error",
     "hs2_abi_version", "hs2_profile_next", "hs2_fa_select_noalloc", "hs2_fa_select_noalloc_capacity",
 )
@@ -62,6 +62,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.hs2_sa_reuse_workspace.restype = sz
     lib.hs2_sa_reuse.argtypes = [vp, i32, i32, kvp, i32, vp, vp, i32, f32, i32, vp, vp, sz, vp, vp]
     lib.hs2_sa_reuse.restype = i32
+    lib.hs2_sa_reuse_ex.argtypes = [vp, i32, i32, kvp, i32, vp, vp, i32, f32, i32, vp, vp, vp, vp, sz, vp, vp]
+    lib.hs2_sa_reuse_ex.restype = i32
     lib.hs2_hier_reindex_workspace.argtypes = [i32, i32, kvp, i32, i32, i32, i32]
     lib.hs2_hier_reindex_workspace.restype = sz
     lib.hs2_hier_reindex.argtypes = [i32, vp, vp, i32, kvp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
@@ -165,17 +167,30 @@ def hs2_sa_reuse_workspace(B_or_n: int, Hq: int, kv: KV, w: int, k: int, prefill
 
 
 def hs2_sa_reuse(q: torch.Tensor, kv: KV, w: int, idx: torch.Tensor, idx_cnt: torch.Tensor, k: int,
-                 scale: float, prefill: bool = False, out=None, workspace=None, dev_err=None, stream=None):
-    """SA layer reusing the FA's KV and indices with its own query. Returns o (float32)."""
+                 scale: float, prefill: bool = False, out=None, workspace=None, dev_err=None, stream=None,
+                 sink: torch.Tensor | None = None, gate: torch.Tensor | None = None):
+    """SA layer reusing the FA's KV and indices with its own query. Returns o (float32).
+
+    ``sink`` (float32 [Hq]) and ``gate`` (float32 [Bq][Hq][d]) are the optional per-head sink
+    logits and output gate logits (``hs2_sa_reuse_ex``); without them this is ``hs2_sa_reuse``."""
     lib = load()
     Bq, Hq, d = q.shape
     c = kv.c()
     o = out if out is not None else torch.empty((Bq, Hq, d), dtype=torch.float32, device=q.device)
     nb = int(lib.hs2_sa_reuse_workspace(Bq, Hq, ctypes.byref(c), w, k, int(prefill)))
     ws = _workspace(nb, q.device, workspace)
-    st = lib.hs2_sa_reuse(_ptr(q), Bq, Hq, ctypes.byref(c), w, _ptr(idx), _ptr(idx_cnt), k, float(scale),
-                          int(prefill), _ptr(o), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_err),
-                          _stream(stream))
+    if sink is not None:
+        assert sink.dtype == torch.float32 and sink.is_contiguous() and sink.numel() == Hq
+    if gate is not None:
+        assert gate.dtype == torch.float32 and gate.is_contiguous() and tuple(gate.shape) == (Bq, Hq, d)
+    if sink is None and gate is None:
+        st = lib.hs2_sa_reuse(_ptr(q), Bq, Hq, ctypes.byref(c), w, _ptr(idx), _ptr(idx_cnt), k, float(scale),
+                              int(prefill), _ptr(o), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_err),
+                              _stream(stream))
+    else:
+        st = lib.hs2_sa_reuse_ex(_ptr(q), Bq, Hq, ctypes.byref(c), w, _ptr(idx), _ptr(idx_cnt), k, float(scale),
+                                 int(prefill), _ptr(sink), _ptr(gate), _ptr(o), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _ptr(dev_err), _stream(stream))
     _check(st)
     return o
 
