@@ -117,14 +117,31 @@ def topk_lower_index(score: np.ndarray, k: int) -> np.ndarray:
     return np.sort(order[:kk])
 
 
+def block_topk(score: np.ndarray, k: int, blk: int) -> np.ndarray:
+    """Block-level selection of HySparse's first version ([HS2] §2 "第一版": 16 blocks of 64
+    tokens = 1024 positions): far position s belongs to block s // blk; a block's key is the
+    largest score among its far positions; the min(k // blk, #blocks) best blocks by (key
+    descending, block ascending) are taken whole (their far positions), returned ascending.
+    blk = 1 is token-level selection."""
+    n = len(score)
+    nb = (n + blk - 1) // blk
+    kb = min(int(k) // blk, nb)
+    if kb <= 0:
+        return np.zeros(0, dtype=np.int64)
+    keys = np.array([np.max(score[b * blk:min(n, b * blk + blk)]) for b in range(nb)])
+    blocks = np.sort(np.lexsort((np.arange(nb), -keys))[:kb])
+    return np.concatenate([np.arange(b * blk, min(n, b * blk + blk)) for b in blocks]).astype(np.int64)
+
+
 def _pad(sel: np.ndarray, k: int) -> np.ndarray:
     out = np.full(k, -1, dtype=np.int32)
     out[:len(sel)] = sel
     return out
 
 
-def fa_decode(q: np.ndarray, kv, w: int, k: int, scale: float, return_scores: bool = False):
-    """FA layer for one decode query per sequence plus its window-excluding top-k.
+def fa_decode(q: np.ndarray, kv, w: int, k: int, scale: float, return_scores: bool = False, blk: int = 1):
+    """FA layer for one decode query per sequence plus its window-excluding top-k
+    (token-level; ``blk`` > 1: the block-level selection of ``block_topk``).
 
     ``q``: stored [B][Hq][d]; ``kv``: object with k, v, block_table, seq_len, dtype, page.
     Returns o float64 [B][Hq][d], lse [B][Hq], idx int32 [B][Hkv][k] (-1 padded,
@@ -150,7 +167,7 @@ def fa_decode(q: np.ndarray, kv, w: int, k: int, scale: float, return_scores: bo
             x, l, og = full_attention(qf[b, hs], K, V, scale)
             o[b, hs], lse[b, hs] = og, l
             sc = selection_scores(x, l, far_count(t, w))
-            sel = topk_lower_index(sc, k)
+            sel = topk_lower_index(sc, k) if blk == 1 else block_topk(sc, k, blk)
             idx[b, g], cnt[b, g] = _pad(sel, k), len(sel)
             if return_scores:
                 scores[(b, g)] = sc

@@ -70,6 +70,17 @@ def _gate_wrong_side(o, gate):  # o * (1 - sigmoid(g))
     return o if gate is None else o / (1.0 + np.exp(np.asarray(gate, np.float64)))
 
 
+def _block_topk_mean(score, k, blk):  # block key = mean instead of max
+    n = len(score)
+    nb = (n + blk - 1) // blk
+    kb = min(int(k) // blk, nb)
+    if kb <= 0:
+        return np.zeros(0, dtype=np.int64)
+    keys = np.array([np.mean(score[b * blk:min(n, b * blk + blk)]) for b in range(nb)])
+    blocks = np.sort(np.lexsort((np.arange(nb), -keys))[:kb])
+    return np.concatenate([np.arange(b * blk, min(n, b * blk + blk)) for b in blocks]).astype(np.int64)
+
+
 def _lightning_no_relu(q_idx, w_idx, K):
     return (np.asarray(w_idx)[:, None] * (q_idx @ K.T)).sum(axis=0)
 
@@ -100,6 +111,7 @@ MUTATIONS = [
     ("sparse_attention", _sparse_sink_ignored),
     ("sparse_attention", _sparse_sink_base2),
     ("output_gate", _gate_wrong_side),
+    ("block_topk", _block_topk_mean),
 ]
 
 PINS = [
@@ -121,6 +133,9 @@ PINS = [
     P.test_sa_sink_limits_and_closed_form,
     P.test_output_gate_limits,
     P.test_sa_decode_sink_and_gate_reach_their_heads,
+    P.test_block_topk_with_unit_blocks_is_token_topk,
+    P.test_block_topk_bruteforce_and_invariants,
+    P.test_block_decode_selection_respects_window_and_budget,
 ]
 
 

@@ -437,3 +437,48 @@ def test_sa_decode_sink_and_gate_reach_their_heads():
     gate[1] = 0.0
     og = O.sa_decode(grp.q_sa[0], grp.kv, grp.w, idx, cnt, grp.scale, gate=gate)
     assert np.allclose(og[1], 0.5 * base[1]) and np.allclose(og[0], base[0])
+
+
+# ----------------------------------------------------------------------------- block-level selection
+def test_block_topk_with_unit_blocks_is_token_topk():
+    sc = np.random.default_rng(21).random(300)
+    for k in (0, 1, 17, 299, 400):
+        assert np.array_equal(O.block_topk(sc, k, 1), O.topk_lower_index(sc, k))
+
+
+def test_block_topk_bruteforce_and_invariants():
+    """Against enumeration of every block subset of the budget's size on small inputs: the
+    chosen blocks maximise the sorted vector of block maxima (ties to lower block ids);
+    the output is whole blocks (a partial last block included), ascending, within F."""
+    import itertools
+
+    for seed in range(6):
+        rng = np.random.default_rng(30 + seed)
+        n, blk = int(rng.integers(20, 60)), int(rng.integers(2, 9))
+        sc = rng.random(n)
+        if seed % 2:
+            sc = np.round(sc * 4) / 4  # many ties
+        k = blk * int(rng.integers(1, 5))
+        sel = O.block_topk(sc, k, blk)
+        nb = (n + blk - 1) // blk
+        kb = min(k // blk, nb)
+        maxes = [sc[b * blk:min(n, b * blk + blk)].max() for b in range(nb)]
+        best = max(itertools.combinations(range(nb), kb), key=lambda c: (sorted((maxes[b] for b in c), reverse=True),
+                                                                         [-b for b in c]))
+        expect = np.concatenate([np.arange(b * blk, min(n, b * blk + blk)) for b in best]) if kb else np.zeros(0)
+        assert np.array_equal(sel, expect), (seed, sel, expect)
+        assert np.all(np.diff(sel) > 0) and (len(sel) == 0 or (sel.min() >= 0 and sel.max() < n))
+
+
+def test_block_decode_selection_respects_window_and_budget():
+    grp = W.decode_group([1500, 777], Hq=4, Hkv=1, d=32, w=64, k=256, dtype="f32", seed=22, n_sa=0, needles=4)
+    _, _, idx, cnt, _ = O.fa_decode(grp.q_fa, grp.kv, grp.w, grp.k, grp.scale, return_scores=True, blk=64)
+    for b, t in enumerate([1500, 777]):
+        s = idx[b, 0, :cnt[b, 0]]
+        assert cnt[b, 0] <= 256 and (s < t - 64).all()
+        assert set(grp.needles[b].tolist()) <= set(s.tolist())  # needles' blocks are chosen
+        blocks = np.unique(s // 64)
+        assert len(blocks) <= 4
+        for bl in blocks:  # whole blocks (clipped to the far range)
+            lo, hi = bl * 64, min(t - 64, bl * 64 + 64)
+            assert set(range(lo, hi)) <= set(s.tolist())
