@@ -138,9 +138,9 @@ class Decode:
     roofline_source = ("top_hs2_fa_gb300/csrc/fa_decode.cu", "top_hs2_fa_gb300/csrc/mma_attn.cuh")
     unit = "queries/s"
 
-    def __init__(self, name, B, t_lo, t_hi, groups, needles, qproj):
+    def __init__(self, name, B, t_lo, t_hi, groups, needles, qproj, sel_block=1):
         self.name, self.B, self.t_lo, self.t_hi, self.groups = name, B, t_lo, t_hi, groups
-        self.needles, self.qproj = needles, qproj
+        self.needles, self.qproj, self.sel_block = needles, qproj, sel_block
         self.Hq, self.Hkv, self.D, self.w, self.k = 32, 4, 128, 128, 1024
 
     def host_setup(self, seed):
@@ -193,7 +193,7 @@ class Decode:
                 hs2.hs2_profile_next(hs2.STAGE_FA_SCAN, *profile)
             hs2.hs2_fa_select(q[0], d["kv"], self.w, self.k, self.host[gi].scale, max_t=d["max_t"],
                               out=(d["o"][0], d["lse"], d["idx"], d["cnt"]), workspace=d["ws_fa"], dev_err=err,
-                              stream=stream)
+                              stream=stream, sel_block=self.sel_block)
             for j in range(NSA):
                 hs2.hs2_sa_reuse(q[1 + j], d["kv"], self.w, d["idx"], d["cnt"], self.k, self.host[gi].scale,
                                  out=d["o"][1 + j], workspace=d["ws_sa"], dev_err=err, stream=stream)
@@ -216,7 +216,8 @@ class Decode:
         return {"workload": self.name, "batch": self.B,
                 "seq_len": f"U[{self.t_lo},{self.t_hi}]" if self.t_lo != self.t_hi else self.t_lo,
                 "groups": self.groups, "Hq": self.Hq, "Hkv": self.Hkv, "head_dim": self.D, "window": self.w,
-                "top_k": self.k, "sa_layers_per_group": NSA, "page": 64, "kv_dtype": "bf16"}
+                "top_k": self.k, "sa_layers_per_group": NSA, "page": 64, "kv_dtype": "bf16",
+                "selection": "token" if self.sel_block == 1 else f"blocks of {self.sel_block}"}
 
     def oracle_sample(self, budget_s):
         """Oracle FA + 5 SA per query (in every group) on the host cores, query by query."""
@@ -230,7 +231,7 @@ class Decode:
                 kv, sel = grp.kv, [done]
                 sub = W.PagedKV(k=kv.k, v=kv.v, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel],
                                 dtype=kv.dtype, page=kv.page)
-                _, _, idx, cnt = O.fa_decode(grp.q_fa[sel], sub, self.w, self.k, grp.scale)
+                _, _, idx, cnt = O.fa_decode(grp.q_fa[sel], sub, self.w, self.k, grp.scale, blk=self.sel_block)
                 for j in range(NSA):
                     O.sa_decode(grp.q_sa[j][sel], sub, self.w, idx, cnt, grp.scale)
             elapsed += time.perf_counter() - t0
@@ -429,6 +430,8 @@ class Csa2:
 SCENARIOS = {
     "decode": lambda: Decode("decode_bf16_b64_t16k-32k", 64, 16384, 32768, 1, 32, True),
     "long_decode": lambda: Decode("long_decode_bf16_b16_t131072_x4", 16, 131072, 131072, 4, 64, False),
+    # the decode workload with HySparse's first-version block-level selection (16 blocks of 64)
+    "decode_block": lambda: Decode("decode_bf16_b64_t16k-32k_block64", 64, 16384, 32768, 1, 32, True, sel_block=64),
     "prefill": lambda: Prefill(32768),
     "csa2": lambda: Csa2(),
 }

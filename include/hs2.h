@@ -116,6 +116,19 @@ hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, in
                          int32_t* idx_cnt, void* workspace, size_t ws_bytes, int32_t* dev_err,
                          void* stream);
 
+/* hs2_fa_select with block-level selection, the first HySparse version's scheme ([HS2] §2:
+ * 16 blocks of 64 tokens = 1024 positions). sel_block = 1 is hs2_fa_select. sel_block > 1
+ * (decode only; sel_block a multiple of 4, at most 4096, and k a multiple of sel_block): far position s belongs to
+ * block s / sel_block, a block's key is the largest selection score among its far
+ * positions, and the min(k / sel_block, #blocks) best blocks by (key descending, block
+ * ascending) are taken whole: idx holds their far positions ascending (-1 padded),
+ * idx_cnt their number. Prefill with sel_block > 1: HS2_ERR_UNSUPPORTED. The workspace
+ * size is hs2_fa_select_workspace's. */
+hs2_status hs2_fa_select_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w,
+                            int k, float scale, int prefill, int sel_block, float* o, float* lse,
+                            int32_t* idx, int32_t* idx_cnt, void* workspace, size_t ws_bytes,
+                            int32_t* dev_err, void* stream);
+
 /* ---------------------------------------------------------------------------
  * hs2_fa_select_noalloc — hs2_fa_select for callers that cannot allocate device
  * memory (an engine that has reserved nearly all HBM for its KV pool and forbids

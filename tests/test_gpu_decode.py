@@ -182,3 +182,53 @@ def test_sa_sink_bias_and_output_gate(H, dtype, Hq, Hkv):
     ref = O.sa_decode(grp.q_sa[0], kv, grp.w, idx.cpu().numpy(), cnt.cpu().numpy(), grp.scale, sink=sink, gate=gate)
     assert max_abs(osa, ref) <= tol(dtype), max_abs(osa, ref)
     assert np.abs(osa[:, 1]).max() < 1e-6  # the dominant sink takes the head's mass
+
+
+@pytest.mark.parametrize("dtype,lens,k,blk", [("bf16", [3000, 1500, 700, 5000], 256, 64),
+                                              ("f32", [900, 2222], 128, 32),
+                                              ("bf16", [520, 610], 1024, 64)])
+def test_block_level_selection(H, dtype, lens, k, blk):
+    """hs2_fa_select_ex with sel_block > 1 against the oracle's block-level selection: whole
+    blocks by block maximum (ties to lower blocks), including a partial last far block and a
+    budget that covers every block; SA over the chosen positions."""
+    import torch
+
+    grp = W.decode_group(lens, Hq=8, Hkv=2, d=128, w=32, k=k, dtype=dtype, seed=19, n_sa=1, needles=4)
+    kv = grp.kv
+    dkv = kv_to_device(kv)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse, idx, cnt = H.hs2_fa_select(to_torch(grp.q_fa, dtype), dkv, grp.w, k, grp.scale,
+                                       max_t=int(kv.seq_len.max()), dev_err=err, sel_block=blk)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o_r, _, idx_r, cnt_r, sc = O.fa_decode(grp.q_fa, kv, grp.w, k, grp.scale, return_scores=True, blk=blk)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    assert max_abs(o.cpu().numpy(), o_r) <= tol(dtype)
+    for b in range(len(lens)):
+        for g in range(2):
+            got, ref = idx[b, g, :cnt[b, g]], idx_r[b, g, :cnt_r[b, g]]
+            if not np.array_equal(got, ref):
+                # near ties between block maxima may swap whole blocks: compare block maxima
+                s = sc[(b, g)]
+                gb, rb = set(got // blk), set(ref // blk)
+                kth = sorted((s[bl * blk:min(len(s), bl * blk + blk)].max() for bl in rb))[0]
+                for bl in gb ^ rb:
+                    m = s[bl * blk:min(len(s), bl * blk + blk)].max()
+                    assert abs(m - kth) <= 1e-3 * kth, (b, g, bl, m, kth)
+            assert (idx[b, g, cnt[b, g]:] == -1).all()
+    osa = H.hs2_sa_reuse(to_torch(grp.q_sa[0], dtype), dkv, grp.w, to_torch(idx, "i32"), to_torch(cnt, "i32"), k,
+                         grp.scale).cpu().numpy()
+    ref = O.sa_decode(grp.q_sa[0], kv, grp.w, idx, cnt, grp.scale)
+    assert max_abs(osa, ref) <= tol(dtype)
+
+
+def test_block_level_selection_rejects_bad_sizes(H):
+    import torch
+
+    grp = W.decode_group([300], Hq=8, Hkv=1, d=128, w=16, k=96, dtype="bf16", seed=20, n_sa=0, needles=0)
+    dkv = kv_to_device(grp.kv)
+    q = to_torch(grp.q_fa, "bf16")
+    with pytest.raises(H.HS2Error):
+        H.hs2_fa_select(q, dkv, 16, 96, grp.scale, max_t=300, sel_block=64)  # k not a multiple
+    with pytest.raises(H.HS2Error):
+        H.hs2_fa_select(q, dkv, 16, 96, grp.scale, max_t=300, sel_block=6)  # not a multiple of 4

@@ -348,9 +348,19 @@ static hs2_status fa_select_prefill_tc(const void* q, int n, int Hq, const hs2_k
 hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w, int k,
                          float scale, int prefill, float* o, float* lse, int32_t* idx, int32_t* idx_cnt,
                          void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  return hs2_fa_select_ex(q, B_or_n, Hq, kv, max_t, w, k, scale, prefill, 1, o, lse, idx, idx_cnt, workspace,
+                          ws_bytes, dev_err, stream);
+}
+
+hs2_status hs2_fa_select_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w, int k,
+                            float scale, int prefill, int sel_block, float* o, float* lse, int32_t* idx,
+                            int32_t* idx_cnt, void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
   hs2_status st = common_checks(q, B_or_n, Hq, kv, prefill, true);
   if (st != HS2_OK) return st;
   if (w < 0 || k < 0 || max_t < 1 || !std::isfinite(scale)) return HS2_ERR_ARG;
+  if (sel_block < 1 || sel_block > 4096 || (sel_block > 1 && (sel_block % 4 != 0 || k % sel_block != 0)))
+    return HS2_ERR_ARG;
+  if (sel_block > 1 && prefill) return HS2_ERR_UNSUPPORTED;
   if ((long long)max_t > (long long)kv->max_pages * 64) return HS2_ERR_ARG;
   if (prefill && B_or_n > max_t) return HS2_ERR_ARG;
   if (!o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
@@ -410,6 +420,7 @@ hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, in
   c.o = o;
   c.lse = lse;
   c.select = 1;
+  c.sel_block = sel_block;
   c.k = k;
   c.kcap = k;
   c.idx = idx;

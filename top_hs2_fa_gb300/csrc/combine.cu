@@ -181,6 +181,53 @@ __global__ void __launch_bounds__(kSelectThreads, 2) select_kernel(const Combine
   block_topk<NT>(nF, kk, key, emit, sm);
 }
 
+// Block-level selection (the first HySparse version: whole blocks of far positions): one
+// CTA per (query, KV head); block maxima of the position keys, radix top-k over the blocks,
+// then the chosen blocks' far positions in ascending order.
+__global__ void __launch_bounds__(kSelectThreads) block_select_kernel(const CombineArgs a) {
+  constexpr int NT = kSelectThreads;
+  const int g = blockIdx.x, qi = blockIdx.y;
+  const QueryGeom qg = query_geom(qi, a.prefill, a.seq_len);
+  const int t = qg.t;
+  if ((t < 1) || (t > a.max_t) || ((t + kPage - 1) / kPage > a.max_pages)) return;
+  const int nF = max(0, t - a.w);
+  const int kk = min(a.k, nF);
+  if (kk == 0 || kk >= nF) return;  // written by merge_score_kernel (none, or all of F)
+  const int blk = a.sel_block;
+  const int nb = (nF + blk - 1) / blk, kb = min(a.k / blk, nb);
+  __shared__ TopkSmem<NT> sm;
+  extern __shared__ uint32_t bkey[];  // [nb] block maxima, then [kb] chosen blocks
+  const uint32_t* keys = a.scores + ((size_t)qi * a.Hkv + g) * a.ld_logits;
+  for (int b = threadIdx.x; b < nb; b += NT) bkey[b] = 0u;
+  __syncthreads();
+  // block maxima: 4-key chunks (blk is a multiple of 4, so a chunk lies in one block)
+  const int nch = (nF + 3) / 4;  // the key row is readable up to nF rounded up to 4
+#pragma unroll 4
+  for (int c = threadIdx.x; c < nch; c += NT) {
+    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(keys) + c);
+    const int s = 4 * c;
+    uint32_t m = v.x;
+    if (s + 1 < nF) m = max(m, v.y);
+    if (s + 2 < nF) m = max(m, v.z);
+    if (s + 3 < nF) m = max(m, v.w);
+    atomicMax(&bkey[s / blk], m);
+  }
+  __syncthreads();
+  uint32_t* chosen = bkey + nb;
+  block_topk<NT>(nb, kb, [&](int i) { return bkey[i]; }, [&](int j, int i) { chosen[j] = (uint32_t)i; }, sm);
+  __syncthreads();
+  // every chosen block but the last far block is full, so block j's positions start at j*blk
+  int32_t* out = a.idx + ((size_t)qi * a.Hkv + g) * a.kcap;
+  for (int e = threadIdx.x; e < kb * blk; e += NT) {
+    const int j = e / blk, r = e % blk;
+    const int s = (int)chosen[j] * blk + r;
+    out[e] = s < nF ? s : -1;
+  }
+  const int tail = (int)chosen[kb - 1] == nb - 1 ? nb * blk - nF : 0;  // missing positions of a partial last block
+  for (int j = kb * blk + threadIdx.x; j < a.kcap; j += NT) out[j] = -1;
+  if (threadIdx.x == 0) a.cnt[(size_t)qi * a.Hkv + g] = kb * blk - tail;
+}
+
 // ============================================================================ generic row top-k
 __global__ void __launch_bounds__(kSelectThreads, 2) select_rows_kernel(const SelectArgs a) {
   constexpr int NT = kSelectThreads;
@@ -258,6 +305,14 @@ cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s) {
   else return cudaErrorInvalidValue;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !a.select) return e;
+  if (a.sel_block > 1) {
+    const int nb_max = (int)((a.ld_logits + a.sel_block - 1) / a.sel_block);
+    const size_t smb = (size_t)(nb_max + a.k / a.sel_block) * sizeof(uint32_t);
+    e = cudaFuncSetAttribute(block_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smb);
+    if (e != cudaSuccess) return e;
+    block_select_kernel<<<dim3(a.Hkv, Bq), kSelectThreads, smb, s>>>(a);
+    return cudaGetLastError();
+  }
   const size_t sm = select_smem(a.kcap);
   e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;

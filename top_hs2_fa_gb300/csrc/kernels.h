@@ -64,6 +64,7 @@ struct CombineArgs {
   const float* sink;  // SA partials: [Hq] sink logits, or null
   const float* gate;  // SA partials: [Bq][Hq][D] output gate logits, or null
   int select;  // 1: run the window-excluding top-k from the logits
+  int sel_block;  // 1: token-level selection; > 1: whole blocks of that many far positions
   int k, kcap;
   int32_t* idx;  // [Bq][Hkv][kcap]
   int32_t* cnt;  // [Bq][Hkv]

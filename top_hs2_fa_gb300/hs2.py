@@ -20,7 +20,7 @@ F32, BF16 = 0, 1
 FULL, REINDEX = 0, 1
 DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH = 1, 2, 4, 8
 EXPORTS = (
-    "hs2_fa_select_workspace", "hs2_fa_select", "hs2_sa_reuse_workspace", "hs2_sa_reuse", "hs2_sa_reuse_ex",
+    "hs2_fa_select_workspace", "hs2_fa_select", "hs2_fa_select_ex", "hs2_sa_reuse_workspace", "hs2_sa_reuse", "hs2_sa_reuse_ex",
     "hs2_hier_reindex_workspace", "hs2_hier_reindex", "hs2_strerror", "hs2_last_cuda_error",
     "hs2_abi_version", "hs2_profile_next", "hs2_fa_select_noalloc", "hs2_fa_select_noalloc_capacity",
 )
@@ -58,6 +58,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.hs2_fa_select_workspace.restype = sz
     lib.hs2_fa_select.argtypes = [vp, i32, i32, kvp, i32, i32, i32, f32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.hs2_fa_select.restype = i32
+    lib.hs2_fa_select_ex.argtypes = [vp, i32, i32, kvp, i32, i32, i32, f32, i32, i32, vp, vp, vp, vp, vp, sz, vp,
+                                     vp]
+    lib.hs2_fa_select_ex.restype = i32
     lib.hs2_sa_reuse_workspace.argtypes = [i32, i32, kvp, i32, i32, i32]
     lib.hs2_sa_reuse_workspace.restype = sz
     lib.hs2_sa_reuse.argtypes = [vp, i32, i32, kvp, i32, vp, vp, i32, f32, i32, vp, vp, sz, vp, vp]
@@ -135,9 +138,11 @@ def hs2_fa_select_workspace(B_or_n: int, Hq: int, kv: KV, max_t: int, k: int, pr
 
 
 def hs2_fa_select(q: torch.Tensor, kv: KV, w: int, k: int, scale: float, prefill: bool = False,
-                  max_t: int | None = None, out=None, workspace=None, dev_err=None, stream=None):
+                  max_t: int | None = None, out=None, workspace=None, dev_err=None, stream=None,
+                  sel_block: int = 1):
     """FA layer + window-excluding top-k. Returns (o, lse, idx, idx_cnt) (float32, float32,
-    int32, int32). ``max_t`` defaults to the table's capacity (decode) or n (prefill)."""
+    int32, int32). ``max_t`` defaults to the table's capacity (decode) or n (prefill).
+    ``sel_block`` > 1 selects whole blocks of that many far positions (``hs2_fa_select_ex``)."""
     lib = load()
     Bq, Hq, d = q.shape
     c = kv.c()
@@ -154,9 +159,14 @@ def hs2_fa_select(q: torch.Tensor, kv: KV, w: int, k: int, scale: float, prefill
         o, lse, idx, cnt = out
     nb = int(lib.hs2_fa_select_workspace(Bq, Hq, ctypes.byref(c), max_t, k, int(prefill)))
     ws = _workspace(nb, dev, workspace)
-    st = lib.hs2_fa_select(_ptr(q), Bq, Hq, ctypes.byref(c), max_t, w, k, float(scale), int(prefill),
-                           _ptr(o), _ptr(lse), _ptr(idx), _ptr(cnt), _ptr(ws), ws.numel() * ws.element_size(),
-                           _ptr(dev_err), _stream(stream))
+    if sel_block == 1:
+        st = lib.hs2_fa_select(_ptr(q), Bq, Hq, ctypes.byref(c), max_t, w, k, float(scale), int(prefill),
+                               _ptr(o), _ptr(lse), _ptr(idx), _ptr(cnt), _ptr(ws), ws.numel() * ws.element_size(),
+                               _ptr(dev_err), _stream(stream))
+    else:
+        st = lib.hs2_fa_select_ex(_ptr(q), Bq, Hq, ctypes.byref(c), max_t, w, k, float(scale), int(prefill),
+                                  int(sel_block), _ptr(o), _ptr(lse), _ptr(idx), _ptr(cnt), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _ptr(dev_err), _stream(stream))
     _check(st)
     return o, lse, idx, cnt
 
