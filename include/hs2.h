@@ -211,6 +211,11 @@ typedef enum {
   HS2_STAGE_INDEXER = 2     /* lightning-indexer scan (hs2_hier_reindex) */
 } hs2_stage;
 void hs2_profile_next(hs2_stage stage, void* start, void* stop);
+/* hs2_selftest_wait_timeout: launches one warp that waits, through the library's bounded
+ * mbarrier wait and with a limit of timeout_us microseconds (1 .. 2000000), on a barrier nothing
+ * arrives on; the wait gives up, HS2_DEV_TIMEOUT is set in *dev_err (device memory) and the
+ * kernel finishes. Lets a caller check the device-side timeout path without a fault. */
+hs2_status hs2_selftest_wait_timeout(int timeout_us, int32_t* dev_err, void* stream);
 const char* hs2_strerror(hs2_status st);
 int hs2_last_cuda_error(void); /* cudaError_t of the last HS2_ERR_CUDA, 0 if none */
 int hs2_abi_version(void);

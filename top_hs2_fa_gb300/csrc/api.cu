@@ -345,6 +345,13 @@ static hs2_status fa_select_prefill_tc(const void* q, int n, int Hq, const hs2_k
   return HS2_OK;
 }
 
+hs2_status hs2_selftest_wait_timeout(int timeout_us, int32_t* dev_err, void* stream) {
+  if (timeout_us < 1 || timeout_us > 2000000 || !dev_err) return HS2_ERR_ARG;
+  cudaError_t e = hs2::launch_wait_selftest(dev_err, 1000ull * (unsigned long long)timeout_us, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return HS2_OK;
+}
+
 hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w, int k,
                          float scale, int prefill, float* o, float* lse, int32_t* idx, int32_t* idx_cnt,
                          void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {

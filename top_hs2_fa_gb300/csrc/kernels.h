@@ -163,4 +163,6 @@ cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, 
 cudaError_t launch_fa_prefill_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PfArgs& a,
                                   cudaStream_t s);
 
+cudaError_t launch_wait_selftest(int32_t* dev_err, unsigned long long limit_ns, cudaStream_t s);
+
 }  // namespace hs2

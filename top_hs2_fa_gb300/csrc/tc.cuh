@@ -47,12 +47,12 @@ HS2_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete; false on timeout.
-HS2_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity) {
+HS2_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 

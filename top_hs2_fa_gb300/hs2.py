@@ -22,7 +22,7 @@ DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH = 1, 2, 4, 8
 EXPORTS = (
     "hs2_fa_select_workspace", "hs2_fa_select", "hs2_fa_select_ex", "hs2_sa_reuse_workspace", "hs2_sa_reuse", "hs2_sa_reuse_ex",
     "hs2_hier_reindex_workspace", "hs2_hier_reindex", "hs2_strerror", "hs2_last_cuda_error",
-    "hs2_abi_version", "hs2_profile_next", "hs2_fa_select_noalloc", "hs2_fa_select_noalloc_capacity",
+    "hs2_abi_version", "hs2_profile_next", "hs2_selftest_wait_timeout", "hs2_fa_select_noalloc", "hs2_fa_select_noalloc_capacity",
 )
 STAGE_FA_SCAN, STAGE_SA_GATHER, STAGE_INDEXER = 0, 1, 2
 
@@ -71,6 +71,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.hs2_hier_reindex_workspace.restype = sz
     lib.hs2_hier_reindex.argtypes = [i32, vp, vp, i32, kvp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.hs2_hier_reindex.restype = i32
+    lib.hs2_selftest_wait_timeout.argtypes = [i32, vp, vp]
+    lib.hs2_selftest_wait_timeout.restype = i32
     lib.hs2_strerror.argtypes = [i32]
     lib.hs2_strerror.restype = ctypes.c_char_p
     lib.hs2_last_cuda_error.restype = i32
@@ -267,3 +269,9 @@ def hs2_fa_select_noalloc(q: torch.Tensor, kv: KV, w: int, k: int, scale: float,
                                    _ptr(o), _ptr(lse), _ptr(idx), _ptr(cnt), _ptr(dev_err), _stream(stream))
     _check(st)
     return o, lse, idx, cnt
+
+
+def hs2_selftest_wait_timeout(timeout_us: int, dev_err: torch.Tensor, stream=None) -> None:
+    """One warp waits (bounded, timeout_us) on an mbarrier nothing arrives on: the wait must
+    give up and set DEV_TIMEOUT in dev_err."""
+    _check(load().hs2_selftest_wait_timeout(int(timeout_us), _ptr(dev_err), _stream(stream)))
