@@ -50,8 +50,23 @@ __all__ = [
 
 
 # ----------------------------------------------------------------------------- inputs
+def fp8_e4m3_to_f64(b: np.ndarray) -> np.ndarray:
+    """Exact value of FP8 E4M3 bytes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+    exponent 0 is subnormal, m * 2^-9; exponent 15 with mantissa 7 is NaN, there is no
+    infinity): the storage of the low-precision KV option (the pages' case for cutting main-KV
+    bytes: [CSA2] §3, "KV 字节与 FP4")."""
+    b = np.asarray(b, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e, m = (b >> 3) & 0xF, b & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    return np.where((e == 15) & (m == 7), np.nan, sign * mag)
+
+
 def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact widening of stored values: bfloat16 bit patterns (uint16) or float32."""
+    """Exact widening of stored values: bfloat16 bit patterns (uint16), float32, or FP8 E4M3
+    bytes (uint8; scaling is applied by the caller)."""
+    if dtype == "fp8":
+        return fp8_e4m3_to_f64(x)
     if dtype == "bf16":
         u = np.ascontiguousarray(x, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
         return u.view(np.float32).astype(np.float64)
@@ -61,15 +76,29 @@ def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def gather_rows(pool: np.ndarray, bt_row: np.ndarray, g: int, positions: np.ndarray,
-                page: int, dtype: str) -> np.ndarray:
+                page: int, dtype: str, scale=None) -> np.ndarray:
     """Block-table resolve: logical position s of one sequence -> row
     pool[bt[s // page]][g][s % page] of the paged pool, as float64 [len(positions)][d].
-    Entries are read in place through the table ([HS2] §7.2: "按索引直接访问 paged KV")."""
+    Entries are read in place through the table ([HS2] §7.2: "按索引直接访问 paged KV").
+    ``scale`` ([num_pages][Hkv], FP8 pools): row values are stored / scale[page][g]."""
     positions = np.asarray(positions, dtype=np.int64)
     pages = np.asarray(bt_row, dtype=np.int64)[positions // page]
     if positions.size and (pages < 0).any():
         raise ValueError("block table entry < 0 for a visible position")
-    return to_f64(pool[pages, g, positions % page, :], dtype)
+    rows = to_f64(pool[pages, g, positions % page, :], dtype)
+    if scale is not None:
+        rows = rows * np.asarray(scale, dtype=np.float64)[pages, g][:, None]
+    return rows
+
+
+def _scale(kv, which: str):
+    """The per-(page, KV head) dequantisation scale of an FP8 pool (None otherwise)."""
+    return getattr(kv, which + "_scale", None) if kv.dtype == "fp8" else None
+
+
+def _qdtype(kv) -> str:
+    """Queries are bf16 when the KV cache is FP8, else the cache's dtype."""
+    return "bf16" if kv.dtype == "fp8" else kv.dtype
 
 
 # ----------------------------------------------------------------------------- window / far range
@@ -148,7 +177,7 @@ def fa_decode(q: np.ndarray, kv, w: int, k: int, scale: float, return_scores: bo
     ascending), cnt int32 [B][Hkv]; with ``return_scores`` also a dict
     {(b, g): score array over F}.
     """
-    qf = to_f64(q, kv.dtype)
+    qf = to_f64(q, _qdtype(kv))
     B, Hq, d = qf.shape
     Hkv = kv.k.shape[1]
     G = Hq // Hkv
@@ -161,8 +190,8 @@ def fa_decode(q: np.ndarray, kv, w: int, k: int, scale: float, return_scores: bo
         t = int(kv.seq_len[b])
         pos = np.arange(t)
         for g in range(Hkv):
-            K = gather_rows(kv.k, kv.block_table[b], g, pos, kv.page, kv.dtype)
-            V = gather_rows(kv.v, kv.block_table[b], g, pos, kv.page, kv.dtype)
+            K = gather_rows(kv.k, kv.block_table[b], g, pos, kv.page, kv.dtype, _scale(kv, "k"))
+            V = gather_rows(kv.v, kv.block_table[b], g, pos, kv.page, kv.dtype, _scale(kv, "v"))
             hs = slice(g * G, (g + 1) * G)
             x, l, og = full_attention(qf[b, hs], K, V, scale)
             o[b, hs], lse[b, hs] = og, l
@@ -222,7 +251,7 @@ def sa_decode(q: np.ndarray, kv, w: int, idx: np.ndarray, cnt: np.ndarray, scale
     O_h = sum over U = W(t) ∪ S(t) of softmax_U(scale q_h.k) v. Optional sink bias [Hq] and
     output gate logits [B][Hq][d] ([HS2] §17.1, see sparse_attention / output_gate).
     Returns float64 [B][Hq][d]."""
-    qf = to_f64(q, kv.dtype)
+    qf = to_f64(q, _qdtype(kv))
     B, Hq, d = qf.shape
     Hkv = kv.k.shape[1]
     G = Hq // Hkv
@@ -231,8 +260,8 @@ def sa_decode(q: np.ndarray, kv, w: int, idx: np.ndarray, cnt: np.ndarray, scale
         t = int(kv.seq_len[b])
         for g in range(Hkv):
             U = _union(t, w, idx[b, g, :cnt[b, g]])
-            K = gather_rows(kv.k, kv.block_table[b], g, U, kv.page, kv.dtype)
-            V = gather_rows(kv.v, kv.block_table[b], g, U, kv.page, kv.dtype)
+            K = gather_rows(kv.k, kv.block_table[b], g, U, kv.page, kv.dtype, _scale(kv, "k"))
+            V = gather_rows(kv.v, kv.block_table[b], g, U, kv.page, kv.dtype, _scale(kv, "v"))
             hs = slice(g * G, (g + 1) * G)
             o[b, hs] = sparse_attention(qf[b, hs], K, V, scale, None if sink is None else np.asarray(sink)[hs])
     return output_gate(o, None if gate is None else to_f64(gate, "f32"))
@@ -247,7 +276,7 @@ def fa_prefill_rows(q: np.ndarray, kv, rows, w: int, k: int, scale: float, retur
     (and per-(r, g) scores with ``return_scores``).
     """
     rows = np.asarray(rows, dtype=np.int64)
-    qf = to_f64(q, kv.dtype)
+    qf = to_f64(q, _qdtype(kv))
     _, Hq, d = qf.shape
     Hkv = kv.k.shape[1]
     G = Hq // Hkv
@@ -261,8 +290,8 @@ def fa_prefill_rows(q: np.ndarray, kv, rows, w: int, k: int, scale: float, retur
     Vall = [None] * Hkv
     tmax = int(rows.max()) + 1 if R else 0
     for g in range(Hkv):
-        Kall[g] = gather_rows(kv.k, kv.block_table[0], g, np.arange(tmax), kv.page, kv.dtype)
-        Vall[g] = gather_rows(kv.v, kv.block_table[0], g, np.arange(tmax), kv.page, kv.dtype)
+        Kall[g] = gather_rows(kv.k, kv.block_table[0], g, np.arange(tmax), kv.page, kv.dtype, _scale(kv, "k"))
+        Vall[g] = gather_rows(kv.v, kv.block_table[0], g, np.arange(tmax), kv.page, kv.dtype, _scale(kv, "v"))
     for r, i in enumerate(rows):
         t = int(i) + 1
         for g in range(Hkv):
@@ -285,7 +314,7 @@ def sa_prefill_rows(q: np.ndarray, kv, rows, w: int, idx: np.ndarray, cnt: np.nd
     ([n][Hkv][k] and [n][Hkv]); optional sink [Hq] and gate logits [n][Hq][d].
     Returns float64 [R][Hq][d]."""
     rows = np.asarray(rows, dtype=np.int64)
-    qf = to_f64(q, kv.dtype)
+    qf = to_f64(q, _qdtype(kv))
     _, Hq, d = qf.shape
     Hkv = kv.k.shape[1]
     G = Hq // Hkv
@@ -294,8 +323,8 @@ def sa_prefill_rows(q: np.ndarray, kv, rows, w: int, idx: np.ndarray, cnt: np.nd
         t = int(i) + 1
         for g in range(Hkv):
             U = _union(t, w, idx[i, g, :cnt[i, g]])
-            K = gather_rows(kv.k, kv.block_table[0], g, U, kv.page, kv.dtype)
-            V = gather_rows(kv.v, kv.block_table[0], g, U, kv.page, kv.dtype)
+            K = gather_rows(kv.k, kv.block_table[0], g, U, kv.page, kv.dtype, _scale(kv, "k"))
+            V = gather_rows(kv.v, kv.block_table[0], g, U, kv.page, kv.dtype, _scale(kv, "v"))
             hs = slice(g * G, (g + 1) * G)
             o[r, hs] = sparse_attention(qf[i, hs], K, V, scale, None if sink is None else np.asarray(sink)[hs])
     return output_gate(o, None if gate is None else to_f64(np.asarray(gate)[rows], "f32"))

@@ -81,6 +81,14 @@ def _block_topk_mean(score, k, blk):  # block key = mean instead of max
     return np.concatenate([np.arange(b * blk, min(n, b * blk + blk)) for b in blocks]).astype(np.int64)
 
 
+def _fp8_bias8(b):  # exponent bias 8 instead of 7
+    b = np.asarray(b, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e, m = (b >> 3) & 0xF, b & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -10, (1.0 + m / 8.0) * np.exp2(e - 8.0))
+    return np.where((e == 15) & (m == 7), np.nan, sign * mag)
+
+
 def _lightning_no_relu(q_idx, w_idx, K):
     return (np.asarray(w_idx)[:, None] * (q_idx @ K.T)).sum(axis=0)
 
@@ -112,6 +120,7 @@ MUTATIONS = [
     ("sparse_attention", _sparse_sink_base2),
     ("output_gate", _gate_wrong_side),
     ("block_topk", _block_topk_mean),
+    ("fp8_e4m3_to_f64", _fp8_bias8),
 ]
 
 PINS = [
@@ -136,6 +145,8 @@ PINS = [
     P.test_block_topk_with_unit_blocks_is_token_topk,
     P.test_block_topk_bruteforce_and_invariants,
     P.test_block_decode_selection_respects_window_and_budget,
+    P.test_fp8_e4m3_values_from_the_format,
+    P.test_fp8_encoder_rounds_to_nearest_even,
 ]
 
 

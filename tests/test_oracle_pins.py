@@ -482,3 +482,51 @@ def test_block_decode_selection_respects_window_and_budget():
         for bl in blocks:  # whole blocks (clipped to the far range)
             lo, hi = bl * 64, min(t - 64, bl * 64 + 64)
             assert set(range(lo, hi)) <= set(s.tolist())
+
+
+# ----------------------------------------------------------------------------- FP8 KV
+def test_fp8_e4m3_values_from_the_format():
+    """E4M3 facts: 0x00 = 0, 0x01 = 2^-9 (smallest subnormal), 0x08 = 2^-6 (smallest normal),
+    0x38 = 1, 0x7E = 448 (largest), 0xB8 = -1, 0x7F = NaN (no infinity)."""
+    v = O.fp8_e4m3_to_f64(np.array([0x00, 0x01, 0x08, 0x38, 0x7E, 0xB8, 0x7F], dtype=np.uint8))
+    assert v[0] == 0.0 and v[1] == 2.0 ** -9 and v[2] == 2.0 ** -6 and v[3] == 1.0 and v[4] == 448.0
+    assert v[5] == -1.0 and np.isnan(v[6])
+    every = O.fp8_e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    finite = every[np.isfinite(every)]
+    assert len(finite) == 254 and np.all(np.diff(np.sort(np.unique(np.abs(finite)))) > 0)
+
+
+def test_fp8_encoder_rounds_to_nearest_even():
+    """The input encoder: decode(encode(x)) is a nearest finite E4M3 value (ties to the even
+    code), by enumeration of all 254 finite values; every finite code round-trips."""
+    table = O.fp8_e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    fin = np.isfinite(table)
+    x = np.concatenate([np.random.default_rng(40).standard_normal(3000) * 30, table[fin][:126] + 1e-12,
+                        (table[1:126] + table[2:127]) / 2])  # includes exact midpoints
+    c = W.f32_to_fp8_e4m3(x)
+    got = O.fp8_e4m3_to_f64(c)
+    err = np.abs(table[fin][None, :] - np.clip(x, -448, 448)[:, None])
+    assert np.allclose(np.abs(got - np.clip(x, -448, 448)), err.min(axis=1), atol=0, rtol=0)
+    mids = slice(3000 + 126, None)
+    assert np.all((c[mids] & 1) == 0)  # ties went to the even code
+    codes = np.arange(127, dtype=np.uint8)
+    assert np.array_equal(W.f32_to_fp8_e4m3(table[:127]), codes)
+
+
+def test_oracle_on_fp8_pool_equals_oracle_on_its_dequantised_values():
+    """FA + selection + SA on an FP8 pool equal the same on a float32 pool holding code *
+    scale, dequantised independently here."""
+    grp = W.decode_group_fp8([300, 170], Hq=4, Hkv=2, d=32, w=8, k=16, seed=41, n_sa=1, needles=0)
+    kv = grp.kv
+    table = O.fp8_e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    deq = lambda codes, sc: (table[codes] * sc[:, :, None, None]).astype(np.float32)
+    kv32 = W.PagedKV(k=deq(kv.k, kv.k_scale), v=deq(kv.v, kv.v_scale), block_table=kv.block_table,
+                     seq_len=kv.seq_len, dtype="f32")
+    q32 = O.to_f64(grp.q_fa, "bf16").astype(np.float32)
+    qs32 = O.to_f64(grp.q_sa[0], "bf16").astype(np.float32)
+    a = O.fa_decode(grp.q_fa, kv, grp.w, grp.k, grp.scale)
+    b = O.fa_decode(q32, kv32, grp.w, grp.k, grp.scale)
+    assert np.allclose(a[0], b[0], atol=1e-12) and np.array_equal(a[2], b[2])
+    sa = O.sa_decode(grp.q_sa[0], kv, grp.w, a[2], a[3], grp.scale)
+    sb = O.sa_decode(qs32, kv32, grp.w, a[2], a[3], grp.scale)
+    assert np.allclose(sa, sb, atol=1e-12)

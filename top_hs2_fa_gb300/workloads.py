@@ -48,6 +48,30 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def _fp8_e4m3_table() -> np.ndarray:
+    """Values of the 127 non-negative finite FP8 E4M3 codes 0x00..0x7E, ascending (the
+    format's magnitude order is its code order): exponent e (bias 7, 0 = subnormal), 3-bit m."""
+    c = np.arange(127)
+    e, m = c >> 3, c & 7
+    return np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+
+
+_E4M3 = _fp8_e4m3_table()
+
+
+def f32_to_fp8_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest FP8 E4M3 value (ties to the even code), saturating at +-448;
+    returns the uint8 codes."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3, a), 1, 126)
+    lo = hi - 1
+    dl, dh = a - _E4M3[lo], _E4M3[hi] - a
+    code = np.where(dl < dh, lo, np.where(dh < dl, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a <= 0.0, 0, code)
+    return (code | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
 def store(x: np.ndarray, dtype: str) -> np.ndarray:
     """Convert float32 values to the storage form of ``dtype``."""
     if dtype == "bf16":
@@ -114,6 +138,8 @@ class PagedKV:
     seq_len: np.ndarray  # int32 [B]
     dtype: str
     page: int = PAGE
+    k_scale: np.ndarray | None = None  # FP8 pools: float32 [num_pages][Hkv], value = code * scale
+    v_scale: np.ndarray | None = None
 
     @property
     def num_pages(self) -> int:
@@ -268,6 +294,27 @@ def decode_group(seq_len, Hq: int, Hkv: int, d: int, w: int, k: int, dtype: str,
     pos = plant_needles(kv, q_fa_vals, needles, w, s_needle) if needles else []
     return DecodeGroup(kv=kv, q_fa=qs[0], q_sa=qs[1:], Hq=Hq, w=w, k=k, scale=1.0 / math.sqrt(d),
                        needles=pos)
+
+
+def quantize_kv_fp8(kv: PagedKV) -> PagedKV:
+    """FP8 E4M3 copy of a paged pool with one scale per (page, KV head) slab for K and for V:
+    scale = max |value| / 448 (1 for an all-zero slab), code = E4M3(value / scale)."""
+    out = {}
+    for name in ("k", "v"):
+        x = values(getattr(kv, name), kv.dtype).astype(np.float64)
+        amax = np.abs(x).max(axis=(2, 3))
+        sc = np.where(amax > 0, amax / 448.0, 1.0).astype(np.float32)
+        out[name] = f32_to_fp8_e4m3(x / sc[:, :, None, None].astype(np.float64))
+        out[name + "_scale"] = sc
+    return PagedKV(k=out["k"], v=out["v"], block_table=kv.block_table, seq_len=kv.seq_len, dtype="fp8", page=kv.page,
+                   k_scale=out["k_scale"], v_scale=out["v_scale"])
+
+
+def decode_group_fp8(seq_len, Hq: int, Hkv: int, d: int, w: int, k: int, seed, **kw) -> DecodeGroup:
+    """The bf16 decode workload with its paged KV stored as FP8 E4M3 (queries stay bf16)."""
+    grp = decode_group(seq_len, Hq, Hkv, d, w, k, "bf16", seed, **kw)
+    grp.kv = quantize_kv_fp8(grp.kv)
+    return grp
 
 
 @dataclass
