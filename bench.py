@@ -138,9 +138,9 @@ class Decode:
     roofline_source = ("top_hs2_fa_gb300/csrc/fa_decode.cu", "top_hs2_fa_gb300/csrc/mma_attn.cuh")
     unit = "queries/s"
 
-    def __init__(self, name, B, t_lo, t_hi, groups, needles, qproj, sel_block=1):
+    def __init__(self, name, B, t_lo, t_hi, groups, needles, qproj, sel_block=1, kv_fp8=False):
         self.name, self.B, self.t_lo, self.t_hi, self.groups = name, B, t_lo, t_hi, groups
-        self.needles, self.qproj, self.sel_block = needles, qproj, sel_block
+        self.needles, self.qproj, self.sel_block, self.kv_fp8 = needles, qproj, sel_block, kv_fp8
         self.Hq, self.Hkv, self.D, self.w, self.k = 32, 4, 128, 128, 1024
 
     def host_setup(self, seed):
@@ -151,8 +151,11 @@ class Decode:
         for gi in range(self.groups):
             s_len, s_grp = np.random.SeedSequence([seed, gi]).spawn(2)
             lens = W.uniform_lengths(self.B, self.t_lo, self.t_hi, s_len)
-            self.host.append(W.decode_group(lens, self.Hq, self.Hkv, self.D, self.w, self.k, "bf16", s_grp,
-                                            n_sa=NSA, needles=self.needles, qproj=self.qproj))
+            grp = W.decode_group(lens, self.Hq, self.Hkv, self.D, self.w, self.k, "bf16", s_grp, n_sa=NSA,
+                                 needles=self.needles, qproj=self.qproj)
+            if self.kv_fp8:  # the same values stored as FP8 E4M3 with per-(page, KV head) scales
+                grp.kv = W.quantize_kv_fp8(grp.kv)
+            self.host.append(grp)
 
     def setup(self, dev, seed):
         import torch
@@ -164,8 +167,10 @@ class Decode:
         fa, total = [], 0
         for grp in self.host:
             kv = grp.kv
-            d = {"kv": hs2.KV(k=up(kv.k, dev, True), v=up(kv.v, dev, True), block_table=up(kv.block_table, dev),
-                              seq_len=up(kv.seq_len, dev)),
+            bf = not self.kv_fp8
+            d = {"kv": hs2.KV(k=up(kv.k, dev, bf), v=up(kv.v, dev, bf), block_table=up(kv.block_table, dev),
+                              seq_len=up(kv.seq_len, dev),
+                              k_scale=None if bf else up(kv.k_scale, dev), v_scale=None if bf else up(kv.v_scale, dev)),
                  "max_t": int(kv.seq_len.max()), "q": [up(x, dev, True) for x in [grp.q_fa, *grp.q_sa]]}
             B = self.B
             d["o"] = [torch.empty((B, self.Hq, self.D), dtype=torch.float32, device=dev) for _ in range(1 + NSA)]
@@ -177,7 +182,8 @@ class Decode:
             d["ws_sa"] = torch.empty(hs2.hs2_sa_reuse_workspace(B, self.Hq, d["kv"], self.w, self.k),
                                      dtype=torch.uint8, device=dev)
             self.dev.append(d)
-            m = C.decode_group_bytes(kv.seq_len, self.Hq, self.Hkv, self.D, self.w, self.k, 2, NSA, kv.max_pages)
+            m = C.decode_group_bytes(kv.seq_len, self.Hq, self.Hkv, self.D, self.w, self.k, 1 if self.kv_fp8 else 2, NSA,
+                                     kv.max_pages)
             fa.append(m["fa"])
             total += m["total"]
         self.alg_per_launch = fa[0]  # the profiled launch is group 0's FA scan
@@ -216,7 +222,8 @@ class Decode:
         return {"workload": self.name, "batch": self.B,
                 "seq_len": f"U[{self.t_lo},{self.t_hi}]" if self.t_lo != self.t_hi else self.t_lo,
                 "groups": self.groups, "Hq": self.Hq, "Hkv": self.Hkv, "head_dim": self.D, "window": self.w,
-                "top_k": self.k, "sa_layers_per_group": NSA, "page": 64, "kv_dtype": "bf16",
+                "top_k": self.k, "sa_layers_per_group": NSA, "page": 64,
+                "kv_dtype": "fp8_e4m3 (scale per page and KV head)" if self.kv_fp8 else "bf16",
                 "selection": "token" if self.sel_block == 1 else f"blocks of {self.sel_block}"}
 
     def oracle_sample(self, budget_s):
@@ -230,6 +237,7 @@ class Decode:
             for grp in self.host:
                 kv, sel = grp.kv, [done]
                 sub = W.PagedKV(k=kv.k, v=kv.v, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel],
+                                k_scale=kv.k_scale, v_scale=kv.v_scale,
                                 dtype=kv.dtype, page=kv.page)
                 _, _, idx, cnt = O.fa_decode(grp.q_fa[sel], sub, self.w, self.k, grp.scale, blk=self.sel_block)
                 for j in range(NSA):
@@ -432,6 +440,8 @@ SCENARIOS = {
     "long_decode": lambda: Decode("long_decode_bf16_b16_t131072_x4", 16, 131072, 131072, 4, 64, False),
     # the decode workload with HySparse's first-version block-level selection (16 blocks of 64)
     "decode_block": lambda: Decode("decode_bf16_b64_t16k-32k_block64", 64, 16384, 32768, 1, 32, True, sel_block=64),
+    # the decode workload with its cache stored as FP8 E4M3 (queries bf16)
+    "decode_fp8": lambda: Decode("decode_fp8kv_b64_t16k-32k", 64, 16384, 32768, 1, 32, True, kv_fp8=True),
     "prefill": lambda: Prefill(32768),
     "csa2": lambda: Csa2(),
 }

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define HS2_ABI_VERSION 1
+#define HS2_ABI_VERSION 2
 
 typedef enum {
   HS2_OK = 0,
@@ -67,7 +67,7 @@ typedef enum {
 #define HS2_DEV_SELECT 16     /* a prefill row's streamed candidates could not prove its top-k
                                  (its idx_cnt is written as -1); see hs2_fa_select */
 
-typedef enum { HS2_F32 = 0, HS2_BF16 = 1 } hs2_dtype;
+typedef enum { HS2_F32 = 0, HS2_BF16 = 1, HS2_FP8_E4M3 = 2 } hs2_dtype;
 
 /* Paged KV of ONE group, shared by its FA and SA layers ([HS2] §5, §7.2).
  * k, v:        [num_pages][Hkv][page_size][d] elements of `dtype`, 16-byte aligned.
@@ -75,6 +75,9 @@ typedef enum { HS2_F32 = 0, HS2_BF16 = 1 } hs2_dtype;
  * block_table: int32 [batch][max_pages]; entry j of sequence b is the physical page
  *              holding logical positions [j*page_size, (j+1)*page_size).
  * seq_len:     int32 [batch], keys visible to the query (its own included), >= 1.
+ * k_scale, v_scale: HS2_FP8_E4M3 only (else NULL): float32 [num_pages][Hkv]; a stored
+ *              E4M3 code c of page p, KV head g stands for c * scale[p][g]. An FP8 cache is
+ *              read by hs2_fa_select (decode) and hs2_sa_reuse (decode); queries are bf16.
  * page_size must be 64; d must be 64 or 128.                                        */
 typedef struct {
   const void* k;
@@ -88,6 +91,8 @@ typedef struct {
   int32_t Hkv;
   int32_t d;
   hs2_dtype dtype;
+  const float* k_scale;
+  const float* v_scale;
 } hs2_kv;
 
 /* ---------------------------------------------------------------------------

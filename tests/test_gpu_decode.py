@@ -26,17 +26,22 @@ def H():
     return hs2
 
 
+def qdt(kv):
+    """Storage dtype of the queries: bf16 for an FP8 cache, else the cache's dtype."""
+    return "bf16" if kv.dtype == "fp8" else kv.dtype
+
+
 def run_decode_group(H, grp, sa_layers=None):
     import torch
 
     kv = grp.kv
     dkv = kv_to_device(kv)
-    q = to_torch(grp.q_fa, kv.dtype)
+    q = to_torch(grp.q_fa, qdt(kv))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     o, lse, idx, cnt = H.hs2_fa_select(q, dkv, grp.w, grp.k, grp.scale, max_t=int(kv.seq_len.max()), dev_err=err)
     sa = []
     for j in range(len(grp.q_sa) if sa_layers is None else sa_layers):
-        qs = to_torch(grp.q_sa[j], kv.dtype)
+        qs = to_torch(grp.q_sa[j], qdt(kv))
         sa.append(H.hs2_sa_reuse(qs, dkv, grp.w, idx, cnt, grp.k, grp.scale, dev_err=err).cpu().numpy())
     torch.cuda.synchronize()
     return o.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy(), cnt.cpu().numpy(), sa, int(err.item())
@@ -48,10 +53,10 @@ def check_group(H, grp, batches=None, sa_layers=None):
     assert err == 0, f"device error flags {err}"
     sel = list(range(kv.B)) if batches is None else list(batches)
     sub = W.PagedKV(k=kv.k, v=kv.v, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel], dtype=kv.dtype,
-                    page=kv.page)
+                    page=kv.page, k_scale=kv.k_scale, v_scale=kv.v_scale)
     o_r, lse_r, idx_r, cnt_r, scores = O.fa_decode(grp.q_fa[sel], sub, grp.w, grp.k, grp.scale,
                                                    return_scores=True)
-    t_ = tol(kv.dtype)
+    t_ = tol(qdt(kv))
     assert max_abs(o[sel], o_r) <= t_, f"FA output error {max_abs(o[sel], o_r)}"
     assert max_abs(lse[sel], lse_r) <= t_, f"lse error {max_abs(lse[sel], lse_r)}"
     check_index_sets(idx[sel], cnt[sel], idx_r, cnt_r, scores, "decode ")
@@ -63,7 +68,7 @@ def check_group(H, grp, batches=None, sa_layers=None):
         # ... and with the oracle's index sets fed to both
         import torch
         dkv = kv_to_device(sub)
-        o2 = H.hs2_sa_reuse(to_torch(grp.q_sa[0][sel], kv.dtype), dkv, grp.w, to_torch(idx_r, "i32"),
+        o2 = H.hs2_sa_reuse(to_torch(grp.q_sa[0][sel], qdt(kv)), dkv, grp.w, to_torch(idx_r, "i32"),
                             to_torch(cnt_r, "i32"), grp.k, grp.scale).cpu().numpy()
         ref2 = O.sa_decode(grp.q_sa[0][sel], sub, grp.w, idx_r, cnt_r, grp.scale)
         assert max_abs(o2, ref2) <= t_
@@ -232,3 +237,21 @@ def test_block_level_selection_rejects_bad_sizes(H):
         H.hs2_fa_select(q, dkv, 16, 96, grp.scale, max_t=300, sel_block=64)  # k not a multiple
     with pytest.raises(H.HS2Error):
         H.hs2_fa_select(q, dkv, 16, 96, grp.scale, max_t=300, sel_block=6)  # not a multiple of 4
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 4, 128), (8, 8, 64), (32, 1, 128)])
+def test_fp8_kv_decode(H, Hq, Hkv, d):
+    """FP8 E4M3 cache (one scale per page and KV head): FA output, lse and index sets against
+    the oracle on the same codes and scales, and the SA layers over them."""
+    grp = W.decode_group_fp8([3000, 1700, 130, 5000], Hq, Hkv, d, 64, 256, seed=23, n_sa=2, needles=8)
+    check_group(H, grp)
+
+
+def test_fp8_kv_rejects_prefill(H):
+    import torch
+
+    grp = W.prefill_group(300, 8, 1, 128, w=16, k=32, dtype="bf16", seed=24, n_sa=0)
+    kv = W.quantize_kv_fp8(grp.kv)
+    with pytest.raises(H.HS2Error):
+        H.hs2_fa_select(to_torch(grp.q_fa, "bf16"), kv_to_device(kv), 16, 32, grp.scale, prefill=True)
+    torch.cuda.synchronize()

@@ -47,7 +47,8 @@ bool valid_kv(const hs2_kv* kv, bool need_v) {
   if (kv->batch < 1 || kv->num_pages < 1 || kv->max_pages < 1 || kv->Hkv < 1) return false;
   if (kv->page_size != 64) return false;
   if (kv->d != 64 && kv->d != 128) return false;
-  if (kv->dtype != HS2_F32 && kv->dtype != HS2_BF16) return false;
+  if (kv->dtype != HS2_F32 && kv->dtype != HS2_BF16 && kv->dtype != HS2_FP8_E4M3) return false;
+  if (kv->dtype == HS2_FP8_E4M3 && (!kv->k_scale || (need_v && !kv->v_scale))) return false;
   if (!aligned16(kv->k) || (need_v && !aligned16(kv->v))) return false;
   return true;
 }
@@ -66,7 +67,7 @@ struct FaPlan {
 FaPlan fa_plan(int Bq, int Hq, const hs2_kv* kv, int max_t) {
   FaPlan p{};
   const int G = Hq / kv->Hkv;
-  p.mma = kv->dtype == HS2_BF16 && G <= 32 && (G <= 8 || G == 16 || G == 32);
+  p.mma = (kv->dtype == HS2_BF16 || kv->dtype == HS2_FP8_E4M3) && G <= 32 && (G <= 8 || G == 16 || G == 32);
   const int maxpg = cdiv(max_t, 64);
   if (p.mma) {
     // enough CTAs to fill 152 SMs several times over, splits of at most 16 pages
@@ -105,7 +106,8 @@ SaPlan sa_plan(int Bq, int Hq, const hs2_kv* kv, int w, int k, int prefill) {
   const int G = Hq / kv->Hkv;
   const bool bf16 = kv->dtype == HS2_BF16;
   size_t off = 0;
-  if (!prefill && hs2::sa_stream_plan(G, kv->d, bf16, w, k, Bq, kv->Hkv, &p.sp, &p.grid)) {
+  const int kvt = bf16 ? 1 : kv->dtype == HS2_FP8_E4M3 ? 2 : 0;
+  if (!prefill && hs2::sa_stream_plan(G, kv->d, kvt, w, k, Bq, kv->Hkv, &p.sp, &p.grid)) {
     p.stream = true;
     const size_t units = (size_t)Bq * kv->Hkv * p.sp.hg;
     const size_t slots = units * p.sp.maxc * 8;
@@ -368,6 +370,7 @@ hs2_status hs2_fa_select_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv,
   if (sel_block < 1 || sel_block > 4096 || (sel_block > 1 && (sel_block % 4 != 0 || k % sel_block != 0)))
     return HS2_ERR_ARG;
   if (sel_block > 1 && prefill) return HS2_ERR_UNSUPPORTED;
+  if (kv->dtype == HS2_FP8_E4M3 && prefill) return HS2_ERR_UNSUPPORTED;  // FP8 caches: decode only
   if ((long long)max_t > (long long)kv->max_pages * 64) return HS2_ERR_ARG;
   if (prefill && B_or_n > max_t) return HS2_ERR_ARG;
   if (!o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
@@ -402,6 +405,11 @@ hs2_status hs2_fa_select_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv,
   a.part_o = (float*)(ws + p.off_o);
   a.logits = (float*)(ws + p.off_logits);
   a.ld_logits = p.ld;
+  if (kv->dtype == HS2_FP8_E4M3) {
+    if (!p.mma) return HS2_ERR_UNSUPPORTED;
+    a.k_scale = kv->k_scale;
+    a.v_scale = kv->v_scale;
+  }
   a.dev_err = dev_err;
   cudaError_t e = profiled(HS2_STAGE_FA_SCAN, s, [&] {
     return p.mma ? hs2::launch_fa_decode_mma(a, B_or_n, s)
@@ -465,6 +473,7 @@ hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, 
   if (w < 0 || k < 0 || !std::isfinite(scale) || !o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
   if (B_or_n == 0) return HS2_OK;
   const SaPlan p = sa_plan(B_or_n, Hq, kv, w, k, prefill);
+  if (kv->dtype == HS2_FP8_E4M3 && !p.stream) return HS2_ERR_UNSUPPORTED;  // FP8: the decode stream only
   if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   char* ws = (char*)workspace;
@@ -497,6 +506,10 @@ hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, 
   a.out_o = o;
   a.sink = sink;
   a.gate = gate;
+  if (kv->dtype == HS2_FP8_E4M3) {
+    a.k_scale = kv->k_scale;
+    a.v_scale = kv->v_scale;
+  }
   a.dev_err = dev_err;
   if (p.stream) {
     // bf16 decode: one persistent warp stream over all (query, KV head) pairs' entries

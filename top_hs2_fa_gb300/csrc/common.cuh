@@ -72,6 +72,12 @@ HS2_DEVI uint4 ldg_nc_v4_keep(const void* p, uint64_t pol) {
   return r;
 }
 
+HS2_DEVI uint2 ldg_nc_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
 HS2_DEVI void flag_error(int32_t* dev_err, int bits) {
   if (dev_err) atomicOr(dev_err, bits);
 }
@@ -119,6 +125,11 @@ HS2_DEVI void cp_async16_keep(uint32_t s, const void* gmem, bool valid, uint64_t
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(s), "l"(gmem), "r"(n), "l"(pol)
                : "memory");
 }
+// 4-byte global -> shared copy (cp.async.ca); zero-fills when `valid` is false.
+HS2_DEVI void cp_async4(uint32_t s, const void* gmem, bool valid) {
+  const int n = valid ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
 HS2_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 HS2_DEVI void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -136,6 +147,38 @@ HS2_DEVI float sa_norm_factor(float M, float L, float b2) {
 // The SA output's sigmoid gate (same section): out * 1 / (1 + e^-g).
 HS2_DEVI float sa_gate(float g) { return 1.f / (1.f + __expf(-g)); }
 HS2_DEVI float sink_b2(const float* sink, int head) { return sink ? sink[head] * kLog2e : -INFINITY; }
+
+// FP8 E4M3 pairs to f16 pairs (exact: every E4M3 value is an f16 value); element order kept.
+HS2_DEVI uint32_t fp8x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  const uint16_t v = (uint16_t)two_bytes;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+// 8 E4M3 bytes (uint2) to 8 f16 (uint4), element order kept.
+HS2_DEVI uint4 fp8x8_to_f16x8(uint2 b) {
+  return make_uint4(fp8x2_to_f16x2(b.x & 0xFFFFu), fp8x2_to_f16x2(b.x >> 16), fp8x2_to_f16x2(b.y & 0xFFFFu),
+                    fp8x2_to_f16x2(b.y >> 16));
+}
+// (lo, hi) floats to an f16 pair, round to nearest.
+HS2_DEVI uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// bf16 pair to f16 pair (queries of an FP8 cache run the f16 MMA).
+HS2_DEVI uint32_t bf16x2_to_f16x2(uint32_t x) {
+  return pack_f16(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+}
+// m16n8k16 f16 MMA with fp32 accumulate.
+HS2_DEVI void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                            uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 HS2_DEVI uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;

@@ -16,9 +16,12 @@ namespace hs2 {
 // ============================================================================ bf16 split-KV FA
 // Per CTA: one (query, KV head, split of `pps` pages); 4 warps take the split's pages
 // round-robin; per warp step: 16 keys (see mma_attn.cuh for the register mappings).
-template <int D, int NT>
+// FP8 = true: the cache holds E4M3 codes with one scale per (page, KV head); rows load at half
+// the bytes and convert to f16 (exact), the page's K scale multiplies the logits and its V
+// scale the weights entering P.V (mma_attn.cuh, F16 mode).
+template <int D, int NT, bool FP8>
 __global__ void __launch_bounds__(128) fa_decode_mma_kernel(const AttnArgs a) {
-  using Attn = MmaAttn<D, NT>;
+  using Attn = MmaAttn<D, NT, FP8>;
   constexpr int KC = Attn::KC, VC = Attn::VC;
   const int qi = blockIdx.z, g = blockIdx.y, split = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -49,8 +52,16 @@ __global__ void __launch_bounds__(128) fa_decode_mma_kernel(const AttnArgs a) {
       if (lane == 0) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
       continue;
     }
-    const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(a.k) + ((size_t)phys * a.Hkv + g) * head_stride;
-    const __nv_bfloat16* vp = reinterpret_cast<const __nv_bfloat16*>(a.v) + ((size_t)phys * a.Hkv + g) * head_stride;
+    constexpr int EB = FP8 ? 1 : 2;  // bytes per element
+    const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k) + ((size_t)phys * a.Hkv + g) * head_stride * EB;
+    const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v) + ((size_t)phys * a.Hkv + g) * head_stride * EB;
+    // 8 consecutive elements of a row as 8 bf16 / f16 in a uint4
+    auto ld8 = [&](const uint8_t* base, size_t el) -> uint4 {
+      if (FP8) return fp8x8_to_f16x8(ldg_nc_v2(base + el));
+      return ldg_nc_v4(base + 2 * el);
+    };
+    const float ks = FP8 ? a.k_scale[(size_t)phys * a.Hkv + g] : 1.f;
+    const float vs = FP8 ? a.v_scale[(size_t)phys * a.Hkv + g] : 1.f;
 #pragma unroll 1
     for (int ch = 0; ch < 4; ++ch) {
       const int key0 = page * kPage + ch * 16;
@@ -59,14 +70,14 @@ __global__ void __launch_bounds__(128) fa_decode_mma_kernel(const AttnArgs a) {
       uint4 kr0[KC], kr1[KC], vr[4][VC];
 #pragma unroll
       for (int j = 0; j < KC; ++j) {
-        kr0[j] = ldg_nc_v4(kp + (size_t)r0 * D + 32 * j + 8 * tig);
-        kr1[j] = ldg_nc_v4(kp + (size_t)(r0 + 8) * D + 32 * j + 8 * tig);
+        kr0[j] = ld8(kp, (size_t)r0 * D + 32 * j + 8 * tig);
+        kr1[j] = ld8(kp, (size_t)(r0 + 8) * D + 32 * j + 8 * tig);
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int vrow = ch * 16 + 2 * tig + (e & 1) + 8 * (e >> 1);
 #pragma unroll
-        for (int j = 0; j < VC; ++j) vr[e][j] = ldg_nc_v4(vp + (size_t)vrow * D + (D / 8) * gid + 8 * j);
+        for (int j = 0; j < VC; ++j) vr[e][j] = ld8(vp, (size_t)vrow * D + (D / 8) * gid + 8 * j);
       }
       if (key0 + 16 > t) {  // rows past t: never read their values
 #pragma unroll
@@ -80,7 +91,7 @@ __global__ void __launch_bounds__(128) fa_decode_mma_kernel(const AttnArgs a) {
       const int keyA = key0 + gid, keyB = key0 + gid + 8;
       const bool okA = keyA < t, okB = keyB < t;
       float x[NT][4];
-      at.step(kr0, kr1, vr, okA, okB, a.scale_log2, x);
+      at.step(kr0, kr1, vr, okA, okB, a.scale_log2 * ks, x, vs);
       if (logit_base) {  // base-2 logits for the selection
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -123,7 +134,7 @@ template <int D, int NT>
 static cudaError_t launch_mma(const AttnArgs& a, int Bq, cudaStream_t s) {
   dim3 grid(a.nsplit, a.Hkv, Bq);
   const size_t sm = (size_t)(64 * NT + 32 * NT * D) * sizeof(float);
-  auto kern = fa_decode_mma_kernel<D, NT>;
+  auto kern = a.k_scale ? fa_decode_mma_kernel<D, NT, true> : fa_decode_mma_kernel<D, NT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   kern<<<grid, 128, sm, s>>>(a);

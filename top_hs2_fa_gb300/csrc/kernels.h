@@ -33,6 +33,8 @@ struct AttnArgs {
   float* logits;    // [Bq][Hq][ld_logits] base-2 logits, or null
   float* out_o;     // [Bq][Hq][D] final output (kernels that normalise in place)
   int32_t* arrive;  // SA stream: per-unit arrival counters, zero at launch
+  const float* k_scale;  // FP8 cache: [num_pages][Hkv] dequantisation scales, else null
+  const float* v_scale;
   const float* sink;  // SA: [Hq] sink logits (natural log), or null
   const float* gate;  // SA: [Bq][Hq][D] output gate logits, or null
   long long ld_logits;
@@ -149,7 +151,7 @@ cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s);
 bool sa_mma_supported(int G, int D, int bf16, int w, int k);
 // Decode: plan the warp stream on the current device (false if it does not apply);
 // a.part_ml / a.part_o hold [units][maxc][8] partials and a.arrive [units] zeroed counters.
-bool sa_stream_plan(int G, int D, int bf16, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid);
+bool sa_stream_plan(int G, int D, int kv_dtype, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid);
 cudaError_t launch_sa_stream(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s);
 cudaError_t launch_sa_mma(const AttnArgs& a, int Bq, cudaStream_t s);
 size_t lightning_scan_smem();

@@ -11,12 +11,15 @@
 //    m-tile mt, row hi <-> d = (D/8)*gid + 2mt + hi. P^T fragments come from the S^T
 //    accumulators through an 8x8 movmatrix transpose.
 // Softmax is base 2; the normaliser sums the bf16-rounded weights that enter P.V.
+// F16 = true (an FP8 cache, converted to f16 on load): queries are converted from bf16 to
+// f16 once, both contractions run on the f16 MMA, and P enters P.V as f16(p * pscale) with
+// the caller's per-step V scale; the normaliser then sums p itself (fp32).
 #pragma once
 #include "common.cuh"
 
 namespace hs2 {
 
-template <int D, int NT>
+template <int D, int NT, bool F16 = false>
 struct MmaAttn {
   static constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of PV
   static constexpr int KC = D / 32;  // 16-byte K chunks per lane and row
@@ -38,6 +41,10 @@ struct MmaAttn {
         const int base = 32 * (s >> 1) + 8 * tig + 4 * (s & 1);
         qb[s][nt][0] = hv ? qrow[base / 2] : 0u;
         qb[s][nt][1] = hv ? qrow[base / 2 + 1] : 0u;
+        if (F16) {
+          qb[s][nt][0] = bf16x2_to_f16x2(qb[s][nt][0]);
+          qb[s][nt][1] = bf16x2_to_f16x2(qb[s][nt][1]);
+        }
       }
       m[nt][0] = m[nt][1] = -INFINITY;
       l[nt][0] = l[nt][1] = 0.f;
@@ -49,8 +56,14 @@ struct MmaAttn {
   // K rows gid (kr0) and gid+8 (kr1); V keys 2tig, 2tig+1, 2tig+8, 2tig+9 (vr, zeroed when
   // invalid); okA / okB mask keys gid / gid+8. x receives the scaled base-2 logits
   // (x[nt][0..1]: key gid, heads 2tig, 2tig+1; x[nt][2..3]: key gid+8), -inf when masked.
+  HS2_DEVI static void mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                           uint32_t b1) {
+    if (F16) mma_f16_16816(c, a0, a1, a2, a3, b0, b1);
+    else mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
+  }
+
   HS2_DEVI void step(const uint4 (&kr0)[KC], const uint4 (&kr1)[KC], const uint4 (&vr)[4][VC], bool okA, bool okB,
-                     float scale_log2, float (&x)[NT][4]) {
+                     float scale_log2, float (&x)[NT][4], float pscale = 1.f) {
     float sc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -62,7 +75,7 @@ struct MmaAttn {
         const uint32_t a2 = u ? kr0[j].w : kr0[j].y;
         const uint32_t a1 = u ? kr1[j].z : kr1[j].x;
         const uint32_t a3 = u ? kr1[j].w : kr1[j].y;
-        mma_bf16_16816(sc[nt], a0, a1, a2, a3, qb[s][nt][0], qb[s][nt][1]);
+        mma(sc[nt], a0, a1, a2, a3, qb[s][nt][0], qb[s][nt][1]);
       }
     }
     uint32_t pb[NT][2];
@@ -91,10 +104,18 @@ struct MmaAttn {
           acc[mt][nt][hs + 2] *= alpha;
         }
       }
-      const uint32_t pA = pack_bf16(p[0], p[1]);  // key gid,   heads 2tig, 2tig+1
-      const uint32_t pB = pack_bf16(p[2], p[3]);  // key gid+8
-      l[nt][0] += bf16_lo(pA) + bf16_lo(pB);
-      l[nt][1] += bf16_hi(pA) + bf16_hi(pB);
+      uint32_t pA, pB;  // key gid / gid+8, heads 2tig, 2tig+1
+      if (F16) {
+        pA = pack_f16(p[0] * pscale, p[1] * pscale);
+        pB = pack_f16(p[2] * pscale, p[3] * pscale);
+        l[nt][0] += p[0] + p[2];
+        l[nt][1] += p[1] + p[3];
+      } else {
+        pA = pack_bf16(p[0], p[1]);
+        pB = pack_bf16(p[2], p[3]);
+        l[nt][0] += bf16_lo(pA) + bf16_lo(pB);
+        l[nt][1] += bf16_hi(pA) + bf16_hi(pB);
+      }
       pb[nt][0] = movmatrix_trans(pA);
       pb[nt][1] = movmatrix_trans(pB);
     }
@@ -108,7 +129,7 @@ struct MmaAttn {
       const uint32_t a2 = __byte_perm(v2, v3, 0x5410);
       const uint32_t a3 = __byte_perm(v2, v3, 0x7632);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+      for (int nt = 0; nt < NT; ++nt) mma(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
     }
   }
 

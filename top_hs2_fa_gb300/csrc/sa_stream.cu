@@ -37,24 +37,40 @@ constexpr uint32_t str_slot_bytes() {  // 16 K rows and 16 V rows
   return 2u * (D / 64) * 2048u;
 }
 template <int D>
-constexpr size_t str_warp_bytes() {  // ring + row ids + step table
-  return (size_t)kStrStages * str_slot_bytes<D>() + (kStrMaxSteps * 16 + 6 * kStrMaxSteps) * sizeof(int32_t);
+constexpr uint32_t str_slot8_bytes() {  // FP8: 16 K rows, 16 V rows (D bytes each), 16 + 16 scales
+  return 2u * 16u * D + 128u;
 }
-template <int D>
+template <int D, bool FP8>
+constexpr uint32_t str_ring_bytes() {  // per warp, a multiple of 1024
+  return FP8 ? (str_slot_bytes<D>() + kStrStages * str_slot8_bytes<D>() + 1023u) / 1024u * 1024u
+             : kStrStages * str_slot_bytes<D>();
+}
+template <int D, bool FP8>
+constexpr size_t str_warp_bytes() {  // ring + row ids + step table
+  return (size_t)str_ring_bytes<D, FP8>() + (kStrMaxSteps * 16 + 6 * kStrMaxSteps) * sizeof(int32_t);
+}
+template <int D, bool FP8>
 constexpr size_t str_smem_bytes() {
-  return 1024 + 4 * str_warp_bytes<D>();
+  return 1024 + 4 * str_warp_bytes<D, FP8>();
 }
 
 // Warp holding global step s when `total` steps are cut into `nw` equal ranges
 // [floor(total*w/nw), floor(total*(w+1)/nw)) (every range non-empty when nw <= total).
 HS2_DEVI int warp_of_step(long long s, long long total, int nw) { return (int)(((s + 1) * nw - 1) / total); }
 
-template <int D>
+// FP8 = true: the cache holds E4M3 codes with one scale per (page, KV head). A warp's ring then
+// holds raw slots (the 16 K and 16 V rows at D bytes each, plus each entry's K and V scale,
+// staged by cp.async) and one f16 slot: every step converts its raw slot into the f16 slot
+// (exact, the same swizzled layout) and computes from there with per-entry scales.
+template <int D, bool FP8>
 __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const SaStreamArgs sp) {
   constexpr int NT = 1;  // 8 query heads per unit
   constexpr int HALVES = D / 64;
-  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  constexpr int CPR = D / 8;  // 16-byte chunks per bf16 / f16 row
+  constexpr int CP8 = D / 16;  // 16-byte chunks per FP8 row
   constexpr uint32_t kSlot = str_slot_bytes<D>();
+  constexpr uint32_t kSlot8 = str_slot8_bytes<D>();
+  constexpr uint32_t kRing = str_ring_bytes<D, FP8>();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int wid = blockIdx.x * 4 + warp;
@@ -67,8 +83,9 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  const uint32_t ring = base + (uint32_t)warp * kStrStages * kSlot;
-  int32_t* rowid = reinterpret_cast<int32_t*>(smem_raw + (base - raw) + 4 * (size_t)kStrStages * kSlot) +
+  const uint32_t ring = base + (uint32_t)warp * kRing;  // bf16: the slots; FP8: the f16 slot, then raw slots
+  uint8_t* ring_g = smem_raw + (base - raw) + (size_t)warp * kRing;  // the same bytes, generic address
+  int32_t* rowid = reinterpret_cast<int32_t*>(smem_raw + (base - raw) + 4 * (size_t)kRing) +
                    warp * (kStrMaxSteps * 16 + 6 * kStrMaxSteps);
   int32_t* st_p = rowid + kStrMaxSteps * 16;  // step table: unit, step within the unit,
   int32_t* st_i = st_p + kStrMaxSteps;         // t, sequence, |W|, |S|
@@ -161,6 +178,25 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
   // the group's SA layers re-read the same rows: ask L2 to keep them
   const uint64_t keep = l2_keep_policy();
   auto issue = [&](int j, int slot) {
+    if (FP8) {
+      const uint32_t dst = ring + kSlot + (uint32_t)slot * kSlot8;
+      const uint8_t* kb8 = reinterpret_cast<const uint8_t*>(a.k);
+      const uint8_t* vb8 = reinterpret_cast<const uint8_t*>(a.v);
+#pragma unroll
+      for (int m = 0; m < 16 * CP8 / 32; ++m) {
+        const int c = lane + 32 * m;
+        const int r = c / CP8, cc = c % CP8;
+        const int rid = rowid[16 * j + r];
+        const size_t off = (size_t)(rid >= 0 ? rid : 0) * D + 16 * cc;
+        cp_async16_keep(dst + r * D + 16 * cc, kb8 + off, rid >= 0, keep);
+        cp_async16_keep(dst + 16 * D + r * D + 16 * cc, vb8 + off, rid >= 0, keep);
+      }
+      // lanes 0-15: the entries' K scales, lanes 16-31: their V scales (page-head = row id / 64)
+      const int rid = rowid[16 * j + (lane & 15)];
+      const float* src = (lane < 16 ? a.k_scale : a.v_scale) + (rid >= 0 ? (rid >> 6) : 0);
+      cp_async4(dst + 32 * D + 4 * lane, src, rid >= 0);
+      return;
+    }
     const uint32_t dst = ring + (uint32_t)slot * kSlot;
 #pragma unroll
     for (int m = 0; m < 16 * CPR / 32; ++m) {
@@ -178,7 +214,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
     if (j < ns) issue(j, j);
     cp_async_commit();
   }
-  StagedAttn<D, 1> at;
+  StagedAttn<D, 1, FP8> at;
   int cur_p = -1;
   for (int j = 0; j < ns; ++j) {
     if (j + kStrStages - 1 < ns) issue(j + kStrStages - 1, (j + kStrStages - 1) % kStrStages);
@@ -193,7 +229,31 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
       cur_p = un;
     }
     const bool okA = rowid[16 * j + gid] >= 0, okB = rowid[16 * j + gid + 8] >= 0;
-    if (__any_sync(0xffffffffu, okA || okB)) at.step(ring + (uint32_t)(j % kStrStages) * kSlot, okA, okB, a.scale_log2);
+    if (FP8) {
+      // raw slot -> f16 slot: a 16-byte FP8 chunk (16 values of row r) becomes two f16 chunks
+      const uint8_t* src = ring_g + kSlot + (size_t)(j % kStrStages) * kSlot8;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {  // K, V
+#pragma unroll
+        for (int m = 0; m < 16 * CP8 / 32; ++m) {
+          const int c = lane + 32 * m;
+          const int r = c / CP8, cc = c % CP8;
+          const uint4 raw8 = *reinterpret_cast<const uint4*>(src + part * 16 * D + r * D + 16 * cc);
+          const uint4 lo = fp8x8_to_f16x8(make_uint2(raw8.x, raw8.y));
+          const uint4 hi = fp8x8_to_f16x8(make_uint2(raw8.z, raw8.w));
+          const int f0 = 2 * cc, f1 = 2 * cc + 1;  // f16 chunk indices of the row
+          uint8_t* dst = ring_g + part * HALVES * 2048;
+          *reinterpret_cast<uint4*>(dst + (f0 >> 3) * 2048 + sw128(r, f0 & 7)) = lo;
+          *reinterpret_cast<uint4*>(dst + (f1 >> 3) * 2048 + sw128(r, f1 & 7)) = hi;
+        }
+      }
+      __syncwarp();
+      const float* scl = reinterpret_cast<const float*>(src + 32 * D);
+      if (__any_sync(0xffffffffu, okA || okB))
+        at.step(ring, okA, okB, a.scale_log2, scl[gid], scl[gid + 8], scl[16 + gid], scl[16 + gid + 8]);
+    } else if (__any_sync(0xffffffffu, okA || okB)) {
+      at.step(ring + (uint32_t)(j % kStrStages) * kSlot, okA, okB, a.scale_log2);
+    }
     __syncwarp();
     if (i != ms - 1 && j != ns - 1) continue;
 
@@ -308,13 +368,15 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
   cp_async_wait<0>();
 }
 
-template <int D>
+template <int D, bool FP8>
 static bool stream_plan_t(int G, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
   int dev = 0, sms = 0, per_sm = 0;
-  const size_t sm = str_smem_bytes<D>();
+  const size_t sm = str_smem_bytes<D, FP8>();
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaFuncSetAttribute(sa_stream_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sa_stream_kernel<D>, 128, sm) != cudaSuccess || per_sm < 1) {
+      cudaFuncSetAttribute(sa_stream_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sa_stream_kernel<D, FP8>, 128, sm) != cudaSuccess ||
+      per_sm < 1) {
     (void)cudaGetLastError();
     return false;
   }
@@ -342,18 +404,29 @@ static bool stream_plan_t(int G, int w, int k, int Bq, int Hkv, SaStreamArgs* sp
   return true;
 }
 
-bool sa_stream_plan(int G, int D, int bf16, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
-  if (!bf16 || (D != 64 && D != 128) || G < 1 || G > 32) return false;
-  return D == 128 ? stream_plan_t<128>(G, w, k, Bq, Hkv, sp, grid) : stream_plan_t<64>(G, w, k, Bq, Hkv, sp, grid);
+// kv_dtype: 1 bf16, 2 FP8 E4M3 (others: not this kernel)
+bool sa_stream_plan(int G, int D, int kv_dtype, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
+  if ((kv_dtype != 1 && kv_dtype != 2) || (D != 64 && D != 128) || G < 1 || G > 32) return false;
+  if (kv_dtype == 2)
+    return D == 128 ? stream_plan_t<128, true>(G, w, k, Bq, Hkv, sp, grid)
+                    : stream_plan_t<64, true>(G, w, k, Bq, Hkv, sp, grid);
+  return D == 128 ? stream_plan_t<128, false>(G, w, k, Bq, Hkv, sp, grid)
+                  : stream_plan_t<64, false>(G, w, k, Bq, Hkv, sp, grid);
+}
+
+template <int D, bool FP8>
+static cudaError_t launch_stream_t(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
+  const size_t sm = str_smem_bytes<D, FP8>();
+  cudaError_t e = cudaFuncSetAttribute(sa_stream_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  sa_stream_kernel<D, FP8><<<grid, 128, sm, s>>>(a, sp);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_sa_stream(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
-  const size_t sm = a.D == 128 ? str_smem_bytes<128>() : str_smem_bytes<64>();
-  auto kern = a.D == 128 ? sa_stream_kernel<128> : sa_stream_kernel<64>;
-  if (a.D != 128 && a.D != 64) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, 128, sm, s>>>(a, sp);
-  return cudaGetLastError();
+  const bool fp8 = a.k_scale != nullptr;
+  if (a.D == 128) return fp8 ? launch_stream_t<128, true>(a, sp, grid, s) : launch_stream_t<128, false>(a, sp, grid, s);
+  if (a.D == 64) return fp8 ? launch_stream_t<64, true>(a, sp, grid, s) : launch_stream_t<64, false>(a, sp, grid, s);
+  return cudaErrorInvalidValue;
 }
 }  // namespace hs2

@@ -28,7 +28,10 @@ HS2_DEVI uint32_t sw128(int row, int chunk) { return (uint32_t)(row * 128 + ((ch
 //   S^T[16 entries x 8 heads] = K[16 x 16 d] Q^T[16 d x 8 heads], k-step s covers d 16s..16s+15
 //   O^T[16 d x 8 heads] += V^T[16 d x 16 entries] P^T[16 entries x 8 heads];
 //   acc[mt][nt][0..1]: d = 16mt + gid, heads nt*8 + 2tig, +1; acc[mt][nt][2..3]: d + 8.
-template <int D, int NT>
+// F16 = true (an FP8 cache converted to f16 when staged): queries become f16 at init, both
+// contractions use the f16 MMA, entries carry their own K scale (on the logits) and V scale
+// (on the weights entering P.V), and the normaliser sums the unscaled weights.
+template <int D, int NT, bool F16 = false>
 struct StagedAttn {
   static constexpr int KS = D / 16;
   static constexpr int HALVES = D / 64;
@@ -47,6 +50,10 @@ struct StagedAttn {
       for (int s = 0; s < KS; ++s) {
         qb[s][nt][0] = hv ? qrow[8 * s + tig] : 0u;
         qb[s][nt][1] = hv ? qrow[8 * s + 4 + tig] : 0u;
+        if (F16) {
+          qb[s][nt][0] = bf16x2_to_f16x2(qb[s][nt][0]);
+          qb[s][nt][1] = bf16x2_to_f16x2(qb[s][nt][1]);
+        }
       }
       m[nt][0] = m[nt][1] = -INFINITY;
       l[nt][0] = l[nt][1] = 0.f;
@@ -57,7 +64,15 @@ struct StagedAttn {
 
   // slot: shared address of the staged entries; okA / okB: entries gid / gid+8 are valid.
   // Invalid entries must be staged as zero rows (their weight is zero, and so is V).
-  HS2_DEVI void step(uint32_t slot, bool okA, bool okB, float scale_log2) {
+  HS2_DEVI static void mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                           uint32_t b1) {
+    if (F16) mma_f16_16816(c, a0, a1, a2, a3, b0, b1);
+    else mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
+  }
+
+  // F16 mode: ksA / ksB scale the logits of entries gid / gid+8, vsA / vsB their weights.
+  HS2_DEVI void step(uint32_t slot, bool okA, bool okB, float scale_log2, float ksA = 1.f, float ksB = 1.f,
+                     float vsA = 1.f, float vsB = 1.f) {
     const int lane = threadIdx.x & 31;
     const int mi = lane >> 3, rr = lane & 7;
     float sc[NT][4];
@@ -72,17 +87,17 @@ struct StagedAttn {
         uint32_t a[4];
         ldsm_x4(slot + (d0 >> 6) * 2048 + sw128(row, (d0 & 63) >> 3), a);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a[0], a[1], a[2], a[3], qb[s][nt][0], qb[s][nt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma(sc[nt], a[0], a[1], a[2], a[3], qb[s][nt][0], qb[s][nt][1]);
       }
     }
     uint32_t pb[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float x[4];
-      x[0] = okA ? sc[nt][0] * scale_log2 : -INFINITY;
-      x[1] = okA ? sc[nt][1] * scale_log2 : -INFINITY;
-      x[2] = okB ? sc[nt][2] * scale_log2 : -INFINITY;
-      x[3] = okB ? sc[nt][3] * scale_log2 : -INFINITY;
+      x[0] = okA ? sc[nt][0] * (scale_log2 * ksA) : -INFINITY;
+      x[1] = okA ? sc[nt][1] * (scale_log2 * ksA) : -INFINITY;
+      x[2] = okB ? sc[nt][2] * (scale_log2 * ksB) : -INFINITY;
+      x[3] = okB ? sc[nt][3] * (scale_log2 * ksB) : -INFINITY;
       float p[4];
 #pragma unroll
       for (int hs = 0; hs < 2; ++hs) {
@@ -102,10 +117,18 @@ struct StagedAttn {
           acc[mt][nt][hs + 2] *= alpha;
         }
       }
-      const uint32_t pA = pack_bf16(p[0], p[1]);  // entry gid,   heads 2tig, 2tig+1
-      const uint32_t pB = pack_bf16(p[2], p[3]);  // entry gid+8
-      l[nt][0] += bf16_lo(pA) + bf16_lo(pB);
-      l[nt][1] += bf16_hi(pA) + bf16_hi(pB);
+      uint32_t pA, pB;  // entry gid / gid+8, heads 2tig, 2tig+1
+      if (F16) {
+        pA = pack_f16(p[0] * vsA, p[1] * vsA);
+        pB = pack_f16(p[2] * vsB, p[3] * vsB);
+        l[nt][0] += p[0] + p[2];
+        l[nt][1] += p[1] + p[3];
+      } else {
+        pA = pack_bf16(p[0], p[1]);
+        pB = pack_bf16(p[2], p[3]);
+        l[nt][0] += bf16_lo(pA) + bf16_lo(pB);
+        l[nt][1] += bf16_hi(pA) + bf16_hi(pB);
+      }
       pb[nt][0] = movmatrix_trans(pA);
       pb[nt][1] = movmatrix_trans(pB);
     }
@@ -120,7 +143,7 @@ struct StagedAttn {
         uint32_t a[4];
         ldsm_x4_t(vbase + (d0 >> 6) * 2048 + sw128(row, (d0 & 63) >> 3), a);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a[0], a[1], a[2], a[3], pb[nt][0], pb[nt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma(acc[mt][nt], a[0], a[1], a[2], a[3], pb[nt][0], pb[nt][1]);
       }
     }
   }

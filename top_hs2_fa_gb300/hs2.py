@@ -16,7 +16,7 @@ import torch
 
 from . import build as _build
 
-F32, BF16 = 0, 1
+F32, BF16, FP8_E4M3 = 0, 1, 2
 FULL, REINDEX = 0, 1
 DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH = 1, 2, 4, 8
 EXPORTS = (
@@ -32,7 +32,7 @@ class hs2_kv(ctypes.Structure):
         ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
         ("seq_len", ctypes.c_void_p), ("batch", ctypes.c_int32), ("num_pages", ctypes.c_int32),
         ("max_pages", ctypes.c_int32), ("page_size", ctypes.c_int32), ("Hkv", ctypes.c_int32),
-        ("d", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("d", ctypes.c_int32), ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
     ]
 
 
@@ -109,21 +109,29 @@ def _stream(stream) -> int:
 class KV:
     """Device tensors of one group's paged KV cache."""
 
-    k: torch.Tensor  # [num_pages][Hkv][64][d], float32 or bfloat16
+    k: torch.Tensor  # [num_pages][Hkv][64][d], float32, bfloat16 or uint8 (FP8 E4M3 codes)
     v: torch.Tensor | None
     block_table: torch.Tensor  # int32 [B][max_pages]
     seq_len: torch.Tensor  # int32 [B]
+    k_scale: torch.Tensor | None = None  # FP8: float32 [num_pages][Hkv]
+    v_scale: torch.Tensor | None = None
 
     def c(self) -> hs2_kv:
-        dt = BF16 if self.k.dtype == torch.bfloat16 else F32
-        if self.k.dtype not in (torch.bfloat16, torch.float32):
+        if self.k.dtype == torch.uint8:
+            dt = FP8_E4M3
+            if self.k_scale is None or (self.v is not None and self.v_scale is None):
+                raise HS2Error("an FP8 KV cache needs k_scale and v_scale")
+        elif self.k.dtype in (torch.bfloat16, torch.float32):
+            dt = BF16 if self.k.dtype == torch.bfloat16 else F32
+        else:
             raise HS2Error(f"unsupported KV dtype {self.k.dtype}")
-        for t in (self.k, self.v, self.block_table, self.seq_len):
+        for t in (self.k, self.v, self.block_table, self.seq_len, self.k_scale, self.v_scale):
             if t is not None and not t.is_contiguous():
                 raise HS2Error("KV tensors must be contiguous")
         return hs2_kv(_ptr(self.k), _ptr(self.v), _ptr(self.block_table), _ptr(self.seq_len),
                       int(self.seq_len.shape[0]), int(self.k.shape[0]), int(self.block_table.shape[1]),
-                      int(self.k.shape[2]), int(self.k.shape[1]), int(self.k.shape[3]), dt)
+                      int(self.k.shape[2]), int(self.k.shape[1]), int(self.k.shape[3]), dt,
+                      _ptr(self.k_scale), _ptr(self.v_scale))
 
 
 def _workspace(nbytes: int, device, ws):

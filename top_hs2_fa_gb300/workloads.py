@@ -301,11 +301,16 @@ def quantize_kv_fp8(kv: PagedKV) -> PagedKV:
     scale = max |value| / 448 (1 for an all-zero slab), code = E4M3(value / scale)."""
     out = {}
     for name in ("k", "v"):
-        x = values(getattr(kv, name), kv.dtype).astype(np.float64)
-        amax = np.abs(x).max(axis=(2, 3))
-        sc = np.where(amax > 0, amax / 448.0, 1.0).astype(np.float32)
-        out[name] = f32_to_fp8_e4m3(x / sc[:, :, None, None].astype(np.float64))
-        out[name + "_scale"] = sc
+        src = getattr(kv, name)
+        codes = np.empty(src.shape, dtype=np.uint8)
+        sc = np.empty(src.shape[:2], dtype=np.float32)
+        for p0 in range(0, src.shape[0], 2048):  # page chunks bound the temporaries
+            x = values(src[p0:p0 + 2048], kv.dtype).astype(np.float64)
+            amax = np.abs(x).max(axis=(2, 3))
+            s_ = np.where(amax > 0, amax / 448.0, 1.0).astype(np.float32)
+            codes[p0:p0 + 2048] = f32_to_fp8_e4m3(x / s_[:, :, None, None].astype(np.float64))
+            sc[p0:p0 + 2048] = s_
+        out[name], out[name + "_scale"] = codes, sc
     return PagedKV(k=out["k"], v=out["v"], block_table=kv.block_table, seq_len=kv.seq_len, dtype="fp8", page=kv.page,
                    k_scale=out["k_scale"], v_scale=out["v_scale"])
 
