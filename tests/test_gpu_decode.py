@@ -247,6 +247,27 @@ def test_fp8_kv_decode(H, Hq, Hkv, d):
     check_group(H, grp)
 
 
+def test_fp8_kv_small_wide_values(H):
+    """FP8 cache whose V slabs are tiny and span four decades (V scales ~1e-9..1e-5): the FA
+    and SA outputs keep their accuracy relative to their own magnitude."""
+    grp = W.decode_group([2600, 900, 4100], 16, 2, 128, 64, 128, "bf16", seed=29, n_sa=1, needles=4)
+    kv = grp.kv
+    rng = np.random.default_rng(31)
+    fac = 1e-4 * 10.0 ** rng.uniform(-2.0, 2.0, size=kv.v.shape[:2])
+    vf = (W.values(kv.v, "bf16") * fac[:, :, None, None]).astype(np.float32)
+    f32 = W.PagedKV(k=W.values(kv.k, "bf16"), v=vf, block_table=kv.block_table, seq_len=kv.seq_len, dtype="f32",
+                    page=kv.page)
+    grp.kv = W.quantize_kv_fp8(f32)
+    o, lse, idx, cnt, sa, err = run_decode_group(H, grp)
+    assert err == 0
+    o_r, lse_r, idx_r, cnt_r, scores = O.fa_decode(grp.q_fa, grp.kv, grp.w, grp.k, grp.scale, return_scores=True)
+    assert max_abs(o, o_r) <= 1e-2 * np.abs(o_r).max(), f"FA relative error {max_abs(o, o_r) / np.abs(o_r).max()}"
+    assert max_abs(lse, lse_r) <= 2e-2
+    check_index_sets(idx, cnt, idx_r, cnt_r, scores, "decode ")
+    ref = O.sa_decode(grp.q_sa[0], grp.kv, grp.w, idx, cnt, grp.scale)
+    assert max_abs(sa[0], ref) <= 1e-2 * np.abs(ref).max(), f"SA relative error {max_abs(sa[0], ref) / np.abs(ref).max()}"
+
+
 def test_fp8_kv_rejects_prefill(H):
     import torch
 

@@ -130,6 +130,7 @@ HS2_DEVI void cp_async4(uint32_t s, const void* gmem, bool valid) {
   const int n = valid ? 4 : 0;
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
 }
+HS2_DEVI void st_shared_s32(uint32_t s, int v) { asm volatile("st.shared.s32 [%0], %1;" ::"r"(s), "r"(v) : "memory"); }
 HS2_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 HS2_DEVI void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -155,10 +156,18 @@ HS2_DEVI uint32_t fp8x2_to_f16x2(uint32_t two_bytes) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
 }
+// 4 E4M3 bytes to two f16 pairs: bytes (0, 1) -> lo, bytes (2, 3) -> hi, element order kept.
+HS2_DEVI void fp8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
 // 8 E4M3 bytes (uint2) to 8 f16 (uint4), element order kept.
 HS2_DEVI uint4 fp8x8_to_f16x8(uint2 b) {
-  return make_uint4(fp8x2_to_f16x2(b.x & 0xFFFFu), fp8x2_to_f16x2(b.x >> 16), fp8x2_to_f16x2(b.y & 0xFFFFu),
-                    fp8x2_to_f16x2(b.y >> 16));
+  uint4 r;
+  fp8x4_to_f16x4(b.x, r.x, r.y);
+  fp8x4_to_f16x4(b.y, r.z, r.w);
+  return r;
 }
 // (lo, hi) floats to an f16 pair, round to nearest.
 HS2_DEVI uint32_t pack_f16(float lo, float hi) {

@@ -1,4 +1,4 @@
-// fa_decode.cu — bf16 split-KV scan of the FA layer (decode and causal rows).
+// fa_decode.cu — bf16 / FP8 split-KV scan of the FA layer (decode and causal rows).
 //
 // The FA layer of a HySparse2 Cross group attends to every visible key of the group's
 // shared paged KV ("HySparse2：整体架构、KV 生命周期与 PD 分离", §5; §16.1: the FA layers
@@ -7,6 +7,8 @@
 // heads of one KV head) runs on mma.sync with the keys as the M dimension, so no MMA
 // row is padding. It writes per-split softmax partials and the base-2 logits that the
 // selection (combine.cu) needs once the per-head normaliser is known.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "mma_attn.cuh"
@@ -19,8 +21,13 @@ namespace hs2 {
 // FP8 = true: the cache holds E4M3 codes with one scale per (page, KV head); rows load at half
 // the bytes and convert to f16 (exact), the page's K scale multiplies the logits and its V
 // scale the weights entering P.V (mma_attn.cuh, F16 mode).
+constexpr int kRing8 = 3;  // FP8 chunk slots per warp
+// one FP8 slot: 16 K rows, 16 V rows, then k scale, v scale, key0 (padded to 16 bytes)
+template <int D>
+constexpr int fa8_slot_bytes() { return 2 * 16 * D + 16; }
+
 template <int D, int NT, bool FP8>
-__global__ void __launch_bounds__(128) fa_decode_mma_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(128, (FP8 && NT == 1) ? 4 : 0) fa_decode_mma_kernel(const AttnArgs a) {
   using Attn = MmaAttn<D, NT, FP8>;
   constexpr int KC = Attn::KC, VC = Attn::VC;
   const int qi = blockIdx.z, g = blockIdx.y, split = blockIdx.x;
@@ -46,69 +53,185 @@ __global__ void __launch_bounds__(128) fa_decode_mma_kernel(const AttnArgs a) {
   const size_t head_stride = (size_t)kPage * D;  // elements per (page, KV head)
   float* logit_base = a.logits ? a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits : nullptr;
 
-  for (int page = page0 + warp; page < page1; page += 4) {
-    const int phys = bt[page];
-    if (phys < 0 || phys >= a.num_pages) {
-      if (lane == 0) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
-      continue;
+  // base-2 logits of one 16-key chunk for the selection
+  auto write_logits = [&](const float (&x)[NT][4], int keyA, int keyB, bool okA, bool okB) {
+    if (!logit_base) return;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h0 = nt * 8 + 2 * tig;
+      if (h0 < G) {
+        if (okA) logit_base[(size_t)h0 * a.ld_logits + keyA] = x[nt][0];
+        if (okB) logit_base[(size_t)h0 * a.ld_logits + keyB] = x[nt][2];
+      }
+      if (h0 + 1 < G) {
+        if (okA) logit_base[(size_t)(h0 + 1) * a.ld_logits + keyA] = x[nt][1];
+        if (okB) logit_base[(size_t)(h0 + 1) * a.ld_logits + keyB] = x[nt][3];
+      }
     }
-    constexpr int EB = FP8 ? 1 : 2;  // bytes per element
-    const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k) + ((size_t)phys * a.Hkv + g) * head_stride * EB;
-    const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v) + ((size_t)phys * a.Hkv + g) * head_stride * EB;
-    // 8 consecutive elements of a row as 8 bf16 / f16 in a uint4
-    auto ld8 = [&](const uint8_t* base, size_t el) -> uint4 {
-      if (FP8) return fp8x8_to_f16x8(ldg_nc_v2(base + el));
-      return ldg_nc_v4(base + 2 * el);
-    };
-    const float ks = FP8 ? a.k_scale[(size_t)phys * a.Hkv + g] : 1.f;
-    const float vs = FP8 ? a.v_scale[(size_t)phys * a.Hkv + g] : 1.f;
+  };
+
+  if constexpr (!FP8) {
+    for (int page = page0 + warp; page < page1; page += 4) {
+      const int phys = bt[page];
+      if (phys < 0 || phys >= a.num_pages) {
+        if (lane == 0) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+        continue;
+      }
+      const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(a.k) + ((size_t)phys * a.Hkv + g) * head_stride;
+      const __nv_bfloat16* vp = reinterpret_cast<const __nv_bfloat16*>(a.v) + ((size_t)phys * a.Hkv + g) * head_stride;
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
-      const int key0 = page * kPage + ch * 16;
-      if (key0 >= t) break;
-      const int r0 = ch * 16 + gid;  // row within the page
-      uint4 kr0[KC], kr1[KC], vr[4][VC];
+      for (int ch = 0; ch < 4; ++ch) {
+        const int key0 = page * kPage + ch * 16;
+        if (key0 >= t) break;
+        const int r0 = ch * 16 + gid;  // row within the page
+        uint4 kr0[KC], kr1[KC], vr[4][VC];
 #pragma unroll
-      for (int j = 0; j < KC; ++j) {
-        kr0[j] = ld8(kp, (size_t)r0 * D + 32 * j + 8 * tig);
-        kr1[j] = ld8(kp, (size_t)(r0 + 8) * D + 32 * j + 8 * tig);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int vrow = ch * 16 + 2 * tig + (e & 1) + 8 * (e >> 1);
-#pragma unroll
-        for (int j = 0; j < VC; ++j) vr[e][j] = ld8(vp, (size_t)vrow * D + (D / 8) * gid + 8 * j);
-      }
-      if (key0 + 16 > t) {  // rows past t: never read their values
+        for (int j = 0; j < KC; ++j) {
+          kr0[j] = ldg_nc_v4(kp + (size_t)r0 * D + 32 * j + 8 * tig);
+          kr1[j] = ldg_nc_v4(kp + (size_t)(r0 + 8) * D + 32 * j + 8 * tig);
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int key = key0 + 2 * tig + (e & 1) + 8 * (e >> 1);
-          if (key >= t)
+          const int vrow = ch * 16 + 2 * tig + (e & 1) + 8 * (e >> 1);
 #pragma unroll
-            for (int j = 0; j < VC; ++j) vr[e][j] = make_uint4(0, 0, 0, 0);
+          for (int j = 0; j < VC; ++j) vr[e][j] = ldg_nc_v4(vp + (size_t)vrow * D + (D / 8) * gid + 8 * j);
         }
+        if (key0 + 16 > t) {  // rows past t: never read their values
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = key0 + 2 * tig + (e & 1) + 8 * (e >> 1);
+            if (key >= t)
+#pragma unroll
+              for (int j = 0; j < VC; ++j) vr[e][j] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        const int keyA = key0 + gid, keyB = key0 + gid + 8;
+        const bool okA = keyA < t, okB = keyB < t;
+        float x[NT][4];
+        at.step(kr0, kr1, vr, okA, okB, a.scale_log2, x);
+        write_logits(x, keyA, keyB, okA, okB);
+      }
+    }
+  } else {
+    // FP8: each warp streams its 16-key chunks through a ring of kRing8 shared-memory slots
+    // filled by 16-byte cp.async copies, so kRing8 - 1 chunks (12 KB at d = 128) are in
+    // flight per warp without holding registers. The 16-byte units of a row are stored
+    // XOR-swizzled by the row, which keeps the fragment reads below free of bank conflicts.
+    constexpr int CB = 16 * D;           // bytes of K (or V) in one chunk
+    constexpr int UPR = D / 16;          // 16-byte units per row
+    constexpr int SLOT = fa8_slot_bytes<D>();
+    const uint32_t ring = (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kRing8 * SLOT);
+    const uint8_t* ring_p = reinterpret_cast<const uint8_t*>(smem) + warp * kRing8 * SLOT;
+    auto swz = [](int row) { return D == 128 ? (row & 7) : ((row >> 1) & 3); };
+    auto unit_off = [&](int row, int c) { return row * D + ((c ^ swz(row)) << 4); };
+    float v_unit = 1.f;  // acc holds P.V in units of this V scale
+
+    // first page >= pg of this warp with a valid block-table entry (bad ones are flagged)
+    auto good_page = [&](int pg, int& phys) {
+      for (; pg < page1; pg += 4) {
+        phys = bt[pg];
+        if (phys >= 0 && phys < a.num_pages) break;
+        if (lane == 0) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+      }
+      return pg;
+    };
+    // copies of chunk (pg, ch) into a slot: K, V, then the page's two scales and key0
+    auto issue = [&](int pg, int phys, int ch, int slot) {
+      const uint32_t sl = ring + slot * SLOT;
+      const size_t ph = (size_t)phys * a.Hkv + g;
+      const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k) + ph * head_stride + (size_t)ch * CB;
+      const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v) + ph * head_stride + (size_t)ch * CB;
+#pragma unroll
+      for (int i = 0; i < CB / 512; ++i) {
+        const int u = lane + 32 * i, off = unit_off(u / UPR, u % UPR);
+        cp_async16(sl + off, kp + 16 * u, true);
+        cp_async16(sl + CB + off, vp + 16 * u, true);
+      }
+      if (lane == 0) cp_async4(sl + 2 * CB, a.k_scale + ph, true);
+      if (lane == 1) cp_async4(sl + 2 * CB + 4, a.v_scale + ph, true);
+      if (lane == 2) st_shared_s32(sl + 2 * CB + 8, pg * kPage + ch * 16);
+    };
+    auto compute = [&](int slot) {
+      const uint8_t* sl = ring_p + slot * SLOT;
+      const float ks = *reinterpret_cast<const float*>(sl + 2 * CB);
+      const float vs = *reinterpret_cast<const float*>(sl + 2 * CB + 4);
+      const int key0 = *reinterpret_cast<const int*>(sl + 2 * CB + 8);
+      if (vs != v_unit && vs != 0.f) {  // acc moves to this page's V scale as its unit
+        at.scale_acc(v_unit / vs);
+        v_unit = vs;
+      }
+      uint4 kr0[KC], kr1[KC];
+#pragma unroll
+      for (int j = 0; j < KC; ++j) {  // 8 bytes of rows gid and gid + 8 at byte 32j + 8tig
+        const int c = 2 * j + (tig >> 1), h = 8 * (tig & 1);
+        kr0[j] = fp8x8_to_f16x8(*reinterpret_cast<const uint2*>(sl + unit_off(gid, c) + h));
+        kr1[j] = fp8x8_to_f16x8(*reinterpret_cast<const uint2*>(sl + unit_off(gid + 8, c) + h));
+      }
+      // V: the lane's D/8 bytes (d = (D/8) * gid ...) of keys 2tig, 2tig+1, 2tig+8, 2tig+9,
+      // as D/32 words per key; rows past t (and a zero V scale) read as zero
+      constexpr int VW = D / 32;
+      uint32_t vw[4][VW];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int vrow = 2 * tig + (e & 1) + 8 * (e >> 1);
+        const bool live = key0 + vrow < t && vs != 0.f;
+        const int b = (D / 8) * gid;
+        const uint8_t* src = sl + CB + unit_off(vrow, b >> 4) + (b & 15);
+        if constexpr (VW == 4) {
+          const uint4 w = *reinterpret_cast<const uint4*>(src);
+          vw[e][0] = live ? w.x : 0u, vw[e][1] = live ? w.y : 0u, vw[e][2] = live ? w.z : 0u, vw[e][3] = live ? w.w : 0u;
+        } else {
+          const uint2 w = *reinterpret_cast<const uint2*>(src);
+          vw[e][0] = live ? w.x : 0u, vw[e][1] = live ? w.y : 0u;
+        }
+      }
+      // V^T A-fragments straight from the bytes: interleave two keys' bytes, then each
+      // byte pair converts to the (key, key + 1) f16 pair of one d
+      uint32_t va[Attn::KS][4];
+#pragma unroll
+      for (int mt = 0; mt < Attn::KS; ++mt) {
+        const int r = mt >> 1;
+        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+        fp8x4_to_f16x4(__byte_perm(vw[0][r], vw[1][r], sel), va[mt][0], va[mt][1]);
+        fp8x4_to_f16x4(__byte_perm(vw[2][r], vw[3][r], sel), va[mt][2], va[mt][3]);
       }
       const int keyA = key0 + gid, keyB = key0 + gid + 8;
       const bool okA = keyA < t, okB = keyB < t;
       float x[NT][4];
-      at.step(kr0, kr1, vr, okA, okB, a.scale_log2 * ks, x, vs);
-      if (logit_base) {  // base-2 logits for the selection
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int h0 = nt * 8 + 2 * tig;
-          if (h0 < G) {
-            if (okA) logit_base[(size_t)h0 * a.ld_logits + keyA] = x[nt][0];
-            if (okB) logit_base[(size_t)h0 * a.ld_logits + keyB] = x[nt][2];
-          }
-          if (h0 + 1 < G) {
-            if (okA) logit_base[(size_t)(h0 + 1) * a.ld_logits + keyA] = x[nt][1];
-            if (okB) logit_base[(size_t)(h0 + 1) * a.ld_logits + keyB] = x[nt][3];
-          }
+      at.step(kr0, kr1, va, okA, okB, a.scale_log2 * ks, x);
+      write_logits(x, keyA, keyB, okA, okB);
+    };
+    // issue cursor (pg, ch) over the warp's chunks: 4 per page, fewer on the last page of t
+    int phys = 0;
+    int pg = good_page(page0 + warp, phys), ch = 0;
+    int issued = 0;
+    auto issue_next = [&]() {
+      if (pg < page1) {
+        issue(pg, phys, ch, issued % kRing8);
+        ++issued;
+        if (ch + 1 < 4 && pg * kPage + (ch + 1) * 16 < t) {
+          ++ch;
+        } else {
+          pg = good_page(pg + 4, phys);
+          ch = 0;
         }
       }
+      cp_async_commit();  // one group per call, empty or not, so the wait count below holds
+    };
+#pragma unroll
+    for (int i = 0; i < kRing8 - 1; ++i) issue_next();
+#pragma unroll 1
+    for (int done = 0; done < issued; ++done) {
+      issue_next();
+      cp_async_wait<kRing8 - 1>();  // this lane's copies of chunk `done` have landed
+      __syncwarp();                 // ... and every lane's
+      compute(done % kRing8);
+      __syncwarp();  // the slot is refilled by the next issue
     }
+    __syncthreads();  // the merge buffers below alias the rings
+    at.store(warp, sm_m, sm_l, sm_o, v_unit);
   }
-  at.store(warp, sm_m, sm_l, sm_o);
+  if constexpr (!FP8) at.store(warp, sm_m, sm_l, sm_o);
   __syncthreads();
   // ---- merge the 4 warps and write this split's partial
   for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
@@ -133,7 +256,8 @@ __global__ void __launch_bounds__(128) fa_decode_mma_kernel(const AttnArgs a) {
 template <int D, int NT>
 static cudaError_t launch_mma(const AttnArgs& a, int Bq, cudaStream_t s) {
   dim3 grid(a.nsplit, a.Hkv, Bq);
-  const size_t sm = (size_t)(64 * NT + 32 * NT * D) * sizeof(float);
+  const size_t merge = (size_t)(64 * NT + 32 * NT * D) * sizeof(float);
+  const size_t sm = a.k_scale ? std::max(merge, (size_t)4 * kRing8 * fa8_slot_bytes<D>()) : merge;
   auto kern = a.k_scale ? fa_decode_mma_kernel<D, NT, true> : fa_decode_mma_kernel<D, NT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;

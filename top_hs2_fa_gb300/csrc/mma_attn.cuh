@@ -10,14 +10,21 @@
 //    the lane holds keys {2tig, 2tig+1, 2tig+8, 2tig+9} at d in [(D/8)gid, (D/8)(gid+1));
 //    m-tile mt, row hi <-> d = (D/8)*gid + 2mt + hi. P^T fragments come from the S^T
 //    accumulators through an 8x8 movmatrix transpose.
-// Softmax is base 2; the normaliser sums the bf16-rounded weights that enter P.V.
+// Softmax is base 2 with a lazily moved running max; the normaliser sums the bf16-rounded
+// weights that enter P.V.
 // F16 = true (an FP8 cache, converted to f16 on load): queries are converted from bf16 to
-// f16 once, both contractions run on the f16 MMA, and P enters P.V as f16(p * pscale) with
-// the caller's per-step V scale; the normaliser then sums p itself (fp32).
+// f16 once, both contractions run on the f16 MMA on the unscaled E4M3 codes, and P enters
+// P.V as f16(p) (p <= 2^8, the codes <= 448: no f16 overflow or underflow of note); the
+// normaliser sums p itself (fp32). The caller keeps acc in units of the current page's V
+// scale (scale_acc when the page changes) and hands the last unit to store().
 #pragma once
 #include "common.cuh"
 
 namespace hs2 {
+
+// Weights are computed against a running max that may lag the true one by up to this
+// much (base 2), i.e. they are at most 2^8: well inside bf16, f16 and fp32 range.
+constexpr float kLazyRescale = 8.f;
 
 template <int D, int NT, bool F16 = false>
 struct MmaAttn {
@@ -62,12 +69,35 @@ struct MmaAttn {
     else mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
   }
 
+  // V^T A-fragments of m-tile mt from the per-key rows: va[mt] = {keys (2tig, 2tig+1) at
+  // d, at d+1; keys (2tig+8, 2tig+9) at d, at d+1}, d = (D/8)*gid + 2mt.
+  HS2_DEVI static void v_frags(const uint4 (&vr)[4][VC], uint32_t (&va)[KS][4]) {
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      const int j = mt >> 2, w4 = mt & 3;
+      const uint32_t v0 = (&vr[0][j].x)[w4], v1 = (&vr[1][j].x)[w4];
+      const uint32_t v2 = (&vr[2][j].x)[w4], v3 = (&vr[3][j].x)[w4];
+      va[mt][0] = __byte_perm(v0, v1, 0x5410);
+      va[mt][1] = __byte_perm(v0, v1, 0x7632);
+      va[mt][2] = __byte_perm(v2, v3, 0x5410);
+      va[mt][3] = __byte_perm(v2, v3, 0x7632);
+    }
+  }
+
   HS2_DEVI void step(const uint4 (&kr0)[KC], const uint4 (&kr1)[KC], const uint4 (&vr)[4][VC], bool okA, bool okB,
-                     float scale_log2, float (&x)[NT][4], float pscale = 1.f) {
+                     float scale_log2, float (&x)[NT][4]) {
+    uint32_t va[KS][4];
+    v_frags(vr, va);
+    step(kr0, kr1, va, okA, okB, scale_log2, x);
+  }
+
+  HS2_DEVI void step(const uint4 (&kr0)[KC], const uint4 (&kr1)[KC], const uint32_t (&va)[KS][4], bool okA,
+                     bool okB, float scale_log2, float (&x)[NT][4]) {
     float sc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      // even and odd k-steps accumulate apart (two independent MMA chains), then add
+      float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int s = 0; s < KS; ++s) {
         const int j = s >> 1, u = s & 1;
@@ -75,8 +105,10 @@ struct MmaAttn {
         const uint32_t a2 = u ? kr0[j].w : kr0[j].y;
         const uint32_t a1 = u ? kr1[j].z : kr1[j].x;
         const uint32_t a3 = u ? kr1[j].w : kr1[j].y;
-        mma(sc[nt], a0, a1, a2, a3, qb[s][nt][0], qb[s][nt][1]);
+        mma(s2[u], a0, a1, a2, a3, qb[s][nt][0], qb[s][nt][1]);
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[nt][i] = s2[0][i] + s2[1][i];
     }
     uint32_t pb[NT][2];
 #pragma unroll
@@ -85,29 +117,42 @@ struct MmaAttn {
       x[nt][1] = okA ? sc[nt][1] * scale_log2 : -INFINITY;
       x[nt][2] = okB ? sc[nt][2] * scale_log2 : -INFINITY;
       x[nt][3] = okB ? sc[nt][3] * scale_log2 : -INFINITY;
-      float p[4];
+      float p[4], cm[2];
+      bool grow = false;
 #pragma unroll
       for (int hs = 0; hs < 2; ++hs) {
-        float cm = fmaxf(x[nt][hs], x[nt][hs + 2]);
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
-        const float mn = fmaxf(m[nt][hs], cm);
-        const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m[nt][hs] - mn);
-        m[nt][hs] = mn;
-        p[hs] = exp2_rel(x[nt][hs], mn);
-        p[hs + 2] = exp2_rel(x[nt][hs + 2], mn);
-        l[nt][hs] *= alpha;
+        cm[hs] = fmaxf(x[nt][hs], x[nt][hs + 2]);
+        cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 4));
+        cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 8));
+        cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 16));
+        grow |= cm[hs] > m[nt][hs] + kLazyRescale;
+      }
+      // Lazy rescale: the running max moves (and l, acc are rescaled) only when a head's
+      // chunk max exceeds it by more than kLazyRescale (base 2), so weights stay <= 2^8;
+      // the final normalisation divides by the same stale max, so the result is unchanged.
+      if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          acc[mt][nt][hs] *= alpha;
-          acc[mt][nt][hs + 2] *= alpha;
+        for (int hs = 0; hs < 2; ++hs) {
+          const float mn = fmaxf(m[nt][hs], cm[hs]);
+          const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m[nt][hs] - mn);
+          m[nt][hs] = mn;
+          l[nt][hs] *= alpha;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            acc[mt][nt][hs] *= alpha;
+            acc[mt][nt][hs + 2] *= alpha;
+          }
         }
+      }
+#pragma unroll
+      for (int hs = 0; hs < 2; ++hs) {
+        p[hs] = exp2_rel(x[nt][hs], m[nt][hs]);
+        p[hs + 2] = exp2_rel(x[nt][hs + 2], m[nt][hs]);
       }
       uint32_t pA, pB;  // key gid / gid+8, heads 2tig, 2tig+1
       if (F16) {
-        pA = pack_f16(p[0] * pscale, p[1] * pscale);
-        pB = pack_f16(p[2] * pscale, p[3] * pscale);
+        pA = pack_f16(p[0], p[1]);
+        pB = pack_f16(p[2], p[3]);
         l[nt][0] += p[0] + p[2];
         l[nt][1] += p[1] + p[3];
       } else {
@@ -120,22 +165,24 @@ struct MmaAttn {
       pb[nt][1] = movmatrix_trans(pB);
     }
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      const int j = mt >> 2, w4 = mt & 3;
-      const uint32_t v0 = (&vr[0][j].x)[w4], v1 = (&vr[1][j].x)[w4];
-      const uint32_t v2 = (&vr[2][j].x)[w4], v3 = (&vr[3][j].x)[w4];
-      const uint32_t a0 = __byte_perm(v0, v1, 0x5410);
-      const uint32_t a1 = __byte_perm(v0, v1, 0x7632);
-      const uint32_t a2 = __byte_perm(v2, v3, 0x5410);
-      const uint32_t a3 = __byte_perm(v2, v3, 0x7632);
+    for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
-    }
+      for (int nt = 0; nt < NT; ++nt) mma(acc[mt][nt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pb[nt][0], pb[nt][1]);
   }
 
-  // Write this warp's (m, l, unnormalised o) for its 8*NT heads to shared memory:
+  // acc *= f (a change of the unit acc is kept in)
+  HS2_DEVI void scale_acc(float f) {
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mt][nt][i] *= f;
+  }
+
+  // Write this warp's (m, l, unnormalised o * unit) for its 8*NT heads to shared memory:
   // sm_m / sm_l [warp][NT*8], sm_o [warp][NT*8][D].
-  HS2_DEVI void store(int warp, float* sm_m, float* sm_l, float* sm_o) const {
+  HS2_DEVI void store(int warp, float* sm_m, float* sm_l, float* sm_o, float unit = 1.f) const {
     const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -153,8 +200,8 @@ struct MmaAttn {
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           const int d0 = (D / 8) * gid + 2 * mt;
-          sm_o[((size_t)warp * NT * 8 + hl) * D + d0] = acc[mt][nt][hs];
-          sm_o[((size_t)warp * NT * 8 + hl) * D + d0 + 1] = acc[mt][nt][hs + 2];
+          sm_o[((size_t)warp * NT * 8 + hl) * D + d0] = acc[mt][nt][hs] * unit;
+          sm_o[((size_t)warp * NT * 8 + hl) * D + d0 + 1] = acc[mt][nt][hs + 2] * unit;
         }
       }
     }

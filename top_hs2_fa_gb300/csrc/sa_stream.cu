@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
           const int hl = nt * 8 + 2 * tig + hs;
           if (hl < Gh) {
             const int hq = g * G + h0 + hl;  // query head
-            const float inv = sa_norm_factor(at.m[nt][hs], lsum[nt][hs], sink_b2(a.sink, hq));
+            const float inv = sa_norm_factor(at.m[nt][hs], lsum[nt][hs], sink_b2(a.sink, hq)) * at.unit();
             const float* gl = a.gate ? a.gate + ((size_t)qi * a.Hq + hq) * D : nullptr;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
@@ -305,8 +305,8 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
           float* po = a.part_o + (pbase + hl) * D;
 #pragma unroll
           for (int mt = 0; mt < D / 16; ++mt) {
-            po[16 * mt + gid] = at.acc[mt][nt][hs];
-            po[16 * mt + gid + 8] = at.acc[mt][nt][hs + 2];
+            po[16 * mt + gid] = at.acc[mt][nt][hs] * at.unit();
+            po[16 * mt + gid + 8] = at.acc[mt][nt][hs + 2] * at.unit();
           }
         }
       }

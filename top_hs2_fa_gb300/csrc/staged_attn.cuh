@@ -30,7 +30,10 @@ HS2_DEVI uint32_t sw128(int row, int chunk) { return (uint32_t)(row * 128 + ((ch
 //   acc[mt][nt][0..1]: d = 16mt + gid, heads nt*8 + 2tig, +1; acc[mt][nt][2..3]: d + 8.
 // F16 = true (an FP8 cache converted to f16 when staged): queries become f16 at init, both
 // contractions use the f16 MMA, entries carry their own K scale (on the logits) and V scale
-// (on the weights entering P.V), and the normaliser sums the unscaled weights.
+// (on the weights entering P.V), and the normaliser sums the unscaled weights. acc is kept
+// in units of vu, the largest |V scale| seen so far, so each weight enters P.V as
+// f16(p * vs / vu) in [-1, 1]: tiny V scales do not fall into the f16 subnormal range.
+// The true P.V is acc * unit().
 template <int D, int NT, bool F16 = false>
 struct StagedAttn {
   static constexpr int KS = D / 16;
@@ -38,9 +41,13 @@ struct StagedAttn {
   uint32_t qb[KS][NT][2];
   float m[NT][2], l[NT][2];
   float acc[KS][NT][4];
+  float vu, vinv;  // F16: the unit of acc (0 until a nonzero V scale is seen) and 1 / vu (or 0)
+
+  HS2_DEVI float unit() const { return F16 ? vu : 1.f; }
 
   HS2_DEVI void init(const __nv_bfloat16* q_heads, int G) {
     const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    vu = vinv = 0.f;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int hl = nt * 8 + gid;
@@ -90,6 +97,25 @@ struct StagedAttn {
         for (int nt = 0; nt < NT; ++nt) mma(sc[nt], a[0], a[1], a[2], a[3], qb[s][nt][0], qb[s][nt][1]);
       }
     }
+    if (F16) {
+      // a step whose largest |V scale| (vsA / vsB depend on gid only) exceeds the unit makes
+      // that scale the unit, acc rescaled to it
+      float vm = fmaxf(fabsf(vsA), fabsf(vsB));
+      if (__any_sync(0xffffffffu, vm > vu)) {
+        vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 4));
+        vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 8));
+        vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 16));
+        const float f = vu / vm;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[mt][nt][i] *= f;
+        vu = vm;
+        vinv = 1.f / vm;
+      }
+    }
     uint32_t pb[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -119,8 +145,9 @@ struct StagedAttn {
       }
       uint32_t pA, pB;  // entry gid / gid+8, heads 2tig, 2tig+1
       if (F16) {
-        pA = pack_f16(p[0] * vsA, p[1] * vsA);
-        pB = pack_f16(p[2] * vsB, p[3] * vsB);
+        const float wA = vsA * vinv, wB = vsB * vinv;
+        pA = pack_f16(p[0] * wA, p[1] * wA);
+        pB = pack_f16(p[2] * wB, p[3] * wB);
         l[nt][0] += p[0] + p[2];
         l[nt][1] += p[1] + p[3];
       } else {
@@ -167,8 +194,8 @@ struct StagedAttn {
         float* o = sm_o + ((size_t)warp * NT * 8 + hl) * D;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          o[16 * mt + gid] = acc[mt][nt][hs];
-          o[16 * mt + gid + 8] = acc[mt][nt][hs + 2];
+          o[16 * mt + gid] = acc[mt][nt][hs] * unit();
+          o[16 * mt + gid + 8] = acc[mt][nt][hs + 2] * unit();
         }
       }
     }

@@ -2,7 +2,8 @@
 
 A self-contained driver for ``ncu -k regex:<kernel>`` captures of one workload shape:
 
-  decode   FA + selection, then SA layers (``--batch`` sequences, lengths in [t-lo, t-hi])
+  decode   FA + selection, then SA layers (``--batch`` sequences, lengths in [t-lo, t-hi];
+           ``--kv-fp8``: the KV stored as FP8 E4M3)
   prefill  causal FA + per-row selection, then SA layers over ``--n`` rows
   csa2     Full indexer + SA, Reindex indexer + SA (``--batch`` sequences of ``--t`` keys)
 
@@ -25,8 +26,14 @@ def up(x, bf16=False):
 
 def run_decode(a) -> float:
     grp = W.decode_bf16_workload(seed=0, B=a.batch, t_lo=a.t_lo, t_hi=a.t_hi, qproj=False)
+    if a.kv_fp8:
+        grp.kv = W.quantize_kv_fp8(grp.kv)
     kv = grp.kv
-    dkv = hs2.KV(k=up(kv.k, True), v=up(kv.v, True), block_table=up(kv.block_table), seq_len=up(kv.seq_len))
+    if a.kv_fp8:
+        dkv = hs2.KV(k=up(kv.k), v=up(kv.v), block_table=up(kv.block_table), seq_len=up(kv.seq_len),
+                     k_scale=up(kv.k_scale), v_scale=up(kv.v_scale))
+    else:
+        dkv = hs2.KV(k=up(kv.k, True), v=up(kv.v, True), block_table=up(kv.block_table), seq_len=up(kv.seq_len))
     q = up(grp.q_fa, True)
     qs = [up(x, True) for x in grp.q_sa[:a.sa_layers]]
     max_t = int(kv.seq_len.max())
@@ -79,6 +86,7 @@ def main() -> None:
     ap.add_argument("--t", type=int, default=131072, help="csa2 keys per sequence")
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--sa-layers", type=int, default=5)
+    ap.add_argument("--kv-fp8", action="store_true", help="decode: FP8 E4M3 paged KV")
     a = ap.parse_args()
     build.build()
     v = {"decode": run_decode, "prefill": run_prefill, "csa2": run_csa2}[a.mode](a)
