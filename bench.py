@@ -141,6 +141,8 @@ class Decode:
     def __init__(self, name, B, t_lo, t_hi, groups, needles, qproj, sel_block=1, kv_fp8=False):
         self.name, self.B, self.t_lo, self.t_hi, self.groups = name, B, t_lo, t_hi, groups
         self.needles, self.qproj, self.sel_block, self.kv_fp8 = needles, qproj, sel_block, kv_fp8
+        # arithmetic type: an FP8 cache converts to f16 MMA operands (fp32 accumulation)
+        self.dtype = "f16" if kv_fp8 else "bf16"
         self.Hq, self.Hkv, self.D, self.w, self.k = 32, 4, 128, 128, 1024
 
     def host_setup(self, seed):
@@ -620,7 +622,7 @@ def run_gpu(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": sc.unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "vs_baseline": None, "dtype": getattr(sc, "dtype", "bf16"), "data": "synthetic", "config": cfg,
         "roofline": {"bound": sc.bound, "kernel": sc.roofline_kernel, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic, "peak_source": psrc,
                      "algorithmic_per_launch": sc.alg_per_launch, "launch_ms": k_ms},
