@@ -138,9 +138,13 @@ class Decode:
     roofline_source = ("top_hs2_fa_gb300/csrc/fa_decode.cu", "top_hs2_fa_gb300/csrc/mma_attn.cuh")
     unit = "queries/s"
 
-    def __init__(self, name, B, t_lo, t_hi, groups, needles, qproj, sel_block=1, kv_fp8=False):
+    def __init__(self, name, B, t_lo, t_hi, groups, needles, qproj, sel_block=1, kv_fp8=False, append=None):
         self.name, self.B, self.t_lo, self.t_hi, self.groups = name, B, t_lo, t_hi, groups
         self.needles, self.qproj, self.sel_block, self.kv_fp8 = needles, qproj, sel_block, kv_fp8
+        # the current token's K/V enter the cache in the step: None (already there), "fused"
+        # (each group's FA call appends its own rows) or "batched" (one hs2_kv_append for all
+        # groups' caches before the first group runs)
+        self.append = append
         # arithmetic type: an FP8 cache converts to f16 MMA operands (fp32 accumulation)
         self.dtype = "f16" if kv_fp8 else "bf16"
         self.Hq, self.Hkv, self.D, self.w, self.k = 32, 4, 128, 128, 1024
@@ -157,6 +161,11 @@ class Decode:
                                  needles=self.needles, qproj=self.qproj)
             if self.kv_fp8:  # the same values stored as FP8 E4M3 with per-(page, KV head) scales
                 grp.kv = W.quantize_kv_fp8(grp.kv)
+            if self.append:  # the new token's K and V rows ([B][Hkv][d], bf16)
+                rng = np.random.default_rng(np.random.SeedSequence([seed, gi, 7]))
+                shape = (self.B, self.Hkv, self.D)
+                grp.k_new = W.store(rng.standard_normal(shape, dtype=np.float32), "bf16")
+                grp.v_new = W.store(rng.standard_normal(shape, dtype=np.float32), "bf16")
             self.host.append(grp)
 
     def setup(self, dev, seed):
@@ -183,6 +192,9 @@ class Decode:
                                      dtype=torch.uint8, device=dev)
             d["ws_sa"] = torch.empty(hs2.hs2_sa_reuse_workspace(B, self.Hq, d["kv"], self.w, self.k),
                                      dtype=torch.uint8, device=dev)
+            if self.append:
+                d["k_new"], d["v_new"] = up(grp.k_new, dev, True), up(grp.v_new, dev, True)
+                total += 2 * grp.k_new.nbytes  # the rows written into the cache
             self.dev.append(d)
             m = C.decode_group_bytes(kv.seq_len, self.Hq, self.Hkv, self.D, self.w, self.k, 1 if self.kv_fp8 else 2, NSA,
                                      kv.max_pages)
@@ -191,17 +203,22 @@ class Decode:
         self.alg_per_launch = fa[0]  # the profiled launch is group 0's FA scan
         self.alg_total = total
         self.units_per_step = self.B
-        self.launches_per_step = self.groups * (3 + NSA)
+        self.launches_per_step = self.groups * (3 + NSA) + (1 if self.append == "batched" else 0)
 
     def step(self, stream, err, qs=None, profile=None):
         hs2 = self.hs2
+        if self.append == "batched":  # every group's new entry in one launch
+            hs2.hs2_kv_append([d["kv"] for d in self.dev], [d["k_new"] for d in self.dev],
+                              [d["v_new"] for d in self.dev], dev_err=err, stream=stream)
+        fused = self.append == "fused"
         for gi, d in enumerate(self.dev):
             q = qs[gi] if qs is not None else d["q"]
             if profile is not None and gi == 0:
                 hs2.hs2_profile_next(hs2.STAGE_FA_SCAN, *profile)
             hs2.hs2_fa_select(q[0], d["kv"], self.w, self.k, self.host[gi].scale, max_t=d["max_t"],
                               out=(d["o"][0], d["lse"], d["idx"], d["cnt"]), workspace=d["ws_fa"], dev_err=err,
-                              stream=stream, sel_block=self.sel_block)
+                              stream=stream, sel_block=self.sel_block, k_new=d["k_new"] if fused else None,
+                              v_new=d["v_new"] if fused else None)
             for j in range(NSA):
                 hs2.hs2_sa_reuse(q[1 + j], d["kv"], self.w, d["idx"], d["cnt"], self.k, self.host[gi].scale,
                                  out=d["o"][1 + j], workspace=d["ws_sa"], dev_err=err, stream=stream)
@@ -216,6 +233,9 @@ class Decode:
             self.q_views.append([x.view(torch.bfloat16) for x in self.d_in[-(1 + NSA):]])
             pinned_copies(self.h_in, self.d_in, [grp.kv.block_table, grp.kv.seq_len], dev, False)
             self.d_in[-2:] = [d["kv"].block_table, d["kv"].seq_len]
+            if self.append:  # the new token's rows arrive with the step's inputs
+                pinned_copies(self.h_in, self.d_in, [grp.k_new, grp.v_new], dev, True)
+                self.d_in[-2:] = [d["k_new"].view(torch.int16), d["v_new"].view(torch.int16)]
             for t in [*d["o"], d["idx"], d["cnt"]]:
                 self.h_out.append(torch.empty(t.shape, dtype=t.dtype).pin_memory())
                 self.d_out.append(t)
@@ -226,7 +246,8 @@ class Decode:
                 "groups": self.groups, "Hq": self.Hq, "Hkv": self.Hkv, "head_dim": self.D, "window": self.w,
                 "top_k": self.k, "sa_layers_per_group": NSA, "page": 64,
                 "kv_dtype": "fp8_e4m3 (scale per page and KV head)" if self.kv_fp8 else "bf16",
-                "selection": "token" if self.sel_block == 1 else f"blocks of {self.sel_block}"}
+                "selection": "token" if self.sel_block == 1 else f"blocks of {self.sel_block}",
+                "kv_append": self.append or "none"}
 
     def oracle_sample(self, budget_s):
         """Oracle FA + 5 SA per query (in every group) on the host cores, query by query."""
@@ -241,6 +262,8 @@ class Decode:
                 sub = W.PagedKV(k=kv.k, v=kv.v, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel],
                                 k_scale=kv.k_scale, v_scale=kv.v_scale,
                                 dtype=kv.dtype, page=kv.page)
+                if self.append:
+                    sub = O.kv_append(sub, grp.k_new[sel], grp.v_new[sel])
                 _, _, idx, cnt = O.fa_decode(grp.q_fa[sel], sub, self.w, self.k, grp.scale, blk=self.sel_block)
                 for j in range(NSA):
                     O.sa_decode(grp.q_sa[j][sel], sub, self.w, idx, cnt, grp.scale)
@@ -444,6 +467,12 @@ SCENARIOS = {
     "decode_block": lambda: Decode("decode_bf16_b64_t16k-32k_block64", 64, 16384, 32768, 1, 32, True, sel_block=64),
     # the decode workload with its cache stored as FP8 E4M3 (queries bf16)
     "decode_fp8": lambda: Decode("decode_fp8kv_b64_t16k-32k", 64, 16384, 32768, 1, 32, True, kv_fp8=True),
+    # decode with the current token's K/V appended by the FA call itself
+    "decode_append": lambda: Decode("decode_bf16_b64_t16k-32k_append", 64, 16384, 32768, 1, 32, True,
+                                    append="fused"),
+    # the four Cross-group caches: one batched append of the new token, then each group in turn
+    "long_decode_append": lambda: Decode("long_decode_bf16_b16_t131072_x4_append", 16, 131072, 131072, 4, 64, False,
+                                         append="batched"),
     "prefill": lambda: Prefill(32768),
     "csa2": lambda: Csa2(),
 }

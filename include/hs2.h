@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define HS2_ABI_VERSION 2
+#define HS2_ABI_VERSION 3
 
 typedef enum {
   HS2_OK = 0,
@@ -133,6 +133,40 @@ hs2_status hs2_fa_select_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv,
                             int k, float scale, int prefill, int sel_block, float* o, float* lse,
                             int32_t* idx, int32_t* idx_cnt, void* workspace, size_t ws_bytes,
                             int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Decode KV append  ([HS2] §10.1, step 3: once the source hidden state is ready, each
+ * Cross group's cache gains one entry; §4.2: the groups' KV branches are independent).
+ * The new token is the last visible key of its sequence: for every cache c < n_caches and
+ * sequence b < kvs[c].batch, with t = kvs[c].seq_len[b] (already counting the new token),
+ *   K row t-1 of KV head g  <-  k_new[c][b][g][:]   (and V likewise from v_new[c]),
+ * i.e. slot (t-1) % 64 of page block_table[b][(t-1) / 64]. One launch for all caches.
+ * kvs: host array of n_caches descriptors (1 <= n_caches <= 8), bf16 or f32 pools; an FP8
+ *   pool returns HS2_ERR_UNSUPPORTED (its per-page scale would have to change). A key-only
+ *   cache (v = NULL, e.g. a CSA2 indexer-key cache) takes k_new only.
+ * k_new, v_new: host arrays of n_caches device pointers, each [batch][Hkv][d] in the
+ *   cache's dtype, 16-byte aligned; v_new may be NULL when every cache is key-only.
+ * The pools are written through the descriptors' k / v pointers, which must therefore be
+ *   writable device memory owned by the caller. The page holding position t-1 must belong
+ *   to that sequence alone for the duration of the call.
+ * Device-side: t < 1 or t > 64 * max_pages sets HS2_DEV_BAD_LENGTH, a block-table entry
+ *   outside [0, num_pages) sets HS2_DEV_BAD_PAGE; that sequence's rows are not written. */
+hs2_status hs2_kv_append(int n_caches, const hs2_kv* kvs, const void* const* k_new, const void* const* v_new,
+                         int32_t* dev_err, void* stream);
+
+/* Decode FA + selection with the current token's K/V append fused in (hs2_fa_select_ex,
+ * decode only, plus hs2_kv_append of one cache): k_new / v_new [batch][Hq / G = Hkv][d]
+ * (device, kv->dtype, 16-byte aligned) are written to position t-1 as hs2_kv_append does,
+ * and the scan uses them for key t-1. On the bf16 tensor-core scan the write happens inside
+ * the scan kernel, which takes key t-1 from k_new / v_new rather than the pool; otherwise
+ * (f32, or a head-sharing factor that path does not take) a separate append kernel runs
+ * first on the same stream. Outputs equal those of hs2_kv_append followed by
+ * hs2_fa_select_ex. FP8 pools: HS2_ERR_UNSUPPORTED. The workspace size is
+ * hs2_fa_select_workspace(B, Hq, kv, max_t, k, 0). */
+hs2_status hs2_fa_select_append(const void* q, int B, int Hq, const hs2_kv* kv, int max_t, int w, int k,
+                                float scale, int sel_block, const void* k_new, const void* v_new, float* o,
+                                float* lse, int32_t* idx, int32_t* idx_cnt, void* workspace, size_t ws_bytes,
+                                int32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------------------
  * hs2_fa_select_noalloc — hs2_fa_select for callers that cannot allocate device

@@ -37,6 +37,7 @@ No function here is blocked, fused or reordered beyond these definitions.
 """
 from __future__ import annotations
 
+import copy
 import math
 
 import numpy as np
@@ -45,7 +46,7 @@ __all__ = [
     "to_f64", "gather_rows", "window", "far_count", "full_attention", "selection_scores",
     "topk_lower_index", "fa_decode", "sparse_attention", "sa_decode", "fa_prefill_rows",
     "sa_prefill_rows", "lightning_scores", "block_max", "indexer_full", "indexer_reindex",
-    "pool_positions", "renormalisation_bound",
+    "pool_positions", "renormalisation_bound", "kv_append",
 ]
 
 
@@ -99,6 +100,29 @@ def _scale(kv, which: str):
 def _qdtype(kv) -> str:
     """Queries are bf16 when the KV cache is FP8, else the cache's dtype."""
     return "bf16" if kv.dtype == "fp8" else kv.dtype
+
+
+# ----------------------------------------------------------------------------- decode KV append
+def kv_append(kv, k_new: np.ndarray, v_new=None):
+    """Decode KV append ([HS2] §10.1, step 3: once the source hidden state is ready, each
+    Cross group's cache gains one entry for the new token). The new token is the last visible
+    key of its sequence, position t-1 with t = seq_len[b] already counting it, so its rows
+    k_new[b][g] (and v_new[b][g]) go to slot (t-1) % page of page bt[b][(t-1) // page].
+    Returns a copy of the cache with those rows written in storage form; nothing else moves."""
+    out = copy.copy(kv)
+    out.k = np.array(kv.k, copy=True)
+    out.v = None if kv.v is None else np.array(kv.v, copy=True)
+    for b in range(len(kv.seq_len)):
+        pos = int(kv.seq_len[b]) - 1
+        if pos < 0:
+            raise ValueError("a sequence with no visible key has no current token")
+        pg = int(kv.block_table[b][pos // kv.page])
+        if pg < 0:
+            raise ValueError("block table entry < 0 for the current token")
+        out.k[pg, :, pos % kv.page, :] = k_new[b]
+        if out.v is not None:
+            out.v[pg, :, pos % kv.page, :] = v_new[b]
+    return out
 
 
 # ----------------------------------------------------------------------------- window / far range

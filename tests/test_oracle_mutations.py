@@ -105,6 +105,19 @@ def _gather_wrong_slot(pool, bt_row, g, positions, page, dtype):
     return O.to_f64(pool[pages, g, (positions + 1) % page, :], dtype)
 
 
+def _append_past_current(kv, k_new, v_new=None):
+    """Writes the new rows one position late (at t instead of t-1)."""
+    import copy
+    out = copy.copy(kv)
+    out.k, out.v = np.array(kv.k, copy=True), np.array(kv.v, copy=True)
+    for b in range(len(kv.seq_len)):
+        pos = int(kv.seq_len[b])
+        pg = int(kv.block_table[b][min(pos // kv.page, kv.block_table.shape[1] - 1)])
+        out.k[pg, :, pos % kv.page, :] = k_new[b]
+        out.v[pg, :, pos % kv.page, :] = v_new[b]
+    return out
+
+
 MUTATIONS = [
     ("selection_scores", _sel_no_lse),
     ("selection_scores", _sel_max_not_sum),
@@ -121,6 +134,7 @@ MUTATIONS = [
     ("output_gate", _gate_wrong_side),
     ("block_topk", _block_topk_mean),
     ("fp8_e4m3_to_f64", _fp8_bias8),
+    ("kv_append", _append_past_current),
 ]
 
 PINS = [
@@ -147,6 +161,8 @@ PINS = [
     P.test_block_decode_selection_respects_window_and_budget,
     P.test_fp8_e4m3_values_from_the_format,
     P.test_fp8_encoder_rounds_to_nearest_even,
+    lambda: P.test_kv_append_writes_exactly_the_current_token_row("bf16"),
+    P.test_fa_after_append_is_dense_over_sequence_ending_in_new_row,
 ]
 
 

@@ -530,3 +530,62 @@ def test_oracle_on_fp8_pool_equals_oracle_on_its_dequantised_values():
     sa = O.sa_decode(grp.q_sa[0], kv, grp.w, a[2], a[3], grp.scale)
     sb = O.sa_decode(qs32, kv32, grp.w, a[2], a[3], grp.scale)
     assert np.allclose(sa, sb, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- decode KV append
+def logical_view(pool, bt_row, npages):
+    """[Hkv][npages * page][d] rows of one sequence, by concatenating its pages in table
+    order (a route independent of the oracle's position arithmetic)."""
+    return np.concatenate([pool[int(p)] for p in bt_row[:npages]], axis=1)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_kv_append_writes_exactly_the_current_token_row(dtype):
+    # current tokens on the first, the last and a middle slot of a page
+    lens = [17, 16, 1, 40]
+    grp = W.decode_group(lens, Hq=4, Hkv=2, d=8, w=4, k=6, dtype=dtype, seed=41, n_sa=0, needles=0, page=16)
+    kv = grp.kv
+    rng = np.random.default_rng(5)
+    shape = (len(lens), kv.Hkv, 8)
+    k_new = W.store(rng.standard_normal(shape).astype(np.float32), dtype)
+    v_new = W.store(rng.standard_normal(shape).astype(np.float32), dtype)
+    out = O.kv_append(kv, k_new, v_new)
+    owned = set()
+    for b, t in enumerate(lens):
+        npg = (t + kv.page - 1) // kv.page
+        owned.update(int(p) for p in kv.block_table[b][:npg])
+        for pool0, pool1, new in ((kv.k, out.k, k_new), (kv.v, out.v, v_new)):
+            before = logical_view(pool0, kv.block_table[b], npg)
+            after = logical_view(pool1, kv.block_table[b], npg)
+            np.testing.assert_array_equal(after[:, t - 1], new[b])
+            keep = np.ones(npg * kv.page, dtype=bool)
+            keep[t - 1] = False
+            np.testing.assert_array_equal(after[:, keep], before[:, keep])
+    for p in range(kv.num_pages):  # pages of no sequence are untouched
+        if p not in owned:
+            np.testing.assert_array_equal(out.k[p], kv.k[p])
+            np.testing.assert_array_equal(out.v[p], kv.v[p])
+
+
+def test_fa_after_append_is_dense_over_sequence_ending_in_new_row():
+    lens = [23, 9]
+    grp = W.decode_group(lens, Hq=2, Hkv=1, d=8, w=4, k=5, dtype="f32", seed=43, n_sa=0, needles=0, page=8)
+    kv = grp.kv
+    rng = np.random.default_rng(6)
+    k_new = rng.standard_normal((2, 1, 8)).astype(np.float32)
+    v_new = rng.standard_normal((2, 1, 8)).astype(np.float32)
+    o, lse, _, _ = O.fa_decode(grp.q_fa, O.kv_append(kv, k_new, v_new), 4, 5, grp.scale)
+    Q = O.to_f64(grp.q_fa, "f32")
+    for b, t in enumerate(lens):
+        npg = (t + kv.page - 1) // kv.page
+        K = logical_view(kv.k, kv.block_table[b], npg)[0, :t].astype(np.float64)
+        V = logical_view(kv.v, kv.block_table[b], npg)[0, :t].astype(np.float64)
+        K[t - 1], V[t - 1] = k_new[b, 0], v_new[b, 0]
+        for h in range(2):
+            x = [float(Q[b, h] @ K[s]) * grp.scale for s in range(t)]
+            m = max(x)
+            ex = [math.exp(v - m) for v in x]
+            z = sum(ex)
+            ref = sum((e / z) * V[s] for s, e in enumerate(ex))
+            np.testing.assert_allclose(o[b, h], ref, rtol=0, atol=1e-12)
+            assert abs(lse[b, h] - (m + math.log(z))) < 1e-12

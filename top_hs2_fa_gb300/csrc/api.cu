@@ -361,9 +361,49 @@ hs2_status hs2_fa_select(const void* q, int B_or_n, int Hq, const hs2_kv* kv, in
                           ws_bytes, dev_err, stream);
 }
 
-hs2_status hs2_fa_select_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w, int k,
-                            float scale, int prefill, int sel_block, float* o, float* lse, int32_t* idx,
-                            int32_t* idx_cnt, void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+static bool append_rows_ok(const hs2_kv* kv, const void* k_new, const void* v_new) {
+  if (!valid_kv(kv, false) || !k_new || !aligned16(k_new)) return false;
+  return !kv->v || (v_new && aligned16(v_new));
+}
+
+static hs2::AppendCache append_cache(const hs2_kv* kv, const void* k_new, const void* v_new) {
+  hs2::AppendCache c{};
+  c.k = const_cast<void*>(kv->k);  // the caller owns the pool; an append writes into it
+  c.v = const_cast<void*>(kv->v);
+  c.bt = kv->block_table;
+  c.seq_len = kv->seq_len;
+  c.k_new = k_new;
+  c.v_new = kv->v ? v_new : nullptr;
+  c.num_pages = kv->num_pages;
+  c.max_pages = kv->max_pages;
+  c.Hkv = kv->Hkv;
+  c.row_bytes = kv->d * (kv->dtype == HS2_F32 ? 4 : 2);
+  c.B = kv->batch;
+  return c;
+}
+
+hs2_status hs2_kv_append(int n_caches, const hs2_kv* kvs, const void* const* k_new, const void* const* v_new,
+                         int32_t* dev_err, void* stream) {
+  if (n_caches < 1 || n_caches > hs2::kMaxAppendCaches || !kvs || !k_new) return HS2_ERR_ARG;
+  hs2::AppendArgs a{};
+  a.n = n_caches;
+  a.dev_err = dev_err;
+  for (int c = 0; c < n_caches; ++c) {
+    const hs2_kv* kv = &kvs[c];
+    const void* vn = v_new ? v_new[c] : nullptr;
+    if (!append_rows_ok(kv, k_new[c], vn)) return HS2_ERR_ARG;
+    if (kv->dtype == HS2_FP8_E4M3) return HS2_ERR_UNSUPPORTED;
+    a.c[c] = append_cache(kv, k_new[c], vn);
+    a.B = std::max(a.B, (int)kv->batch);
+  }
+  cudaError_t e = hs2::launch_kv_append(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? HS2_OK : cuda_fail(e);
+}
+
+static hs2_status fa_select_impl(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w, int k,
+                                 float scale, int prefill, int sel_block, const void* k_new, const void* v_new,
+                                 float* o, float* lse, int32_t* idx, int32_t* idx_cnt, void* workspace,
+                                 size_t ws_bytes, int32_t* dev_err, void* stream) {
   hs2_status st = common_checks(q, B_or_n, Hq, kv, prefill, true);
   if (st != HS2_OK) return st;
   if (w < 0 || k < 0 || max_t < 1 || !std::isfinite(scale)) return HS2_ERR_ARG;
@@ -382,9 +422,24 @@ hs2_status hs2_fa_select_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv,
   if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   char* ws = (char*)workspace;
+  // the current token's rows: fused into the bf16 tensor-core scan, else appended first
+  const bool fused_append = k_new && p.mma && kv->dtype == HS2_BF16;
+  if (k_new && !fused_append) {
+    hs2::AppendArgs ap{};
+    ap.n = 1;
+    ap.B = B_or_n;
+    ap.dev_err = dev_err;
+    ap.c[0] = append_cache(kv, k_new, v_new);
+    cudaError_t e = hs2::launch_kv_append(ap, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
 
   hs2::AttnArgs a{};
   a.q = q;
+  if (fused_append) {
+    a.k_new = k_new;
+    a.v_new = v_new;
+  }
   a.Hq = Hq;
   a.G = Hq / kv->Hkv;
   a.D = kv->d;
@@ -450,6 +505,23 @@ hs2_status hs2_fa_select_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv,
   e = hs2::launch_combine(c, B_or_n, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return HS2_OK;
+}
+
+hs2_status hs2_fa_select_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w, int k,
+                            float scale, int prefill, int sel_block, float* o, float* lse, int32_t* idx,
+                            int32_t* idx_cnt, void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  return fa_select_impl(q, B_or_n, Hq, kv, max_t, w, k, scale, prefill, sel_block, nullptr, nullptr, o, lse, idx,
+                        idx_cnt, workspace, ws_bytes, dev_err, stream);
+}
+
+hs2_status hs2_fa_select_append(const void* q, int B, int Hq, const hs2_kv* kv, int max_t, int w, int k, float scale,
+                                int sel_block, const void* k_new, const void* v_new, float* o, float* lse,
+                                int32_t* idx, int32_t* idx_cnt, void* workspace, size_t ws_bytes, int32_t* dev_err,
+                                void* stream) {
+  if (!kv || !append_rows_ok(kv, k_new, v_new) || !kv->v) return HS2_ERR_ARG;
+  if (kv->dtype == HS2_FP8_E4M3) return HS2_ERR_UNSUPPORTED;
+  return fa_select_impl(q, B, Hq, kv, max_t, w, k, scale, 0, sel_block, k_new, v_new, o, lse, idx, idx_cnt, workspace,
+                        ws_bytes, dev_err, stream);
 }
 
 size_t hs2_sa_reuse_workspace(int B_or_n, int Hq, const hs2_kv* kv, int w, int k, int prefill) {

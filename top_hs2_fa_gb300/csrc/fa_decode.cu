@@ -71,6 +71,10 @@ __global__ void __launch_bounds__(128, (FP8 && NT == 1) ? 4 : 0) fa_decode_mma_k
   };
 
   if constexpr (!FP8) {
+    const bool append = a.k_new != nullptr;  // decode only (the host refuses it for prefill)
+    const size_t row_new = ((size_t)qi * a.Hkv + g) * D;
+    const __nv_bfloat16* k_new_row = append ? reinterpret_cast<const __nv_bfloat16*>(a.k_new) + row_new : nullptr;
+    const __nv_bfloat16* v_new_row = append ? reinterpret_cast<const __nv_bfloat16*>(a.v_new) + row_new : nullptr;
     for (int page = page0 + warp; page < page1; page += 4) {
       const int phys = bt[page];
       if (phys < 0 || phys >= a.num_pages) {
@@ -84,17 +88,42 @@ __global__ void __launch_bounds__(128, (FP8 && NT == 1) ? 4 : 0) fa_decode_mma_k
         const int key0 = page * kPage + ch * 16;
         if (key0 >= t) break;
         const int r0 = ch * 16 + gid;  // row within the page
+        // fused append: the chunk holding key t-1 takes that row from k_new / v_new instead
+        // of the pool (which this kernel then writes; no lane reads it from the pool)
+        const bool tail = append && key0 + 16 >= t;
+        const __nv_bfloat16* kA = kp + (size_t)r0 * D;
+        const __nv_bfloat16* kB = kp + (size_t)(r0 + 8) * D;
+        if (tail) {
+          if (key0 + gid == t - 1) kA = k_new_row;
+          if (key0 + gid + 8 == t - 1) kB = k_new_row;
+        }
         uint4 kr0[KC], kr1[KC], vr[4][VC];
 #pragma unroll
         for (int j = 0; j < KC; ++j) {
-          kr0[j] = ldg_nc_v4(kp + (size_t)r0 * D + 32 * j + 8 * tig);
-          kr1[j] = ldg_nc_v4(kp + (size_t)(r0 + 8) * D + 32 * j + 8 * tig);
+          kr0[j] = ldg_nc_v4(kA + 32 * j + 8 * tig);
+          kr1[j] = ldg_nc_v4(kB + 32 * j + 8 * tig);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int vrow = ch * 16 + 2 * tig + (e & 1) + 8 * (e >> 1);
+          const __nv_bfloat16* vsrc = (tail && page * kPage + vrow == t - 1) ? v_new_row : vp + (size_t)vrow * D;
 #pragma unroll
-          for (int j = 0; j < VC; ++j) vr[e][j] = ldg_nc_v4(vp + (size_t)vrow * D + (D / 8) * gid + 8 * j);
+          for (int j = 0; j < VC; ++j) vr[e][j] = ldg_nc_v4(vsrc + (D / 8) * gid + 8 * j);
+        }
+        if (tail) {  // write-through of the new rows (each element by exactly one lane)
+          __nv_bfloat16* kw = const_cast<__nv_bfloat16*>(kp) + (size_t)((t - 1) % kPage) * D;
+          if (key0 + gid == t - 1)
+#pragma unroll
+            for (int j = 0; j < KC; ++j) *reinterpret_cast<uint4*>(kw + 32 * j + 8 * tig) = kr0[j];
+          if (key0 + gid + 8 == t - 1)
+#pragma unroll
+            for (int j = 0; j < KC; ++j) *reinterpret_cast<uint4*>(kw + 32 * j + 8 * tig) = kr1[j];
+          __nv_bfloat16* vw = const_cast<__nv_bfloat16*>(vp) + (size_t)((t - 1) % kPage) * D;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (page * kPage + ch * 16 + 2 * tig + (e & 1) + 8 * (e >> 1) == t - 1)
+#pragma unroll
+              for (int j = 0; j < VC; ++j) *reinterpret_cast<uint4*>(vw + (D / 8) * gid + 8 * j) = vr[e][j];
         }
         if (key0 + 16 > t) {  // rows past t: never read their values
 #pragma unroll

@@ -37,7 +37,26 @@ struct AttnArgs {
   const float* v_scale;
   const float* sink;  // SA: [Hq] sink logits (natural log), or null
   const float* gate;  // SA: [Bq][Hq][D] output gate logits, or null
+  const void* k_new;  // decode FA with a fused append: [Bq][Hkv][D] rows of key t-1, or null
+  const void* v_new;
   long long ld_logits;
+  int32_t* dev_err;
+};
+
+// Decode KV append over up to kMaxAppendCaches independent caches in one launch.
+constexpr int kMaxAppendCaches = 8;
+struct AppendCache {
+  void* k;
+  void* v;  // null: a key-only cache
+  const int32_t* bt;
+  const int32_t* seq_len;
+  const void* k_new;  // [B][Hkv][row_bytes]
+  const void* v_new;
+  int num_pages, max_pages, Hkv, row_bytes, B;
+};
+struct AppendArgs {
+  AppendCache c[kMaxAppendCaches];
+  int n, B;  // B: the largest batch of the caches
   int32_t* dev_err;
 };
 
@@ -146,6 +165,7 @@ struct SelectArgs {
 };
 
 cudaError_t launch_fa_decode_mma(const AttnArgs& a, int Bq, cudaStream_t s);
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_attn_partial(const AttnArgs& a, int Bq, int bf16, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s);
 bool sa_mma_supported(int G, int D, int bf16, int w, int k);

@@ -23,6 +23,7 @@ EXPORTS = (
     "hs2_fa_select_workspace", "hs2_fa_select", "hs2_fa_select_ex", "hs2_sa_reuse_workspace", "hs2_sa_reuse", "hs2_sa_reuse_ex",
     "hs2_hier_reindex_workspace", "hs2_hier_reindex", "hs2_strerror", "hs2_last_cuda_error",
     "hs2_abi_version", "hs2_profile_next", "hs2_selftest_wait_timeout", "hs2_fa_select_noalloc", "hs2_fa_select_noalloc_capacity",
+    "hs2_kv_append", "hs2_fa_select_append",
 )
 STAGE_FA_SCAN, STAGE_SA_GATHER, STAGE_INDEXER = 0, 1, 2
 
@@ -81,6 +82,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.hs2_profile_next.restype = None
     lib.hs2_fa_select_noalloc.argtypes = [vp, i32, i32, kvp, i32, i32, i32, f32, i32, vp, vp, vp, vp, vp, vp]
     lib.hs2_fa_select_noalloc.restype = i32
+    lib.hs2_kv_append.argtypes = [i32, kvp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp]
+    lib.hs2_kv_append.restype = i32
+    lib.hs2_fa_select_append.argtypes = [vp, i32, i32, kvp, i32, i32, i32, f32, i32, vp, vp, vp, vp, vp, vp, vp, sz,
+                                         vp, vp]
+    lib.hs2_fa_select_append.restype = i32
     lib.hs2_fa_select_noalloc_capacity.argtypes = []
     lib.hs2_fa_select_noalloc_capacity.restype = sz
     _lib = lib
@@ -147,12 +153,32 @@ def hs2_fa_select_workspace(B_or_n: int, Hq: int, kv: KV, max_t: int, k: int, pr
     return int(load().hs2_fa_select_workspace(B_or_n, Hq, ctypes.byref(c), max_t, k, int(prefill)))
 
 
+def hs2_kv_append(kvs, k_new, v_new=None, dev_err=None, stream=None) -> None:
+    """Decode KV append for several caches in one launch: row t-1 (t = seq_len[b]) of
+    every sequence of cache c takes k_new[c][b] / v_new[c][b] ([batch][Hkv][d], the cache's
+    dtype). ``kvs``: list of KV (bf16 or f32 pools, written in place)."""
+    lib = load()
+    n = len(kvs)
+    if n != len(k_new) or (v_new is not None and n != len(v_new)):
+        raise HS2Error("one k_new (and v_new) tensor per cache")
+    for kv, kn, vn in zip(kvs, k_new, v_new if v_new is not None else [None] * n):
+        for x in (kn, vn):
+            if x is not None and (not x.is_contiguous() or x.dtype != kv.k.dtype):
+                raise HS2Error("new rows must be contiguous and of the cache's dtype")
+    cs = (hs2_kv * n)(*[kv.c() for kv in kvs])
+    kp = (ctypes.c_void_p * n)(*[_ptr(x) for x in k_new])
+    vpa = (ctypes.c_void_p * n)(*[_ptr(x) for x in v_new]) if v_new is not None else None
+    _check(lib.hs2_kv_append(n, cs, kp, vpa, _ptr(dev_err), _stream(stream)))
+
+
 def hs2_fa_select(q: torch.Tensor, kv: KV, w: int, k: int, scale: float, prefill: bool = False,
                   max_t: int | None = None, out=None, workspace=None, dev_err=None, stream=None,
-                  sel_block: int = 1):
+                  sel_block: int = 1, k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None):
     """FA layer + window-excluding top-k. Returns (o, lse, idx, idx_cnt) (float32, float32,
     int32, int32). ``max_t`` defaults to the table's capacity (decode) or n (prefill).
-    ``sel_block`` > 1 selects whole blocks of that many far positions (``hs2_fa_select_ex``)."""
+    ``sel_block`` > 1 selects whole blocks of that many far positions (``hs2_fa_select_ex``).
+    ``k_new`` / ``v_new`` ([B][Hkv][d], decode): the current token's rows, appended to the
+    cache at position t-1 by the same call (``hs2_fa_select_append``)."""
     lib = load()
     Bq, Hq, d = q.shape
     c = kv.c()
@@ -169,7 +195,16 @@ def hs2_fa_select(q: torch.Tensor, kv: KV, w: int, k: int, scale: float, prefill
         o, lse, idx, cnt = out
     nb = int(lib.hs2_fa_select_workspace(Bq, Hq, ctypes.byref(c), max_t, k, int(prefill)))
     ws = _workspace(nb, dev, workspace)
-    if sel_block == 1:
+    if k_new is not None:
+        if prefill:
+            raise HS2Error("the fused append is decode only")
+        for x in (k_new, v_new):
+            if x is None or not x.is_contiguous() or x.dtype != kv.k.dtype:
+                raise HS2Error("k_new and v_new must be contiguous and of the cache's dtype")
+        st = lib.hs2_fa_select_append(_ptr(q), Bq, Hq, ctypes.byref(c), max_t, w, k, float(scale), int(sel_block),
+                                      _ptr(k_new), _ptr(v_new), _ptr(o), _ptr(lse), _ptr(idx), _ptr(cnt), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _ptr(dev_err), _stream(stream))
+    elif sel_block == 1:
         st = lib.hs2_fa_select(_ptr(q), Bq, Hq, ctypes.byref(c), max_t, w, k, float(scale), int(prefill),
                                _ptr(o), _ptr(lse), _ptr(idx), _ptr(cnt), _ptr(ws), ws.numel() * ws.element_size(),
                                _ptr(dev_err), _stream(stream))
