@@ -63,6 +63,27 @@ def fp8_e4m3_to_f64(b: np.ndarray) -> np.ndarray:
     return np.where((e == 15) & (m == 7), np.nan, sign * mag)
 
 
+def fp4_e2m1_to_f64(c: np.ndarray) -> np.ndarray:
+    """Exact value of FP4 E2M1 codes (the low 4 bits of each entry: 1 sign, 2 exponent bits
+    with bias 1, 1 mantissa bit; exponent 0 is subnormal, m * 0.5; no infinity or NaN, so the
+    largest magnitude is 6): the main-KV format of the FP4 cache ([CSA2] §3, "KV 字节与 FP4":
+    E2M1 values with one E4M3 scale per 16 channels)."""
+    c = np.asarray(c, dtype=np.uint8).astype(np.int64) & 0xF
+    sign = np.where(c & 0x8, -1.0, 1.0)
+    e, m = (c >> 1) & 0x3, c & 0x1
+    return sign * np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(e - 1.0))
+
+
+def fp4_unpack(packed: np.ndarray) -> np.ndarray:
+    """Two E2M1 codes per byte along the last axis: channel 2i is the low nibble of byte i,
+    channel 2i+1 the high nibble."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(packed.shape[:-1] + (2 * packed.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = packed & 0xF
+    out[..., 1::2] = packed >> 4
+    return out
+
+
 def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
     """Exact widening of stored values: bfloat16 bit patterns (uint16), float32, or FP8 E4M3
     bytes (uint8; scaling is applied by the caller)."""
@@ -81,11 +102,20 @@ def gather_rows(pool: np.ndarray, bt_row: np.ndarray, g: int, positions: np.ndar
     """Block-table resolve: logical position s of one sequence -> row
     pool[bt[s // page]][g][s % page] of the paged pool, as float64 [len(positions)][d].
     Entries are read in place through the table ([HS2] §7.2: "按索引直接访问 paged KV").
-    ``scale`` ([num_pages][Hkv], FP8 pools): row values are stored / scale[page][g]."""
+    ``scale`` ([num_pages][Hkv], FP8 pools): row values are stored / scale[page][g].
+    FP4 pools (``dtype`` "fp4"): ``scale`` is (slab, sf) with slab [num_pages][Hkv] float32
+    and sf [num_pages][Hkv][page][d/16] E4M3 codes; channel c of a row is
+    e2m1(code) * e4m3(sf[.., c // 16]) * slab[page][g]."""
     positions = np.asarray(positions, dtype=np.int64)
     pages = np.asarray(bt_row, dtype=np.int64)[positions // page]
     if positions.size and (pages < 0).any():
         raise ValueError("block table entry < 0 for a visible position")
+    if dtype == "fp4":
+        slab, sf = scale
+        vals = fp4_e2m1_to_f64(fp4_unpack(pool[pages, g, positions % page, :]))
+        gs = fp8_e4m3_to_f64(np.asarray(sf)[pages, g, positions % page, :])
+        rows = vals * np.repeat(gs, 16, axis=-1)
+        return rows * np.asarray(slab, dtype=np.float64)[pages, g][:, None]
     rows = to_f64(pool[pages, g, positions % page, :], dtype)
     if scale is not None:
         rows = rows * np.asarray(scale, dtype=np.float64)[pages, g][:, None]
@@ -93,13 +123,18 @@ def gather_rows(pool: np.ndarray, bt_row: np.ndarray, g: int, positions: np.ndar
 
 
 def _scale(kv, which: str):
-    """The per-(page, KV head) dequantisation scale of an FP8 pool (None otherwise)."""
-    return getattr(kv, which + "_scale", None) if kv.dtype == "fp8" else None
+    """The dequantisation scales of a low-precision pool: FP8, the per-(page, KV head)
+    scale; FP4, that scale and the per-16-channel E4M3 scales; None otherwise."""
+    if kv.dtype == "fp8":
+        return getattr(kv, which + "_scale", None)
+    if kv.dtype == "fp4":
+        return getattr(kv, which + "_scale"), getattr(kv, which + "_sf")
+    return None
 
 
 def _qdtype(kv) -> str:
-    """Queries are bf16 when the KV cache is FP8, else the cache's dtype."""
-    return "bf16" if kv.dtype == "fp8" else kv.dtype
+    """Queries are bf16 when the KV cache is FP8 or FP4, else the cache's dtype."""
+    return "bf16" if kv.dtype in ("fp8", "fp4") else kv.dtype
 
 
 # ----------------------------------------------------------------------------- decode KV append

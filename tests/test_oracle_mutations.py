@@ -118,6 +118,21 @@ def _append_past_current(kv, k_new, v_new=None):
     return out
 
 
+def _fp4_high_nibble_first(packed):
+    packed = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(packed.shape[:-1] + (2 * packed.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = packed >> 4
+    out[..., 1::2] = packed & 0xF
+    return out
+
+
+def _fp4_bias2(c):
+    c = np.asarray(c, dtype=np.uint8).astype(np.int64) & 0xF
+    sign = np.where(c & 0x8, -1.0, 1.0)
+    e, m = (c >> 1) & 0x3, c & 0x1
+    return sign * np.where(e == 0, m * 0.25, (1.0 + m / 2.0) * np.exp2(e - 2.0))
+
+
 MUTATIONS = [
     ("selection_scores", _sel_no_lse),
     ("selection_scores", _sel_max_not_sum),
@@ -135,6 +150,8 @@ MUTATIONS = [
     ("block_topk", _block_topk_mean),
     ("fp8_e4m3_to_f64", _fp8_bias8),
     ("kv_append", _append_past_current),
+    ("fp4_unpack", _fp4_high_nibble_first),
+    ("fp4_e2m1_to_f64", _fp4_bias2),
 ]
 
 PINS = [
@@ -163,6 +180,9 @@ PINS = [
     P.test_fp8_encoder_rounds_to_nearest_even,
     lambda: P.test_kv_append_writes_exactly_the_current_token_row("bf16"),
     P.test_fa_after_append_is_dense_over_sequence_ending_in_new_row,
+    P.test_fp4_e2m1_values_from_the_format,
+    P.test_fp4_unpack_channel_order,
+    P.test_oracle_on_fp4_pool_equals_oracle_on_its_dequantised_values,
 ]
 
 

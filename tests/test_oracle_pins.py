@@ -532,6 +532,66 @@ def test_oracle_on_fp8_pool_equals_oracle_on_its_dequantised_values():
     assert np.allclose(sa, sb, atol=1e-12)
 
 
+def test_fp4_e2m1_values_from_the_format():
+    """E2M1 facts (1 sign, 2 exponent bits with bias 1, 1 mantissa bit, no inf/NaN): the eight
+    magnitudes are 0, 0.5 (the one subnormal), 1, 1.5, 2, 3, 4, 6; bit 3 is the sign."""
+    v = O.fp4_e2m1_to_f64(np.arange(16, dtype=np.uint8))
+    assert list(v[:8]) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert list(v[8:]) == [-0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_fp4_unpack_channel_order():
+    """Channel 2i is the low nibble of byte i, channel 2i+1 the high nibble."""
+    packed = np.array([[0x21, 0xF7]], dtype=np.uint8)
+    np.testing.assert_array_equal(O.fp4_unpack(packed), [[1, 2, 7, 15]])
+    np.testing.assert_array_equal(O.fp4_e2m1_to_f64(O.fp4_unpack(packed)), [[0.5, 1.0, 6.0, -6.0]])
+
+
+def test_fp4_encoder_rounds_to_nearest_even():
+    """The input encoder: decode(encode(x)) is a nearest E2M1 value (ties to the even code)
+    among all 15 distinct values, saturating at 6; every code round-trips."""
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    vals = np.concatenate([-mags[:0:-1], mags])
+    x = np.concatenate([np.random.default_rng(42).standard_normal(2000) * 3, (mags[:-1] + mags[1:]) / 2,
+                        -(mags[:-1] + mags[1:]) / 2])
+    c = W.f32_to_fp4_e2m1(x)
+    got = O.fp4_e2m1_to_f64(c)
+    xc = np.clip(x, -6, 6)
+    best = np.abs(vals[None, :] - xc[:, None]).min(axis=1)
+    assert np.array_equal(np.abs(got - xc), best)
+    assert np.all((c[2000:] & 1) == 0)  # midpoints went to the even code
+    assert np.array_equal(W.f32_to_fp4_e2m1(mags), np.arange(8))
+
+
+def test_oracle_on_fp4_pool_equals_oracle_on_its_dequantised_values():
+    """FA + selection + SA on an FP4 pool (E2M1 codes, E4M3 scales per 16 channels, a slab
+    scale) equal the same on a float32 pool dequantised here with a table written out."""
+    grp = W.decode_group_fp4([300, 170], Hq=4, Hkv=2, d=32, w=8, k=16, seed=41, n_sa=1, needles=0)
+    kv = grp.kv
+    e2m1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+    e4m3 = O.fp8_e4m3_to_f64(np.arange(256, dtype=np.uint8))  # pinned by its own tests above
+
+    def deq(packed, sf, slab):
+        P, Hh, S, half = packed.shape
+        out = np.empty((P, Hh, S, 2 * half))
+        for c in range(2 * half):
+            nib = (packed[..., c // 2] >> (4 * (c % 2))) & 0xF
+            out[..., c] = e2m1[nib] * e4m3[sf[..., c // 16]]
+        return (out * slab[:, :, None, None]).astype(np.float32)
+
+    kv32 = W.PagedKV(k=deq(kv.k, kv.k_sf, kv.k_scale), v=deq(kv.v, kv.v_sf, kv.v_scale),
+                     block_table=kv.block_table, seq_len=kv.seq_len, dtype="f32")
+    assert np.all(np.abs(kv32.k) < 1e30)  # dequantised in float32 without overflow
+    q32 = O.to_f64(grp.q_fa, "bf16").astype(np.float32)
+    qs32 = O.to_f64(grp.q_sa[0], "bf16").astype(np.float32)
+    a = O.fa_decode(grp.q_fa, kv, grp.w, grp.k, grp.scale)
+    b = O.fa_decode(q32, kv32, grp.w, grp.k, grp.scale)
+    assert np.allclose(a[0], b[0], atol=1e-6) and np.array_equal(a[2], b[2])
+    sa = O.sa_decode(grp.q_sa[0], kv, grp.w, a[2], a[3], grp.scale)
+    sb = O.sa_decode(qs32, kv32, grp.w, a[2], a[3], grp.scale)
+    assert np.allclose(sa, sb, atol=1e-6)
+
+
 # ----------------------------------------------------------------------------- decode KV append
 def logical_view(pool, bt_row, npages):
     """[Hkv][npages * page][d] rows of one sequence, by concatenating its pages in table

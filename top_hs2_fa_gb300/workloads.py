@@ -138,8 +138,10 @@ class PagedKV:
     seq_len: np.ndarray  # int32 [B]
     dtype: str
     page: int = PAGE
-    k_scale: np.ndarray | None = None  # FP8 pools: float32 [num_pages][Hkv], value = code * scale
+    k_scale: np.ndarray | None = None  # FP8 / FP4 pools: float32 [num_pages][Hkv] per-slab scale
     v_scale: np.ndarray | None = None
+    k_sf: np.ndarray | None = None  # FP4 pools: uint8 E4M3 codes [num_pages][Hkv][page][d/16]
+    v_sf: np.ndarray | None = None
 
     @property
     def num_pages(self) -> int:
@@ -151,7 +153,7 @@ class PagedKV:
 
     @property
     def d(self) -> int:
-        return int(self.k.shape[3])
+        return int(self.k.shape[3]) * (2 if self.dtype == "fp4" else 1)  # FP4: two codes per byte
 
     @property
     def B(self) -> int:
@@ -313,6 +315,61 @@ def quantize_kv_fp8(kv: PagedKV) -> PagedKV:
         out[name], out[name + "_scale"] = codes, sc
     return PagedKV(k=out["k"], v=out["v"], block_table=kv.block_table, seq_len=kv.seq_len, dtype="fp8", page=kv.page,
                    k_scale=out["k_scale"], v_scale=out["v_scale"])
+
+
+_E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])  # magnitudes of E2M1 codes 0..7
+
+
+def f32_to_fp4_e2m1(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest FP4 E2M1 value (ties to the even code), saturating at +-6;
+    returns the 4-bit codes (uint8 0..15, bit 3 = sign)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 6.0)
+    hi = np.clip(np.searchsorted(_E2M1, a), 1, 7)
+    lo = hi - 1
+    dl, dh = a - _E2M1[lo], _E2M1[hi] - a
+    code = np.where(dl < dh, lo, np.where(dh < dl, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a <= 0.0, 0, code)
+    return (code | np.where(np.signbit(x) & (code > 0), 8, 0)).astype(np.uint8)
+
+
+def quantize_kv_fp4(kv: PagedKV) -> PagedKV:
+    """FP4 copy of a paged pool: E2M1 codes (two per byte, channel 2i in the low nibble) with
+    one E4M3 scale per 16 channels of a row and one float32 scale per (page, KV head) slab.
+    slab = max |value| / (6 * 448) (1 for an all-zero slab); a group's E4M3 scale is the
+    smallest E4M3 value >= its max |value / slab| / 6 (so no code saturates); code =
+    E2M1(value / slab / group scale)."""
+    out = {}
+    for name in ("k", "v"):
+        src = getattr(kv, name)
+        P, Hh, S, d = src.shape
+        codes = np.empty((P, Hh, S, d // 2), dtype=np.uint8)
+        sf = np.empty((P, Hh, S, d // 16), dtype=np.uint8)
+        slab = np.empty((P, Hh), dtype=np.float32)
+        for p0 in range(0, P, 1024):  # page chunks bound the temporaries
+            x = values(src[p0:p0 + 1024], kv.dtype).astype(np.float64)
+            amax = np.abs(x).max(axis=(2, 3))
+            sl = np.where(amax > 0, amax / (6.0 * 448.0), 1.0).astype(np.float32)
+            y = x / sl[:, :, None, None].astype(np.float64)
+            yg = y.reshape(y.shape[:3] + (d // 16, 16))
+            need = np.abs(yg).max(axis=-1) / 6.0
+            gc = np.clip(np.searchsorted(_E4M3, need, side="left"), 0, 126)  # smallest value >= need
+            gs = _E4M3[gc]
+            q = f32_to_fp4_e2m1(np.where(gs[..., None] > 0, yg / np.where(gs > 0, gs, 1.0)[..., None], 0.0))
+            q = q.reshape(y.shape)
+            codes[p0:p0 + 1024] = q[..., 0::2] | (q[..., 1::2] << 4)
+            sf[p0:p0 + 1024] = gc.astype(np.uint8)
+            slab[p0:p0 + 1024] = sl
+        out[name], out[name + "_sf"], out[name + "_scale"] = codes, sf, slab
+    return PagedKV(k=out["k"], v=out["v"], block_table=kv.block_table, seq_len=kv.seq_len, dtype="fp4", page=kv.page,
+                   k_scale=out["k_scale"], v_scale=out["v_scale"], k_sf=out["k_sf"], v_sf=out["v_sf"])
+
+
+def decode_group_fp4(seq_len, Hq: int, Hkv: int, d: int, w: int, k: int, seed, **kw) -> DecodeGroup:
+    """The bf16 decode workload with its paged KV stored as FP4 E2M1 + E4M3 group scales."""
+    grp = decode_group(seq_len, Hq, Hkv, d, w, k, "bf16", seed, **kw)
+    grp.kv = quantize_kv_fp4(grp.kv)
+    return grp
 
 
 def decode_group_fp8(seq_len, Hq: int, Hkv: int, d: int, w: int, k: int, seed, **kw) -> DecodeGroup:
