@@ -18,6 +18,7 @@ the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -138,15 +139,16 @@ class Decode:
     roofline_source = ("top_hs2_fa_gb300/csrc/fa_decode.cu", "top_hs2_fa_gb300/csrc/mma_attn.cuh")
     unit = "queries/s"
 
-    def __init__(self, name, B, t_lo, t_hi, groups, needles, qproj, sel_block=1, kv_fp8=False, append=None):
+    def __init__(self, name, B, t_lo, t_hi, groups, needles, qproj, sel_block=1, kv_fmt=None, append=None):
         self.name, self.B, self.t_lo, self.t_hi, self.groups = name, B, t_lo, t_hi, groups
-        self.needles, self.qproj, self.sel_block, self.kv_fp8 = needles, qproj, sel_block, kv_fp8
+        self.needles, self.qproj, self.sel_block, self.kv_fmt = needles, qproj, sel_block, kv_fmt
+        self.kv_fp8 = kv_fmt is not None  # a low-precision cache (FP8 or FP4 codes with scales)
         # the current token's K/V enter the cache in the step: None (already there), "fused"
         # (each group's FA call appends its own rows) or "batched" (one hs2_kv_append for all
         # groups' caches before the first group runs)
         self.append = append
         # arithmetic type: an FP8 cache converts to f16 MMA operands (fp32 accumulation)
-        self.dtype = "f16" if kv_fp8 else "bf16"
+        self.dtype = "f16" if self.kv_fp8 else "bf16"
         self.Hq, self.Hkv, self.D, self.w, self.k = 32, 4, 128, 128, 1024
 
     def host_setup(self, seed):
@@ -159,8 +161,10 @@ class Decode:
             lens = W.uniform_lengths(self.B, self.t_lo, self.t_hi, s_len)
             grp = W.decode_group(lens, self.Hq, self.Hkv, self.D, self.w, self.k, "bf16", s_grp, n_sa=NSA,
                                  needles=self.needles, qproj=self.qproj)
-            if self.kv_fp8:  # the same values stored as FP8 E4M3 with per-(page, KV head) scales
+            if self.kv_fmt == "fp8":  # the same values stored as FP8 E4M3 with per-(page, KV head) scales
                 grp.kv = W.quantize_kv_fp8(grp.kv)
+            elif self.kv_fmt == "fp4":  # E2M1 with E4M3 scales of 16 channels and per-(page, KV head) scales
+                grp.kv = W.quantize_kv_fp4(grp.kv)
             if self.append:  # the new token's K and V rows ([B][Hkv][d], bf16)
                 rng = np.random.default_rng(np.random.SeedSequence([seed, gi, 7]))
                 shape = (self.B, self.Hkv, self.D)
@@ -179,9 +183,11 @@ class Decode:
         for grp in self.host:
             kv = grp.kv
             bf = not self.kv_fp8
+            fp4 = self.kv_fmt == "fp4"
             d = {"kv": hs2.KV(k=up(kv.k, dev, bf), v=up(kv.v, dev, bf), block_table=up(kv.block_table, dev),
                               seq_len=up(kv.seq_len, dev),
-                              k_scale=None if bf else up(kv.k_scale, dev), v_scale=None if bf else up(kv.v_scale, dev)),
+                              k_scale=None if bf else up(kv.k_scale, dev), v_scale=None if bf else up(kv.v_scale, dev),
+                              k_sf=up(kv.k_sf, dev) if fp4 else None, v_sf=up(kv.v_sf, dev) if fp4 else None),
                  "max_t": int(kv.seq_len.max()), "q": [up(x, dev, True) for x in [grp.q_fa, *grp.q_sa]]}
             B = self.B
             d["o"] = [torch.empty((B, self.Hq, self.D), dtype=torch.float32, device=dev) for _ in range(1 + NSA)]
@@ -196,8 +202,9 @@ class Decode:
                 d["k_new"], d["v_new"] = up(grp.k_new, dev, True), up(grp.v_new, dev, True)
                 total += 2 * grp.k_new.nbytes  # the rows written into the cache
             self.dev.append(d)
-            m = C.decode_group_bytes(kv.seq_len, self.Hq, self.Hkv, self.D, self.w, self.k, 1 if self.kv_fp8 else 2, NSA,
-                                     kv.max_pages)
+            elem = {"fp8": 1, "fp4": 0.5 + 1 / 16}.get(self.kv_fmt, 2)  # cache bytes per channel
+            m = C.decode_group_bytes(kv.seq_len, self.Hq, self.Hkv, self.D, self.w, self.k, elem, NSA,
+                                     kv.max_pages, q_elem=2)
             fa.append(m["fa"])
             total += m["total"]
         self.alg_per_launch = fa[0]  # the profiled launch is group 0's FA scan
@@ -245,7 +252,9 @@ class Decode:
                 "seq_len": f"U[{self.t_lo},{self.t_hi}]" if self.t_lo != self.t_hi else self.t_lo,
                 "groups": self.groups, "Hq": self.Hq, "Hkv": self.Hkv, "head_dim": self.D, "window": self.w,
                 "top_k": self.k, "sa_layers_per_group": NSA, "page": 64,
-                "kv_dtype": "fp8_e4m3 (scale per page and KV head)" if self.kv_fp8 else "bf16",
+                "kv_dtype": {"fp8": "fp8_e4m3 (scale per page and KV head)",
+                             "fp4": "fp4_e2m1 (e4m3 scale per 16 channels, scale per page and KV head)"}.get(
+                                 self.kv_fmt, "bf16"),
                 "selection": "token" if self.sel_block == 1 else f"blocks of {self.sel_block}",
                 "kv_append": self.append or "none"}
 
@@ -259,9 +268,7 @@ class Decode:
             t0 = time.perf_counter()
             for grp in self.host:
                 kv, sel = grp.kv, [done]
-                sub = W.PagedKV(k=kv.k, v=kv.v, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel],
-                                k_scale=kv.k_scale, v_scale=kv.v_scale,
-                                dtype=kv.dtype, page=kv.page)
+                sub = dataclasses.replace(kv, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel])
                 if self.append:
                     sub = O.kv_append(sub, grp.k_new[sel], grp.v_new[sel])
                 _, _, idx, cnt = O.fa_decode(grp.q_fa[sel], sub, self.w, self.k, grp.scale, blk=self.sel_block)
@@ -466,7 +473,9 @@ SCENARIOS = {
     # the decode workload with HySparse's first-version block-level selection (16 blocks of 64)
     "decode_block": lambda: Decode("decode_bf16_b64_t16k-32k_block64", 64, 16384, 32768, 1, 32, True, sel_block=64),
     # the decode workload with its cache stored as FP8 E4M3 (queries bf16)
-    "decode_fp8": lambda: Decode("decode_fp8kv_b64_t16k-32k", 64, 16384, 32768, 1, 32, True, kv_fp8=True),
+    "decode_fp8": lambda: Decode("decode_fp8kv_b64_t16k-32k", 64, 16384, 32768, 1, 32, True, kv_fmt="fp8"),
+    # ... and as FP4 E2M1 with an E4M3 scale per 16 channels
+    "decode_fp4": lambda: Decode("decode_fp4kv_b64_t16k-32k", 64, 16384, 32768, 1, 32, True, kv_fmt="fp4"),
     # decode with the current token's K/V appended by the FA call itself
     "decode_append": lambda: Decode("decode_bf16_b64_t16k-32k_append", 64, 16384, 32768, 1, 32, True,
                                     append="fused"),

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define HS2_ABI_VERSION 3
+#define HS2_ABI_VERSION 4
 
 typedef enum {
   HS2_OK = 0,
@@ -67,7 +67,7 @@ typedef enum {
 #define HS2_DEV_SELECT 16     /* a prefill row's streamed candidates could not prove its top-k
                                  (its idx_cnt is written as -1); see hs2_fa_select */
 
-typedef enum { HS2_F32 = 0, HS2_BF16 = 1, HS2_FP8_E4M3 = 2 } hs2_dtype;
+typedef enum { HS2_F32 = 0, HS2_BF16 = 1, HS2_FP8_E4M3 = 2, HS2_FP4_E2M1 = 3 } hs2_dtype;
 
 /* Paged KV of ONE group, shared by its FA and SA layers ([HS2] §5, §7.2).
  * k, v:        [num_pages][Hkv][page_size][d] elements of `dtype`, 16-byte aligned.
@@ -75,9 +75,17 @@ typedef enum { HS2_F32 = 0, HS2_BF16 = 1, HS2_FP8_E4M3 = 2 } hs2_dtype;
  * block_table: int32 [batch][max_pages]; entry j of sequence b is the physical page
  *              holding logical positions [j*page_size, (j+1)*page_size).
  * seq_len:     int32 [batch], keys visible to the query (its own included), >= 1.
- * k_scale, v_scale: HS2_FP8_E4M3 only (else NULL): float32 [num_pages][Hkv]; a stored
- *              E4M3 code c of page p, KV head g stands for c * scale[p][g]. An FP8 cache is
- *              read by hs2_fa_select (decode) and hs2_sa_reuse (decode); queries are bf16.
+ * k_scale, v_scale: HS2_FP8_E4M3 and HS2_FP4_E2M1 only (else NULL): float32
+ *              [num_pages][Hkv]; FP8: a stored E4M3 code c of page p, KV head g stands for
+ *              c * scale[p][g].
+ * k_sf, v_sf:  HS2_FP4_E2M1 only (else NULL): uint8 E4M3 codes [num_pages][Hkv][page_size]
+ *              [d/16], one per 16 channels of a row ([CSA2] §3, "KV 字节与 FP4": E2M1 main KV
+ *              with an E4M3 scale per 16 channels). k and v then hold [num_pages][Hkv]
+ *              [page_size][d/2] bytes, channel 2i in the low nibble of byte i (E2M1: sign,
+ *              2 exponent bits with bias 1, 1 mantissa bit); channel c of a row stands for
+ *              e2m1(code) * e4m3(sf[c / 16]) * scale[p][g].
+ *              FP8 and FP4 caches are read by hs2_fa_select (decode) and hs2_sa_reuse
+ *              (decode); queries are bf16; prefill and the KV append refuse them.
  * page_size must be 64; d must be 64 or 128.                                        */
 typedef struct {
   const void* k;
@@ -93,6 +101,8 @@ typedef struct {
   hs2_dtype dtype;
   const float* k_scale;
   const float* v_scale;
+  const uint8_t* k_sf;
+  const uint8_t* v_sf;
 } hs2_kv;
 
 /* ---------------------------------------------------------------------------

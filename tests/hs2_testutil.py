@@ -23,13 +23,16 @@ def to_torch(arr: np.ndarray, dtype: str, device="cuda"):
 def kv_to_device(kv, device="cuda"):
     from top_hs2_fa_gb300.hs2 import KV
 
-    fp8 = kv.dtype == "fp8"  # E4M3 codes (uint8) with per-(page, KV head) scales
+    lowp = kv.dtype in ("fp8", "fp4")  # uint8 codes with per-(page, KV head) scales
+    fp4 = kv.dtype == "fp4"  # plus E4M3 scales of 16 channels
     return KV(k=to_torch(kv.k, kv.dtype, device),
               v=None if kv.v is None else to_torch(kv.v, kv.dtype, device),
               block_table=to_torch(kv.block_table, "i32", device),
               seq_len=to_torch(kv.seq_len, "i32", device),
-              k_scale=to_torch(kv.k_scale, "f32", device) if fp8 else None,
-              v_scale=to_torch(kv.v_scale, "f32", device) if fp8 else None)
+              k_scale=to_torch(kv.k_scale, "f32", device) if lowp else None,
+              v_scale=to_torch(kv.v_scale, "f32", device) if lowp and kv.v is not None else None,
+              k_sf=to_torch(kv.k_sf, "u8", device) if fp4 else None,
+              v_sf=to_torch(kv.v_sf, "u8", device) if fp4 and kv.v is not None else None)
 
 
 def check_index_sets(gpu_idx, gpu_cnt, ora_idx, ora_cnt, ora_scores, label=""):

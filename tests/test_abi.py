@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.hs2_abi_version() == 3
+    assert lib.hs2_abi_version() == H.ABI_VERSION == 4
     for st, word in [(0, "ok"), (-1, "invalid"), (-2, "unsupported"), (-3, "CUDA"), (-4, "device")]:
         assert word in lib.hs2_strerror(st).decode()
 

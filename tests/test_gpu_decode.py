@@ -3,6 +3,8 @@
 Every call goes through the C ABI (ctypes binding). Oracle inputs are the same
 seeded arrays the GPU receives; no expected value comes from the GPU.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -28,7 +30,7 @@ def H():
 
 def qdt(kv):
     """Storage dtype of the queries: bf16 for an FP8 cache, else the cache's dtype."""
-    return "bf16" if kv.dtype == "fp8" else kv.dtype
+    return "bf16" if kv.dtype in ("fp8", "fp4") else kv.dtype
 
 
 def run_decode_group(H, grp, sa_layers=None):
@@ -52,8 +54,7 @@ def check_group(H, grp, batches=None, sa_layers=None):
     o, lse, idx, cnt, sa, err = run_decode_group(H, grp, sa_layers)
     assert err == 0, f"device error flags {err}"
     sel = list(range(kv.B)) if batches is None else list(batches)
-    sub = W.PagedKV(k=kv.k, v=kv.v, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel], dtype=kv.dtype,
-                    page=kv.page, k_scale=kv.k_scale, v_scale=kv.v_scale)
+    sub = dataclasses.replace(kv, block_table=kv.block_table[sel], seq_len=kv.seq_len[sel])
     o_r, lse_r, idx_r, cnt_r, scores = O.fa_decode(grp.q_fa[sel], sub, grp.w, grp.k, grp.scale,
                                                    return_scores=True)
     t_ = tol(qdt(kv))
@@ -266,6 +267,46 @@ def test_fp8_kv_small_wide_values(H):
     check_index_sets(idx, cnt, idx_r, cnt_r, scores, "decode ")
     ref = O.sa_decode(grp.q_sa[0], grp.kv, grp.w, idx, cnt, grp.scale)
     assert max_abs(sa[0], ref) <= 1e-2 * np.abs(ref).max(), f"SA relative error {max_abs(sa[0], ref) / np.abs(ref).max()}"
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 4, 128), (8, 8, 64), (32, 1, 128), (16, 2, 64)])
+def test_fp4_kv_decode(H, Hq, Hkv, d):
+    """FP4 cache (E2M1 codes, an E4M3 scale per 16 channels, a slab scale per page and KV
+    head): FA output, lse and index sets against the oracle on the same codes and scales,
+    and the SA layers over them."""
+    grp = W.decode_group_fp4([3000, 1700, 130, 5000], Hq, Hkv, d, 64, 256, seed=25, n_sa=2, needles=8)
+    check_group(H, grp)
+
+
+def test_fp4_kv_small_wide_values(H):
+    """FP4 cache whose V slabs are tiny and span four decades: outputs keep their accuracy
+    relative to their own magnitude."""
+    grp = W.decode_group([2600, 900, 4100], 16, 2, 128, 64, 128, "bf16", seed=29, n_sa=1, needles=4)
+    kv = grp.kv
+    rng = np.random.default_rng(33)
+    fac = 1e-4 * 10.0 ** rng.uniform(-2.0, 2.0, size=kv.v.shape[:2])
+    vf = (W.values(kv.v, "bf16") * fac[:, :, None, None]).astype(np.float32)
+    f32 = W.PagedKV(k=W.values(kv.k, "bf16"), v=vf, block_table=kv.block_table, seq_len=kv.seq_len, dtype="f32",
+                    page=kv.page)
+    grp.kv = W.quantize_kv_fp4(f32)
+    o, lse, idx, cnt, sa, err = run_decode_group(H, grp)
+    assert err == 0
+    o_r, lse_r, idx_r, cnt_r, scores = O.fa_decode(grp.q_fa, grp.kv, grp.w, grp.k, grp.scale, return_scores=True)
+    assert max_abs(o, o_r) <= 1e-2 * np.abs(o_r).max(), f"FA relative error {max_abs(o, o_r) / np.abs(o_r).max()}"
+    assert max_abs(lse, lse_r) <= 2e-2
+    check_index_sets(idx, cnt, idx_r, cnt_r, scores, "decode ")
+    ref = O.sa_decode(grp.q_sa[0], grp.kv, grp.w, idx, cnt, grp.scale)
+    assert max_abs(sa[0], ref) <= 1e-2 * np.abs(ref).max(), f"SA relative error {max_abs(sa[0], ref) / np.abs(ref).max()}"
+
+
+def test_fp4_kv_rejects_prefill(H):
+    import torch
+
+    grp = W.prefill_group(300, 8, 1, 128, w=16, k=32, dtype="bf16", seed=26, n_sa=0)
+    kv = W.quantize_kv_fp4(grp.kv)
+    with pytest.raises(H.HS2Error):
+        H.hs2_fa_select(to_torch(grp.q_fa, "bf16"), kv_to_device(kv), 16, 32, grp.scale, prefill=True)
+    torch.cuda.synchronize()
 
 
 def test_fp8_kv_rejects_prefill(H):

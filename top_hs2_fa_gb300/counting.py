@@ -19,20 +19,22 @@ def union_size(t: int, w: int, k: int) -> int:
     return min(w, t) + min(k, max(0, t - w))
 
 
-def decode_group_bytes(seq_len, Hq: int, Hkv: int, d: int, w: int, k: int, elem: int,
-                       n_sa: int, max_pages: int | None = None) -> dict:
+def decode_group_bytes(seq_len, Hq: int, Hkv: int, d: int, w: int, k: int, elem: float,
+                       n_sa: int, max_pages: int | None = None, q_elem: float | None = None) -> dict:
     """HBM bytes one decode step of one group must move (FA + n_sa SA layers).
 
     FA reads every visible K and V row once; each SA layer reads the K and V rows
     of W ∪ S once per KV head (its query heads share the gathered row). Small
-    terms: queries, fp32 outputs, indices and the block table.
+    terms: queries, fp32 outputs, indices and the block table. ``elem``: cache bytes
+    per channel (2 bf16, 1 FP8, 0.5625 FP4 with its E4M3 scale per 16 channels);
+    ``q_elem``: query bytes per channel (default ``elem``).
     """
     seq_len = [int(t) for t in seq_len]
     B = len(seq_len)
     row = d * elem
     fa = sum(t * Hkv * row * 2 for t in seq_len)
     sa_layer = sum(Hkv * union_size(t, w, k) * row * 2 for t in seq_len)
-    q = B * Hq * d * elem
+    q = B * Hq * d * (elem if q_elem is None else q_elem)
     o = B * Hq * d * 4
     idx = B * Hkv * k * 4
     mp = max_pages if max_pages is not None else max((t + 63) // 64 for t in seq_len)

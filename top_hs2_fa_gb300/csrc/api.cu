@@ -47,11 +47,18 @@ bool valid_kv(const hs2_kv* kv, bool need_v) {
   if (kv->batch < 1 || kv->num_pages < 1 || kv->max_pages < 1 || kv->Hkv < 1) return false;
   if (kv->page_size != 64) return false;
   if (kv->d != 64 && kv->d != 128) return false;
-  if (kv->dtype != HS2_F32 && kv->dtype != HS2_BF16 && kv->dtype != HS2_FP8_E4M3) return false;
-  if (kv->dtype == HS2_FP8_E4M3 && (!kv->k_scale || (need_v && !kv->v_scale))) return false;
+  if (kv->dtype != HS2_F32 && kv->dtype != HS2_BF16 && kv->dtype != HS2_FP8_E4M3 && kv->dtype != HS2_FP4_E2M1)
+    return false;
+  if ((kv->dtype == HS2_FP8_E4M3 || kv->dtype == HS2_FP4_E2M1) && (!kv->k_scale || (need_v && !kv->v_scale)))
+    return false;
+  if (kv->dtype == HS2_FP4_E2M1 && (!kv->k_sf || !aligned16(kv->k_sf) || (need_v && (!kv->v_sf || !aligned16(kv->v_sf)))))
+    return false;
   if (!aligned16(kv->k) || (need_v && !aligned16(kv->v))) return false;
   return true;
 }
+
+// FP8 / FP4 caches (quantised codes with scales): decode only
+bool low_precision(const hs2_kv* kv) { return kv->dtype == HS2_FP8_E4M3 || kv->dtype == HS2_FP4_E2M1; }
 
 bool pow2_le32(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16 || g == 32; }
 
@@ -67,7 +74,7 @@ struct FaPlan {
 FaPlan fa_plan(int Bq, int Hq, const hs2_kv* kv, int max_t) {
   FaPlan p{};
   const int G = Hq / kv->Hkv;
-  p.mma = (kv->dtype == HS2_BF16 || kv->dtype == HS2_FP8_E4M3) && G <= 32 && (G <= 8 || G == 16 || G == 32);
+  p.mma = (kv->dtype == HS2_BF16 || low_precision(kv)) && G <= 32 && (G <= 8 || G == 16 || G == 32);
   const int maxpg = cdiv(max_t, 64);
   if (p.mma) {
     // enough CTAs to fill 152 SMs several times over, splits of at most 16 pages
@@ -106,7 +113,7 @@ SaPlan sa_plan(int Bq, int Hq, const hs2_kv* kv, int w, int k, int prefill) {
   const int G = Hq / kv->Hkv;
   const bool bf16 = kv->dtype == HS2_BF16;
   size_t off = 0;
-  const int kvt = bf16 ? 1 : kv->dtype == HS2_FP8_E4M3 ? 2 : 0;
+  const int kvt = bf16 ? 1 : kv->dtype == HS2_FP8_E4M3 ? 2 : kv->dtype == HS2_FP4_E2M1 ? 3 : 0;
   if (!prefill && hs2::sa_stream_plan(G, kv->d, kvt, w, k, Bq, kv->Hkv, &p.sp, &p.grid)) {
     p.stream = true;
     const size_t units = (size_t)Bq * kv->Hkv * p.sp.hg;
@@ -392,7 +399,7 @@ hs2_status hs2_kv_append(int n_caches, const hs2_kv* kvs, const void* const* k_n
     const hs2_kv* kv = &kvs[c];
     const void* vn = v_new ? v_new[c] : nullptr;
     if (!append_rows_ok(kv, k_new[c], vn)) return HS2_ERR_ARG;
-    if (kv->dtype == HS2_FP8_E4M3) return HS2_ERR_UNSUPPORTED;
+    if (low_precision(kv)) return HS2_ERR_UNSUPPORTED;
     a.c[c] = append_cache(kv, k_new[c], vn);
     a.B = std::max(a.B, (int)kv->batch);
   }
@@ -410,7 +417,7 @@ static hs2_status fa_select_impl(const void* q, int B_or_n, int Hq, const hs2_kv
   if (sel_block < 1 || sel_block > 4096 || (sel_block > 1 && (sel_block % 4 != 0 || k % sel_block != 0)))
     return HS2_ERR_ARG;
   if (sel_block > 1 && prefill) return HS2_ERR_UNSUPPORTED;
-  if (kv->dtype == HS2_FP8_E4M3 && prefill) return HS2_ERR_UNSUPPORTED;  // FP8 caches: decode only
+  if (low_precision(kv) && prefill) return HS2_ERR_UNSUPPORTED;  // FP8 / FP4 caches: decode only
   if ((long long)max_t > (long long)kv->max_pages * 64) return HS2_ERR_ARG;
   if (prefill && B_or_n > max_t) return HS2_ERR_ARG;
   if (!o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
@@ -460,10 +467,12 @@ static hs2_status fa_select_impl(const void* q, int B_or_n, int Hq, const hs2_kv
   a.part_o = (float*)(ws + p.off_o);
   a.logits = (float*)(ws + p.off_logits);
   a.ld_logits = p.ld;
-  if (kv->dtype == HS2_FP8_E4M3) {
+  if (low_precision(kv)) {
     if (!p.mma) return HS2_ERR_UNSUPPORTED;
     a.k_scale = kv->k_scale;
     a.v_scale = kv->v_scale;
+    a.k_sf = kv->k_sf;
+    a.v_sf = kv->v_sf;
   }
   a.dev_err = dev_err;
   cudaError_t e = profiled(HS2_STAGE_FA_SCAN, s, [&] {
@@ -519,7 +528,7 @@ hs2_status hs2_fa_select_append(const void* q, int B, int Hq, const hs2_kv* kv, 
                                 int32_t* idx, int32_t* idx_cnt, void* workspace, size_t ws_bytes, int32_t* dev_err,
                                 void* stream) {
   if (!kv || !append_rows_ok(kv, k_new, v_new) || !kv->v) return HS2_ERR_ARG;
-  if (kv->dtype == HS2_FP8_E4M3) return HS2_ERR_UNSUPPORTED;
+  if (low_precision(kv)) return HS2_ERR_UNSUPPORTED;
   return fa_select_impl(q, B, Hq, kv, max_t, w, k, scale, 0, sel_block, k_new, v_new, o, lse, idx, idx_cnt, workspace,
                         ws_bytes, dev_err, stream);
 }
@@ -545,7 +554,7 @@ hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, 
   if (w < 0 || k < 0 || !std::isfinite(scale) || !o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
   if (B_or_n == 0) return HS2_OK;
   const SaPlan p = sa_plan(B_or_n, Hq, kv, w, k, prefill);
-  if (kv->dtype == HS2_FP8_E4M3 && !p.stream) return HS2_ERR_UNSUPPORTED;  // FP8: the decode stream only
+  if (low_precision(kv) && !p.stream) return HS2_ERR_UNSUPPORTED;  // FP8 / FP4: the decode stream only
   if (!workspace || ws_bytes < p.total || ((uintptr_t)workspace & 255u)) return HS2_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   char* ws = (char*)workspace;
@@ -578,9 +587,11 @@ hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, 
   a.out_o = o;
   a.sink = sink;
   a.gate = gate;
-  if (kv->dtype == HS2_FP8_E4M3) {
+  if (low_precision(kv)) {
     a.k_scale = kv->k_scale;
     a.v_scale = kv->v_scale;
+    a.k_sf = kv->k_sf;
+    a.v_sf = kv->v_sf;
   }
   a.dev_err = dev_err;
   if (p.stream) {

@@ -125,6 +125,11 @@ HS2_DEVI void cp_async16_keep(uint32_t s, const void* gmem, bool valid, uint64_t
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(s), "l"(gmem), "r"(n), "l"(pol)
                : "memory");
 }
+// 8-byte global -> shared copy (cp.async.ca); zero-fills when `valid` is false.
+HS2_DEVI void cp_async8(uint32_t s, const void* gmem, bool valid) {
+  const int n = valid ? 8 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
 // 4-byte global -> shared copy (cp.async.ca); zero-fills when `valid` is false.
 HS2_DEVI void cp_async4(uint32_t s, const void* gmem, bool valid) {
   const int n = valid ? 4 : 0;
@@ -169,6 +174,25 @@ HS2_DEVI uint4 fp8x8_to_f16x8(uint2 b) {
   fp8x4_to_f16x4(b.y, r.z, r.w);
   return r;
 }
+// 8 E2M1 codes (a 32-bit word; channel 2i in the low nibble of byte i) to 8 f16 as 4 pairs,
+// order kept (cvt.rn.f16x2.e2m1x2 takes the low nibble to the low half).
+HS2_DEVI void fp4x8_to_f16x8(uint32_t w, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm("{\n\t.reg .b8 a, b, c, d;\n\tmov.b32 {a, b, c, d}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, a;\n\tcvt.rn.f16x2.e2m1x2 %1, b;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, c;\n\tcvt.rn.f16x2.e2m1x2 %3, d;\n\t}"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(w));
+}
+// f16 pair product (exact for an E2M1 value times an E4M3 scale: at most 5 significant bits,
+// magnitude within [2^-10, 2688])
+HS2_DEVI uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// The E4M3 scale byte `lo` (and `hi`) as an f16 pair (lo, hi).
+HS2_DEVI uint32_t e4m3_pair(uint32_t lo, uint32_t hi) { return fp8x2_to_f16x2((lo & 0xFFu) | ((hi & 0xFFu) << 8)); }
+
 // (lo, hi) floats to an f16 pair, round to nearest.
 HS2_DEVI uint32_t pack_f16(float lo, float hi) {
   uint32_t r;

@@ -1,4 +1,4 @@
-// fa_decode.cu — bf16 / FP8 split-KV scan of the FA layer (decode and causal rows).
+// fa_decode.cu — bf16 / FP8 / FP4 split-KV scan of the FA layer (decode and causal rows).
 //
 // The FA layer of a HySparse2 Cross group attends to every visible key of the group's
 // shared paged KV ("HySparse2：整体架构、KV 生命周期与 PD 分离", §5; §16.1: the FA layers
@@ -18,16 +18,21 @@ namespace hs2 {
 // ============================================================================ bf16 split-KV FA
 // Per CTA: one (query, KV head, split of `pps` pages); 4 warps take the split's pages
 // round-robin; per warp step: 16 keys (see mma_attn.cuh for the register mappings).
-// FP8 = true: the cache holds E4M3 codes with one scale per (page, KV head); rows load at half
-// the bytes and convert to f16 (exact), the page's K scale multiplies the logits and its V
-// scale the weights entering P.V (mma_attn.cuh, F16 mode).
-constexpr int kRing8 = 3;  // FP8 chunk slots per warp
-// one FP8 slot: 16 K rows, 16 V rows, then k scale, v scale, key0 (padded to 16 bytes)
-template <int D>
-constexpr int fa8_slot_bytes() { return 2 * 16 * D + 16; }
+// FMT = kFaFp8: the cache holds E4M3 codes with one scale per (page, KV head); rows load at
+// half the bytes and convert to f16 (exact), the page's K scale multiplies the logits and its
+// V scale the weights entering P.V (mma_attn.cuh, F16 mode). FMT = kFaFp4: E2M1 codes (a
+// quarter of the bytes) with an E4M3 scale per 16 channels of a row, each value times its
+// group scale in f16 (exact), the slab scales as FP8's.
+constexpr int kFaBf16 = 0, kFaFp8 = 1, kFaFp4 = 2;
+constexpr int kRing8 = 3;  // low-precision chunk slots per warp
+// one low-precision slot: 16 K rows, 16 V rows, (FP4) their group scales, then k scale,
+// v scale, key0 (padded to 16 bytes)
+template <int D, int FMT>
+constexpr int fa8_slot_bytes() { return FMT == kFaFp4 ? 2 * 8 * D + 2 * D + 16 : 2 * 16 * D + 16; }
 
-template <int D, int NT, bool FP8>
-__global__ void __launch_bounds__(128, (FP8 && NT == 1) ? 4 : 0) fa_decode_mma_kernel(const AttnArgs a) {
+template <int D, int NT, int FMT>
+__global__ void __launch_bounds__(128, (FMT != kFaBf16 && NT == 1) ? 4 : 0) fa_decode_mma_kernel(const AttnArgs a) {
+  constexpr bool FP8 = FMT != kFaBf16;  // a low-precision cache (the f16 MMA path)
   using Attn = MmaAttn<D, NT, FP8>;
   constexpr int KC = Attn::KC, VC = Attn::VC;
   const int qi = blockIdx.z, g = blockIdx.y, split = blockIdx.x;
@@ -146,13 +151,21 @@ __global__ void __launch_bounds__(128, (FP8 && NT == 1) ? 4 : 0) fa_decode_mma_k
     // filled by 16-byte cp.async copies, so kRing8 - 1 chunks (12 KB at d = 128) are in
     // flight per warp without holding registers. The 16-byte units of a row are stored
     // XOR-swizzled by the row, which keeps the fragment reads below free of bank conflicts.
-    constexpr int CB = 16 * D;           // bytes of K (or V) in one chunk
-    constexpr int UPR = D / 16;          // 16-byte units per row
-    constexpr int SLOT = fa8_slot_bytes<D>();
+    constexpr bool FP4 = FMT == kFaFp4;
+    constexpr int RB = FP4 ? D / 2 : D;  // bytes per row of codes
+    constexpr int CB = 16 * RB;          // bytes of K (or V) codes in one chunk
+    constexpr int SFB = FP4 ? D : 0;     // bytes of K (or V) group scales in one chunk (16 rows x D/16)
+    constexpr int FT = 2 * CB + 2 * SFB; // the footer: k scale, v scale, key0
+    constexpr int UPR = RB / 16;         // 16-byte units per row
+    constexpr int SLOT = fa8_slot_bytes<D, FMT>();
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kRing8 * SLOT);
     const uint8_t* ring_p = reinterpret_cast<const uint8_t*>(smem) + warp * kRing8 * SLOT;
-    auto swz = [](int row) { return D == 128 ? (row & 7) : ((row >> 1) & 3); };
-    auto unit_off = [&](int row, int c) { return row * D + ((c ^ swz(row)) << 4); };
+    // 16-byte units XOR-swizzled by row: 8 consecutive rows hit 8 distinct bank groups
+    auto swz = [](int row) {
+      if constexpr (FP4) return D == 128 ? ((row >> 1) & 3) : ((row >> 2) & 1);
+      else return D == 128 ? (row & 7) : ((row >> 1) & 3);
+    };
+    auto unit_off = [&](int row, int c) { return row * RB + ((c ^ swz(row)) << 4); };
     float v_unit = 1.f;  // acc holds P.V in units of this V scale
 
     // first page >= pg of this warp with a valid block-table entry (bad ones are flagged)
@@ -168,34 +181,103 @@ __global__ void __launch_bounds__(128, (FP8 && NT == 1) ? 4 : 0) fa_decode_mma_k
     auto issue = [&](int pg, int phys, int ch, int slot) {
       const uint32_t sl = ring + slot * SLOT;
       const size_t ph = (size_t)phys * a.Hkv + g;
-      const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k) + ph * head_stride + (size_t)ch * CB;
-      const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v) + ph * head_stride + (size_t)ch * CB;
+      const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k) + ph * kPage * RB + (size_t)ch * CB;
+      const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v) + ph * kPage * RB + (size_t)ch * CB;
 #pragma unroll
       for (int i = 0; i < CB / 512; ++i) {
         const int u = lane + 32 * i, off = unit_off(u / UPR, u % UPR);
         cp_async16(sl + off, kp + 16 * u, true);
         cp_async16(sl + CB + off, vp + 16 * u, true);
       }
-      if (lane == 0) cp_async4(sl + 2 * CB, a.k_scale + ph, true);
-      if (lane == 1) cp_async4(sl + 2 * CB + 4, a.v_scale + ph, true);
-      if (lane == 2) st_shared_s32(sl + 2 * CB + 8, pg * kPage + ch * 16);
+      if constexpr (FP4) {  // the chunk's 16 rows of group scales: D/16 16-byte units each for K and V
+        const size_t so = (ph * kPage + (size_t)ch * 16) * (D / 16);
+        if (lane < D / 16) cp_async16(sl + 2 * CB + 16 * lane, a.k_sf + so + 16 * lane, true);
+        else if (lane >= 16 && lane < 16 + D / 16)
+          cp_async16(sl + 2 * CB + SFB + 16 * (lane - 16), a.v_sf + so + 16 * (lane - 16), true);
+      }
+      if (lane == 0) cp_async4(sl + FT, a.k_scale + ph, true);
+      if (lane == 1) cp_async4(sl + FT + 4, a.v_scale + ph, true);
+      if (lane == 2) st_shared_s32(sl + FT + 8, pg * kPage + ch * 16);
     };
     auto compute = [&](int slot) {
       const uint8_t* sl = ring_p + slot * SLOT;
-      const float ks = *reinterpret_cast<const float*>(sl + 2 * CB);
-      const float vs = *reinterpret_cast<const float*>(sl + 2 * CB + 4);
-      const int key0 = *reinterpret_cast<const int*>(sl + 2 * CB + 8);
+      const float ks = *reinterpret_cast<const float*>(sl + FT);
+      const float vs = *reinterpret_cast<const float*>(sl + FT + 4);
+      const int key0 = *reinterpret_cast<const int*>(sl + FT + 8);
       if (vs != v_unit && vs != 0.f) {  // acc moves to this page's V scale as its unit
         at.scale_acc(v_unit / vs);
         v_unit = vs;
       }
       uint4 kr0[KC], kr1[KC];
+      if constexpr (FP4) {
+        // 8 values (4 bytes) of rows gid and gid + 8 at channel 32j + 8tig, i.e. unit j,
+        // byte 4tig; times the E4M3 scale of group 2j + tig/2 of that row
+        const uint8_t* ksf = sl + 2 * CB;
 #pragma unroll
-      for (int j = 0; j < KC; ++j) {  // 8 bytes of rows gid and gid + 8 at byte 32j + 8tig
-        const int c = 2 * j + (tig >> 1), h = 8 * (tig & 1);
-        kr0[j] = fp8x8_to_f16x8(*reinterpret_cast<const uint2*>(sl + unit_off(gid, c) + h));
-        kr1[j] = fp8x8_to_f16x8(*reinterpret_cast<const uint2*>(sl + unit_off(gid + 8, c) + h));
+        for (int j = 0; j < KC; ++j) {
+          const int grp = 2 * j + (tig >> 1);
+          const uint32_t sA = e4m3_pair(ksf[gid * (D / 16) + grp], ksf[gid * (D / 16) + grp]);
+          const uint32_t sB = e4m3_pair(ksf[(gid + 8) * (D / 16) + grp], ksf[(gid + 8) * (D / 16) + grp]);
+          uint32_t h0, h1, h2, h3;
+          fp4x8_to_f16x8(*reinterpret_cast<const uint32_t*>(sl + unit_off(gid, j) + 4 * tig), h0, h1, h2, h3);
+          kr0[j] = make_uint4(hmul2(h0, sA), hmul2(h1, sA), hmul2(h2, sA), hmul2(h3, sA));
+          fp4x8_to_f16x8(*reinterpret_cast<const uint32_t*>(sl + unit_off(gid + 8, j) + 4 * tig), h0, h1, h2, h3);
+          kr1[j] = make_uint4(hmul2(h0, sB), hmul2(h1, sB), hmul2(h2, sB), hmul2(h3, sB));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < KC; ++j) {  // 8 bytes of rows gid and gid + 8 at byte 32j + 8tig
+          const int c = 2 * j + (tig >> 1), h = 8 * (tig & 1);
+          kr0[j] = fp8x8_to_f16x8(*reinterpret_cast<const uint2*>(sl + unit_off(gid, c) + h));
+          kr1[j] = fp8x8_to_f16x8(*reinterpret_cast<const uint2*>(sl + unit_off(gid + 8, c) + h));
+        }
       }
+      uint32_t va[Attn::KS][4];
+      if constexpr (FP4) {
+        // V: the lane's D/8 channels (d = (D/8) * gid ...) of keys 2tig, 2tig+1, 2tig+8,
+        // 2tig+9 as D/64 words of 8 codes per key, inside one group of 16 channels
+        constexpr int VW4 = D / 64;
+        const uint8_t* vsf = sl + 2 * CB + SFB;
+        const int grp = (D / 8) * gid / 16;
+        uint32_t vw[4][VW4], vsc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int vrow = 2 * tig + (e & 1) + 8 * (e >> 1);
+          const bool live = key0 + vrow < t && vs != 0.f;  // rows past t: never read their values
+          const int b = (D / 16) * gid;  // byte of the row
+          const uint8_t* src = sl + CB + unit_off(vrow, b >> 4) + (b & 15);
+          if constexpr (VW4 == 2) {
+            const uint2 w = *reinterpret_cast<const uint2*>(src);
+            vw[e][0] = live ? w.x : 0u, vw[e][1] = live ? w.y : 0u;
+          } else {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+            vw[e][0] = live ? w : 0u;
+          }
+          vsc[e] = live ? vsf[vrow * (D / 16) + grp] : 0u;
+        }
+        // interleave two keys' codes: byte i of LO = (key e0, key e1) codes of channel 2i,
+        // of HI the same of channel 2i+1; each byte converts to the (e0, e1) f16 pair
+        const uint32_t s01 = e4m3_pair(vsc[0], vsc[1]), s23 = e4m3_pair(vsc[2], vsc[3]);
+#pragma unroll
+        for (int r = 0; r < VW4; ++r) {
+          const uint32_t lo01 = (vw[0][r] & 0x0F0F0F0Fu) | ((vw[1][r] & 0x0F0F0F0Fu) << 4);
+          const uint32_t hi01 = ((vw[0][r] >> 4) & 0x0F0F0F0Fu) | (vw[1][r] & 0xF0F0F0F0u);
+          const uint32_t lo23 = (vw[2][r] & 0x0F0F0F0Fu) | ((vw[3][r] & 0x0F0F0F0Fu) << 4);
+          const uint32_t hi23 = ((vw[2][r] >> 4) & 0x0F0F0F0Fu) | (vw[3][r] & 0xF0F0F0F0u);
+          uint32_t a0[4], a1[4], a2[4], a3[4];
+          fp4x8_to_f16x8(lo01, a0[0], a0[1], a0[2], a0[3]);
+          fp4x8_to_f16x8(hi01, a1[0], a1[1], a1[2], a1[3]);
+          fp4x8_to_f16x8(lo23, a2[0], a2[1], a2[2], a2[3]);
+          fp4x8_to_f16x8(hi23, a3[0], a3[1], a3[2], a3[3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {  // m-tile 4r + i: channels 8r + 2i, 8r + 2i + 1 of the lane
+            va[4 * r + i][0] = hmul2(a0[i], s01);
+            va[4 * r + i][1] = hmul2(a1[i], s01);
+            va[4 * r + i][2] = hmul2(a2[i], s23);
+            va[4 * r + i][3] = hmul2(a3[i], s23);
+          }
+        }
+      } else {
       // V: the lane's D/8 bytes (d = (D/8) * gid ...) of keys 2tig, 2tig+1, 2tig+8, 2tig+9,
       // as D/32 words per key; rows past t (and a zero V scale) read as zero
       constexpr int VW = D / 32;
@@ -216,13 +298,13 @@ __global__ void __launch_bounds__(128, (FP8 && NT == 1) ? 4 : 0) fa_decode_mma_k
       }
       // V^T A-fragments straight from the bytes: interleave two keys' bytes, then each
       // byte pair converts to the (key, key + 1) f16 pair of one d
-      uint32_t va[Attn::KS][4];
 #pragma unroll
       for (int mt = 0; mt < Attn::KS; ++mt) {
         const int r = mt >> 1;
         const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
         fp8x4_to_f16x4(__byte_perm(vw[0][r], vw[1][r], sel), va[mt][0], va[mt][1]);
         fp8x4_to_f16x4(__byte_perm(vw[2][r], vw[3][r], sel), va[mt][2], va[mt][3]);
+      }
       }
       const int keyA = key0 + gid, keyB = key0 + gid + 8;
       const bool okA = keyA < t, okB = keyB < t;
@@ -286,8 +368,12 @@ template <int D, int NT>
 static cudaError_t launch_mma(const AttnArgs& a, int Bq, cudaStream_t s) {
   dim3 grid(a.nsplit, a.Hkv, Bq);
   const size_t merge = (size_t)(64 * NT + 32 * NT * D) * sizeof(float);
-  const size_t sm = a.k_scale ? std::max(merge, (size_t)4 * kRing8 * fa8_slot_bytes<D>()) : merge;
-  auto kern = a.k_scale ? fa_decode_mma_kernel<D, NT, true> : fa_decode_mma_kernel<D, NT, false>;
+  const int fmt = a.k_sf ? kFaFp4 : a.k_scale ? kFaFp8 : kFaBf16;
+  const size_t ring = (size_t)4 * kRing8 * (fmt == kFaFp4 ? fa8_slot_bytes<D, kFaFp4>() : fa8_slot_bytes<D, kFaFp8>());
+  const size_t sm = fmt != kFaBf16 ? std::max(merge, ring) : merge;
+  auto kern = fmt == kFaFp4   ? fa_decode_mma_kernel<D, NT, kFaFp4>
+              : fmt == kFaFp8 ? fa_decode_mma_kernel<D, NT, kFaFp8>
+                              : fa_decode_mma_kernel<D, NT, kFaBf16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   kern<<<grid, 128, sm, s>>>(a);

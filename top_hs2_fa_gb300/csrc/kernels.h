@@ -35,6 +35,8 @@ struct AttnArgs {
   int32_t* arrive;  // SA stream: per-unit arrival counters, zero at launch
   const float* k_scale;  // FP8 cache: [num_pages][Hkv] dequantisation scales, else null
   const float* v_scale;
+  const uint8_t* k_sf;  // FP4 cache: [num_pages][Hkv][64][D/16] E4M3 scales of 16 channels, else null
+  const uint8_t* v_sf;
   const float* sink;  // SA: [Hq] sink logits (natural log), or null
   const float* gate;  // SA: [Bq][Hq][D] output gate logits, or null
   const void* k_new;  // decode FA with a fused append: [Bq][Hkv][D] rows of key t-1, or null

@@ -36,41 +36,52 @@ template <int D>
 constexpr uint32_t str_slot_bytes() {  // 16 K rows and 16 V rows
   return 2u * (D / 64) * 2048u;
 }
-template <int D>
-constexpr uint32_t str_slot8_bytes() {  // FP8: 16 K rows, 16 V rows (D bytes each), 16 + 16 scales
-  return 2u * 16u * D + 128u;
+// Cache formats of the kernel: bf16 rows, FP8 E4M3 codes, FP4 E2M1 codes with E4M3 group scales.
+constexpr int kFmtBf16 = 0, kFmtFp8 = 1, kFmtFp4 = 2;
+
+template <int D, int FMT>
+constexpr uint32_t str_raw_bytes() {
+  // FP8: 16 K rows, 16 V rows (D bytes each), then 16 + 16 slab scales.
+  // FP4: 16 K rows, 16 V rows (D/2 bytes each), 16 + 16 rows of D/16 group scales, then
+  //      16 + 16 slab scales.
+  return FMT == kFmtFp8 ? 2u * 16u * D + 128u : 18u * D + 128u;
 }
-template <int D, bool FP8>
+template <int D, int FMT>
 constexpr uint32_t str_ring_bytes() {  // per warp, a multiple of 1024
-  return FP8 ? (str_slot_bytes<D>() + kStrStages * str_slot8_bytes<D>() + 1023u) / 1024u * 1024u
-             : kStrStages * str_slot_bytes<D>();
+  return FMT != kFmtBf16 ? (str_slot_bytes<D>() + kStrStages * str_raw_bytes<D, FMT>() + 1023u) / 1024u * 1024u
+                         : kStrStages * str_slot_bytes<D>();
 }
-template <int D, bool FP8>
+template <int D, int FMT>
 constexpr size_t str_warp_bytes() {  // ring + row ids + step table
-  return (size_t)str_ring_bytes<D, FP8>() + (kStrMaxSteps * 16 + 6 * kStrMaxSteps) * sizeof(int32_t);
+  return (size_t)str_ring_bytes<D, FMT>() + (kStrMaxSteps * 16 + 6 * kStrMaxSteps) * sizeof(int32_t);
 }
-template <int D, bool FP8>
+template <int D, int FMT>
 constexpr size_t str_smem_bytes() {
-  return 1024 + 4 * str_warp_bytes<D, FP8>();
+  return 1024 + 4 * str_warp_bytes<D, FMT>();
 }
 
 // Warp holding global step s when `total` steps are cut into `nw` equal ranges
 // [floor(total*w/nw), floor(total*(w+1)/nw)) (every range non-empty when nw <= total).
 HS2_DEVI int warp_of_step(long long s, long long total, int nw) { return (int)(((s + 1) * nw - 1) / total); }
 
-// FP8 = true: the cache holds E4M3 codes with one scale per (page, KV head). A warp's ring then
-// holds raw slots (the 16 K and 16 V rows at D bytes each, plus each entry's K and V scale,
-// staged by cp.async) and one f16 slot: every step converts its raw slot into the f16 slot
-// (exact, the same swizzled layout) and computes from there with per-entry scales.
-template <int D, bool FP8>
+// FMT = kFmtFp8: the cache holds E4M3 codes with one scale per (page, KV head). A warp's ring
+// then holds raw slots (the 16 K and 16 V rows at D bytes each, plus each entry's K and V
+// scale, staged by cp.async) and one f16 slot: every step converts its raw slot into the f16
+// slot (exact, the same swizzled layout) and computes from there with per-entry scales.
+// FMT = kFmtFp4: the same with E2M1 rows (D/2 bytes) and their E4M3 scales of 16 channels
+// staged too; the conversion multiplies each value by its group scale (exact in f16) and the
+// slab scales act as FP8's.
+template <int D, int FMT>
 __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const SaStreamArgs sp) {
+  constexpr bool LOWP = FMT != kFmtBf16;
   constexpr int NT = 1;  // 8 query heads per unit
   constexpr int HALVES = D / 64;
   constexpr int CPR = D / 8;  // 16-byte chunks per bf16 / f16 row
   constexpr int CP8 = D / 16;  // 16-byte chunks per FP8 row
+  constexpr int CP4 = D / 32;  // 16-byte chunks per FP4 row
   constexpr uint32_t kSlot = str_slot_bytes<D>();
-  constexpr uint32_t kSlot8 = str_slot8_bytes<D>();
-  constexpr uint32_t kRing = str_ring_bytes<D, FP8>();
+  constexpr uint32_t kSlot8 = str_raw_bytes<D, FMT>();
+  constexpr uint32_t kRing = str_ring_bytes<D, FMT>();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int wid = blockIdx.x * 4 + warp;
@@ -178,7 +189,30 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
   // the group's SA layers re-read the same rows: ask L2 to keep them
   const uint64_t keep = l2_keep_policy();
   auto issue = [&](int j, int slot) {
-    if (FP8) {
+    if constexpr (FMT == kFmtFp4) {
+      const uint32_t dst = ring + kSlot + (uint32_t)slot * kSlot8;
+      const uint8_t* kb4 = reinterpret_cast<const uint8_t*>(a.k);
+      const uint8_t* vb4 = reinterpret_cast<const uint8_t*>(a.v);
+#pragma unroll
+      for (int m = 0; m < 16 * CP4 / 32; ++m) {
+        const int c = lane + 32 * m;
+        const int r = c / CP4, cc = c % CP4;
+        const int rid = rowid[16 * j + r];
+        const size_t off = (size_t)(rid >= 0 ? rid : 0) * (D / 2) + 16 * cc;
+        cp_async16_keep(dst + r * (D / 2) + 16 * cc, kb4 + off, rid >= 0, keep);
+        cp_async16_keep(dst + 8 * D + r * (D / 2) + 16 * cc, vb4 + off, rid >= 0, keep);
+      }
+      // lanes 0-15: the entries' K group scales, lanes 16-31: their V group scales (D/16 bytes)
+      const int rs = rowid[16 * j + (lane & 15)];
+      const uint8_t* sfs = (lane < 16 ? a.k_sf : a.v_sf) + (size_t)(rs >= 0 ? rs : 0) * (D / 16);
+      const uint32_t sfd = dst + 16 * D + (lane < 16 ? 0 : D) + (lane & 15) * (D / 16);
+      if constexpr (D == 128) cp_async8(sfd, sfs, rs >= 0);
+      else cp_async4(sfd, sfs, rs >= 0);
+      const float* src = (lane < 16 ? a.k_scale : a.v_scale) + (rs >= 0 ? (rs >> 6) : 0);
+      cp_async4(dst + 18 * D + 4 * lane, src, rs >= 0);
+      return;
+    }
+    if (FMT == kFmtFp8) {
       const uint32_t dst = ring + kSlot + (uint32_t)slot * kSlot8;
       const uint8_t* kb8 = reinterpret_cast<const uint8_t*>(a.k);
       const uint8_t* vb8 = reinterpret_cast<const uint8_t*>(a.v);
@@ -214,7 +248,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
     if (j < ns) issue(j, j);
     cp_async_commit();
   }
-  StagedAttn<D, 1, FP8> at;
+  StagedAttn<D, 1, LOWP> at;
   int cur_p = -1;
   for (int j = 0; j < ns; ++j) {
     if (j + kStrStages - 1 < ns) issue(j + kStrStages - 1, (j + kStrStages - 1) % kStrStages);
@@ -229,7 +263,37 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
       cur_p = un;
     }
     const bool okA = rowid[16 * j + gid] >= 0, okB = rowid[16 * j + gid + 8] >= 0;
-    if (FP8) {
+    if constexpr (FMT == kFmtFp4) {
+      // raw slot -> f16 slot: a 16-byte FP4 chunk (32 values of row r, two groups of 16)
+      // becomes four f16 chunks, each value times its group's E4M3 scale
+      const uint8_t* src = ring_g + kSlot + (size_t)(j % kStrStages) * kSlot8;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {  // K, V
+#pragma unroll
+        for (int m = 0; m < 16 * CP4 / 32; ++m) {
+          const int c = lane + 32 * m;
+          const int r = c / CP4, cc = c % CP4;
+          const uint4 raw4 = *reinterpret_cast<const uint4*>(src + part * 8 * D + r * (D / 2) + 16 * cc);
+          const uint8_t* sfr = src + 16 * D + part * D + r * (D / 16) + 2 * cc;
+          const uint32_t s0 = e4m3_pair(sfr[0], sfr[0]), s1 = e4m3_pair(sfr[1], sfr[1]);
+          const uint32_t words[4] = {raw4.x, raw4.y, raw4.z, raw4.w};
+          uint8_t* dst = ring_g + part * HALVES * 2048;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {  // 8 values -> one f16 chunk
+            uint32_t h0, h1, h2, h3;
+            fp4x8_to_f16x8(words[q], h0, h1, h2, h3);
+            const uint32_t sq = q < 2 ? s0 : s1;
+            const int f = 4 * cc + q;  // f16 chunk index of the row
+            *reinterpret_cast<uint4*>(dst + (f >> 3) * 2048 + sw128(r, f & 7)) =
+                make_uint4(hmul2(h0, sq), hmul2(h1, sq), hmul2(h2, sq), hmul2(h3, sq));
+          }
+        }
+      }
+      __syncwarp();
+      const float* scl = reinterpret_cast<const float*>(src + 18 * D);
+      if (__any_sync(0xffffffffu, okA || okB))
+        at.step(ring, okA, okB, a.scale_log2, scl[gid], scl[gid + 8], scl[16 + gid], scl[16 + gid + 8]);
+    } else if (FMT == kFmtFp8) {
       // raw slot -> f16 slot: a 16-byte FP8 chunk (16 values of row r) becomes two f16 chunks
       const uint8_t* src = ring_g + kSlot + (size_t)(j % kStrStages) * kSlot8;
 #pragma unroll
@@ -368,14 +432,14 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
   cp_async_wait<0>();
 }
 
-template <int D, bool FP8>
+template <int D, int FMT>
 static bool stream_plan_t(int G, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
   int dev = 0, sms = 0, per_sm = 0;
-  const size_t sm = str_smem_bytes<D, FP8>();
+  const size_t sm = str_smem_bytes<D, FMT>();
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaFuncSetAttribute(sa_stream_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+      cudaFuncSetAttribute(sa_stream_kernel<D, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sa_stream_kernel<D, FP8>, 128, sm) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sa_stream_kernel<D, FMT>, 128, sm) != cudaSuccess ||
       per_sm < 1) {
     (void)cudaGetLastError();
     return false;
@@ -404,29 +468,39 @@ static bool stream_plan_t(int G, int w, int k, int Bq, int Hkv, SaStreamArgs* sp
   return true;
 }
 
-// kv_dtype: 1 bf16, 2 FP8 E4M3 (others: not this kernel)
-bool sa_stream_plan(int G, int D, int kv_dtype, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
-  if ((kv_dtype != 1 && kv_dtype != 2) || (D != 64 && D != 128) || G < 1 || G > 32) return false;
-  if (kv_dtype == 2)
-    return D == 128 ? stream_plan_t<128, true>(G, w, k, Bq, Hkv, sp, grid)
-                    : stream_plan_t<64, true>(G, w, k, Bq, Hkv, sp, grid);
-  return D == 128 ? stream_plan_t<128, false>(G, w, k, Bq, Hkv, sp, grid)
-                  : stream_plan_t<64, false>(G, w, k, Bq, Hkv, sp, grid);
+template <int FMT>
+static bool stream_plan_f(int G, int D, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
+  return D == 128 ? stream_plan_t<128, FMT>(G, w, k, Bq, Hkv, sp, grid)
+                  : stream_plan_t<64, FMT>(G, w, k, Bq, Hkv, sp, grid);
 }
 
-template <int D, bool FP8>
+// kv_dtype: 1 bf16, 2 FP8 E4M3, 3 FP4 E2M1 (others: not this kernel)
+bool sa_stream_plan(int G, int D, int kv_dtype, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
+  if (kv_dtype < 1 || kv_dtype > 3 || (D != 64 && D != 128) || G < 1 || G > 32) return false;
+  if (kv_dtype == 2) return stream_plan_f<kFmtFp8>(G, D, w, k, Bq, Hkv, sp, grid);
+  if (kv_dtype == 3) return stream_plan_f<kFmtFp4>(G, D, w, k, Bq, Hkv, sp, grid);
+  return stream_plan_f<kFmtBf16>(G, D, w, k, Bq, Hkv, sp, grid);
+}
+
+template <int D, int FMT>
 static cudaError_t launch_stream_t(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
-  const size_t sm = str_smem_bytes<D, FP8>();
-  cudaError_t e = cudaFuncSetAttribute(sa_stream_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  const size_t sm = str_smem_bytes<D, FMT>();
+  cudaError_t e = cudaFuncSetAttribute(sa_stream_kernel<D, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  sa_stream_kernel<D, FP8><<<grid, 128, sm, s>>>(a, sp);
+  sa_stream_kernel<D, FMT><<<grid, 128, sm, s>>>(a, sp);
   return cudaGetLastError();
 }
 
-cudaError_t launch_sa_stream(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
-  const bool fp8 = a.k_scale != nullptr;
-  if (a.D == 128) return fp8 ? launch_stream_t<128, true>(a, sp, grid, s) : launch_stream_t<128, false>(a, sp, grid, s);
-  if (a.D == 64) return fp8 ? launch_stream_t<64, true>(a, sp, grid, s) : launch_stream_t<64, false>(a, sp, grid, s);
+template <int FMT>
+static cudaError_t launch_stream_f(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
+  if (a.D == 128) return launch_stream_t<128, FMT>(a, sp, grid, s);
+  if (a.D == 64) return launch_stream_t<64, FMT>(a, sp, grid, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_sa_stream(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
+  if (a.k_sf) return launch_stream_f<kFmtFp4>(a, sp, grid, s);
+  if (a.k_scale) return launch_stream_f<kFmtFp8>(a, sp, grid, s);
+  return launch_stream_f<kFmtBf16>(a, sp, grid, s);
 }
 }  // namespace hs2

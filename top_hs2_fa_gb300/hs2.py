@@ -16,7 +16,8 @@ import torch
 
 from . import build as _build
 
-F32, BF16, FP8_E4M3 = 0, 1, 2
+ABI_VERSION = 4  # include/hs2.h HS2_ABI_VERSION this binding marshals for
+F32, BF16, FP8_E4M3, FP4_E2M1 = 0, 1, 2, 3
 FULL, REINDEX = 0, 1
 DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH = 1, 2, 4, 8
 EXPORTS = (
@@ -34,6 +35,7 @@ class hs2_kv(ctypes.Structure):
         ("seq_len", ctypes.c_void_p), ("batch", ctypes.c_int32), ("num_pages", ctypes.c_int32),
         ("max_pages", ctypes.c_int32), ("page_size", ctypes.c_int32), ("Hkv", ctypes.c_int32),
         ("d", ctypes.c_int32), ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("k_sf", ctypes.c_void_p), ("v_sf", ctypes.c_void_p),
     ]
 
 
@@ -89,6 +91,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.hs2_fa_select_append.restype = i32
     lib.hs2_fa_select_noalloc_capacity.argtypes = []
     lib.hs2_fa_select_noalloc_capacity.restype = sz
+    if lib.hs2_abi_version() != ABI_VERSION:
+        raise HS2Error(f"libhs2 ABI {lib.hs2_abi_version()} != binding ABI {ABI_VERSION}: rebuild the library")
     _lib = lib
     return lib
 
@@ -115,15 +119,22 @@ def _stream(stream) -> int:
 class KV:
     """Device tensors of one group's paged KV cache."""
 
-    k: torch.Tensor  # [num_pages][Hkv][64][d], float32, bfloat16 or uint8 (FP8 E4M3 codes)
-    v: torch.Tensor | None
+    k: torch.Tensor  # [num_pages][Hkv][64][d], float32, bfloat16 or uint8 (FP8 E4M3 codes);
+    v: torch.Tensor | None  # FP4: uint8 [num_pages][Hkv][64][d/2], two E2M1 codes per byte
     block_table: torch.Tensor  # int32 [B][max_pages]
     seq_len: torch.Tensor  # int32 [B]
-    k_scale: torch.Tensor | None = None  # FP8: float32 [num_pages][Hkv]
+    k_scale: torch.Tensor | None = None  # FP8 / FP4: float32 [num_pages][Hkv]
     v_scale: torch.Tensor | None = None
+    k_sf: torch.Tensor | None = None  # FP4: uint8 E4M3 [num_pages][Hkv][64][d/16]
+    v_sf: torch.Tensor | None = None
 
     def c(self) -> hs2_kv:
-        if self.k.dtype == torch.uint8:
+        d = int(self.k.shape[3])
+        if self.k.dtype == torch.uint8 and self.k_sf is not None:
+            dt, d = FP4_E2M1, 2 * d
+            if self.k_scale is None or (self.v is not None and (self.v_scale is None or self.v_sf is None)):
+                raise HS2Error("an FP4 KV cache needs k_scale, v_scale, k_sf and v_sf")
+        elif self.k.dtype == torch.uint8:
             dt = FP8_E4M3
             if self.k_scale is None or (self.v is not None and self.v_scale is None):
                 raise HS2Error("an FP8 KV cache needs k_scale and v_scale")
@@ -131,13 +142,13 @@ class KV:
             dt = BF16 if self.k.dtype == torch.bfloat16 else F32
         else:
             raise HS2Error(f"unsupported KV dtype {self.k.dtype}")
-        for t in (self.k, self.v, self.block_table, self.seq_len, self.k_scale, self.v_scale):
+        for t in (self.k, self.v, self.block_table, self.seq_len, self.k_scale, self.v_scale, self.k_sf, self.v_sf):
             if t is not None and not t.is_contiguous():
                 raise HS2Error("KV tensors must be contiguous")
         return hs2_kv(_ptr(self.k), _ptr(self.v), _ptr(self.block_table), _ptr(self.seq_len),
                       int(self.seq_len.shape[0]), int(self.k.shape[0]), int(self.block_table.shape[1]),
-                      int(self.k.shape[2]), int(self.k.shape[1]), int(self.k.shape[3]), dt,
-                      _ptr(self.k_scale), _ptr(self.v_scale))
+                      int(self.k.shape[2]), int(self.k.shape[1]), d, dt,
+                      _ptr(self.k_scale), _ptr(self.v_scale), _ptr(self.k_sf), _ptr(self.v_sf))
 
 
 def _workspace(nbytes: int, device, ws):
