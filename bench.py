@@ -131,6 +131,73 @@ def pinned_copies(h_in, d_in, xs, dev, as_bf16):
         d_in.append(torch.empty(h_in[-1].shape, dtype=h_in[-1].dtype, device=dev))
 
 
+class StepIO:
+    """Host <-> device traffic of one end-to-end step, overlapped with the step's kernels.
+
+    Inputs and outputs are tagged by the layer that reads or writes them. At the start of a
+    step a copy stream (after everything before the step) uploads the inputs in tag order,
+    recording an event per tag; a layer waits only for its own inputs (need). When a layer
+    is done, the copy stream downloads its outputs (done) while later layers compute; the
+    step ends when both streams have finished (end). Every byte still crosses every step."""
+
+    def __init__(self, dev):
+        import torch
+
+        self.cs = torch.cuda.Stream(device=dev)
+        self.inputs, self.outputs, self.ev_in, self.ev_out = {}, {}, {}, {}
+
+    def add_in(self, tag, h, d):
+        import torch
+
+        self.inputs.setdefault(tag, []).append((h, d))
+        self.ev_in.setdefault(tag, torch.cuda.Event())
+
+    def add_out(self, tag, h, d):
+        import torch
+
+        self.outputs.setdefault(tag, []).append((h, d))
+        self.ev_out.setdefault(tag, torch.cuda.Event())
+
+    def begin(self, st):
+        import torch
+
+        self.cs.wait_stream(st)
+        with torch.cuda.stream(self.cs):
+            for tag, pairs in self.inputs.items():
+                for h, d in pairs:
+                    d.copy_(h, non_blocking=True)
+                self.ev_in[tag].record(self.cs)
+
+    def need(self, st, tag):
+        if tag in self.ev_in:
+            st.wait_event(self.ev_in[tag])
+
+    def done(self, st, tag):
+        import torch
+
+        if tag not in self.outputs:
+            return
+        self.ev_out[tag].record(st)
+        self.cs.wait_event(self.ev_out[tag])
+        with torch.cuda.stream(self.cs):
+            for h, d in self.outputs[tag]:
+                h.copy_(d, non_blocking=True)
+
+    def end(self, st):
+        st.wait_stream(self.cs)
+
+
+class _NoIO:
+    def need(self, st, tag):
+        pass
+
+    def done(self, st, tag):
+        pass
+
+
+NO_IO = _NoIO()
+
+
 # ============================================================================ scenarios
 class Decode:
     """Decode step of one or more Cross groups: per group hs2_fa_select + 5 x hs2_sa_reuse."""
@@ -212,9 +279,10 @@ class Decode:
         self.units_per_step = self.B
         self.launches_per_step = self.groups * (3 + NSA) + (1 if self.append == "batched" else 0)
 
-    def step(self, stream, err, qs=None, profile=None):
+    def step(self, stream, err, qs=None, profile=None, io=NO_IO):
         hs2 = self.hs2
         if self.append == "batched":  # every group's new entry in one launch
+            io.need(stream, "append")
             hs2.hs2_kv_append([d["kv"] for d in self.dev], [d["k_new"] for d in self.dev],
                               [d["v_new"] for d in self.dev], dev_err=err, stream=stream)
         fused = self.append == "fused"
@@ -222,30 +290,48 @@ class Decode:
             q = qs[gi] if qs is not None else d["q"]
             if profile is not None and gi == 0:
                 hs2.hs2_profile_next(hs2.STAGE_FA_SCAN, *profile)
+            io.need(stream, ("fa", gi))
             hs2.hs2_fa_select(q[0], d["kv"], self.w, self.k, self.host[gi].scale, max_t=d["max_t"],
                               out=(d["o"][0], d["lse"], d["idx"], d["cnt"]), workspace=d["ws_fa"], dev_err=err,
                               stream=stream, sel_block=self.sel_block, k_new=d["k_new"] if fused else None,
                               v_new=d["v_new"] if fused else None)
+            io.done(stream, ("fa", gi))
             for j in range(NSA):
+                io.need(stream, ("sa", gi, j))
                 hs2.hs2_sa_reuse(q[1 + j], d["kv"], self.w, d["idx"], d["cnt"], self.k, self.host[gi].scale,
                                  out=d["o"][1 + j], workspace=d["ws_sa"], dev_err=err, stream=stream)
+                io.done(stream, ("sa", gi, j))
 
     def e2e_buffers(self, dev):
-        """Pinned host inputs (every layer's queries, table, lengths) and outputs (all layers, indices)."""
+        """Pinned host inputs (every layer's queries, table, lengths, new rows) and outputs (all
+        layers, indices), tagged by the layer that reads or writes them (StepIO)."""
         import torch
 
         self.h_in, self.d_in, self.h_out, self.d_out, self.q_views = [], [], [], [], []
-        for grp, d in zip(self.host, self.dev):
-            pinned_copies(self.h_in, self.d_in, [grp.q_fa, *grp.q_sa], dev, True)
-            self.q_views.append([x.view(torch.bfloat16) for x in self.d_in[-(1 + NSA):]])
+        self.io = StepIO(dev)
+        for gi, (grp, d) in enumerate(zip(self.host, self.dev)):
+            n0 = len(self.d_in)
             pinned_copies(self.h_in, self.d_in, [grp.kv.block_table, grp.kv.seq_len], dev, False)
             self.d_in[-2:] = [d["kv"].block_table, d["kv"].seq_len]
+            tags = [("fa", gi), ("fa", gi)]
+            pinned_copies(self.h_in, self.d_in, [grp.q_fa, *grp.q_sa], dev, True)
+            self.q_views.append([x.view(torch.bfloat16) for x in self.d_in[-(1 + NSA):]])
+            tags += [("fa", gi)] + [("sa", gi, j) for j in range(NSA)]
             if self.append:  # the new token's rows arrive with the step's inputs
                 pinned_copies(self.h_in, self.d_in, [grp.k_new, grp.v_new], dev, True)
                 self.d_in[-2:] = [d["k_new"].view(torch.int16), d["v_new"].view(torch.int16)]
-            for t in [*d["o"], d["idx"], d["cnt"]]:
+                tags += [("fa", gi) if self.append == "fused" else "append"] * 2
+            for tag, h, dd in zip(tags, self.h_in[n0:], self.d_in[n0:]):
+                self.io.add_in(tag, h, dd)
+            outs = [(("fa", gi), d["o"][0]), (("fa", gi), d["idx"]), (("fa", gi), d["cnt"])]
+            outs += [(("sa", gi, j), d["o"][1 + j]) for j in range(NSA)]
+            for tag, t in outs:
                 self.h_out.append(torch.empty(t.shape, dtype=t.dtype).pin_memory())
                 self.d_out.append(t)
+                self.io.add_out(tag, self.h_out[-1], t)
+        if self.append == "batched":  # the append runs first: its rows lead the uploads
+            first = self.io.inputs.pop("append")
+            self.io.inputs = {"append": first, **self.io.inputs}
 
     def config(self):
         return {"workload": self.name, "batch": self.B,
@@ -320,19 +406,24 @@ class Prefill:
         self.units_per_step = n
         self.launches_per_step = 3 + NSA
 
-    def step(self, stream, err, qs=None, profile=None):
+    def step(self, stream, err, qs=None, profile=None, io=NO_IO):
         hs2, d, g = self.hs2, self.dev[0], self.host[0]
         q = qs[0] if qs is not None else d["q"]
         if profile is not None:
             hs2.hs2_profile_next(hs2.STAGE_FA_SCAN, *profile)
+        io.need(stream, ("fa", 0))
         hs2.hs2_fa_select(q[0], d["kv"], self.w, self.k, g.scale, prefill=True,
                           out=(d["o"][0], d["lse"], d["idx"], d["cnt"]), workspace=d["ws_fa"], dev_err=err,
                           stream=stream)
+        io.done(stream, ("fa", 0))
         for j in range(NSA):
+            io.need(stream, ("sa", 0, j))
             hs2.hs2_sa_reuse(q[1 + j], d["kv"], self.w, d["idx"], d["cnt"], self.k, g.scale, prefill=True,
                              out=d["o"][1 + j], workspace=d["ws_sa"], dev_err=err, stream=stream)
+            io.done(stream, ("sa", 0, j))
 
     e2e_buffers = Decode.e2e_buffers
+    append = None
     groups = 1
 
     def config(self):
@@ -408,36 +499,49 @@ class Csa2:
         self.units_per_step = B
         self.launches_per_step = 3 + 2 + 5 * 2
 
-    def step(self, stream, err, qs=None, profile=None):
+    def step(self, stream, err, qs=None, profile=None, io=NO_IO):
         hs2, d, g = self.hs2, self.dev[0], self.host[0]
         q = qs[0] if qs is not None else d["q"]
         if profile is not None:
             hs2.hs2_profile_next(hs2.STAGE_INDEXER, *profile)
         for mode in (hs2.FULL, hs2.REINDEX):
+            io.need(stream, ("layer", mode))
             hs2.hs2_hier_reindex(mode, d["qi"][mode], d["wi"][mode], d["kidx"], self.k_top, 8, self.max_blocks,
                                  pool_blocks=d["pool"], pool_cnt=d["pcnt"], max_t=self.t,
                                  out=(d["idx"][mode].view(self.B, self.k_top), d["cnt"][mode].view(self.B)),
                                  workspace=d["ws_i"], dev_err=err, stream=stream)
             hs2.hs2_sa_reuse(q[mode], d["kv"], 0, d["idx"][mode], d["cnt"][mode], self.k_top, g.scale,
                              out=d["o"][mode], workspace=d["ws_sa"], dev_err=err, stream=stream)
+            io.done(stream, ("layer", mode))
         for j in range(2, 5):  # Reuse layers read the Reindex layer's indices
+            io.need(stream, ("layer", j))
             hs2.hs2_sa_reuse(q[j], d["kv"], 0, d["idx"][1], d["cnt"][1], self.k_top, g.scale, out=d["o"][j],
                              workspace=d["ws_sa"], dev_err=err, stream=stream)
+            io.done(stream, ("layer", j))
 
     def e2e_buffers(self, dev):
         import torch
 
         g, d = self.host[0], self.dev[0]
         self.h_in, self.d_in, self.h_out, self.d_out = [], [], [], []
-        pinned_copies(self.h_in, self.d_in, g.q_main, dev, True)
-        self.q_views = [[x.view(torch.bfloat16) for x in self.d_in]]
+        self.io = StepIO(dev)
         pinned_copies(self.h_in, self.d_in, g.q_idx, dev, True)
         self.d_in[-2:] = [t.view(torch.int16) for t in d["qi"]]
         pinned_copies(self.h_in, self.d_in, g.w_idx, dev, False)
         self.d_in[-2:] = d["wi"]
-        for t in [*d["o"], *d["idx"], *d["cnt"], d["pool"], d["pcnt"]]:
+        pinned_copies(self.h_in, self.d_in, g.q_main, dev, True)
+        self.q_views = [[x.view(torch.bfloat16) for x in self.d_in[-5:]]]
+        tags = [("layer", 0), ("layer", 1)] * 2 + [("layer", j) for j in range(5)]
+        order = [0, 2, 4, 1, 3, 5, 6, 7, 8]  # by the layer that needs them: Full's first
+        for i in order:
+            self.io.add_in(tags[i], self.h_in[i], self.d_in[i])
+        outs = [(("layer", j), d["o"][j]) for j in range(5)]
+        outs += [(("layer", m), d["idx"][m]) for m in range(2)] + [(("layer", m), d["cnt"][m]) for m in range(2)]
+        outs += [(("layer", 1), d["pool"]), (("layer", 1), d["pcnt"])]
+        for tag, t in outs:
             self.h_out.append(torch.empty(t.shape, dtype=t.dtype).pin_memory())
             self.d_out.append(t)
+            self.io.add_out(tag, self.h_out[-1], t)
 
     def config(self):
         return {"workload": self.name, "batch": self.B, "seq_len": self.t, "Hq": self.Hq, "Hkv": 1,
@@ -611,12 +715,12 @@ def run_gpu(args, rank, world, local_rank):
     d2h = sum(x.numel() * x.element_size() for x in sc.h_out)
 
     def e2e_body():
+        # uploads and downloads on a copy stream, each layer waiting for its own inputs and
+        # its outputs leaving while later layers run (StepIO)
         st = torch.cuda.current_stream()
-        for h, d in zip(sc.h_in, sc.d_in):
-            d.copy_(h, non_blocking=True)
-        sc.step(st, err, qs=sc.q_views)
-        for h, d in zip(sc.h_out, sc.d_out):
-            h.copy_(d, non_blocking=True)
+        sc.io.begin(st)
+        sc.step(st, err, qs=sc.q_views, io=sc.io)
+        sc.io.end(st)
 
     e2e_step = graph_of(e2e_body, stream) if args.graph else e2e_body
 
