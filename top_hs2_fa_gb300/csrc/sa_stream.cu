@@ -71,7 +71,9 @@ HS2_DEVI int warp_of_step(long long s, long long total, int nw) { return (int)((
 // FMT = kFmtFp4: the same with E2M1 rows (D/2 bytes) and their E4M3 scales of 16 channels
 // staged too; the conversion multiplies each value by its group scale (exact in f16) and the
 // slab scales act as FP8's.
-template <int D, int FMT>
+// EPI = true: the SA layer has a sink bias or an output gate (sa_norm_factor, sa_gate); false
+// keeps the plain 1 / L epilogue, whose smaller register footprint the streaming loop feels.
+template <int D, int FMT, bool EPI>
 __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const SaStreamArgs sp) {
   constexpr bool LOWP = FMT != kFmtBf16;
   constexpr int NT = 1;  // 8 query heads per unit
@@ -344,14 +346,23 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
         for (int hs = 0; hs < 2; ++hs) {
           const int hl = nt * 8 + 2 * tig + hs;
           if (hl < Gh) {
-            const int hq = g * G + h0 + hl;  // query head
-            const float inv = sa_norm_factor(at.m[nt][hs], lsum[nt][hs], sink_b2(a.sink, hq)) * at.unit();
-            const float* gl = a.gate ? a.gate + ((size_t)qi * a.Hq + hq) * D : nullptr;
+            if constexpr (EPI) {
+              const int hq = g * G + h0 + hl;  // query head
+              const float inv = sa_norm_factor(at.m[nt][hs], lsum[nt][hs], sink_b2(a.sink, hq)) * at.unit();
+              const float* gl = a.gate ? a.gate + ((size_t)qi * a.Hq + hq) * D : nullptr;
 #pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-              const int d0 = 16 * mt + gid;
-              out[hl * D + d0] = at.acc[mt][nt][hs] * inv * (gl ? sa_gate(gl[d0]) : 1.f);
-              out[hl * D + d0 + 8] = at.acc[mt][nt][hs + 2] * inv * (gl ? sa_gate(gl[d0 + 8]) : 1.f);
+              for (int mt = 0; mt < D / 16; ++mt) {
+                const int d0 = 16 * mt + gid;
+                out[hl * D + d0] = at.acc[mt][nt][hs] * inv * (gl ? sa_gate(gl[d0]) : 1.f);
+                out[hl * D + d0 + 8] = at.acc[mt][nt][hs + 2] * inv * (gl ? sa_gate(gl[d0 + 8]) : 1.f);
+              }
+            } else {
+              const float inv = (lsum[nt][hs] > 0.f ? 1.f / lsum[nt][hs] : 0.f) * at.unit();
+#pragma unroll
+              for (int mt = 0; mt < D / 16; ++mt) {
+                out[hl * D + 16 * mt + gid] = at.acc[mt][nt][hs] * inv;
+                out[hl * D + 16 * mt + gid + 8] = at.acc[mt][nt][hs + 2] * inv;
+              }
             }
           }
         }
@@ -394,7 +405,8 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
       const float M = warp_max(mlv[h].x);
       f[h] = lane < nc ? exp2_rel(mlv[h].x, M) : 0.f;
       const float L = warp_sum(f[h] * mlv[h].y);
-      inv[h] = sa_norm_factor(M, L, h < Gh ? sink_b2(a.sink, g * G + h0 + h) : -INFINITY);
+      if constexpr (EPI) inv[h] = sa_norm_factor(M, L, h < Gh ? sink_b2(a.sink, g * G + h0 + h) : -INFINITY);
+      else inv[h] = L > 0.f ? 1.f / L : 0.f;
     }
     float4 o4[8];
 #pragma unroll
@@ -418,7 +430,7 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
     for (int h = 0; h < 8; ++h)
       if (h < Gh && 4 * lane < D) {
         float4 r4 = make_float4(o4[h].x * inv[h], o4[h].y * inv[h], o4[h].z * inv[h], o4[h].w * inv[h]);
-        if (a.gate) {
+        if (EPI && a.gate) {
           const float4 g4 = __ldg(reinterpret_cast<const float4*>(a.gate + ((size_t)qi * a.Hq + g * G + h0 + h) * D) + lane);
           r4.x *= sa_gate(g4.x);
           r4.y *= sa_gate(g4.y);
@@ -434,16 +446,20 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
 
 template <int D, int FMT>
 static bool stream_plan_t(int G, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid) {
-  int dev = 0, sms = 0, per_sm = 0;
+  int dev = 0, sms = 0, per_sm = 0, per_sm2 = 0;
   const size_t sm = str_smem_bytes<D, FMT>();
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaFuncSetAttribute(sa_stream_kernel<D, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+      cudaFuncSetAttribute(sa_stream_kernel<D, FMT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sa_stream_kernel<D, FMT>, 128, sm) != cudaSuccess ||
-      per_sm < 1) {
+      cudaFuncSetAttribute(sa_stream_kernel<D, FMT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sa_stream_kernel<D, FMT, true>, 128, sm) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm2, sa_stream_kernel<D, FMT, false>, 128, sm) != cudaSuccess ||
+      std::min(per_sm, per_sm2) < 1) {
     (void)cudaGetLastError();
     return false;
   }
+  per_sm = std::min(per_sm, per_sm2);  // the grid is sized for the variant with fewer resident CTAs
   const int hg = (G + 7) / 8;  // units of 8 query heads per (row, KV head)
   const int ms = (w + k + 15) / 16;
   const long long total = (long long)Bq * Hkv * hg * ms;
@@ -485,9 +501,10 @@ bool sa_stream_plan(int G, int D, int kv_dtype, int w, int k, int Bq, int Hkv, S
 template <int D, int FMT>
 static cudaError_t launch_stream_t(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s) {
   const size_t sm = str_smem_bytes<D, FMT>();
-  cudaError_t e = cudaFuncSetAttribute(sa_stream_kernel<D, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  auto kern = (a.sink || a.gate) ? sa_stream_kernel<D, FMT, true> : sa_stream_kernel<D, FMT, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  sa_stream_kernel<D, FMT><<<grid, 128, sm, s>>>(a, sp);
+  kern<<<grid, 128, sm, s>>>(a, sp);
   return cudaGetLastError();
 }
 
