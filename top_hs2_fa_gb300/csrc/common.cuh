@@ -64,12 +64,25 @@ HS2_DEVI uint64_t l2_keep_policy() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// (any L2 policy: keep or evict-first)
 HS2_DEVI uint4 ldg_nc_v4_keep(const void* p, uint64_t pol) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p), "l"(pol));
   return r;
+}
+
+// L2 cache policy that evicts lines first: for data read exactly once (the FA scan's K/V
+// stream), so it does not push out what the next kernel reads.
+HS2_DEVI uint64_t l2_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// fp32 store with an L2 cache policy
+HS2_DEVI void stg_f32_pol(float* p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
 }
 
 HS2_DEVI uint2 ldg_nc_v2(const void* p) {

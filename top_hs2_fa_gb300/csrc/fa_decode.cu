@@ -58,6 +58,9 @@ __global__ void __launch_bounds__(128, (FMT != kFaBf16 && NT == 1) ? 4 : 0) fa_d
   const size_t head_stride = (size_t)kPage * D;  // elements per (page, KV head)
   float* logit_base = a.logits ? a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits : nullptr;
 
+  // The K/V stream is read once: evict it first. The base-2 logits are read by the
+  // selection right after this kernel: keep them.
+  const uint64_t pol_stream = l2_first_policy(), pol_keep = l2_keep_policy();
   // base-2 logits of one 16-key chunk for the selection
   auto write_logits = [&](const float (&x)[NT][4], int keyA, int keyB, bool okA, bool okB) {
     if (!logit_base) return;
@@ -65,12 +68,12 @@ __global__ void __launch_bounds__(128, (FMT != kFaBf16 && NT == 1) ? 4 : 0) fa_d
     for (int nt = 0; nt < NT; ++nt) {
       const int h0 = nt * 8 + 2 * tig;
       if (h0 < G) {
-        if (okA) logit_base[(size_t)h0 * a.ld_logits + keyA] = x[nt][0];
-        if (okB) logit_base[(size_t)h0 * a.ld_logits + keyB] = x[nt][2];
+        if (okA) stg_f32_pol(logit_base + (size_t)h0 * a.ld_logits + keyA, x[nt][0], pol_keep);
+        if (okB) stg_f32_pol(logit_base + (size_t)h0 * a.ld_logits + keyB, x[nt][2], pol_keep);
       }
       if (h0 + 1 < G) {
-        if (okA) logit_base[(size_t)(h0 + 1) * a.ld_logits + keyA] = x[nt][1];
-        if (okB) logit_base[(size_t)(h0 + 1) * a.ld_logits + keyB] = x[nt][3];
+        if (okA) stg_f32_pol(logit_base + (size_t)(h0 + 1) * a.ld_logits + keyA, x[nt][1], pol_keep);
+        if (okB) stg_f32_pol(logit_base + (size_t)(h0 + 1) * a.ld_logits + keyB, x[nt][3], pol_keep);
       }
     }
   };
@@ -105,15 +108,15 @@ __global__ void __launch_bounds__(128, (FMT != kFaBf16 && NT == 1) ? 4 : 0) fa_d
         uint4 kr0[KC], kr1[KC], vr[4][VC];
 #pragma unroll
         for (int j = 0; j < KC; ++j) {
-          kr0[j] = ldg_nc_v4(kA + 32 * j + 8 * tig);
-          kr1[j] = ldg_nc_v4(kB + 32 * j + 8 * tig);
+          kr0[j] = ldg_nc_v4_keep(kA + 32 * j + 8 * tig, pol_stream);
+          kr1[j] = ldg_nc_v4_keep(kB + 32 * j + 8 * tig, pol_stream);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int vrow = ch * 16 + 2 * tig + (e & 1) + 8 * (e >> 1);
           const __nv_bfloat16* vsrc = (tail && page * kPage + vrow == t - 1) ? v_new_row : vp + (size_t)vrow * D;
 #pragma unroll
-          for (int j = 0; j < VC; ++j) vr[e][j] = ldg_nc_v4(vsrc + (D / 8) * gid + 8 * j);
+          for (int j = 0; j < VC; ++j) vr[e][j] = ldg_nc_v4_keep(vsrc + (D / 8) * gid + 8 * j, pol_stream);
         }
         if (tail) {  // write-through of the new rows (each element by exactly one lane)
           __nv_bfloat16* kw = const_cast<__nv_bfloat16*>(kp) + (size_t)((t - 1) % kPage) * D;
@@ -186,8 +189,8 @@ __global__ void __launch_bounds__(128, (FMT != kFaBf16 && NT == 1) ? 4 : 0) fa_d
 #pragma unroll
       for (int i = 0; i < CB / 512; ++i) {
         const int u = lane + 32 * i, off = unit_off(u / UPR, u % UPR);
-        cp_async16(sl + off, kp + 16 * u, true);
-        cp_async16(sl + CB + off, vp + 16 * u, true);
+        cp_async16_keep(sl + off, kp + 16 * u, true, pol_stream);
+        cp_async16_keep(sl + CB + off, vp + 16 * u, true, pol_stream);
       }
       if constexpr (FP4) {  // the chunk's 16 rows of group scales: D/16 16-byte units each for K and V
         const size_t so = (ph * kPage + (size_t)ch * 16) * (D / 16);

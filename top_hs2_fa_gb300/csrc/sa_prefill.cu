@@ -31,7 +31,7 @@ namespace hs2 {
 constexpr int kSaMaxSplit = 8;  // portable cluster size
 
 template <int D, int NT>
-__global__ void __launch_bounds__(128) sa_mma_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(128, NT == 1 ? 4 : 0) sa_mma_kernel(const AttnArgs a) {
   using Attn = MmaAttn<D, NT>;
   constexpr int KC = Attn::KC, VC = Attn::VC;
   const int qi = blockIdx.y, g = blockIdx.x;
