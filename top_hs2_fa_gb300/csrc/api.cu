@@ -165,7 +165,10 @@ IdxPlan idx_plan(hs2_idx_mode mode, int B, int max_t, int max_blocks) {
 // 2-D bf16 tensor map: rows x cols (cols contiguous), box of 64 columns x box_rows rows,
 // 128-byte swizzle. cuTensorMapEncodeTiled is fetched from the driver at run time so the
 // library has no link-time dependency on libcuda.
-bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+// rows x cols bf16, tiles of box_rows x 64 in the 128-byte swizzle. row_step > 1: a view of
+// every row_step-th row (rows / row_step view rows, row stride row_step * cols * 2 bytes).
+bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows,
+                    uint32_t row_step = 1) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -177,8 +180,8 @@ bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t 
     }
     encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
   }
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint64_t dims[2] = {cols, rows / row_step};
+  const cuuint64_t strides[1] = {cols * 2 * row_step};
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -348,7 +351,10 @@ static hs2_status fa_select_prefill_tc(const void* q, int n, int Hq, const hs2_k
   for (int r0 = 0; r0 < n; r0 += p.chunk) {
     b.row0 = r0;
     b.row1 = std::min(n, r0 + p.chunk);
-    e = hs2::launch_prefill_select(tq, tk, b, s);
+    // the sampled sweep of the selection scan reads every 4th key (kPsSampleStride) only
+    CUtensorMap tks;
+    if (!encode_2d_bf16(&tks, kv->k, 128, rows, hs2::kPsSampleRowsPerPage, hs2::kPsSampleStride)) return HS2_ERR_ARG;
+    e = hs2::launch_prefill_select(tq, tk, tks, b, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return HS2_OK;

@@ -183,7 +183,12 @@ cudaError_t launch_select_rows(const SelectArgs& a, int B, cudaStream_t s);
 cudaError_t launch_prefill_trivial_select(int32_t* idx, int32_t* cnt, int n, int Hkv, int w, int k, cudaStream_t s);
 size_t fa_prefill_fwd_smem();
 size_t prefill_scan_smem();
-cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, const PsArgs& a, cudaStream_t s);
+// The selection scan's sampled sweep: every kPsSampleStride-th key, through a tensor map of
+// those rows only (box: the kPsSampleRowsPerPage sampled rows of a 64-row page).
+constexpr int kPsSampleStride = 4;
+constexpr int kPsSampleRowsPerPage = 64 / kPsSampleStride;
+cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tks,
+                                  const PsArgs& a, cudaStream_t s);
 cudaError_t launch_fa_prefill_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PfArgs& a,
                                   cudaStream_t s);
 

@@ -7,7 +7,8 @@
 // a tcgen05 recomputation of Q K^T and consumed on the fly.
 //
 // prefill_scan_kernel — one CTA per (128-row tile, KV head), one row per scoring thread:
-//   sweep 0 (sampled): every key tile, every 4th column; each thread bins the sampled
+//   sweep 0 (sampled): every 4th key position only, 128 of them per tile (512 positions;
+//            a strided tensor map loads just those K rows); each thread bins the sampled
 //            scores of its row into a 256-bin log histogram (1/8 octave per bin) held in
 //            shared memory, then picks a threshold tau whose estimated count of keys at or
 //            above it is twice the budget;
@@ -37,9 +38,12 @@ constexpr int kSThreads = 320;  // TMA warp, MMA warp, 8 scoring warps (two per 
 constexpr uint32_t kSTile = kST * 128 * 2;
 constexpr int kBins = 256;
 constexpr uint32_t kBinBase = 0x410 - (kBins - 1);  // bin 255 holds keys >> 20 == 0x410 (score 8.0)
-// The sampled sweep scores every 4th position of every key tile (position-correlated
-// scores would bias a sample of whole tiles).
-constexpr int kSampleStride = 4;
+// The sampled sweep scores every 4th position (position-correlated scores would bias a
+// sample of whole tiles); a sampled key tile holds 128 such positions, 512 apart at most.
+constexpr int kSampleStride = kPsSampleStride;
+constexpr int kSampSpan = kST * kSampleStride;                // positions covered by a sampled key tile
+constexpr int kSampPages = kSampSpan / kPage;                 // pages of a sampled key tile (8)
+constexpr uint32_t kSampBoxBytes = kPsSampleRowsPerPage * 128;  // one 64-column half of a page's sampled rows
 
 constexpr int kQStages = 2;
 
@@ -63,7 +67,7 @@ HS2_DEVI void set_abort(PsSmem& sm, int32_t* dev_err) {
 
 __global__ void __launch_bounds__(kSThreads, 1)
     prefill_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const PsArgs a) {
+                        const __grid_constant__ CUtensorMap tm_ks, const PsArgs a) {
   extern __shared__ __align__(1024) uint8_t dsmem[];
   PsSmem& sm = *reinterpret_cast<PsSmem*>(dsmem + ((1024 - (tc::smem_u32(dsmem) & 1023)) & 1023));
   const int tiles = (a.row1 - a.row0 + kST - 1) / kST;
@@ -73,7 +77,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int i_last = min(a.row1, i0 + kST) - 1;
   const int keys_needed = max(0, i_last + 1 - a.w);
   const int J = (keys_needed + kST - 1) / kST;  // key tiles of the exact sweep
-  const int J0 = J;                             // sampled sweep: every key tile, every 4th column
+  const int J0 = (keys_needed + kSampSpan - 1) / kSampSpan;  // sampled sweep: tiles of sampled keys
   const int NKT = J0 + J;                       // key-tile items over both sweeps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = a.seq_len[0];
@@ -115,22 +119,43 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int ks = kt & 1;
         if (!tc::mbar_wait(&sm.k_empty[ks], ((kt >> 1) & 1) ^ 1)) { set_abort(sm, a.dev_err); break; }
         const int j = jof(kt);
-        int rows[2];
-        uint32_t bytes = 0;
-        for (int pg = 0; pg < 2; ++pg) {
-          const int lp = 2 * j + pg;
-          rows[pg] = -1;
-          if (lp < npages) {
-            const int phys = a.bt[lp];
-            if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
-            else { rows[pg] = (phys * a.Hkv + g) * kPage; bytes += 2 * 8192; }
+        if (kt < J0) {
+          // sampled keys: rows 0, 4, ..., 60 of each of 8 pages, 16 tile rows per page
+          int rows[kSampPages];
+          uint32_t bytes = 0;
+          for (int pg = 0; pg < kSampPages; ++pg) {
+            const int lp = kSampPages * j + pg;
+            rows[pg] = -1;
+            if (lp < npages) {
+              const int phys = a.bt[lp];
+              if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+              else { rows[pg] = (phys * a.Hkv + g) * kPsSampleRowsPerPage; bytes += 2 * kSampBoxBytes; }
+            }
           }
+          tc::mbar_arrive_expect_tx(&sm.k_full[ks], bytes);
+          for (int pg = 0; pg < kSampPages; ++pg)
+            if (rows[pg] >= 0)
+              for (int hh = 0; hh < 2; ++hh)
+                tc::tma_load_2d(sm.k[ks] + hh * 16384 + pg * kSampBoxBytes, &tm_ks, 64 * hh, rows[pg],
+                                &sm.k_full[ks]);
+        } else {
+          int rows[2];
+          uint32_t bytes = 0;
+          for (int pg = 0; pg < 2; ++pg) {
+            const int lp = 2 * j + pg;
+            rows[pg] = -1;
+            if (lp < npages) {
+              const int phys = a.bt[lp];
+              if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+              else { rows[pg] = (phys * a.Hkv + g) * kPage; bytes += 2 * 8192; }
+            }
+          }
+          tc::mbar_arrive_expect_tx(&sm.k_full[ks], bytes);
+          for (int pg = 0; pg < 2; ++pg)
+            if (rows[pg] >= 0)
+              for (int hh = 0; hh < 2; ++hh)
+                tc::tma_load_2d(sm.k[ks] + hh * 16384 + pg * 8192, &tm_k, 64 * hh, rows[pg], &sm.k_full[ks]);
         }
-        tc::mbar_arrive_expect_tx(&sm.k_full[ks], bytes);
-        for (int pg = 0; pg < 2; ++pg)
-          if (rows[pg] >= 0)
-            for (int hh = 0; hh < 2; ++hh)
-              tc::tma_load_2d(sm.k[ks] + hh * 16384 + pg * 8192, &tm_k, 64 * hh, rows[pg], &sm.k_full[ks]);
         kissued = kt + 1;
         bool ok = true;
         for (int hl = 0; hl < G; ++hl) {
@@ -221,15 +246,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         tc::tmem_regs_ready(raw[0]);
         tc::tc_fence_before();
         tc::mbar_arrive(&sm.s_empty[sb]);
-        if (sample) {
 #pragma unroll
-          for (int e = 0; e < 64; e += kSampleStride)
-            sc[e] += tc::ex2(fmaf(__uint_as_float(raw[e >> 5][e & 31]), a.scale_log2, -l2));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; ++e)
-            sc[e] += tc::ex2(fmaf(__uint_as_float(raw[e >> 5][e & 31]), a.scale_log2, -l2));
-        }
+        for (int e = 0; e < 64; ++e) sc[e] += tc::ex2(fmaf(__uint_as_float(raw[e >> 5][e & 31]), a.scale_log2, -l2));
       }
       if (!ok) break;
       if (half == 1) {
@@ -249,9 +267,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (!ranked) {
         // rows whose far range fits the budget keep no candidates
       } else if (sample) {
+        // column e of a sampled tile is position j * kSampSpan + kSampleStride * e
 #pragma unroll
-        for (int e = 0; e < 128; e += kSampleStride) {
-          if (s0 + e < nF) {
+        for (int e = 0; e < 128; ++e) {
+          if (j * kSampSpan + kSampleStride * e < nF) {
             const float v = e < 64 ? sc[e] : sc2[e - 64];
             const int bin = min(kBins - 1, max(0, (int)(__float_as_uint(v) >> 20) - (int)kBinBase));
             const uint8_t hv = sm.hist[bin][r];
@@ -393,12 +412,13 @@ __global__ void __launch_bounds__(kTopkThreads) prefill_topk_kernel(const PsArgs
 
 size_t prefill_scan_smem() { return sizeof(PsSmem) + 1024; }
 
-cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, const PsArgs& a, cudaStream_t s) {
+cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tks,
+                                  const PsArgs& a, cudaStream_t s) {
   const size_t sm = prefill_scan_smem();
   cudaError_t e = cudaFuncSetAttribute(prefill_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   const int tiles = (a.row1 - a.row0 + kST - 1) / kST;
-  prefill_scan_kernel<<<dim3(tiles, a.Hkv), kSThreads, sm, s>>>(tq, tk, a);
+  prefill_scan_kernel<<<dim3(tiles, a.Hkv), kSThreads, sm, s>>>(tq, tk, tks, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.cap > kTopkThreads * kTopkSeg) return cudaErrorInvalidValue;
