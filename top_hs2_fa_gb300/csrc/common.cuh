@@ -91,6 +91,9 @@ HS2_DEVI uint2 ldg_nc_v2(const void* p) {
   return r;
 }
 
+// Barrier `id` (1..15) over `n` threads (a multiple of 32) of the CTA.
+HS2_DEVI void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
 HS2_DEVI void flag_error(int32_t* dev_err, int bits) {
   if (dev_err) atomicOr(dev_err, bits);
 }

@@ -52,6 +52,7 @@ struct PsSmem {
   uint8_t k[2][kSTile];            // B of S (keys x d)
   uint8_t hist[kBins][kST];        // per-row sample histograms ([bin][row]), saturating counts
   float xch[64][kST];              // columns 64-127 of a key tile's scores, handed to the row owner
+  float lse2[32][kST];             // the rows' base-2 lse of each query head of the KV head (G <= 32)
   uint64_t q_full[kQStages], q_empty[kQStages], k_full[2], k_empty[2], s_full[2], s_empty[2], x_full, x_empty;
   uint32_t tmem_base;
   int abort;
@@ -217,6 +218,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const bool ranked = nF > a.k;  // rows whose far range fits the budget need no candidates
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const float* lse2_row = a.lse2 + (size_t)(row_ok ? i : a.row0) * a.Hq + g * G;
+    // the row's lse of every head, once: the per-tile head loop reads them from shared memory
+    // (each scoring thread of the pair holding row r writes half of them)
+    for (int hl = half; hl < G; hl += 2) sm.lse2[hl][r] = __ldg(lse2_row + hl);
+    named_bar_sync(1, 256);
     const size_t slot = ((size_t)(i - a.row0) * a.Hkv + g) * a.cap;
     uint32_t* bkey = a.cand_key + slot;
     int32_t* bpos = a.cand_pos + slot;
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (!__all_sync(0xffffffffu, !aborted(sm) && tc::mbar_wait(&sm.s_full[sb], (it >> 1) & 1))) { ok = false; break; }
         __syncwarp();
         tc::tc_fence_after();
-        const float l2 = __ldg(lse2_row + hl);
+        const float l2 = sm.lse2[hl][r];
         uint32_t raw[2][32];
         const uint32_t ta = tS + lane_off + sb * 128 + half * 64;
         tc::tmem_ld32_async(ta, raw[0]);
