@@ -23,6 +23,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "mma_attn.cuh"
+#include "staged_attn.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -174,6 +175,144 @@ __global__ void __launch_bounds__(128, NT == 1 ? 4 : 0) sa_mma_kernel(const Attn
   cluster.sync();
 }
 
+// ============================================================================ staged variant
+// Prefill with at most 8 query heads per KV head: the same CTA per (row, KV head) and steps
+// per warp, but each warp streams its steps through a 2-slot shared-memory ring (cp.async,
+// zero rows for invalid entries, 128-byte swizzle), so the next step's rows are in flight
+// from L2 while the current one is contracted from shared memory (ldmatrix + mma.sync,
+// staged_attn.cuh). The warps' merge buffers reuse the rings once the stream is done.
+constexpr int kStgSlots = 2;
+template <int D>
+constexpr uint32_t stg_slot_bytes() {  // 16 K rows and 16 V rows
+  return 2u * (D / 64) * 2048u;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128, 3) sa_staged_kernel(const AttnArgs a) {
+  constexpr int HALVES = D / 64;
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  constexpr uint32_t kSlot = stg_slot_bytes<D>();
+  const int qi = blockIdx.y, g = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gid = lane >> 2;
+  const int G = a.G;  // <= 8
+  const QueryGeom qg = query_geom(qi, a.prefill, a.seq_len);
+  const int t = qg.t;
+  float* out = a.out_o + ((size_t)qi * a.Hq + (size_t)g * G) * D;
+  if (t < 1 || t > a.max_t || (t + kPage - 1) / kPage > a.max_pages) {
+    if (tid == 0) flag_error(a.dev_err, HS2_DEV_BAD_LENGTH);
+    for (int e = tid; e < G * D; e += 128) out[e] = 0.f;
+    return;
+  }
+  const int nW = min(a.w, t);
+  const int c0 = a.cnt[(size_t)qi * a.Hkv + g];
+  if (tid == 0 && (c0 < 0 || c0 > a.kcap)) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+  const int nS = max(0, min(a.kcap, c0));
+  const int nU = nW + nS;
+  const int32_t* sel = a.idx + ((size_t)qi * a.Hkv + g) * a.kcap;
+  const int32_t* bt = a.bt + (size_t)qg.b * a.max_pages;
+  const int lim = a.w > 0 ? t - a.w : t;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // the swizzled slots want 1024-byte alignment
+  uint8_t* basep = smem_raw + (base - raw);
+  int32_t* rowid = reinterpret_cast<int32_t*>(basep + 4 * kStgSlots * kSlot);  // [nU] pool row, -1 invalid
+
+  for (int u = tid; u < nU; u += 128) {
+    int pos, r = -1;
+    bool ok = true;
+    if (u < nW) {
+      pos = t - nW + u;
+    } else {
+      pos = __ldcs(&sel[u - nW]);  // read once: do not keep in L2
+      if (pos < 0 || pos >= lim) {
+        flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+        ok = false;
+      }
+    }
+    if (ok) {
+      const int phys = bt[pos / kPage];
+      if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+      else r = (phys * a.Hkv + g) * kPage + pos % kPage;
+    }
+    rowid[u] = r;
+  }
+  StagedAttn<D, 1> at;
+  at.init(reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)qi * a.Hq + (size_t)g * G) * D, G);
+  __syncthreads();
+
+  const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(a.v);
+  const uint64_t keep = l2_keep_policy();  // rows are re-read by other rows' CTAs
+  const uint32_t ring = base + (uint32_t)warp * kStgSlots * kSlot;
+  auto issue = [&](int st, int slot) {
+    const uint32_t dst = ring + (uint32_t)slot * kSlot;
+#pragma unroll
+    for (int m = 0; m < 16 * CPR / 32; ++m) {
+      const int c = lane + 32 * m;
+      const int r = c / CPR, cc = c % CPR;
+      const int u = st * 16 + r;
+      const int rid = u < nU ? rowid[u] : -1;
+      const size_t off = (size_t)(rid >= 0 ? rid : 0) * D + 8 * cc;
+      const uint32_t so = (uint32_t)(cc >> 3) * 2048u + sw128(r, cc & 7);
+      cp_async16_keep(dst + so, kb + off, rid >= 0, keep);
+      cp_async16_keep(dst + HALVES * 2048u + so, vb + off, rid >= 0, keep);
+    }
+  };
+  const int nsteps = (nU + 15) / 16;
+  if (warp < nsteps) issue(warp, 0);
+  cp_async_commit();
+  int li = 0;
+  for (int st = warp; st < nsteps; st += 4, ++li) {
+    if (st + 4 < nsteps) issue(st + 4, (li + 1) & 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // this step's copies (issued one step earlier) have landed
+    __syncwarp();
+    const int ua = st * 16 + gid, ub = ua + 8;
+    const bool okA = ua < nU && rowid[ua] >= 0, okB = ub < nU && rowid[ub] >= 0;
+    if (__any_sync(0xffffffffu, okA || okB)) at.step(ring + (uint32_t)(li & 1) * kSlot, okA, okB, a.scale_log2);
+    __syncwarp();  // the slot is refilled by the next issue
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // the merge buffers below reuse the rings
+  float* sm_m = reinterpret_cast<float*>(basep);  // [4][8]
+  float* sm_l = sm_m + 4 * 8;                      // [4][8]
+  float* sm_o = sm_l + 4 * 8;                      // [4][8][D]
+  at.store(warp, sm_m, sm_l, sm_o);
+  __syncthreads();
+  for (int e = tid; e < G * D; e += 128) {
+    const int hl = e / D, dd = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w * 8 + hl]);
+    float L = 0.f, Ov = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float f = exp2_rel(sm_m[w * 8 + hl], M);
+      L += f * sm_l[w * 8 + hl];
+      Ov += f * sm_o[((size_t)w * 8 + hl) * D + dd];
+    }
+    const int hq = g * G + hl;
+    float v = Ov * sa_norm_factor(M, L, sink_b2(a.sink, hq));
+    if (a.gate) v *= sa_gate(__ldcs(&a.gate[((size_t)qi * a.Hq + hq) * D + dd]));
+    __stcs(&out[e], v);  // streaming store: keep L2 for the K/V rows
+  }
+}
+
+static size_t sa_staged_smem(int D, long long w, long long k) {
+  return 1024 + 4 * kStgSlots * (size_t)(D == 128 ? stg_slot_bytes<128>() : stg_slot_bytes<64>()) + (size_t)(w + k) * 4;
+}
+
+template <int D>
+static cudaError_t launch_sa_staged_t(const AttnArgs& a, int Bq, cudaStream_t s) {
+  const size_t sm = sa_staged_smem(D, a.w, a.kcap);
+  cudaError_t e = cudaFuncSetAttribute(sa_staged_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  sa_staged_kernel<D><<<dim3(a.Hkv, Bq), 128, sm, s>>>(a);
+  return cudaGetLastError();
+}
+
 static long long sa_mma_smem(int NT, int D, long long w, long long k) {
   return (64LL * NT + 32LL * NT * D + 16LL * NT + 8LL * NT * D) * 4 + (w + k) * 4;
 }
@@ -220,6 +359,9 @@ bool sa_mma_supported(int G, int D, int bf16, int w, int k) {
 
 cudaError_t launch_sa_mma(const AttnArgs& a, int Bq, cudaStream_t s) {
   const int NTl = (a.G + 7) / 8;
+  // prefill rows fill the GPU on their own: the staged stream for up to 8 heads per KV head
+  if (a.prefill && NTl == 1 && sa_staged_smem(a.D, a.w, a.kcap) <= 227u * 1024u)
+    return a.D == 128 ? launch_sa_staged_t<128>(a, Bq, s) : launch_sa_staged_t<64>(a, Bq, s);
   if (a.D == 128) {
     switch (NTl) {
       case 1: return launch_sa_mma_t<128, 1>(a, Bq, s);
