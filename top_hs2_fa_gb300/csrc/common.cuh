@@ -110,6 +110,10 @@ HS2_DEVI float warp_sum(float v) {
   return v;
 }
 
+// Weights are computed against a running max that may lag the true one by up to this
+// much (base 2), i.e. they are at most 2^8: well inside bf16, f16 and fp32 range.
+constexpr float kLazyRescale = 8.f;
+
 // exp2 of a (possibly -inf) base-2 logit relative to a (possibly -inf) max:
 // a row whose max is still -inf contributes exactly zero.
 HS2_DEVI float exp2_rel(float x, float m) { return (m == -INFINITY) ? 0.f : exp2f(x - m); }

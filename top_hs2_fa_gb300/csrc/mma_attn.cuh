@@ -22,10 +22,6 @@
 
 namespace hs2 {
 
-// Weights are computed against a running max that may lag the true one by up to this
-// much (base 2), i.e. they are at most 2^8: well inside bf16, f16 and fp32 range.
-constexpr float kLazyRescale = 8.f;
-
 template <int D, int NT, bool F16 = false>
 struct MmaAttn {
   static constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of PV

@@ -83,9 +83,13 @@ struct StagedAttn {
     const int lane = threadIdx.x & 31;
     const int mi = lane >> 3, rr = lane & 7;
     float sc[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
     {
+      // even and odd k-steps accumulate apart (two independent MMA chains), then add
+      float s2[2][NT][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) s2[u][nt][0] = s2[u][nt][1] = s2[u][nt][2] = s2[u][nt][3] = 0.f;
       // matrices: (entries 0-7 | 8-15) x (d +0 | +8): a0 = (0-7, +0), a1 = (8-15, +0), a2 = (0-7, +8), a3 = (8-15, +8)
       const int row = rr + 8 * (mi & 1), dsub = 8 * (mi >> 1);
 #pragma unroll
@@ -94,8 +98,12 @@ struct StagedAttn {
         uint32_t a[4];
         ldsm_x4(slot + (d0 >> 6) * 2048 + sw128(row, (d0 & 63) >> 3), a);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma(sc[nt], a[0], a[1], a[2], a[3], qb[s][nt][0], qb[s][nt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma(s2[s & 1][nt], a[0], a[1], a[2], a[3], qb[s][nt][0], qb[s][nt][1]);
       }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sc[nt][i] = s2[0][nt][i] + s2[1][nt][i];
     }
     if (F16) {
       // a step whose largest |V scale| (vsA / vsB depend on gid only) exceeds the unit makes
@@ -124,24 +132,37 @@ struct StagedAttn {
       x[1] = okA ? sc[nt][1] * (scale_log2 * ksA) : -INFINITY;
       x[2] = okB ? sc[nt][2] * (scale_log2 * ksB) : -INFINITY;
       x[3] = okB ? sc[nt][3] * (scale_log2 * ksB) : -INFINITY;
-      float p[4];
+      float p[4], cm[2];
+      bool grow = false;
 #pragma unroll
       for (int hs = 0; hs < 2; ++hs) {
-        float cm = fmaxf(x[hs], x[hs + 2]);
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
-        const float mn = fmaxf(m[nt][hs], cm);
-        const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m[nt][hs] - mn);
-        m[nt][hs] = mn;
-        p[hs] = exp2_rel(x[hs], mn);
-        p[hs + 2] = exp2_rel(x[hs + 2], mn);
-        l[nt][hs] *= alpha;
+        cm[hs] = fmaxf(x[hs], x[hs + 2]);
+        cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 4));
+        cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 8));
+        cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 16));
+        grow |= cm[hs] > m[nt][hs] + kLazyRescale;
+      }
+      // lazy rescale: the running max moves (l and acc rescaled) only when a head's step max
+      // exceeds it by more than kLazyRescale, so weights stay <= 2^8; the final normalisation
+      // uses the same max
+      if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          acc[mt][nt][hs] *= alpha;
-          acc[mt][nt][hs + 2] *= alpha;
+        for (int hs = 0; hs < 2; ++hs) {
+          const float mn = fmaxf(m[nt][hs], cm[hs]);
+          const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m[nt][hs] - mn);
+          m[nt][hs] = mn;
+          l[nt][hs] *= alpha;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            acc[mt][nt][hs] *= alpha;
+            acc[mt][nt][hs + 2] *= alpha;
+          }
         }
+      }
+#pragma unroll
+      for (int hs = 0; hs < 2; ++hs) {
+        p[hs] = exp2_rel(x[hs], m[nt][hs]);
+        p[hs + 2] = exp2_rel(x[hs + 2], m[nt][hs]);
       }
       uint32_t pA, pB;  // entry gid / gid+8, heads 2tig, 2tig+1
       if (F16) {
