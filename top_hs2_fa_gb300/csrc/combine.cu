@@ -126,26 +126,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_score_kernel(const Combin
   float sc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (s0 < nF) {
     const float* lg = a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits + s0;
-    // heads in groups of 4: the group's 8 loads are all in flight before the first use
-    for (int hb = 0; hb < G; hb += 4) {
-      float4 x0[4], x1[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (hb + u < G) {
-          x0[u] = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)(hb + u) * a.ld_logits));
-          x1[u] = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)(hb + u) * a.ld_logits + 4));
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (hb + u < G) {
-          const float l2 = lse2_s[hb + u];
-          sc[0] += exp2f(x0[u].x - l2); sc[1] += exp2f(x0[u].y - l2);
-          sc[2] += exp2f(x0[u].z - l2); sc[3] += exp2f(x0[u].w - l2);
-          sc[4] += exp2f(x1[u].x - l2); sc[5] += exp2f(x1[u].y - l2);
-          sc[6] += exp2f(x1[u].z - l2); sc[7] += exp2f(x1[u].w - l2);
-        }
-      }
+    for (int h = 0; h < G; ++h) {
+      const float4 x0 = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)h * a.ld_logits));
+      const float4 x1 = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)h * a.ld_logits + 4));
+      const float l2 = lse2_s[h];
+      sc[0] += exp2f(x0.x - l2); sc[1] += exp2f(x0.y - l2); sc[2] += exp2f(x0.z - l2); sc[3] += exp2f(x0.w - l2);
+      sc[4] += exp2f(x1.x - l2); sc[5] += exp2f(x1.y - l2); sc[6] += exp2f(x1.z - l2); sc[7] += exp2f(x1.w - l2);
     }
   }
   uint32_t key[8];
