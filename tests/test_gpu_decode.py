@@ -309,6 +309,33 @@ def test_fp4_kv_rejects_prefill(H):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("fmt", ["fp8", "fp4"])
+def test_low_precision_kv_sink_and_gate(H, fmt):
+    """The FP8 / FP4 SA stream with the sink bias and the output gate (its richer epilogue
+    variant), against the oracle on the same codes and scales."""
+    import torch
+
+    lens = [900, 2500, 130, 4000]
+    make = W.decode_group_fp8 if fmt == "fp8" else W.decode_group_fp4
+    grp = make(lens, 32, 4, 128, 32, 100, seed=19, n_sa=1, needles=4)
+    kv = grp.kv
+    dkv = kv_to_device(kv)
+    _, _, idx, cnt = H.hs2_fa_select(to_torch(grp.q_fa, "bf16"), dkv, grp.w, grp.k, grp.scale,
+                                     max_t=int(kv.seq_len.max()))
+    rng = np.random.default_rng(4)
+    sink = rng.normal(0.0, 2.0, 32).astype(np.float32)
+    sink[0], sink[1] = -np.inf, 30.0
+    gate = rng.normal(0.0, 2.0, (len(lens), 32, 128)).astype(np.float32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    osa = H.hs2_sa_reuse(to_torch(grp.q_sa[0], "bf16"), dkv, grp.w, idx, cnt, grp.k, grp.scale, dev_err=err,
+                         sink=torch.from_numpy(sink).cuda(), gate=torch.from_numpy(gate).cuda()).cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = O.sa_decode(grp.q_sa[0], kv, grp.w, idx.cpu().numpy(), cnt.cpu().numpy(), grp.scale, sink=sink, gate=gate)
+    assert max_abs(osa, ref) <= tol("bf16"), max_abs(osa, ref)
+    assert np.abs(osa[:, 1]).max() < 1e-6  # the dominant sink takes the head's mass
+
+
 def test_fp8_kv_rejects_prefill(H):
     import torch
 
