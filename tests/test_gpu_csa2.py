@@ -122,6 +122,29 @@ def test_indexer_rejects_unsupported(H):
         H.hs2_hier_reindex(H.FULL, q, to_torch(grp.w_idx[0], "f32"), kidx, 8, 16, 4)
 
 
+@pytest.mark.parametrize("distinct", [7, 300])
+def test_indexer_cluster_selection_with_ties(H, distinct):
+    """Few long rows (the multi-CTA cluster selection) whose indexer keys repeat `distinct`
+    rows, so scores tie exactly: the GPU's top-k (positions) and block pool must equal the
+    oracle's element by element (ties to the lower position / block). 7 distinct rows put
+    thousands of candidates on the k-th key's digit (the single-CTA fallback passes); 300
+    keep them within the candidate buffer (the cluster path)."""
+    grp = W.csa2_group([40000, 29000], Hq=8, d=128, Hi=64, di=128, k_top=256, blk=8, max_blocks=512,
+                       n_reuse=1, needles=0, seed=13)
+    kx = grp.kidx
+    rng = np.random.default_rng(14)
+    P, _, S, d = kx.k.shape
+    src = kx.k.reshape(P * S, d)
+    pick = rng.integers(0, distinct, size=P * S)
+    kx.k = np.ascontiguousarray(src[:distinct][pick].reshape(P, 1, S, d))
+    idx_f, cnt_f, pool, pcnt, _, _ = run_group(H, grp, 512, 256)
+    o_idx, o_cnt, o_pool, o_pcnt = O.indexer_full(grp.q_idx[0], grp.w_idx[0], kx, 256, 8, 512)
+    np.testing.assert_array_equal(cnt_f, o_cnt)
+    np.testing.assert_array_equal(idx_f, o_idx)
+    np.testing.assert_array_equal(pcnt, o_pcnt)
+    np.testing.assert_array_equal(pool, o_pool)
+
+
 @pytest.mark.slow
 def test_csa2_full_size_sampled(H):
     """CSA2 decode at full size (B=8, t=131072, 64 indexer heads, top-512, 2048-block pool):

@@ -19,9 +19,15 @@
 //                     (candidates) lists in shared memory; a radix select over the
 //                     candidates alone fixes the k-th key and the ties to take; the two
 //                     sorted lists are merged into the ascending output (topk.cuh).
+#include <cooperative_groups.h>
+
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "topk.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace hs2 {
 
@@ -154,11 +160,55 @@ __global__ void __launch_bounds__(kMergeThreads) merge_score_kernel(const Combin
 
 // Shared memory of the selection kernels: A list (kcap), chosen-C list (kcap), C list.
 constexpr int kFilterCap = 4096;
-static size_t select_smem(int kcap) { return (size_t)2 * kcap * sizeof(int) + (size_t)kFilterCap * sizeof(uint2); }
+static size_t select_smem(int kcap) {
+  return (size_t)2 * kcap * sizeof(int) + (size_t)kFilterCap * sizeof(uint2) + 2 * sizeof(int);
+}
 
+// The CTAs of one cluster share one row's selection (cluster_filter_topk; a cluster of one
+// CTA takes filter_topk); the fallback passes over all keys run on rank 0 alone.
+struct ClusterSel {
+  int rank, n;
+  HS2_DEVI ClusterSel() : rank((int)cg::this_cluster().block_rank()), n((int)cg::this_cluster().num_blocks()) {}
+  HS2_DEVI void sync() const { cg::this_cluster().sync(); }
+  template <typename T>
+  HS2_DEVI T* remote(T* p, int r) const {
+    return cg::this_cluster().map_shared_rank(p, r);
+  }
+};
+
+// Launch `kern` on grid (gx * csize, gy) in clusters of csize CTAs along x.
+template <typename Args>
+static cudaError_t launch_clustered(void (*kern)(Args), int gx, int gy, size_t smem, int csize, cudaStream_t s,
+                                    const Args& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(gx * csize, gy);
+  cfg.blockDim = dim3(kSelectThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+// CTAs per row selection: one per 8192 keys of the longest row, at most 8 (portable
+// clusters), and only while the rows alone leave the GPU idle (a few long CSA2 rows); with
+// hundreds of rows (decode) one CTA per row is faster (measured 26.6 vs 76.9 us at 4 CTAs).
+static int sel_cluster_size(long long max_keys, long long rows) {
+  int c = (int)std::min<long long>(8, std::max<long long>(1, (max_keys + 8191) / 8192));
+  while (c > 1 && rows * c > 2 * 152) --c;
+  return c;
+}
+
+// grid: clusters of CTAs along x (sel_cluster_size), one cluster per (query, KV head)
 __global__ void __launch_bounds__(kSelectThreads, 2) select_kernel(const CombineArgs a) {
   constexpr int NT = kSelectThreads;
-  const int g = blockIdx.x, qi = blockIdx.y;
+  const ClusterSel cl;
+  const int g = blockIdx.x / cl.n, qi = blockIdx.y;
   const QueryGeom qg = query_geom(qi, a.prefill, a.seq_len);
   const int t = qg.t;
   if ((t < 1) || (t > a.max_t) || ((t + kPage - 1) / kPage > a.max_pages)) return;
@@ -170,13 +220,19 @@ __global__ void __launch_bounds__(kSelectThreads, 2) select_kernel(const Combine
   int* la = fbuf;
   int* lsel = la + a.kcap;
   uint2* lc = reinterpret_cast<uint2*>(lsel + a.kcap);
+  int* meta = reinterpret_cast<int*>(lc + kFilterCap);
   const uint32_t* gkeys = a.scores + ((size_t)qi * a.Hkv + g) * a.ld_logits;
   const uint32_t* gh = a.hist + ((size_t)qi * a.Hkv + g) * kRadixBins;
   int32_t* out = a.idx + ((size_t)qi * a.Hkv + g) * a.kcap;
   auto emit = [&](int j, int i) { out[j] = i; };
-  if (filter_topk<NT, 16>(gkeys, nF, kk, gh, la, a.kcap, lc, kFilterCap, lsel, emit, sm)) return;
+  if (cl.n == 1 ? filter_topk<NT, 16>(gkeys, nF, kk, gh, la, a.kcap, lc, kFilterCap, lsel, emit, sm)
+                : cluster_filter_topk<NT, 16>(gkeys, nF, kk, gh, la, a.kcap, lc, kFilterCap, lsel, meta, cl.rank, cl.n,
+                                              emit, [&] { cl.sync(); },
+                                              [&](auto* p, int r) { return cl.remote(p, r); }, sm))
+    return;
   // more candidates share the k-th key's top digit than the buffer holds: radix passes
-  // over all keys
+  // over all keys, on rank 0
+  if (cl.rank != 0) return;
   auto key = [&](int i) { return __ldcg(gkeys + i); };
   block_topk<NT>(nF, kk, key, emit, sm);
 }
@@ -229,9 +285,11 @@ __global__ void __launch_bounds__(kSelectThreads) block_select_kernel(const Comb
 }
 
 // ============================================================================ generic row top-k
+// grid: clusters of CTAs along x (sel_cluster_size), one cluster per sequence
 __global__ void __launch_bounds__(kSelectThreads, 2) select_rows_kernel(const SelectArgs a) {
   constexpr int NT = kSelectThreads;
-  const int b = blockIdx.x;
+  const ClusterSel cl;
+  const int b = blockIdx.x / cl.n;
   const int tid = threadIdx.x;
   const int t = a.seq_len[b];
   int32_t* out = a.out + (size_t)b * a.kcap;
@@ -250,12 +308,15 @@ __global__ void __launch_bounds__(kSelectThreads, 2) select_rows_kernel(const Se
     }
   }
   const int kk = min(a.k, n);
-  if (tid == 0) a.cnt[b] = kk;
-  for (int j = kk + tid; j < a.kcap; j += NT) out[j] = -1;
+  if (cl.rank == 0) {
+    if (tid == 0) a.cnt[b] = kk;
+    for (int j = kk + tid; j < a.kcap; j += NT) out[j] = -1;
+  }
   auto map = [&](int i) { return a.mode == 3 ? pool[i >> 3] * 8 + (i & 7) : i; };
   if (kk == 0) return;
   if (kk == n) {
-    for (int i = tid; i < n; i += NT) out[i] = map(i);
+    if (cl.rank == 0)
+      for (int i = tid; i < n; i += NT) out[i] = map(i);
     return;
   }
   __shared__ TopkSmem<NT> sm;
@@ -263,10 +324,16 @@ __global__ void __launch_bounds__(kSelectThreads, 2) select_rows_kernel(const Se
   int* la = fbuf;
   int* lsel = la + a.kcap;
   uint2* lc = reinterpret_cast<uint2*>(lsel + a.kcap);
+  int* meta = reinterpret_cast<int*>(lc + kFilterCap);
   const uint32_t* gkeys = a.keys + (size_t)b * a.ld_keys;
   const uint32_t* gh = a.hist + (size_t)b * kRadixBins;
   auto emit = [&](int j, int i) { out[j] = map(i); };
-  if (filter_topk<NT, 16>(gkeys, n, kk, gh, la, a.kcap, lc, kFilterCap, lsel, emit, sm)) return;
+  if (cl.n == 1 ? filter_topk<NT, 16>(gkeys, n, kk, gh, la, a.kcap, lc, kFilterCap, lsel, emit, sm)
+                : cluster_filter_topk<NT, 16>(gkeys, n, kk, gh, la, a.kcap, lc, kFilterCap, lsel, meta, cl.rank, cl.n,
+                                              emit, [&] { cl.sync(); },
+                                              [&](auto* p, int r) { return cl.remote(p, r); }, sm))
+    return;
+  if (cl.rank != 0) return;
   auto key = [&](int i) { return __ldcg(gkeys + i); };
   block_topk<NT>(n, kk, key, emit, sm);
 }
@@ -275,8 +342,8 @@ cudaError_t launch_select_rows(const SelectArgs& a, int B, cudaStream_t s) {
   const size_t sm = select_smem(a.kcap);
   cudaError_t e = cudaFuncSetAttribute(select_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  select_rows_kernel<<<B, kSelectThreads, sm, s>>>(a);
-  return cudaGetLastError();
+  const long long n_max = a.mode == 1 ? a.max_t : a.mode == 2 ? (a.max_t + 7) / 8 : 8LL * a.max_blocks;
+  return launch_clustered(select_rows_kernel, B, 1, sm, sel_cluster_size(n_max, B), s, a);
 }
 
 // Prefill rows i whose far range F(i+1) = [0, i+1-w) fits the budget take all of it.
@@ -316,8 +383,7 @@ cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s) {
   const size_t sm = select_smem(a.kcap);
   e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  select_kernel<<<dim3(a.Hkv, Bq), kSelectThreads, sm, s>>>(a);
-  return cudaGetLastError();
+  return launch_clustered(select_kernel, a.Hkv, Bq, sm, sel_cluster_size(a.ld_logits, (long long)a.Hkv * Bq), s, a);
 }
 
 }  // namespace hs2

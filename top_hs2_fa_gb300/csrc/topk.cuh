@@ -270,4 +270,104 @@ __device__ bool filter_topk(const uint32_t* gkeys, int n, int kk, const uint32_t
   return true;
 }
 
+// filter_topk over a thread-block cluster: the kk-th key's digit d comes from the global
+// histogram in every CTA (the same value everywhere); CTA `rank` of `nrank` splits its
+// contiguous slice [lo, hi) of the keys (lo a multiple of 4) into its own A and C lists;
+// rank 0 gathers every CTA's C list through distributed shared memory, in rank order (so in
+// index order), refines it by radix select and keeps the chosen part in lsel; then every CTA
+// emits its own A entries and the chosen entries inside its slice at their global output
+// slots (the A counts of the lower ranks plus the local merge rank). `cta_sync` is the
+// cluster barrier and `remote(ptr, r)` maps a shared-memory pointer to rank r's copy. Returns
+// false, uniformly and before any cluster barrier, when a list would overflow (the caller
+// then runs the single-CTA fallback on rank 0). meta: 2 ints of shared memory.
+template <int NT, int V, typename EmitFn, typename SyncFn, typename RemoteFn>
+__device__ bool cluster_filter_topk(const uint32_t* gkeys, int n, int kk, const uint32_t* ghist, int* la, int cap_a,
+                                    uint2* lc, int cap_c, int* lsel, int* meta, int rank, int nrank, EmitFn emit,
+                                    SyncFn cta_sync, RemoteFn remote, TopkSmem<NT>& sm) {
+  static_assert(V % 4 == 0 && NT * V < 65536, "chunk counts are packed in 16 bits");
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kRadixBins; i += NT) sm.hist[i] = __ldcg(ghist + i);
+  __syncthreads();
+  int remaining = kk;
+  const uint32_t d = find_digit<NT>(sm.hist, kRadixBins, remaining, sm);
+  const int nA = kk - remaining, nC = (int)sm.hist[d];
+  if (nC > cap_c || nA > cap_a) return false;  // uniform across the cluster
+  const int per = (((n + nrank - 1) / nrank) + 3) & ~3;
+  const int lo = min(n, rank * per), hi = min(n, lo + per);
+  int baseA = 0, baseC = 0;
+  for (int c0 = lo; c0 < hi; c0 += NT * V) {
+    const int i0 = c0 + tid * V;
+    uint32_t kv[V];
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q) {
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
+      if (i0 + 4 * q < hi) x = __ldcg(reinterpret_cast<const uint4*>(gkeys + i0 + 4 * q));
+      kv[4 * q] = x.x;
+      kv[4 * q + 1] = x.y;
+      kv[4 * q + 2] = x.z;
+      kv[4 * q + 3] = x.w;
+    }
+    int ca = 0, cc = 0;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const bool ok = i0 + v < hi;
+      const uint32_t dg = kv[v] >> 20;
+      ca += ok && dg > d;
+      cc += ok && dg == d;
+    }
+    const int mine = ca | (cc << 16);
+    const int off = block_exclusive_scan<NT>(mine, sm.warp_tot);
+    int oa = baseA + (off & 0xffff), oc = baseC + (off >> 16);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int i = i0 + v;
+      if (i < hi) {
+        const uint32_t dg = kv[v] >> 20;
+        if (dg > d) la[oa++] = i;
+        else if (dg == d) lc[oc++] = make_uint2((uint32_t)i, kv[v]);
+      }
+    }
+    if (tid == NT - 1) sm.bcast[0] = off + mine;
+    __syncthreads();
+    const int tot = sm.bcast[0];
+    baseA += tot & 0xffff;
+    baseC += tot >> 16;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    meta[0] = baseA;
+    meta[1] = baseC;
+  }
+  cta_sync();
+  const int nS = kk - nA;
+  if (rank == 0) {
+    // append the other ranks' candidates after this CTA's own, in rank order
+    int off = baseC;
+    for (int r = 1; r < nrank; ++r) {
+      const int nr = remote(meta, r)[1];
+      const uint2* src = remote(lc, r);
+      for (int j = tid; j < nr; j += NT) lc[off + j] = src[j];
+      off += nr;
+    }
+    __syncthreads();
+    uint32_t prefix = d << 20, mask = 0xfff00000u;
+    auto ckey = [&](int j) { return lc[j].y; };
+    radix_pass<NT>(nC, ckey, 8, 12, prefix, mask, remaining, sm);
+    radix_pass<NT>(nC, ckey, 0, 8, prefix, mask, remaining, sm);
+    compact_selected<NT>(nC, ckey, prefix, remaining, [&](int j, int i) { lsel[j] = (int)lc[i].x; }, sm);
+  }
+  cta_sync();
+  int prefA = 0;
+  for (int r = 0; r < rank; ++r) prefA += remote(meta, r)[0];
+  const int* lsel0 = remote(lsel, 0);
+  for (int j = tid; j < baseA; j += NT) emit(prefA + j + count_below(lsel0, nS, la[j]), la[j]);
+  const int j0 = count_below(lsel0, nS, lo), j1 = count_below(lsel0, nS, hi);
+  for (int j = j0 + tid; j < j1; j += NT) {
+    const int i = lsel0[j];
+    emit(j + prefA + count_below(la, baseA, i), i);
+  }
+  cta_sync();  // rank 0's lists stay alive until every rank has read them
+  return true;
+}
+
 }  // namespace hs2
