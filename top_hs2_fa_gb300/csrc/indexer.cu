@@ -105,22 +105,45 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
+    // Lane 0 issues; in Reindex mode the warp's lanes 0-15 first resolve the tile's 16 pool
+    // blocks in parallel (pool entry, then block table: two dependent loads, not 32).
     if (lane == 0) {
       tc::prefetch_tmap(&tm_k);
       tc::mbar_arrive_expect_tx(&sm.qbar, kQBytes);
       tc::tma_load_2d(sm.q, &tm_q, 0, b * kIdxHeads, &sm.qbar);
       tc::tma_load_2d(sm.q + kQBytes / 2, &tm_q, 64, b * kIdxHeads, &sm.qbar);
-      int issued = 0;
-      for (int li = 0; li < ntl && !*(volatile int*)&sm.abort; ++li) {
-        const int st = li % kIdxStages;
-        if (!tc::mbar_wait(&sm.empty[st], ((li / kIdxStages) & 1) ^ 1)) {
+    }
+    int issued = 0;
+    for (int li = 0; li < ntl; ++li) {
+      if (__shfl_sync(0xffffffffu, *(volatile int*)&sm.abort, 0)) break;
+      const int st = li % kIdxStages;
+      const int tile = tile0 + li;
+      int row = -1;  // Reindex: the pool row of block tile * 16 + lane (lanes 0-15)
+      if (a.mode != 0 && lane < 16) {
+        const int e = tile * 16 + lane;
+        if (e < pc) {
+          const int bid = pool[e];
+          const int prev = e > 0 ? pool[e - 1] : -1;
+          const int p0 = bid * 8;
+          const bool bad_idx = bid < 0 || p0 >= t || (e > 0 && prev >= bid);
+          const int phys = bad_idx ? 0 : bt[p0 / kPage];
+          if (bad_idx) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+          else if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+          else row = phys * kPage + p0 % kPage;
+        }
+      }
+      bool ok = true;
+      if (lane == 0) ok = tc::mbar_wait(&sm.empty[st], ((li / kIdxStages) & 1) ^ 1);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) {
           flag_error(a.dev_err, HS2_DEV_TIMEOUT);
           atomicExch(&sm.abort, 1);
-          break;
         }
-        const int tile = tile0 + li;
-        uint8_t* dst = sm.k[st];
-        if (a.mode == 0) {
+        break;
+      }
+      uint8_t* dst = sm.k[st];
+      if (a.mode == 0) {
+        if (lane == 0) {
           int rows[2];
           uint32_t bytes = 0;
           for (int pg = 0; pg < 2; ++pg) {
@@ -136,31 +159,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           for (int pg = 0; pg < 2; ++pg)
             if (rows[pg] >= 0)
               for (int h = 0; h < 2; ++h) tc::tma_load_2d(dst + h * 16384 + pg * 8192, &tm_k, 64 * h, rows[pg], &sm.full[st]);
-        } else {
-          int rows[16];
-          uint32_t bytes = 0;
-          for (int j = 0; j < 16; ++j) {
-            const int e = tile * 16 + j;
-            rows[j] = -1;
-            if (e < pc) {
-              const int bid = pool[e];
-              const int p0 = bid * 8;
-              if (bid < 0 || p0 >= t || (e > 0 && pool[e - 1] >= bid)) {
-                flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
-              } else {
-                const int phys = bt[p0 / kPage];
-                if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
-                else { rows[j] = phys * kPage + p0 % kPage; bytes += 2 * 1024; }
-              }
-            }
-          }
-          tc::mbar_arrive_expect_tx(&sm.full[st], bytes);
-          for (int j = 0; j < 16; ++j)
-            if (rows[j] >= 0)
-              for (int h = 0; h < 2; ++h) tc::tma_load_2d(dst + h * 16384 + j * 1024, &tm_k, 64 * h, rows[j], &sm.full[st]);
         }
-        issued = li + 1;
+      } else {
+        const unsigned have = __ballot_sync(0xffffffffu, row >= 0);
+        if (lane == 0) tc::mbar_arrive_expect_tx(&sm.full[st], (uint32_t)__popc(have) * 2 * 1024);
+        __syncwarp();  // the expected bytes are armed before any copy can complete
+        if (row >= 0)
+          for (int h = 0; h < 2; ++h) tc::tma_load_2d(dst + h * 16384 + lane * 1024, &tm_k, 64 * h, row, &sm.full[st]);
       }
+      issued = li + 1;
+    }
+    if (lane == 0) {
       // leave no copy in flight: wait (bounded) for the last tiles issued to each stage
       for (int li = max(0, issued - kIdxStages); li < issued; ++li)
         (void)tc::mbar_wait(&sm.full[li % kIdxStages], (li / kIdxStages) & 1);
