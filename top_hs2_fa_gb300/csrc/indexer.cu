@@ -33,6 +33,7 @@ constexpr int kIdxThreads = 192;   // 6 warps: TMA, MMA, 4 x epilogue
 constexpr uint32_t kStageBytes = kIdxTile * kIdxDim * 2;       // 32 KB
 constexpr uint32_t kQBytes = kIdxHeads * kIdxDim * 2;          // 16 KB
 constexpr uint32_t kTmemCols = 128;                            // 2 accumulators x 64 columns
+constexpr int kIdxPoolBatch = 16;  // Reindex tiles whose pool rows the producer warp resolves at once
 
 struct IdxSmem {
   uint8_t q[kQBytes];                       // B operand, 2 K-blocks of [64 rows x 128 B]
@@ -40,6 +41,7 @@ struct IdxSmem {
   uint32_t hist[kRadixBins];
   uint32_t bhist[kRadixBins];
   uint64_t full[kIdxStages], empty[kIdxStages], qbar, accf[2], acce[2];
+  int prow[kIdxPoolBatch * 16];  // Reindex: pool rows of the next kIdxPoolBatch tiles
   uint32_t tmem_base;
   int abort;
 };
@@ -105,8 +107,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
-    // Lane 0 issues; in Reindex mode the warp's lanes 0-15 first resolve the tile's 16 pool
-    // blocks in parallel (pool entry, then block table: two dependent loads, not 32).
+    // Lane 0 issues; in Reindex mode the whole warp first resolves the pool blocks of the next
+    // kIdxPoolBatch tiles together (pool entries, then the block table: two dependent rounds
+    // of loads per batch) into shared memory.
     if (lane == 0) {
       tc::prefetch_tmap(&tm_k);
       tc::mbar_arrive_expect_tx(&sm.qbar, kQBytes);
@@ -118,20 +121,39 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       if (__shfl_sync(0xffffffffu, *(volatile int*)&sm.abort, 0)) break;
       const int st = li % kIdxStages;
       const int tile = tile0 + li;
-      int row = -1;  // Reindex: the pool row of block tile * 16 + lane (lanes 0-15)
-      if (a.mode != 0 && lane < 16) {
-        const int e = tile * 16 + lane;
-        if (e < pc) {
-          const int bid = pool[e];
-          const int prev = e > 0 ? pool[e - 1] : -1;
-          const int p0 = bid * 8;
-          const bool bad_idx = bid < 0 || p0 >= t || (e > 0 && prev >= bid);
-          const int phys = bad_idx ? 0 : bt[p0 / kPage];
-          if (bad_idx) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
-          else if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
-          else row = phys * kPage + p0 % kPage;
+      if (a.mode != 0 && li % kIdxPoolBatch == 0) {
+        // pool rows of tiles li .. li + kIdxPoolBatch - 1: every load of a round issued before
+        // any check (a flagged error is an atomic later loads cannot move across)
+        constexpr int PER = kIdxPoolBatch * 16 / 32;
+        int bid[PER], prev[PER], phys[PER];
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+          const int e = tile * 16 + lane + 32 * q;
+          bid[q] = e < pc ? pool[e] : -1;
+          prev[q] = (e < pc && e > 0) ? pool[e - 1] : -1;
         }
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+          const int e = tile * 16 + lane + 32 * q;
+          const bool bad = e < pc && (bid[q] < 0 || bid[q] * 8 >= t || (e > 0 && prev[q] >= bid[q]));
+          if (bad) bid[q] = -2;
+          phys[q] = (e < pc && !bad) ? bt[bid[q] * 8 / kPage] : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+          const int e = tile * 16 + lane + 32 * q;
+          int r = -1;
+          if (e < pc) {
+            if (bid[q] == -2) flag_error(a.dev_err, HS2_DEV_BAD_INDEX);
+            else if (phys[q] < 0 || phys[q] >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+            else r = phys[q] * kPage + (bid[q] * 8) % kPage;
+          }
+          sm.prow[lane + 32 * q] = r;
+        }
+        __syncwarp();
       }
+      // Reindex: the pool row of block tile * 16 + lane (lanes 0-15)
+      const int row = (a.mode != 0 && lane < 16) ? sm.prow[(li % kIdxPoolBatch) * 16 + lane] : -1;
       bool ok = true;
       if (lane == 0) ok = tc::mbar_wait(&sm.empty[st], ((li / kIdxStages) & 1) ^ 1);
       if (!__shfl_sync(0xffffffffu, ok, 0)) {
