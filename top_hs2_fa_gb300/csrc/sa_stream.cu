@@ -467,8 +467,10 @@ static bool stream_plan_t(int G, int w, int k, int Bq, int Hkv, SaStreamArgs* sp
   const long long resident = 4LL * sms * per_sm;  // every warp of the grid resident at once
   long long nw = std::min(resident, total);
   long long per = total / nw;  // >= 1; ranges hold per or per + 1 steps
-  // at most 32 warps share a unit (the merge holds one partial per lane)
-  const long long per_min = (ms + 30) / 31;
+  // at most 32 warps share a unit (the merge holds one partial per lane), and at least 4
+  // steps per warp: on small problems (few units) a unit split over many short warps ends
+  // in a long merge of many partials, which is the critical path
+  const long long per_min = std::max<long long>((ms + 30) / 31, std::min<long long>(4, ms));
   if (per < per_min) {
     per = per_min;
     nw = std::max(1LL, total / per);
