@@ -5,18 +5,21 @@
 // the FA builds the cache and attends over all positions). Row i sees keys [0, i].
 //
 // One CTA per (128-row query tile, query head); heaviest tiles are scheduled first.
-//   warps 0, 6  TMA producers: Q tile once (3-D map over [n][Hq][d]); K tiles (warp 0) and
-//               V tiles (warp 6) of 128 keys (two 64-row pages each, through the block
+//   warps 0, 10 TMA producers: Q tile once (3-D map over [n][Hq][d]); K tiles (warp 0) and
+//               V tiles (warp 10) of 128 keys (two 64-row pages each, through the block
 //               table) into 2-slot rings, 128-byte swizzle; a K slot frees when its QK is
 //               done, a V slot when its PV is done.
 //   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers (M=128, N=128,
 //               K=128), then O += P_j V_j (A = P from shared memory, B = V MN-major);
 //               S_{j+1} is issued before waiting for P_j so the tensor core stays busy.
-//   warps 2-5   softmax, one query row per thread: row max, exp2 (base-2 logits), P in
+//   warps 2-9   softmax, two threads per query row (warps w and w+4 share a TMEM lane
+//               quadrant, each takes 64 of the tile's 128 columns; the halves swap their
+//               row maxima through shared memory): row max, exp2 (base-2 logits), P in
 //               bf16 to one of two shared-memory buffers (the normaliser sums the same
 //               rounded values), and a lazy O rescale: the reference max only moves when
 //               the row max grows by more than 2^8, which keeps every weight below 256 and
 //               needs no approximation; only a rescale waits for the previous PV.
+//   warp 10     TMA producer of the V tiles.
 // TMEM: S0 columns [0,128), S1 [128,256), O [256,384). Every mbarrier wait is bounded.
 #include <cuda.h>
 
@@ -29,7 +32,8 @@ namespace hs2 {
 namespace {
 
 constexpr int kPT = 128;           // query rows per tile = keys per KV tile
-constexpr int kPThreads = 224;     // TMA warps (K; Q and V), MMA warp, 4 softmax warps
+constexpr int kPThreads = 352;     // TMA warps (Q and K; V), MMA warp, 8 softmax warps
+constexpr int kVWarp = 10;         // the V producer
 constexpr uint32_t kTileBytes = kPT * 128 * 2;  // 32 KB: 128 rows x 128 bf16
 constexpr uint32_t kTmemColsPf = 512;
 constexpr float kRescaleLog2 = 8.f;
@@ -39,7 +43,10 @@ struct PfSmem {
   uint8_t k[2][kTileBytes];   // B of S: same layout, rows = keys
   uint8_t v[2][kTileBytes];   // B of PV (MN-major): d-halves x [128 keys x 128 B]
   uint8_t p[2][kTileBytes];   // A of PV, double-buffered: K-blocks (keys 0-63, 64-127) x [128 rows x 128 B]
+  float xch[2][kPT];           // [half] a tile's row maxima of the two column halves (then
+                               // the row normaliser's halves, at the end)
   uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2];
+  uint64_t x_full[4], x_empty[4];  // per lane quadrant: both halves wrote / read xch
   uint32_t tmem_base;
   int abort;
 };
@@ -77,9 +84,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tc::mbar_init(&sm.v_full[s], 1);
       tc::mbar_init(&sm.v_empty[s], 1);  // PV of the slot's tile done
       tc::mbar_init(&sm.s_full[s], 1);
-      tc::mbar_init(&sm.s_empty[s], 128);
-      tc::mbar_init(&sm.p_full[s], 128);
+      tc::mbar_init(&sm.s_empty[s], 256);
+      tc::mbar_init(&sm.p_full[s], 256);
       tc::mbar_init(&sm.p_empty[s], 1);  // PV of the buffer's tile done (and every MMA before it)
+    }
+    for (int q = 0; q < 4; ++q) {
+      tc::mbar_init(&sm.x_full[q], 64);
+      tc::mbar_init(&sm.x_empty[q], 64);
     }
     sm.abort = 0;
     tc::fence_mbar_init();
@@ -91,7 +102,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   const uint32_t tS = tmem, tO = tmem + 256;
 
-  if (warp == 0 || warp == 6) {
+  if (warp == 0 || warp == kVWarp) {
     // ------------------------------------------------------------------ TMA producers
     // warp 0: Q once, then K tiles; warp 6: V tiles. K slots free up when a tile's QK is
     // done and V slots when its PV is done, so the K loads run ahead of the V loads.
@@ -183,27 +194,37 @@ __global__ void __launch_bounds__(kPThreads, 1)
   } else {
     // ------------------------------------------------------------------ softmax warps
     const int qd = warp & 3;
+    const int half = (warp - 2) >> 2;  // columns [64 half, 64 half + 64) of every tile
     const int r = qd * 32 + lane;
     const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     float m_used = -INFINITY, l = 0.f;
+    // hand a value to the other half of the row through xch (round x: bounded mbarrier
+    // waits, so a half that stopped cannot leave the other waiting for ever)
+    auto swap = [&](float v, int x, float& other) -> bool {
+      if (x > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(&sm.x_empty[qd], (x - 1) & 1))) return false;
+      sm.xch[half][r] = v;
+      tc::mbar_arrive(&sm.x_full[qd]);
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.x_full[qd], x & 1))) return false;
+      other = sm.xch[half ^ 1][r];
+      tc::mbar_arrive(&sm.x_empty[qd]);
+      return true;
+    };
     bool ok = true;
     for (int j = 0; j < J; ++j) {
       const int sb = j & 1;
       // votes keep the warp converged for the warp-collective TMEM accesses
       if (!__all_sync(0xffffffffu, !aborted(sm) && tc::mbar_wait(&sm.s_full[sb], (j >> 1) & 1))) { ok = false; break; }
       tc::tc_fence_after();
-      float x[4][32];
+      float x[2][32];
       {
-        uint32_t raw[4][32];
+        uint32_t raw[2][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tc::tmem_ld32_async(tS + lane_off + sb * 128 + c * 32, raw[c]);
-        tc::tmem_wait_ld(raw[3]);
+        for (int c = 0; c < 2; ++c) tc::tmem_ld32_async(tS + lane_off + sb * 128 + half * 64 + c * 32, raw[c]);
+        tc::tmem_wait_ld(raw[1]);
         tc::tmem_regs_ready(raw[0]);
-        tc::tmem_regs_ready(raw[1]);
-        tc::tmem_regs_ready(raw[2]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[c][e] = __uint_as_float(raw[c][e]);
       }
@@ -212,18 +233,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // raw logits: only the diagonal tile crosses the causal boundary; the scale (> 0) is
       // applied to the max and folded into the exponent's FMA below
       if (j == J - 1) {
-        const int kbase = j * kPT;
+        const int kbase = j * kPT + half * 64;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (kbase + c * 32 + e > i) x[c][e] = -INFINITY;
       }
       float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int e = 0; e < 32; ++e) mt = fmaxf(mt, x[c][e]);
+      // the row max over both halves
+      float mo;
+      if (!swap(mt, j, mo)) {
+        ok = false;
+        break;
+      }
+      mt = fmaxf(mt, mo);
       const float m_new = fmaxf(m_used, mt * a.scale_log2);
       const bool need = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new > -INFINITY);
       const float alpha = (need && m_used > -INFINITY) ? tc::ex2(m_used - m_new) : 1.f;
@@ -242,12 +270,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
           tc::tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             float ov[32];
-            tc::tmem_ld32(tO + lane_off + c * 32, ov);
+            tc::tmem_ld32(tO + lane_off + half * 64 + c * 32, ov);
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-            tc::tmem_st32(tO + lane_off + c * 32, ov);
+            tc::tmem_st32(tO + lane_off + half * 64 + c * 32, ov);
           }
         }
         l *= alpha;
@@ -259,12 +287,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const float neg_m = -m_used;
       constexpr uint32_t kOnes = 0x3F803F80u;  // bf16 1.0, 1.0
 #pragma unroll
-      for (int cc = 0; cc < 16; ++cc) {
+      for (int c8 = 0; c8 < 8; ++c8) {  // this half's 8-column chunks cc = 8 half + c8
+        const int cc = 8 * half + c8;
         uint32_t w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float p0 = tc::ex2(fmaf(x[cc >> 2][(cc & 3) * 8 + 2 * u], a.scale_log2, neg_m));
-          const float p1 = tc::ex2(fmaf(x[cc >> 2][(cc & 3) * 8 + 2 * u + 1], a.scale_log2, neg_m));
+          const float p0 = tc::ex2(fmaf(x[c8 >> 2][(c8 & 3) * 8 + 2 * u], a.scale_log2, neg_m));
+          const float p1 = tc::ex2(fmaf(x[c8 >> 2][(c8 & 3) * 8 + 2 * u + 1], a.scale_log2, neg_m));
           w[u] = pack_bf16(p0, p1);
           l = fmab_ll(w[u], kOnes, l);
           l = fmab_hl(w[u], kOnes, l);
@@ -274,14 +303,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tc::fence_async_smem();
       tc::mbar_arrive(&sm.p_full[j & 1]);
     }
+    // the two halves' normalisers (they share m_used)
+    float lo_ = 0.f;
+    if (ok && !swap(l, J, lo_)) ok = false;
+    l += lo_;
     if (__all_sync(0xffffffffu, ok && !aborted(sm) && tc::mbar_wait(&sm.p_empty[(J - 1) & 1], ((J - 1) >> 1) & 1))) {
       tc::tc_fence_after();
       const float linv = l > 0.f ? 1.f / l : 0.f;
-      float* orow = a.o + ((size_t)i * a.Hq + h) * 128;
+      float* orow = a.o + ((size_t)i * a.Hq + h) * 128 + half * 64;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float ov[32];
-        tc::tmem_ld32(tO + lane_off + c * 32, ov);
+        tc::tmem_ld32(tO + lane_off + half * 64 + c * 32, ov);
         if (i < a.n) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
@@ -289,7 +322,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 make_float4(ov[e] * linv, ov[e + 1] * linv, ov[e + 2] * linv, ov[e + 3] * linv);
         }
       }
-      if (i < a.n) {
+      if (i < a.n && half == 0) {
         a.lse2[(size_t)i * a.Hq + h] = m_used + log2f(l);
         if (a.lse) a.lse[(size_t)i * a.Hq + h] = (m_used + log2f(l)) / kLog2e;
       }
