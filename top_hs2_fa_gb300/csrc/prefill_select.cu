@@ -17,11 +17,12 @@
 //            past capacity it keeps only the largest dropped key.
 //   Warp 0 streams K tiles and, per head, the head's Q tile (TMA); warp 1 issues
 //   S_h = Q_h K^T (M=128 rows, N=128 keys, K=128) into double-buffered TMEM.
-// prefill_topk_kernel — per (row, KV head): exact top-k over the row's candidates (radix
-//   select, ties to the lower position, ascending output). The candidates are a superset of
-//   the answer when (a) at least k of them are >= tau and (b) no dropped key exceeds the k-th
-//   largest kept key (dropped positions come after every kept one, so equal keys lose);
-//   otherwise the row is flagged (HS2_DEV_SELECT) and written as count -1.
+// prefill_topk_warp_kernel — one warp per (row, KV head): exact top-k over the row's
+//   candidates (radix select with warp-level ballots and shuffles, ties to the lower
+//   position, ascending output). The candidates are a superset of the answer when (a) at
+//   least k of them are >= tau and (b) no dropped key exceeds the k-th largest kept key
+//   (dropped positions come after every kept one, so equal keys lose); otherwise the row is
+//   flagged (HS2_DEV_SELECT) and written as count -1.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -327,16 +328,22 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (warp == 1) tc::tmem_dealloc(sm.tmem_base, 256);
 }
 
-// One CTA per (row, KV head) of the chunk; each thread keeps a contiguous run of the row's
-// candidate keys in registers, so the three radix passes and the ordered compaction read
-// global memory once.
-constexpr int kTopkThreads = 256;
-constexpr int kTopkSeg = 16;  // candidates per thread (cap <= 4096)
+// prefill_topk_warp_kernel — one warp per (row, KV head), warp-level primitives only (no CTA
+// barrier): the exact top-k of the row's candidates (radix select, ties to the lower position,
+// ascending output). The candidates are a superset of the answer when (a) at least k of
+// them are >= tau and (b) no dropped key exceeds the k-th largest kept key (dropped positions
+// come after every kept one, so equal keys lose); otherwise the row is flagged
+// (HS2_DEV_SELECT) and written as count -1. Four radix passes of 8 bits, each a histogram of the
+// candidates still matching the chosen prefix in the warp's own 256 shared-memory bins
+// (read from L2 on every pass), the digit holding the kk-th key found from the top bin
+// down with a warp scan; then the candidates in index order (= ascending position) are
+// compacted with ballots: every key above T and the first take_eq keys equal to T.
+constexpr int kTopkWarps = 8;
 
-__global__ void __launch_bounds__(kTopkThreads) prefill_topk_kernel(const PsArgs a) {
-  constexpr int NT = kTopkThreads;
-  const int tid = threadIdx.x;
-  const int rs = blockIdx.x;  // (i - row0) * Hkv + g
+__global__ void __launch_bounds__(kTopkWarps * 32) prefill_topk_warp_kernel(const PsArgs a) {
+  __shared__ uint32_t hist[kTopkWarps][256];
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const int rs = blockIdx.x * kTopkWarps + wl;  // (i - row0) * Hkv + g
   const int i = a.row0 + rs / a.Hkv;
   if (i >= a.row1) return;
   const int nF = max(0, i + 1 - a.w);
@@ -344,75 +351,92 @@ __global__ void __launch_bounds__(kTopkThreads) prefill_topk_kernel(const PsArgs
   int32_t* out = a.idx + ((size_t)i * a.Hkv + rs % a.Hkv) * a.k;
   int32_t* cnt_out = a.cnt + (size_t)i * a.Hkv + rs % a.Hkv;
   if (kk == nF) {  // trivial rows: all of F
-    if (tid == 0) *cnt_out = kk;
-    for (int j = tid; j < a.k; j += NT) out[j] = j < kk ? j : -1;
+    if (lane == 0) *cnt_out = kk;
+    for (int j = lane; j < a.k; j += 32) out[j] = j < kk ? j : -1;
     return;
   }
   const int c = min(a.cand_cnt[rs], a.cap);
   const uint32_t* keys = a.cand_key + (size_t)rs * a.cap;
   const int32_t* pos = a.cand_pos + (size_t)rs * a.cap;
-  __shared__ TopkSmem<NT> sm;
+  uint32_t* h = hist[wl];
   bool fail = c < kk;
-  uint32_t T = 0;
-  int take_eq = 0;
-  const int seg = (c + NT - 1) / NT;
-  const int lo = min(c, tid * seg), hi = min(c, lo + seg);
-  uint32_t kr[kTopkSeg];
-#pragma unroll
-  for (int e = 0; e < kTopkSeg; ++e) kr[e] = (lo + e < hi) ? __ldcg(keys + lo + e) : 0u;
+  uint32_t prefix = 0, mask = 0;
+  int remaining = kk;
   if (!fail) {
-    uint32_t prefix = 0, mask = 0;
-    int remaining = kk;
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-      const int sh = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
-      const int nb = pass == 2 ? 256 : 4096;
-      for (int b = tid; b < nb; b += NT) sm.hist[b] = 0;
-      __syncthreads();
+    for (int sh = 24; sh >= 0; sh -= 8) {
 #pragma unroll
-      for (int e = 0; e < kTopkSeg; ++e) {
-        const bool part = lo + e < hi && (kr[e] & mask) == prefix;
-        hist_add_warp(sm.hist, part, (kr[e] >> sh) & (uint32_t)(nb - 1));
+      for (int b = 0; b < 8; ++b) h[lane * 8 + b] = 0;
+      __syncwarp();
+      for (int j = lane; j < c; j += 32) {
+        const uint32_t key = __ldcg(keys + j);
+        if ((key & mask) == prefix) atomicAdd(&h[(key >> sh) & 255u], 1u);
       }
-      __syncthreads();
-      const uint32_t dig = find_digit<NT>(sm.hist, nb, remaining, sm);
-      prefix |= dig << sh;
-      mask |= (uint32_t)(nb - 1) << sh;
+      __syncwarp();
+      // lane L holds bins 255 - 8L .. 248 - 8L (descending); cumulative counts from the top
+      uint32_t cnt8[8], own = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        cnt8[b] = h[255 - 8 * lane - b];
+        own += cnt8[b];
+      }
+      uint32_t incl = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const uint32_t excl = incl - own;
+      // the lane whose bins reach `remaining`: the first with incl >= remaining
+      const unsigned hit = __ballot_sync(0xffffffffu, incl >= (uint32_t)remaining);
+      const int src = __ffs(hit) - 1;  // exists: the total is >= remaining (c >= kk)
+      int digit = 0, above = 0;
+      if (lane == src) {
+        uint32_t cum = excl;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (cum + cnt8[b] >= (uint32_t)remaining) {
+            digit = 255 - 8 * lane - b;
+            above = (int)cum;
+            break;
+          }
+          cum += cnt8[b];
+        }
+      }
+      digit = __shfl_sync(0xffffffffu, digit, src);
+      above = __shfl_sync(0xffffffffu, above, src);
+      remaining -= above;
+      prefix |= (uint32_t)digit << sh;
+      mask |= 255u << sh;
+      __syncwarp();  // the bins are cleared again by the next pass
     }
-    T = prefix;  // the kk-th largest kept key
-    take_eq = remaining;
     // a larger dropped key would belong in the answer (equal ones come later and lose)
-    fail = a.cand_drop[rs] > T;
+    fail = a.cand_drop[rs] > prefix;
   }
   if (fail) {
-    if (tid == 0) {
+    if (lane == 0) {
       *cnt_out = -1;
       flag_error(a.dev_err, HS2_DEV_SELECT);
     }
-    for (int j = tid; j < a.k; j += NT) out[j] = -1;
+    for (int j = lane; j < a.k; j += 32) out[j] = -1;
     return;
   }
-  int n_eq = 0, n_gt = 0;
-#pragma unroll
-  for (int e = 0; e < kTopkSeg; ++e)
-    if (lo + e < hi) {
-      n_eq += kr[e] == T;
-      n_gt += kr[e] > T;
-    }
-  const int eq_before = block_exclusive_scan<NT>(n_eq, sm.warp_tot);
-  const int eq_take = max(0, min(n_eq, take_eq - eq_before));
-  int p = block_exclusive_scan<NT>(n_gt + eq_take, sm.warp_tot);
-  int eq_seen = eq_before;
-#pragma unroll
-  for (int e = 0; e < kTopkSeg; ++e) {
-    if (lo + e < hi) {
-      bool sel = kr[e] > T;
-      if (kr[e] == T) sel = eq_seen++ < take_eq;
-      if (sel) out[p++] = __ldcg(pos + lo + e);
-    }
+  const uint32_t T = prefix;  // the kk-th largest key; take the first `remaining` equal to it
+  const unsigned lt = (1u << lane) - 1u;
+  int o = 0, eq_seen = 0;
+  for (int base = 0; base < c; base += 32) {
+    const int j = base + lane;
+    const uint32_t key = j < c ? __ldcg(keys + j) : 0u;
+    const bool eq = j < c && key == T;
+    const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+    const bool sel = j < c && (key > T || (eq && eq_seen + __popc(eqm & lt) < remaining));
+    const unsigned selm = __ballot_sync(0xffffffffu, sel);
+    if (sel) out[o + __popc(selm & lt)] = __ldcg(pos + j);
+    o += __popc(selm);
+    eq_seen += __popc(eqm);
   }
-  if (tid == 0) *cnt_out = kk;
-  for (int j = kk + tid; j < a.k; j += NT) out[j] = -1;
+  if (lane == 0) *cnt_out = kk;
+  for (int j = kk + lane; j < a.k; j += 32) out[j] = -1;
 }
 
 size_t prefill_scan_smem() { return sizeof(PsSmem) + 1024; }
@@ -426,8 +450,8 @@ cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, 
   prefill_scan_kernel<<<dim3(tiles, a.Hkv), kSThreads, sm, s>>>(tq, tk, tks, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (a.cap > kTopkThreads * kTopkSeg) return cudaErrorInvalidValue;
-  prefill_topk_kernel<<<(a.row1 - a.row0) * a.Hkv, kTopkThreads, 0, s>>>(a);
+  const int rows = (a.row1 - a.row0) * a.Hkv;
+  prefill_topk_warp_kernel<<<(rows + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 
