@@ -328,16 +328,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (warp == 1) tc::tmem_dealloc(sm.tmem_base, 256);
 }
 
-// prefill_topk_warp_kernel — one warp per (row, KV head), warp-level primitives only (no CTA
-// barrier): the exact top-k of the row's candidates (radix select, ties to the lower position,
-// ascending output). The candidates are a superset of the answer when (a) at least k of
-// them are >= tau and (b) no dropped key exceeds the k-th largest kept key (dropped positions
-// come after every kept one, so equal keys lose); otherwise the row is flagged
-// (HS2_DEV_SELECT) and written as count -1. Four radix passes of 8 bits, each a histogram of the
-// candidates still matching the chosen prefix in the warp's own 256 shared-memory bins
-// (read from L2 on every pass), the digit holding the kk-th key found from the top bin
-// down with a warp scan; then the candidates in index order (= ascending position) are
-// compacted with ballots: every key above T and the first take_eq keys equal to T.
+// prefill_topk_warp_kernel (see the top of the file): no CTA barrier anywhere. Four radix
+// passes of 8 bits, each a histogram of the candidates still matching the chosen prefix in
+// the warp's own 256 shared-memory bins (keys read from L2 on every pass), the digit holding
+// the kk-th key found from the top bin down with a warp scan; then the candidates in index
+// order (= ascending position) are compacted with ballots: every key above T and the first
+// take_eq keys equal to T.
 constexpr int kTopkWarps = 8;
 
 __global__ void __launch_bounds__(kTopkWarps * 32) prefill_topk_warp_kernel(const PsArgs a) {
