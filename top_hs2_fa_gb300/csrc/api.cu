@@ -101,7 +101,7 @@ FaPlan fa_plan(int Bq, int Hq, const hs2_kv* kv, int max_t) {
 }
 
 struct SaPlan {
-  bool stream;  // bf16 decode: persistent warp stream
+  bool stream;  // decode (bf16, FP8, FP4): persistent warp stream
   int nsplit;   // CUDA-core path: chunks of 128 entries of W ∪ S
   hs2::SaStreamArgs sp;
   int grid;
@@ -601,7 +601,7 @@ hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, 
   }
   a.dev_err = dev_err;
   if (p.stream) {
-    // bf16 decode: one persistent warp stream over all (query, KV head) pairs' entries
+    // decode (bf16, FP8, FP4): one persistent warp stream over all (query, KV head) pairs' entries
     a.arrive = (int32_t*)(ws + p.off_arrive);
     cudaError_t e = cudaMemsetAsync(a.arrive, 0, (size_t)B_or_n * kv->Hkv * p.sp.hg * sizeof(int32_t), s);
     if (e != cudaSuccess) return cuda_fail(e);
