@@ -6,17 +6,20 @@
 // kernel). The n x n score matrix is never stored: scores are produced tile by tile from
 // a tcgen05 recomputation of Q K^T and consumed on the fly.
 //
-// prefill_scan_kernel — one CTA per (128-row tile, KV head), one row per scoring thread:
+// prefill_scan_kernel — one CTA per (128-row tile, KV head), two scoring threads per row:
 //   sweep 0 (sampled): every 4th key position only, 128 of them per tile (512 positions;
 //            a strided tensor map loads just those K rows); each thread bins the sampled
-//            scores of its row into a 256-bin log histogram (1/8 octave per bin) held in
-//            shared memory, then picks a threshold tau whose estimated count of keys at or
-//            above it is twice the budget;
-//   sweep 1 (exact): every key tile; each thread appends (key, position) of the scores >= tau
-//            of its row, in ascending position, into its row's candidate buffer (capacity C);
+//            scores of its half of the row's columns into a 256-bin log histogram (1/8
+//            octave per bin) held in shared memory, then the row's first thread picks from
+//            the two histograms a threshold tau whose estimated count of keys at or above it
+//            is twice the budget;
+//   sweep 1 (exact): every key tile; the scoring threads stage the tile's 128 x 128 scores in
+//            shared memory, then each scoring warp takes 16 rows and appends (key, position)
+//            of the scores >= tau of a row, in ascending position, into the row's candidate
+//            buffer (capacity C) with ballot compaction, so each store is a contiguous run;
 //            past capacity it keeps only the largest dropped key.
 //   Warp 0 streams K tiles and, per head, the head's Q tile (TMA); warp 1 issues
-//   S_h = Q_h K^T (M=128 rows, N=128 keys, K=128) into double-buffered TMEM.
+//   S_h = Q_h K^T (M=128 rows, N=128 keys, K=128) into four TMEM buffers.
 // prefill_topk_warp_kernel — one warp per (row, KV head): exact top-k over the row's
 //   candidates (radix select with warp-level ballots and shuffles, ties to the lower
 //   position, ascending output). The candidates are a superset of the answer when (a) at
@@ -46,18 +49,28 @@ constexpr int kSampSpan = kST * kSampleStride;                // positions cover
 constexpr int kSampPages = kSampSpan / kPage;                 // pages of a sampled key tile (8)
 constexpr uint32_t kSampBoxBytes = kPsSampleRowsPerPage * 128;  // one 64-column half of a page's sampled rows
 
-constexpr int kQStages = 2;
+constexpr int kCompRows = 8;  // rows compacted together by a scoring warp (of its 16)
+constexpr int kQStages = 3;  // Q tiles in flight: a head's load overlaps the two MMAs before it
 
 struct PsSmem {
   uint8_t q[kQStages][kSTile];     // A of S (query rows x d), one head per stage
   uint8_t k[2][kSTile];            // B of S (keys x d)
-  uint8_t hist[kBins][kST];        // per-row sample histograms ([bin][row]), saturating counts
-  float xch[64][kST];              // columns 64-127 of a key tile's scores, handed to the row owner
-  float lse2[32][kST];             // the rows' base-2 lse of each query head of the KV head (G <= 32)
-  uint64_t q_full[kQStages], q_empty[kQStages], k_full[2], k_empty[2], s_full[2], s_empty[2], x_full, x_empty;
+  union {
+    struct {
+      uint8_t hist[2][kBins][kST];  // per-row sample histograms ([half][bin][row]), saturating counts,
+    } samp;                         // one per column half of the sampled tiles
+    float tile[kST * kST];         // exact sweep: the key tile's scores, row-major, swizzled (tile_at)
+  };
+  uint32_t tau[kST];               // each row's threshold, set at the end of the sampled sweep
+  uint64_t q_full[kQStages], q_empty[kQStages], k_full[2], k_empty[2], s_full[4], s_empty[4], h_done;
+  uint64_t t_full, t_free;         // exact sweep: tile written by all scoring threads / tile consumed
   uint32_t tmem_base;
   int abort;
 };
+
+// element (row r, column c) of the staged score tile; the XOR keeps both the row owners'
+// 16-byte column writes and the row-wise 32-lane reads free of bank conflicts
+HS2_DEVI int tile_at(int r, int c) { return r * kST + (c ^ ((r & 7) << 2)); }
 
 HS2_DEVI bool aborted(PsSmem& sm) { return *(volatile int*)&sm.abort != 0; }
 HS2_DEVI void set_abort(PsSmem& sm, int32_t* dev_err) {
@@ -94,19 +107,22 @@ __global__ void __launch_bounds__(kSThreads, 1)
       tc::mbar_init(&sm.q_full[s], 1);
       tc::mbar_init(&sm.q_empty[s], 1);
     }
+    for (int s = 0; s < 4; ++s) {
+      tc::mbar_init(&sm.s_full[s], 1);
+      tc::mbar_init(&sm.s_empty[s], 8);
+    }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&sm.k_full[s], 1);
       tc::mbar_init(&sm.k_empty[s], 1);
-      tc::mbar_init(&sm.s_full[s], 1);
-      tc::mbar_init(&sm.s_empty[s], 256);
     }
-    tc::mbar_init(&sm.x_full, 128);
-    tc::mbar_init(&sm.x_empty, 128);
+    tc::mbar_init(&sm.h_done, 128);
+    tc::mbar_init(&sm.t_full, 256);
+    tc::mbar_init(&sm.t_free, 256);
     sm.abort = 0;
     tc::fence_mbar_init();
   }
-  for (int e = threadIdx.x; e < kBins * kST / 4; e += kSThreads) reinterpret_cast<uint32_t*>(sm.hist)[e] = 0;
-  if (warp == 1) tc::tmem_alloc(&sm.tmem_base, 256);
+  for (int e = threadIdx.x; e < 2 * kBins * kST / 4; e += kSThreads) reinterpret_cast<uint32_t*>(sm.samp.hist)[e] = 0;
+  if (warp == 1) tc::tmem_alloc(&sm.tmem_base, 512);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -185,8 +201,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (!tc::mbar_wait(&sm.k_full[ks], (kt >> 1) & 1)) { ok = false; break; }
         const uint32_t kb = tc::smem_u32(sm.k[ks]);
         for (int hl = 0; hl < G; ++hl) {
-          const int it = kt * G + hl, qs = it % kQStages, sb = it & 1;
-          if (!tc::mbar_wait(&sm.q_full[qs], (it / kQStages) & 1) || !tc::mbar_wait(&sm.s_empty[sb], ((it >> 1) & 1) ^ 1)) {
+          const int it = kt * G + hl, qs = it % kQStages, sb = it & 3;
+          if (!tc::mbar_wait(&sm.q_full[qs], (it / kQStages) & 1) || !tc::mbar_wait(&sm.s_empty[sb], ((it >> 2) & 1) ^ 1)) {
             ok = false;
             break;
           }
@@ -204,12 +220,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (ok) tc::mma_commit(&sm.k_empty[ks]);
       }
       if (!ok) set_abort(sm, a.dev_err);
-      if (last >= 0) (void)tc::mbar_wait(&sm.s_full[last & 1], (last >> 1) & 1);
+      if (last >= 0) (void)tc::mbar_wait(&sm.s_full[last & 3], (last >> 2) & 1);
     }
   } else {
     // ---------------------------------------------------------------- scoring warps
     // warps 2-5 own rows and columns 0-63 of every S tile; warps 6-9 take columns 64-127
-    // of the same rows and hand their partial scores over through shared memory.
+    // of the same rows. In the sampled sweep each half bins its columns into its own
+    // histograms and the row owner (first half) sets the threshold from both; in the exact
+    // sweep all eight warps stage the tile's scores, then each compacts 16 rows.
     const int half = (warp - 2) >> 2;
     const int qd = warp & 3;
     const int r = qd * 32 + lane;
@@ -218,18 +236,19 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int nF = row_ok ? max(0, i + 1 - a.w) : 0;
     const bool ranked = nF > a.k;  // rows whose far range fits the budget need no candidates
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    // the row's lse of each head: G floats, read through L1 one head ahead of their use
     const float* lse2_row = a.lse2 + (size_t)(row_ok ? i : a.row0) * a.Hq + g * G;
-    // the row's lse of every head, once: the per-tile head loop reads them from shared memory
-    // (each scoring thread of the pair holding row r writes half of them)
-    for (int hl = half; hl < G; hl += 2) sm.lse2[hl][r] = __ldg(lse2_row + hl);
-    named_bar_sync(1, 256);
-    const size_t slot = ((size_t)(i - a.row0) * a.Hkv + g) * a.cap;
-    uint32_t* bkey = a.cand_key + slot;
-    int32_t* bpos = a.cand_pos + slot;
-    uint32_t tau = 0xffffffffu;
-    int n_samp = 0;  // far positions of this row seen by the sampled sweep
-    int cnt = 0;
-    uint32_t dropped = 0;
+    // rows this warp compacts in the exact sweep: lane l < 16 keeps the state of row 16 sw + l
+    const int sw = warp - 2;
+    const int cr = sw * 16 + (lane & 15);
+    const int ci = i0 + cr;
+    const bool c_ok = lane < 16 && ci < a.row1;
+    const int c_nF = c_ok ? max(0, ci + 1 - a.w) : 0;
+    const bool c_ranked = c_nF > a.k;
+    uint32_t c_tau = 0xffffffffu;  // read from shared memory once the sampled sweep is over
+    int c_cnt = 0;
+    uint32_t c_drop = 0;
+    uint32_t tau = 0xffffffffu;  // the owner's threshold, from its row's sample histogram
     bool ok = true;
     for (int kt = 0; kt < NKT && ok; ++kt) {
       const bool sample = kt < J0;
@@ -237,13 +256,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
       float sc[64];
 #pragma unroll
       for (int e = 0; e < 64; ++e) sc[e] = 0.f;
+      float l2_next = __ldg(lse2_row);
       for (int hl = 0; hl < G; ++hl) {
-        const int it = kt * G + hl, sb = it & 1;
+        const float l2 = l2_next;
+        if (hl + 1 < G) l2_next = __ldg(lse2_row + hl + 1);
+        const int it = kt * G + hl, sb = it & 3;
         // votes keep the warp converged for the warp-collective TMEM loads
-        if (!__all_sync(0xffffffffu, !aborted(sm) && tc::mbar_wait(&sm.s_full[sb], (it >> 1) & 1))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, !aborted(sm) && tc::mbar_wait(&sm.s_full[sb], (it >> 2) & 1))) { ok = false; break; }
         __syncwarp();
         tc::tc_fence_after();
-        const float l2 = sm.lse2[hl][r];
         uint32_t raw[2][32];
         const uint32_t ta = tS + lane_off + sb * 128 + half * 64;
         tc::tmem_ld32_async(ta, raw[0]);
@@ -251,81 +272,123 @@ __global__ void __launch_bounds__(kSThreads, 1)
         tc::tmem_wait_ld(raw[1]);
         tc::tmem_regs_ready(raw[0]);
         tc::tc_fence_before();
-        tc::mbar_arrive(&sm.s_empty[sb]);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm.s_empty[sb]);
 #pragma unroll
         for (int e = 0; e < 64; ++e) sc[e] += tc::ex2(fmaf(__uint_as_float(raw[e >> 5][e & 31]), a.scale_log2, -l2));
       }
       if (!ok) break;
-      if (half == 1) {
-        // hand columns 64-127 to the row owner
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.x_empty, (kt & 1) ^ 1))) { ok = false; break; }
+      if (sample) {
+        if (ranked) {
+          // column half * 64 + e of a sampled tile is position j * kSampSpan + kSampleStride * (half * 64 + e);
+          // each half bins its own columns
 #pragma unroll
-        for (int e = 0; e < 64; ++e) sm.xch[e][r] = sc[e];
-        tc::mbar_arrive(&sm.x_full);
-        continue;
-      }
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.x_full, kt & 1))) { ok = false; break; }
-      float sc2[64];
-#pragma unroll
-      for (int e = 0; e < 64; ++e) sc2[e] = sm.xch[e][r];
-      tc::mbar_arrive(&sm.x_empty);
-      const int s0 = j * kST;
-      if (!ranked) {
-        // rows whose far range fits the budget keep no candidates
-      } else if (sample) {
-        // column e of a sampled tile is position j * kSampSpan + kSampleStride * e
-#pragma unroll
-        for (int e = 0; e < 128; ++e) {
-          if (j * kSampSpan + kSampleStride * e < nF) {
-            const float v = e < 64 ? sc[e] : sc2[e - 64];
-            const int bin = min(kBins - 1, max(0, (int)(__float_as_uint(v) >> 20) - (int)kBinBase));
-            const uint8_t hv = sm.hist[bin][r];
-            sm.hist[bin][r] = hv == 255 ? hv : (uint8_t)(hv + 1);  // saturating: undercounts only lower tau
-            ++n_samp;
+          for (int e = 0; e < 64; ++e) {
+            if (j * kSampSpan + kSampleStride * (half * 64 + e) < nF) {
+              const int bin = min(kBins - 1, max(0, (int)(__float_as_uint(sc[e]) >> 20) - (int)kBinBase));
+              const uint8_t hv = sm.samp.hist[half][bin][r];
+              sm.samp.hist[half][bin][r] = hv == 255 ? hv : (uint8_t)(hv + 1);  // saturating: undercounts only lower tau
+            }
           }
         }
         if (kt == J0 - 1) {
-          // threshold: the estimated count at or above it (sample count scaled by the row's
-          // sampling rate) reaches twice the budget
-          const float scale = n_samp > 0 ? (float)nF / (float)n_samp : 0.f;
-          const float target = 2.f * (float)a.k;
-          float cum = 0.f;
-          tau = 0u;
-          for (int b = kBins - 1; b >= 0; --b) {
-            cum += scale * (float)sm.hist[b][r];
-            if (cum >= target) {
-              tau = b == 0 ? 0u : (uint32_t)(kBinBase + b) << 20;
-              break;
+          if (half == 1) {
+            tc::mbar_arrive(&sm.h_done);  // this half's histograms are complete
+          } else {
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.h_done, 0))) { ok = false; break; }
+            if (ranked) {
+              // threshold: the estimated count at or above it (sample count scaled by the row's
+              // sampling rate; the sweep saw every position of [0, nF) that is a multiple of the
+              // stride) reaches twice the budget
+              const int n_samp = (nF + kSampleStride - 1) / kSampleStride;
+              const float scale = (float)nF / (float)n_samp;
+              const float target = 2.f * (float)a.k;
+              float cum = 0.f;
+              tau = 0u;
+              for (int b = kBins - 1; b >= 0; --b) {
+                cum += scale * (float)(sm.samp.hist[0][b][r] + sm.samp.hist[1][b][r]);
+                if (cum >= target) {
+                  tau = b == 0 ? 0u : (uint32_t)(kBinBase + b) << 20;
+                  break;
+                }
+              }
             }
+            sm.tau[r] = tau;
           }
+          tc::mbar_arrive(&sm.t_free);  // the histograms are free for the score tile
         }
-      } else {
+        continue;
+      }
+      // exact sweep: stage the tile, then compact rows 16 sw .. 16 sw + 15
+      const int x = kt - J0;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.t_free, x & 1))) { ok = false; break; }
+      if (x == 0) c_tau = sm.tau[cr];
 #pragma unroll
-        for (int e = 0; e < 128; ++e) {
-          const uint32_t key = __float_as_uint(e < 64 ? sc[e] : sc2[e - 64]);
-          if (s0 + e < nF && key >= tau) {
-            if (cnt < a.cap) {
-              bkey[cnt] = key;
-              bpos[cnt] = s0 + e;
-              ++cnt;
-            } else {
-              dropped = max(dropped, key);
+      for (int q = 0; q < 16; ++q)
+        *reinterpret_cast<float4*>(&sm.tile[tile_at(r, half * 64 + 4 * q)]) =
+            make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]);
+      tc::mbar_arrive(&sm.t_full);
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.t_full, x & 1))) { ok = false; break; }
+      const int s0 = j * kST;
+      const int c_lim = c_ranked ? c_nF - s0 : 0;  // columns of this tile inside the row's far range
+      const uint32_t below = (1u << lane) - 1u;
+      // kCompRows rows at a time: their loads, ballots and counts are independent chains
+#pragma unroll 1
+      for (int l0 = 0; l0 < 16; l0 += kCompRows) {
+        int lim[kCompRows], n_r[kCompRows];
+        uint32_t t_r[kCompRows], key[kCompRows][4], bal[kCompRows][4];
+#pragma unroll
+        for (int u = 0; u < kCompRows; ++u) {
+          lim[u] = __shfl_sync(0xffffffffu, c_lim, l0 + u);
+          t_r[u] = __shfl_sync(0xffffffffu, c_tau, l0 + u);
+          n_r[u] = __shfl_sync(0xffffffffu, c_cnt, l0 + u);
+        }
+#pragma unroll
+        for (int u = 0; u < kCompRows; ++u)
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int c = m * 32 + lane;
+            key[u][m] = __float_as_uint(sm.tile[tile_at(sw * 16 + l0 + u, c)]);
+            bal[u][m] = __ballot_sync(0xffffffffu, c < lim[u] && key[u][m] >= t_r[u]);
+          }
+#pragma unroll
+        for (int u = 0; u < kCompRows; ++u) {
+          // rows outside the block or the budget have empty ballots: nothing is stored for them
+          const size_t slot = ((size_t)(i0 + sw * 16 + l0 + u - a.row0) * a.Hkv + g) * a.cap;
+          uint32_t d_r = 0;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const bool pass = (bal[u][m] >> lane) & 1u;
+            const int at = n_r[u] + __popc(bal[u][m] & below);
+            const bool st = pass && at < a.cap;
+            if (st) {
+              a.cand_key[slot + at] = key[u][m];
+              a.cand_pos[slot + at] = s0 + m * 32 + lane;
             }
+            d_r = max(d_r, (pass && !st) ? key[u][m] : 0u);
+            n_r[u] += __popc(bal[u][m]);
+          }
+          if (__any_sync(0xffffffffu, d_r != 0))
+            for (int o = 16; o > 0; o >>= 1) d_r = max(d_r, __shfl_xor_sync(0xffffffffu, d_r, o));
+          if (lane == l0 + u) {
+            c_cnt = min(n_r[u], a.cap);
+            c_drop = max(c_drop, d_r);
           }
         }
       }
+      tc::mbar_arrive(&sm.t_free);
     }
     if (!ok) set_abort(sm, a.dev_err);
-    if (half == 0 && row_ok) {
-      const size_t rs = (size_t)(i - a.row0) * a.Hkv + g;
-      a.cand_cnt[rs] = ranked ? cnt : 0;
-      a.cand_drop[rs] = dropped;
-      a.cand_tau[rs] = tau;
+    if (c_ok) {
+      const size_t rs = (size_t)(ci - a.row0) * a.Hkv + g;
+      a.cand_cnt[rs] = c_ranked ? c_cnt : 0;
+      a.cand_drop[rs] = c_drop;
+      a.cand_tau[rs] = c_tau;
     }
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 1) tc::tmem_dealloc(sm.tmem_base, 256);
+  if (warp == 1) tc::tmem_dealloc(sm.tmem_base, 512);
 }
 
 // prefill_topk_warp_kernel (see the top of the file): no CTA barrier anywhere. Four radix
