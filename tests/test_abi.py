@@ -36,6 +36,17 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(H.EXPORTS) <= set(declared_functions())
 
 
+def test_binding_constants_match_the_header():
+    """The binding's device-error bits and dtype codes are the header's."""
+    text = open(HEADER).read()
+    bits = {m: int(v) for m, v in re.findall(r"#define HS2_DEV_([A-Z_]+)\s+(\d+)", text)}
+    assert bits == {"BAD_PAGE": H.DEV_BAD_PAGE, "BAD_INDEX": H.DEV_BAD_INDEX, "TIMEOUT": H.DEV_TIMEOUT,
+                    "BAD_LENGTH": H.DEV_BAD_LENGTH, "SELECT": H.DEV_SELECT}
+    dt = dict(re.findall(r"HS2_(F32|BF16|FP8_E4M3|FP4_E2M1) = (\d+)", text))
+    assert {k: int(v) for k, v in dt.items()} == {"F32": H.F32, "BF16": H.BF16, "FP8_E4M3": H.FP8_E4M3,
+                                                  "FP4_E2M1": H.FP4_E2M1}
+
+
 def test_version_and_strings(lib):
     assert lib.hs2_abi_version() == H.ABI_VERSION == 4
     for st, word in [(0, "ok"), (-1, "invalid"), (-2, "unsupported"), (-3, "CUDA"), (-4, "device")]:

@@ -19,7 +19,7 @@ from . import build as _build
 ABI_VERSION = 4  # include/hs2.h HS2_ABI_VERSION this binding marshals for
 F32, BF16, FP8_E4M3, FP4_E2M1 = 0, 1, 2, 3
 FULL, REINDEX = 0, 1
-DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH = 1, 2, 4, 8
+DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH, DEV_SELECT = 1, 2, 4, 8, 16
 EXPORTS = (
     "hs2_fa_select_workspace", "hs2_fa_select", "hs2_fa_select_ex", "hs2_sa_reuse_workspace", "hs2_sa_reuse", "hs2_sa_reuse_ex",
     "hs2_hier_reindex_workspace", "hs2_hier_reindex", "hs2_strerror", "hs2_last_cuda_error",
