@@ -6,15 +6,15 @@
 // kernel). The n x n score matrix is never stored: scores are produced tile by tile from
 // a tcgen05 recomputation of Q K^T and consumed on the fly.
 //
-// prefill_scan_kernel — one CTA per (128-row tile, KV head), two scoring threads per row:
+// prefill_scan_kernel — one CTA per (128-row tile, KV head), four scoring threads per row:
 //   sweep 0 (sampled): every 4th key position only, 128 of them per tile (512 positions;
 //            a strided tensor map loads just those K rows); each thread bins the sampled
-//            scores of its half of the row's columns into a 256-bin log histogram (1/8
-//            octave per bin) held in shared memory, then the row's first thread picks from
-//            the two histograms a threshold tau whose estimated count of keys at or above it
+//            scores of its quarter of the row's columns into the row's 256-bin log histogram
+//            (1/8 octave per bin, 16-bit counts in shared memory, atomic adds), then the row's
+//            first thread picks a threshold tau whose estimated count of keys at or above it
 //            is twice the budget;
 //   sweep 1 (exact): every key tile; the scoring threads stage the tile's 128 x 128 scores in
-//            shared memory, then each scoring warp takes 16 rows and appends (key, position)
+//            shared memory, then each scoring warp takes 8 rows and appends (key, position)
 //            of the scores >= tau of a row, in ascending position, into the row's candidate
 //            buffer (capacity C) with ballot compaction, so each store is a contiguous run;
 //            past capacity it keeps only the largest dropped key.
@@ -38,7 +38,7 @@ namespace hs2 {
 namespace {
 
 constexpr int kST = 128;        // rows per tile = keys per key tile
-constexpr int kSThreads = 320;  // TMA warp, MMA warp, 8 scoring warps (two per TMEM lane quadrant)
+constexpr int kSThreads = 576;  // TMA warp, MMA warp, 16 scoring warps (four per TMEM lane quadrant)
 constexpr uint32_t kSTile = kST * 128 * 2;
 constexpr int kBins = 256;
 constexpr uint32_t kBinBase = 0x410 - (kBins - 1);  // bin 255 holds keys >> 20 == 0x410 (score 8.0)
@@ -49,7 +49,7 @@ constexpr int kSampSpan = kST * kSampleStride;                // positions cover
 constexpr int kSampPages = kSampSpan / kPage;                 // pages of a sampled key tile (8)
 constexpr uint32_t kSampBoxBytes = kPsSampleRowsPerPage * 128;  // one 64-column half of a page's sampled rows
 
-constexpr int kCompRows = 8;  // rows compacted together by a scoring warp (of its 16)
+constexpr int kCompRows = 4;  // rows compacted together by a scoring warp (of its 8)
 constexpr int kQStages = 3;  // Q tiles in flight: a head's load overlaps the two MMAs before it
 
 struct PsSmem {
@@ -57,8 +57,8 @@ struct PsSmem {
   uint8_t k[2][kSTile];            // B of S (keys x d)
   union {
     struct {
-      uint8_t hist[2][kBins][kST];  // per-row sample histograms ([half][bin][row]), saturating counts,
-    } samp;                         // one per column half of the sampled tiles
+      uint32_t hist[kBins][kST / 2];  // per-row sample histograms, 16-bit counts (rows 2m, 2m+1 share
+    } samp;                           // a word), filled with shared-memory atomics
     float tile[kST * kST];         // exact sweep: the key tile's scores, row-major, swizzled (tile_at)
   };
   uint32_t tau[kST];               // each row's threshold, set at the end of the sampled sweep
@@ -109,19 +109,19 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
     for (int s = 0; s < 4; ++s) {
       tc::mbar_init(&sm.s_full[s], 1);
-      tc::mbar_init(&sm.s_empty[s], 8);
+      tc::mbar_init(&sm.s_empty[s], 16);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&sm.k_full[s], 1);
       tc::mbar_init(&sm.k_empty[s], 1);
     }
-    tc::mbar_init(&sm.h_done, 128);
-    tc::mbar_init(&sm.t_full, 256);
-    tc::mbar_init(&sm.t_free, 256);
+    tc::mbar_init(&sm.h_done, 384);
+    tc::mbar_init(&sm.t_full, 512);
+    tc::mbar_init(&sm.t_free, 512);
     sm.abort = 0;
     tc::fence_mbar_init();
   }
-  for (int e = threadIdx.x; e < 2 * kBins * kST / 4; e += kSThreads) reinterpret_cast<uint32_t*>(sm.samp.hist)[e] = 0;
+  for (int e = threadIdx.x; e < kBins * kST / 2; e += kSThreads) (&sm.samp.hist[0][0])[e] = 0u;
   if (warp == 1) tc::tmem_alloc(&sm.tmem_base, 512);
   tc::tc_fence_before();
   __syncthreads();
@@ -224,11 +224,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- scoring warps
-    // warps 2-5 own rows and columns 0-63 of every S tile; warps 6-9 take columns 64-127
-    // of the same rows. In the sampled sweep each half bins its columns into its own
-    // histograms and the row owner (first half) sets the threshold from both; in the exact
-    // sweep all eight warps stage the tile's scores, then each compacts 16 rows.
-    const int half = (warp - 2) >> 2;
+    // warps 2-5 own rows and columns 0-31 of every S tile; warps 6-9, 10-13 and 14-17 take
+    // columns 32-63, 64-95 and 96-127 of the same rows (a warp reaches only its TMEM lane
+    // quadrant, warp % 4). In the sampled sweep every warp bins its columns into the rows'
+    // shared histograms and the row owner (first quarter) sets the threshold; in the exact
+    // sweep all sixteen warps stage the tile's scores, then each compacts 8 rows.
+    const int quarter = (warp - 2) >> 2;
     const int qd = warp & 3;
     const int r = qd * 32 + lane;
     const int i = i0 + r;
@@ -238,11 +239,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     // the row's lse of each head: G floats, read through L1 one head ahead of their use
     const float* lse2_row = a.lse2 + (size_t)(row_ok ? i : a.row0) * a.Hq + g * G;
-    // rows this warp compacts in the exact sweep: lane l < 16 keeps the state of row 16 sw + l
+    // rows this warp compacts in the exact sweep: lane l < 8 keeps the state of row 8 sw + l
     const int sw = warp - 2;
-    const int cr = sw * 16 + (lane & 15);
+    const int cr = sw * 8 + (lane & 7);
     const int ci = i0 + cr;
-    const bool c_ok = lane < 16 && ci < a.row1;
+    const bool c_ok = lane < 8 && ci < a.row1;
     const int c_nF = c_ok ? max(0, ci + 1 - a.w) : 0;
     const bool c_ranked = c_nF > a.k;
     uint32_t c_tau = 0xffffffffu;  // read from shared memory once the sampled sweep is over
@@ -253,9 +254,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
     for (int kt = 0; kt < NKT && ok; ++kt) {
       const bool sample = kt < J0;
       const int j = jof(kt);
-      float sc[64];
+      float sc[32];
 #pragma unroll
-      for (int e = 0; e < 64; ++e) sc[e] = 0.f;
+      for (int e = 0; e < 32; ++e) sc[e] = 0.f;
       float l2_next = __ldg(lse2_row);
       for (int hl = 0; hl < G; ++hl) {
         const float l2 = l2_next;
@@ -265,35 +266,30 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (!__all_sync(0xffffffffu, !aborted(sm) && tc::mbar_wait(&sm.s_full[sb], (it >> 2) & 1))) { ok = false; break; }
         __syncwarp();
         tc::tc_fence_after();
-        uint32_t raw[2][32];
-        const uint32_t ta = tS + lane_off + sb * 128 + half * 64;
-        tc::tmem_ld32_async(ta, raw[0]);
-        tc::tmem_ld32_async(ta + 32, raw[1]);
-        tc::tmem_wait_ld(raw[1]);
-        tc::tmem_regs_ready(raw[0]);
+        uint32_t raw[32];
+        tc::tmem_ld32_async(tS + lane_off + sb * 128 + quarter * 32, raw);
+        tc::tmem_wait_ld(raw);
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sm.s_empty[sb]);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) sc[e] += tc::ex2(fmaf(__uint_as_float(raw[e >> 5][e & 31]), a.scale_log2, -l2));
+        for (int e = 0; e < 32; ++e) sc[e] += tc::ex2(fmaf(__uint_as_float(raw[e]), a.scale_log2, -l2));
       }
       if (!ok) break;
       if (sample) {
         if (ranked) {
-          // column half * 64 + e of a sampled tile is position j * kSampSpan + kSampleStride * (half * 64 + e);
-          // each half bins its own columns
+          // column 32 quarter + e of a sampled tile is position j * kSampSpan + kSampleStride * (32 quarter + e)
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            if (j * kSampSpan + kSampleStride * (half * 64 + e) < nF) {
+          for (int e = 0; e < 32; ++e) {
+            if (j * kSampSpan + kSampleStride * (quarter * 32 + e) < nF) {
               const int bin = min(kBins - 1, max(0, (int)(__float_as_uint(sc[e]) >> 20) - (int)kBinBase));
-              const uint8_t hv = sm.samp.hist[half][bin][r];
-              sm.samp.hist[half][bin][r] = hv == 255 ? hv : (uint8_t)(hv + 1);  // saturating: undercounts only lower tau
+              atomicAdd(&sm.samp.hist[bin][r >> 1], 1u << ((r & 1) * 16));
             }
           }
         }
         if (kt == J0 - 1) {
-          if (half == 1) {
-            tc::mbar_arrive(&sm.h_done);  // this half's histograms are complete
+          if (quarter != 0) {
+            tc::mbar_arrive(&sm.h_done);  // this thread's counts are in
           } else {
             if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.h_done, 0))) { ok = false; break; }
             if (ranked) {
@@ -306,7 +302,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
               float cum = 0.f;
               tau = 0u;
               for (int b = kBins - 1; b >= 0; --b) {
-                cum += scale * (float)(sm.samp.hist[0][b][r] + sm.samp.hist[1][b][r]);
+                cum += scale * (float)((sm.samp.hist[b][r >> 1] >> ((r & 1) * 16)) & 0xffffu);
                 if (cum >= target) {
                   tau = b == 0 ? 0u : (uint32_t)(kBinBase + b) << 20;
                   break;
@@ -319,13 +315,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
         continue;
       }
-      // exact sweep: stage the tile, then compact rows 16 sw .. 16 sw + 15
+      // exact sweep: stage the tile, then compact rows 8 sw .. 8 sw + 7
       const int x = kt - J0;
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.t_free, x & 1))) { ok = false; break; }
       if (x == 0) c_tau = sm.tau[cr];
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        *reinterpret_cast<float4*>(&sm.tile[tile_at(r, half * 64 + 4 * q)]) =
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(&sm.tile[tile_at(r, quarter * 32 + 4 * q)]) =
             make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]);
       tc::mbar_arrive(&sm.t_full);
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.t_full, x & 1))) { ok = false; break; }
@@ -334,7 +330,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const uint32_t below = (1u << lane) - 1u;
       // kCompRows rows at a time: their loads, ballots and counts are independent chains
 #pragma unroll 1
-      for (int l0 = 0; l0 < 16; l0 += kCompRows) {
+      for (int l0 = 0; l0 < 8; l0 += kCompRows) {
         int lim[kCompRows], n_r[kCompRows];
         uint32_t t_r[kCompRows], key[kCompRows][4], bal[kCompRows][4];
 #pragma unroll
@@ -348,13 +344,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             const int c = m * 32 + lane;
-            key[u][m] = __float_as_uint(sm.tile[tile_at(sw * 16 + l0 + u, c)]);
+            key[u][m] = __float_as_uint(sm.tile[tile_at(sw * 8 + l0 + u, c)]);
             bal[u][m] = __ballot_sync(0xffffffffu, c < lim[u] && key[u][m] >= t_r[u]);
           }
 #pragma unroll
         for (int u = 0; u < kCompRows; ++u) {
           // rows outside the block or the budget have empty ballots: nothing is stored for them
-          const size_t slot = ((size_t)(i0 + sw * 16 + l0 + u - a.row0) * a.Hkv + g) * a.cap;
+          const size_t slot = ((size_t)(i0 + sw * 8 + l0 + u - a.row0) * a.Hkv + g) * a.cap;
           uint32_t d_r = 0;
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
