@@ -62,14 +62,15 @@ struct PsSmem {
     float tile[kST * kST];         // exact sweep: the key tile's scores, row-major, swizzled (tile_at)
   };
   uint32_t tau[kST];               // each row's threshold, set at the end of the sampled sweep
-  uint64_t q_full[kQStages], q_empty[kQStages], k_full[2], k_empty[2], s_full[4], s_empty[4], h_done;
+  uint64_t q_full[kQStages], q_empty[kQStages], k_full[2], k_empty[2], s_full[4], s_empty[4];
+  uint64_t h_done;                 // sampled sweep: the other three quarters' counts are in
   uint64_t t_full, t_free;         // exact sweep: tile written by all scoring threads / tile consumed
   uint32_t tmem_base;
   int abort;
 };
 
-// element (row r, column c) of the staged score tile; the XOR keeps both the row owners'
-// 16-byte column writes and the row-wise 32-lane reads free of bank conflicts
+// element (row r, column c) of the staged score tile; the XOR keeps both the scoring
+// threads' 16-byte column writes and the row-wise 32-lane reads free of bank conflicts
 HS2_DEVI int tile_at(int r, int c) { return r * kST + (c ^ ((r & 7) << 2)); }
 
 HS2_DEVI bool aborted(PsSmem& sm) { return *(volatile int*)&sm.abort != 0; }
