@@ -49,14 +49,6 @@ HS2_FMA_BF16(fmab_lh, 0, 1)
 HS2_FMA_BF16(fmab_hl, 1, 0)
 #undef HS2_FMA_BF16
 
-HS2_DEVI uint4 ldg_nc_v4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
 // L2 cache policy that keeps lines (evict last): for K/V rows that the same kernel, or
 // the next SA layer of the group, reads again while other traffic streams past.
 HS2_DEVI uint64_t l2_keep_policy() {
@@ -64,7 +56,7 @@ HS2_DEVI uint64_t l2_keep_policy() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-// (any L2 policy: keep or evict-first)
+// 16-byte read-only load with an L2 policy (keep or evict-first)
 HS2_DEVI uint4 ldg_nc_v4_keep(const void* p, uint64_t pol) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
@@ -84,15 +76,6 @@ HS2_DEVI uint64_t l2_first_policy() {
 HS2_DEVI void stg_f32_pol(float* p, float v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
 }
-
-HS2_DEVI uint2 ldg_nc_v2(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
-}
-
-// Barrier `id` (1..15) over `n` threads (a multiple of 32) of the CTA.
-HS2_DEVI void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 HS2_DEVI void flag_error(int32_t* dev_err, int bits) {
   if (dev_err) atomicOr(dev_err, bits);
