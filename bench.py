@@ -8,7 +8,10 @@ permuted block table), queries x @ W_Q with a distinct W_Q per layer, 32
 needles per sequence. One step = hs2_fa_select + 5 x hs2_sa_reuse on resident
 inputs. ``--workload`` selects the other configurations for measurement:
 ``prefill`` (n=32768), ``long_decode`` (batch 16 x 131072, 4 independent
-caches, 24 layers) and ``csa2`` (Full + Reindex indexer, 5 MQA layers).
+caches, 24 layers), ``csa2`` (Full + Reindex indexer, 5 MQA layers), and the
+decode variants ``decode_block`` (block-level selection, 64-position blocks),
+``decode_fp8`` / ``decode_fp4`` (E4M3 / E2M1 paged KV), ``decode_append`` and
+``long_decode_append`` (the current token's K/V appended inside the step).
 
 Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle on a
 bounded sample of the same workload. Under torchrun every rank runs its own
