@@ -133,6 +133,46 @@ def _fp4_bias2(c):
     return sign * np.where(e == 0, m * 0.25, (1.0 + m / 2.0) * np.exp2(e - 2.0))
 
 
+def _sa_rows_variant(t_of, idx_row, gate_rows):
+    """sa_prefill_rows with one of its three row bookkeeping choices swapped out."""
+    def f(q, kv, rows, w, idx, cnt, scale, sink=None, gate=None):
+        rows = np.asarray(rows, dtype=np.int64)
+        qf = O.to_f64(q, O._qdtype(kv))
+        _, Hq, d = qf.shape
+        Hkv = kv.k.shape[1]
+        G = Hq // Hkv
+        o = np.zeros((len(rows), Hq, d))
+        for r, i in enumerate(rows):
+            t = t_of(int(i))
+            j = idx_row(r, int(i))
+            for g in range(Hkv):
+                U = O._union(t, w, idx[j, g, :cnt[j, g]])
+                K = O.gather_rows(kv.k, kv.block_table[0], g, U, kv.page, kv.dtype, O._scale(kv, "k"))
+                V = O.gather_rows(kv.v, kv.block_table[0], g, U, kv.page, kv.dtype, O._scale(kv, "v"))
+                hs = slice(g * G, (g + 1) * G)
+                o[r, hs] = O.sparse_attention(qf[i, hs], K, V, scale, None if sink is None else np.asarray(sink)[hs])
+        return O.output_gate(o, None if gate is None else O.to_f64(np.asarray(gate)[gate_rows(rows)], "f32"))
+    return f
+
+
+_sa_rows_t_is_i = _sa_rows_variant(lambda i: i, lambda r, i: i, lambda rows: rows)  # t = i, not i + 1
+_sa_rows_t_is_i.__name__ = "_sa_rows_t_is_i"
+_sa_rows_idx_by_sample = _sa_rows_variant(lambda i: i + 1, lambda r, i: r, lambda rows: rows)  # idx[r]
+_sa_rows_idx_by_sample.__name__ = "_sa_rows_idx_by_sample"
+_sa_rows_gate_by_sample = _sa_rows_variant(lambda i: i + 1, lambda r, i: i,
+                                           lambda rows: np.arange(len(rows)))  # gate[r]
+_sa_rows_gate_by_sample.__name__ = "_sa_rows_gate_by_sample"
+
+
+def _bf16_as_f16(x, dtype):  # bf16 bit patterns read as IEEE half
+    if dtype == "bf16":
+        return np.ascontiguousarray(x, dtype=np.uint16).view(np.float16).astype(np.float64)
+    return _to_f64_ref(x, dtype)
+
+
+_to_f64_ref = O.to_f64
+
+
 MUTATIONS = [
     ("selection_scores", _sel_no_lse),
     ("selection_scores", _sel_max_not_sum),
@@ -152,6 +192,10 @@ MUTATIONS = [
     ("kv_append", _append_past_current),
     ("fp4_unpack", _fp4_high_nibble_first),
     ("fp4_e2m1_to_f64", _fp4_bias2),
+    ("sa_prefill_rows", _sa_rows_t_is_i),
+    ("sa_prefill_rows", _sa_rows_idx_by_sample),
+    ("sa_prefill_rows", _sa_rows_gate_by_sample),
+    ("to_f64", _bf16_as_f16),
 ]
 
 PINS = [
@@ -183,6 +227,10 @@ PINS = [
     P.test_fp4_e2m1_values_from_the_format,
     P.test_fp4_unpack_channel_order,
     P.test_oracle_on_fp4_pool_equals_oracle_on_its_dequantised_values,
+    *[(lambda sg=sg: P.test_sa_prefill_rows_dense_when_k_covers_far_range(sg)) for sg in (False, True)],
+    *[(lambda sg=sg: P.test_sa_prefill_rows_partial_sets_bruteforce(sg)) for sg in (False, True)],
+    P.test_sa_prefill_last_row_equals_decode,
+    P.test_bf16_widening_known_bit_patterns,
 ]
 
 

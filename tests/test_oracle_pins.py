@@ -649,3 +649,121 @@ def test_fa_after_append_is_dense_over_sequence_ending_in_new_row():
             ref = sum((e / z) * V[s] for s, e in enumerate(ex))
             np.testing.assert_allclose(o[b, h], ref, rtol=0, atol=1e-12)
             assert abs(lse[b, h] - (m + math.log(z))) < 1e-12
+
+
+# ----------------------------------------------------------------------------- SA prefill rows
+def sa_rows_bruteforce(Q, K, V, scale, rows, allowed, sink=None, gate=None):
+    """SA of query rows ``rows`` written with an explicit mask: ``allowed(i, s)`` says whether
+    row i may attend to key position s; one softmax over the allowed keys with Python loops and
+    math.exp, a sink logit b adding exp(b) to the denominator, and a gate g multiplying each
+    output element by 1 / (1 + exp(-g)). Q [n][d], K, V [n][d]; returns [len(rows)][d]."""
+    n, d = K.shape[0], V.shape[1]
+    out = np.zeros((len(rows), d))
+    for r, i in enumerate(rows):
+        logits = [float(Q[i] @ K[s]) * scale for s in range(n) if allowed(i, s)]
+        pos = [s for s in range(n) if allowed(i, s)]
+        m = max(logits + ([sink] if sink is not None else []))
+        ex = [math.exp(x - m) for x in logits]
+        z = sum(ex) + (math.exp(sink - m) if sink is not None else 0.0)
+        for e, s in zip(ex, pos):
+            out[r] += (e / z) * V[s]
+        if gate is not None:
+            out[r] = [out[r][c] / (1.0 + math.exp(-float(gate[i][c]))) for c in range(d)]
+    return out
+
+
+def _random_far_sets(n, Hkv, w, k, seed):
+    """Independent of the FA: row i's set is a random subset of F(i + 1) = [0, i - w] of size
+    min(k, |F|), ascending and -1 padded, so every row's set differs from its neighbours'."""
+    rng = np.random.default_rng(seed)
+    idx = np.full((n, Hkv, k), -1, np.int32)
+    cnt = np.zeros((n, Hkv), np.int32)
+    for i in range(n):
+        nf = max(0, i + 1 - w)
+        for g in range(Hkv):
+            c = min(k, nf)
+            idx[i, g, :c] = np.sort(rng.choice(nf, size=c, replace=False)) if c else []
+            cnt[i, g] = c
+    return idx, cnt
+
+
+_SA_ROWS = [44, 3, 20, 0, 5, 4, 31]  # unsorted, not 0..R-1: row i and sample r differ
+
+
+@pytest.mark.parametrize("sink_gate", [False, True])
+def test_sa_prefill_rows_dense_when_k_covers_far_range(sink_gate):
+    """k >= |F| for every row => SA prefill row i is dense causal attention of the SA query of
+    row i over keys 0..i ([CSA2] §5.1 degeneration check; [HS2] §7.2 window + far set under one
+    normaliser), through a permuted block table, with and without sink bias and output gate."""
+    n, Hq, Hkv, d, w, k = 45, 4, 2, 8, 5, 60
+    grp = W.prefill_group(n, Hq, Hkv, d, w=w, k=k, dtype="f32", seed=31, n_sa=1, page=8, permute=True)
+    kv = grp.kv
+    idx = np.full((n, Hkv, k), -1, np.int32)
+    cnt = np.zeros((n, Hkv), np.int32)
+    for i in range(n):
+        f = max(0, i + 1 - w)
+        idx[i, :, :f] = np.arange(f)
+        cnt[i, :] = f
+    rng = np.random.default_rng(5)
+    sink = rng.standard_normal(Hq) if sink_gate else None
+    gate = rng.standard_normal((n, Hq, d)).astype(np.float32) if sink_gate else None
+    o = O.sa_prefill_rows(grp.q_sa[0], kv, _SA_ROWS, w, idx, cnt, grp.scale, sink=sink, gate=gate)
+    Q = O.to_f64(grp.q_sa[0], "f32")
+    G = Hq // Hkv
+    for g in range(Hkv):
+        K, V = contiguous_rows(kv, 0, g, n)
+        for h in range(g * G, (g + 1) * G):
+            ref = sa_rows_bruteforce(Q[:, h], K, V, grp.scale, _SA_ROWS, lambda i, s: s <= i,
+                                     sink=None if sink is None else float(sink[h]),
+                                     gate=None if gate is None else gate[:, h].astype(np.float64))
+            np.testing.assert_allclose(o[:, h], ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("sink_gate", [False, True])
+def test_sa_prefill_rows_partial_sets_bruteforce(sink_gate):
+    """Each row attends exactly to its own window W(i + 1) = [i - w + 1, i] and its own far set
+    idx[i] (a random subset of [0, i - w]), under one softmax: an explicit per-row mask."""
+    n, Hq, Hkv, d, w, k = 40, 4, 2, 8, 4, 3
+    grp = W.prefill_group(n, Hq, Hkv, d, w=w, k=k, dtype="f32", seed=32, n_sa=1, page=8, permute=True)
+    kv = grp.kv
+    idx, cnt = _random_far_sets(n, Hkv, w, k, seed=9)
+    rng = np.random.default_rng(6)
+    sink = rng.standard_normal(Hq) if sink_gate else None
+    gate = rng.standard_normal((n, Hq, d)).astype(np.float32) if sink_gate else None
+    rows = [39, 2, 17, 0, 8, 4, 3, 25]
+    o = O.sa_prefill_rows(grp.q_sa[0], kv, rows, w, idx, cnt, grp.scale, sink=sink, gate=gate)
+    Q = O.to_f64(grp.q_sa[0], "f32")
+    G = Hq // Hkv
+    for g in range(Hkv):
+        K, V = contiguous_rows(kv, 0, g, n)
+        sets = [set(idx[i, g, :cnt[i, g]].tolist()) for i in range(n)]
+        allowed = (lambda i, s, sets=sets: (i - w < s <= i) or s in sets[i])
+        for h in range(g * G, (g + 1) * G):
+            ref = sa_rows_bruteforce(Q[:, h], K, V, grp.scale, rows, allowed,
+                                     sink=None if sink is None else float(sink[h]),
+                                     gate=None if gate is None else gate[:, h].astype(np.float64))
+            np.testing.assert_allclose(o[:, h], ref, rtol=0, atol=1e-12)
+
+
+def test_sa_prefill_last_row_equals_decode():
+    """SA prefill row n-1 (t = n) and an SA decode query with seq_len n over the same cache,
+    query and indices give the same output (both are [HS2] §7.2 at one query)."""
+    n, Hq, Hkv, d, w, k = 70, 4, 2, 8, 6, 9
+    grp = W.prefill_group(n, Hq, Hkv, d, w=w, k=k, dtype="bf16", seed=33, n_sa=1, page=16, permute=True)
+    kv = grp.kv
+    idx, cnt = _random_far_sets(n, Hkv, w, k, seed=10)
+    pre = O.sa_prefill_rows(grp.q_sa[0], kv, [n - 1], w, idx, cnt, grp.scale)
+    dec = O.sa_decode(grp.q_sa[0][n - 1:n], kv, w, idx[n - 1:n], cnt[n - 1:n], grp.scale)
+    np.testing.assert_allclose(pre, dec, rtol=0, atol=1e-13)
+
+
+def test_bf16_widening_known_bit_patterns():
+    """bfloat16 is the top half of an IEEE binary32 word: 1 sign, 8 exponent bits (bias 127),
+    7 mantissa bits; values written out from the format, not from a conversion routine."""
+    bits = np.array([0x3F80, 0xC000, 0x0001, 0x8000, 0x7F7F, 0x3F81, 0x0080, 0x4049], np.uint16)
+    want = [1.0, -2.0, 2.0 ** -133, 0.0, (2.0 - 2.0 ** -7) * 2.0 ** 127, 1.0 + 2.0 ** -7, 2.0 ** -126,
+            3.140625]
+    got = O.to_f64(bits, "bf16")
+    assert got.dtype == np.float64
+    assert list(got) == want
+    assert math.copysign(1.0, got[3]) == -1.0  # 0x8000 is negative zero
