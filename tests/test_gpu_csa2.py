@@ -148,12 +148,31 @@ def test_indexer_cluster_selection_with_ties(H, distinct):
 @pytest.mark.slow
 def test_csa2_full_size_sampled(H):
     """CSA2 decode at full size (B=8, t=131072, 64 indexer heads, top-512, 2048-block pool):
-    two sampled rows against the oracle, invariants on all rows."""
+    two sampled rows against the oracle, invariants on all rows; then the five attention
+    layers (Full -> SA with its own top-512, Reindex -> SA, three Reuse -> SA with the
+    Reindex indices; w = 0, MQA) on the sampled rows against the oracle."""
+    import torch
+
     grp = W.csa2_group([131072] * 8, Hq=32, d=128, Hi=64, di=128, k_top=512, blk=8, max_blocks=2048,
                        n_reuse=3, needles=32, seed=0)
-    idx_f, cnt_f, pool, pcnt, idx_r, cnt_r = check_indexer(H, grp, 2048, 512, batches=[0, 5])
+    sample = [0, 5]
+    idx_f, cnt_f, pool, pcnt, idx_r, cnt_r = check_indexer(H, grp, 2048, 512, batches=sample)
     assert (cnt_f == 512).all() and (pcnt == 2048).all() and (cnt_r == 512).all()
     for b in range(8):
         assert set(grp.needles[b].tolist()) <= set(idx_f[b].tolist())
         pos = set(O.pool_positions(pool[b], 131072, 8).tolist())
         assert set(idx_f[b].tolist()) <= pos and set(idx_r[b].tolist()) <= pos
+    kv = grp.kv
+    dkv = kv_to_device(kv)
+    sub = W.PagedKV(k=kv.k, v=kv.v, block_table=kv.block_table[sample], seq_len=kv.seq_len[sample], dtype=kv.dtype,
+                    page=kv.page)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layers = [(idx_f, cnt_f), (idx_r, cnt_r)] + [(idx_r, cnt_r)] * 3
+    assert len(grp.q_main) == len(layers)
+    for layer, (ii, cc) in enumerate(layers):
+        o = H.hs2_sa_reuse(to_torch(grp.q_main[layer], "bf16"), dkv, 0, to_torch(ii[:, None, :], "i32"),
+                           to_torch(cc[:, None], "i32"), 512, grp.scale, dev_err=err).cpu().numpy()
+        ref = O.sa_decode(grp.q_main[layer][sample], sub, 0, ii[sample][:, None, :], cc[sample][:, None], grp.scale)
+        assert max_abs(o[sample], ref) <= tol("bf16"), (layer, max_abs(o[sample], ref))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0

@@ -163,6 +163,49 @@ def test_decode_bf16_full_size_sampled(H):
             assert set(grp.needles[b].tolist()) <= set(s.tolist())
 
 
+@pytest.mark.parametrize("lens,Hkv", [([60000, 33000, 20000], 2), ([17000, 12000], 1)])
+def test_decode_cluster_selection_long_rows(H, lens, Hkv):
+    """Few long rows: the window-excluding top-k of each (query, KV head) is shared by a
+    thread-block cluster (one CTA per 8192 keys of the longest row: 8 CTAs for the first
+    case, 3 for the second), each CTA filtering its slice and rank 0 refining the candidates
+    from the others' shared memory. Unit-variance keys and queries: no ties, so the cluster
+    filter completes without the all-keys fallback. Every sequence against the oracle."""
+    grp = W.decode_group(lens, Hq=8, Hkv=Hkv, d=128, w=128, k=1024, dtype="bf16", seed=51, n_sa=1, needles=16)
+    o, idx, cnt = check_group(H, grp)
+    for b, t in enumerate(lens):
+        assert (cnt[b] == 1024).all()
+        for g in range(Hkv):
+            assert set(grp.needles[b].tolist()) <= set(idx[b, g, :1024].tolist())
+
+
+def long_decode_cache(gi: int, seed: int = 0):
+    """Cache ``gi`` of the long-context decode workload, drawn exactly as the benchmark draws
+    it: B=16, t=131072, Hq=32, Hkv=4, d=128, w=128, k=1024, 64 needles, five SA layers."""
+    s_len, s_grp = np.random.SeedSequence([seed, gi]).spawn(2)
+    lens = W.uniform_lengths(16, 131072, 131072, s_len)
+    return W.decode_group(lens, 32, 4, 128, 128, 1024, "bf16", s_grp, n_sa=5, needles=64, qproj=False)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("gi", range(4))
+def test_long_decode_full_size_sampled(H, gi):
+    """Long-context decode at full size, one of the four independent Cross-group caches per
+    case (each runs the same calls and launch shapes as in the timed step, including the
+    4-CTA cluster selection over 130,944 far keys per row): two sampled sequences against the
+    oracle element by element (FA output, lse, index sets, all five SA layers), and on every
+    sequence the set invariants and the needles."""
+    grp = long_decode_cache(gi)
+    sample = sorted(np.random.default_rng(100 + gi).choice(16, size=2, replace=False).tolist())
+    o, idx, cnt = check_group(H, grp, batches=sample)
+    t = grp.kv.seq_len
+    assert (cnt == 1024).all()
+    for b in range(16):
+        for g in range(4):
+            s = idx[b, g]
+            assert s.min() >= 0 and s.max() < t[b] - 128 and np.all(np.diff(s) > 0)
+            assert set(grp.needles[b].tolist()) <= set(s.tolist())
+
+
 @pytest.mark.parametrize("dtype,Hq,Hkv", [("bf16", 32, 4), ("bf16", 32, 1), ("f32", 8, 2)])
 def test_sa_sink_bias_and_output_gate(H, dtype, Hq, Hkv):
     """hs2_sa_reuse_ex: per-head sink logits (one -inf, one dominant) and elementwise gate

@@ -148,14 +148,69 @@ def test_prefill_selection_needles(H):
 
 @pytest.mark.slow
 def test_prefill_full_size_sampled_rows(H):
-    """Prefill workload at full size (n=32768, Hq=32, Hkv=4, d=128, w=128, k=1024, AR(1) keys):
-    256 seeded random rows plus {0, w-1, w, w+k-1, w+k, n-1}, each exact against all its keys."""
+    """Prefill workload at full size (n=32768, Hq=32, Hkv=4, d=128, w=128, k=1024, AR(1) keys,
+    five SA layers): 256 seeded random rows plus {0, w-1, w, w+k-1, w+k, n-1}, each exact
+    against all its keys: FA output, lse and index sets; then every SA layer at those rows with
+    the GPU's index sets, and the first SA layer again with the oracle's sets at those rows."""
+    import torch
+
     n, w, k = 32768, 128, 1024
-    grp = W.prefill_group(n, 32, 4, 128, w=w, k=k, dtype="bf16", seed=0, n_sa=0, rho=0.999)
+    grp = W.prefill_group(n, 32, 4, 128, w=w, k=k, dtype="bf16", seed=0, n_sa=5, rho=0.999)
     rows = np.unique(np.concatenate([np.random.default_rng(7).choice(n, 256, replace=False),
                                      [0, w - 1, w, w + k - 1, w + k, n - 1]]))
-    idx, cnt, _ = check_selection(H, grp, rows)
+    o, lse, idx, cnt = run_fa(H, grp)
+    o_r, lse_r, idx_r, cnt_r, sc = O.fa_prefill_rows(grp.q_fa, grp.kv, rows, w, k, grp.scale, return_scores=True)
+    assert max_abs(o[rows], o_r) <= tol("bf16"), max_abs(o[rows], o_r)
+    assert max_abs(lse[rows], lse_r) <= tol("bf16"), max_abs(lse[rows], lse_r)
+    check_index_sets(idx[rows], cnt[rows], idx_r, cnt_r, sc, "prefill ")
     assert (cnt >= 0).all()
+    dkv = kv_to_device(grp.kv)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d_idx, d_cnt = to_torch(idx, "i32"), to_torch(cnt, "i32")
+    for j in range(5):
+        osa = H.hs2_sa_reuse(to_torch(grp.q_sa[j], "bf16"), dkv, w, d_idx, d_cnt, k, grp.scale, prefill=True,
+                             dev_err=err)[torch.from_numpy(rows).cuda()].cpu().numpy()
+        ref = O.sa_prefill_rows(grp.q_sa[j], grp.kv, rows, w, idx, cnt, grp.scale)
+        assert max_abs(osa, ref) <= tol("bf16"), (j, max_abs(osa, ref))
+    mix_idx, mix_cnt = idx.copy(), cnt.copy()
+    mix_idx[rows], mix_cnt[rows] = idx_r, cnt_r
+    osa = H.hs2_sa_reuse(to_torch(grp.q_sa[0], "bf16"), dkv, w, to_torch(mix_idx, "i32"), to_torch(mix_cnt, "i32"),
+                         k, grp.scale, prefill=True, dev_err=err)[torch.from_numpy(rows).cuda()].cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = O.sa_prefill_rows(grp.q_sa[0], grp.kv, rows, w, mix_idx, mix_cnt, grp.scale)
+    assert max_abs(osa, ref) <= tol("bf16"), max_abs(osa, ref)
+
+
+def test_tiny_fp32_prefill_all_rows(H):
+    """Tiny fp32 group, prefill half: all 2048 rows of the FA (output, lse, index sets) and
+    the SA layer over every row, at the fp32 tolerance; the SA layer also with the oracle's
+    index sets fed to both."""
+    import torch
+
+    tg = W.tiny_group(seed=0)
+    pre = tg.prefill
+    n = pre.q_fa.shape[0]
+    o, lse, idx, cnt = run_fa(H, pre)
+    rows = np.arange(n)
+    o_r, lse_r, idx_r, cnt_r, sc = O.fa_prefill_rows(pre.q_fa, pre.kv, rows, pre.w, pre.k, pre.scale,
+                                                     return_scores=True)
+    assert max_abs(o, o_r) <= tol("f32"), max_abs(o, o_r)
+    assert max_abs(lse, lse_r) <= tol("f32"), max_abs(lse, lse_r)
+    check_index_sets(idx, cnt, idx_r, cnt_r, sc, "tiny prefill ")
+    dkv = kv_to_device(pre.kv)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q = to_torch(pre.q_sa[0], "f32")
+    osa = H.hs2_sa_reuse(q, dkv, pre.w, to_torch(idx, "i32"), to_torch(cnt, "i32"), pre.k, pre.scale, prefill=True,
+                         dev_err=err).cpu().numpy()
+    ref = O.sa_prefill_rows(pre.q_sa[0], pre.kv, rows, pre.w, idx, cnt, pre.scale)
+    assert max_abs(osa, ref) <= tol("f32"), max_abs(osa, ref)
+    osa = H.hs2_sa_reuse(q, dkv, pre.w, to_torch(idx_r, "i32"), to_torch(cnt_r, "i32"), pre.k, pre.scale,
+                         prefill=True, dev_err=err).cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = O.sa_prefill_rows(pre.q_sa[0], pre.kv, rows, pre.w, idx_r, cnt_r, pre.scale)
+    assert max_abs(osa, ref) <= tol("f32"), max_abs(osa, ref)
 
 
 @pytest.mark.parametrize("n,Hq,Hkv,w,k", [(1000, 8, 2, 16, 64), (777, 32, 4, 128, 256), (600, 16, 1, 32, 100)])
