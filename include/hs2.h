@@ -64,8 +64,9 @@ typedef enum {
 #define HS2_DEV_BAD_INDEX 2   /* selected position outside F(t) (or outside [0,t) with w=0) */
 #define HS2_DEV_TIMEOUT 4     /* a bounded wait (mbarrier / TMA / MMA) gave up */
 #define HS2_DEV_BAD_LENGTH 8  /* seq_len < 1 or beyond max_pages * page_size */
-#define HS2_DEV_SELECT 16     /* a prefill row's streamed candidates could not prove its top-k
-                                 (its idx_cnt is written as -1); see hs2_fa_select */
+#define HS2_DEV_SELECT 16     /* reserved: no longer raised. A prefill row whose streamed
+                                 candidates cannot prove its top-k is recomputed exactly over
+                                 its whole far range inside hs2_fa_select */
 
 typedef enum { HS2_F32 = 0, HS2_BF16 = 1, HS2_FP8_E4M3 = 2, HS2_FP4_E2M1 = 3 } hs2_dtype;
 

@@ -221,7 +221,8 @@ constexpr int kPrefillChunk = 32768;
 
 struct PrefillPlan {
   int chunk, cap;
-  size_t off_lse2, off_ckey, off_cpos, off_ccnt, off_cdrop, off_ctau, total;
+  size_t off_lse2, off_ckey, off_cpos, off_ccnt, off_cdrop, off_ctau, off_redo_list, off_redo_cnt, off_redo_keys,
+      total;
 };
 
 PrefillPlan prefill_plan(int n, int Hq, const hs2_kv* kv, int k) {
@@ -242,6 +243,12 @@ PrefillPlan prefill_plan(int n, int Hq, const hs2_kv* kv, int k) {
   off = align256(off + rows * 4);
   p.off_ctau = off;
   off = align256(off + rows * 4);
+  p.off_redo_list = off;  // rows the candidates cannot prove, completed exactly
+  off = align256(off + rows * 4);
+  p.off_redo_cnt = off;
+  off = align256(off + 4);
+  p.off_redo_keys = off;  // one key row of up to n far positions per completion CTA
+  off = align256(off + (size_t)hs2::kPsCompleteCtas * n * 4);
   p.total = off;
   return p;
 }
@@ -347,8 +354,16 @@ static hs2_status fa_select_prefill_tc(const void* q, int n, int Hq, const hs2_k
   b.cand_tau = (uint32_t*)(ws + p.off_ctau);
   b.idx = idx;
   b.cnt = idx_cnt;
+  b.q = q;
+  b.kpool = kv->k;
+  b.redo_list = (int32_t*)(ws + p.off_redo_list);
+  b.redo_cnt = (int32_t*)(ws + p.off_redo_cnt);
+  b.redo_keys = (uint32_t*)(ws + p.off_redo_keys);
+  b.ld_redo = n;
   b.dev_err = dev_err;
   for (int r0 = 0; r0 < n; r0 += p.chunk) {
+    e = cudaMemsetAsync(b.redo_cnt, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e);
     b.row0 = r0;
     b.row1 = std::min(n, r0 + p.chunk);
     // the sampled sweep of the selection scan reads every 4th key (kPsSampleStride) only

@@ -146,8 +146,20 @@ struct PsArgs {
   uint32_t* cand_tau;   // [(row1-row0)][Hkv] threshold (diagnostic)
   int32_t* idx;         // [n][Hkv][k]
   int32_t* cnt;         // [n][Hkv]
+  // completion of the rows the candidates cannot prove: their (row - row0) * Hkv + g go to
+  // redo_list (redo_cnt zeroed before the scan), and each CTA of the completion pass keeps
+  // one row's exact keys in redo_keys + blockIdx.x * ld_redo
+  const void* q;        // [n][Hq][128] bf16 queries
+  const void* kpool;    // [num_pages][Hkv][64][128] bf16 keys
+  int32_t* redo_list;   // [(row1-row0)][Hkv]
+  int32_t* redo_cnt;    // [1]
+  uint32_t* redo_keys;  // [kPsCompleteCtas][ld_redo]
+  long long ld_redo;
   int32_t* dev_err;
 };
+
+// CTAs of the prefill selection's completion pass (each takes flagged rows in turn).
+constexpr int kPsCompleteCtas = 304;
 
 // Row-wise exact top-k over precomputed keys, starting from a global top-digit histogram.
 struct SelectArgs {

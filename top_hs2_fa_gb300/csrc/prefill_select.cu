@@ -24,9 +24,15 @@
 //   candidates (radix select with warp-level ballots and shuffles, ties to the lower
 //   position, ascending output). The candidates are a superset of the answer when (a) at
 //   least k of them are >= tau and (b) no dropped key exceeds the k-th largest kept key
-//   (dropped positions come after every kept one, so equal keys lose); otherwise the row is
-//   flagged (HS2_DEV_SELECT) and written as count -1.
+//   (dropped positions come after every kept one, so equal keys lose); otherwise the row
+//   goes to a list of rows to complete.
+// prefill_complete_kernel — each listed (row, KV head) again, exactly: its scores over the
+//   whole far range recomputed (mma.sync, keys as M, the heads of the KV head as N) into a
+//   per-CTA key row, then a block-wide radix top-k over all of them. Every row therefore
+//   gets its exact top-k, whatever the score distribution.
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -469,10 +475,10 @@ __global__ void __launch_bounds__(kTopkWarps * 32) prefill_topk_warp_kernel(cons
     // a larger dropped key would belong in the answer (equal ones come later and lose)
     fail = a.cand_drop[rs] > prefix;
   }
-  if (fail) {
+  if (fail) {  // completed exactly by prefill_complete_kernel
     if (lane == 0) {
       *cnt_out = -1;
-      flag_error(a.dev_err, HS2_DEV_SELECT);
+      a.redo_list[atomicAdd(a.redo_cnt, 1)] = rs;
     }
     for (int j = lane; j < a.k; j += 32) out[j] = -1;
     return;
@@ -495,6 +501,101 @@ __global__ void __launch_bounds__(kTopkWarps * 32) prefill_topk_warp_kernel(cons
   for (int j = kk + lane; j < a.k; j += 32) out[j] = -1;
 }
 
+// prefill_complete_kernel (see the top of the file). A CTA takes listed rows in turn; its
+// warps take 16-key chunks of the row's far range: lane (gid, tig) loads K rows gid and
+// gid + 8 of the chunk as four 16-byte pieces at d = 32j + 8 tig (mma_attn.cuh's layout,
+// the contraction index permuted identically for Q), S^T = K Q^T on mma.sync (8 heads per
+// N tile, NT tiles), and the four lanes of a key sum its heads' exp2(x scale_log2 - lse2).
+// Heads past G have zero queries and an infinite lse2, so they add nothing.
+constexpr int kCompleteThreads = 256;
+
+template <int NT>
+__global__ void __launch_bounds__(kCompleteThreads) prefill_complete_kernel(const PsArgs a) {
+  __shared__ TopkSmem<kCompleteThreads> tsm;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int nredo = *(volatile int32_t*)a.redo_cnt;
+  uint32_t* keys = a.redo_keys + (size_t)blockIdx.x * a.ld_redo;
+  const __nv_bfloat16* qb16 = reinterpret_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(a.kpool);
+  for (int f = blockIdx.x; f < nredo; f += gridDim.x) {
+    const int rs = a.redo_list[f];
+    const int i = a.row0 + rs / a.Hkv, g = rs % a.Hkv;
+    const int nF = max(0, i + 1 - a.w);
+    const int kk = min(a.k, nF);
+    uint32_t qf[8][NT][2];
+    float l2[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int hl = nt * 8 + gid;
+      const bool hv = hl < a.G;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qb16 + ((size_t)i * a.Hq + g * a.G + (hv ? hl : 0)) * 128);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int base = 32 * (s >> 1) + 8 * tig + 4 * (s & 1);
+        qf[s][nt][0] = hv ? __ldg(qrow + base / 2) : 0u;
+        qf[s][nt][1] = hv ? __ldg(qrow + base / 2 + 1) : 0u;
+      }
+#pragma unroll
+      for (int hs = 0; hs < 2; ++hs) {
+        const int h = nt * 8 + 2 * tig + hs;
+        l2[nt][hs] = h < a.G ? __ldg(a.lse2 + (size_t)i * a.Hq + g * a.G + h) : INFINITY;
+      }
+    }
+    const int nchunks = (nF + 15) / 16;
+    for (int c = warp; c < nchunks; c += kCompleteThreads / 32) {
+      const int s0 = 16 * c;
+      uint4 kr[2][4];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int s = s0 + gid + 8 * half;
+        int phys = -1;
+        if (s < nF) {
+          phys = a.bt[s / kPage];
+          if (phys < 0 || phys >= a.num_pages) {
+            flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
+            phys = -1;
+          }
+        }
+        const uint4* row = reinterpret_cast<const uint4*>(kp + (((size_t)(phys < 0 ? 0 : phys) * a.Hkv + g) * kPage +
+                                                                 s % kPage) * 128);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) kr[half][j] = phys >= 0 ? __ldg(row + 4 * j + tig) : make_uint4(0, 0, 0, 0);
+      }
+      float pA = 0.f, pB = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const int j = s >> 1, u = s & 1;
+          const uint32_t a0 = u ? kr[0][j].z : kr[0][j].x, a2 = u ? kr[0][j].w : kr[0][j].y;
+          const uint32_t a1 = u ? kr[1][j].z : kr[1][j].x, a3 = u ? kr[1][j].w : kr[1][j].y;
+          mma_bf16_16816(acc[u], a0, a1, a2, a3, qf[s][nt][0], qf[s][nt][1]);
+        }
+        pA += tc::ex2(fmaf(acc[0][0] + acc[1][0], a.scale_log2, -l2[nt][0])) +
+              tc::ex2(fmaf(acc[0][1] + acc[1][1], a.scale_log2, -l2[nt][1]));
+        pB += tc::ex2(fmaf(acc[0][2] + acc[1][2], a.scale_log2, -l2[nt][0])) +
+              tc::ex2(fmaf(acc[0][3] + acc[1][3], a.scale_log2, -l2[nt][1]));
+      }
+      pA += __shfl_xor_sync(0xffffffffu, pA, 1);
+      pA += __shfl_xor_sync(0xffffffffu, pA, 2);
+      pB += __shfl_xor_sync(0xffffffffu, pB, 1);
+      pB += __shfl_xor_sync(0xffffffffu, pB, 2);
+      if (tig == 0) {
+        if (s0 + gid < nF) keys[s0 + gid] = __float_as_uint(pA);
+        if (s0 + gid + 8 < nF) keys[s0 + gid + 8] = __float_as_uint(pB);
+      }
+    }
+    __syncthreads();  // the key row is complete (global writes visible to the block)
+    int32_t* out = a.idx + ((size_t)i * a.Hkv + g) * a.k;
+    block_topk<kCompleteThreads>(
+        nF, kk, [&](int s) { return __ldcg(keys + s); }, [&](int j, int s) { out[j] = s; }, tsm);
+    if (threadIdx.x == 0) a.cnt[(size_t)i * a.Hkv + g] = kk;
+    __syncthreads();  // the next listed row overwrites the key row
+  }
+}
+
 size_t prefill_scan_smem() { return sizeof(PsSmem) + 1024; }
 
 cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tks,
@@ -508,6 +609,13 @@ cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, 
   if (e != cudaSuccess) return e;
   const int rows = (a.row1 - a.row0) * a.Hkv;
   prefill_topk_warp_kernel<<<(rows + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int grid = std::min(rows, kPsCompleteCtas);
+  if (a.G <= 8) prefill_complete_kernel<1><<<grid, kCompleteThreads, 0, s>>>(a);
+  else if (a.G <= 16) prefill_complete_kernel<2><<<grid, kCompleteThreads, 0, s>>>(a);
+  else if (a.G <= 32) prefill_complete_kernel<4><<<grid, kCompleteThreads, 0, s>>>(a);
+  else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

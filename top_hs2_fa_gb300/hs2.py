@@ -190,9 +190,9 @@ def hs2_fa_select(q: torch.Tensor, kv: KV, w: int, k: int, scale: float, prefill
     ``sel_block`` > 1 selects whole blocks of that many far positions (``hs2_fa_select_ex``).
     ``k_new`` / ``v_new`` ([B][Hkv][d], decode): the current token's rows, appended to the
     cache at position t-1 by the same call (``hs2_fa_select_append``).
-    ``dev_err`` (int32 device tensor) collects the device-side error bits (``DEV_*``); a
-    prefill row whose streamed candidates cannot prove its top-k sets ``DEV_SELECT`` and
-    has ``idx_cnt`` -1."""
+    ``dev_err`` (int32 device tensor) collects the device-side error bits (``DEV_*``). Every
+    row gets its exact top-k: a prefill row whose streamed candidates cannot prove it is
+    recomputed over its whole far range in the same call."""
     lib = load()
     Bq, Hq, d = q.shape
     c = kv.c()
