@@ -530,8 +530,10 @@ static hs2_status fa_select_impl(const void* q, int B_or_n, int Hq, const hs2_kv
   c.hist = (uint32_t*)(ws + p.off_hist);
   c.ld_logits = p.ld;
   c.dev_err = dev_err;
-  e = cudaMemsetAsync(c.hist, 0, (size_t)B_or_n * kv->Hkv * 4096 * sizeof(uint32_t), s);
-  if (e != cudaSuccess) return cuda_fail(e);
+  if (!hs2::score_select_fused(c, B_or_n)) {  // the fused kernel keeps its histogram in shared memory
+    e = cudaMemsetAsync(c.hist, 0, (size_t)B_or_n * kv->Hkv * 4096 * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   e = hs2::launch_combine(c, B_or_n, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return HS2_OK;

@@ -19,6 +19,8 @@
 //                     (candidates) lists in shared memory; a radix select over the
 //                     candidates alone fixes the k-th key and the ties to take; the two
 //                     sorted lists are merged into the ascending output (topk.cuh).
+// score_select_kernel decode with at least 152 (query, KV head) pairs: both of the above
+//                     for one pair in one CTA (histogram in shared memory, no global one).
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -363,8 +365,140 @@ cudaError_t launch_prefill_trivial_select(int32_t* idx, int32_t* cnt, int n, int
   return cudaGetLastError();
 }
 
+// Decode, token-level selection, many (query, KV head) pairs: the split merge, the scoring
+// and the top-k of one (query, KV head) in one CTA (512 threads; every pair's CTA resident
+// at once). The CTA derives lse from the split partials, merges o, then streams the far
+// range's base-2 logits of its heads (four positions of up to eight heads per thread in
+// flight), writes the scores as keys into the L2-resident scratch row and bins their top 12
+// bits in shared memory, and selects from that histogram and the keys it has just written
+// (filter_topk; the radix passes over all keys when the candidates overflow). Against
+// merge_score_kernel + select_kernel this drops the global histogram (and its zeroing),
+// one launch and a re-read of the keys from a second kernel.
+constexpr int kFusedMinPairs = 152;  // below this, too few CTAs to stream the logits fast
+constexpr int kScoreHeads = 4;       // heads whose logit loads a thread has in flight (64 registers)
+
+bool score_select_fused(const CombineArgs& a, int Bq) {
+  return a.select && a.sel_block == 1 && !a.prefill && !a.gather && (long long)Bq * a.Hkv >= kFusedMinPairs &&
+         (a.D == 64 || a.D == 128);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kSelectThreads, 2) score_select_kernel(const CombineArgs a) {
+  constexpr int NT = kSelectThreads;
+  const int g = blockIdx.x, qi = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.G;
+  const QueryGeom qg = query_geom(qi, a.prefill, a.seq_len);
+  const int t = qg.t;
+  __shared__ TopkSmem<NT> sm;
+  __shared__ float lse2_s[32], M_s[32], Linv_s[32];
+  extern __shared__ int fbuf[];
+  float* o_out = a.o + ((size_t)qi * a.Hq + (size_t)g * G) * D;
+  int32_t* out = a.idx + ((size_t)qi * a.Hkv + g) * a.kcap;
+  if ((t < 1) || (t > a.max_t) || ((t + kPage - 1) / kPage > a.max_pages)) {
+    if (tid == 0) flag_error(a.dev_err, HS2_DEV_BAD_LENGTH);
+    for (int e = tid; e < G * D; e += NT) o_out[e] = 0.f;
+    for (int j = tid; j < a.kcap; j += NT) out[j] = -1;
+    if (tid == 0) a.cnt[(size_t)qi * a.Hkv + g] = 0;
+    return;
+  }
+  const int nF = max(0, t - a.w);
+  const int kk = min(a.k, nF);
+  const int nchunk = ((t + kPage - 1) / kPage + a.pps - 1) / a.pps;
+  // ---- per-head merge statistics (warp w handles heads w, w + 16, ...)
+  for (int h = warp; h < G; h += NT / 32) {
+    const float2* ml = a.part_ml + ((size_t)qi * a.Hq + (size_t)g * G + h) * a.nsplit;
+    float M = -INFINITY;
+    for (int c = lane; c < nchunk; c += 32) M = fmaxf(M, ml[c].x);
+    M = warp_max(M);
+    float L = 0.f;
+    for (int c = lane; c < nchunk; c += 32) L += exp2_rel(ml[c].x, M) * ml[c].y;
+    L = warp_sum(L);
+    if (lane == 0) {
+      M_s[h] = M;
+      Linv_s[h] = L > 0.f ? 1.f / L : 0.f;
+      lse2_s[h] = M + log2f(L);
+    }
+  }
+  for (int i = tid; i < kRadixBins; i += NT) sm.hist[i] = 0;
+  __syncthreads();
+  if (a.lse && tid < G) a.lse[(size_t)qi * a.Hq + (size_t)g * G + tid] = lse2_s[tid] / kLog2e;
+  // o = sum_c 2^(m_c - M) o_c / L; thread -> 4 consecutive outputs of one head
+  for (int e4 = tid; e4 < G * D / 4; e4 += NT) {
+    const int h = (4 * e4) / D, d0 = (4 * e4) % D;
+    const size_t ph = ((size_t)qi * a.Hq + (size_t)g * G + h) * a.nsplit;
+    const float M = M_s[h];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int c = 0; c < nchunk; ++c) {
+      const float wgt = exp2_rel(a.part_ml[ph + c].x, M);
+      const float4 v = *reinterpret_cast<const float4*>(a.part_o + (ph + c) * D + d0);
+      acc.x = fmaf(wgt, v.x, acc.x);
+      acc.y = fmaf(wgt, v.y, acc.y);
+      acc.z = fmaf(wgt, v.z, acc.z);
+      acc.w = fmaf(wgt, v.w, acc.w);
+    }
+    const float li = Linv_s[h];
+    *reinterpret_cast<float4*>(o_out + (size_t)h * D + d0) = make_float4(acc.x * li, acc.y * li, acc.z * li, acc.w * li);
+  }
+  for (int j = kk + tid; j < a.kcap; j += NT) out[j] = -1;
+  if (tid == 0) a.cnt[(size_t)qi * a.Hkv + g] = kk;
+  if (kk == 0) return;
+  if (kk == nF) {  // the budget covers the whole far range
+    for (int j = tid; j < nF; j += NT) out[j] = j;
+    return;
+  }
+  // ---- scores of the far range, 4 positions per thread and pass, kScoreHeads heads' loads in flight
+  const float* lg = a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits;
+  uint32_t* keys = a.scores + ((size_t)qi * a.Hkv + g) * a.ld_logits;
+  // the trip count is the same for every thread: the histogram update is warp-collective
+  for (int base = 0; base < nF; base += 4 * NT) {
+    const int s0 = base + 4 * tid;
+    const bool mine = s0 < nF;
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int h0 = 0; h0 < G; h0 += kScoreHeads) {
+      float4 x[kScoreHeads];
+#pragma unroll
+      for (int hh = 0; hh < kScoreHeads; ++hh)
+        if (mine && h0 + hh < G) x[hh] = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)(h0 + hh) * a.ld_logits + s0));
+#pragma unroll
+      for (int hh = 0; hh < kScoreHeads; ++hh)
+        if (mine && h0 + hh < G) {
+          const float l2 = lse2_s[h0 + hh];
+          sc[0] += exp2f(x[hh].x - l2);
+          sc[1] += exp2f(x[hh].y - l2);
+          sc[2] += exp2f(x[hh].z - l2);
+          sc[3] += exp2f(x[hh].w - l2);
+        }
+    }
+    uint32_t key[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) key[e] = (s0 + e < nF) ? __float_as_uint(sc[e]) : 0u;
+    if (mine) *reinterpret_cast<uint4*>(keys + s0) = make_uint4(key[0], key[1], key[2], key[3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) hist_add_warp(sm.hist, s0 + e < nF, key[e] >> 20);
+  }
+  __syncthreads();  // keys (global, read back through L2) and the histogram are complete
+  int* la = fbuf;
+  int* lsel = la + a.kcap;
+  uint2* lc = reinterpret_cast<uint2*>(lsel + a.kcap);
+  auto emit = [&](int j, int i) { out[j] = i; };
+  if (filter_topk<NT, 8>(keys, nF, kk, nullptr, la, a.kcap, lc, kFilterCap, lsel, emit, sm)) return;
+  // more candidates share the k-th key's top digit than the buffer holds: radix passes
+  auto key = [&](int i) { return __ldcg(keys + i); };
+  block_topk<NT>(nF, kk, key, emit, sm);
+}
+
 // ============================================================================ launchers
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s) {
+  if (score_select_fused(a, Bq)) {
+    const size_t sm = select_smem(a.kcap);
+    auto kern = a.D == 128 ? score_select_kernel<128> : score_select_kernel<64>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(a.Hkv, Bq), kSelectThreads, sm, s>>>(a);
+    return cudaGetLastError();
+  }
   const int nscore = a.select ? (int)((a.ld_logits + kScoreChunk - 1) / kScoreChunk) : 1;
   dim3 grid(nscore, a.Hkv, Bq);
   if (a.D == 128) merge_score_kernel<128><<<grid, kMergeThreads, 0, s>>>(a);

@@ -182,6 +182,9 @@ cudaError_t launch_fa_decode_mma(const AttnArgs& a, int Bq, cudaStream_t s);
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_attn_partial(const AttnArgs& a, int Bq, int bf16, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s);
+// Whether launch_combine runs the fused merge + score + top-k kernel (which needs no
+// zeroed global histogram) for these arguments.
+bool score_select_fused(const CombineArgs& a, int Bq);
 bool sa_mma_supported(int G, int D, int bf16, int w, int k);
 // Decode: plan the warp stream on the current device (false if it does not apply);
 // a.part_ml / a.part_o hold [units][maxc][8] partials and a.arrive [units] zeroed counters.

@@ -206,12 +206,14 @@ HS2_DEVI int count_below(const int* a, int n, int x) {
 // (kk ints) in index order, and A and it are merged: emit(j, i) writes output slot j (ascending
 // index order) <- key index i. Returns false, having emitted nothing, when C or A exceed their
 // buffers (the caller then runs block_topk-style passes over all keys). All NT threads call.
+// ghist = null: the histogram is already in sm.hist (filled by the calling CTA).
 template <int NT, int V, typename EmitFn>
 __device__ bool filter_topk(const uint32_t* gkeys, int n, int kk, const uint32_t* ghist, int* la, int cap_a,
                             uint2* lc, int cap_c, int* lsel, EmitFn emit, TopkSmem<NT>& sm) {
   static_assert(V % 4 == 0 && NT * V < 65536, "chunk counts are packed in 16 bits");
   const int tid = threadIdx.x;
-  for (int i = tid; i < kRadixBins; i += NT) sm.hist[i] = __ldcg(ghist + i);
+  if (ghist)
+    for (int i = tid; i < kRadixBins; i += NT) sm.hist[i] = __ldcg(ghist + i);
   __syncthreads();
   int remaining = kk;
   const uint32_t d = find_digit<NT>(sm.hist, kRadixBins, remaining, sm);
