@@ -97,6 +97,14 @@ HS2_DEVI float warp_sum(float v) {
 // much (base 2), i.e. they are at most 2^8: well inside bf16, f16 and fp32 range.
 constexpr float kLazyRescale = 8.f;
 
+// 2^x by the hardware approximation (relative error about 2^-22; results below 2^-126
+// flush to zero, -inf gives 0): the softmax weights, which are rounded to 16 bits anyway.
+HS2_DEVI float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // exp2 of a (possibly -inf) base-2 logit relative to a (possibly -inf) max:
 // a row whose max is still -inf contributes exactly zero.
 HS2_DEVI float exp2_rel(float x, float m) { return (m == -INFINITY) ? 0.f : exp2f(x - m); }

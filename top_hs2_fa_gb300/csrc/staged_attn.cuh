@@ -105,6 +105,18 @@ struct StagedAttn {
 #pragma unroll
         for (int i = 0; i < 4; ++i) sc[nt][i] = s2[0][nt][i] + s2[1][nt][i];
     }
+    // V^T fragments by transposed loads, issued before the softmax so their latency overlaps
+    // it: a0 = (entries 0-7, d +0), a1 = (0-7, d +8), a2 = (8-15, d +0), a3 = (8-15, d +8)
+    uint32_t va[KS][4];
+    {
+      const int row = rr + 8 * (mi >> 1), dsub = 8 * (mi & 1);
+      const uint32_t vbase = slot + HALVES * 2048;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int d0 = 16 * mt + dsub;
+        ldsm_x4_t(vbase + (d0 >> 6) * 2048 + sw128(row, (d0 & 63) >> 3), va[mt]);
+      }
+    }
     if (F16) {
       // a step whose largest |V scale| (vsA / vsB depend on gid only) exceeds the unit makes
       // that scale the unit, acc rescaled to it
@@ -132,20 +144,24 @@ struct StagedAttn {
       x[1] = okA ? sc[nt][1] * (scale_log2 * ksA) : -INFINITY;
       x[2] = okB ? sc[nt][2] * (scale_log2 * ksB) : -INFINITY;
       x[3] = okB ? sc[nt][3] * (scale_log2 * ksB) : -INFINITY;
-      float p[4], cm[2];
-      bool grow = false;
-#pragma unroll
-      for (int hs = 0; hs < 2; ++hs) {
-        cm[hs] = fmaxf(x[hs], x[hs + 2]);
-        cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 4));
-        cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 8));
-        cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 16));
-        grow |= cm[hs] > m[nt][hs] + kLazyRescale;
-      }
-      // lazy rescale: the running max moves (l and acc rescaled) only when a head's step max
-      // exceeds it by more than kLazyRescale, so weights stay <= 2^8; the final normalisation
-      // uses the same max
+      float p[4];
+      // lazy rescale: the running max moves (l and acc rescaled) only when a logit exceeds it
+      // by more than kLazyRescale, so weights stay <= 2^8; the final normalisation uses the
+      // same max. Each lane checks its own logits; the column maxima are reduced across the
+      // warp only when some lane needs a move (after the first step, rarely). The first
+      // step with a valid entry moves every head's max off -inf (every head then has a finite
+      // logit), so x - m below is never -inf - (-inf).
+      const bool grow = x[0] > m[nt][0] + kLazyRescale || x[2] > m[nt][0] + kLazyRescale ||
+                        x[1] > m[nt][1] + kLazyRescale || x[3] > m[nt][1] + kLazyRescale;
       if (__any_sync(0xffffffffu, grow)) {
+        float cm[2];
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          cm[hs] = fmaxf(x[hs], x[hs + 2]);
+          cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 4));
+          cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 8));
+          cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 16));
+        }
 #pragma unroll
         for (int hs = 0; hs < 2; ++hs) {
           const float mn = fmaxf(m[nt][hs], cm[hs]);
@@ -161,8 +177,8 @@ struct StagedAttn {
       }
 #pragma unroll
       for (int hs = 0; hs < 2; ++hs) {
-        p[hs] = exp2_rel(x[hs], m[nt][hs]);
-        p[hs + 2] = exp2_rel(x[hs + 2], m[nt][hs]);
+        p[hs] = ex2_approx(x[hs] - m[nt][hs]);
+        p[hs + 2] = ex2_approx(x[hs + 2] - m[nt][hs]);
       }
       uint32_t pA, pB;  // entry gid / gid+8, heads 2tig, 2tig+1
       if (F16) {
@@ -180,20 +196,10 @@ struct StagedAttn {
       pb[nt][0] = movmatrix_trans(pA);
       pb[nt][1] = movmatrix_trans(pB);
     }
-    {
-      // V^T fragments by transposed loads: a0 = (entries 0-7, d +0), a1 = (0-7, d +8),
-      // a2 = (8-15, d +0), a3 = (8-15, d +8)
-      const int row = rr + 8 * (mi >> 1), dsub = 8 * (mi & 1);
-      const uint32_t vbase = slot + HALVES * 2048;
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        const int d0 = 16 * mt + dsub;
-        uint32_t a[4];
-        ldsm_x4_t(vbase + (d0 >> 6) * 2048 + sw128(row, (d0 & 63) >> 3), a);
+    for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma(acc[mt][nt], a[0], a[1], a[2], a[3], pb[nt][0], pb[nt][1]);
-      }
-    }
+      for (int nt = 0; nt < NT; ++nt) mma(acc[mt][nt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pb[nt][0], pb[nt][1]);
   }
 
   // Write this warp's (m, l, unnormalised o): sm_m / sm_l [warp][NT*8], sm_o [warp][NT*8][D].
