@@ -192,6 +192,9 @@ hs2_status hs2_fa_select_append(const void* q, int B, int Hq, const hs2_kv* kv, 
  *   hs2_fa_select_workspace(...) of the call exceeds the capacity.
  * - The first call on a device looks up the array's device address on that device
  *   (it must be the current device); make that first call before any stream capture.
+ *   The address is looked up again when the device's current context has changed since
+ *   (after a cudaDeviceReset, say); make the first call after such a change before any
+ *   stream capture too.
  * - All calls share the one array: calls that overlap on the GPU (concurrent streams
  *   or host threads) race and corrupt each other's results; serialise them.
  * - It allocates nothing and calls no cudaMalloc / cudaFree.                        */
