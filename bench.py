@@ -280,7 +280,12 @@ class Decode:
         self.alg_per_launch = fa[0]  # the profiled launch is group 0's FA scan
         self.alg_total = total
         self.units_per_step = self.B
-        self.launches_per_step = self.groups * (3 + NSA) + (1 if self.append == "batched" else 0)
+        # kernels per step, as the library reports them for these calls
+        d0 = self.dev[0]
+        per_group = (hs2.hs2_fa_select_launches(self.B, self.Hq, d0["kv"], d0["max_t"], self.w, self.k,
+                                                sel_block=self.sel_block, append=self.append == "fused") +
+                     NSA * hs2.hs2_sa_reuse_launches(self.B, self.Hq, d0["kv"], self.w, self.k))
+        self.launches_per_step = self.groups * per_group + (1 if self.append == "batched" else 0)
 
     def step(self, stream, err, qs=None, profile=None, io=NO_IO):
         hs2 = self.hs2
@@ -407,7 +412,8 @@ class Prefill:
         self.alg_per_launch = f["fa"]
         self.alg_total = f["fa"] + NSA * f["sa_per_layer"]
         self.units_per_step = n
-        self.launches_per_step = 3 + NSA
+        self.launches_per_step = (hs2.hs2_fa_select_launches(n, self.Hq, d["kv"], n, self.w, self.k, prefill=True) +
+                                  NSA * hs2.hs2_sa_reuse_launches(n, self.Hq, d["kv"], self.w, self.k, prefill=True))
 
     def step(self, stream, err, qs=None, profile=None, io=NO_IO):
         hs2, d, g = self.hs2, self.dev[0], self.host[0]
@@ -500,7 +506,8 @@ class Csa2:
         self.alg_per_launch = m["full"]
         self.alg_total = m["total"]
         self.units_per_step = B
-        self.launches_per_step = 3 + 2 + 5 * 2
+        # Full: indexer scan + position and block selections; Reindex: scan + selection; 5 SA calls
+        self.launches_per_step = 3 + 2 + 5 * hs2.hs2_sa_reuse_launches(B, self.Hq, d["kv"], 0, self.k_top)
 
     def step(self, stream, err, qs=None, profile=None, io=NO_IO):
         hs2, d, g = self.hs2, self.dev[0], self.host[0]

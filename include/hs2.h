@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define HS2_ABI_VERSION 4
+#define HS2_ABI_VERSION 5
 
 typedef enum {
   HS2_OK = 0,
@@ -269,6 +269,14 @@ void hs2_profile_next(hs2_stage stage, void* start, void* stop);
  * arrives on; the wait gives up, HS2_DEV_TIMEOUT is set in *dev_err (device memory) and the
  * kernel finishes. Lets a caller check the device-side timeout path without a fault. */
 hs2_status hs2_selftest_wait_timeout(int timeout_us, int32_t* dev_err, void* stream);
+/* hs2_fa_select_launches / hs2_sa_reuse_launches: how many kernels hs2_fa_select_ex (with
+ * append != 0: hs2_fa_select_append) and hs2_sa_reuse_ex launch for these arguments (device
+ * memsets not counted), or -1 for arguments they reject on the host. Lets a caller account
+ * for the library's launches inside a step; launches nothing (it may query the current
+ * device's properties, as the calls themselves do to plan their grids). */
+int hs2_fa_select_launches(int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w, int k, int prefill,
+                           int sel_block, int append);
+int hs2_sa_reuse_launches(int B_or_n, int Hq, const hs2_kv* kv, int w, int k, int prefill);
 const char* hs2_strerror(hs2_status st);
 int hs2_last_cuda_error(void); /* cudaError_t of the last HS2_ERR_CUDA, 0 if none */
 int hs2_abi_version(void);

@@ -48,7 +48,7 @@ def test_binding_constants_match_the_header():
 
 
 def test_version_and_strings(lib):
-    assert lib.hs2_abi_version() == H.ABI_VERSION == 4
+    assert lib.hs2_abi_version() == H.ABI_VERSION == 5
     for st, word in [(0, "ok"), (-1, "invalid"), (-2, "unsupported"), (-3, "CUDA"), (-4, "device")]:
         assert word in lib.hs2_strerror(st).decode()
 

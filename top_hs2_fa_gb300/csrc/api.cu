@@ -375,6 +375,40 @@ static hs2_status fa_select_prefill_tc(const void* q, int n, int Hq, const hs2_k
   return HS2_OK;
 }
 
+int hs2_fa_select_launches(int B_or_n, int Hq, const hs2_kv* kv, int max_t, int w, int k, int prefill, int sel_block,
+                           int append) {
+  if (!kv || !valid_kv(kv, true) || Hq < 1 || Hq % kv->Hkv != 0 || !pow2_le32(Hq / kv->Hkv) || B_or_n < 0 || w < 0 ||
+      k < 0 || max_t < 1 || sel_block < 1 || (append && prefill))
+    return -1;
+  if (B_or_n == 0) return 0;
+  if (use_prefill_tc(kv, prefill)) {
+    if (!(k > 0 && B_or_n - w > k)) return 2;  // forward + the all-of-F select
+    const int chunks = cdiv(B_or_n, prefill_plan(B_or_n, Hq, kv, k).chunk);
+    return 1 + 3 * chunks;  // forward; per chunk: candidate scan, top-k, completion
+  }
+  const FaPlan p = fa_plan(B_or_n, Hq, kv, max_t);
+  int n = 1;  // the scan (tensor-core or CUDA-core)
+  if (append && !(p.mma && kv->dtype == HS2_BF16)) n += 1;  // a separate append kernel
+  hs2::CombineArgs c{};
+  c.select = 1;
+  c.sel_block = sel_block;
+  c.prefill = prefill ? 1 : 0;
+  c.gather = 0;
+  c.Hkv = kv->Hkv;
+  c.D = kv->d;
+  return n + (hs2::score_select_fused(c, B_or_n) ? 1 : 2);  // fused, else merge + select
+}
+
+int hs2_sa_reuse_launches(int B_or_n, int Hq, const hs2_kv* kv, int w, int k, int prefill) {
+  if (!kv || !valid_kv(kv, true) || Hq < 1 || Hq % kv->Hkv != 0 || !pow2_le32(Hq / kv->Hkv) || B_or_n < 0 || w < 0 ||
+      k < 0)
+    return -1;
+  if (B_or_n == 0) return 0;
+  const SaPlan p = sa_plan(B_or_n, Hq, kv, w, k, prefill);
+  if (p.stream || hs2::sa_mma_supported(Hq / kv->Hkv, kv->d, kv->dtype == HS2_BF16, w, k)) return 1;
+  return 2;  // partial attention + merge
+}
+
 hs2_status hs2_selftest_wait_timeout(int timeout_us, int32_t* dev_err, void* stream) {
   if (timeout_us < 1 || timeout_us > 2000000 || !dev_err) return HS2_ERR_ARG;
   cudaError_t e = hs2::launch_wait_selftest(dev_err, 1000ull * (unsigned long long)timeout_us, (cudaStream_t)stream);

@@ -16,7 +16,7 @@ import torch
 
 from . import build as _build
 
-ABI_VERSION = 4  # include/hs2.h HS2_ABI_VERSION this binding marshals for
+ABI_VERSION = 5  # include/hs2.h HS2_ABI_VERSION this binding marshals for
 F32, BF16, FP8_E4M3, FP4_E2M1 = 0, 1, 2, 3
 FULL, REINDEX = 0, 1
 DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH, DEV_SELECT = 1, 2, 4, 8, 16
@@ -24,7 +24,7 @@ EXPORTS = (
     "hs2_fa_select_workspace", "hs2_fa_select", "hs2_fa_select_ex", "hs2_sa_reuse_workspace", "hs2_sa_reuse", "hs2_sa_reuse_ex",
     "hs2_hier_reindex_workspace", "hs2_hier_reindex", "hs2_strerror", "hs2_last_cuda_error",
     "hs2_abi_version", "hs2_profile_next", "hs2_selftest_wait_timeout", "hs2_fa_select_noalloc", "hs2_fa_select_noalloc_capacity",
-    "hs2_kv_append", "hs2_fa_select_append",
+    "hs2_kv_append", "hs2_fa_select_append", "hs2_fa_select_launches", "hs2_sa_reuse_launches",
 )
 STAGE_FA_SCAN, STAGE_SA_GATHER, STAGE_INDEXER = 0, 1, 2
 
@@ -91,6 +91,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.hs2_fa_select_append.restype = i32
     lib.hs2_fa_select_noalloc_capacity.argtypes = []
     lib.hs2_fa_select_noalloc_capacity.restype = sz
+    lib.hs2_fa_select_launches.argtypes = [i32, i32, kvp, i32, i32, i32, i32, i32, i32]
+    lib.hs2_fa_select_launches.restype = i32
+    lib.hs2_sa_reuse_launches.argtypes = [i32, i32, kvp, i32, i32, i32]
+    lib.hs2_sa_reuse_launches.restype = i32
     if lib.hs2_abi_version() != ABI_VERSION:
         raise HS2Error(f"libhs2 ABI {lib.hs2_abi_version()} != binding ABI {ABI_VERSION}: rebuild the library")
     _lib = lib
@@ -162,6 +166,20 @@ def _workspace(nbytes: int, device, ws):
 def hs2_fa_select_workspace(B_or_n: int, Hq: int, kv: KV, max_t: int, k: int, prefill: bool = False) -> int:
     c = kv.c()
     return int(load().hs2_fa_select_workspace(B_or_n, Hq, ctypes.byref(c), max_t, k, int(prefill)))
+
+
+def hs2_fa_select_launches(B_or_n: int, Hq: int, kv: KV, max_t: int, w: int, k: int, prefill: bool = False,
+                           sel_block: int = 1, append: bool = False) -> int:
+    """Kernels one hs2_fa_select call with these arguments launches (-1: rejected)."""
+    c = kv.c()
+    return int(load().hs2_fa_select_launches(B_or_n, Hq, ctypes.byref(c), max_t, w, k, int(prefill), sel_block,
+                                              int(append)))
+
+
+def hs2_sa_reuse_launches(B_or_n: int, Hq: int, kv: KV, w: int, k: int, prefill: bool = False) -> int:
+    """Kernels one hs2_sa_reuse call with these arguments launches (-1: rejected)."""
+    c = kv.c()
+    return int(load().hs2_sa_reuse_launches(B_or_n, Hq, ctypes.byref(c), w, k, int(prefill)))
 
 
 def hs2_kv_append(kvs, k_new, v_new=None, dev_err=None, stream=None) -> None:
