@@ -163,6 +163,36 @@ def test_decode_bf16_full_size_sampled(H):
             assert set(grp.needles[b].tolist()) <= set(s.tolist())
 
 
+def fused_lengths(B, seed):
+    """B ragged lengths around the window and budget edges (w = 16, k = 64) and a few long
+    ones, so every branch of the fused selection runs: t < w, t - w <= k, t - w = k + 1, and
+    thousands of far keys."""
+    edge = [1, 15, 16, 17, 63, 64, 80, 81, 100, 129, 1000, 3001, 4097, 7000]
+    rng = np.random.default_rng(seed)
+    return [edge[i] if i < len(edge) else int(rng.integers(200, 6000)) for i in range(B)]
+
+
+def test_decode_fused_selection_ragged(H):
+    """The fused merge + score + top-k kernel (taken when a call has at least 152 (query, KV
+    head) pairs: here 40 sequences x 4 KV heads) on ragged lengths at the window and budget
+    edges, every sequence against the oracle."""
+    lens = fused_lengths(40, 52)
+    grp = W.decode_group(lens, Hq=32, Hkv=4, d=128, w=16, k=64, dtype="bf16", seed=53, n_sa=1, needles=4)
+    check_group(H, grp)
+
+
+@pytest.mark.parametrize("n_tied", [3000, 9000])
+def test_decode_fused_selection_ties(H, n_tied):
+    """The fused kernel on rows whose far scores are all equal (identical keys): each takes its
+    first k positions; 3000 tied keys fit the candidate list, 9000 overflow it and take the
+    radix passes over all keys. 38 sequences x 4 KV heads = 152 pairs."""
+    lens = [n_tied] * 38
+    grp = W.decode_group(lens, Hq=16, Hkv=4, d=128, w=32, k=100, dtype="bf16", seed=54, n_sa=1, needles=0)
+    grp.kv.k[:] = grp.kv.k[0:1, :, 0:1, :]
+    o, idx, cnt = check_group(H, grp, batches=[0, 17, 37])
+    assert (cnt == 100).all() and (idx == np.arange(100)).all()
+
+
 @pytest.mark.parametrize("lens,Hkv", [([60000, 33000, 20000], 2), ([17000, 12000], 1)])
 def test_decode_cluster_selection_long_rows(H, lens, Hkv):
     """Few long rows: the window-excluding top-k of each (query, KV head) is shared by a
