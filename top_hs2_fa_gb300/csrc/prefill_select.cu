@@ -12,7 +12,7 @@
 //            scores of its quarter of the row's columns into the row's 256-bin log histogram
 //            (1/8 octave per bin, 16-bit counts in shared memory, atomic adds), then the row's
 //            first thread picks a threshold tau whose estimated count of keys at or above it
-//            is twice the budget;
+//            is 1.25 times the budget;
 //   sweep 1 (exact): every key tile; the scoring threads stage the tile's 128 x 128 scores in
 //            shared memory, then each scoring warp takes 8 rows and appends (key, position)
 //            of the scores >= tau of a row, in ascending position, into the row's candidate
@@ -302,10 +302,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
             if (ranked) {
               // threshold: the estimated count at or above it (sample count scaled by the row's
               // sampling rate; the sweep saw every position of [0, nF) that is a multiple of the
-              // stride) reaches twice the budget
+              // stride) reaches 1.25 times the budget. Fewer candidates mean fewer stores here
+              // and a shorter top-k; a row the estimate leaves short of k is completed exactly
+              // (prefill_complete_kernel). On the AR(1) workload 1.25 completes no row (1.1: 221
+              // rows, slower overall; 2: 0.74 ms slower at n = 32768).
               const int n_samp = (nF + kSampleStride - 1) / kSampleStride;
               const float scale = (float)nF / (float)n_samp;
-              const float target = 2.f * (float)a.k;
+              const float target = 1.25f * (float)a.k;
               float cum = 0.f;
               tau = 0u;
               for (int b = kBins - 1; b >= 0; --b) {
