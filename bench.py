@@ -506,8 +506,9 @@ class Csa2:
         self.alg_per_launch = m["full"]
         self.alg_total = m["total"]
         self.units_per_step = B
-        # Full: indexer scan + position and block selections; Reindex: scan + selection; 5 SA calls
-        self.launches_per_step = 3 + 2 + 5 * hs2.hs2_sa_reuse_launches(B, self.Hq, d["kv"], 0, self.k_top)
+        # Full: indexer scan + one launch for the position and block selections; Reindex: scan +
+        # selection; 5 SA calls
+        self.launches_per_step = 2 + 2 + 5 * hs2.hs2_sa_reuse_launches(B, self.Hq, d["kv"], 0, self.k_top)
 
     def step(self, stream, err, qs=None, profile=None, io=NO_IO):
         hs2, d, g = self.hs2, self.dev[0], self.host[0]

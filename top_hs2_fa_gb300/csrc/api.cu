@@ -771,9 +771,10 @@ hs2_status hs2_hier_reindex(hs2_idx_mode mode, const void* q_idx, const float* w
   sa.hist = a.hist;
   sa.out = idx;
   sa.cnt = idx_cnt;
-  e = hs2::launch_select_rows(sa, B, s);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (mode == HS2_FULL) {
+  hs2::SelectJobs jobs{};
+  jobs.job[0] = sa;
+  jobs.n = 1;
+  if (mode == HS2_FULL) {  // the pool's block selection runs in the same launch
     sa.mode = 2;
     sa.k = max_blocks;
     sa.kcap = max_blocks;
@@ -782,9 +783,11 @@ hs2_status hs2_hier_reindex(hs2_idx_mode mode, const void* q_idx, const float* w
     sa.hist = a.bhist;
     sa.out = pool_blocks;
     sa.cnt = pool_cnt;
-    e = hs2::launch_select_rows(sa, B, s);
-    if (e != cudaSuccess) return cuda_fail(e);
+    jobs.job[1] = sa;
+    jobs.n = 2;
   }
+  e = hs2::launch_select_rows(jobs, B, s);
+  if (e != cudaSuccess) return cuda_fail(e);
   return HS2_OK;
 }
 

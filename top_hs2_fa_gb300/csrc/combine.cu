@@ -287,9 +287,11 @@ __global__ void __launch_bounds__(kSelectThreads) block_select_kernel(const Comb
 }
 
 // ============================================================================ generic row top-k
-// grid: clusters of CTAs along x (sel_cluster_size), one cluster per sequence
-__global__ void __launch_bounds__(kSelectThreads, 2) select_rows_kernel(const SelectArgs a) {
+// grid: clusters of CTAs along x (sel_cluster_size), one cluster per sequence; y = the job
+// (the Full layer's position and block selections run as two jobs of one launch)
+__global__ void __launch_bounds__(kSelectThreads, 2) select_rows_kernel(const SelectJobs jobs) {
   constexpr int NT = kSelectThreads;
+  const SelectArgs& a = jobs.job[blockIdx.y];
   const ClusterSel cl;
   const int b = blockIdx.x / cl.n;
   const int tid = threadIdx.x;
@@ -340,12 +342,18 @@ __global__ void __launch_bounds__(kSelectThreads, 2) select_rows_kernel(const Se
   block_topk<NT>(n, kk, key, emit, sm);
 }
 
-cudaError_t launch_select_rows(const SelectArgs& a, int B, cudaStream_t s) {
-  const size_t sm = select_smem(a.kcap);
+cudaError_t launch_select_rows(const SelectJobs& jobs, int B, cudaStream_t s) {
+  if (jobs.n < 1 || jobs.n > kMaxSelectJobs) return cudaErrorInvalidValue;
+  size_t sm = 0;
+  long long n_max = 0;  // the longest row of any job sets the cluster size of all
+  for (int j = 0; j < jobs.n; ++j) {
+    const SelectArgs& a = jobs.job[j];
+    sm = std::max(sm, select_smem(a.kcap));
+    n_max = std::max(n_max, a.mode == 1 ? (long long)a.max_t : a.mode == 2 ? (a.max_t + 7) / 8 : 8LL * a.max_blocks);
+  }
   cudaError_t e = cudaFuncSetAttribute(select_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  const long long n_max = a.mode == 1 ? a.max_t : a.mode == 2 ? (a.max_t + 7) / 8 : 8LL * a.max_blocks;
-  return launch_clustered(select_rows_kernel, B, 1, sm, sel_cluster_size(n_max, B), s, a);
+  return launch_clustered(select_rows_kernel, B, jobs.n, sm, sel_cluster_size(n_max, (long long)B * jobs.n), s, jobs);
 }
 
 // Prefill rows i whose far range F(i+1) = [0, i+1-w) fits the budget take all of it.

@@ -194,7 +194,13 @@ cudaError_t launch_sa_mma(const AttnArgs& a, int Bq, cudaStream_t s);
 size_t lightning_scan_smem();
 cudaError_t launch_lightning_scan(const CUtensorMap& tm_k, const CUtensorMap& tm_q, const IdxArgs& a, int B,
                                   int grid_x, cudaStream_t s);
-cudaError_t launch_select_rows(const SelectArgs& a, int B, cudaStream_t s);
+// Independent selections over the same batch in one launch (grid y = job).
+constexpr int kMaxSelectJobs = 2;
+struct SelectJobs {
+  SelectArgs job[kMaxSelectJobs];
+  int n;
+};
+cudaError_t launch_select_rows(const SelectJobs& jobs, int B, cudaStream_t s);
 cudaError_t launch_prefill_trivial_select(int32_t* idx, int32_t* cnt, int n, int Hkv, int w, int k, cudaStream_t s);
 size_t fa_prefill_fwd_smem();
 size_t prefill_scan_smem();
