@@ -10,17 +10,21 @@
 //               table) into 2-slot rings, 128-byte swizzle; a K slot frees when its QK is
 //               done, a V slot when its PV is done.
 //   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers (M=128, N=128,
-//               K=128), then O += P_j V_j (A = P from shared memory, B = V MN-major);
+//               K=128), then O += P_j V_j (A = P from tensor memory, B = V MN-major);
 //               S_{j+1} is issued before waiting for P_j so the tensor core stays busy.
 //   warps 2-9   softmax, two threads per query row (warps w and w+4 share a TMEM lane
 //               quadrant, each takes 64 of the tile's 128 columns; the halves swap their
 //               row maxima through shared memory): row max, exp2 (base-2 logits), P in
-//               bf16 to one of two shared-memory buffers (the normaliser sums the same
-//               rounded values), and a lazy O rescale: the reference max only moves when
-//               the row max grows by more than 2^8, which keeps every weight below 256 and
-//               needs no approximation; only a rescale waits for the previous PV.
+//               bf16 written back over the tile's own S buffer (the normaliser sums the
+//               same rounded values), and a lazy O rescale: the reference max only moves
+//               when the row max grows by more than 2^8, which keeps every weight below
+//               256 and needs no approximation; only a rescale waits for the previous PV.
 //   warp 10     TMA producer of the V tiles.
-// TMEM: S0 columns [0,128), S1 [128,256), O [256,384). Every mbarrier wait is bounded.
+// TMEM: S0 columns [0,128), S1 [128,256), O [256,384); P_j occupies the first 64 columns
+// of S_j's buffer (two bf16 per column), so it never passes through shared memory. A
+// buffer is rewritten by S_{j+2} only after PV_j has read P_j: one thread issues both in
+// that order and the tensor pipe executes one thread's MMAs in order. Every mbarrier wait
+// is bounded.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -42,10 +46,9 @@ struct PfSmem {
   uint8_t q[kTileBytes];      // A of S: K-blocks (d 0-63, d 64-127) x [128 rows x 128 B]
   uint8_t k[2][kTileBytes];   // B of S: same layout, rows = keys
   uint8_t v[2][kTileBytes];   // B of PV (MN-major): d-halves x [128 keys x 128 B]
-  uint8_t p[2][kTileBytes];   // A of PV, double-buffered: K-blocks (keys 0-63, 64-127) x [128 rows x 128 B]
   float xch[2][kPT];           // [half] a tile's row maxima of the two column halves (then
                                // the row normaliser's halves, at the end)
-  uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2];
+  uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], p_empty[2];
   uint64_t x_full[4], x_empty[4];  // per lane quadrant: both halves wrote / read xch
   uint32_t tmem_base;
   int abort;
@@ -84,9 +87,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tc::mbar_init(&sm.v_full[s], 1);
       tc::mbar_init(&sm.v_empty[s], 1);  // PV of the slot's tile done
       tc::mbar_init(&sm.s_full[s], 1);
-      tc::mbar_init(&sm.s_empty[s], 256);
-      tc::mbar_init(&sm.p_full[s], 256);
-      tc::mbar_init(&sm.p_empty[s], 1);  // PV of the buffer's tile done (and every MMA before it)
+      tc::mbar_init(&sm.p_full[s], 256);  // every softmax thread wrote its part of P into TMEM
+      tc::mbar_init(&sm.p_empty[s], 1);   // PV of the buffer's tile done (and every MMA before it)
     }
     for (int q = 0; q < 4; ++q) {
       tc::mbar_init(&sm.x_full[q], 64);
@@ -153,10 +155,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
       constexpr uint32_t idO = tc::idesc_bf16_f32_bmn(kPT, 128);
       const uint32_t qb = tc::smem_u32(sm.q);
       int pv_issued = 0;
+      // S_j's buffer held P_{j-2}, read by PV_{j-2}, which this thread issued before S_j
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!tc::mbar_wait(&sm.k_full[st], (j >> 1) & 1) || !tc::mbar_wait(&sm.s_empty[st], ((j >> 1) & 1) ^ 1))
-          return false;
+        if (!tc::mbar_wait(&sm.k_full[st], (j >> 1) & 1)) return false;
         tc::tc_fence_after();
         const uint32_t kb = tc::smem_u32(sm.k[st]);
 #pragma unroll
@@ -177,12 +179,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
           break;
         }
         tc::tc_fence_after();
-        const uint32_t vb = tc::smem_u32(sm.v[st]), pb = tc::smem_u32(sm.p[st]);
+        const uint32_t vb = tc::smem_u32(sm.v[st]);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t ad = tc::sdesc_sw128(pb + (ks >> 2) * 16384u + (ks & 3) * 32u);
+        for (int ks = 0; ks < 8; ++ks) {  // keys 16 ks .. 16 ks + 15 of P_j: columns 8 ks .. 8 ks + 7
           const uint64_t bd = tc::sdesc_sw128_mn(vb + ks * 2048u, 16384u, 1024u);
-          tc::mma_bf16(tO, ad, bd, idO, (j > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_bf16_ts(tO, tS + st * 128 + ks * 8, bd, idO, (j > 0 || ks > 0) ? 1u : 0u);
         }
         tc::mma_commit(&sm.v_empty[st]);
         tc::mma_commit(&sm.p_empty[st]);
@@ -228,8 +229,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[c][e] = __uint_as_float(raw[c][e]);
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(&sm.s_empty[sb]);
       // raw logits: only the diagonal tile crosses the causal boundary; the scale (> 0) is
       // applied to the max and folded into the exponent's FMA below
       if (j == J - 1) {
@@ -256,11 +255,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const bool need = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new > -INFINITY);
       const float alpha = (need && m_used > -INFINITY) ? tc::ex2(m_used - m_new) : 1.f;
       if (need) m_used = m_new;
-      // P buffer j&1 is free once PV_{j-2} is done
-      if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(&sm.p_empty[j & 1], ((j >> 1) - 1) & 1))) {
-        ok = false;
-        break;
-      }
       if (j > 0) {
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           // O holds every earlier tile once PV_{j-1} is done
@@ -280,28 +274,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         l *= alpha;
       }
-      // P row (bf16) into shared memory, 128-byte swizzled K-major layout. p = 2^(x*s - m):
-      // one FMA and ex2 (which maps -inf to +0); the normaliser adds the same bf16-rounded
-      // weights through a mixed-precision FMA against bf16 1.0 (exact: no unpacking).
-      uint8_t* prow = sm.p[j & 1] + (r >> 3) * 1024 + (r & 7) * 128;
+      // P row (bf16) back into tensor memory over S_j: this half's keys 64 half + 2c, +1 go to
+      // column 32 half + c of the buffer (the other half read its S columns before the max
+      // exchange above). p = 2^(x*s - m): one FMA and ex2 (which maps -inf to +0); the
+      // normaliser adds the same bf16-rounded weights through a mixed-precision FMA against
+      // bf16 1.0 (exact: no unpacking).
       const float neg_m = -m_used;
       constexpr uint32_t kOnes = 0x3F803F80u;  // bf16 1.0, 1.0
+      uint32_t w[32];
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {  // this half's 8-column chunks cc = 8 half + c8
-        const int cc = 8 * half + c8;
-        uint32_t w[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float p0 = tc::ex2(fmaf(x[c8 >> 2][(c8 & 3) * 8 + 2 * u], a.scale_log2, neg_m));
-          const float p1 = tc::ex2(fmaf(x[c8 >> 2][(c8 & 3) * 8 + 2 * u + 1], a.scale_log2, neg_m));
-          w[u] = pack_bf16(p0, p1);
-          l = fmab_ll(w[u], kOnes, l);
-          l = fmab_hl(w[u], kOnes, l);
-        }
-        *reinterpret_cast<uint4*>(prow + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = tc::ex2(fmaf(x[c >> 4][(2 * c) & 31], a.scale_log2, neg_m));
+        const float p1 = tc::ex2(fmaf(x[c >> 4][(2 * c + 1) & 31], a.scale_log2, neg_m));
+        w[c] = pack_bf16(p0, p1);
+        l = fmab_ll(w[c], kOnes, l);
+        l = fmab_hl(w[c], kOnes, l);
       }
-      tc::fence_async_smem();
-      tc::mbar_arrive(&sm.p_full[j & 1]);
+      tc::tmem_st32u(tS + lane_off + sb * 128 + half * 32, w);
+      tc::tc_fence_before();
+      tc::mbar_arrive(&sm.p_full[sb]);
     }
     // the two halves' normalisers (they share m_used)
     float lo_ = 0.f;
