@@ -7,8 +7,8 @@
 // One CTA per (128-row query tile, query head); heaviest tiles are scheduled first.
 //   warps 0, 10 TMA producers: Q tile once (3-D map over [n][Hq][d]); K tiles (warp 0) and
 //               V tiles (warp 10) of 128 keys (two 64-row pages each, through the block
-//               table) into 2-slot rings, 128-byte swizzle; a K slot frees when its QK is
-//               done, a V slot when its PV is done.
+//               table) into kKV-slot rings, 128-byte swizzle; a K slot frees when its QK
+//               is done, a V slot when its PV is done.
 //   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers (M=128, N=128,
 //               K=128), then O += P_j V_j (A = P from tensor memory, B = V MN-major);
 //               S_{j+1} is issued before waiting for P_j so the tensor core stays busy.
@@ -41,14 +41,15 @@ constexpr int kVWarp = 10;         // the V producer
 constexpr uint32_t kTileBytes = kPT * 128 * 2;  // 32 KB: 128 rows x 128 bf16
 constexpr uint32_t kTmemColsPf = 512;
 constexpr float kRescaleLog2 = 8.f;
+constexpr int kKV = 2;             // K slots and V slots (tile j in slot j % kKV)
 
 struct PfSmem {
   uint8_t q[kTileBytes];      // A of S: K-blocks (d 0-63, d 64-127) x [128 rows x 128 B]
-  uint8_t k[2][kTileBytes];   // B of S: same layout, rows = keys
-  uint8_t v[2][kTileBytes];   // B of PV (MN-major): d-halves x [128 keys x 128 B]
+  uint8_t k[kKV][kTileBytes];  // B of S: same layout, rows = keys
+  uint8_t v[kKV][kTileBytes];  // B of PV (MN-major): d-halves x [128 keys x 128 B]
   float xch[2][kPT];           // [half] a tile's row maxima of the two column halves (then
                                // the row normaliser's halves, at the end)
-  uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], p_empty[2];
+  uint64_t q_full, k_full[kKV], k_empty[kKV], v_full[kKV], v_empty[kKV], s_full[2], p_full[2], p_empty[2];
   uint64_t x_full[4], x_empty[4];  // per lane quadrant: both halves wrote / read xch
   uint32_t tmem_base;
   int abort;
@@ -81,11 +82,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
   if (threadIdx.x == 0) {
     tc::mbar_init(&sm.q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kKV; ++s) {
       tc::mbar_init(&sm.k_full[s], 1);
       tc::mbar_init(&sm.k_empty[s], 1);  // QK of the slot's tile done
       tc::mbar_init(&sm.v_full[s], 1);
       tc::mbar_init(&sm.v_empty[s], 1);  // PV of the slot's tile done
+    }
+    for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&sm.s_full[s], 1);
       tc::mbar_init(&sm.p_full[s], 256);  // every softmax thread wrote its part of P into TMEM
       tc::mbar_init(&sm.p_empty[s], 1);   // PV of the buffer's tile done (and every MMA before it)
@@ -121,8 +124,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
       int issued = 0;
       for (int j = 0; j < J && !aborted(sm); ++j) {
-        const int st = j & 1;
-        if (!tc::mbar_wait(&empty[st], ((j >> 1) & 1) ^ 1)) {
+        const int st = j % kKV;
+        if (!tc::mbar_wait(&empty[st], ((j / kKV) & 1) ^ 1)) {
           set_abort(sm, a.dev_err);
           break;
         }
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         issued = j + 1;
       }
-      for (int j = max(0, issued - 2); j < issued; ++j) (void)tc::mbar_wait(&full[j & 1], (j >> 1) & 1);
+      for (int j = max(0, issued - kKV); j < issued; ++j) (void)tc::mbar_wait(&full[j % kKV], (j / kKV) & 1);
       if (is_k) (void)tc::mbar_wait(&sm.q_full, 0);
     }
   } else if (warp == 1) {
@@ -157,35 +160,35 @@ __global__ void __launch_bounds__(kPThreads, 1)
       int pv_issued = 0;
       // S_j's buffer held P_{j-2}, read by PV_{j-2}, which this thread issued before S_j
       auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!tc::mbar_wait(&sm.k_full[st], (j >> 1) & 1)) return false;
+        const int st = j & 1, kv = j % kKV;
+        if (!tc::mbar_wait(&sm.k_full[kv], (j / kKV) & 1)) return false;
         tc::tc_fence_after();
-        const uint32_t kb = tc::smem_u32(sm.k[st]);
+        const uint32_t kb = tc::smem_u32(sm.k[kv]);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
           tc::mma_bf16(tS + st * 128, tc::sdesc_sw128(qb + off), tc::sdesc_sw128(kb + off), idS, ks > 0 ? 1u : 0u);
         }
         tc::mma_commit(&sm.s_full[st]);
-        tc::mma_commit(&sm.k_empty[st]);
+        tc::mma_commit(&sm.k_empty[kv]);
         return true;
       };
       bool ok = tc::mbar_wait(&sm.q_full, 0) && issue_s(0);
       for (int j = 0; ok && j < J; ++j) {
         if (j + 1 < J && !issue_s(j + 1)) { ok = false; break; }
-        const int st = j & 1;
-        if (!tc::mbar_wait(&sm.p_full[st], (j >> 1) & 1) || !tc::mbar_wait(&sm.v_full[st], (j >> 1) & 1)) {
+        const int st = j & 1, kv = j % kKV;
+        if (!tc::mbar_wait(&sm.p_full[st], (j >> 1) & 1) || !tc::mbar_wait(&sm.v_full[kv], (j / kKV) & 1)) {
           ok = false;
           break;
         }
         tc::tc_fence_after();
-        const uint32_t vb = tc::smem_u32(sm.v[st]);
+        const uint32_t vb = tc::smem_u32(sm.v[kv]);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // keys 16 ks .. 16 ks + 15 of P_j: columns 8 ks .. 8 ks + 7
           const uint64_t bd = tc::sdesc_sw128_mn(vb + ks * 2048u, 16384u, 1024u);
           tc::mma_bf16_ts(tO, tS + st * 128 + ks * 8, bd, idO, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        tc::mma_commit(&sm.v_empty[st]);
+        tc::mma_commit(&sm.v_empty[kv]);
         tc::mma_commit(&sm.p_empty[st]);
         pv_issued = j + 1;
       }
