@@ -15,12 +15,16 @@
 //   warps 2-9   softmax, two threads per query row (warps w and w+4 share a TMEM lane
 //               quadrant, each takes 64 of the tile's 128 columns; the halves swap their
 //               row maxima through shared memory): row max, exp2 (base-2 logits), P in
-//               bf16 written back over the tile's own S buffer (the normaliser sums the
-//               same rounded values), and a lazy O rescale: the reference max only moves
-//               when the row max grows by more than 2^8, which keeps every weight below
-//               256 and needs no approximation; only a rescale waits for the previous PV.
+//               bf16 written back over the tile's own S buffer, and a lazy O rescale: the
+//               reference max only moves when the row max grows by more than 2^8, which
+//               keeps every weight below 256 and needs no approximation; only a rescale
+//               waits for the previous PV. The normaliser is not summed here: every V slot
+//               carries a third 64-column block of ones, the P.V MMA runs with N = 144, and
+//               O's column 128 accumulates the sum of the same bf16 weights on the tensor
+//               core.
 //   warp 10     TMA producer of the V tiles.
-// TMEM: S0 columns [0,128), S1 [128,256), O [256,384); P_j occupies the first 64 columns
+// TMEM: S0 columns [0,128), S1 [128,256), O [256,400) (d, then the normaliser's 16
+// columns, 128-143, all equal); P_j occupies the first 64 columns
 // of S_j's buffer (two bf16 per column), so it never passes through shared memory. A
 // buffer is rewritten by S_{j+2} only after PV_j has read P_j: one thread issues both in
 // that order and the tensor pipe executes one thread's MMAs in order. Every mbarrier wait
@@ -39,6 +43,8 @@ constexpr int kPT = 128;           // query rows per tile = keys per KV tile
 constexpr int kPThreads = 352;     // TMA warps (Q and K; V), MMA warp, 8 softmax warps
 constexpr int kVWarp = 10;         // the V producer
 constexpr uint32_t kTileBytes = kPT * 128 * 2;  // 32 KB: 128 rows x 128 bf16
+constexpr uint32_t kVSlotBytes = kTileBytes + 16384;  // a V tile and its block of ones
+constexpr int kPVN = 144;          // P.V width: 128 d columns and 16 of the normaliser
 constexpr uint32_t kTmemColsPf = 512;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kKV = 2;             // K slots and V slots (tile j in slot j % kKV)
@@ -46,7 +52,7 @@ constexpr int kKV = 2;             // K slots and V slots (tile j in slot j % kK
 struct PfSmem {
   uint8_t q[kTileBytes];      // A of S: K-blocks (d 0-63, d 64-127) x [128 rows x 128 B]
   uint8_t k[kKV][kTileBytes];  // B of S: same layout, rows = keys
-  uint8_t v[kKV][kTileBytes];  // B of PV (MN-major): d-halves x [128 keys x 128 B]
+  uint8_t v[kKV][kVSlotBytes];  // B of PV (MN-major): d-halves then ones x [128 keys x 128 B]
   float xch[2][kPT];           // [half] a tile's row maxima of the two column halves (then
                                // the row normaliser's halves, at the end)
   uint64_t q_full, k_full[kKV], k_empty[kKV], v_full[kKV], v_empty[kKV], s_full[2], p_full[2], p_empty[2];
@@ -100,6 +106,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     sm.abort = 0;
     tc::fence_mbar_init();
   }
+  // the V slots' third 64-column block: all ones (bf16), written once; the TMA loads fill
+  // only the first two
+  for (int e = threadIdx.x; e < kKV * 1024; e += kPThreads)
+    *reinterpret_cast<uint4*>(sm.v[e >> 10] + kTileBytes + 16 * (e & 1023)) =
+        make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  tc::fence_async_smem();  // visible to the tensor core's reads
   if (warp == 1) tc::tmem_alloc(&sm.tmem_base, kTmemColsPf);
   tc::tc_fence_before();
   __syncthreads();
@@ -155,7 +167,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16_f32(kPT, kPT);
-      constexpr uint32_t idO = tc::idesc_bf16_f32_bmn(kPT, 128);
+      constexpr uint32_t idO = tc::idesc_bf16_f32_bmn(kPT, kPVN);
       const uint32_t qb = tc::smem_u32(sm.q);
       int pv_issued = 0;
       // S_j's buffer held P_{j-2}, read by PV_{j-2}, which this thread issued before S_j
@@ -202,7 +214,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int r = qd * 32 + lane;
     const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-    float m_used = -INFINITY, l = 0.f;
+    float m_used = -INFINITY;
     // hand a value to the other half of the row through xch (round x: bounded mbarrier
     // waits, so a half that stopped cannot leave the other waiting for ever)
     auto swap = [&](float v, int x, float& other) -> bool {
@@ -266,43 +278,38 @@ __global__ void __launch_bounds__(kPThreads, 1)
             break;
           }
           tc::tc_fence_after();
+          // this half's 64 d columns; half 0 also the normaliser's block (128 onwards)
 #pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 2 + (half == 0); ++c) {
             float ov[32];
-            tc::tmem_ld32(tO + lane_off + half * 64 + c * 32, ov);
+            const uint32_t col = c < 2 ? half * 64 + c * 32 : 128;
+            tc::tmem_ld32(tO + lane_off + col, ov);
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-            tc::tmem_st32(tO + lane_off + half * 64 + c * 32, ov);
+            tc::tmem_st32(tO + lane_off + col, ov);
           }
         }
-        l *= alpha;
       }
       // P row (bf16) back into tensor memory over S_j: this half's keys 64 half + 2c, +1 go to
       // column 32 half + c of the buffer (the other half read its S columns before the max
-      // exchange above). p = 2^(x*s - m): one FMA and ex2 (which maps -inf to +0); the
-      // normaliser adds the same bf16-rounded weights through a mixed-precision FMA against
-      // bf16 1.0 (exact: no unpacking).
+      // exchange above). p = 2^(x*s - m): one FMA and ex2 (which maps -inf to +0).
       const float neg_m = -m_used;
-      constexpr uint32_t kOnes = 0x3F803F80u;  // bf16 1.0, 1.0
       uint32_t w[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float p0 = tc::ex2(fmaf(x[c >> 4][(2 * c) & 31], a.scale_log2, neg_m));
         const float p1 = tc::ex2(fmaf(x[c >> 4][(2 * c + 1) & 31], a.scale_log2, neg_m));
         w[c] = pack_bf16(p0, p1);
-        l = fmab_ll(w[c], kOnes, l);
-        l = fmab_hl(w[c], kOnes, l);
       }
       tc::tmem_st32u(tS + lane_off + sb * 128 + half * 32, w);
       tc::tc_fence_before();
       tc::mbar_arrive(&sm.p_full[sb]);
     }
-    // the two halves' normalisers (they share m_used)
-    float lo_ = 0.f;
-    if (ok && !swap(l, J, lo_)) ok = false;
-    l += lo_;
     if (__all_sync(0xffffffffu, ok && !aborted(sm) && tc::mbar_wait(&sm.p_empty[(J - 1) & 1], ((J - 1) >> 1) & 1))) {
       tc::tc_fence_after();
+      float lv[32];
+      tc::tmem_ld32(tO + lane_off + 128, lv);  // the row's normaliser (both halves' weights)
+      const float l = lv[0];
       const float linv = l > 0.f ? 1.f / l : 0.f;
       float* orow = a.o + ((size_t)i * a.Hq + h) * 128 + half * 64;
 #pragma unroll 1
