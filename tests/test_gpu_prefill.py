@@ -53,6 +53,20 @@ def test_prefill_fa_rows_outputs(H, n, Hq, Hkv, permute):
     assert (cnt == 0).all()
 
 
+@pytest.mark.parametrize("n", [1, 50, 64, 65, 130, 200])
+def test_prefill_short_sequences(H, n):
+    """Sequences shorter than a key tile or ending inside one: the tile's second page lies
+    past the pool, and must read as zeros (not as whatever the slot held). FA output, lse and
+    the selection (k covers every far range here) on every row."""
+    grp = W.prefill_group(n, 8, 1, 128, w=16, k=300, dtype="bf16", seed=27, n_sa=1, rho=0.99, permute=True)
+    o, lse, idx, cnt = run_fa(H, grp)
+    rows = np.arange(n)
+    o_r, lse_r, idx_r, cnt_r = O.fa_prefill_rows(grp.q_fa, grp.kv, rows, grp.w, grp.k, grp.scale)
+    assert np.isfinite(o).all() and max_abs(o, o_r) <= tol("bf16"), max_abs(o, o_r)
+    assert max_abs(lse, lse_r) <= tol("bf16")
+    assert np.array_equal(cnt, cnt_r) and np.array_equal(idx, idx_r)
+
+
 def test_prefill_fa_sharp_needles(H):
     # unit-variance q and k: concentrated rows, needles aligned with the last row
     grp = W.prefill_group(700, 8, 1, 128, w=16, k=0, dtype="bf16", seed=22, n_sa=0, needles=8)

@@ -141,23 +141,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
           set_abort(sm, a.dev_err);
           break;
         }
+        // a page past the sequence (or a bad table entry, flagged) is loaded from the row just
+        // past the pool, which the TMA fills with zeros: the slot never keeps stale or
+        // uninitialised rows (a NaN among V's rows would reach every row through P.V, even
+        // with its weight 0)
+        const int oob = a.num_pages * a.Hkv * kPage;
         int rows[2];
-        uint32_t bytes = 0;
         for (int pg = 0; pg < 2; ++pg) {
           const int lp = 2 * j + pg;
-          rows[pg] = -1;
+          rows[pg] = oob;
           if (lp < npages) {
             const int phys = bt[lp];
             if (phys < 0 || phys >= a.num_pages) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
-            else { rows[pg] = (phys * a.Hkv + g) * kPage; bytes += 2 * 8192; }
+            else rows[pg] = (phys * a.Hkv + g) * kPage;
           }
         }
-        tc::mbar_arrive_expect_tx(&full[st], bytes);
+        tc::mbar_arrive_expect_tx(&full[st], 4 * 8192);
         uint8_t* dst = is_k ? sm.k[st] : sm.v[st];
-        for (int pg = 0; pg < 2; ++pg) {
-          if (rows[pg] < 0) continue;
+        for (int pg = 0; pg < 2; ++pg)
           for (int hh = 0; hh < 2; ++hh) tc::tma_load_2d(dst + hh * 16384 + pg * 8192, tm, 64 * hh, rows[pg], &full[st]);
-        }
         issued = j + 1;
       }
       for (int j = max(0, issued - kKV); j < issued; ++j) (void)tc::mbar_wait(&full[j % kKV], (j / kKV) & 1);
