@@ -107,6 +107,10 @@ HS2_DEVI float ex2_approx(float x) {
 
 // exp2 of a (possibly -inf) base-2 logit relative to a (possibly -inf) max:
 // a row whose max is still -inf contributes exactly zero.
+// Barrier `id` (1-15) over the first `nthreads` threads (a multiple of 32) that reach it.
+HS2_DEVI void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 HS2_DEVI float exp2_rel(float x, float m) { return (m == -INFINITY) ? 0.f : exp2f(x - m); }
 
 // m16n8k16 bf16 MMA with fp32 accumulate (legacy warp-level tensor path; used where

@@ -21,6 +21,9 @@
 //   3. at the end of each pair in its range, writes the pair's output directly when it
 //      covered the whole pair, otherwise writes a partial (m, l, o) and arrives on the
 //      pair's counter; the last warp to arrive merges the partials and resets the counter.
+//      When that arrival ends the warp's range (the usual case: a pair's last partial comes
+//      from a warp that ends with it), the merge is left to the end of the kernel, where the
+//      CTA's warps share the recorded merges, two heads per warp and pass.
 #include <algorithm>
 
 #include "common.cuh"
@@ -73,8 +76,11 @@ HS2_DEVI int warp_of_step(long long s, long long total, int nw) { return (int)((
 // slab scales act as FP8's.
 // EPI = true: the SA layer has a sink bias or an output gate (sa_norm_factor, sa_gate); false
 // keeps the plain 1 / L epilogue, whose smaller register footprint the streaming loop feels.
+// Registers are held to three CTAs per SM where shared memory fits three (bf16 rings, and
+// every format at D = 64); the FP8 / FP4 rings at D = 128 fit two.
 template <int D, int FMT, bool EPI>
-__global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const SaStreamArgs sp) {
+__global__ void __launch_bounds__(128, (FMT == kFmtBf16 || D == 64) ? 3 : 1)
+    sa_stream_kernel(const AttnArgs a, const SaStreamArgs sp) {
   constexpr bool LOWP = FMT != kFmtBf16;
   constexpr int NT = 1;  // 8 query heads per unit
   constexpr int HALVES = D / 64;
@@ -87,7 +93,10 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int wid = blockIdx.x * 4 + warp;
+  // pairs whose last partial arrives at the end of a warp's range; merged by the CTA's warps
+  __shared__ int pend_s[4];
   if (wid >= sp.nwarps) return;
+  if (lane == 0) pend_s[warp] = -1;
   const int G = a.G, HG = sp.hg, ms = sp.ms;
   const long long total = sp.total;
   const long long s0 = total * wid / sp.nwarps, s1 = total * (wid + 1) / sp.nwarps;
@@ -391,6 +400,14 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
     if (lane == 0) is_last = atomicAdd(&a.arrive[un], 1) == nc - 1;
     is_last = __shfl_sync(0xffffffffu, is_last, 0);
     if (!is_last) continue;
+    if (j == ns - 1) {  // the range ends here: the CTA's warps merge it together below
+      if (lane == 0) {
+        pend_s[warp] = un;
+        a.arrive[un] = 0;
+      }
+      __threadfence();
+      continue;
+    }
     __threadfence();
     // merge (nc <= 32): lane r holds partial r's (m, l) of each head; lanes then sweep the
     // heads' D columns four at a time, weights broadcast by shuffle
@@ -442,6 +459,81 @@ __global__ void __launch_bounds__(128) sa_stream_kernel(const AttnArgs a, const 
     if (lane == 0) a.arrive[un] = 0;
   }
   cp_async_wait<0>();
+
+  // ---- 4. the merges recorded at range ends finish the kernel: the CTA's active warps take
+  // them together, two heads per warp and pass, loading eight partials per head at once
+  const int cta_warps = min(4, sp.nwarps - (int)blockIdx.x * 4);
+  named_barrier_sync(1, 32 * cta_warps);
+  __threadfence();
+  for (int e = warp;; e += cta_warps) {
+    int want = e >> 2, un = -1;  // item e: pending pair e / 4 (in warp order), heads 2 (e % 4) + {0, 1}
+    for (int w2 = 0; w2 < cta_warps; ++w2)
+      if (pend_s[w2] >= 0) {
+        if (want == 0) {
+          un = pend_s[w2];
+          break;
+        }
+        --want;
+      }
+    if (un < 0) break;
+    const int p = un / HG, h0 = (un % HG) * 8, Gh = min(8, G - h0);
+    const int ha = 2 * (e & 3);
+    if (ha >= Gh) continue;
+    const int qi = p / a.Hkv, g = p % a.Hkv;
+    const int first = warp_of_step((long long)un * ms, total, sp.nwarps);
+    const int last = warp_of_step((long long)(un + 1) * ms - 1, total, sp.nwarps);
+    const int nc = last - first + 1;
+    const size_t p0 = (size_t)un * sp.maxc * 8;
+    float f[2], inv[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int h = ha + hh;
+      const float2 ml = (lane < nc && h < Gh) ? __ldcg(&a.part_ml[p0 + (size_t)lane * 8 + h]) : make_float2(-INFINITY, 0.f);
+      const float M = warp_max(ml.x);
+      f[hh] = lane < nc ? exp2_rel(ml.x, M) : 0.f;
+      const float L = warp_sum(f[hh] * ml.y);
+      if constexpr (EPI) inv[hh] = sa_norm_factor(M, L, h < Gh ? sink_b2(a.sink, g * G + h0 + h) : -INFINITY);
+      else inv[hh] = L > 0.f ? 1.f / L : 0.f;
+    }
+    float4 o4[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    const float* pob = a.part_o + p0 * D + 4 * lane;
+    for (int r0 = 0; r0 < nc; r0 += 8) {
+      float4 v[8][2];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          v[q][hh] = (r0 + q < nc && ha + hh < Gh && 4 * lane < D)
+                         ? __ldcg(reinterpret_cast<const float4*>(pob + ((size_t)(r0 + q) * 8 + ha + hh) * D))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const float fr = __shfl_sync(0xffffffffu, f[hh], (r0 + q) & 31);
+          o4[hh].x += fr * v[q][hh].x;
+          o4[hh].y += fr * v[q][hh].y;
+          o4[hh].z += fr * v[q][hh].z;
+          o4[hh].w += fr * v[q][hh].w;
+        }
+    }
+    float* out = a.out_o + ((size_t)qi * a.Hq + (size_t)g * G + h0) * D;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int h = ha + hh;
+      if (h < Gh && 4 * lane < D) {
+        float4 r4 = make_float4(o4[hh].x * inv[hh], o4[hh].y * inv[hh], o4[hh].z * inv[hh], o4[hh].w * inv[hh]);
+        if (EPI && a.gate) {
+          const float4 g4 = __ldg(reinterpret_cast<const float4*>(a.gate + ((size_t)qi * a.Hq + g * G + h0 + h) * D) + lane);
+          r4.x *= sa_gate(g4.x);
+          r4.y *= sa_gate(g4.y);
+          r4.z *= sa_gate(g4.z);
+          r4.w *= sa_gate(g4.w);
+        }
+        *reinterpret_cast<float4*>(out + h * D + 4 * lane) = r4;
+      }
+    }
+  }
 }
 
 template <int D, int FMT>
