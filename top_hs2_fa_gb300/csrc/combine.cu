@@ -138,8 +138,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_score_kernel(const Combin
       const float4 x0 = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)h * a.ld_logits));
       const float4 x1 = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)h * a.ld_logits + 4));
       const float l2 = lse2_s[h];
-      sc[0] += exp2f(x0.x - l2); sc[1] += exp2f(x0.y - l2); sc[2] += exp2f(x0.z - l2); sc[3] += exp2f(x0.w - l2);
-      sc[4] += exp2f(x1.x - l2); sc[5] += exp2f(x1.y - l2); sc[6] += exp2f(x1.z - l2); sc[7] += exp2f(x1.w - l2);
+      sc[0] += ex2_approx(x0.x - l2); sc[1] += ex2_approx(x0.y - l2);
+      sc[2] += ex2_approx(x0.z - l2); sc[3] += ex2_approx(x0.w - l2);
+      sc[4] += ex2_approx(x1.x - l2); sc[5] += ex2_approx(x1.y - l2);
+      sc[6] += ex2_approx(x1.z - l2); sc[7] += ex2_approx(x1.w - l2);
     }
   }
   uint32_t key[8];
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_score_kernel(const Combin
     *reinterpret_cast<uint4*>(keys + s0 + 4) = make_uint4(key[4], key[5], key[6], key[7]);
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) hist_add_warp(hist, s0 + e < nF, key[e] >> 20);
+  for (int e = 0; e < 8; ++e) hist_add(hist, s0 + e < nF, key[e] >> 20);
   __syncthreads();
   uint32_t* gh = a.hist + ((size_t)qi * a.Hkv + g) * kRadixBins;
   for (int i = tid; i < kRadixBins; i += NT) {
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(kSelectThreads, 2) score_select_kernel(const C
   // ---- scores of the far range, 4 positions per thread and pass, kScoreHeads heads' loads in flight
   const float* lg = a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits;
   uint32_t* keys = a.scores + ((size_t)qi * a.Hkv + g) * a.ld_logits;
-  // the trip count is the same for every thread: the histogram update is warp-collective
+  // (one CTA-wide trip count: threads past nF only skip their loads)
   for (int base = 0; base < nF; base += 4 * NT) {
     const int s0 = base + 4 * tid;
     const bool mine = s0 < nF;
@@ -473,10 +475,10 @@ __global__ void __launch_bounds__(kSelectThreads, 2) score_select_kernel(const C
       for (int hh = 0; hh < kScoreHeads; ++hh)
         if (mine && h0 + hh < G) {
           const float l2 = lse2_s[h0 + hh];
-          sc[0] += exp2f(x[hh].x - l2);
-          sc[1] += exp2f(x[hh].y - l2);
-          sc[2] += exp2f(x[hh].z - l2);
-          sc[3] += exp2f(x[hh].w - l2);
+          sc[0] += ex2_approx(x[hh].x - l2);
+          sc[1] += ex2_approx(x[hh].y - l2);
+          sc[2] += ex2_approx(x[hh].z - l2);
+          sc[3] += ex2_approx(x[hh].w - l2);
         }
     }
     uint32_t key[4];
@@ -484,7 +486,7 @@ __global__ void __launch_bounds__(kSelectThreads, 2) score_select_kernel(const C
     for (int e = 0; e < 4; ++e) key[e] = (s0 + e < nF) ? __float_as_uint(sc[e]) : 0u;
     if (mine) *reinterpret_cast<uint4*>(keys + s0) = make_uint4(key[0], key[1], key[2], key[3]);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) hist_add_warp(sm.hist, s0 + e < nF, key[e] >> 20);
+    for (int e = 0; e < 4; ++e) hist_add(sm.hist, s0 + e < nF, key[e] >> 20);
   }
   __syncthreads();  // keys (global, read back through L2) and the histogram are complete
   int* la = fbuf;

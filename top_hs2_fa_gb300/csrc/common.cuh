@@ -98,7 +98,8 @@ HS2_DEVI float warp_sum(float v) {
 constexpr float kLazyRescale = 8.f;
 
 // 2^x by the hardware approximation (relative error about 2^-22; results below 2^-126
-// flush to zero, -inf gives 0): the softmax weights, which are rounded to 16 bits anyway.
+// flush to zero, -inf gives 0): the softmax weights, which are rounded to 16 bits anyway,
+// and the decode selection scores (a head's share under 2^-126 is dropped from the sum).
 HS2_DEVI float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

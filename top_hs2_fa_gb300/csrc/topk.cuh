@@ -51,6 +51,12 @@ HS2_DEVI int block_exclusive_scan(int v, int* warp_tot) {
 }
 
 // Add `cnt` to hist[dig] for every participating lane, one atomic per distinct digit.
+// One shared-memory atomic per key: cheaper than hist_add_warp's ballot and match when
+// the digits of a warp's keys are spread out (the first digit of scores over a sequence),
+// dearer when they pile onto a few bins (later radix passes, tied keys).
+HS2_DEVI void hist_add(uint32_t* hist, bool part, uint32_t dig) {
+  if (part) atomicAdd(&hist[dig], 1u);
+}
 HS2_DEVI void hist_add_warp(uint32_t* hist, bool part, uint32_t dig) {
   const unsigned pm = __ballot_sync(0xffffffffu, part);
   if (part) {
