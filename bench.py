@@ -306,8 +306,10 @@ class Decode:
             io.done(stream, ("fa", gi))
             for j in range(NSA):
                 io.need(stream, ("sa", gi, j))
+                # layers after the first follow an SA launch that wrote none of idx, cnt, table, lengths
                 hs2.hs2_sa_reuse(q[1 + j], d["kv"], self.w, d["idx"], d["cnt"], self.k, self.host[gi].scale,
-                                 out=d["o"][1 + j], workspace=d["ws_sa"], dev_err=err, stream=stream)
+                                 out=d["o"][1 + j], workspace=d["ws_sa"], dev_err=err, stream=stream,
+                                 overlap=j > 0)
                 io.done(stream, ("sa", gi, j))
 
     def e2e_buffers(self, dev):
@@ -527,7 +529,7 @@ class Csa2:
         for j in range(2, 5):  # Reuse layers read the Reindex layer's indices
             io.need(stream, ("layer", j))
             hs2.hs2_sa_reuse(q[j], d["kv"], 0, d["idx"][1], d["cnt"][1], self.k_top, g.scale, out=d["o"][j],
-                             workspace=d["ws_sa"], dev_err=err, stream=stream)
+                             workspace=d["ws_sa"], dev_err=err, stream=stream, overlap=True)
             io.done(stream, ("layer", j))
 
     def e2e_buffers(self, dev):

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define HS2_ABI_VERSION 5
+#define HS2_ABI_VERSION 6
 
 typedef enum {
   HS2_OK = 0,
@@ -211,7 +211,8 @@ hs2_status hs2_fa_select_noalloc(const void* q, int B_or_n, int Hq, const hs2_kv
  *   o[..][h][:] = sum_{s in U} softmax_U(scale * q_h . k_g(s)) v_g(s), one softmax.
  * Shapes and the decode / prefill convention are those of hs2_fa_select; idx and
  * idx_cnt have the layout hs2_fa_select writes ([B_or_n][Hkv][k], [B_or_n][Hkv]).
- * workspace: at least hs2_sa_reuse_workspace(...) bytes, 256-byte aligned.        */
+ * workspace: at least hs2_sa_reuse_workspace(...) bytes, 256-byte aligned, no
+ *   initialisation needed; calls that run at the same time need workspaces of their own. */
 size_t hs2_sa_reuse_workspace(int B_or_n, int Hq, const hs2_kv* kv, int w, int k, int prefill);
 hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int w,
                         const int32_t* idx, const int32_t* idx_cnt, int k, float scale, int prefill,
@@ -222,12 +223,25 @@ hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int
  * with logit sink[h] and a zero value, i.e. the single softmax denominator over W ∪ S
  * gains exp(sink[h]) (-inf = no sink). gate: float32 [B_or_n][Hq][d] logits, or NULL:
  * the output is multiplied elementwise by 1 / (1 + exp(-gate)). Both are read-only,
- * device memory, owned by the caller. Everything else as hs2_sa_reuse (which is this
- * call with sink = gate = NULL); the workspace size does not change. */
+ * device memory, owned by the caller.
+ * flags: 0 or HS2_SA_OVERLAP. The decode kernel is always launched so that it may start
+ *   while the previous launch on `stream` finishes (programmatic dependent launch), and
+ *   waits for that launch before it reads anything. HS2_SA_OVERLAP (decode) is for the SA
+ *   layers of a group after the first, each issued right after the one before it:
+ *   - the call reads idx, idx_cnt, kv->block_table and kv->seq_len before that wait, so
+ *     those four must have been complete before the previous launch on the stream began
+ *     (not written by it);
+ *   - `workspace` must be the one the previous hs2_sa_reuse call on this stream used,
+ *     with the same B_or_n, Hq, kv sizes, w and k: the call keeps the state that call
+ *     left in it instead of clearing it, and makes no launch but its kernel.
+ *   Prefill ignores the flag; other bits: HS2_ERR_ARG.
+ * Everything else as hs2_sa_reuse (which is this call with sink = gate = NULL, flags = 0);
+ * the workspace size does not change. */
+#define HS2_SA_OVERLAP 1
 hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int w,
                            const int32_t* idx, const int32_t* idx_cnt, int k, float scale, int prefill,
-                           const float* sink, const float* gate, float* o, void* workspace, size_t ws_bytes,
-                           int32_t* dev_err, void* stream);
+                           const float* sink, const float* gate, int flags, float* o, void* workspace,
+                           size_t ws_bytes, int32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------------------
  * CSA2 hierarchical sparse indexer  ([CSA2] §3.1-3.2; score from [L10] §5.1).

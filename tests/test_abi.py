@@ -48,7 +48,7 @@ def test_binding_constants_match_the_header():
 
 
 def test_version_and_strings(lib):
-    assert lib.hs2_abi_version() == H.ABI_VERSION == 5
+    assert lib.hs2_abi_version() == H.ABI_VERSION == 6
     for st, word in [(0, "ok"), (-1, "invalid"), (-2, "unsupported"), (-3, "CUDA"), (-4, "device")]:
         assert word in lib.hs2_strerror(st).decode()
 
@@ -90,6 +90,15 @@ def test_sa_validation(lib):
     assert st == -1
     st = lib.hs2_sa_reuse(256, 2, 8, ctypes.byref(kv), 16, 512, 0, 8, 0.1, 0, 1024, 4096, 1 << 30, None, None)
     assert st == -1
+
+
+def test_sa_flags_validation(lib):
+    """hs2_sa_reuse_ex takes 0 or HS2_SA_OVERLAP; any other bit is refused before any launch."""
+    kv = _kv()
+    for bad in (2, 4, -1):
+        st = lib.hs2_sa_reuse_ex(256, 2, 8, ctypes.byref(kv), 16, 512, 768, 8, 0.1, 0, None, None,
+                                 H.SA_OVERLAP | bad, 1024, 4096, 1 << 30, None, None)
+        assert st == -1
 
 
 def test_workspace_sizes_grow_with_problem(lib):

@@ -42,9 +42,16 @@ def run_decode_group(H, grp, sa_layers=None):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     o, lse, idx, cnt = H.hs2_fa_select(q, dkv, grp.w, grp.k, grp.scale, max_t=int(kv.seq_len.max()), dev_err=err)
     sa = []
+    outs = []
+    Hq = grp.q_fa.shape[1]
+    ws = torch.empty(H.hs2_sa_reuse_workspace(kv.B, Hq, dkv, grp.w, grp.k), dtype=torch.uint8, device="cuda")
     for j in range(len(grp.q_sa) if sa_layers is None else sa_layers):
         qs = to_torch(grp.q_sa[j], qdt(kv))
-        sa.append(H.hs2_sa_reuse(qs, dkv, grp.w, idx, cnt, grp.k, grp.scale, dev_err=err).cpu().numpy())
+        # layers after the first run back to back on one workspace with HS2_SA_OVERLAP, as a
+        # group step does
+        outs.append(H.hs2_sa_reuse(qs, dkv, grp.w, idx, cnt, grp.k, grp.scale, workspace=ws, dev_err=err,
+                                   overlap=j > 0))
+    sa = [x.cpu().numpy() for x in outs]
     torch.cuda.synchronize()
     return o.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy(), cnt.cpu().numpy(), sa, int(err.item())
 
@@ -417,3 +424,29 @@ def test_fp8_kv_rejects_prefill(H):
     with pytest.raises(H.HS2Error):
         H.hs2_fa_select(to_torch(grp.q_fa, "bf16"), kv_to_device(kv), 16, 32, grp.scale, prefill=True)
     torch.cuda.synchronize()
+
+
+def test_sa_layers_share_a_workspace_with_overlap(H):
+    """Three decode SA layers back to back on one workspace that starts as random bytes: the
+    first call clears the pair counters, the next two (HS2_SA_OVERLAP) take them as the call
+    before left them; twice over, against the oracle."""
+    import torch
+
+    grp = W.decode_group([3000, 9000, 20000, 5000], Hq=32, Hkv=4, d=128, w=128, k=512, dtype="bf16", seed=31,
+                         n_sa=3, needles=8)
+    kv = grp.kv
+    dkv = kv_to_device(kv)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q = to_torch(grp.q_fa, "bf16")
+    _, _, idx, cnt = H.hs2_fa_select(q, dkv, grp.w, grp.k, grp.scale, max_t=int(kv.seq_len.max()), dev_err=err)
+    nb = H.hs2_sa_reuse_workspace(kv.B, 32, dkv, grp.w, grp.k)
+    ws = torch.randint(0, 256, (nb,), dtype=torch.uint8, device="cuda")
+    idx_h, cnt_h = idx.cpu().numpy(), cnt.cpu().numpy()
+    for rep in range(2):
+        outs = [H.hs2_sa_reuse(to_torch(grp.q_sa[j], "bf16"), dkv, grp.w, idx, cnt, grp.k, grp.scale, workspace=ws,
+                               dev_err=err, overlap=j > 0) for j in range(3)]
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        for j, o in enumerate(outs):
+            ref = O.sa_decode(grp.q_sa[j], kv, grp.w, idx_h, cnt_h, grp.scale)
+            assert max_abs(o.cpu().numpy(), ref) <= tol("bf16"), (rep, j)

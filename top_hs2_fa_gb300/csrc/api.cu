@@ -598,17 +598,18 @@ size_t hs2_sa_reuse_workspace(int B_or_n, int Hq, const hs2_kv* kv, int w, int k
 hs2_status hs2_sa_reuse(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int w, const int32_t* idx,
                         const int32_t* idx_cnt, int k, float scale, int prefill, float* o, void* workspace,
                         size_t ws_bytes, int32_t* dev_err, void* stream) {
-  return hs2_sa_reuse_ex(q, B_or_n, Hq, kv, w, idx, idx_cnt, k, scale, prefill, nullptr, nullptr, o, workspace,
+  return hs2_sa_reuse_ex(q, B_or_n, Hq, kv, w, idx, idx_cnt, k, scale, prefill, nullptr, nullptr, 0, o, workspace,
                          ws_bytes, dev_err, stream);
 }
 
 hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, int w, const int32_t* idx,
                            const int32_t* idx_cnt, int k, float scale, int prefill, const float* sink,
-                           const float* gate, float* o, void* workspace, size_t ws_bytes, int32_t* dev_err,
-                           void* stream) {
+                           const float* gate, int flags, float* o, void* workspace, size_t ws_bytes,
+                           int32_t* dev_err, void* stream) {
   hs2_status st = common_checks(q, B_or_n, Hq, kv, prefill, true);
   if (st != HS2_OK) return st;
   if (w < 0 || k < 0 || !std::isfinite(scale) || !o || !idx_cnt || (k > 0 && !idx)) return HS2_ERR_ARG;
+  if (flags & ~HS2_SA_OVERLAP) return HS2_ERR_ARG;
   if (B_or_n == 0) return HS2_OK;
   const SaPlan p = sa_plan(B_or_n, Hq, kv, w, k, prefill);
   if (low_precision(kv) && !p.stream) return HS2_ERR_UNSUPPORTED;  // FP8 / FP4: the decode stream only
@@ -653,10 +654,17 @@ hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, 
   a.dev_err = dev_err;
   if (p.stream) {
     // decode (bf16, FP8, FP4): one persistent warp stream over all (query, KV head) pairs' entries
+    // the counters start at zero; an HS2_SA_OVERLAP call takes them as the SA call before it
+    // on this workspace left them (zero), so it is a single launch whose row resolve can
+    // overlap the end of that call's kernel
     a.arrive = (int32_t*)(ws + p.off_arrive);
-    cudaError_t e = cudaMemsetAsync(a.arrive, 0, (size_t)B_or_n * kv->Hkv * p.sp.hg * sizeof(int32_t), s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    e = profiled(HS2_STAGE_SA_GATHER, s, [&] { return hs2::launch_sa_stream(a, p.sp, p.grid, s); });
+    hs2::SaStreamArgs sp = p.sp;
+    sp.early = (flags & HS2_SA_OVERLAP) ? 1 : 0;
+    if (!sp.early) {
+      cudaError_t e = cudaMemsetAsync(a.arrive, 0, (size_t)B_or_n * kv->Hkv * p.sp.hg * sizeof(int32_t), s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    cudaError_t e = profiled(HS2_STAGE_SA_GATHER, s, [&] { return hs2::launch_sa_stream(a, sp, p.grid, s); });
     if (e != cudaSuccess) return cuda_fail(e);
     return HS2_OK;
   }

@@ -108,6 +108,13 @@ HS2_DEVI float ex2_approx(float x) {
 
 // exp2 of a (possibly -inf) base-2 logit relative to a (possibly -inf) max:
 // a row whose max is still -inf contributes exactly zero.
+// Programmatic dependent launch. griddep_wait: returns once the grids this launch depends
+// on have completed and their memory is visible (at once when it has no such dependency).
+// griddep_launch_dependents: the next launch on the stream, if it allows programmatic
+// serialization, may begin once every CTA of this grid has called it or exited.
+HS2_DEVI void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+HS2_DEVI void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Barrier `id` (1-15) over the first `nthreads` threads (a multiple of 32) that reach it.
 HS2_DEVI void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -32,7 +32,7 @@ struct AttnArgs {
   float* part_o;    // [Bq][Hq][nsplit][D]
   float* logits;    // [Bq][Hq][ld_logits] base-2 logits, or null
   float* out_o;     // [Bq][Hq][D] final output (kernels that normalise in place)
-  int32_t* arrive;  // SA stream: per-unit arrival counters, zero at launch
+  int32_t* arrive;  // SA stream: per-unit arrival counters, zero at launch (the merges leave them zero)
   const float* k_scale;  // FP8 cache: [num_pages][Hkv] dequantisation scales, else null
   const float* v_scale;
   const uint8_t* k_sf;  // FP4 cache: [num_pages][Hkv][64][D/16] E4M3 scales of 16 channels, else null
@@ -68,6 +68,7 @@ struct AppendArgs {
 struct SaStreamArgs {
   int nwarps, hg, ms, maxc;
   long long total;
+  int early;  // resolve rows before waiting on the previous launch
 };
 
 struct CombineArgs {
@@ -187,7 +188,8 @@ cudaError_t launch_combine(const CombineArgs& a, int Bq, cudaStream_t s);
 bool score_select_fused(const CombineArgs& a, int Bq);
 bool sa_mma_supported(int G, int D, int bf16, int w, int k);
 // Decode: plan the warp stream on the current device (false if it does not apply);
-// a.part_ml / a.part_o hold [units][maxc][8] partials and a.arrive [units] zeroed counters.
+// a.part_ml / a.part_o hold [units][maxc][8] partials and a.arrive [units] zeroed counters
+// (the kernel's merges leave them zero again).
 bool sa_stream_plan(int G, int D, int kv_dtype, int w, int k, int Bq, int Hkv, SaStreamArgs* sp, int* grid);
 cudaError_t launch_sa_stream(const AttnArgs& a, const SaStreamArgs& sp, int grid, cudaStream_t s);
 cudaError_t launch_sa_mma(const AttnArgs& a, int Bq, cudaStream_t s);

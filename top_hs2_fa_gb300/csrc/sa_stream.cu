@@ -24,6 +24,12 @@
 //      When that arrival ends the warp's range (the usual case: a pair's last partial comes
 //      from a warp that ends with it), the merge is left to the end of the kernel, where the
 //      CTA's warps share the recorded merges, two heads per warp and pass.
+// The merges leave every counter zero, so a call that follows another on the same workspace
+// needs no clearing launch between the two. The kernel is launched with programmatic stream
+// serialization: it waits on the previous launch (griddep_wait) before its first read of
+// anything that launch may write, and lets the next launch start once its own wait is over;
+// with sp.early the row resolve (reads of the indices, counts, block table and lengths only)
+// runs before that wait, overlapping the previous launch's tail.
 #include <algorithm>
 
 #include "common.cuh"
@@ -67,6 +73,7 @@ constexpr size_t str_smem_bytes() {
 // [floor(total*w/nw), floor(total*(w+1)/nw)) (every range non-empty when nw <= total).
 HS2_DEVI int warp_of_step(long long s, long long total, int nw) { return (int)(((s + 1) * nw - 1) / total); }
 
+
 // FMT = kFmtFp8: the cache holds E4M3 codes with one scale per (page, KV head). A warp's ring
 // then holds raw slots (the 16 K and 16 V rows at D bytes each, plus each entry's K and V
 // scale, staged by cp.async) and one f16 slot: every step converts its raw slot into the f16
@@ -97,6 +104,7 @@ __global__ void __launch_bounds__(128, (FMT == kFmtBf16 || D == 64) ? 3 : 1)
   __shared__ int pend_s[4];
   if (wid >= sp.nwarps) return;
   if (lane == 0) pend_s[warp] = -1;
+  if (!sp.early) griddep_wait();
   const int G = a.G, HG = sp.hg, ms = sp.ms;
   const long long total = sp.total;
   const long long s0 = total * wid / sp.nwarps, s1 = total * (wid + 1) / sp.nwarps;
@@ -193,6 +201,10 @@ __global__ void __launch_bounds__(128, (FMT == kFmtBf16 || D == 64) ? 3 : 1)
     if (bad_page) flag_error(a.dev_err, HS2_DEV_BAD_PAGE);
   }
   __syncwarp();
+  // everything below reads or writes what the previous launch may touch (queries, the
+  // partials and counters of a shared workspace, the output)
+  if (sp.early) griddep_wait();
+  griddep_launch_dependents();
 
   // ---- 2. stream the steps
   const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
@@ -598,7 +610,18 @@ static cudaError_t launch_stream_t(const AttnArgs& a, const SaStreamArgs& sp, in
   auto kern = (a.sink || a.gate) ? sa_stream_kernel<D, FMT, true> : sa_stream_kernel<D, FMT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 128, sm, s>>>(a, sp);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a, sp);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -16,7 +16,7 @@ import torch
 
 from . import build as _build
 
-ABI_VERSION = 5  # include/hs2.h HS2_ABI_VERSION this binding marshals for
+ABI_VERSION = 6  # include/hs2.h HS2_ABI_VERSION this binding marshals for
 F32, BF16, FP8_E4M3, FP4_E2M1 = 0, 1, 2, 3
 FULL, REINDEX = 0, 1
 DEV_BAD_PAGE, DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_LENGTH, DEV_SELECT = 1, 2, 4, 8, 16
@@ -27,6 +27,7 @@ EXPORTS = (
     "hs2_kv_append", "hs2_fa_select_append", "hs2_fa_select_launches", "hs2_sa_reuse_launches",
 )
 STAGE_FA_SCAN, STAGE_SA_GATHER, STAGE_INDEXER = 0, 1, 2
+SA_OVERLAP = 1  # HS2_SA_OVERLAP
 
 
 class hs2_kv(ctypes.Structure):
@@ -68,7 +69,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.hs2_sa_reuse_workspace.restype = sz
     lib.hs2_sa_reuse.argtypes = [vp, i32, i32, kvp, i32, vp, vp, i32, f32, i32, vp, vp, sz, vp, vp]
     lib.hs2_sa_reuse.restype = i32
-    lib.hs2_sa_reuse_ex.argtypes = [vp, i32, i32, kvp, i32, vp, vp, i32, f32, i32, vp, vp, vp, vp, sz, vp, vp]
+    lib.hs2_sa_reuse_ex.argtypes = [vp, i32, i32, kvp, i32, vp, vp, i32, f32, i32, vp, vp, i32, vp, vp, sz, vp, vp]
     lib.hs2_sa_reuse_ex.restype = i32
     lib.hs2_hier_reindex_workspace.argtypes = [i32, i32, kvp, i32, i32, i32, i32]
     lib.hs2_hier_reindex_workspace.restype = sz
@@ -255,29 +256,36 @@ def hs2_sa_reuse_workspace(B_or_n: int, Hq: int, kv: KV, w: int, k: int, prefill
 
 def hs2_sa_reuse(q: torch.Tensor, kv: KV, w: int, idx: torch.Tensor, idx_cnt: torch.Tensor, k: int,
                  scale: float, prefill: bool = False, out=None, workspace=None, dev_err=None, stream=None,
-                 sink: torch.Tensor | None = None, gate: torch.Tensor | None = None):
+                 sink: torch.Tensor | None = None, gate: torch.Tensor | None = None, overlap: bool = False):
     """SA layer reusing the FA's KV and indices with its own query. Returns o (float32).
 
     ``sink`` (float32 [Hq]) and ``gate`` (float32 [Bq][Hq][d]) are the optional per-head sink
-    logits and output gate logits (``hs2_sa_reuse_ex``); without them this is ``hs2_sa_reuse``."""
+    logits and output gate logits. ``overlap`` (``HS2_SA_OVERLAP``, the SA layers of a group
+    after the first): idx, idx_cnt, the block table and the lengths were complete before the
+    previous launch on the stream began, and ``workspace`` is the one the previous SA call on
+    this stream used with the same sizes, so the decode kernel is one launch that may read
+    them while that launch finishes. Without these three this is ``hs2_sa_reuse``, else
+    ``hs2_sa_reuse_ex``."""
     lib = load()
     Bq, Hq, d = q.shape
     c = kv.c()
     o = out if out is not None else torch.empty((Bq, Hq, d), dtype=torch.float32, device=q.device)
     nb = int(lib.hs2_sa_reuse_workspace(Bq, Hq, ctypes.byref(c), w, k, int(prefill)))
+    if overlap and workspace is None:
+        raise HS2Error("overlap continues the previous SA call's workspace: pass it")
     ws = _workspace(nb, q.device, workspace)
     if sink is not None:
         assert sink.dtype == torch.float32 and sink.is_contiguous() and sink.numel() == Hq
     if gate is not None:
         assert gate.dtype == torch.float32 and gate.is_contiguous() and tuple(gate.shape) == (Bq, Hq, d)
-    if sink is None and gate is None:
+    if sink is None and gate is None and not overlap:
         st = lib.hs2_sa_reuse(_ptr(q), Bq, Hq, ctypes.byref(c), w, _ptr(idx), _ptr(idx_cnt), k, float(scale),
                               int(prefill), _ptr(o), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_err),
                               _stream(stream))
     else:
         st = lib.hs2_sa_reuse_ex(_ptr(q), Bq, Hq, ctypes.byref(c), w, _ptr(idx), _ptr(idx_cnt), k, float(scale),
-                                 int(prefill), _ptr(sink), _ptr(gate), _ptr(o), _ptr(ws),
-                                 ws.numel() * ws.element_size(), _ptr(dev_err), _stream(stream))
+                                 int(prefill), _ptr(sink), _ptr(gate), SA_OVERLAP if overlap else 0, _ptr(o),
+                                 _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_err), _stream(stream))
     _check(st)
     return o
 
