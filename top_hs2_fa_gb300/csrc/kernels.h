@@ -6,6 +6,26 @@
 
 namespace hs2 {
 
+// Launch with programmatic stream serialization: the kernel may begin while the previous
+// launch on the stream finishes, so it must call griddep_wait before reading anything that
+// launch may write (and griddep_launch_dependents to let the next one begin early).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 constexpr int kCombineThreads = 512;
 
 // One attention pass over a set of rows of one group's paged KV, producing per

@@ -610,19 +610,7 @@ static cudaError_t launch_stream_t(const AttnArgs& a, const SaStreamArgs& sp, in
   auto kern = (a.sink || a.gate) ? sa_stream_kernel<D, FMT, true> : sa_stream_kernel<D, FMT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = sm;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, a, sp);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(128), sm, s, a, sp);
 }
 
 template <int FMT>
