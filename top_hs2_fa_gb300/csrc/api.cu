@@ -68,7 +68,7 @@ struct FaPlan {
   int pps;    // pages per split
   int nsplit;
   long long ld;  // logits row length
-  size_t off_ml, off_o, off_logits, off_scores, off_hist, total;
+  size_t off_ml, off_o, off_lcode, off_lmax, off_scores, off_hist, total;
 };
 
 FaPlan fa_plan(int Bq, int Hq, const hs2_kv* kv, int max_t) {
@@ -90,8 +90,10 @@ FaPlan fa_plan(int Bq, int Hq, const hs2_kv* kv, int max_t) {
   off = align256(off + (size_t)Bq * Hq * p.nsplit * sizeof(float) * 2);
   p.off_o = off;
   off = align256(off + (size_t)Bq * Hq * p.nsplit * kv->d * sizeof(float));
-  p.off_logits = off;
-  off = align256(off + (size_t)Bq * Hq * p.ld * sizeof(float));
+  p.off_lcode = off;
+  off = align256(off + (size_t)Bq * Hq * p.ld * sizeof(uint16_t));
+  p.off_lmax = off;
+  off = align256(off + (size_t)Bq * Hq * (p.ld / 16) * sizeof(float));
   p.off_scores = off;
   off = align256(off + (size_t)Bq * kv->Hkv * p.ld * sizeof(uint32_t));
   p.off_hist = off;
@@ -520,7 +522,8 @@ static hs2_status fa_select_impl(const void* q, int B_or_n, int Hq, const hs2_kv
   a.nsplit = p.nsplit;
   a.part_ml = (float2*)(ws + p.off_ml);
   a.part_o = (float*)(ws + p.off_o);
-  a.logits = (float*)(ws + p.off_logits);
+  a.lcode = (uint16_t*)(ws + p.off_lcode);
+  a.lmax = (float*)(ws + p.off_lmax);
   a.ld_logits = p.ld;
   if (low_precision(kv)) {
     if (!p.mma) return HS2_ERR_UNSUPPORTED;
@@ -559,7 +562,8 @@ static hs2_status fa_select_impl(const void* q, int B_or_n, int Hq, const hs2_kv
   c.kcap = k;
   c.idx = idx;
   c.cnt = idx_cnt;
-  c.logits = a.logits;
+  c.lcode = a.lcode;
+  c.lmax = a.lmax;
   c.scores = (uint32_t*)(ws + p.off_scores);
   c.hist = (uint32_t*)(ws + p.off_hist);
   c.ld_logits = p.ld;
@@ -641,7 +645,8 @@ hs2_status hs2_sa_reuse_ex(const void* q, int B_or_n, int Hq, const hs2_kv* kv, 
   a.kcap = k;
   a.part_ml = (float2*)(ws + p.off_ml);
   a.part_o = (float*)(ws + p.off_o);
-  a.logits = nullptr;
+  a.lcode = nullptr;
+  a.lmax = nullptr;
   a.out_o = o;
   a.sink = sink;
   a.gate = gate;

@@ -65,7 +65,11 @@ __global__ void __launch_bounds__(128) attn_partial_kernel(const AttnArgs a) {
   for (int h = 0; h < G; ++h) oacc[h][0] = oacc[h][1] = 0.f;
   const int dp = tid % DP, rg = tid / DP;
   const int32_t* bt = a.bt + (size_t)qg.b * a.max_pages;
-  float* logit_base = a.logits ? a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits : nullptr;
+  // selection logits (FA layer, consecutive positions over consecutive threads): codes below
+  // each 16-position group's per-head max, and the max (logit_code)
+  const size_t lrow = (size_t)qi * a.Hq + (size_t)g * G;
+  uint16_t* code_base = a.lcode ? a.lcode + lrow * a.ld_logits : nullptr;
+  float* max_base = a.lcode ? a.lmax + lrow * (a.ld_logits / kLogitGroup) : nullptr;
   __syncthreads();
 
   for (int r0 = row_begin; r0 < row_end; r0 += ROWS) {
@@ -128,9 +132,20 @@ __global__ void __launch_bounds__(128) attn_partial_kernel(const AttnArgs a) {
       }
     }
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      x[h] = ok ? x[h] * a.scale_log2 : -INFINITY;
-      if (ok && logit_base) logit_base[(size_t)h * a.ld_logits + pos] = x[h];
+    for (int h = 0; h < G; ++h) x[h] = ok ? x[h] * a.scale_log2 : -INFINITY;
+    if (code_base) {  // the block's rows start on a multiple of 16 positions (whole pages)
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float gm = x[h];
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
+        if (ok) {
+          code_base[(size_t)h * a.ld_logits + pos] = (uint16_t)logit_code(x[h], gm);
+          if ((tid & (kLogitGroup - 1)) == 0) max_base[(size_t)h * (a.ld_logits / kLogitGroup) + pos / kLogitGroup] = gm;
+        }
+      }
     }
     vrow_s[tid] = ok ? vrow : nullptr;
     // chunk max per head (block reduction), running max update

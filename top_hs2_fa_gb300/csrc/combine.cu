@@ -133,15 +133,17 @@ __global__ void __launch_bounds__(kMergeThreads) merge_score_kernel(const Combin
   const int s0 = s_lo + 8 * tid;
   float sc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (s0 < nF) {
-    const float* lg = a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits + s0;
+    // 8 positions of one 16-position group: 8 codes and the group's max per head
+    const size_t lrow = (size_t)qi * a.Hq + (size_t)g * G;
+    const uint16_t* lc = a.lcode + lrow * a.ld_logits + s0;
+    const float* lm = a.lmax + lrow * (a.ld_logits / kLogitGroup) + s0 / kLogitGroup;
     for (int h = 0; h < G; ++h) {
-      const float4 x0 = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)h * a.ld_logits));
-      const float4 x1 = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)h * a.ld_logits + 4));
-      const float l2 = lse2_s[h];
-      sc[0] += ex2_approx(x0.x - l2); sc[1] += ex2_approx(x0.y - l2);
-      sc[2] += ex2_approx(x0.z - l2); sc[3] += ex2_approx(x0.w - l2);
-      sc[4] += ex2_approx(x1.x - l2); sc[5] += ex2_approx(x1.y - l2);
-      sc[6] += ex2_approx(x1.z - l2); sc[7] += ex2_approx(x1.w - l2);
+      const uint4 c = __ldcs(reinterpret_cast<const uint4*>(lc + (size_t)h * a.ld_logits));
+      const float d = __ldg(lm + (size_t)h * (a.ld_logits / kLogitGroup)) - lse2_s[h];
+      sc[0] += logit_term(c.x & 0xffffu, d); sc[1] += logit_term(c.x >> 16, d);
+      sc[2] += logit_term(c.y & 0xffffu, d); sc[3] += logit_term(c.y >> 16, d);
+      sc[4] += logit_term(c.z & 0xffffu, d); sc[5] += logit_term(c.z >> 16, d);
+      sc[6] += logit_term(c.w & 0xffffu, d); sc[7] += logit_term(c.w >> 16, d);
     }
   }
   uint32_t key[8];
@@ -385,7 +387,7 @@ cudaError_t launch_prefill_trivial_select(int32_t* idx, int32_t* cnt, int n, int
 // merge_score_kernel + select_kernel this drops the global histogram (and its zeroing),
 // one launch and a re-read of the keys from a second kernel.
 constexpr int kFusedMinPairs = 152;  // below this, too few CTAs to stream the logits fast
-constexpr int kScoreHeads = 4;       // heads whose logit loads a thread has in flight (64 registers)
+constexpr int kScoreHeads = 8;       // heads whose logit-code loads a thread has in flight
 
 bool score_select_fused(const CombineArgs& a, int Bq) {
   return a.select && a.sel_block == 1 && !a.prefill && !a.gather && (long long)Bq * a.Hkv >= kFusedMinPairs &&
@@ -459,7 +461,9 @@ __global__ void __launch_bounds__(kSelectThreads, 2) score_select_kernel(const C
     return;
   }
   // ---- scores of the far range, 4 positions per thread and pass, kScoreHeads heads' loads in flight
-  const float* lg = a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits;
+  const size_t lrow = (size_t)qi * a.Hq + (size_t)g * G;
+  const uint16_t* lcd = a.lcode + lrow * a.ld_logits;
+  const float* lmx = a.lmax + lrow * (a.ld_logits / kLogitGroup);
   uint32_t* keys = a.scores + ((size_t)qi * a.Hkv + g) * a.ld_logits;
   // (one CTA-wide trip count: threads past nF only skip their loads)
   for (int base = 0; base < nF; base += 4 * NT) {
@@ -467,18 +471,22 @@ __global__ void __launch_bounds__(kSelectThreads, 2) score_select_kernel(const C
     const bool mine = s0 < nF;
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int h0 = 0; h0 < G; h0 += kScoreHeads) {
-      float4 x[kScoreHeads];
-#pragma unroll
-      for (int hh = 0; hh < kScoreHeads; ++hh)
-        if (mine && h0 + hh < G) x[hh] = __ldcs(reinterpret_cast<const float4*>(lg + (size_t)(h0 + hh) * a.ld_logits + s0));
+      uint2 c[kScoreHeads];  // 4 codes of one 16-position group
+      float d[kScoreHeads];  // the group's max minus the head's lse
 #pragma unroll
       for (int hh = 0; hh < kScoreHeads; ++hh)
         if (mine && h0 + hh < G) {
-          const float l2 = lse2_s[h0 + hh];
-          sc[0] += ex2_approx(x[hh].x - l2);
-          sc[1] += ex2_approx(x[hh].y - l2);
-          sc[2] += ex2_approx(x[hh].z - l2);
-          sc[3] += ex2_approx(x[hh].w - l2);
+          c[hh] = __ldcs(reinterpret_cast<const uint2*>(lcd + (size_t)(h0 + hh) * a.ld_logits + s0));
+          d[hh] = __ldg(lmx + (size_t)(h0 + hh) * (a.ld_logits / kLogitGroup) + s0 / kLogitGroup);
+        }
+#pragma unroll
+      for (int hh = 0; hh < kScoreHeads; ++hh)
+        if (mine && h0 + hh < G) {
+          const float dd = d[hh] - lse2_s[h0 + hh];
+          sc[0] += logit_term(c[hh].x & 0xffffu, dd);
+          sc[1] += logit_term(c[hh].x >> 16, dd);
+          sc[2] += logit_term(c[hh].y & 0xffffu, dd);
+          sc[3] += logit_term(c[hh].y >> 16, dd);
         }
     }
     uint32_t key[4];

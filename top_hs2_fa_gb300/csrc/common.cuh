@@ -77,6 +77,10 @@ HS2_DEVI void stg_f32_pol(float* p, float v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
 }
 
+HS2_DEVI void stg_u16_pol(uint16_t* p, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.u16 [%0], %1, %2;" ::"l"(p), "h"((unsigned short)v), "l"(pol) : "memory");
+}
+
 HS2_DEVI void flag_error(int32_t* dev_err, int bits) {
   if (dev_err) atomicOr(dev_err, bits);
 }
@@ -106,8 +110,20 @@ HS2_DEVI float ex2_approx(float x) {
   return y;
 }
 
-// exp2 of a (possibly -inf) base-2 logit relative to a (possibly -inf) max:
-// a row whose max is still -inf contributes exactly zero.
+// Selection logits between the FA scan and the selection: a key's base-2 logit x is kept as
+// a 16-bit code below the max m of its group of 16 keys (same query head, groups aligned to
+// multiples of 16 positions), code = round((m - x) * 2^11), 65535 for x = -inf or 32 or more
+// below m; m itself is kept as a float per group. Decoding recovers x to within 2^-12, so
+// a head's term 2^(x - lse) to within a relative 1.7e-4 (an omitted term far below m adds
+// less than 2^-32 of the group's largest).
+constexpr int kLogitGroup = 16;
+constexpr float kLogitCodeUnit = 1.f / 2048.f;
+HS2_DEVI uint32_t logit_code(float x, float m) { return __float2uint_rn(fminf((m - x) * 2048.f, 65535.f)); }
+// 2^(x - lse2) from x's code and (m - lse2) of its group
+HS2_DEVI float logit_term(uint32_t code, float m_minus_lse2) {
+  return ex2_approx(fmaf(-(float)code, kLogitCodeUnit, m_minus_lse2));
+}
+
 // Programmatic dependent launch. griddep_wait: returns once the grids this launch depends
 // on have completed and their memory is visible (at once when it has no such dependency).
 // griddep_launch_dependents: the next launch on the stream, if it allows programmatic
@@ -119,6 +135,8 @@ HS2_DEVI void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_
 HS2_DEVI void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// exp2 of a (possibly -inf) base-2 logit relative to a (possibly -inf) max:
+// a row whose max is still -inf contributes exactly zero.
 HS2_DEVI float exp2_rel(float x, float m) { return (m == -INFINITY) ? 0.f : exp2f(x - m); }
 
 // m16n8k16 bf16 MMA with fp32 accumulate (legacy warp-level tensor path; used where

@@ -56,24 +56,30 @@ __global__ void __launch_bounds__(128, (FMT != kFaBf16 && NT == 1) ? 4 : 0) fa_d
 
   const int32_t* bt = a.bt + (size_t)qg.b * a.max_pages;
   const size_t head_stride = (size_t)kPage * D;  // elements per (page, KV head)
-  float* logit_base = a.logits ? a.logits + ((size_t)qi * a.Hq + (size_t)g * G) * a.ld_logits : nullptr;
+  const size_t lrow = (size_t)qi * a.Hq + (size_t)g * G;  // the pair's first head row
+  uint16_t* code_base = a.lcode ? a.lcode + lrow * a.ld_logits : nullptr;
+  float* max_base = a.lcode ? a.lmax + lrow * (a.ld_logits / kLogitGroup) : nullptr;
 
-  // The K/V stream is read once: evict it first. The base-2 logits are read by the
-  // selection right after this kernel: keep them.
+  // The K/V stream is read once: evict it first. The logit codes are read by the selection
+  // right after this kernel: keep them.
   const uint64_t pol_stream = l2_first_policy(), pol_keep = l2_keep_policy();
-  // base-2 logits of one 16-key chunk for the selection
-  auto write_logits = [&](const float (&x)[NT][4], int keyA, int keyB, bool okA, bool okB) {
-    if (!logit_base) return;
+  // one 16-key group's logits for the selection: codes below the group's per-head max
+  // (logit_code), and the max itself (lanes 0-3, two heads each)
+  auto write_logits = [&](const float (&x)[NT][4], const float (&gm)[NT][2], int key0, bool okA, bool okB) {
+    if (!code_base) return;
+    const int keyA = key0 + gid, keyB = keyA + 8;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int h0 = nt * 8 + 2 * tig;
-      if (h0 < G) {
-        if (okA) stg_f32_pol(logit_base + (size_t)h0 * a.ld_logits + keyA, x[nt][0], pol_keep);
-        if (okB) stg_f32_pol(logit_base + (size_t)h0 * a.ld_logits + keyB, x[nt][2], pol_keep);
-      }
-      if (h0 + 1 < G) {
-        if (okA) stg_f32_pol(logit_base + (size_t)(h0 + 1) * a.ld_logits + keyA, x[nt][1], pol_keep);
-        if (okB) stg_f32_pol(logit_base + (size_t)(h0 + 1) * a.ld_logits + keyB, x[nt][3], pol_keep);
+#pragma unroll
+      for (int hs = 0; hs < 2; ++hs) {
+        const int h = nt * 8 + 2 * tig + hs;
+        if (h < G) {
+          uint16_t* row = code_base + (size_t)h * a.ld_logits;
+          if (okA) stg_u16_pol(row + keyA, logit_code(x[nt][hs], gm[nt][hs]), pol_keep);
+          if (okB) stg_u16_pol(row + keyB, logit_code(x[nt][hs + 2], gm[nt][hs]), pol_keep);
+          if (gid == 0) stg_f32_pol(max_base + (size_t)h * (a.ld_logits / kLogitGroup) + key0 / kLogitGroup,
+                                    gm[nt][hs], pol_keep);
+        }
       }
     }
   };
@@ -146,7 +152,7 @@ __global__ void __launch_bounds__(128, (FMT != kFaBf16 && NT == 1) ? 4 : 0) fa_d
         const bool okA = keyA < t, okB = keyB < t;
         float x[NT][4];
         at.step(kr0, kr1, vr, okA, okB, a.scale_log2, x);
-        write_logits(x, keyA, keyB, okA, okB);
+        write_logits(x, at.gmax, key0, okA, okB);
       }
     }
   } else {
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(128, (FMT != kFaBf16 && NT == 1) ? 4 : 0) fa_d
       const bool okA = keyA < t, okB = keyB < t;
       float x[NT][4];
       at.step(kr0, kr1, va, okA, okB, a.scale_log2 * ks, x);
-      write_logits(x, keyA, keyB, okA, okB);
+      write_logits(x, at.gmax, key0, okA, okB);
     };
     // issue cursor (pg, ch) over the warp's chunks: 4 per page, fewer on the last page of t
     int phys = 0;

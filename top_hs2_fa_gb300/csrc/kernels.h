@@ -50,7 +50,8 @@ struct AttnArgs {
   int kcap;
   float2* part_ml;  // [Bq][Hq][nsplit]
   float* part_o;    // [Bq][Hq][nsplit][D]
-  float* logits;    // [Bq][Hq][ld_logits] base-2 logits, or null
+  uint16_t* lcode;  // [Bq][Hq][ld_logits] selection logits as codes below their group max (logit_code), or null
+  float* lmax;      // [Bq][Hq][ld_logits / 16] each 16-key group's max base-2 logit
   float* out_o;     // [Bq][Hq][D] final output (kernels that normalise in place)
   int32_t* arrive;  // SA stream: per-unit arrival counters, zero at launch (the merges leave them zero)
   const float* k_scale;  // FP8 cache: [num_pages][Hkv] dequantisation scales, else null
@@ -112,7 +113,8 @@ struct CombineArgs {
   int k, kcap;
   int32_t* idx;  // [Bq][Hkv][kcap]
   int32_t* cnt;  // [Bq][Hkv]
-  const float* logits;
+  const uint16_t* lcode;  // [Bq][Hq][ld_logits] logit codes and [Bq][Hq][ld_logits / 16] group maxima
+  const float* lmax;
   uint32_t* scores;  // [Bq][Hkv][ld_logits] selection keys (scratch)
   uint32_t* hist;    // [Bq][Hkv][4096] top-digit histograms (scratch, zeroed per call)
   long long ld_logits;

@@ -29,6 +29,7 @@ struct MmaAttn {
   static constexpr int VC = D / 64;  // 16-byte V chunks per lane and key
   uint32_t qb[KS][NT][2];
   float m[NT][2], l[NT][2];
+  float gmax[NT][2];  // the last step's max logit over its 16 keys, heads 2tig and 2tig+1
   float acc[KS][NT][4];
 
   // Q^T B-fragments of heads nt*8 + gid (heads >= G contribute zeros).
@@ -121,6 +122,7 @@ struct MmaAttn {
         cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 4));
         cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 8));
         cm[hs] = fmaxf(cm[hs], __shfl_xor_sync(0xffffffffu, cm[hs], 16));
+        gmax[nt][hs] = cm[hs];
         grow |= cm[hs] > m[nt][hs] + kLazyRescale;
       }
       // Lazy rescale: the running max moves (and l, acc are rescaled) only when a head's
