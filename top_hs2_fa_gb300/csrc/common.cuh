@@ -119,9 +119,11 @@ HS2_DEVI float ex2_approx(float x) {
 constexpr int kLogitGroup = 16;
 constexpr float kLogitCodeUnit = 1.f / 2048.f;
 HS2_DEVI uint32_t logit_code(float x, float m) { return __float2uint_rn(fminf((m - x) * 2048.f, 65535.f)); }
-// 2^(x - lse2) from x's code and (m - lse2) of its group
+// 2^(x - lse2) from x's code and (m - lse2) of its group. The code becomes a float without
+// a conversion instruction: 2^23 + code is exact in the mantissa, and subtracting 2^23 is exact.
 HS2_DEVI float logit_term(uint32_t code, float m_minus_lse2) {
-  return ex2_approx(fmaf(-(float)code, kLogitCodeUnit, m_minus_lse2));
+  const float c = __uint_as_float(0x4B000000u | code) - 8388608.f;
+  return ex2_approx(fmaf(-c, kLogitCodeUnit, m_minus_lse2));
 }
 
 // Programmatic dependent launch. griddep_wait: returns once the grids this launch depends
