@@ -77,8 +77,9 @@ FaPlan fa_plan(int Bq, int Hq, const hs2_kv* kv, int max_t) {
   p.mma = (kv->dtype == HS2_BF16 || low_precision(kv)) && G <= 32 && (G <= 8 || G == 16 || G == 32);
   const int maxpg = cdiv(max_t, 64);
   if (p.mma) {
-    // enough CTAs to fill 152 SMs several times over, splits of at most 16 pages
-    p.pps = 16;
+    // enough CTAs to fill 152 SMs several times over, splits of at most 32 pages (2048 keys:
+    // 16 wrote and merged twice the partials, 6.6 us more per decode step; 64 left too few CTAs)
+    p.pps = 32;
     while (p.pps > 1 && (long long)Bq * kv->Hkv * cdiv(maxpg, p.pps) < 152LL * 8) p.pps >>= 1;
   } else {
     p.pps = 2;
