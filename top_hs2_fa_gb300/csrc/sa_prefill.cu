@@ -238,6 +238,8 @@ __global__ void __launch_bounds__(128, 3) sa_staged_kernel(const AttnArgs a) {
     }
     rowid[u] = r;
   }
+  // the last step's tail: no rows
+  for (int u = nU + tid; u < (nU + 15) / 16 * 16; u += 128) rowid[u] = -1;
   StagedAttn<D, 1> at;
   at.init(reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)qi * a.Hq + (size_t)g * G) * D, G);
   __syncthreads();
@@ -246,18 +248,25 @@ __global__ void __launch_bounds__(128, 3) sa_staged_kernel(const AttnArgs a) {
   const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(a.v);
   const uint64_t keep = l2_keep_policy();  // rows are re-read by other rows' CTAs
   const uint32_t ring = base + (uint32_t)warp * kStgSlots * kSlot;
+  // A warp instruction copies 16-byte chunk cc = lane % CPR of rows r0 + RSTEP m, r0 =
+  // lane / CPR < RSTEP. Everything but the row id is fixed per lane: the source is the row's
+  // base plus this lane's chunk, and the swizzled destination of row r0 + RSTEP m is this
+  // lane's row-r0 offset with bits 4-6 flipped by (RSTEP m) & 7 (r0 and RSTEP m share no bit).
+  constexpr int RSTEP = 32 / CPR;
+  const int cc = lane % CPR, r0 = lane / CPR;
+  const __nv_bfloat16* kl = kb + 8 * cc;
+  const __nv_bfloat16* vl = vb + 8 * cc;
+  const uint32_t so0 = (uint32_t)(cc >> 3) * 2048u + sw128(r0, cc & 7);
   auto issue = [&](int st, int slot) {
     const uint32_t dst = ring + (uint32_t)slot * kSlot;
+    const int32_t* rid_st = rowid + st * 16 + r0;  // padded with -1 to a whole step
 #pragma unroll
-    for (int m = 0; m < 16 * CPR / 32; ++m) {
-      const int c = lane + 32 * m;
-      const int r = c / CPR, cc = c % CPR;
-      const int u = st * 16 + r;
-      const int rid = u < nU ? rowid[u] : -1;
-      const size_t off = (size_t)(rid >= 0 ? rid : 0) * D + 8 * cc;
-      const uint32_t so = (uint32_t)(cc >> 3) * 2048u + sw128(r, cc & 7);
-      cp_async16_keep(dst + so, kb + off, rid >= 0, keep);
-      cp_async16_keep(dst + HALVES * 2048u + so, vb + off, rid >= 0, keep);
+    for (int m = 0; m < 16 / RSTEP; ++m) {
+      const int rid = rid_st[RSTEP * m];
+      const size_t off = (size_t)max(rid, 0) * D;
+      const uint32_t so = (so0 ^ ((uint32_t)((RSTEP * m) & 7) << 4)) + (uint32_t)(RSTEP * m) * 128u;
+      cp_async16_keep(dst + so, kl + off, rid >= 0, keep);
+      cp_async16_keep(dst + HALVES * 2048u + so, vl + off, rid >= 0, keep);
     }
   };
   const int nsteps = (nU + 15) / 16;
@@ -300,8 +309,9 @@ __global__ void __launch_bounds__(128, 3) sa_staged_kernel(const AttnArgs a) {
   }
 }
 
-static size_t sa_staged_smem(int D, long long w, long long k) {
-  return 1024 + 4 * kStgSlots * (size_t)(D == 128 ? stg_slot_bytes<128>() : stg_slot_bytes<64>()) + (size_t)(w + k) * 4;
+static size_t sa_staged_smem(int D, long long w, long long k) {  // rings, then the row ids of whole steps
+  return 1024 + 4 * kStgSlots * (size_t)(D == 128 ? stg_slot_bytes<128>() : stg_slot_bytes<64>()) +
+         (size_t)((w + k + 15) / 16 * 16) * 4;
 }
 
 template <int D>
