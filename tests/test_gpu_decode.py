@@ -450,3 +450,58 @@ def test_sa_layers_share_a_workspace_with_overlap(H):
         for j, o in enumerate(outs):
             ref = O.sa_decode(grp.q_sa[j], kv, grp.w, idx_h, cnt_h, grp.scale)
             assert max_abs(o.cpu().numpy(), ref) <= tol("bf16"), (rep, j)
+
+
+def test_group_step_in_a_cuda_graph_matches_eager(H):
+    """The decode group step as bench.py runs it, captured in a CUDA graph: the FA call, then
+    three SA layers on one workspace (the second and third with HS2_SA_OVERLAP, so their
+    kernels overlap the previous one through programmatic dependent launch). Two replays give
+    the eager run's outputs bit for bit (the merges sum partials in a fixed order) and those
+    match the oracle."""
+    import torch
+
+    grp = W.decode_group([3000, 9000, 20000, 5000, 12000, 7000], Hq=32, Hkv=4, d=128, w=128, k=512, dtype="bf16",
+                         seed=41, n_sa=3, needles=8)
+    kv = grp.kv
+    dkv = kv_to_device(kv)
+    B, Hq, d = grp.q_fa.shape
+    max_t = int(kv.seq_len.max())
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q = to_torch(grp.q_fa, "bf16")
+    qs = [to_torch(x, "bf16") for x in grp.q_sa]
+    ws_fa = torch.empty(H.hs2_fa_select_workspace(B, Hq, dkv, max_t, grp.k), dtype=torch.uint8, device="cuda")
+    ws_sa = torch.empty(H.hs2_sa_reuse_workspace(B, Hq, dkv, grp.w, grp.k), dtype=torch.uint8, device="cuda")
+    o = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    idx = torch.empty((B, 4, grp.k), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((B, 4), dtype=torch.int32, device="cuda")
+    osa = [torch.empty((B, Hq, d), dtype=torch.float32, device="cuda") for _ in range(3)]
+
+    def step(stream):
+        H.hs2_fa_select(q, dkv, grp.w, grp.k, grp.scale, max_t=max_t, out=(o, lse, idx, cnt), workspace=ws_fa,
+                        dev_err=err, stream=stream)
+        for j in range(3):
+            H.hs2_sa_reuse(qs[j], dkv, grp.w, idx, cnt, grp.k, grp.scale, out=osa[j], workspace=ws_sa, dev_err=err,
+                           stream=stream, overlap=j > 0)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step(s)
+    torch.cuda.synchronize()
+    eager = [x.clone() for x in (o, lse, idx, cnt, *osa)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(s)
+    for rep in range(2):
+        for x in (o, lse, *osa):
+            x.fill_(float("nan"))
+        idx.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(eager, (o, lse, idx, cnt, *osa)):
+            assert torch.equal(a, b), rep
+    assert int(err.item()) == 0
+    idx_h, cnt_h = idx.cpu().numpy(), cnt.cpu().numpy()
+    for j in range(3):
+        ref = O.sa_decode(grp.q_sa[j], kv, grp.w, idx_h, cnt_h, grp.scale)
+        assert max_abs(osa[j].cpu().numpy(), ref) <= tol("bf16"), j
