@@ -122,8 +122,9 @@ def test_prefill_selection_ties_take_lowest_positions(H):
 
 def sample_hiding_keys(n, Hq, Hkv, w, k, seed):
     """Prefill inputs on which the streamed candidates cannot prove many rows' top-k: keys
-    at the positions the sampled sweep sees (multiples of 4) score low and all others high,
-    so the sampled threshold lets about 3/4 of every far range through, long rows overflow
+    at multiples of 4 (a superset of the positions the sampled sweep sees, multiples of 8)
+    score low and all others high, so the sampled threshold lets about 3/4 of every far
+    range through, long rows overflow
     their candidate buffers (capacity max(256, 4k)) with high keys, and the largest dropped
     key beats the k-th kept one (tests/test_selection_proof.py restates the mechanism)."""
     d = 128

@@ -369,7 +369,7 @@ static hs2_status fa_select_prefill_tc(const void* q, int n, int Hq, const hs2_k
     if (e != cudaSuccess) return cuda_fail(e);
     b.row0 = r0;
     b.row1 = std::min(n, r0 + p.chunk);
-    // the sampled sweep of the selection scan reads every 4th key (kPsSampleStride) only
+    // the sampled sweep of the selection scan reads every kPsSampleStride-th key only
     CUtensorMap tks;
     if (!encode_2d_bf16(&tks, kv->k, 128, rows, hs2::kPsSampleRowsPerPage, hs2::kPsSampleStride)) return HS2_ERR_ARG;
     e = hs2::launch_prefill_select(tq, tk, tks, b, s);

@@ -230,7 +230,7 @@ size_t fa_prefill_fwd_smem();
 size_t prefill_scan_smem();
 // The selection scan's sampled sweep: every kPsSampleStride-th key, through a tensor map of
 // those rows only (box: the kPsSampleRowsPerPage sampled rows of a 64-row page).
-constexpr int kPsSampleStride = 4;
+constexpr int kPsSampleStride = 8;
 constexpr int kPsSampleRowsPerPage = 64 / kPsSampleStride;
 cudaError_t launch_prefill_select(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tks,
                                   const PsArgs& a, cudaStream_t s);

@@ -7,12 +7,12 @@
 // a tcgen05 recomputation of Q K^T and consumed on the fly.
 //
 // prefill_scan_kernel — one CTA per (128-row tile, KV head), four scoring threads per row:
-//   sweep 0 (sampled): every 4th key position only, 128 of them per tile (512 positions;
+//   sweep 0 (sampled): every 8th key position only, 128 of them per tile (1024 positions;
 //            a strided tensor map loads just those K rows); each thread bins the sampled
 //            scores of its quarter of the row's columns into the row's 256-bin log histogram
 //            (1/8 octave per bin, 16-bit counts in shared memory, atomic adds), then the row's
 //            first thread picks a threshold tau whose estimated count of keys at or above it
-//            is 1.25 times the budget;
+//            is 1.35 times the budget;
 //   sweep 1 (exact): every key tile; the scoring threads stage the tile's 128 x 128 scores in
 //            shared memory, then each scoring warp takes 8 rows and appends (key, position)
 //            of the scores >= tau of a row, in ascending position, into the row's candidate
@@ -49,10 +49,10 @@ constexpr uint32_t kSTile = kST * 128 * 2;
 constexpr int kBins = 256;
 constexpr uint32_t kBinBase = 0x410 - (kBins - 1);  // bin 255 holds keys >> 20 == 0x410 (score 8.0)
 // The sampled sweep scores every 4th position (position-correlated scores would bias a
-// sample of whole tiles); a sampled key tile holds 128 such positions, 512 apart at most.
+// sample of whole tiles); a sampled key tile holds 128 such positions, 1024 apart at most.
 constexpr int kSampleStride = kPsSampleStride;
 constexpr int kSampSpan = kST * kSampleStride;                // positions covered by a sampled key tile
-constexpr int kSampPages = kSampSpan / kPage;                 // pages of a sampled key tile (8)
+constexpr int kSampPages = kSampSpan / kPage;                 // pages of a sampled key tile (16)
 constexpr uint32_t kSampBoxBytes = kPsSampleRowsPerPage * 128;  // one 64-column half of a page's sampled rows
 
 constexpr int kCompRows = 4;  // rows compacted together by a scoring warp (of its 8)
@@ -145,7 +145,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (!tc::mbar_wait(&sm.k_empty[ks], ((kt >> 1) & 1) ^ 1)) { set_abort(sm, a.dev_err); break; }
         const int j = jof(kt);
         if (kt < J0) {
-          // sampled keys: rows 0, 4, ..., 60 of each of 8 pages, 16 tile rows per page
+          // sampled keys: rows 0, 8, ..., 56 of each of 16 pages, 8 tile rows (one 1 KB swizzle
+          // atom) per page
           int rows[kSampPages];
           uint32_t bytes = 0;
           for (int pg = 0; pg < kSampPages; ++pg) {
@@ -302,13 +303,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
             if (ranked) {
               // threshold: the estimated count at or above it (sample count scaled by the row's
               // sampling rate; the sweep saw every position of [0, nF) that is a multiple of the
-              // stride) reaches 1.25 times the budget. Fewer candidates mean fewer stores here
+              // stride) reaches 1.35 times the budget. Fewer candidates mean fewer stores here
               // and a shorter top-k; a row the estimate leaves short of k is completed exactly
-              // (prefill_complete_kernel). On the AR(1) workload 1.25 completes no row (1.1: 221
-              // rows, slower overall; 2: 0.74 ms slower at n = 32768).
+              // (prefill_complete_kernel). On the AR(1) workload at n = 32768 (whole call):
+              // stride 4 with 1.25 15.43 ms; stride 8 with 1.25 15.33 ms, 7 rows completed;
+              // stride 8 with 1.35 15.06 ms, none (stride 4: 1.1 left 221 rows to complete and
+              // was slower overall, 2 was 0.74 ms slower).
               const int n_samp = (nF + kSampleStride - 1) / kSampleStride;
               const float scale = (float)nF / (float)n_samp;
-              const float target = 1.25f * (float)a.k;
+              const float target = 1.35f * (float)a.k;
               float cum = 0.f;
               tau = 0u;
               for (int b = kBins - 1; b >= 0; --b) {
